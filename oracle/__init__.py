@@ -1,0 +1,118 @@
+"""Oracle for causal linear attention / retention / gated linear attention.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. It shares no code
+with the CUDA library and never imports it.
+
+Two parts:
+
+* ``forward`` / ``decode_step``: the definition, the recurrent form in fp64
+  (``la_oracle.c``, called through ctypes, OpenMP over (batch, head)).
+* ``forms``: independent numpy restatements (parallel masked matmul, brute
+  force double sum, chunkwise) used to pin the definition, plus a numpy copy
+  of the recurrence for tiny cases.
+
+Parity unpinned: the absolute output values at the large workloads (pinned
+only transitively through the small-case pins) and the gate temperature 16 of
+the per-channel gate, which no page fixes.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from ._build import build_oracle
+from . import forms  # noqa: F401  (re-exported)
+
+# mode bits, as the problem statement defines them
+PHI_ELU1 = 0x1
+NORMALIZE = 0x2
+GATE_HEAD = 0x4
+GATE_CHANNEL = 0x8
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = build_oracle()
+        lib = ctypes.CDLL(path)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i = ctypes.c_int
+        lib.oracle_forward.argtypes = [f32p, f32p, f32p, f32p, f64p, i, i, i, i, i, i,
+                                       f64p, f64p, i]
+        lib.oracle_forward.restype = i
+        lib.oracle_decode_step.argtypes = [f32p, f32p, f32p, f32p, f64p, i, i, i, i, i,
+                                           f64p, i]
+        lib.oracle_decode_step.restype = i
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = i
+        _lib = lib
+    return _lib
+
+
+def _f32(a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    return a
+
+
+def _ptr(a, ct):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def state_block(dk, dv, mode):
+    """Per-(b,h) state size: S (dk*dv) followed by z (dk) when normalised."""
+    return dk * dv + (dk if mode & NORMALIZE else 0)
+
+
+def max_threads():
+    return _load().oracle_max_threads()
+
+
+def forward(q, k, v, gate=None, mode=0, state_in=None, nthreads=0):
+    """Recurrent fp64 forward. q,k: [B,H,L,dk]; v: [B,H,L,dv]; gate: None,
+    gamma[H] or g[B,H,L,dk]. Returns (out [B,H,L,dv] f64, state [B,H,blk] f64)."""
+    lib = _load()
+    q, k, v, gate = _f32(q), _f32(k), _f32(v), _f32(gate)
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape[:3] == q.shape[:3]
+    blk = state_block(dk, dv, mode)
+    out = np.empty((B, H, L, dv), dtype=np.float64)
+    st = np.empty((B, H, blk), dtype=np.float64)
+    sin = None
+    if state_in is not None:
+        sin = np.ascontiguousarray(np.asarray(state_in, dtype=np.float64)).reshape(B, H, blk)
+    rc = lib.oracle_forward(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float),
+                            _ptr(v, ctypes.c_float), _ptr(gate, ctypes.c_float),
+                            _ptr(sin, ctypes.c_double), B, H, L, dk, dv, mode,
+                            _ptr(out, ctypes.c_double), _ptr(st, ctypes.c_double),
+                            int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_forward rejected its arguments")
+    return out, st
+
+
+def decode_step(q, k, v, state, gate=None, mode=0, nthreads=0):
+    """One recurrent step per (b,h), in place on ``state`` (float64 [B,H,blk]).
+    q,k: [B,H,dk]; v: [B,H,dv]; gate: None, gamma[H] or g[B,H,dk]. Returns out."""
+    lib = _load()
+    q, k, v, gate = _f32(q), _f32(k), _f32(v), _f32(gate)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    assert state.dtype == np.float64 and state.flags.c_contiguous
+    assert state.size == B * H * state_block(dk, dv, mode)
+    out = np.empty((B, H, dv), dtype=np.float64)
+    rc = lib.oracle_decode_step(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float),
+                                _ptr(v, ctypes.c_float), _ptr(gate, ctypes.c_float),
+                                _ptr(state, ctypes.c_double), B, H, dk, dv, mode,
+                                _ptr(out, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode_step rejected its arguments")
+    return out

@@ -1,0 +1,187 @@
+/*
+ * la_oracle.c -- the oracle for causal linear attention, retention and gated
+ * linear attention: the plain recurrent form, evaluated in fp64.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do. It shares no code, header, table or constant generator with the CUDA
+ * library.
+ *
+ * What it computes, for every (b, h) sequence independently:
+ *
+ *   S_0 = 0 (d_k x d_v), z_0 = 0 (d_k)          "causal linear attention as an
+ *                                                 RNN": S_0 = Z_0 = 0
+ *   for t = 0 .. L-1:
+ *     qf = phi(q_t), kf = phi(k_t)               phi = identity or elu(x)+1
+ *                                                 (learnllm m22, "The Math:
+ *                                                 Linear Attention")
+ *     a  = 1 | gamma_h | alpha_t                 the gate A_t of the unified
+ *                                                 recurrence (learnllm m22,
+ *                                                 "Interactive Exploration")
+ *     S  = diag(a) S + kf v_t^T                  k v^T orientation, d_k x d_v
+ *                                                 (insideout lesson 16, Ex. 1.1)
+ *     z  = a * z + kf                            only when normalised
+ *     out_t = qf^T S            (unnormalised)   read AFTER the update
+ *     out_t = qf^T S / (qf . z) (normalised)     (linear_sparse_attention.py,
+ *                                                 linear_attn_recurrent)
+ *
+ * alpha_t[i] = exp(logsigmoid(g_t[i]) / 16) for the per-channel gate (the gated
+ * linear attention gate with temperature 16; Yang et al. 2023, cited on the
+ * troisinh and learnllm pages). logsigmoid is evaluated in the overflow-free
+ * split form. The denominator has no epsilon: phi > 0 keeps it positive
+ * (learnllm m22, "Common Pitfalls" 1).
+ *
+ * Inputs arrive as float32 arrays: bf16 inputs are carried exactly in float32,
+ * and every value is upcast to double before any arithmetic.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* mode bits: the problem statement's flags, restated here for the oracle */
+#define OR_PHI_ELU1     0x1
+#define OR_NORMALIZE    0x2
+#define OR_GATE_HEAD    0x4
+#define OR_GATE_CHANNEL 0x8
+
+static double or_phi(double x, int elu1)
+{
+    if (!elu1) return x;
+    return x > 0.0 ? x + 1.0 : exp(x);   /* elu with alpha = 1, plus one */
+}
+
+static double or_log_sigmoid(double x)
+{
+    /* log(1/(1+e^-x)), split so that neither branch overflows */
+    if (x >= 0.0) return -log1p(exp(-x));
+    return x - log1p(exp(x));
+}
+
+/* One sequence of L tokens; S (dk*dv) and z (dk) hold the running state on
+ * entry and on exit. g is [L, dk] for the per-channel gate, else unused. */
+static void or_sequence(const float *q, const float *k, const float *v,
+                        const float *g, double gamma, int L, int dk, int dv,
+                        int mode, double *S, double *z, double *out)
+{
+    const int elu1 = (mode & OR_PHI_ELU1) != 0;
+    const int norm = (mode & OR_NORMALIZE) != 0;
+    double *qf = (double *)malloc(sizeof(double) * (size_t)dk * 3);
+    double *kf = qf + dk;
+    double *a = kf + dk;
+    for (int t = 0; t < L; ++t) {
+        const float *qt = q + (size_t)t * dk;
+        const float *kt = k + (size_t)t * dk;
+        const float *vt = v + (size_t)t * dv;
+        for (int i = 0; i < dk; ++i) {
+            qf[i] = or_phi((double)qt[i], elu1);
+            kf[i] = or_phi((double)kt[i], elu1);
+            if (mode & OR_GATE_CHANNEL)
+                a[i] = exp(or_log_sigmoid((double)g[(size_t)t * dk + i]) / 16.0);
+            else if (mode & OR_GATE_HEAD)
+                a[i] = gamma;
+            else
+                a[i] = 1.0;
+        }
+        for (int i = 0; i < dk; ++i) {
+            double *Si = S + (size_t)i * dv;
+            for (int j = 0; j < dv; ++j)
+                Si[j] = a[i] * Si[j] + kf[i] * (double)vt[j];
+            if (norm) z[i] = a[i] * z[i] + kf[i];
+        }
+        double den = 0.0;
+        if (norm)
+            for (int i = 0; i < dk; ++i) den += qf[i] * z[i];
+        double *ot = out + (size_t)t * dv;
+        for (int j = 0; j < dv; ++j) {
+            double num = 0.0;
+            for (int i = 0; i < dk; ++i) num += qf[i] * S[(size_t)i * dv + j];
+            ot[j] = norm ? num / den : num;
+        }
+    }
+    free(qf);
+}
+
+/*
+ * oracle_forward: the whole forward pass over q, k, v [B,H,L,dk|dv].
+ *   gate: NULL, gamma[H] (OR_GATE_HEAD) or g[B,H,L,dk] (OR_GATE_CHANNEL)
+ *   state_in: NULL (start from zero) or [B,H] blocks of S (dk*dv) followed,
+ *             when normalised, by z (dk) -- the block layout of state_out
+ *   out: [B,H,L,dv] doubles; state_out: same block layout as state_in
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_forward(const float *q, const float *k, const float *v,
+                   const float *gate, const double *state_in, int B, int H,
+                   int L, int dk, int dv, int mode, double *out,
+                   double *state_out, int nthreads)
+{
+    if (B < 0 || H < 0 || L < 0 || dk <= 0 || dv <= 0) return -1;
+    if ((mode & OR_GATE_HEAD) && (mode & OR_GATE_CHANNEL)) return -1;
+    if ((mode & (OR_GATE_HEAD | OR_GATE_CHANNEL)) && !gate) return -1;
+    const int norm = (mode & OR_NORMALIZE) != 0;
+    const size_t blk = (size_t)dk * dv + (norm ? (size_t)dk : 0);
+    const long nbh = (long)B * H;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (long bh = 0; bh < nbh; ++bh) {
+        const int h = (int)(bh % H);
+        double *st = state_out + (size_t)bh * blk;
+        if (state_in) memcpy(st, state_in + (size_t)bh * blk, blk * sizeof(double));
+        else memset(st, 0, blk * sizeof(double));
+        const float *g = NULL;
+        double gamma = 1.0;
+        if (mode & OR_GATE_CHANNEL) g = gate + (size_t)bh * L * dk;
+        if (mode & OR_GATE_HEAD) gamma = (double)gate[h];
+        or_sequence(q + (size_t)bh * L * dk, k + (size_t)bh * L * dk,
+                    v + (size_t)bh * L * dv, g, gamma, L, dk, dv, mode, st,
+                    norm ? st + (size_t)dk * dv : NULL, out + (size_t)bh * L * dv);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+/* oracle_decode_step: one token per (b, h) on an existing state, in place.
+ * q, k: [B,H,dk]; v: [B,H,dv]; gate as above with L = 1; state: block layout
+ * as above; out: [B,H,dv]. It is oracle_forward at L = 1 from state. */
+int oracle_decode_step(const float *q, const float *k, const float *v,
+                       const float *gate, double *state, int B, int H, int dk,
+                       int dv, int mode, double *out, int nthreads)
+{
+    if (B < 0 || H < 0 || dk <= 0 || dv <= 0) return -1;
+    if ((mode & OR_GATE_HEAD) && (mode & OR_GATE_CHANNEL)) return -1;
+    if ((mode & (OR_GATE_HEAD | OR_GATE_CHANNEL)) && !gate) return -1;
+    const int norm = (mode & OR_NORMALIZE) != 0;
+    const size_t blk = (size_t)dk * dv + (norm ? (size_t)dk : 0);
+    const long nbh = (long)B * H;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (long bh = 0; bh < nbh; ++bh) {
+        const int h = (int)(bh % H);
+        double *st = state + (size_t)bh * blk;
+        const float *g = NULL;
+        double gamma = 1.0;
+        if (mode & OR_GATE_CHANNEL) g = gate + (size_t)bh * dk;
+        if (mode & OR_GATE_HEAD) gamma = (double)gate[h];
+        or_sequence(q + (size_t)bh * dk, k + (size_t)bh * dk, v + (size_t)bh * dv,
+                    g, gamma, 1, dk, dv, mode, st, norm ? st + (size_t)dk * dv : NULL,
+                    out + (size_t)bh * dv);
+    }
+    (void)nthreads;
+    return 0;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
