@@ -1,0 +1,133 @@
+/*
+ * la.h -- causal linear attention, retention and gated linear attention on one
+ * NVIDIA GB300 (sm_103a): the chunkwise-parallel forward pass and the
+ * single-token recurrent decode step.
+ *
+ * The operation (one (b, h) sequence; every (b, h) is independent):
+ *
+ *   S_t = diag(A_t) S_{t-1} + phi(k_t) v_t^T        S: d_k x d_v, S_0 = 0
+ *   z_t = A_t * z_{t-1} + phi(k_t)                  only with LA_NORMALIZE
+ *   out_t = phi(q_t)^T S_t                          read after the update
+ *   out_t = phi(q_t)^T S_t / (phi(q_t) . z_t)       with LA_NORMALIZE
+ *
+ * Sources: learnllm m22 "Linear & Recurrent Attention" -- "The Math: Linear
+ * Attention" (phi = elu + 1, S_i, Z_i, y_i), "Retention: Add a Decay to the
+ * State" (S_n = gamma S_{n-1} + k_n^T v_n), "The Three Faces of Retention"
+ * (chunkwise form) and "Interactive Exploration" (the gate A_t: 1 for linear
+ * attention, gamma for retention, input-dependent for gated linear attention);
+ * linear_sparse_attention.py, linear_attn_recurrent and linear_attn_chunkwise
+ * (self-inclusive read, ragged last chunk); "causal linear attention as an RNN"
+ * (S_0 = Z_0 = 0). The per-channel gate alpha = exp(logsigmoid(g) / 16) is the
+ * gated-linear-attention gate (Yang et al. 2023, named on the troisinh and
+ * learnllm pages) with temperature 16.
+ *
+ * Conventions for every call:
+ *  - All pointers are DEVICE pointers to row-major, contiguous arrays, each
+ *    16-byte aligned (LA_ERR_MISALIGNED otherwise). The caller owns every
+ *    buffer; outputs must not alias inputs.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *    The return value reports argument validation (done before any launch)
+ *    and launch errors; errors during execution surface at the caller's next
+ *    synchronisation.
+ *  - State block: per (b, h), S as fp32 [d_k][d_v], followed by z as fp32
+ *    [d_k] when LA_NORMALIZE is set. A state array is [B][H][block].
+ *  - Element type of q, k, v, out and the per-channel gate g: bf16 by default,
+ *    fp32 with LA_DTYPE_F32. Accumulation and the state are always fp32.
+ *  - d_k, d_v in {16, 32, 64, 128}.
+ */
+#ifndef RETENTION_GB300_LA_H
+#define RETENTION_GB300_LA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *la_stream_t;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad mode combination */
+    LA_ERR_UNSUPPORTED = -2, /* valid request this build does not run (e.g. d_k = 48) */
+    LA_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned */
+    LA_ERR_CUDA = -4,        /* a CUDA call or kernel launch failed */
+    LA_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out */
+    LA_ERR_INTERNAL = -6     /* an internal consistency check failed */
+} la_status;
+
+/* mode bits */
+#define LA_PHI_IDENTITY 0x0  /* phi(x) = x */
+#define LA_PHI_ELU1 0x1      /* phi(x) = elu(x) + 1 on q and k */
+#define LA_NORMALIZE 0x2     /* out = phi(q)S / phi(q).z; the state carries z */
+#define LA_GATE_NONE 0x0     /* A_t = 1 (linear attention) */
+#define LA_GATE_HEAD 0x4     /* retention: gate = const float gamma[H], A_t = gamma_h */
+#define LA_GATE_CHANNEL 0x8  /* gated: gate = g [B][H][L][d_k] (decode: [B][H][d_k]),
+                                same type as q; A_t = diag(exp(logsigmoid(g_t) / 16)) */
+#define LA_DTYPE_F32 0x10    /* q, k, v, g, out are fp32 instead of bf16 */
+#define LA_KERNEL_SIMT 0x20  /* la_chunk_fwd: force the general CUDA-core kernel */
+
+/*
+ * la_chunk_fwd -- the chunkwise-parallel forward pass over whole sequences,
+ * starting from S_0 = 0 (and z_0 = 0).
+ *
+ * Chunkwise form (learnllm m22 "The Three Faces of Retention";
+ * linear_sparse_attention.py linear_attn_chunkwise): the L tokens are cut into
+ * chunks of `chunk` tokens, the last one ragged. Inside a chunk the output is
+ * the causally masked (diagonal included) product (Q K^T (.) D) V with the
+ * decay D_ij = prod_{r=j+1..i} A_r; across chunks a fixed d_k x d_v state is
+ * carried, read by each query with the decay since the chunk start and
+ * advanced as S <- (decay over the chunk) S + sum_s (decay s -> chunk end)
+ * k_s^T v_s. The result equals the recurrence above up to rounding.
+ *
+ *   q, k   [B][H][L][d_k]     v, out [B][H][L][d_v]
+ *   gate   NULL (LA_GATE_NONE), const float gamma[H] (LA_GATE_HEAD, each in
+ *          [0, 1]) or g [B][H][L][d_k] (LA_GATE_CHANNEL)
+ *   final_state  NULL, or [B][H][block] fp32: the state after the last token
+ *   B, H >= 0; L >= 0 (L = 0 writes a zero final state and no output)
+ *   chunk  1..128. The tensor-core kernel (bf16, d_k = d_v = 128, chunk 64)
+ *          is chosen automatically; other cases run the general kernel, which
+ *          returns LA_ERR_UNSUPPORTED when its tiles do not fit on chip.
+ *   mode   LA_PHI_* | LA_NORMALIZE | LA_GATE_* | LA_DTYPE_F32 | LA_KERNEL_SIMT
+ *
+ * Scratch: when the batch has too few (b, h) sequences to fill the GPU, the
+ * gated tensor-core path splits each sequence into segments and takes
+ * stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`) for the
+ * per-segment states; a failed allocation returns LA_ERR_CUDA.
+ *
+ * Range of the tensor-core kernel: it factors the decay inside a chunk as
+ * exp(b_t - beta) * exp(beta - b_s) around the chunk's middle, which is exact
+ * in real arithmetic and stays in fp32/bf16 range while the log-decay over one
+ * chunk, per channel, is above -170 (retention: gamma^chunk > 1e-74).
+ */
+int la_chunk_fwd(const void *q, const void *k, const void *v, const void *gate,
+                 void *out, float *final_state, int B, int H, int L, int dk,
+                 int dv, int mode, int chunk, la_stream_t stream);
+
+/*
+ * la_decode_step -- one recurrent step for every (b, h), in place on `state`
+ * (learnllm m22 "Code: The Two Faces", the LinearAttentionState.step object;
+ * insideout lesson 16: S <- S + k v^T, z <- z + k, out = q^T S / (q . z)):
+ *
+ *   S <- diag(A) S + phi(k) v^T ; z <- A * z + phi(k) ; out = phi(q)^T S [/ phi(q).z]
+ *
+ *   q, k   [B][H][d_k]   v, out [B][H][d_v]   (bf16, or fp32 with LA_DTYPE_F32)
+ *   gate   NULL, const float gamma[H], or g [B][H][d_k]
+ *   state  [B][H][block] fp32, read and written in place (S, then z when
+ *          LA_NORMALIZE). A final_state of la_chunk_fwd continues here.
+ *   mode   LA_PHI_* | LA_NORMALIZE | LA_GATE_* | LA_DTYPE_F32
+ */
+int la_decode_step(const void *q, const void *k, const void *v, const void *gate,
+                   float *state, void *out, int B, int H, int dk, int dv, int mode,
+                   la_stream_t stream);
+
+/* A static, human-readable name for a la_status value. */
+const char *la_status_string(int status);
+
+/* Number of kernels this library has launched in this process (diagnostics). */
+unsigned long long la_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RETENTION_GB300_LA_H */

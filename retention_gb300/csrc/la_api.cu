@@ -1,0 +1,107 @@
+// la_api.cu -- the C ABI of include/la.h: argument validation, kernel choice,
+// status strings. Every check runs before any launch; nothing is allocated
+// here.
+#include <atomic>
+#include <stdint.h>
+
+#include "la_common.cuh"
+
+namespace {
+
+std::atomic<unsigned long long> g_launches{0};
+
+constexpr int kKnownModeBits = LA_PHI_ELU1 | LA_NORMALIZE | LA_GATE_HEAD | LA_GATE_CHANNEL |
+                               LA_DTYPE_F32 | LA_KERNEL_SIMT;
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_mode(int mode, const void *gate, bool decode) {
+    if (mode & ~kKnownModeBits) return LA_ERR_INVALID_ARG;
+    if (decode && (mode & LA_KERNEL_SIMT)) return LA_ERR_INVALID_ARG;
+    const bool gh = mode & LA_GATE_HEAD, gc = mode & LA_GATE_CHANNEL;
+    if (gh && gc) return LA_ERR_INVALID_ARG;
+    if ((gh || gc) && gate == nullptr) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int la_chunk_fwd(const void *q, const void *k, const void *v, const void *gate, void *out,
+                 float *final_state, int B, int H, int L, int dk, int dv, int mode, int chunk,
+                 la_stream_t stream) {
+    if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
+    if (chunk < 1 || chunk > 128) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
+    int rc = check_mode(mode, gate, false);
+    if (rc != LA_OK) return rc;
+    const long nbh = (long)B * H;
+    if (nbh > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool norm = mode & LA_NORMALIZE;
+    if (nbh == 0) return LA_OK;
+    if (L == 0) {
+        // an empty sequence leaves S_0 = 0 (and z_0 = 0)
+        if (final_state) {
+            if (!aligned16(final_state)) return LA_ERR_MISALIGNED;
+            const size_t blk = (size_t)dk * dv + (norm ? dk : 0);
+            if (cudaMemsetAsync(final_state, 0, (size_t)nbh * blk * sizeof(float), s) != cudaSuccess)
+                return LA_ERR_CUDA;
+        }
+        return LA_OK;
+    }
+    if (!q || !k || !v || !out) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LA_ERR_MISALIGNED;
+    if (final_state && !aligned16(final_state)) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_CHANNEL) && !aligned16(gate)) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
+
+    la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode, chunk};
+    int launches = 0;
+    if (!(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a))
+        rc = la::launch_chunk_tc(a, s, &launches);
+    else
+        rc = la::launch_chunk_simt(a, s, &launches);
+    g_launches += (unsigned long long)launches;
+    return rc;
+}
+
+int la_decode_step(const void *q, const void *k, const void *v, const void *gate, float *state,
+                   void *out, int B, int H, int dk, int dv, int mode, la_stream_t stream) {
+    if (B < 0 || H < 0) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
+    int rc = check_mode(mode, gate, true);
+    if (rc != LA_OK) return rc;
+    const long nbh = (long)B * H;
+    if (nbh > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
+    if (nbh == 0) return LA_OK;
+    if (!q || !k || !v || !state || !out) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(state))
+        return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_CHANNEL) && !aligned16(gate)) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
+    la::DecodeArgs a{q, k, v, gate, state, out, B, H, dk, dv, mode};
+    int launches = 0;
+    rc = la::launch_decode(a, reinterpret_cast<cudaStream_t>(stream), &launches);
+    g_launches += (unsigned long long)launches;
+    return rc;
+}
+
+const char *la_status_string(int status) {
+    switch (status) {
+        case LA_OK: return "LA_OK";
+        case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG: invalid argument";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: shape or mode not supported by this build";
+        case LA_ERR_MISALIGNED: return "LA_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+        case LA_ERR_CUDA: return "LA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device-side wait ran out";
+        case LA_ERR_INTERNAL: return "LA_ERR_INTERNAL: internal consistency check failed";
+        default: return "unknown la_status";
+    }
+}
+
+unsigned long long la_kernel_launches(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// la_common.cuh -- device helpers and internal launch interfaces shared by the
+// kernels of the library (never by the oracle).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/la.h"
+
+namespace la {
+
+// ---------------------------------------------------------------- elements
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// phi(x) = elu(x) + 1: x + 1 for x > 0, e^x otherwise (learnllm m22, "The Math:
+// Linear Attention"); the identity when elu1 is false.
+__device__ __forceinline__ float phi(float x, bool elu1) {
+    if (!elu1) return x;
+    return x > 0.f ? x + 1.f : expf(x);
+}
+
+// log(sigmoid(x)) without overflow in either tail.
+__device__ __forceinline__ float log_sigmoid(float x) {
+    return x >= 0.f ? -log1pf(expf(-x)) : x - log1pf(expf(x));
+}
+
+// Per-step log-decay of the per-channel gate: log alpha = logsigmoid(g) / 16.
+__device__ __forceinline__ float channel_log_decay(float g) { return log_sigmoid(g) * 0.0625f; }
+
+// ---------------------------------------------------------------- launches
+struct ChunkArgs {
+    const void *q, *k, *v, *gate;
+    void *out;
+    float *final_state;
+    int B, H, L, dk, dv, mode, chunk;
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v, *gate;
+    float *state;
+    void *out;
+    int B, H, dk, dv, mode;
+};
+
+// Each returns LA_OK or an la_status; `launches` counts kernels launched.
+int launch_chunk_simt(const ChunkArgs &a, cudaStream_t s, int *launches);
+int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
+int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
+bool chunk_tc_supports(const ChunkArgs &a);
+
+}  // namespace la

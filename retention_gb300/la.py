@@ -1,0 +1,141 @@
+"""Thin Python binding of ``include/la.h``: the same calls, argument
+marshalling only (torch CUDA tensors in, data pointers and sizes out). Every
+step of the computation runs in the CUDA library; if the library has not been
+built, or there is no CUDA device, the calls raise instead of computing
+anything another way.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+# mode bits (include/la.h)
+LA_PHI_IDENTITY = 0x0
+LA_PHI_ELU1 = 0x1
+LA_NORMALIZE = 0x2
+LA_GATE_NONE = 0x0
+LA_GATE_HEAD = 0x4
+LA_GATE_CHANNEL = 0x8
+LA_DTYPE_F32 = 0x10
+LA_KERNEL_SIMT = 0x20
+
+LA_OK = 0
+STATUS = {0: "LA_OK", -1: "LA_ERR_INVALID_ARG", -2: "LA_ERR_UNSUPPORTED", -3: "LA_ERR_MISALIGNED",
+          -4: "LA_ERR_CUDA", -5: "LA_ERR_TIMEOUT", -6: "LA_ERR_INTERNAL"}
+
+# every function include/la.h declares, with its ctypes signature
+_VP, _I = ctypes.c_void_p, ctypes.c_int
+SIGNATURES = {
+    "la_chunk_fwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
+    "la_decode_step": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
+    "la_status_string": ([_I], ctypes.c_char_p),
+    "la_kernel_launches": ([], ctypes.c_ulonglong),
+}
+
+_lib = None
+
+
+class LAError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s returned %d (%s)" % (fn, status, STATUS.get(status, "?")))
+
+
+def library_path():
+    return _build.LIB
+
+
+def load():
+    """Load the built library (building it is ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError("the CUDA library %s is not built; run __graft_entry__.build()" % path)
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def mode_bits(phi="elu1", normalize=False, gate=None, dtype=torch.bfloat16, simt=False):
+    m = LA_PHI_ELU1 if phi == "elu1" else LA_PHI_IDENTITY
+    if normalize:
+        m |= LA_NORMALIZE
+    if gate == "head":
+        m |= LA_GATE_HEAD
+    elif gate == "channel":
+        m |= LA_GATE_CHANNEL
+    elif gate is not None:
+        raise ValueError("gate must be None, 'head' or 'channel'")
+    if dtype == torch.float32:
+        m |= LA_DTYPE_F32
+    elif dtype != torch.bfloat16:
+        raise ValueError("q, k, v must be bfloat16 or float32")
+    if simt:
+        m |= LA_KERNEL_SIMT
+    return m
+
+
+def _dev(t, name):
+    if t is None:
+        return None
+    if not (isinstance(t, torch.Tensor) and t.is_cuda):
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def state_block(dk, dv, normalize):
+    return dk * dv + (dk if normalize else 0)
+
+
+def chunk_fwd(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None, chunk=64,
+              out=None, final_state=None, want_state=True, simt=False, stream=None):
+    """la_chunk_fwd over q, k [B,H,L,dk], v [B,H,L,dv]. Returns (out, final_state)."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, H, L, dv, dtype=q.dtype, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty(B, H, state_block(dk, dv, normalize), dtype=torch.float32,
+                                  device=q.device)
+    mode = mode_bits(phi, normalize, gate_kind, q.dtype, simt)
+    rc = load().la_chunk_fwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
+                             _dev(out, "out"), _dev(final_state, "final_state"),
+                             B, H, L, dk, dv, mode, chunk, _stream(stream))
+    if rc != LA_OK:
+        raise LAError("la_chunk_fwd", rc)
+    return out, final_state
+
+
+def decode_step(q, k, v, state, gate=None, *, phi="elu1", normalize=False, gate_kind=None,
+                out=None, stream=None):
+    """la_decode_step: q, k [B,H,dk], v [B,H,dv]; ``state`` [B,H,block] fp32 updated in place."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    mode = mode_bits(phi, normalize, gate_kind, q.dtype)
+    rc = load().la_decode_step(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
+                               _dev(state, "state"), _dev(out, "out"), B, H, dk, dv, mode,
+                               _stream(stream))
+    if rc != LA_OK:
+        raise LAError("la_decode_step", rc)
+    return out
+
+
+def kernel_launches():
+    return int(load().la_kernel_launches())

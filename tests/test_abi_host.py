@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI, no GPU needed: the library builds for
+sm_103a, loads, exports every function ``include/la.h`` declares, and rejects
+bad arguments before touching the GPU (these calls return during validation,
+so no CUDA work is issued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from retention_gb300 import build as la_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "la.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = la_build.build()
+    from retention_gb300 import la
+    return la.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = _declared()
+    for n in ("la_chunk_fwd", "la_decode_step", "la_status_string", "la_kernel_launches"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from retention_gb300 import la
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in la.SIGNATURES, name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, b"LA_OK"), (-1, b"LA_ERR_INVALID_ARG"), (-2, b"LA_ERR_UNSUPPORTED"),
+                       (-3, b"LA_ERR_MISALIGNED"), (-4, b"LA_ERR_CUDA"), (-5, b"LA_ERR_TIMEOUT"),
+                       (-6, b"LA_ERR_INTERNAL")]:
+        assert lib.la_status_string(code).startswith(name)
+    assert lib.la_status_string(12345) == b"unknown la_status"
+
+
+A = ctypes.c_void_p(0x10000)          # fake, 16-byte aligned, never dereferenced
+M = ctypes.c_void_p(0x10002)          # fake, misaligned
+
+
+def _fwd(lib, q=A, k=A, v=A, gate=None, out=A, st=None, B=1, H=1, L=8, dk=16, dv=16, mode=0,
+         chunk=4):
+    return lib.la_chunk_fwd(q, k, v, gate, out, st, B, H, L, dk, dv, mode, chunk, None)
+
+
+def _dec(lib, q=A, k=A, v=A, gate=None, st=A, out=A, B=1, H=1, dk=16, dv=16, mode=0):
+    return lib.la_decode_step(q, k, v, gate, st, out, B, H, dk, dv, mode, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=-1), -1), (dict(H=-2), -1), (dict(L=-1), -1),
+    (dict(chunk=0), -1), (dict(chunk=129), -1),
+    (dict(dk=48), -2), (dict(dv=256), -2), (dict(dk=0), -2),
+    (dict(mode=0x400), -1),                       # unknown bit
+    (dict(mode=0x4 | 0x8, gate=A), -1),           # both gates
+    (dict(mode=0x4), -1), (dict(mode=0x8), -1),   # gate mode, no gate
+    (dict(q=None), -1), (dict(out=None), -1),
+    (dict(q=M), -3), (dict(v=M), -3), (dict(out=M), -3), (dict(st=M), -3),
+    (dict(mode=0x8, gate=M), -3),
+])
+def test_chunk_fwd_validation(lib, kw, expect):
+    assert _fwd(lib, **kw) == expect
+
+
+def test_chunk_fwd_empty_batch_is_a_no_op(lib):
+    assert _fwd(lib, B=0) == 0
+    assert _fwd(lib, H=0, q=None, k=None, v=None, out=None) == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=-1), -1), (dict(dk=24), -2), (dict(mode=0x20), -1), (dict(mode=0x40), -1),
+    (dict(mode=0x8), -1), (dict(st=None), -1), (dict(st=M), -3), (dict(q=M), -3),
+])
+def test_decode_validation(lib, kw, expect):
+    assert _dec(lib, **kw) == expect

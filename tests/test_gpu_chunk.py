@@ -1,0 +1,139 @@
+"""GPU parity of la_chunk_fwd against the fp64 oracle on the same seeded
+inputs: the five workloads' chunk-forward shapes, the worked example, every
+mode, ragged lengths, several chunk sizes and the edge cases."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from parity import TOL, rel_err, run_gpu, run_oracle, to_dev
+from retention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_example.json")
+
+
+def _check(cfg, seed=0, chunk=None, simt=False, tol=None):
+    inp = W.chunk_inputs(cfg, seed)
+    out_ref, st_ref = run_oracle(inp, cfg)
+    out, st = run_gpu(inp, cfg, chunk=chunk, simt=simt)
+    tol = tol or TOL[cfg["dtype"]]
+    e_out, e_st = rel_err(out, out_ref), rel_err(st, st_ref)
+    assert e_out <= tol and e_st <= tol, (e_out, e_st)
+    return e_out, e_st
+
+
+# ------------------------------------------------------------------ fp32 path
+
+def test_tiny_workload():
+    _check(W.workload("tiny"))
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 3, 16])
+def test_worked_example_through_the_kernel(chunk):
+    """insideout lesson 16, Example 1.1 and "Your turn", zero-padded to d = 16:
+    (0.5, 3) after two tokens and (1.5, 2.5) after the third."""
+    gd = json.load(open(GOLDEN))
+    pad = lambda rows: torch.tensor([r + [0.0] * 14 for r in rows], dtype=torch.float32)[None, None]
+    inp = dict(q=pad(gd["queries"]), k=pad(gd["keys"]), v=pad(gd["values"]), gate=None)
+    cfg = W.workload("tiny", B=1, H=1, L=3, phi="identity", normalize=True)
+    out, st = run_gpu(inp, cfg, chunk=chunk)
+    np.testing.assert_allclose(out[0, 0, 1, :2], gd["after_two_tokens"]["out"], atol=1e-6)
+    np.testing.assert_allclose(out[0, 0, 2, :2], gd["after_three_tokens"]["out"], atol=1e-6)
+    S = st[0, 0, :256].reshape(16, 16)
+    np.testing.assert_allclose(S[:2, :2], gd["after_three_tokens"]["state_S"], atol=1e-6)
+    np.testing.assert_allclose(st[0, 0, 256:258], gd["after_three_tokens"]["state_z"], atol=1e-6)
+
+
+FP32_MODES = [
+    dict(phi="elu1", normalize=True, gate=None),
+    dict(phi="elu1", normalize=False, gate=None),
+    dict(phi="identity", normalize=False, gate=None),
+    dict(phi="identity", normalize=False, gate="head"),
+    dict(phi="elu1", normalize=True, gate="head"),
+    dict(phi="elu1", normalize=False, gate="channel"),
+    dict(phi="elu1", normalize=True, gate="channel"),
+    dict(phi="identity", normalize=False, gate="channel"),
+]
+
+
+@pytest.mark.parametrize("m", FP32_MODES, ids=lambda m: "%s-%s-%s" % (m["phi"], m["normalize"], m["gate"]))
+@pytest.mark.parametrize("L,chunk", [(13, 1), (13, 4), (13, 7), (13, 13), (77, 16), (77, 64), (200, 128)])
+def test_fp32_modes_chunks_ragged(m, L, chunk):
+    cfg = W.workload("tiny", B=2, H=3, L=L, dk=32, dv=16, gamma_step=1.0, **m)
+    _check(cfg, seed=L + chunk)
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 128), (128, 16), (64, 64), (128, 128)])
+def test_fp32_head_dims(dk, dv):
+    cfg = W.workload("tiny", B=1, H=2, L=70, dk=dk, dv=dv, gate="channel", normalize=False)
+    _check(cfg, seed=dk + dv, chunk=32)
+
+
+# ------------------------------------------------------------------ bf16, small
+
+BF16_SMALL = {
+    "la": dict(B=2, H=3, L=333),
+    "retention": dict(B=2, H=16, L=333),
+    "gla": dict(B=1, H=3, L=1000),
+}
+
+
+@pytest.mark.parametrize("name", list(BF16_SMALL))
+@pytest.mark.parametrize("simt", [False, True], ids=["default", "simt"])
+def test_bf16_small_ragged(name, simt):
+    cfg = W.workload(name, **BF16_SMALL[name])
+    _check(cfg, seed=3, simt=simt)
+
+
+@pytest.mark.parametrize("name", list(BF16_SMALL))
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 129])
+def test_bf16_chunk_boundaries(name, L):
+    cfg = W.workload(name, **dict(BF16_SMALL[name], L=L))
+    _check(cfg, seed=L)
+
+
+# ------------------------------------------------------------------ full size
+
+@pytest.mark.parametrize("name", ["la", "retention", "gla"])
+def test_full_size_workload(name):
+    """The full workloads, in the launch configuration the benchmark times,
+    compared element by element with the oracle."""
+    _check(W.workload(name))
+
+
+# ------------------------------------------------------------------ edges
+
+def test_empty_sequence_gives_zero_state():
+    from retention_gb300 import la
+    q = torch.zeros(2, 3, 0, 16, device="cuda")
+    st = torch.full((2, 3, 16 * 16 + 16), float("nan"), device="cuda")
+    out = torch.empty(2, 3, 0, 16, device="cuda")
+    la.chunk_fwd(q, q, torch.zeros(2, 3, 0, 16, device="cuda"), normalize=True, out=out,
+                 final_state=st, chunk=16)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(st).item() == 0
+
+
+def test_misaligned_and_missing_gate_are_rejected():
+    from retention_gb300 import la
+    base = torch.zeros(1 * 1 * 9 * 16 + 1, device="cuda")
+    q = base[1:].view(1, 1, 9, 16)             # 4-byte offset
+    good = torch.zeros(1, 1, 9, 16, device="cuda")
+    with pytest.raises(la.LAError) as e:
+        la.chunk_fwd(q, good, good, chunk=4)
+    assert e.value.status == -3
+    with pytest.raises(la.LAError) as e:
+        la.chunk_fwd(good, good, good, None, gate_kind="channel", chunk=4)
+    assert e.value.status == -1
+
+
+def test_launch_counter_advances():
+    from retention_gb300 import la
+    n0 = la.kernel_launches()
+    cfg = W.workload("tiny", L=16)
+    run_gpu(W.chunk_inputs(cfg), cfg)
+    assert la.kernel_launches() >= n0 + 1
