@@ -416,7 +416,8 @@ def main():
         v, cores, desc = oracle_sample(2)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
-    tc = la_res["launches_per_step"] == 1
+    tc = la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"],
+                           la.mode_bits(cfg["phi"], cfg["normalize"], cfg["gate"]), cfg["chunk"]) == 1
     kernel = "la_chunk_tc_kernel" if tc else "chunk_simt_kernel"
     srcs = ["retention_gb300/csrc/la_tc.cu" if tc else "retention_gb300/csrc/la_simt.cu",
             "retention_gb300/csrc/la_common.cuh"]

@@ -120,6 +120,14 @@ int la_decode_step(const void *q, const void *k, const void *v, const void *gate
                    float *state, void *out, int B, int H, int dk, int dv, int mode,
                    la_stream_t stream);
 
+/*
+ * la_chunk_fwd_path -- which kernel la_chunk_fwd would run for these sizes and
+ * mode on the current device, without launching anything: 1 = tensor-core
+ * kernel, 0 = general CUDA-core kernel, or a negative la_status for arguments
+ * la_chunk_fwd would reject. Diagnostics only.
+ */
+int la_chunk_fwd_path(int B, int H, int L, int dk, int dv, int mode, int chunk);
+
 /* A static, human-readable name for a la_status value. */
 const char *la_status_string(int status);
 

@@ -89,6 +89,16 @@ int la_decode_step(const void *q, const void *k, const void *v, const void *gate
     return rc;
 }
 
+int la_chunk_fwd_path(int B, int H, int L, int dk, int dv, int mode, int chunk) {
+    if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
+    if (chunk < 1 || chunk > 128) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
+    if (mode & ~kKnownModeBits) return LA_ERR_INVALID_ARG;
+    if ((mode & LA_GATE_HEAD) && (mode & LA_GATE_CHANNEL)) return LA_ERR_INVALID_ARG;
+    la::ChunkArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, L, dk, dv, mode, chunk};
+    return (!(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a)) ? 1 : 0;
+}
+
 const char *la_status_string(int status) {
     switch (status) {
         case LA_OK: return "LA_OK";

@@ -30,6 +30,7 @@ _VP, _I = ctypes.c_void_p, ctypes.c_int
 SIGNATURES = {
     "la_chunk_fwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_decode_step": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
+    "la_chunk_fwd_path": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "la_status_string": ([_I], ctypes.c_char_p),
     "la_kernel_launches": ([], ctypes.c_ulonglong),
 }
@@ -135,6 +136,11 @@ def decode_step(q, k, v, state, gate=None, *, phi="elu1", normalize=False, gate_
     if rc != LA_OK:
         raise LAError("la_decode_step", rc)
     return out
+
+
+def chunk_fwd_path(B, H, L, dk, dv, mode, chunk):
+    """1 = tensor-core kernel, 0 = general kernel, < 0 = rejected (la_status)."""
+    return int(load().la_chunk_fwd_path(B, H, L, dk, dv, mode, chunk))
 
 
 def kernel_launches():

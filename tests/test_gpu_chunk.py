@@ -137,3 +137,13 @@ def test_launch_counter_advances():
     cfg = W.workload("tiny", L=16)
     run_gpu(W.chunk_inputs(cfg), cfg)
     assert la.kernel_launches() >= n0 + 1
+
+
+@pytest.mark.parametrize("name", ["la", "retention", "gla"])
+def test_bf16_workloads_take_the_tensor_core_kernel(name):
+    from retention_gb300 import la
+    cfg = W.workload(name)
+    mode = la.mode_bits(cfg["phi"], cfg["normalize"], cfg["gate"])
+    assert la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], 128, 128, mode, 64) == 1
+    assert la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], 128, 128, mode | la.LA_KERNEL_SIMT, 64) == 0
+    assert la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], 128, 128, mode, 32) == 0
