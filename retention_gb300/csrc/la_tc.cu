@@ -4,31 +4,46 @@
 // Method (learnllm m22 "The Three Faces of Retention"; linear_sparse_attention.py
 // linear_attn_chunkwise; the gate A_t of learnllm m22 "Interactive Exploration").
 // Inside chunk n (c <= 64 tokens, local index t), with b_t[d] the inclusive
-// running sum of log A over the chunk and beta[d] = b at the chunk's middle:
+// running sum of log A over the chunk:
 //
-//   q~_t = phi(q_t) e^{b_t - beta}        k~_s = phi(k_s) e^{beta - b_s}
-//   P    = causal_mask(q~ k~^T)           (= sum_d phi(q)phi(k) e^{b_t - b_s})
-//   O^T  = V^T P^T + (diag(e^beta) S_{n-1})^T q~^T
-//   T_n  = diag(e^beta) S_{n-1} + k~^T V,  S_n = diag(e^{b_last - beta}) T_n
+//   q~_t = phi(q_t) e^{b_t}          k~_s = phi(k_s) e^{-b_s}
+//   P    = causal_mask(q~ k~^T)      (= sum_d phi(q)phi(k) e^{b_t - b_s}, s <= t)
+//   O    = q~ S_{n-1} + P V
+//   T_n  = S_{n-1} + k~^T V,         S_n = diag(e^{b_last}) T_n
 //
-// which is the chunkwise form with the decay factored around the chunk middle
-// (exact in real arithmetic; every factor stays within e^{+-|b_last|/2}). For
-// linear attention b = 0 and all factors are 1; for retention b_t = (t+1) ln
-// gamma. With the normaliser, z is carried the same way and
-// den_t = rowsum(P)_t + q~_t . (e^beta z_{n-1}).
+// which is the chunkwise form with the decay from the chunk start to t split
+// into a query factor and a key factor (exact in real arithmetic). For linear
+// attention b = 0 and every factor is 1; for retention b_t = (t+1) ln gamma.
 //
-// Tensor-core mapping (all M = 128, accumulators in TMEM, fp32):
-//   QK    D_P [128 x 64]   = q~ (K-major, rows 64..127 unused) . k~^T
-//   inter D_O [128 x 64]  += S'^T (MN-major bf16 copy of S') . q~^T
-//   S     D_S [128 x 128] += k~^T (MN-major) . V (MN-major)
-//   intra D_O             += V^T (MN-major) . P^T (K-major bf16 P)
-// O is produced transposed (lane = value channel), so every operand comes
-// straight from the TMA-written tiles with the 128-byte swizzle, except the
-// bf16 copies of P and S' which the threads write in the same layout.
+// The normaliser z is the state's column for a value that is always 1
+// (z_t = A_t z_{t-1} + phi(k_t)). With LA_NORMALIZE, V is widened by a
+// constant column of ones (N = 144 instead of 128), so the same MMAs carry z in
+// column 128 of the state and produce den_t = rowsum(P)_t + q~_t . z_{n-1} in
+// column 128 of O: out_t = O[t][0..127] / O[t][128].
 //
-// One CTA per (b, h): 4 warps. The S' copy, P masking and the epilogues run on
-// all threads between tcgen05 phases; q, k, v (and g) tiles stream through a
-// multi-stage TMA ring so the next chunks' loads overlap the current chunk.
+// Tensor-core work per chunk (all M = 128, fp32 accumulators in TMEM, NW = 128
+// or 144 value columns):
+//   QK    D_P [128 x 64]  = q~ (K-major, rows 64..127 unused) . k~^T (K-major)
+//   state D_S [128 x NW] += k~^T (MN-major) . [V | 1] (MN-major)     -> T_n
+//   inter D_O [128 x NW]  = q~ (K-major) . S' (MN-major bf16 copy of S_{n-1})
+//   intra D_O            += P (K-major bf16 P) . [V | 1] (MN-major)
+// q, k, v come straight from the 128-byte-swizzled TMA tiles; the threads write
+// the bf16 copies of P and S_{n-1} in the same layout.
+//
+// One CTA per (b, h), 16 warps with fixed roles, connected by mbarriers:
+//   warp 0       TMA producer: q, k, v (, g) tiles of chunk n into a ring of stages
+//   warp 1       MMA issuer (one thread) and TMEM owner
+//   warps 4-7    prologue: phi and decay factors in place on the q and k tiles
+//   warps 8-11   state chain: S_{n-1} = diag(f) T_{n-1} (rescaled in TMEM) and
+//                its bf16 copy for the inter MMA of chunk n; the final state
+//   warps 12-13  outputs: P mask -> bf16; O -> 1/den -> bf16 -> TMA store
+// O lives in two TMEM buffers (one with the normaliser, whose 144-column
+// accumulators leave no room for a second), so chunk n+1's MMAs overlap chunk
+// n's epilogue, and the state chain of chunk n+1 overlaps both.
+//
+// Every wait on an mbarrier is bounded (2 s of wall time); a role that runs
+// out leaves its loop (inside a warpgroup the decision is made uniform with
+// bar.red.or), sets a device error word and the CTA drains what it issued.
 #include <cudaTypedefs.h>
 #include <cstring>
 #include <mutex>
@@ -40,14 +55,14 @@ namespace la {
 namespace {
 using namespace sm100;
 
-constexpr int kC = 64;                 // chunk length
-constexpr int kD = 128;                // d_k = d_v
-constexpr int kThreads = 128;
-constexpr uint32_t kTile = kC * kD * 2;  // one bf16 [64 x 128] tile: 16 KiB (two 8 KiB swizzle blocks)
+constexpr int kC = 64;                   // chunk length
+constexpr int kD = 128;                  // d_k = d_v
+constexpr int kThreads = 512;            // 16 warps
+constexpr uint32_t kTile = kC * kD * 2;  // bf16 [64 x 128] tile: 16 KiB = two 8 KiB swizzle blocks
 constexpr uint32_t kHalf = 8192;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitNs = 2000000000ull;  // far beyond any legitimate wait
+constexpr uint32_t kBarPro = 1, kBarState = 2, kBarOut = 3;  // named barriers
 
 __device__ unsigned int g_tc_error;
 
@@ -58,19 +73,31 @@ struct TcParams {
     int H, L, mode;
 };
 
-template <int NS, int GATE>
+// Shared-memory layout. A stage holds q | k | v | (ones) | (g); the ones block
+// is the 64-column swizzle atom that follows v as the third N atom of [V | 1].
+template <int GATE, bool NORM>
 struct Layout {
-    static constexpr uint32_t stage = (GATE == 2 ? 4 : 3) * kTile;
-    static constexpr uint32_t P = NS * stage;            // bf16 P tile, 8 KiB
-    static constexpr uint32_t S = P + 8192;              // bf16 S' copy, 32 KiB
-    static constexpr uint32_t O = S + 32768;             // bf16 O staging, 16 KiB
-    static constexpr uint32_t Bt = O + 16384;            // fp32 b_t [64][128] (gated), 32 KiB
-    static constexpr uint32_t F = Bt + (GATE == 2 ? 32768 : 0);  // float scratch
-    // float scratch: zT, zU, zsum, beta, bc, beta_prev, bc_prev (128 each), dens, fq, fk (64 each)
-    static constexpr uint32_t nfloat = 7 * 128 + 3 * 64;
-    static constexpr uint32_t Bar = F + nfloat * 4;      // mbarriers
-    static constexpr uint32_t Misc = Bar + (NS + 2) * 8;  // tmem slot, abort flag
-    static constexpr uint32_t bytes = Misc + 16 + 1024;  // + alignment slack
+    static constexpr int NS = (NORM || GATE == 2) ? 2 : 3;
+    static constexpr uint32_t ones = 3 * kTile;                       // offset in a stage
+    static constexpr uint32_t g = 3 * kTile + (NORM ? kHalf : 0);      // offset in a stage
+    static constexpr uint32_t stage = g + (GATE == 2 ? kTile : 0);
+    static constexpr uint32_t P = NS * stage;          // bf16 P tile, 8 KiB
+    static constexpr uint32_t S = P + 8192;            // bf16 copy of S_{n-1} (+ z atom), 32 / 48 KiB
+    static constexpr uint32_t O = S + (NORM ? 49152 : 32768);  // bf16 O staging, two swizzled halves
+    static constexpr uint32_t F = O + 16384;           // floats: fbuf[NS][128] ffinal[128] fq[64] fk[64]
+    static constexpr uint32_t Bar = F + (NS * 128 + 128 + 128) * 4;
+    // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal, drain
+    static constexpr uint32_t nbar = 3 * NS + 12;
+    static constexpr uint32_t Misc = Bar + nbar * 8;  // TMEM base address
+    static constexpr uint32_t bytes = Misc + 16 + 1024;  // + slack for the 1024-byte alignment
+    // TMEM columns (region bases 32-column aligned). With the ones column the
+    // state and O accumulators are 144 wide and O has a single buffer.
+    static constexpr uint32_t NW = NORM ? 144 : 128;
+    static constexpr int NOB = NORM ? 1 : 2;           // O accumulator buffers
+    static constexpr uint32_t colS = 0;
+    static constexpr uint32_t colO0 = NORM ? 160 : 128;
+    static constexpr uint32_t colO1 = NORM ? 160 : 256;
+    static constexpr uint32_t colP = NORM ? 320 : 384;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -82,43 +109,63 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float load_bf16(const uint8_t *p) {
     return __uint_as_float(((uint32_t) * reinterpret_cast<const uint16_t *>(p)) << 16);
 }
-// log alpha = logsigmoid(g) / 16 with the hardware exp/log (absolute error
-// ~1e-7 before the / 16).
+__device__ __forceinline__ void store_bf16(uint8_t *p, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+// log alpha = logsigmoid(g) / 16 with the hardware exp/log
 __device__ __forceinline__ float log_decay_fast(float g) {
     return (fminf(g, 0.f) - __logf(1.f + __expf(-fabsf(g)))) * 0.0625f;
 }
-__device__ __forceinline__ float phi_fast(float x, bool elu1) {
-    return elu1 ? fmaxf(x, 0.f) + __expf(fminf(x, 0.f)) : x;
+template <bool ELU1>
+__device__ __forceinline__ float phi_t(float x) {
+    return ELU1 ? fmaxf(x, 0.f) + __expf(fminf(x, 0.f)) : x;
 }
 
-template <int NS, int GATE>
+template <int GATE, bool ELU1, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
-    using LY = Layout<NS, GATE>;
+    using LY = Layout<GATE, NORM>;
+    constexpr int NS = LY::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, h = bh % p.H, L = p.L;
-    const bool elu1 = p.mode & LA_PHI_ELU1, norm = p.mode & LA_NORMALIZE;
-    const int nchunks = (L + kC - 1) / kC;
+    const int N = (L + kC - 1) / kC;
+    const size_t blk = (size_t)kD * kD + (NORM ? kD : 0);
 
-    float *F = reinterpret_cast<float *>(sm + LY::F);
-    float *zT = F, *zU = F + 128, *zsum = F + 256, *beta = F + 384, *bc = F + 512;
-    float *beta_prev = F + 640, *bc_prev = F + 768, *dens = F + 896, *fq = F + 960, *fk = F + 1024;
-    float *Bt = reinterpret_cast<float *>(sm + LY::Bt);
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + LY::Bar);
-    uint64_t *bar_qk = full + NS, *bar_o = full + NS + 1;
+    float *fbuf = reinterpret_cast<float *>(sm + LY::F);  // [NS][128] state factor e^{b_last(n-1)}
+    float *ffinal = fbuf + NS * 128;                      // [128] e^{b_last} of the last chunk
+    float *fq = ffinal + 128;                             // [64] retention: gamma^(t+1)
+    float *fk = fq + 64;                                  // [64] retention: gamma^-(t+1)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::Bar);
+    uint64_t *full = bars, *empty = bars + NS, *pro = bars + 2 * NS;
+    uint64_t *ofull = bars + 3 * NS, *oempty = ofull + 2;
+    uint64_t *qk = oempty + 2, *pfull = qk + 1, *pempty = pfull + 1, *sdone = pempty + 1, *sfree = sdone + 1;
+    uint64_t *sready = sfree + 1, *profinal = sready + 1, *drain = profinal + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::Misc);
-    int bad = 0;  // this thread saw a bounded wait run out (block-wide OR at barriers)
     uint8_t *sP = sm + LY::P, *sS = sm + LY::S, *sO = sm + LY::O;
 
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
-        mbar_init(bar_qk, 1);
-        mbar_init(bar_o, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&pro[s], 128);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ofull[b], 1);
+            mbar_init(&oempty[b], 64);
+        }
+        mbar_init(qk, 1);
+        mbar_init(pfull, 64);
+        mbar_init(pempty, 64);
+        mbar_init(sdone, 1);
+        mbar_init(sfree, 1);
+        mbar_init(sready, 128);
+        mbar_init(profinal, 128);
+        mbar_init(drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
         tma_prefetch_desc(&p.tk);
@@ -126,127 +173,246 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         tma_prefetch_desc(&p.to);
         if (GATE == 2) tma_prefetch_desc(&p.tg);
     }
-    zT[tid] = 0.f;
-    float ln_gamma = 0.f;
-    if (GATE == 1) ln_gamma = __logf(p.gamma[h]);
+    if (NORM) {
+        // constant blocks: per stage a [64 x 64] atom whose column 0 is 1 (the
+        // ones column of [V | 1]); the z atom of the S' copy starts at zero
+        for (int i = tid; i < NS * 512; i += kThreads) {
+            const int s = i >> 9, r = (i >> 3) & 63, pc = i & 7;
+            const uint32_t one = (((pc ^ r) & 7) == 0) ? 0x3f80u : 0u;  // bf16 1.0 in element 0
+            *reinterpret_cast<uint4 *>(sm + s * LY::stage + LY::ones + r * 128 + pc * 16) = make_uint4(one, 0u, 0u, 0u);
+        }
+        for (int i = tid; i < 1024; i += kThreads)
+            reinterpret_cast<uint4 *>(sS + 32768)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    int bad = 0;
 
-    auto issue_load = [&](int stage, int chunk) {
-        uint8_t *base = sm + stage * LY::stage;
-        const int t0 = chunk * kC;
-        mbar_arrive_expect_tx(&full[stage], LY::stage);
-        tma_load_3d(base, &p.tq, &full[stage], 0, t0, bh);
-        tma_load_3d(base + kHalf, &p.tq, &full[stage], 64, t0, bh);
-        tma_load_3d(base + kTile, &p.tk, &full[stage], 0, t0, bh);
-        tma_load_3d(base + kTile + kHalf, &p.tk, &full[stage], 64, t0, bh);
-        tma_load_3d(base + 2 * kTile, &p.tv, &full[stage], 0, t0, bh);
-        tma_load_3d(base + 2 * kTile + kHalf, &p.tv, &full[stage], 64, t0, bh);
-        if (GATE == 2) {
-            tma_load_3d(base + 3 * kTile, &p.tg, &full[stage], 0, t0, bh);
-            tma_load_3d(base + 3 * kTile + kHalf, &p.tg, &full[stage], 64, t0, bh);
+    if (warp == 0) {
+        // ============================================================ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int n = 0; n < N; ++n) {
+                const int s = n % NS;
+                if (n >= NS && !mbar_wait(&empty[s], (uint32_t)(n / NS - 1) & 1u, kWaitNs)) {
+                    bad = 1;
+                    break;
+                }
+                uint8_t *base = sm + s * LY::stage;
+                const int t0 = n * kC;
+                mbar_arrive_expect_tx(&full[s], (GATE == 2 ? 4 : 3) * kTile);
+#pragma unroll 1
+                for (int tl = 0; tl < (GATE == 2 ? 4 : 3); ++tl) {
+                    const CUtensorMap *m = tl == 0 ? &p.tq : tl == 1 ? &p.tk : tl == 2 ? &p.tv : &p.tg;
+                    uint8_t *dst = base + (tl < 3 ? tl * kTile : LY::g);
+                    tma_load_3d(dst, m, &full[s], 0, t0, bh);
+                    tma_load_3d(dst + kHalf, m, &full[s], 64, t0, bh);
+                }
+                issued = n + 1;
+            }
+            // nothing may still be landing in shared memory when the CTA leaves
+            for (int m = issued > NS ? issued - NS : 0; m < issued; ++m)
+                if (!mbar_wait(&full[m % NS], (uint32_t)(m / NS) & 1u, kWaitNs)) bad = 1;
         }
-    };
-    if (tid == 0)
-        for (int s = 0; s < NS && s < nchunks; ++s) issue_load(s, s);
-
-    constexpr uint32_t id_qk = idesc_bf16(128, 64, false, false);
-    constexpr uint32_t id_o = idesc_bf16(128, 64, true, false);
-    constexpr uint32_t id_s = idesc_bf16(128, 128, true, true);
-
-    int n = 0;
-    for (; n < nchunks; ++n) {
-        const int s = n % NS;
-        const uint32_t ph = (uint32_t)(n / NS) & 1u;
-        const int t0 = n * kC, c = min(kC, L - t0);
-        uint8_t *sQ = sm + s * LY::stage, *sK = sQ + kTile, *sV = sK + kTile, *sG = sV + kTile;
-        if (!mbar_wait(&full[s], ph, kWaitNs)) bad = 1;
-
-        // ------------------------------------------------ prologue: phi, decay factors
-        const int mid = (c - 1) >> 1;
-        if (GATE == 2) {
-            const int d = tid;
-            const uint8_t *gcol = sG + (d >> 6) * kHalf;
-            float b = 0.f, bm = 0.f;
-            for (int t = 0; t < c; ++t) {
-                b += log_decay_fast(load_bf16(gcol + sw128_offset(t, d & 63)));
-                Bt[t * 128 + d] = b;
-                if (t == mid) bm = b;
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_qk = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t id_s = idesc_bf16(128, LY::NW, true, true);
+            constexpr uint32_t id_o = idesc_bf16(128, LY::NW, false, true);
+            const uint32_t sm0 = smem_u32(sm), s0 = smem_u32(sS), p0 = smem_u32(sP);
+            auto issue_qk = [&](int n) {
+                const uint32_t q0 = sm0 + (n % NS) * LY::stage, k0 = q0 + kTile;
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+                    umma_bf16(tmem + LY::colP, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024),
+                              id_qk, ks > 0);
+                }
+                umma_commit(qk);
+            };
+            if (N > 0) {
+                if (!mbar_wait(&pro[0], 0u, kWaitNs)) bad = 1;
+                tc_fence_after();
+                if (!bad) issue_qk(0);
             }
-            beta[d] = bm;
-            bc[d] = b;
-        } else if (GATE == 1) {
-            if (tid < 64) {
-                fq[tid] = __expf((float)(tid - mid) * ln_gamma);
-                fk[tid] = __expf((float)(mid - tid) * ln_gamma);
-            }
-            if (tid == 0) {
-                beta[0] = (float)(mid + 1) * ln_gamma;
-                bc[0] = (float)c * ln_gamma;
-            }
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {
-            const int pidx = it * kThreads + tid;
-            const int isk = pidx >> 10, pp = pidx & 1023;
-            const int kb = pp >> 9, row = (pp >> 3) & 63, pc = pp & 7;
-            const int col = kb * 64 + ((pc ^ row) & 7) * 8;
-            uint4 *addr = reinterpret_cast<uint4 *>((isk ? sK : sQ) + kb * kHalf + row * 128 + pc * 16);
-            uint4 w = *addr;
-            uint32_t u[4] = {w.x, w.y, w.z, w.w};
-            if (isk && row >= c) {
-                u[0] = u[1] = u[2] = u[3] = 0u;
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float x0 = phi_fast(bf16lo(u[e]), elu1), x1 = phi_fast(bf16hi(u[e]), elu1);
-                    if (GATE == 2) {
-                        const int d0 = col + 2 * e;
-                        const float e0 = Bt[row * 128 + d0] - beta[d0];
-                        const float e1 = Bt[row * 128 + d0 + 1] - beta[d0 + 1];
-                        x0 *= __expf(isk ? -e0 : e0);
-                        x1 *= __expf(isk ? -e1 : e1);
-                    } else if (GATE == 1) {
-                        const float f = isk ? fk[row] : fq[row];
-                        x0 *= f;
-                        x1 *= f;
+            for (int n = 0; n < N && !bad; ++n) {
+                const int s = n % NS, b = n % LY::NOB;
+                const uint32_t q0 = sm0 + s * LY::stage, k0 = q0 + kTile, v0 = q0 + 2 * kTile;
+                const uint32_t dO = tmem + (b ? LY::colO1 : LY::colO0);
+                if (n > 0 && !mbar_wait(sready, (uint32_t)(n - 1) & 1u, kWaitNs)) {
+                    bad = 1;
+                    break;
+                }
+                tc_fence_after();
+                // state: T_n = S_{n-1} (rescaled in place) + k~^T [V | 1]
+#pragma unroll 1
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16(tmem + LY::colS, sdesc_sw128(k0 + ks * 2048, kHalf, 1024),
+                              sdesc_sw128(v0 + ks * 2048, kHalf, 1024), id_s, (n > 0 || ks > 0));
+                umma_commit(sdone);
+                // inter: O = q~ S_{n-1}
+                if (n > 0) {
+                    if (n >= LY::NOB && !mbar_wait(&oempty[b], (uint32_t)((n - LY::NOB) / LY::NOB) & 1u, kWaitNs)) {
+                        bad = 1;
+                        break;
                     }
-                    u[e] = pack_bf16(x0, x1);
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_bf16(dO, sdesc_sw128(q0 + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024),
+                                  sdesc_sw128(s0 + ks * 2048, 16384, 1024), id_o, ks > 0);
+                }
+                umma_commit(sfree);
+                // intra: O += P [V | 1]
+                if (!mbar_wait(pfull, (uint32_t)n & 1u, kWaitNs)) {
+                    bad = 1;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16(dO, sdesc_sw128(p0 + ks * 32, 16, 1024), sdesc_sw128(v0 + ks * 2048, kHalf, 1024),
+                              id_o, (n > 0 || ks > 0));
+                umma_commit(&ofull[b]);
+                umma_commit(&empty[s]);
+                // QK of the next chunk (P is read out of TMEM by then)
+                if (n + 1 < N) {
+                    const int n1 = n + 1;
+                    if (!mbar_wait(&pro[n1 % NS], (uint32_t)(n1 / NS) & 1u, kWaitNs) ||
+                        !mbar_wait(pempty, (uint32_t)n & 1u, kWaitNs)) {
+                        bad = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_qk(n1);
                 }
             }
-            *addr = make_uint4(u[0], u[1], u[2], u[3]);
+            // every MMA this thread issued has completed before teardown
+            umma_commit(drain);
+            if (!mbar_wait(drain, 0u, kWaitNs)) bad = 1;
         }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // ------------------------------------------------ z increment and S' = diag(f) T
-        if (norm) {
-            const int d = tid;
-            const uint8_t *kcol = sK + (d >> 6) * kHalf;
-            float zs = 0.f;
-            for (int t = 0; t < c; ++t) zs += load_bf16(kcol + sw128_offset(t, d & 63));
-            zsum[d] = zs;
-        }
-        if (n > 0) {
-            const int i = tid;  // TMEM lane = state row (key channel)
-            float f = 1.f;
-            if (GATE == 2) f = __expf(bc_prev[i] - beta_prev[i] + beta[i]);
-            if (GATE == 1) f = __expf(bc_prev[0] - beta_prev[0] + beta[0]);
+    } else if (warp >= 4 && warp < 8) {
+        // ============================================================ prologue
+        const int d = tid - 128;
+        const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
+        float b_last = 0.f;  // log decay over the previous chunk (this channel)
+        for (int n = 0; n < N; ++n) {
+            const int s = n % NS, t0 = n * kC, c = min(kC, L - t0);
+            const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
+            if (named_sync_or(kBarPro, 128, !ok)) {
+                bad = 1;
+                break;
+            }
+            uint8_t *sQ = sm + s * LY::stage, *sK = sQ + kTile, *sG = sQ + LY::g;
+            fbuf[s * 128 + d] = GATE == 0 ? 1.f : __expf(b_last);
+            if (GATE == 1 && d < 64) {
+                fq[d] = __expf((float)(d + 1) * lg);
+                fk[d] = __expf(-(float)(d + 1) * lg);
+            }
+            if (GATE == 1) named_sync(kBarPro, 128);
+            if (GATE == 2) {
+                // one channel per thread: running log decay down the chunk
+                const uint32_t cb = (d >> 6) * kHalf;
+                float b = 0.f;
+#pragma unroll 1
+                for (int t = 0; t < c; ++t) {
+                    const uint32_t off = cb + sw128_offset(t, d & 63);
+                    b += log_decay_fast(load_bf16(sG + off));
+                    store_bf16(sQ + off, phi_t<ELU1>(load_bf16(sQ + off)) * __expf(b));
+                    store_bf16(sK + off, phi_t<ELU1>(load_bf16(sK + off)) * __expf(-b));
+                }
+#pragma unroll 1
+                for (int t = c; t < kC; ++t) store_bf16(sK + cb + sw128_offset(t, d & 63), 0.f);
+                b_last = b;
+            } else if (ELU1 || GATE == 1 || c < kC) {
+                // 16-byte pieces: this thread owns slot pc of rows r * 16 + d / 8
+                // (r = 0..3) in both 8 KiB blocks of the q and of the k tile.
+                const int pc = d & 7;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                const uint32_t ta = tmem + lane_base + kColS + 32 * j;
-                tmem_ld32(ta, r);
-                tmem_ld_wait();
-                if (GATE != 0) {
+                for (int isk = 0; isk < 2; ++isk) {
+                    uint8_t *tile = isk ? sK : sQ;
+                    uint4 w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        w[i] = *reinterpret_cast<const uint4 *>(tile + (i >> 2) * kHalf +
+                                                                ((i & 3) * 16 + (d >> 3)) * 128 + pc * 16);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = (i & 3) * 16 + (d >> 3);
+                        uint4 &x = w[i];
+                        if (isk && row >= c) {
+                            x = make_uint4(0u, 0u, 0u, 0u);
+                        } else if (ELU1 || GATE == 1) {
+                            const float fr = GATE == 1 ? (isk ? fk[row] : fq[row]) : 1.f;
+                            uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                u[e] = pack_bf16(phi_t<ELU1>(bf16lo(u[e])) * fr, phi_t<ELU1>(bf16hi(u[e])) * fr);
+                            x = make_uint4(u[0], u[1], u[2], u[3]);
+                        }
+                        *reinterpret_cast<uint4 *>(tile + (i >> 2) * kHalf + row * 128 + pc * 16) = x;
+                    }
+                }
+                if (GATE == 1) b_last = (float)c * lg;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&pro[s]);
+            if (GATE == 1) named_sync(kBarPro, 128);  // fq/fk are rewritten for the next chunk
+        }
+        if (!bad) {
+            ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
+            mbar_arrive(profinal);
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ============================================================ state chain
+        const int i = tid - 256;  // TMEM lane = state row (key channel)
+        const uint32_t tS = tmem + lane_base + LY::colS;
+        for (int n = 1; n < N; ++n) {
+            bool ok = mbar_wait(sdone, (uint32_t)(n - 1) & 1u, kWaitNs);
+            if (GATE != 0) ok = ok && mbar_wait(&pro[n % NS], (uint32_t)(n / NS) & 1u, kWaitNs);
+            if (named_sync_or(kBarState, 128, !ok)) {
+                bad = 1;
+                break;
+            }
+            tc_fence_after();
+            const float f = fbuf[(n % NS) * 128 + i];
+            if (GATE != 0) {
+                // S_{n-1} = diag(f) T_{n-1}, in place (z rides in column 128)
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + 32 * j, r);
+                    tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-                    tmem_st32(ta, r);
+                    tmem_st32(tS + 32 * j, r);
                 }
+                if (NORM) {
+                    uint32_t z;
+                    tmem_ld1(tS + 128, z);
+                    tmem_ld_wait();
+                    tmem_st1(tS + 128, __float_as_uint(__uint_as_float(z) * f));
+                }
+                tmem_st_wait();
+            }
+            // the inter MMA of chunk n-1 has finished reading the previous copy
+            ok = mbar_wait(sfree, (uint32_t)(n - 1) & 1u, kWaitNs);
+            if (named_sync_or(kBarState, 128, !ok)) {
+                bad = 1;
+                break;
+            }
+            // bf16 copy, MN-major for the B operand: line i, value columns v
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tS + 32 * j, r);
+                tmem_ld_wait();
+                uint8_t *row = sS + (j >> 1) * 16384 + i * 128;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int lc = 4 * (j & 1) + q4;
@@ -255,175 +421,135 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     w.y = pack_bf16(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
                     w.z = pack_bf16(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
                     w.w = pack_bf16(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
-                    *reinterpret_cast<uint4 *>(sS + (j >> 1) * 16384 + i * 128 + ((lc ^ (i & 7)) << 4)) = w;
+                    *reinterpret_cast<uint4 *>(row + ((lc ^ (i & 7)) << 4)) = w;
                 }
             }
-            if (GATE != 0) tmem_st_wait();
-            if (norm) zU[i] = f * zT[i];
-        } else if (norm) {
-            zU[tid] = 0.f;
+            if (NORM) {
+                uint32_t z;
+                tmem_ld1(tS + 128, z);
+                tmem_ld_wait();
+                *reinterpret_cast<uint4 *>(sS + 32768 + i * 128 + ((i & 7) << 4)) =
+                    make_uint4(pack_bf16(__uint_as_float(z), 0.f), 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(sready);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(bad)) {
-            bad = 1;
-            break;
+        if (!bad && N > 0) {
+            bool ok = mbar_wait(sdone, (uint32_t)(N - 1) & 1u, kWaitNs) && mbar_wait(profinal, 0u, kWaitNs);
+            if (named_sync_or(kBarState, 128, !ok)) {
+                bad = 1;
+            } else if (p.final_state != nullptr) {
+                tc_fence_after();
+                const float ff = ffinal[i];
+                float *dst = p.final_state + (size_t)bh * blk + (size_t)i * kD;
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + 32 * j, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        reinterpret_cast<float4 *>(dst + 32 * j)[q4] = make_float4(
+                            __uint_as_float(r[4 * q4]) * ff, __uint_as_float(r[4 * q4 + 1]) * ff,
+                            __uint_as_float(r[4 * q4 + 2]) * ff, __uint_as_float(r[4 * q4 + 3]) * ff);
+                }
+                if (NORM) {
+                    uint32_t z;
+                    tmem_ld1(tS + 128, z);
+                    tmem_ld_wait();
+                    p.final_state[(size_t)bh * blk + (size_t)kD * kD + i] = __uint_as_float(z) * ff;
+                }
+            }
         }
-
-        // ------------------------------------------------ MMA group 1: QK, inter, state
-        if (tid == 0) {
+    } else if (warp == 12 || warp == 13) {
+        // ============================================================ outputs (TMEM lanes 0..63 = rows t)
+        const int t = tid - 384;
+        for (int n = 0; n < N; ++n) {
+            const int b = n % LY::NOB, t0 = n * kC;
+            bool ok = mbar_wait(qk, (uint32_t)n & 1u, kWaitNs);
+            if (named_sync_or(kBarOut, 64, !ok)) {
+                bad = 1;
+                break;
+            }
             tc_fence_after();
-            const uint32_t q0 = smem_u32(sQ), k0 = smem_u32(sK), v0 = smem_u32(sV);
+            {
+                // P row t: causal mask (key <= t), bf16, K-major A operand of intra
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem + lane_base + LY::colP, r0);
+                tmem_ld32(tmem + lane_base + LY::colP + 32, r1);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(pempty);
+                uint8_t *prow = sP + t * 128;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-                umma_bf16(tmem + kColP, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024),
-                          id_qk, ks > 0);
-            }
-            umma_commit(bar_qk);
-            if (n > 0) {
-                const uint32_t s0 = smem_u32(sS);
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    uint32_t u[4];
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t offb = (ks >> 2) * kHalf + (ks & 3) * 32;
-                    umma_bf16(tmem + kColO, sdesc_sw128(s0 + ks * 2048, 16384, 1024),
-                              sdesc_sw128(q0 + offb, 16, 1024), id_o, ks > 0);
+                    for (int e = 0; e < 4; ++e) {
+                        const int jj = q8 * 8 + 2 * e;
+                        const uint32_t a0 = q8 < 4 ? r0[jj] : r1[jj - 32];
+                        const uint32_t a1 = q8 < 4 ? r0[jj + 1] : r1[jj - 31];
+                        u[e] = pack_bf16(jj <= t ? __uint_as_float(a0) : 0.f, jj + 1 <= t ? __uint_as_float(a1) : 0.f);
+                    }
+                    *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
                 }
             }
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(tmem + kColS, sdesc_sw128(k0 + ks * 2048, kHalf, 1024),
-                          sdesc_sw128(v0 + ks * 2048, kHalf, 1024), id_s, (n > 0 || ks > 0));
-        }
+            fence_proxy_async_smem();
+            mbar_arrive(pfull);
 
-        // ------------------------------------------------ P: mask, bf16, row sums
-        if (!mbar_wait(bar_qk, (uint32_t)n & 1u, kWaitNs)) bad = 1;
-        tc_fence_after();
-        if (warp < 2) {
-            const int t = tid;
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tmem + lane_base + kColP, r0);
-            tmem_ld32(tmem + lane_base + kColP + 32, r1);
-            tmem_ld_wait();
-            float rs = 0.f;
-#pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) {
-                uint32_t u[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j0 = q8 * 8 + 2 * e;
-                    const uint32_t a0 = q8 < 4 ? r0[j0] : r1[j0 - 32];
-                    const uint32_t a1 = q8 < 4 ? r0[j0 + 1] : r1[j0 + 1 - 32];
-                    const float x0 = j0 <= t ? __uint_as_float(a0) : 0.f;
-                    const float x1 = j0 + 1 <= t ? __uint_as_float(a1) : 0.f;
-                    u[e] = pack_bf16(x0, x1);
-                    rs += bf16lo(u[e]) + bf16hi(u[e]);
-                }
-                *reinterpret_cast<uint4 *>(sP + t * 128 + (((q8 ^ t) & 7) << 4)) =
-                    make_uint4(u[0], u[1], u[2], u[3]);
+            ok = mbar_wait(&ofull[b], (uint32_t)(n / LY::NOB) & 1u, kWaitNs);
+            if (t == 0) bulk_wait_read<0>();  // the previous O tile has left the staging buffer
+            if (named_sync_or(kBarOut, 64, !ok)) {
+                bad = 1;
+                break;
             }
-            if (norm) {
-                float den = rs;
-#pragma unroll 4
-                for (int c16 = 0; c16 < 16; ++c16) {
-                    const int kb = c16 >> 3, lc = c16 & 7;
-                    const uint4 w = *reinterpret_cast<const uint4 *>(sQ + kb * kHalf + t * 128 + (((lc ^ t) & 7) << 4));
-                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-                    const float *z8 = zU + kb * 64 + lc * 8;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) den += bf16lo(u[e]) * z8[2 * e] + bf16hi(u[e]) * z8[2 * e + 1];
-                }
-                dens[t] = den;
-            }
-        }
-        fence_proxy_async_smem();
-        if (tid == 0) bulk_wait_read<0>();  // the previous O tile has left the staging buffer
-        tc_fence_before();
-        __syncthreads();
-
-        // ------------------------------------------------ MMA group 2: intra
-        if (tid == 0) {
             tc_fence_after();
-            const uint32_t v0 = smem_u32(sV), p0 = smem_u32(sP);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(tmem + kColO, sdesc_sw128(v0 + ks * 2048, kHalf, 1024),
-                          sdesc_sw128(p0 + ks * 32, 16, 1024), id_o, (n > 0 || ks > 0));
-            umma_commit(bar_o);
-        }
-        if (!mbar_wait(bar_o, (uint32_t)n & 1u, kWaitNs)) bad = 1;
-        tc_fence_after();
-
-        // ------------------------------------------------ O epilogue: lane = value channel
-        {
-            const int v = tid;
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tmem + lane_base + kColO, r0);
-            tmem_ld32(tmem + lane_base + kColO + 32, r1);
-            tmem_ld_wait();
-            __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sO);
-#pragma unroll
-            for (int t = 0; t < 64; ++t) {
-                float o = __uint_as_float(t < 32 ? r0[t] : r1[t - 32]);
-                if (norm) o = o / dens[t];
-                stg[t * 128 + v] = __float2bfloat16_rn(o);
+            const uint32_t tO = tmem + lane_base + (b ? LY::colO1 : LY::colO0);
+            float rden = 1.f;
+            if (NORM) {
+                uint32_t dd;
+                tmem_ld1(tO + 128, dd);
+                tmem_ld_wait();
+                rden = 1.f / __uint_as_float(dd);
             }
-            if (norm) zT[v] = zU[v] + zsum[v];
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tO + 32 * j, r);
+                tmem_ld_wait();
+                // staging: two [64 x 64] halves with the 128-byte swizzle (TMA store box 64 x 64)
+                uint8_t *row = sO + (j >> 1) * 8192 + t * 128;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int lc = 4 * (j & 1) + q4;
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(r[8 * q4 + 0]) * rden, __uint_as_float(r[8 * q4 + 1]) * rden);
+                    w.y = pack_bf16(__uint_as_float(r[8 * q4 + 2]) * rden, __uint_as_float(r[8 * q4 + 3]) * rden);
+                    w.z = pack_bf16(__uint_as_float(r[8 * q4 + 4]) * rden, __uint_as_float(r[8 * q4 + 5]) * rden);
+                    w.w = pack_bf16(__uint_as_float(r[8 * q4 + 6]) * rden, __uint_as_float(r[8 * q4 + 7]) * rden);
+                    *reinterpret_cast<uint4 *>(row + ((lc ^ (t & 7)) << 4)) = w;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&oempty[b]);
+            fence_proxy_async_smem();
+            named_sync(kBarOut, 64);
+            if (t == 0) {
+                tma_store_3d(&p.to, sO, 0, t0, bh);
+                tma_store_3d(&p.to, sO + 8192, 64, t0, bh);
+                bulk_commit();
+            }
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(bad)) bad = 1;
-        if (GATE == 2) {
-            bc_prev[tid] = bc[tid];
-            beta_prev[tid] = beta[tid];
-        } else if (GATE == 1 && tid == 0) {
-            bc_prev[0] = bc[0];
-            beta_prev[0] = beta[0];
-        }
-        if (bad) break;
-        if (tid == 0) {
-            tma_store_3d(&p.to, sO, 0, t0, bh);
-            bulk_commit();
-            if (n + NS < nchunks) issue_load(s, n + NS);
-        }
+        if (t == 0) bulk_wait<0>();
     }
 
-    // ------------------------------------------------ final state S = diag(r) T, z
+    // ============================================================ teardown
     const int aborted = __syncthreads_or(bad);
-    if (!aborted && p.final_state != nullptr) {
-        tc_fence_after();
-        const int i = tid;
-        float f = 1.f;
-        if (GATE == 2) f = __expf(bc_prev[i] - beta_prev[i]);
-        if (GATE == 1) f = __expf(bc_prev[0] - beta_prev[0]);
-        const size_t blk = (size_t)kD * kD + (norm ? kD : 0);
-        float *dst = p.final_state + (size_t)bh * blk + (size_t)i * kD;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + kColS + 32 * j, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                reinterpret_cast<float4 *>(dst + 32 * j)[q4] =
-                    make_float4(__uint_as_float(r[4 * q4]) * f, __uint_as_float(r[4 * q4 + 1]) * f,
-                                __uint_as_float(r[4 * q4 + 2]) * f, __uint_as_float(r[4 * q4 + 3]) * f);
-        }
-        if (norm) p.final_state[(size_t)bh * blk + (size_t)kD * kD + i] = f * zT[i];
-    }
-    if (aborted) {
-        // drain what is in flight before leaving: issued loads, MMAs, stores
-        if (tid == 0) {
-            atomicOr(&g_tc_error, 1u);
-            for (int k2 = n; k2 < nchunks && k2 < n + NS; ++k2)
-                mbar_wait(&full[k2 % NS], (uint32_t)(k2 / NS) & 1u, kWaitNs);
-            mbar_wait(bar_o, (uint32_t)n & 1u, kWaitNs);
-        }
-    }
-    if (tid == 0) bulk_wait<0>();
+    if (aborted && tid == 0) atomicOr(&g_tc_error, 1u);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -445,27 +571,35 @@ bool get_encode() {
     return g_encode != nullptr;
 }
 
-// [BH][L][128] bf16 viewed as a 3-D tensor {128, L, BH}; box {box_x, 64, 1}.
-bool make_map(CUtensorMap *m, const void *base, int L, int BH, uint32_t box_x, bool swizzle) {
+// [BH][L][128] bf16 viewed as a 3-D tensor {128, L, BH}; box {64, 64, 1} with
+// the 128-byte swizzle (every load and store of this kernel uses that box).
+bool make_map(CUtensorMap *m, const void *base, int L, int BH) {
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L, (cuuint64_t)BH};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)L * kD * 2};
-    cuuint32_t box[3] = {box_x, (cuuint32_t)kC, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-template <int NS, int GATE>
+template <int GATE, bool ELU1, bool NORM>
 int launch_t(const TcParams &prm, int grid, cudaStream_t s) {
-    using LY = Layout<NS, GATE>;
-    auto kern = la_chunk_tc_kernel<NS, GATE>;
+    using LY = Layout<GATE, NORM>;
+    static_assert(LY::bytes <= 232448, "shared memory budget");
+    static_assert(LY::colP + 64 <= kTmemCols && LY::colO1 + LY::NW <= LY::colP, "TMEM budget");
+    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes) != cudaSuccess)
         return LA_ERR_CUDA;
     kern<<<grid, kThreads, LY::bytes, s>>>(prm);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+template <int GATE>
+int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm) {
+    if (elu1) return norm ? launch_t<GATE, true, true>(prm, grid, s) : launch_t<GATE, true, false>(prm, grid, s);
+    return norm ? launch_t<GATE, false, true>(prm, grid, s) : launch_t<GATE, false, false>(prm, grid, s);
 }
 
 }  // namespace
@@ -483,23 +617,24 @@ int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches) {
     const int BH = a.B * a.H;
     TcParams prm;
     memset(&prm, 0, sizeof(prm));
-    if (!make_map(&prm.tq, a.q, a.L, BH, 64, true) || !make_map(&prm.tk, a.k, a.L, BH, 64, true) ||
-        !make_map(&prm.tv, a.v, a.L, BH, 64, true) || !make_map(&prm.to, a.out, a.L, BH, 128, false))
+    if (!make_map(&prm.tq, a.q, a.L, BH) || !make_map(&prm.tk, a.k, a.L, BH) ||
+        !make_map(&prm.tv, a.v, a.L, BH) || !make_map(&prm.to, a.out, a.L, BH))
         return LA_ERR_CUDA;
     const bool gch = a.mode & LA_GATE_CHANNEL, ghd = a.mode & LA_GATE_HEAD;
-    if (gch && !make_map(&prm.tg, a.gate, a.L, BH, 64, true)) return LA_ERR_CUDA;
+    if (gch && !make_map(&prm.tg, a.gate, a.L, BH)) return LA_ERR_CUDA;
     prm.gamma = ghd ? static_cast<const float *>(a.gate) : nullptr;
     prm.final_state = a.final_state;
     prm.H = a.H;
     prm.L = a.L;
     prm.mode = a.mode;
+    const bool elu1 = a.mode & LA_PHI_ELU1, norm = a.mode & LA_NORMALIZE;
     int rc;
     if (gch)
-        rc = launch_t<2, 2>(prm, BH, s);
+        rc = launch_g<2>(prm, BH, s, elu1, norm);
     else if (ghd)
-        rc = launch_t<3, 1>(prm, BH, s);
+        rc = launch_g<1>(prm, BH, s, elu1, norm);
     else
-        rc = launch_t<3, 0>(prm, BH, s);
+        rc = launch_g<0>(prm, BH, s, elu1, norm);
     if (rc == LA_OK) *launches += 1;
     return rc;
 }
