@@ -31,8 +31,8 @@
 // the bf16 copies of P and S_{n-1} in the same layout.
 //
 // One CTA per (b, h), 16 warps with fixed roles, connected by mbarriers:
-//   warp 0       TMA producer: q, k, v (, g) tiles of chunk n into a ring of stages
-//   warp 1       MMA issuer (one thread) and TMEM owner
+//   warp 2       TMA producer: q, k, v (, g) tiles of chunk n into a ring of stages
+//   warp 3       MMA issuer (one thread) and TMEM owner
 //   warps 4-7    prologue: phi and decay factors in place on the q and k tiles
 //   warps 8-11   state chain: S_{n-1} = diag(f) T_{n-1} (rescaled in TMEM) and
 //                its bf16 copy for the inter MMA of chunk n; the final state
@@ -62,7 +62,10 @@ constexpr uint32_t kTile = kC * kD * 2;  // bf16 [64 x 128] tile: 16 KiB = two 8
 constexpr uint32_t kHalf = 8192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;  // far beyond any legitimate wait
-constexpr uint32_t kBarPro = 1, kBarState = 2, kBarOut = 3;  // named barriers
+constexpr int kBarPro = 1, kBarState = 2, kBarOut = 3;  // named barrier ids
+// The producer and the MMA issuer sit on the SM sub-partitions (warp % 4) that
+// host the fewest busy warps, so their short instruction streams issue promptly.
+constexpr int kWarpProducer = 2, kWarpMma = 3;
 
 __device__ unsigned int g_tc_error;
 
@@ -120,6 +123,20 @@ template <bool ELU1>
 __device__ __forceinline__ float phi_t(float x) {
     return ELU1 ? fmaxf(x, 0.f) + __expf(fminf(x, 0.f)) : x;
 }
+// elu(x) + 1 on two packed bf16 values in bf16 arithmetic:
+// max(x, 0) + 2^(min(x, 0) * log2 e). The exponent argument is rounded to bf16,
+// so for x < 0 the result carries a relative error below 2^-8 |x| on top of the
+// bf16 rounding the tensor-core operand needs anyway.
+__device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
+    const uint32_t zero = 0u, log2e = 0x3FB93FB9u;  // bf16(log2 e) in both halves
+    uint32_t m, y, e, pos, r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(x), "r"(zero));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(m), "r"(log2e));
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(pos) : "r"(x), "r"(zero));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(pos), "r"(e));
+    return r;
+}
 
 template <int GATE, bool ELU1, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
@@ -144,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::Misc);
     uint8_t *sP = sm + LY::P, *sS = sm + LY::S, *sO = sm + LY::O;
 
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -192,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int bad = 0;
 
-    if (warp == 0) {
+    if (warp == kWarpProducer) {
         // ============================================================ TMA producer
         if (lane == 0) {
             int issued = 0;
@@ -218,20 +235,27 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             for (int m = issued > NS ? issued - NS : 0; m < issued; ++m)
                 if (!mbar_wait(&full[m % NS], (uint32_t)(m / NS) & 1u, kWaitNs)) bad = 1;
         }
-    } else if (warp == 1) {
+    } else if (warp == kWarpMma) {
         // ============================================================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, 64, false, false);
             constexpr uint32_t id_s = idesc_bf16(128, LY::NW, true, true);
             constexpr uint32_t id_o = idesc_bf16(128, LY::NW, false, true);
-            const uint32_t sm0 = smem_u32(sm), s0 = smem_u32(sS), p0 = smem_u32(sP);
+            // descriptors at each operand's base; a K step adds (bytes >> 4) to the
+            // start-address field, which never carries out of its 14 bits here
+            const uint32_t sm0 = smem_u32(sm);
+            const uint64_t dS = sdesc_sw128(smem_u32(sS), 16384, 1024);   // S' copy, MN-major
+            const uint64_t dP = sdesc_sw128(smem_u32(sP), 16, 1024);      // P, K-major
+            auto dq = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage, 16, 1024); };
+            auto dkk = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + kTile, 16, 1024); };
+            auto dkm = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + kTile, kHalf, 1024); };
+            auto dvm = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + 2 * kTile, kHalf, 1024); };
             auto issue_qk = [&](int n) {
-                const uint32_t q0 = sm0 + (n % NS) * LY::stage, k0 = q0 + kTile;
-#pragma unroll 1
+                const uint64_t a = dq(n), bb = dkk(n);
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-                    umma_bf16(tmem + LY::colP, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024),
-                              id_qk, ks > 0);
+                    const uint64_t off = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
+                    umma_bf16(tmem + LY::colP, a + off, bb + off, id_qk, ks > 0);
                 }
                 umma_commit(qk);
             };
@@ -242,18 +266,17 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             for (int n = 0; n < N && !bad; ++n) {
                 const int s = n % NS, b = n % LY::NOB;
-                const uint32_t q0 = sm0 + s * LY::stage, k0 = q0 + kTile, v0 = q0 + 2 * kTile;
                 const uint32_t dO = tmem + (b ? LY::colO1 : LY::colO0);
+                const uint64_t aq = dq(n), ak = dkm(n), bv = dvm(n);
                 if (n > 0 && !mbar_wait(sready, (uint32_t)(n - 1) & 1u, kWaitNs)) {
                     bad = 1;
                     break;
                 }
                 tc_fence_after();
                 // state: T_n = S_{n-1} (rescaled in place) + k~^T [V | 1]
-#pragma unroll 1
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16(tmem + LY::colS, sdesc_sw128(k0 + ks * 2048, kHalf, 1024),
-                              sdesc_sw128(v0 + ks * 2048, kHalf, 1024), id_s, (n > 0 || ks > 0));
+                    umma_bf16(tmem + LY::colS, ak + ks * 128, bv + ks * 128, id_s, (n > 0 || ks > 0));
                 umma_commit(sdone);
                 // inter: O = q~ S_{n-1}
                 if (n > 0) {
@@ -262,10 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         break;
                     }
                     tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        umma_bf16(dO, sdesc_sw128(q0 + (ks >> 2) * kHalf + (ks & 3) * 32, 16, 1024),
-                                  sdesc_sw128(s0 + ks * 2048, 16384, 1024), id_o, ks > 0);
+                        umma_bf16(dO, aq + (((ks >> 2) * kHalf + (ks & 3) * 32) >> 4), dS + ks * 128, id_o, ks > 0);
                 }
                 umma_commit(sfree);
                 // intra: O += P [V | 1]
@@ -274,10 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     break;
                 }
                 tc_fence_after();
-#pragma unroll 1
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16(dO, sdesc_sw128(p0 + ks * 32, 16, 1024), sdesc_sw128(v0 + ks * 2048, kHalf, 1024),
-                              id_o, (n > 0 || ks > 0));
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) umma_bf16(dO, dP + ks * 2, bv + ks * 128, id_o, (n > 0 || ks > 0));
                 umma_commit(&ofull[b]);
                 umma_commit(&empty[s]);
                 // QK of the next chunk (P is read out of TMEM by then)
@@ -304,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         for (int n = 0; n < N; ++n) {
             const int s = n % NS, t0 = n * kC, c = min(kC, L - t0);
             const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
-            if (named_sync_or(kBarPro, 128, !ok)) {
+            if (named_sync_or<kBarPro, 128>(!ok)) {
                 bad = 1;
                 break;
             }
@@ -314,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 fq[d] = __expf((float)(d + 1) * lg);
                 fk[d] = __expf(-(float)(d + 1) * lg);
             }
-            if (GATE == 1) named_sync(kBarPro, 128);
+            if (GATE == 1) named_sync<kBarPro, 128>();
             if (GATE == 2) {
                 // one channel per thread: running log decay down the chunk
                 const uint32_t cb = (d >> 6) * kHalf;
@@ -336,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll
                 for (int isk = 0; isk < 2; ++isk) {
                     uint8_t *tile = isk ? sK : sQ;
+                    const float *fr_arr = isk ? fk : fq;
                     uint4 w[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
@@ -348,11 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         if (isk && row >= c) {
                             x = make_uint4(0u, 0u, 0u, 0u);
                         } else if (ELU1 || GATE == 1) {
-                            const float fr = GATE == 1 ? (isk ? fk[row] : fq[row]) : 1.f;
                             uint32_t u[4] = {x.x, x.y, x.z, x.w};
+                            if (ELU1) {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                u[e] = pack_bf16(phi_t<ELU1>(bf16lo(u[e])) * fr, phi_t<ELU1>(bf16hi(u[e])) * fr);
+                                for (int e = 0; e < 4; ++e) u[e] = phi_elu1_bf16x2(u[e]);
+                            }
+                            if (GATE == 1) {
+                                const float fr = fr_arr[row];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) u[e] = pack_bf16(bf16lo(u[e]) * fr, bf16hi(u[e]) * fr);
+                            }
                             x = make_uint4(u[0], u[1], u[2], u[3]);
                         }
                         *reinterpret_cast<uint4 *>(tile + (i >> 2) * kHalf + row * 128 + pc * 16) = x;
@@ -362,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             fence_proxy_async_smem();
             mbar_arrive(&pro[s]);
-            if (GATE == 1) named_sync(kBarPro, 128);  // fq/fk are rewritten for the next chunk
+            if (GATE == 1) named_sync<kBarPro, 128>();  // fq/fk are rewritten for the next chunk
         }
         if (!bad) {
             ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
@@ -375,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         for (int n = 1; n < N; ++n) {
             bool ok = mbar_wait(sdone, (uint32_t)(n - 1) & 1u, kWaitNs);
             if (GATE != 0) ok = ok && mbar_wait(&pro[n % NS], (uint32_t)(n / NS) & 1u, kWaitNs);
-            if (named_sync_or(kBarState, 128, !ok)) {
+            if (named_sync_or<kBarState, 128>(!ok)) {
                 bad = 1;
                 break;
             }
@@ -402,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             // the inter MMA of chunk n-1 has finished reading the previous copy
             ok = mbar_wait(sfree, (uint32_t)(n - 1) & 1u, kWaitNs);
-            if (named_sync_or(kBarState, 128, !ok)) {
+            if (named_sync_or<kBarState, 128>(!ok)) {
                 bad = 1;
                 break;
             }
@@ -437,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         }
         if (!bad && N > 0) {
             bool ok = mbar_wait(sdone, (uint32_t)(N - 1) & 1u, kWaitNs) && mbar_wait(profinal, 0u, kWaitNs);
-            if (named_sync_or(kBarState, 128, !ok)) {
+            if (named_sync_or<kBarState, 128>(!ok)) {
                 bad = 1;
             } else if (p.final_state != nullptr) {
                 tc_fence_after();
@@ -468,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         for (int n = 0; n < N; ++n) {
             const int b = n % LY::NOB, t0 = n * kC;
             bool ok = mbar_wait(qk, (uint32_t)n & 1u, kWaitNs);
-            if (named_sync_or(kBarOut, 64, !ok)) {
+            if (named_sync_or<kBarOut, 64>(!ok)) {
                 bad = 1;
                 break;
             }
@@ -500,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 
             ok = mbar_wait(&ofull[b], (uint32_t)(n / LY::NOB) & 1u, kWaitNs);
             if (t == 0) bulk_wait_read<0>();  // the previous O tile has left the staging buffer
-            if (named_sync_or(kBarOut, 64, !ok)) {
+            if (named_sync_or<kBarOut, 64>(!ok)) {
                 bad = 1;
                 break;
             }
@@ -534,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             tc_fence_before();
             mbar_arrive(&oempty[b]);
             fence_proxy_async_smem();
-            named_sync(kBarOut, 64);
+            named_sync<kBarOut, 64>();
             if (t == 0) {
                 tma_store_3d(&p.to, sO, 0, t0, bh);
                 tma_store_3d(&p.to, sO + 8192, 64, t0, bh);
@@ -549,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     if (aborted && tid == 0) atomicOr(&g_tc_error, 1u);
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

@@ -79,15 +79,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
 }
 
 // ------------------------------------------------------------------ named barriers
-// bar.sync on a hardware barrier other than 0 (which __syncthreads uses), for a
-// subset of the block whose size is a multiple of 32.
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+// bar.sync / bar.red on a hardware barrier other than 0 (which __syncthreads
+// uses), for a subset of the block whose size is a multiple of 32. The barrier
+// id is an immediate, so the compiler sees exactly which barriers exist.
+template <int ID, int NT>
+__device__ __forceinline__ void named_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(NT) : "memory");
 }
-
-// bar.red.or over a named barrier: every participant gets the OR of `pred`,
-// so a decision to leave a loop is the same in all of them.
-__device__ __forceinline__ int named_sync_or(uint32_t id, uint32_t nthreads, int pred) {
+// bar.red.or: every participant gets the OR of `pred`, so a decision to leave
+// a loop is the same in all of them.
+template <int ID, int NT>
+__device__ __forceinline__ int named_sync_or(int pred) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
@@ -95,7 +97,7 @@ __device__ __forceinline__ int named_sync_or(uint32_t id, uint32_t nthreads, int
         "bar.red.or.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"(pred), "r"(id), "r"(nthreads)
+        : "r"(pred), "n"(ID), "n"(NT)
         : "memory");
     return (int)r;
 }
