@@ -72,8 +72,11 @@ __device__ unsigned int g_tc_error;
 struct TcParams {
     CUtensorMap tq, tk, tv, tg, to;
     const float *gamma;
-    float *final_state;
-    int H, L, mode;
+    float *final_state;      // [BH][blk], written by an unsplit full pass
+    const float *state_in;   // [BH][nseg][blk]: state at each segment start (full pass)
+    float *seg_state;        // [BH][nseg][blk]: segment-local end state (state-only pass)
+    float *seg_logdecay;     // [BH][nseg][128]: log decay over each segment (state-only pass)
+    int H, L, mode, nseg, seg_chunks;
 };
 
 // Shared-memory layout. A stage holds q | k | v | (ones) | (g); the ones block
@@ -138,16 +141,23 @@ __device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
     return r;
 }
 
-template <int GATE, bool ELU1, bool NORM>
+// SO (state only): the first pass over a split sequence. Each CTA runs one
+// segment from a zero state and keeps only the state update (no QK, no
+// outputs): it writes the segment's end state and its total log decay.
+template <int GATE, bool ELU1, bool NORM, bool SO>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     using LY = Layout<GATE, NORM>;
     constexpr int NS = LY::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x, h = bh % p.H, L = p.L;
-    const int N = (L + kC - 1) / kC;
+    // CTA = (b, h, segment); a segment is seg_chunks consecutive chunks
+    const int bh = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg, h = bh % p.H, L = p.L;
+    const int c0 = seg * p.seg_chunks;
+    const int N = max(0, min(p.seg_chunks, (L + kC - 1) / kC - c0));
+    const bool init = !SO && p.state_in != nullptr && seg > 0;  // start from a carried state
     const size_t blk = (size_t)kD * kD + (NORM ? kD : 0);
+    const size_t segblk = (size_t)blockIdx.x * blk;
 
     float *fbuf = reinterpret_cast<float *>(sm + LY::F);  // [NS][128] state factor e^{b_last(n-1)}
     float *ffinal = fbuf + NS * 128;                      // [128] e^{b_last} of the last chunk
@@ -220,10 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     break;
                 }
                 uint8_t *base = sm + s * LY::stage;
-                const int t0 = n * kC;
-                mbar_arrive_expect_tx(&full[s], (GATE == 2 ? 4 : 3) * kTile);
+                const int t0 = (c0 + n) * kC;
+                mbar_arrive_expect_tx(&full[s], ((GATE == 2 ? 4 : 3) - (SO ? 1 : 0)) * kTile);
 #pragma unroll 1
-                for (int tl = 0; tl < (GATE == 2 ? 4 : 3); ++tl) {
+                for (int tl = SO ? 1 : 0; tl < (GATE == 2 ? 4 : 3); ++tl) {
                     const CUtensorMap *m = tl == 0 ? &p.tq : tl == 1 ? &p.tk : tl == 2 ? &p.tv : &p.tg;
                     uint8_t *dst = base + (tl < 3 ? tl * kTile : LY::g);
                     tma_load_3d(dst, m, &full[s], 0, t0, bh);
@@ -259,16 +269,33 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
                 umma_commit(qk);
             };
-            if (N > 0) {
+            if (SO) {
+                // state only: T_n = S_{n-1} + k~^T [V | 1] per chunk
+                for (int n = 0; n < N; ++n) {
+                    const int s = n % NS;
+                    if (!mbar_wait(&pro[s], (uint32_t)(n / NS) & 1u, kWaitNs) ||
+                        (n > 0 && !mbar_wait(sready, (uint32_t)(n - 1) & 1u, kWaitNs))) {
+                        bad = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ak = dkm(n), bv = dvm(n);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_bf16(tmem + LY::colS, ak + ks * 128, bv + ks * 128, id_s, (n > 0 || ks > 0));
+                    umma_commit(sdone);
+                    umma_commit(&empty[s]);
+                }
+            } else if (N > 0) {
                 if (!mbar_wait(&pro[0], 0u, kWaitNs)) bad = 1;
                 tc_fence_after();
                 if (!bad) issue_qk(0);
             }
-            for (int n = 0; n < N && !bad; ++n) {
+            for (int n = 0; n < N && !bad && !SO; ++n) {
                 const int s = n % NS, b = n % LY::NOB;
                 const uint32_t dO = tmem + (b ? LY::colO1 : LY::colO0);
                 const uint64_t aq = dq(n), ak = dkm(n), bv = dvm(n);
-                if (n > 0 && !mbar_wait(sready, (uint32_t)(n - 1) & 1u, kWaitNs)) {
+                if ((n > 0 || init) && !mbar_wait(sready, (uint32_t)(n - 1 + (init ? 1 : 0)) & 1u, kWaitNs)) {
                     bad = 1;
                     break;
                 }
@@ -276,10 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 // state: T_n = S_{n-1} (rescaled in place) + k~^T [V | 1]
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16(tmem + LY::colS, ak + ks * 128, bv + ks * 128, id_s, (n > 0 || ks > 0));
+                    umma_bf16(tmem + LY::colS, ak + ks * 128, bv + ks * 128, id_s, (n > 0 || init || ks > 0));
                 umma_commit(sdone);
                 // inter: O = q~ S_{n-1}
-                if (n > 0) {
+                if (n > 0 || init) {
                     if (n >= LY::NOB && !mbar_wait(&oempty[b], (uint32_t)((n - LY::NOB) / LY::NOB) & 1u, kWaitNs)) {
                         bad = 1;
                         break;
@@ -297,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) umma_bf16(dO, dP + ks * 2, bv + ks * 128, id_o, (n > 0 || ks > 0));
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16(dO, dP + ks * 2, bv + ks * 128, id_o, (n > 0 || init || ks > 0));
                 umma_commit(&ofull[b]);
                 umma_commit(&empty[s]);
                 // QK of the next chunk (P is read out of TMEM by then)
@@ -321,8 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         const int d = tid - 128;
         const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
         float b_last = 0.f;  // log decay over the previous chunk (this channel)
+        float b_total = 0.f; // log decay over the segment so far (this channel)
         for (int n = 0; n < N; ++n) {
-            const int s = n % NS, t0 = n * kC, c = min(kC, L - t0);
+            const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
             const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
             if (named_sync_or<kBarPro, 128>(!ok)) {
                 bad = 1;
@@ -343,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 for (int t = 0; t < c; ++t) {
                     const uint32_t off = cb + sw128_offset(t, d & 63);
                     b += log_decay_fast(load_bf16(sG + off));
-                    store_bf16(sQ + off, phi_t<ELU1>(load_bf16(sQ + off)) * __expf(b));
+                    if (!SO) store_bf16(sQ + off, phi_t<ELU1>(load_bf16(sQ + off)) * __expf(b));
                     store_bf16(sK + off, phi_t<ELU1>(load_bf16(sK + off)) * __expf(-b));
                 }
 #pragma unroll 1
@@ -354,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 // (r = 0..3) in both 8 KiB blocks of the q and of the k tile.
                 const int pc = d & 7;
 #pragma unroll
-                for (int isk = 0; isk < 2; ++isk) {
+                for (int isk = SO ? 1 : 0; isk < 2; ++isk) {
                     uint8_t *tile = isk ? sK : sQ;
                     const float *fr_arr = isk ? fk : fq;
                     uint4 w[8];
@@ -386,18 +415,71 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
                 if (GATE == 1) b_last = (float)c * lg;
             }
+            b_total += b_last;
             fence_proxy_async_smem();
             mbar_arrive(&pro[s]);
             if (GATE == 1) named_sync<kBarPro, 128>();  // fq/fk are rewritten for the next chunk
         }
         if (!bad) {
             ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
+            if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + d] = b_total;
             mbar_arrive(profinal);
         }
     } else if (warp >= 8 && warp < 12) {
         // ============================================================ state chain
         const int i = tid - 256;  // TMEM lane = state row (key channel)
         const uint32_t tS = tmem + lane_base + LY::colS;
+        // bf16 copy of the state row in TMEM, MN-major for the B operand: line i,
+        // value columns v; z goes to element 0 of line i in the third atom
+        auto write_copy = [&]() {
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tS + 32 * j, r);
+                tmem_ld_wait();
+                uint8_t *row = sS + (j >> 1) * 16384 + i * 128;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int lc = 4 * (j & 1) + q4;
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(r[8 * q4 + 0]), __uint_as_float(r[8 * q4 + 1]));
+                    w.y = pack_bf16(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
+                    w.z = pack_bf16(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
+                    w.w = pack_bf16(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
+                    *reinterpret_cast<uint4 *>(row + ((lc ^ (i & 7)) << 4)) = w;
+                }
+            }
+            if (NORM) {
+                uint32_t z;
+                tmem_ld1(tS + 128, z);
+                tmem_ld_wait();
+                *reinterpret_cast<uint4 *>(sS + 32768 + i * 128 + ((i & 7) << 4)) =
+                    make_uint4(pack_bf16(__uint_as_float(z), 0.f), 0u, 0u, 0u);
+            }
+        };
+        if (init) {
+            // the state carried into this segment: into TMEM and its bf16 copy
+            const float *src = p.state_in + segblk + (size_t)i * kD;
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[32];
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 v4 = reinterpret_cast<const float4 *>(src + 32 * j)[q4];
+                    r[4 * q4] = __float_as_uint(v4.x);
+                    r[4 * q4 + 1] = __float_as_uint(v4.y);
+                    r[4 * q4 + 2] = __float_as_uint(v4.z);
+                    r[4 * q4 + 3] = __float_as_uint(v4.w);
+                }
+                tmem_st32(tS + 32 * j, r);
+            }
+            if (NORM) tmem_st1(tS + 128, __float_as_uint(p.state_in[segblk + (size_t)kD * kD + i]));
+            tmem_st_wait();
+            write_copy();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(sready);
+        }
         for (int n = 1; n < N; ++n) {
             bool ok = mbar_wait(sdone, (uint32_t)(n - 1) & 1u, kWaitNs);
             if (GATE != 0) ok = ok && mbar_wait(&pro[n % NS], (uint32_t)(n / NS) & 1u, kWaitNs);
@@ -426,49 +508,30 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
                 tmem_st_wait();
             }
-            // the inter MMA of chunk n-1 has finished reading the previous copy
-            ok = mbar_wait(sfree, (uint32_t)(n - 1) & 1u, kWaitNs);
-            if (named_sync_or<kBarState, 128>(!ok)) {
-                bad = 1;
-                break;
-            }
-            // bf16 copy, MN-major for the B operand: line i, value columns v
-#pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tS + 32 * j, r);
-                tmem_ld_wait();
-                uint8_t *row = sS + (j >> 1) * 16384 + i * 128;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int lc = 4 * (j & 1) + q4;
-                    uint4 w;
-                    w.x = pack_bf16(__uint_as_float(r[8 * q4 + 0]), __uint_as_float(r[8 * q4 + 1]));
-                    w.y = pack_bf16(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
-                    w.z = pack_bf16(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
-                    w.w = pack_bf16(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
-                    *reinterpret_cast<uint4 *>(row + ((lc ^ (i & 7)) << 4)) = w;
+            if (!SO) {
+                // the inter MMA of chunk n-1 has finished reading the previous copy
+                ok = mbar_wait(sfree, (uint32_t)(n - 1) & 1u, kWaitNs);
+                if (named_sync_or<kBarState, 128>(!ok)) {
+                    bad = 1;
+                    break;
                 }
+                write_copy();
+                fence_proxy_async_smem();
             }
-            if (NORM) {
-                uint32_t z;
-                tmem_ld1(tS + 128, z);
-                tmem_ld_wait();
-                *reinterpret_cast<uint4 *>(sS + 32768 + i * 128 + ((i & 7) << 4)) =
-                    make_uint4(pack_bf16(__uint_as_float(z), 0.f), 0u, 0u, 0u);
-            }
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(sready);
         }
+        float *dst = SO ? p.seg_state + segblk : (p.nseg == 1 ? p.final_state : nullptr);
+        if (!SO && dst) dst += (size_t)bh * blk;
         if (!bad && N > 0) {
             bool ok = mbar_wait(sdone, (uint32_t)(N - 1) & 1u, kWaitNs) && mbar_wait(profinal, 0u, kWaitNs);
             if (named_sync_or<kBarState, 128>(!ok)) {
                 bad = 1;
-            } else if (p.final_state != nullptr) {
+            } else if (dst != nullptr) {
+                // end state S = diag(e^{b_last}) T (with z in column 128)
                 tc_fence_after();
                 const float ff = ffinal[i];
-                float *dst = p.final_state + (size_t)bh * blk + (size_t)i * kD;
+                float *row = dst + (size_t)i * kD;
 #pragma unroll 1
                 for (int j = 0; j < 4; ++j) {
                     uint32_t r[32];
@@ -476,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     tmem_ld_wait();
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4)
-                        reinterpret_cast<float4 *>(dst + 32 * j)[q4] = make_float4(
+                        reinterpret_cast<float4 *>(row + 32 * j)[q4] = make_float4(
                             __uint_as_float(r[4 * q4]) * ff, __uint_as_float(r[4 * q4 + 1]) * ff,
                             __uint_as_float(r[4 * q4 + 2]) * ff, __uint_as_float(r[4 * q4 + 3]) * ff);
                 }
@@ -484,15 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     uint32_t z;
                     tmem_ld1(tS + 128, z);
                     tmem_ld_wait();
-                    p.final_state[(size_t)bh * blk + (size_t)kD * kD + i] = __uint_as_float(z) * ff;
+                    dst[(size_t)kD * kD + i] = __uint_as_float(z) * ff;
                 }
             }
         }
-    } else if (warp == 12 || warp == 13) {
+    } else if (!SO && (warp == 12 || warp == 13)) {
         // ============================================================ outputs (TMEM lanes 0..63 = rows t)
         const int t = tid - 384;
         for (int n = 0; n < N; ++n) {
-            const int b = n % LY::NOB, t0 = n * kC;
+            const int b = n % LY::NOB, t0 = (c0 + n) * kC;
             bool ok = mbar_wait(qk, (uint32_t)n & 1u, kWaitNs);
             if (named_sync_or<kBarOut, 64>(!ok)) {
                 bad = 1;
@@ -610,22 +673,58 @@ bool make_map(CUtensorMap *m, const void *base, int L, int BH) {
     return r == CUDA_SUCCESS;
 }
 
-template <int GATE, bool ELU1, bool NORM>
+// Segment scan: S_in(0) = 0, S_in(p+1) = diag(e^{B_p}) S_in(p) + dS_p, and the
+// state after the last segment is the final state. One thread per state
+// element (z included), a sequential loop over the segments.
+__global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restrict__ seg_state,
+                                                          const float *__restrict__ seg_logdecay,
+                                                          float *__restrict__ state_in, float *final_state,
+                                                          int nseg, int blk) {
+    const int bh = blockIdx.x;
+    const int e = blockIdx.y * blockDim.x + threadIdx.x;
+    if (e >= blk) return;
+    const int d = e < kD * kD ? e / kD : e - kD * kD;  // key channel of this element
+    const size_t base = (size_t)bh * nseg;
+    float acc = 0.f;
+    for (int sgi = 0; sgi < nseg; ++sgi) {
+        if (sgi > 0) state_in[(base + sgi) * blk + e] = acc;
+        acc = __expf(seg_logdecay[(base + sgi) * kD + d]) * acc + seg_state[(base + sgi) * blk + e];
+    }
+    if (final_state) final_state[(size_t)bh * blk + e] = acc;
+}
+
+template <int GATE, bool ELU1, bool NORM, bool SO>
 int launch_t(const TcParams &prm, int grid, cudaStream_t s) {
     using LY = Layout<GATE, NORM>;
     static_assert(LY::bytes <= 232448, "shared memory budget");
     static_assert(LY::colP + 64 <= kTmemCols && LY::colO1 + LY::NW <= LY::colP, "TMEM budget");
-    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM>;
+    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes) != cudaSuccess)
         return LA_ERR_CUDA;
     kern<<<grid, kThreads, LY::bytes, s>>>(prm);
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
-template <int GATE>
+template <int GATE, bool SO>
 int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm) {
-    if (elu1) return norm ? launch_t<GATE, true, true>(prm, grid, s) : launch_t<GATE, true, false>(prm, grid, s);
-    return norm ? launch_t<GATE, false, true>(prm, grid, s) : launch_t<GATE, false, false>(prm, grid, s);
+    if (elu1)
+        return norm ? launch_t<GATE, true, true, SO>(prm, grid, s) : launch_t<GATE, true, false, SO>(prm, grid, s);
+    return norm ? launch_t<GATE, false, true, SO>(prm, grid, s) : launch_t<GATE, false, false, SO>(prm, grid, s);
+}
+
+template <bool SO>
+int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode) {
+    const bool elu1 = mode & LA_PHI_ELU1, norm = mode & LA_NORMALIZE;
+    if (mode & LA_GATE_CHANNEL) return launch_g<2, SO>(prm, grid, s, elu1, norm);
+    if (mode & LA_GATE_HEAD) return launch_g<1, SO>(prm, grid, s, elu1, norm);
+    return launch_g<0, SO>(prm, grid, s, elu1, norm);
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
 }
 
 }  // namespace
@@ -638,30 +737,69 @@ bool chunk_tc_supports(const ChunkArgs &a) {
     return major == 10 && get_encode();
 }
 
+// Segments per sequence: one CTA per (b, h) fills the GPU when there are at
+// least half as many sequences as SMs; fewer sequences are each cut into
+// segments of whole chunks so that (b, h, segment) CTAs cover the SMs.
+int tc_segments(int BH, int nchunks, int *seg_chunks) {
+    const int sms = sm_count();
+    int nseg = 1;
+    if (sms > 0 && 2 * BH <= sms) nseg = sms / BH < nchunks ? sms / BH : nchunks;
+    if (nseg < 1) nseg = 1;
+    const int cs = (nchunks + nseg - 1) / nseg;
+    *seg_chunks = cs;
+    return (nchunks + cs - 1) / cs;
+}
+
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches) {
     if (!get_encode()) return LA_ERR_CUDA;
     const int BH = a.B * a.H;
+    const int nchunks = (a.L + kC - 1) / kC;
     TcParams prm;
     memset(&prm, 0, sizeof(prm));
     if (!make_map(&prm.tq, a.q, a.L, BH) || !make_map(&prm.tk, a.k, a.L, BH) ||
         !make_map(&prm.tv, a.v, a.L, BH) || !make_map(&prm.to, a.out, a.L, BH))
         return LA_ERR_CUDA;
-    const bool gch = a.mode & LA_GATE_CHANNEL, ghd = a.mode & LA_GATE_HEAD;
-    if (gch && !make_map(&prm.tg, a.gate, a.L, BH)) return LA_ERR_CUDA;
-    prm.gamma = ghd ? static_cast<const float *>(a.gate) : nullptr;
+    if ((a.mode & LA_GATE_CHANNEL) && !make_map(&prm.tg, a.gate, a.L, BH)) return LA_ERR_CUDA;
+    prm.gamma = (a.mode & LA_GATE_HEAD) ? static_cast<const float *>(a.gate) : nullptr;
     prm.final_state = a.final_state;
     prm.H = a.H;
     prm.L = a.L;
     prm.mode = a.mode;
-    const bool elu1 = a.mode & LA_PHI_ELU1, norm = a.mode & LA_NORMALIZE;
-    int rc;
-    if (gch)
-        rc = launch_g<2>(prm, BH, s, elu1, norm);
-    else if (ghd)
-        rc = launch_g<1>(prm, BH, s, elu1, norm);
-    else
-        rc = launch_g<0>(prm, BH, s, elu1, norm);
-    if (rc == LA_OK) *launches += 1;
+    prm.nseg = tc_segments(BH, nchunks, &prm.seg_chunks);
+    if (prm.nseg == 1) {
+        const int rc = launch_mode<false>(prm, BH, s, a.mode);
+        if (rc == LA_OK) *launches += 1;
+        return rc;
+    }
+    // split sequences: state-only pass, segment scan, full pass from the
+    // carried states; scratch is stream-ordered
+    const size_t blk = (size_t)kD * kD + ((a.mode & LA_NORMALIZE) ? kD : 0);
+    const size_t nsb = (size_t)BH * prm.nseg;
+    const size_t bytes = (2 * nsb * blk + nsb * kD) * sizeof(float);
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    float *seg_state = static_cast<float *>(scratch);
+    float *state_in = seg_state + nsb * blk;
+    float *seg_logdecay = state_in + nsb * blk;
+    prm.seg_state = seg_state;
+    prm.seg_logdecay = seg_logdecay;
+    prm.final_state = nullptr;
+    int rc = launch_mode<true>(prm, (int)nsb, s, a.mode);
+    if (rc == LA_OK) {
+        *launches += 1;
+        la_seg_scan_kernel<<<dim3((unsigned)BH, (unsigned)((blk + 255) / 256)), 256, 0, s>>>(
+            seg_state, seg_logdecay, state_in, a.final_state, prm.nseg, (int)blk);
+        rc = cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    }
+    if (rc == LA_OK) {
+        *launches += 1;
+        prm.state_in = state_in;
+        prm.seg_state = nullptr;
+        prm.seg_logdecay = nullptr;
+        rc = launch_mode<false>(prm, (int)nsb, s, a.mode);
+        if (rc == LA_OK) *launches += 1;
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
     return rc;
 }
 
