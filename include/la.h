@@ -121,6 +121,34 @@ int la_decode_step(const void *q, const void *k, const void *v, const void *gate
                    la_stream_t stream);
 
 /*
+ * la_chunk_fwd_noalloc -- la_chunk_fwd without any device allocation. No page
+ * of the method has a counterpart to this call; it exists for callers that
+ * cannot let a library allocate device memory in the middle of their work,
+ * such as servers that plan all device memory up front or code running while
+ * another allocator owns the device's memory pool.
+ *
+ * Same arguments, results and errors as la_chunk_fwd. Where la_chunk_fwd would
+ * take stream-ordered scratch (the tensor-core path splitting a short batch
+ * into sequence segments), this call uses a fixed device array of
+ * LA_NOALLOC_SCRATCH_BYTES bytes inside the library instead: every GPU that
+ * loads the library holds that array until the process exits. A request that
+ * would need more scratch returns LA_ERR_UNSUPPORTED. It never calls cudaMalloc,
+ * cudaMallocAsync or cudaFree.
+ *
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before starting
+ *   any stream capture.
+ * - Every call on a device shares the one array and leaves its contents behind.
+ *   Nothing in it has to start at zero: each call writes every scratch value
+ *   before reading it. Calls whose work overlaps on the GPU (other streams,
+ *   other host threads) race on the array; the caller must order them.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES (20u * 1024u * 1024u)
+int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *gate,
+                         void *out, float *final_state, int B, int H, int L, int dk,
+                         int dv, int mode, int chunk, la_stream_t stream);
+
+/*
  * la_chunk_fwd_path -- which kernel la_chunk_fwd would run for these sizes and
  * mode on the current device, without launching anything: 1 = tensor-core
  * kernel, 0 = general CUDA-core kernel, or a negative la_status for arguments

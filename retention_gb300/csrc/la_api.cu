@@ -2,6 +2,7 @@
 // status strings. Every check runs before any launch; nothing is allocated
 // here.
 #include <atomic>
+#include <mutex>
 #include <stdint.h>
 
 #include "la_common.cuh"
@@ -115,3 +116,81 @@ const char *la_status_string(int status) {
 unsigned long long la_kernel_launches(void) { return g_launches.load(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// la_chunk_fwd_noalloc: la_chunk_fwd for callers that must not allocate device
+// memory. When a short batch makes the tensor-core path split sequences into
+// segments, its scratch comes from this fixed device array instead of
+// cudaMallocAsync. The array exists once per GPU that loads the library and
+// stays allocated until the process exits.
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. The host-side
+// name of the array is only a stand-in, so the address is looked up once per
+// device (with that device current) and cached; the lookup itself allocates
+// nothing.
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return LA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return LA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return LA_OK;
+}
+
+}  // namespace
+
+extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *gate, void *out,
+                                    float *final_state, int B, int H, int L, int dk, int dv, int mode,
+                                    int chunk, la_stream_t stream) {
+    if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
+    if (chunk < 1 || chunk > 128) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
+    int rc = check_mode(mode, gate, false);
+    if (rc != LA_OK) return rc;
+    const long nbh = (long)B * H;
+    if (nbh > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (nbh == 0) return LA_OK;
+    if (L == 0) {
+        if (final_state) {
+            if (!aligned16(final_state)) return LA_ERR_MISALIGNED;
+            const size_t blk = (size_t)dk * dv + ((mode & LA_NORMALIZE) ? dk : 0);
+            if (cudaMemsetAsync(final_state, 0, (size_t)nbh * blk * sizeof(float), s) != cudaSuccess)
+                return LA_ERR_CUDA;
+        }
+        return LA_OK;
+    }
+    if (!q || !k || !v || !out) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LA_ERR_MISALIGNED;
+    if (final_state && !aligned16(final_state)) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_CHANNEL) && !aligned16(gate)) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
+
+    la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode, chunk};
+    int launches = 0;
+    if (!(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a)) {
+        void *scratch = nullptr;
+        if (la::chunk_tc_scratch_bytes(a) > (size_t)LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_UNSUPPORTED;
+        if (la::chunk_tc_scratch_bytes(a) > 0) {
+            rc = noalloc_scratch(&scratch);
+            if (rc != LA_OK) return rc;
+        }
+        rc = la::launch_chunk_tc_into(a, s, &launches, scratch, LA_NOALLOC_SCRATCH_BYTES);
+    } else {
+        rc = la::launch_chunk_simt(a, s, &launches);
+    }
+    g_launches += (unsigned long long)launches;
+    return rc;
+}

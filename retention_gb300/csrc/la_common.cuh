@@ -55,5 +55,7 @@ int launch_chunk_simt(const ChunkArgs &a, cudaStream_t s, int *launches);
 int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);
+size_t chunk_tc_scratch_bytes(const ChunkArgs &a);
+int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch, size_t scratch_bytes);
 
 }  // namespace la

@@ -30,6 +30,7 @@ _VP, _I = ctypes.c_void_p, ctypes.c_int
 SIGNATURES = {
     "la_chunk_fwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_decode_step": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
+    "la_chunk_fwd_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_path": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "la_status_string": ([_I], ctypes.c_char_p),
     "la_kernel_launches": ([], ctypes.c_ulonglong),
@@ -119,6 +120,22 @@ def chunk_fwd(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None
                              B, H, L, dk, dv, mode, chunk, _stream(stream))
     if rc != LA_OK:
         raise LAError("la_chunk_fwd", rc)
+    return out, final_state
+
+
+def chunk_fwd_noalloc(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None, chunk=64,
+                      out, final_state=None, simt=False, stream=None):
+    """la_chunk_fwd_noalloc: like chunk_fwd, but the caller provides ``out`` (and
+    ``final_state``) and the library allocates nothing; any scratch it needs is
+    the library's fixed device array, shared by all calls on the device."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    mode = mode_bits(phi, normalize, gate_kind, q.dtype, simt)
+    rc = load().la_chunk_fwd_noalloc(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
+                                     _dev(out, "out"), _dev(final_state, "final_state"),
+                                     B, H, L, dk, dv, mode, chunk, _stream(stream))
+    if rc != LA_OK:
+        raise LAError("la_chunk_fwd_noalloc", rc)
     return out, final_state
 
 
