@@ -112,12 +112,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
-__device__ __forceinline__ float load_bf16(const uint8_t *p) {
-    return __uint_as_float(((uint32_t) * reinterpret_cast<const uint16_t *>(p)) << 16);
-}
-__device__ __forceinline__ void store_bf16(uint8_t *p, float x) {
-    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
-}
 // log alpha = logsigmoid(g) / 16 with the hardware exp/log
 __device__ __forceinline__ float log_decay_fast(float g) {
     return (fminf(g, 0.f) - __logf(1.f + __expf(-fabsf(g)))) * 0.0625f;
@@ -149,7 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     using LY = Layout<GATE, NORM>;
     constexpr int NS = LY::NS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, formed by pointer arithmetic on the shared array so
+    // that every access below stays a shared-memory access (an integer round
+    // trip would turn them into generic loads and stores)
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // CTA = (b, h, segment); a segment is seg_chunks consecutive chunks
     const int bh = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg, h = bh % p.H, L = p.L;
@@ -350,6 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
         float b_last = 0.f;  // log decay over the previous chunk (this channel)
         float b_total = 0.f; // log decay over the segment so far (this channel)
+        // gated form: lanes with d % 8 == 7 hold the chunk and segment log decays of
+        // channels 8 (d / 8) .. +7
+        float gl_last[8], gl_total[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gl_last[e] = gl_total[e] = 0.f;
         for (int n = 0; n < N; ++n) {
             const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
             const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
@@ -358,26 +360,87 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 break;
             }
             uint8_t *sQ = sm + s * LY::stage, *sK = sQ + kTile, *sG = sQ + LY::g;
-            fbuf[s * 128 + d] = GATE == 0 ? 1.f : __expf(b_last);
+            if (GATE == 2) {
+                if ((d & 7) == 7)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) fbuf[s * 128 + (d & ~7) + e] = __expf(gl_last[e]);
+            } else {
+                fbuf[s * 128 + d] = GATE == 0 ? 1.f : __expf(b_last);
+            }
             if (GATE == 1 && d < 64) {
                 fq[d] = __expf((float)(d + 1) * lg);
                 fk[d] = __expf(-(float)(d + 1) * lg);
             }
             if (GATE == 1) named_sync<kBarPro, 128>();
             if (GATE == 2) {
-                // one channel per thread: running log decay down the chunk
-                const uint32_t cb = (d >> 6) * kHalf;
-                float b = 0.f;
+                // Thread d owns channels 8cg..8cg+7 (cg = d / 8) of rows 8rg..8rg+7
+                // (rg = d % 8), as 16-byte pieces. The running log decay down the
+                // chunk: pass 1 sums each channel over the thread's rows, an exclusive
+                // scan across the 8 lanes of the channel group gives the decay above
+                // the block, pass 2 recomputes the gate logs as a running sum and
+                // applies the factors. Both passes stay rolled (small code).
+                const int cg = d >> 3, rg = d & 7;
+                const uint32_t base = (cg >> 3) * kHalf + rg * 8 * 128;
+                auto piece = [&](int u) { return base + u * 128 + ((((cg & 7) ^ u) & 7) << 4); };
+                float run[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) run[e] = 0.f;
 #pragma unroll 1
-                for (int t = 0; t < c; ++t) {
-                    const uint32_t off = cb + sw128_offset(t, d & 63);
-                    b += log_decay_fast(load_bf16(sG + off));
-                    if (!SO) store_bf16(sQ + off, phi_t<ELU1>(load_bf16(sQ + off)) * __expf(b));
-                    store_bf16(sK + off, phi_t<ELU1>(load_bf16(sK + off)) * __expf(-b));
+                for (int u = 0; u < 8 && rg * 8 + u < c; ++u) {
+                    const uint4 w4 = *reinterpret_cast<const uint4 *>(sG + piece(u));
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        run[2 * e] += log_decay_fast(bf16lo(wv[e]));
+                        run[2 * e + 1] += log_decay_fast(bf16hi(wv[e]));
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float tot = run[e];
+                    float x = tot;
+#pragma unroll
+                    for (int off = 1; off < 8; off <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, off, 8);
+                        if (rg >= off) x += y;
+                    }
+                    run[e] = x - tot;             // decay of the row blocks above this one
+                    if (rg == 7) gl_last[e] = x;  // whole-chunk log decay of channel 8cg+e
                 }
 #pragma unroll 1
-                for (int t = c; t < kC; ++t) store_bf16(sK + cb + sw128_offset(t, d & 63), 0.f);
-                b_last = b;
+                for (int u = 0; u < 8; ++u) {
+                    uint4 *kp = reinterpret_cast<uint4 *>(sK + piece(u));
+                    if (rg * 8 + u >= c) {
+                        *kp = make_uint4(0u, 0u, 0u, 0u);
+                        continue;
+                    }
+                    const uint4 w4 = *reinterpret_cast<const uint4 *>(sG + piece(u));
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        run[2 * e] += log_decay_fast(bf16lo(wv[e]));
+                        run[2 * e + 1] += log_decay_fast(bf16hi(wv[e]));
+                    }
+                    const uint4 kw = *kp;
+                    uint32_t ku[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (ELU1) ku[e] = phi_elu1_bf16x2(ku[e]);
+                        ku[e] = pack_bf16(bf16lo(ku[e]) * __expf(-run[2 * e]), bf16hi(ku[e]) * __expf(-run[2 * e + 1]));
+                    }
+                    *kp = make_uint4(ku[0], ku[1], ku[2], ku[3]);
+                    if (!SO) {
+                        uint4 *qp = reinterpret_cast<uint4 *>(sQ + piece(u));
+                        const uint4 qw = *qp;
+                        uint32_t qu[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (ELU1) qu[e] = phi_elu1_bf16x2(qu[e]);
+                            qu[e] = pack_bf16(bf16lo(qu[e]) * __expf(run[2 * e]), bf16hi(qu[e]) * __expf(run[2 * e + 1]));
+                        }
+                        *qp = make_uint4(qu[0], qu[1], qu[2], qu[3]);
+                    }
+                }
             } else if (ELU1 || GATE == 1 || c < kC) {
                 // 16-byte pieces: this thread owns slot pc of rows r * 16 + d / 8
                 // (r = 0..3) in both 8 KiB blocks of the q and of the k tile.
@@ -416,13 +479,25 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 if (GATE == 1) b_last = (float)c * lg;
             }
             b_total += b_last;
+            if (GATE == 2)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gl_total[e] += gl_last[e];
             fence_proxy_async_smem();
             mbar_arrive(&pro[s]);
             if (GATE == 1) named_sync<kBarPro, 128>();  // fq/fk are rewritten for the next chunk
         }
         if (!bad) {
-            ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
-            if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + d] = b_total;
+            if (GATE == 2) {
+                if ((d & 7) == 7)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        ffinal[(d & ~7) + e] = __expf(gl_last[e]);
+                        if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + (d & ~7) + e] = gl_total[e];
+                    }
+            } else {
+                ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
+                if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + d] = b_total;
+            }
             mbar_arrive(profinal);
         }
     } else if (warp >= 8 && warp < 12) {
