@@ -112,14 +112,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
-// log alpha = logsigmoid(g) / 16 with the hardware exp/log
-__device__ __forceinline__ float log_decay_fast(float g) {
-    return (fminf(g, 0.f) - __logf(1.f + __expf(-fabsf(g)))) * 0.0625f;
+// The hardware base-2 exponential and logarithm (denormals flushed: the gate
+// factors they make are far from the denormal range, and an underflowing e^-|g|
+// only drops a term below rounding).
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-template <bool ELU1>
-__device__ __forceinline__ float phi_t(float x) {
-    return ELU1 ? fmaxf(x, 0.f) + __expf(fminf(x, 0.f)) : x;
+__device__ __forceinline__ float lg2f(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
+constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 // elu(x) + 1 on two packed bf16 values in bf16 arithmetic:
 // max(x, 0) + 2^(min(x, 0) * log2 e). The exponent argument is rounded to bf16,
 // so for x < 0 the result carries a relative error below 2^-8 |x| on top of the
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             if (GATE == 2) {
                 if ((d & 7) == 7)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) fbuf[s * 128 + (d & ~7) + e] = __expf(gl_last[e]);
+                    for (int e = 0; e < 8; ++e) fbuf[s * 128 + (d & ~7) + e] = ex2f(gl_last[e]);
             } else {
                 fbuf[s * 128 + d] = GATE == 0 ? 1.f : __expf(b_last);
             }
@@ -374,25 +380,47 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             if (GATE == 1) named_sync<kBarPro, 128>();
             if (GATE == 2) {
                 // Thread d owns channels 8cg..8cg+7 (cg = d / 8) of rows 8rg..8rg+7
-                // (rg = d % 8), as 16-byte pieces. The running log decay down the
-                // chunk: pass 1 sums each channel over the thread's rows, an exclusive
-                // scan across the 8 lanes of the channel group gives the decay above
-                // the block, pass 2 recomputes the gate logs as a running sum and
-                // applies the factors. Both passes stay rolled (small code).
+                // (rg = d % 8), as 16-byte pieces. A thread visits its rows in the
+                // rotated order u = rg, rg+1, .., 7, 0, .., rg-1, so that the eight
+                // lanes of a quarter warp touch eight different 16-byte slots of the
+                // swizzled tile (no bank conflicts). Log decays are kept in base 2:
+                //   log2 alpha = (min(g, 0) log2(e) - log2(1 + 2^(-|g| log2(e)))) / 16.
+                // Pass 1 sums them over the block as
+                //   sum min(g, 0) log2(e) - log2 prod (1 + e^-|g|)
+                // (a product of eight factors in [1, 2]: one logarithm per block),
+                // both over the whole block and over its rows u < rg. An exclusive
+                // scan across the eight lanes of the channel group gives the decay
+                // above the block; pass 2 runs the gate logs down the rows and
+                // applies the factors 2^b to q and 2^-b to k.
                 const int cg = d >> 3, rg = d & 7;
                 const uint32_t base = (cg >> 3) * kHalf + rg * 8 * 128;
                 auto piece = [&](int u) { return base + u * 128 + ((((cg & 7) ^ u) & 7) << 4); };
-                float run[8];
+                float run[8], head[8];
+                {
+                    float ms[8], ps[8], mh[8], ph[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) run[e] = 0.f;
+                    for (int e = 0; e < 8; ++e) ms[e] = mh[e] = 0.f, ps[e] = ph[e] = 1.f;
 #pragma unroll 1
-                for (int u = 0; u < 8 && rg * 8 + u < c; ++u) {
-                    const uint4 w4 = *reinterpret_cast<const uint4 *>(sG + piece(u));
-                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    for (int j = 0; j < 8; ++j) {
+                        const int u = (j + rg) & 7;
+                        if (rg * 8 + u >= c) continue;
+                        const bool hd = u < rg;
+                        const uint4 w4 = *reinterpret_cast<const uint4 *>(sG + piece(u));
+                        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        run[2 * e] += log_decay_fast(bf16lo(wv[e]));
-                        run[2 * e + 1] += log_decay_fast(bf16hi(wv[e]));
+                        for (int e = 0; e < 8; ++e) {
+                            const float g = (e & 1) ? bf16hi(wv[e >> 1]) : bf16lo(wv[e >> 1]);
+                            const float mn = fminf(g, 0.f), f = 1.f + ex2f(fabsf(g) * -kLog2e);
+                            ms[e] += mn;
+                            ps[e] *= f;
+                            mh[e] += hd ? mn : 0.f;
+                            ph[e] *= hd ? f : 1.f;
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        run[e] = fmaf(ms[e], kLog2e, -lg2f(ps[e])) * 0.0625f;
+                        head[e] = fmaf(mh[e], kLog2e, -lg2f(ph[e])) * 0.0625f;
                     }
                 }
 #pragma unroll
@@ -405,10 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         if (rg >= off) x += y;
                     }
                     run[e] = x - tot;             // decay of the row blocks above this one
-                    if (rg == 7) gl_last[e] = x;  // whole-chunk log decay of channel 8cg+e
+                    head[e] += run[e];            // ... and of this block's rows u < rg
+                    if (rg == 7) gl_last[e] = x;  // whole-chunk log2 decay of channel 8cg+e
                 }
 #pragma unroll 1
-                for (int u = 0; u < 8; ++u) {
+                for (int j = 0; j < 8; ++j) {
+                    const int u = (j + rg) & 7;
                     uint4 *kp = reinterpret_cast<uint4 *>(sK + piece(u));
                     if (rg * 8 + u >= c) {
                         *kp = make_uint4(0u, 0u, 0u, 0u);
@@ -417,16 +447,19 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     const uint4 w4 = *reinterpret_cast<const uint4 *>(sG + piece(u));
                     const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        run[2 * e] += log_decay_fast(bf16lo(wv[e]));
-                        run[2 * e + 1] += log_decay_fast(bf16hi(wv[e]));
+                    for (int e = 0; e < 8; ++e) {
+                        // rows rg..7 continue from the head; row 0 restarts at the block base
+                        const float r0 = (u == 0 && j != 0) ? run[e] : head[e];
+                        const float g = (e & 1) ? bf16hi(wv[e >> 1]) : bf16lo(wv[e >> 1]);
+                        const float l = lg2f(1.f + ex2f(fabsf(g) * -kLog2e));
+                        head[e] = fmaf(fminf(g, 0.f), kLog2e * 0.0625f, fmaf(l, -0.0625f, r0));
                     }
                     const uint4 kw = *kp;
                     uint32_t ku[4] = {kw.x, kw.y, kw.z, kw.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         if (ELU1) ku[e] = phi_elu1_bf16x2(ku[e]);
-                        ku[e] = pack_bf16(bf16lo(ku[e]) * __expf(-run[2 * e]), bf16hi(ku[e]) * __expf(-run[2 * e + 1]));
+                        ku[e] = pack_bf16(bf16lo(ku[e]) * ex2f(-head[2 * e]), bf16hi(ku[e]) * ex2f(-head[2 * e + 1]));
                     }
                     *kp = make_uint4(ku[0], ku[1], ku[2], ku[3]);
                     if (!SO) {
@@ -436,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             if (ELU1) qu[e] = phi_elu1_bf16x2(qu[e]);
-                            qu[e] = pack_bf16(bf16lo(qu[e]) * __expf(run[2 * e]), bf16hi(qu[e]) * __expf(run[2 * e + 1]));
+                            qu[e] = pack_bf16(bf16lo(qu[e]) * ex2f(head[2 * e]), bf16hi(qu[e]) * ex2f(head[2 * e + 1]));
                         }
                         *qp = make_uint4(qu[0], qu[1], qu[2], qu[3]);
                     }
@@ -491,8 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 if ((d & 7) == 7)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        ffinal[(d & ~7) + e] = __expf(gl_last[e]);
-                        if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + (d & ~7) + e] = gl_total[e];
+                        ffinal[(d & ~7) + e] = ex2f(gl_last[e]);
+                        if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + (d & ~7) + e] = gl_total[e] * kLn2;
                     }
             } else {
                 ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
