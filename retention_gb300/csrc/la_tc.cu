@@ -34,6 +34,8 @@
 //   warp 2       TMA producer: q, k, v (, g) tiles of chunk n into a ring of stages
 //   warp 3       MMA issuer (one thread) and TMEM owner
 //   warps 4-7    prologue: phi and decay factors in place on the q and k tiles
+//                (with the per-channel gate, warps 0, 1, 14, 15 join it: 256
+//                threads, each on two key channels of one quarter of the rows)
 //   warps 8-11   state chain: S_{n-1} = diag(f) T_{n-1} (rescaled in TMEM) and
 //                its bf16 copy for the inter MMA of chunk n; the final state
 //   warps 12-13  outputs: P mask -> bf16; O -> 1/den -> bf16 -> TMA store
@@ -90,8 +92,9 @@ struct Layout {
     static constexpr uint32_t P = NS * stage;          // bf16 P tile, 8 KiB
     static constexpr uint32_t S = P + 8192;            // bf16 copy of S_{n-1} (+ z atom), 32 / 48 KiB
     static constexpr uint32_t O = S + (NORM ? 49152 : 32768);  // bf16 O staging, two swizzled halves
-    static constexpr uint32_t F = O + 16384;           // floats: fbuf[NS][128] ffinal[128] fq[64] fk[64]
-    static constexpr uint32_t Bar = F + (NS * 128 + 128 + 128) * 4;
+    // floats: fbuf[NS][128] ffinal[128] fq[64] fk[64] (gated: tot[4][128])
+    static constexpr uint32_t F = O + 16384;
+    static constexpr uint32_t Bar = F + (NS * 128 + 128 + 128 + (GATE == 2 ? 512 : 0)) * 4;
     // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal, drain
     static constexpr uint32_t nbar = 3 * NS + 12;
     static constexpr uint32_t Misc = Bar + nbar * 8;  // TMEM base address
@@ -126,6 +129,12 @@ __device__ __forceinline__ float lg2f(float x) {
     return y;
 }
 constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
+// log2 of the channel gate alpha = exp(logsigmoid(g) / 16):
+//   (min(g, 0) log2(e) - log2(1 + 2^(-|g| log2(e)))) / 16
+// (g = +huge gives 0: no decay)
+__device__ __forceinline__ float log2_alpha(float g) {
+    return fmaf(fminf(g, 0.f), kLog2e * 0.0625f, lg2f(1.f + ex2f(fabsf(g) * -kLog2e)) * -0.0625f);
+}
 // elu(x) + 1 on two packed bf16 values in bf16 arithmetic:
 // max(x, 0) + 2^(min(x, 0) * log2 e). The exponent argument is rounded to bf16,
 // so for x < 0 the result carries a relative error below 2^-8 |x| on top of the
@@ -182,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&pro[s], 128);
+            mbar_init(&pro[s], GATE == 2 ? 256 : 128);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ofull[b], 1);
@@ -194,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         mbar_init(sdone, 1);
         mbar_init(sfree, 1);
         mbar_init(sready, 128);
-        mbar_init(profinal, 128);
+        mbar_init(profinal, GATE == 2 ? 64 : 128);
         mbar_init(drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
@@ -347,17 +356,122 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             umma_commit(drain);
             if (!mbar_wait(drain, 0u, kWaitNs)) bad = 1;
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if ((warp >= 4 && warp < 8) || (GATE == 2 && (warp < 2 || warp >= 14))) {
         // ============================================================ prologue
-        const int d = tid - 128;
-        const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
-        float b_last = 0.f;  // log decay over the previous chunk (this channel)
-        float b_total = 0.f; // log decay over the segment so far (this channel)
-        // gated form: lanes with d % 8 == 7 hold the chunk and segment log decays of
-        // channels 8 (d / 8) .. +7
-        float gl_last[8], gl_total[8];
+        if constexpr (GATE == 2) {
+            // 256 threads in eight warps, two on each SM sub-partition. Prologue
+            // warp pw (warps 4..7 -> 0..3, warps 0, 1 -> 4, 5, warps 14, 15 -> 6, 7)
+            // takes the channel half ch = pw % 2 and the row quarter qr = pw / 2;
+            // lane l owns key channels 64 ch + 2l and 64 ch + 2l + 1 (one bf16x2
+            // word) of rows 16 qr .. 16 qr + 15. The 32 words a warp touches in one
+            // row fill that row's 128-byte line of one swizzle block: no bank
+            // conflicts, and the swizzle slot of row 16 qr + u depends on u alone.
+            // Per chunk:
+            //   pass 1  log2 alpha of the thread's 32 gate values, kept in registers,
+            //           and their sums over the quarter -> tot[qr][channel]
+            //   barrier; the quarter's starting decay = sum of tot over lower quarters
+            //   pass 2  running log2 decay b_t down the quarter; phi(k_t) * 2^-b_t and
+            //           phi(q_t) * 2^b_t in place, two channels per packed word.
+            // Rows past the end of the sequence (t >= c) get log2 alpha = 0, k = 0
+            // and keep their (zero-filled) q. Quarter 3 ends at the chunk's total
+            // decay and writes the state factors.
+            const int pw = (warp >= 4 && warp < 8) ? warp - 4 : warp < 2 ? warp + 4 : warp - 8;
+            const int ch = pw & 1, qr = pw >> 1;
+            const int cw = 64 * ch + 2 * lane;  // first of the thread's two channels
+            const uint32_t colw = ch * kHalf + ((lane & 3) << 2), slot = lane >> 2;
+            auto offw = [&](int u) { return colw + (16 * qr + u) * 128 + (((slot ^ u) & 7) << 4); };
+            float *tot = fk + 64;  // [4][128] per-quarter log2 decay sums
+            // log2 decay of the two channels over the previous chunk and over the
+            // segment so far (kept by quarter 3)
+            float bl0 = 0.f, bl1 = 0.f, bt0 = 0.f, bt1 = 0.f;
+            for (int n = 0; n < N; ++n) {
+                const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
+                const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
+                if (named_sync_or<kBarPro, 256>(!ok)) {
+                    bad = 1;
+                    break;
+                }
+                uint8_t *sQ = sm + s * LY::stage, *sK = sQ + kTile, *sG = sQ + LY::g;
+                if (qr == 3) *reinterpret_cast<float2 *>(fbuf + s * 128 + cw) = make_float2(ex2f(bl0), ex2f(bl1));
+                float la0[16], la1[16], s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) gl_last[e] = gl_total[e] = 0.f;
+                for (int u = 0; u < 16; ++u) {
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(sG + offw(u));
+                    const bool live = 16 * qr + u < c;
+                    la0[u] = log2_alpha(live ? bf16lo(w) : 3.0e38f);
+                    la1[u] = log2_alpha(live ? bf16hi(w) : 3.0e38f);
+                    s0 += la0[u];
+                    s1 += la1[u];
+                }
+                *reinterpret_cast<float2 *>(tot + qr * 128 + cw) = make_float2(s0, s1);
+                named_sync<kBarPro, 256>();
+                float b0 = 0.f, b1 = 0.f;
+                for (int r = 0; r < qr; ++r) {
+                    const float2 tt = *reinterpret_cast<const float2 *>(tot + r * 128 + cw);
+                    b0 += tt.x;
+                    b1 += tt.y;
+                }
+                // pass 2 in two groups of eight rows; the second group's words are
+                // loaded before the first group's results are stored
+                uint32_t kw[8], qw[8], kn[8], qn[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    kw[u] = *reinterpret_cast<const uint32_t *>(sK + offw(u));
+                    if (!SO) qw[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(u));
+                }
+#pragma unroll
+                for (int g8 = 0; g8 < 2; ++g8) {
+                    if (g8 == 0) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            kn[u] = *reinterpret_cast<const uint32_t *>(sK + offw(8 + u));
+                            if (!SO) qn[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(8 + u));
+                        }
+                    }
+                    uint32_t ko[8], qo[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int uu = 8 * g8 + u;
+                        b0 += la0[uu];
+                        b1 += la1[uu];
+                        uint32_t kx = kw[u];
+                        if (ELU1) kx = phi_elu1_bf16x2(kx);
+                        ko[u] = 16 * qr + uu < c ? pack_bf16(bf16lo(kx) * ex2f(-b0), bf16hi(kx) * ex2f(-b1)) : 0u;
+                        if (!SO) {
+                            uint32_t qx = qw[u];
+                            if (ELU1) qx = phi_elu1_bf16x2(qx);
+                            qo[u] = pack_bf16(bf16lo(qx) * ex2f(b0), bf16hi(qx) * ex2f(b1));
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        *reinterpret_cast<uint32_t *>(sK + offw(8 * g8 + u)) = ko[u];
+                        if (!SO) *reinterpret_cast<uint32_t *>(sQ + offw(8 * g8 + u)) = qo[u];
+                        kw[u] = kn[u];
+                        if (!SO) qw[u] = qn[u];
+                    }
+                }
+                if (qr == 3) {
+                    bl0 = b0;
+                    bl1 = b1;
+                    bt0 += b0;
+                    bt1 += b1;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&pro[s]);
+            }
+            if (!bad && qr == 3) {
+                *reinterpret_cast<float2 *>(ffinal + cw) = make_float2(ex2f(bl0), ex2f(bl1));
+                if (SO)
+                    *reinterpret_cast<float2 *>(p.seg_logdecay + (size_t)blockIdx.x * kD + cw) =
+                        make_float2(bt0 * kLn2, bt1 * kLn2);
+                mbar_arrive(profinal);
+            }
+        } else {
+        const int d = tid - 128;  // key channel
+        const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
+        // log decay of key channel d over the previous chunk and over the segment so far
+        float b_last = 0.f, b_total = 0.f;
         for (int n = 0; n < N; ++n) {
             const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
             const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
@@ -365,116 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 bad = 1;
                 break;
             }
-            uint8_t *sQ = sm + s * LY::stage, *sK = sQ + kTile, *sG = sQ + LY::g;
-            if (GATE == 2) {
-                if ((d & 7) == 7)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) fbuf[s * 128 + (d & ~7) + e] = ex2f(gl_last[e]);
-            } else {
-                fbuf[s * 128 + d] = GATE == 0 ? 1.f : __expf(b_last);
-            }
+            uint8_t *sQ = sm + s * LY::stage, *sK = sQ + kTile;
+            fbuf[s * 128 + d] = GATE == 0 ? 1.f : __expf(b_last);
             if (GATE == 1 && d < 64) {
                 fq[d] = __expf((float)(d + 1) * lg);
                 fk[d] = __expf(-(float)(d + 1) * lg);
             }
             if (GATE == 1) named_sync<kBarPro, 128>();
-            if (GATE == 2) {
-                // Thread d owns channels 8cg..8cg+7 (cg = d / 8) of rows 8rg..8rg+7
-                // (rg = d % 8), as 16-byte pieces. A thread visits its rows in the
-                // rotated order u = rg, rg+1, .., 7, 0, .., rg-1, so that the eight
-                // lanes of a quarter warp touch eight different 16-byte slots of the
-                // swizzled tile (no bank conflicts). Log decays are kept in base 2:
-                //   log2 alpha = (min(g, 0) log2(e) - log2(1 + 2^(-|g| log2(e)))) / 16.
-                // Pass 1 sums them over the block as
-                //   sum min(g, 0) log2(e) - log2 prod (1 + e^-|g|)
-                // (a product of eight factors in [1, 2]: one logarithm per block),
-                // both over the whole block and over its rows u < rg. An exclusive
-                // scan across the eight lanes of the channel group gives the decay
-                // above the block; pass 2 runs the gate logs down the rows and
-                // applies the factors 2^b to q and 2^-b to k.
-                const int cg = d >> 3, rg = d & 7;
-                const uint32_t base = (cg >> 3) * kHalf + rg * 8 * 128;
-                auto piece = [&](int u) { return base + u * 128 + ((((cg & 7) ^ u) & 7) << 4); };
-                float run[8], head[8];
-                {
-                    float ms[8], ps[8], mh[8], ph[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ms[e] = mh[e] = 0.f, ps[e] = ph[e] = 1.f;
-#pragma unroll 1
-                    for (int j = 0; j < 8; ++j) {
-                        const int u = (j + rg) & 7;
-                        if (rg * 8 + u >= c) continue;
-                        const bool hd = u < rg;
-                        const uint4 w4 = *reinterpret_cast<const uint4 *>(sG + piece(u));
-                        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float g = (e & 1) ? bf16hi(wv[e >> 1]) : bf16lo(wv[e >> 1]);
-                            const float mn = fminf(g, 0.f), f = 1.f + ex2f(fabsf(g) * -kLog2e);
-                            ms[e] += mn;
-                            ps[e] *= f;
-                            mh[e] += hd ? mn : 0.f;
-                            ph[e] *= hd ? f : 1.f;
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        run[e] = fmaf(ms[e], kLog2e, -lg2f(ps[e])) * 0.0625f;
-                        head[e] = fmaf(mh[e], kLog2e, -lg2f(ph[e])) * 0.0625f;
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float tot = run[e];
-                    float x = tot;
-#pragma unroll
-                    for (int off = 1; off < 8; off <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, x, off, 8);
-                        if (rg >= off) x += y;
-                    }
-                    run[e] = x - tot;             // decay of the row blocks above this one
-                    head[e] += run[e];            // ... and of this block's rows u < rg
-                    if (rg == 7) gl_last[e] = x;  // whole-chunk log2 decay of channel 8cg+e
-                }
-#pragma unroll 1
-                for (int j = 0; j < 8; ++j) {
-                    const int u = (j + rg) & 7;
-                    uint4 *kp = reinterpret_cast<uint4 *>(sK + piece(u));
-                    if (rg * 8 + u >= c) {
-                        *kp = make_uint4(0u, 0u, 0u, 0u);
-                        continue;
-                    }
-                    const uint4 w4 = *reinterpret_cast<const uint4 *>(sG + piece(u));
-                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        // rows rg..7 continue from the head; row 0 restarts at the block base
-                        const float r0 = (u == 0 && j != 0) ? run[e] : head[e];
-                        const float g = (e & 1) ? bf16hi(wv[e >> 1]) : bf16lo(wv[e >> 1]);
-                        const float l = lg2f(1.f + ex2f(fabsf(g) * -kLog2e));
-                        head[e] = fmaf(fminf(g, 0.f), kLog2e * 0.0625f, fmaf(l, -0.0625f, r0));
-                    }
-                    const uint4 kw = *kp;
-                    uint32_t ku[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (ELU1) ku[e] = phi_elu1_bf16x2(ku[e]);
-                        ku[e] = pack_bf16(bf16lo(ku[e]) * ex2f(-head[2 * e]), bf16hi(ku[e]) * ex2f(-head[2 * e + 1]));
-                    }
-                    *kp = make_uint4(ku[0], ku[1], ku[2], ku[3]);
-                    if (!SO) {
-                        uint4 *qp = reinterpret_cast<uint4 *>(sQ + piece(u));
-                        const uint4 qw = *qp;
-                        uint32_t qu[4] = {qw.x, qw.y, qw.z, qw.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (ELU1) qu[e] = phi_elu1_bf16x2(qu[e]);
-                            qu[e] = pack_bf16(bf16lo(qu[e]) * ex2f(head[2 * e]), bf16hi(qu[e]) * ex2f(head[2 * e + 1]));
-                        }
-                        *qp = make_uint4(qu[0], qu[1], qu[2], qu[3]);
-                    }
-                }
-            } else if (ELU1 || GATE == 1 || c < kC) {
+            if (ELU1 || GATE == 1 || c < kC) {
                 // 16-byte pieces: this thread owns slot pc of rows r * 16 + d / 8
                 // (r = 0..3) in both 8 KiB blocks of the q and of the k tile.
                 const int pc = d & 7;
@@ -512,26 +524,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 if (GATE == 1) b_last = (float)c * lg;
             }
             b_total += b_last;
-            if (GATE == 2)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) gl_total[e] += gl_last[e];
             fence_proxy_async_smem();
             mbar_arrive(&pro[s]);
             if (GATE == 1) named_sync<kBarPro, 128>();  // fq/fk are rewritten for the next chunk
         }
         if (!bad) {
-            if (GATE == 2) {
-                if ((d & 7) == 7)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        ffinal[(d & ~7) + e] = ex2f(gl_last[e]);
-                        if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + (d & ~7) + e] = gl_total[e] * kLn2;
-                    }
-            } else {
-                ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
-                if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + d] = b_total;
-            }
+            ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
+            if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + d] = b_total;
             mbar_arrive(profinal);
+        }
         }
     } else if (warp >= 8 && warp < 12) {
         // ============================================================ state chain
