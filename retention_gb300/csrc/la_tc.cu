@@ -81,19 +81,29 @@ struct TcParams {
     int H, L, mode, nseg, seg_chunks;
 };
 
+constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
+
 // Shared-memory layout. A stage holds q | k | v | (ones) | (g); the ones block
 // is the 64-column swizzle atom that follows v as the third N atom of [V | 1].
-template <int GATE, bool NORM>
+// The state-only pass reads no q and keeps no P, S' or O, so its stages are
+// smaller and its ring deeper (as deep as the budget allows, at most 6).
+template <int GATE, bool NORM, bool SO>
 struct Layout {
-    static constexpr int NS = (NORM || GATE == 2) ? 2 : 3;
-    static constexpr uint32_t ones = 3 * kTile;                       // offset in a stage
-    static constexpr uint32_t g = 3 * kTile + (NORM ? kHalf : 0);      // offset in a stage
+    static constexpr uint32_t q = 0;                            // offsets in a stage
+    static constexpr uint32_t k = SO ? 0 : kTile;
+    static constexpr uint32_t v = k + kTile;
+    static constexpr uint32_t ones = v + kTile;
+    static constexpr uint32_t g = ones + (NORM ? kHalf : 0);
     static constexpr uint32_t stage = g + (GATE == 2 ? kTile : 0);
-    static constexpr uint32_t P = NS * stage;          // bf16 P tile, 8 KiB
-    static constexpr uint32_t S = P + 8192;            // bf16 copy of S_{n-1} (+ z atom), 32 / 48 KiB
-    static constexpr uint32_t O = S + (NORM ? 49152 : 32768);  // bf16 O staging, two swizzled halves
+    // room kept for the float arrays, barriers and alignment slack below
+    static constexpr uint32_t kReserve = 8192;
+    static constexpr int NS = !SO ? ((NORM || GATE == 2) ? 2 : 3)
+                                  : ((kSmemBudget - kReserve) / stage < 6 ? (kSmemBudget - kReserve) / stage : 6);
+    static constexpr uint32_t P = NS * stage;                              // bf16 P tile, 8 KiB
+    static constexpr uint32_t S = P + (SO ? 0 : 8192);                     // bf16 S_{n-1} (+ z atom), 32 / 48 KiB
+    static constexpr uint32_t O = S + (SO ? 0 : (NORM ? 49152 : 32768));   // bf16 O staging, two swizzled halves
     // floats: fbuf[NS][128] ffinal[128] fq[64] fk[64] (gated: tot[4][128])
-    static constexpr uint32_t F = O + 16384;
+    static constexpr uint32_t F = O + (SO ? 0 : 16384);
     static constexpr uint32_t Bar = F + (NS * 128 + 128 + 128 + (GATE == 2 ? 512 : 0)) * 4;
     // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal, drain
     static constexpr uint32_t nbar = 3 * NS + 12;
@@ -155,7 +165,7 @@ __device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
 // outputs): it writes the segment's end state and its total log decay.
 template <int GATE, bool ELU1, bool NORM, bool SO>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
-    using LY = Layout<GATE, NORM>;
+    using LY = Layout<GATE, NORM, SO>;
     constexpr int NS = LY::NS;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, formed by pointer arithmetic on the shared array so
@@ -220,8 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             const uint32_t one = (((pc ^ r) & 7) == 0) ? 0x3f80u : 0u;  // bf16 1.0 in element 0
             *reinterpret_cast<uint4 *>(sm + s * LY::stage + LY::ones + r * 128 + pc * 16) = make_uint4(one, 0u, 0u, 0u);
         }
-        for (int i = tid; i < 1024; i += kThreads)
-            reinterpret_cast<uint4 *>(sS + 32768)[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (!SO)
+            for (int i = tid; i < 1024; i += kThreads)
+                reinterpret_cast<uint4 *>(sS + 32768)[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -247,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll 1
                 for (int tl = SO ? 1 : 0; tl < (GATE == 2 ? 4 : 3); ++tl) {
                     const CUtensorMap *m = tl == 0 ? &p.tq : tl == 1 ? &p.tk : tl == 2 ? &p.tv : &p.tg;
-                    uint8_t *dst = base + (tl < 3 ? tl * kTile : LY::g);
+                    uint8_t *dst = base + (tl == 0 ? LY::q : tl == 1 ? LY::k : tl == 2 ? LY::v : LY::g);
                     tma_load_3d(dst, m, &full[s], 0, t0, bh);
                     tma_load_3d(dst + kHalf, m, &full[s], 64, t0, bh);
                 }
@@ -268,10 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             const uint32_t sm0 = smem_u32(sm);
             const uint64_t dS = sdesc_sw128(smem_u32(sS), 16384, 1024);   // S' copy, MN-major
             const uint64_t dP = sdesc_sw128(smem_u32(sP), 16, 1024);      // P, K-major
-            auto dq = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage, 16, 1024); };
-            auto dkk = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + kTile, 16, 1024); };
-            auto dkm = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + kTile, kHalf, 1024); };
-            auto dvm = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + 2 * kTile, kHalf, 1024); };
+            auto dq = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + LY::q, 16, 1024); };
+            auto dkk = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + LY::k, 16, 1024); };
+            auto dkm = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + LY::k, kHalf, 1024); };
+            auto dvm = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + LY::v, kHalf, 1024); };
             auto issue_qk = [&](int n) {
                 const uint64_t a = dq(n), bb = dkk(n);
 #pragma unroll
@@ -391,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     bad = 1;
                     break;
                 }
-                uint8_t *sQ = sm + s * LY::stage, *sK = sQ + kTile, *sG = sQ + LY::g;
+                uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k, *sG = sm + s * LY::stage + LY::g;
                 if (qr == 3) *reinterpret_cast<float2 *>(fbuf + s * 128 + cw) = make_float2(ex2f(bl0), ex2f(bl1));
                 float la0[16], la1[16], s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -479,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 bad = 1;
                 break;
             }
-            uint8_t *sQ = sm + s * LY::stage, *sK = sQ + kTile;
+            uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k;
             fbuf[s * 128 + d] = GATE == 0 ? 1.f : __expf(b_last);
             if (GATE == 1 && d < 64) {
                 fq[d] = __expf((float)(d + 1) * lg);
@@ -804,8 +815,8 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
 
 template <int GATE, bool ELU1, bool NORM, bool SO>
 int launch_t(const TcParams &prm, int grid, cudaStream_t s) {
-    using LY = Layout<GATE, NORM>;
-    static_assert(LY::bytes <= 232448, "shared memory budget");
+    using LY = Layout<GATE, NORM, SO>;
+    static_assert(LY::NS >= 2 && LY::bytes <= kSmemBudget, "shared memory budget");
     static_assert(LY::colP + 64 <= kTmemCols && LY::colO1 + LY::NW <= LY::colP, "TMEM budget");
     auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes) != cudaSuccess)
