@@ -86,27 +86,37 @@ constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
 // Shared-memory layout. A stage holds q | k | v | (ones) | (g); the ones block
 // is the 64-column swizzle atom that follows v as the third N atom of [V | 1].
 // The state-only pass reads no q and keeps no P, S' or O, so its stages are
-// smaller and its ring deeper (as deep as the budget allows, at most 6).
+// smaller and its ring deeper (as deep as the budget allows, at most 6). In
+// the full pass the gate tiles g have a ring of their own (GR): the prologue
+// is done with g after its first pass, so g is released early and the next
+// chunk's g is already in place when the prologue turns to it.
 template <int GATE, bool NORM, bool SO>
 struct Layout {
+    static constexpr bool GR = GATE == 2 && !SO;
+    static constexpr int NG = GR ? 2 : 0;                       // gate ring slots
     static constexpr uint32_t q = 0;                            // offsets in a stage
     static constexpr uint32_t k = SO ? 0 : kTile;
     static constexpr uint32_t v = k + kTile;
     static constexpr uint32_t ones = v + kTile;
-    static constexpr uint32_t g = ones + (NORM ? kHalf : 0);
-    static constexpr uint32_t stage = g + (GATE == 2 ? kTile : 0);
+    static constexpr uint32_t g = ones + (NORM ? kHalf : 0);    // (in the stage unless GR)
+    static constexpr uint32_t stage = g + (GATE == 2 && !GR ? kTile : 0);
     // room kept for the float arrays, barriers and alignment slack below
     static constexpr uint32_t kReserve = 8192;
     static constexpr int NS = !SO ? ((NORM || GATE == 2) ? 2 : 3)
                                   : ((kSmemBudget - kReserve) / stage < 6 ? (kSmemBudget - kReserve) / stage : 6);
-    static constexpr uint32_t P = NS * stage;                              // bf16 P tile, 8 KiB
+    static constexpr uint32_t Gring = NS * stage;                          // [NG] g tiles
+    static constexpr uint32_t P = Gring + NG * kTile;                      // bf16 P tile, 8 KiB
     static constexpr uint32_t S = P + (SO ? 0 : 8192);                     // bf16 S_{n-1} (+ z atom), 32 / 48 KiB
     static constexpr uint32_t O = S + (SO ? 0 : (NORM ? 49152 : 32768));   // bf16 O staging, two swizzled halves
-    // floats: fbuf[NS][128] ffinal[128] fq[64] fk[64] (gated: tot[4][128])
+    // floats: fbuf[NF][128] ffinal[128] fq[64] fk[64] (gated: tot[4][128]). fbuf is
+    // a ring of NF = NS + 1 slots: chunk n's decay factor goes to slot n % NF at
+    // the end of its prologue, for the state chain to rescale T_n with.
+    static constexpr int NF = NS + 1;
     static constexpr uint32_t F = O + (SO ? 0 : 16384);
-    static constexpr uint32_t Bar = F + (NS * 128 + 128 + 128 + (GATE == 2 ? 512 : 0)) * 4;
-    // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal, drain
-    static constexpr uint32_t nbar = 3 * NS + 12;
+    static constexpr uint32_t Bar = F + (NF * 128 + 128 + 128 + (GATE == 2 ? 512 : 0)) * 4;
+    // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal,
+    // drain; gfull, gempty [NG]; ffull [NF]
+    static constexpr uint32_t nbar = 3 * NS + 12 + 2 * NG + NF;
     static constexpr uint32_t Misc = Bar + nbar * 8;  // TMEM base address
     static constexpr uint32_t bytes = Misc + 16 + 1024;  // + slack for the 1024-byte alignment
     // TMEM columns (region bases 32-column aligned). With the ones column the
@@ -167,6 +177,7 @@ template <int GATE, bool ELU1, bool NORM, bool SO>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     using LY = Layout<GATE, NORM, SO>;
     constexpr int NS = LY::NS;
+    constexpr int NG = LY::GR ? LY::NG : 1;  // gate ring slots (the ring exists only if GR)
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, formed by pointer arithmetic on the shared array so
     // that every access below stays a shared-memory access (an integer round
@@ -181,8 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     const size_t blk = (size_t)kD * kD + (NORM ? kD : 0);
     const size_t segblk = (size_t)blockIdx.x * blk;
 
-    float *fbuf = reinterpret_cast<float *>(sm + LY::F);  // [NS][128] state factor e^{b_last(n-1)}
-    float *ffinal = fbuf + NS * 128;                      // [128] e^{b_last} of the last chunk
+    constexpr int NF = LY::NF;
+    float *fbuf = reinterpret_cast<float *>(sm + LY::F);  // [NF][128] chunk n's decay factor e^{b_last(n)}
+    float *ffinal = fbuf + NF * 128;                      // [128] e^{b_last} of the last chunk
     float *fq = ffinal + 128;                             // [64] retention: gamma^(t+1)
     float *fk = fq + 64;                                  // [64] retention: gamma^-(t+1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::Bar);
@@ -190,6 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     uint64_t *ofull = bars + 3 * NS, *oempty = ofull + 2;
     uint64_t *qk = oempty + 2, *pfull = qk + 1, *pempty = pfull + 1, *sdone = pempty + 1, *sfree = sdone + 1;
     uint64_t *sready = sfree + 1, *profinal = sready + 1, *drain = profinal + 1;
+    uint64_t *gfull = drain + 1, *gempty = gfull + LY::NG;  // (empty arrays unless GR)
+    uint64_t *ffull = gempty + LY::NG;                      // [NF]: fbuf slot written
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::Misc);
     uint8_t *sP = sm + LY::P, *sS = sm + LY::S, *sO = sm + LY::O;
 
@@ -203,6 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             mbar_init(&empty[s], 1);
             mbar_init(&pro[s], GATE == 2 ? 256 : 128);
         }
+        for (int sg = 0; sg < LY::NG; ++sg) {
+            mbar_init(&gfull[sg], 1);
+            mbar_init(&gempty[sg], 256);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ofull[b], 1);
             mbar_init(&oempty[b], 64);
@@ -214,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         mbar_init(sfree, 1);
         mbar_init(sready, 128);
         mbar_init(profinal, GATE == 2 ? 64 : 128);
+        for (int j = 0; j < NF; ++j) mbar_init(&ffull[j], GATE == 2 ? 64 : 128);
         mbar_init(drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
@@ -245,18 +264,32 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     if (warp == kWarpProducer) {
         // ============================================================ TMA producer
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, gissued = 0;
+            constexpr int ntl = (GATE == 2 && !LY::GR) ? 4 : 3;  // q, k, v (, g) tiles of a stage
             for (int n = 0; n < N; ++n) {
                 const int s = n % NS;
+                const int t0 = (c0 + n) * kC;
+                if constexpr (LY::GR) {
+                    // g of chunk n goes out before chunk n's stage is waited for
+                    const int sg = n % NG;
+                    if (n >= NG && !mbar_wait(&gempty[sg], (uint32_t)(n / NG - 1) & 1u, kWaitNs)) {
+                        bad = 1;
+                        break;
+                    }
+                    uint8_t *dst = sm + LY::Gring + sg * kTile;
+                    mbar_arrive_expect_tx(&gfull[sg], kTile);
+                    tma_load_3d(dst, &p.tg, &gfull[sg], 0, t0, bh);
+                    tma_load_3d(dst + kHalf, &p.tg, &gfull[sg], 64, t0, bh);
+                    gissued = n + 1;
+                }
                 if (n >= NS && !mbar_wait(&empty[s], (uint32_t)(n / NS - 1) & 1u, kWaitNs)) {
                     bad = 1;
                     break;
                 }
                 uint8_t *base = sm + s * LY::stage;
-                const int t0 = (c0 + n) * kC;
-                mbar_arrive_expect_tx(&full[s], ((GATE == 2 ? 4 : 3) - (SO ? 1 : 0)) * kTile);
+                mbar_arrive_expect_tx(&full[s], (ntl - (SO ? 1 : 0)) * kTile);
 #pragma unroll 1
-                for (int tl = SO ? 1 : 0; tl < (GATE == 2 ? 4 : 3); ++tl) {
+                for (int tl = SO ? 1 : 0; tl < ntl; ++tl) {
                     const CUtensorMap *m = tl == 0 ? &p.tq : tl == 1 ? &p.tk : tl == 2 ? &p.tv : &p.tg;
                     uint8_t *dst = base + (tl == 0 ? LY::q : tl == 1 ? LY::k : tl == 2 ? LY::v : LY::g);
                     tma_load_3d(dst, m, &full[s], 0, t0, bh);
@@ -267,6 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // nothing may still be landing in shared memory when the CTA leaves
             for (int m = issued > NS ? issued - NS : 0; m < issued; ++m)
                 if (!mbar_wait(&full[m % NS], (uint32_t)(m / NS) & 1u, kWaitNs)) bad = 1;
+            for (int m = gissued > NG ? gissued - NG : 0; m < gissued; ++m)
+                if (!mbar_wait(&gfull[m % NG], (uint32_t)(m / NG) & 1u, kWaitNs)) bad = 1;
         }
     } else if (warp == kWarpMma) {
         // ============================================================ MMA issuer
@@ -397,13 +432,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             float bl0 = 0.f, bl1 = 0.f, bt0 = 0.f, bt1 = 0.f;
             for (int n = 0; n < N; ++n) {
                 const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
-                const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
+                // the gate tile first: from its own ring (full pass) or from the stage
+                bool ok = LY::GR ? mbar_wait(&gfull[n % NG], (uint32_t)(n / NG) & 1u, kWaitNs)
+                                 : mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
                 if (named_sync_or<kBarPro, 256>(!ok)) {
                     bad = 1;
                     break;
                 }
-                uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k, *sG = sm + s * LY::stage + LY::g;
-                if (qr == 3) *reinterpret_cast<float2 *>(fbuf + s * 128 + cw) = make_float2(ex2f(bl0), ex2f(bl1));
+                uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k;
+                const uint8_t *sG = LY::GR ? sm + LY::Gring + (n % NG) * kTile : sm + s * LY::stage + LY::g;
                 float la0[16], la1[16], s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
@@ -414,8 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     s0 += la0[u];
                     s1 += la1[u];
                 }
+                if (LY::GR) mbar_arrive(&gempty[n % NG]);  // g is in registers now
                 *reinterpret_cast<float2 *>(tot + qr * 128 + cw) = make_float2(s0, s1);
-                named_sync<kBarPro, 256>();
+                // then the q, k (, v) stage; the barrier also publishes the quarter sums
+                ok = LY::GR ? mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs) : true;
+                if (named_sync_or<kBarPro, 256>(!ok)) {
+                    bad = 1;
+                    break;
+                }
                 float b0 = 0.f, b1 = 0.f;
                 for (int r = 0; r < qr; ++r) {
                     const float2 tt = *reinterpret_cast<const float2 *>(tot + r * 128 + cw);
@@ -467,6 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     bl1 = b1;
                     bt0 += b0;
                     bt1 += b1;
+                    *reinterpret_cast<float2 *>(fbuf + (n % NF) * 128 + cw) = make_float2(ex2f(b0), ex2f(b1));
+                    mbar_arrive(&ffull[n % NF]);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&pro[s]);
@@ -491,7 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 break;
             }
             uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k;
-            fbuf[s * 128 + d] = GATE == 0 ? 1.f : __expf(b_last);
             if (GATE == 1 && d < 64) {
                 fq[d] = __expf((float)(d + 1) * lg);
                 fk[d] = __expf(-(float)(d + 1) * lg);
@@ -535,6 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 if (GATE == 1) b_last = (float)c * lg;
             }
             b_total += b_last;
+            if (GATE != 0) {
+                fbuf[(n % NF) * 128 + d] = __expf(b_last);
+                mbar_arrive(&ffull[n % NF]);
+            }
             fence_proxy_async_smem();
             mbar_arrive(&pro[s]);
             if (GATE == 1) named_sync<kBarPro, 128>();  // fq/fk are rewritten for the next chunk
@@ -601,14 +649,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             mbar_arrive(sready);
         }
         for (int n = 1; n < N; ++n) {
+            // T_{n-1} is complete, and so is chunk n-1's decay factor
             bool ok = mbar_wait(sdone, (uint32_t)(n - 1) & 1u, kWaitNs);
-            if (GATE != 0) ok = ok && mbar_wait(&pro[n % NS], (uint32_t)(n / NS) & 1u, kWaitNs);
+            if (GATE != 0) ok = ok && mbar_wait(&ffull[(n - 1) % NF], (uint32_t)((n - 1) / NF) & 1u, kWaitNs);
             if (named_sync_or<kBarState, 128>(!ok)) {
                 bad = 1;
                 break;
             }
             tc_fence_after();
-            const float f = fbuf[(n % NS) * 128 + i];
+            const float f = fbuf[((n - 1) % NF) * 128 + i];
             if (GATE != 0) {
                 // S_{n-1} = diag(f) T_{n-1}, in place (z rides in column 128)
 #pragma unroll 1
