@@ -419,8 +419,8 @@ def main():
     tc = la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"],
                            la.mode_bits(cfg["phi"], cfg["normalize"], cfg["gate"]), cfg["chunk"]) == 1
     kernel = "la_chunk_tc_kernel" if tc else "chunk_simt_kernel"
-    srcs = ["retention_gb300/csrc/la_tc.cu" if tc else "retention_gb300/csrc/la_simt.cu",
-            "retention_gb300/csrc/la_common.cuh"]
+    srcs = (["retention_gb300/csrc/la_tc.cu", "retention_gb300/csrc/sm100.cuh"] if tc
+            else ["retention_gb300/csrc/la_simt.cu"]) + ["retention_gb300/csrc/la_common.cuh"]
     t_kernel = la_res["secs"] / args.steps / max(1, la_res["launches_per_step"])
     achieved = la_res["bytes"] / t_kernel / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
