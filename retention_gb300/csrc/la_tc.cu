@@ -33,9 +33,8 @@
 // One CTA per (b, h), 16 warps with fixed roles, connected by mbarriers:
 //   warp 2       TMA producer: q, k, v (, g) tiles of chunk n into a ring of stages
 //   warp 3       MMA issuer (one thread) and TMEM owner
-//   warps 4-7    prologue: phi and decay factors in place on the q and k tiles
-//                (with the per-channel gate, warps 0, 1, 14, 15 join it: 256
-//                threads, each on two key channels of one quarter of the rows)
+//   warps 4-7, 0, 1, 14, 15  prologue (256 threads, two warps per SM
+//                sub-partition): phi and decay factors in place on the q and k tiles
 //   warps 8-11   state chain: S_{n-1} = diag(f) T_{n-1} (rescaled in TMEM) and
 //                its bf16 copy for the inter MMA of chunk n; the final state
 //   warps 12-13  outputs: P mask -> bf16; O -> 1/den -> bf16 -> TMA store
@@ -93,7 +92,9 @@ constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
 template <int GATE, bool NORM, bool SO>
 struct Layout {
     static constexpr bool GR = GATE == 2 && !SO;
-    static constexpr int NG = GR ? 2 : 0;                       // gate ring slots
+    // gated without the normaliser: three q|k|v stages and one gate slot fit;
+    // with it, two stages and two gate slots
+    static constexpr int NG = GR ? (NORM ? 2 : 1) : 0;          // gate ring slots
     static constexpr uint32_t q = 0;                            // offsets in a stage
     static constexpr uint32_t k = SO ? 0 : kTile;
     static constexpr uint32_t v = k + kTile;
@@ -102,7 +103,7 @@ struct Layout {
     static constexpr uint32_t stage = g + (GATE == 2 && !GR ? kTile : 0);
     // room kept for the float arrays, barriers and alignment slack below
     static constexpr uint32_t kReserve = 8192;
-    static constexpr int NS = !SO ? ((NORM || GATE == 2) ? 2 : 3)
+    static constexpr int NS = !SO ? (NORM ? 2 : 3)
                                   : ((kSmemBudget - kReserve) / stage < 6 ? (kSmemBudget - kReserve) / stage : 6);
     static constexpr uint32_t Gring = NS * stage;                          // [NG] g tiles
     static constexpr uint32_t P = Gring + NG * kTile;                      // bf16 P tile, 8 KiB
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&pro[s], GATE == 2 ? 256 : 128);
+            mbar_init(&pro[s], 256);
         }
         for (int sg = 0; sg < LY::NG; ++sg) {
             mbar_init(&gfull[sg], 1);
@@ -402,12 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             umma_commit(drain);
             if (!mbar_wait(drain, 0u, kWaitNs)) bad = 1;
         }
-    } else if ((warp >= 4 && warp < 8) || (GATE == 2 && (warp < 2 || warp >= 14))) {
+    } else if ((warp >= 4 && warp < 8) || warp < 2 || warp >= 14) {
         // ============================================================ prologue
+        // 256 threads in eight warps, two on each SM sub-partition: prologue warp
+        // pw = warps 4..7 -> 0..3, warps 0, 1 -> 4, 5, warps 14, 15 -> 6, 7
+        const int pw = (warp >= 4 && warp < 8) ? warp - 4 : warp < 2 ? warp + 4 : warp - 8;
         if constexpr (GATE == 2) {
-            // 256 threads in eight warps, two on each SM sub-partition. Prologue
-            // warp pw (warps 4..7 -> 0..3, warps 0, 1 -> 4, 5, warps 14, 15 -> 6, 7)
-            // takes the channel half ch = pw % 2 and the row quarter qr = pw / 2;
+            // Prologue warp pw takes the channel half ch = pw % 2 and the row
+            // quarter qr = pw / 2;
             // lane l owns key channels 64 ch + 2l and 64 ch + 2l + 1 (one bf16x2
             // word) of rows 16 qr .. 16 qr + 15. The 32 words a warp touches in one
             // row fill that row's 128-byte line of one swizzle block: no bank
@@ -421,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // Rows past the end of the sequence (t >= c) get log2 alpha = 0, k = 0
             // and keep their (zero-filled) q. Quarter 3 ends at the chunk's total
             // decay and writes the state factors.
-            const int pw = (warp >= 4 && warp < 8) ? warp - 4 : warp < 2 ? warp + 4 : warp - 8;
             const int ch = pw & 1, qr = pw >> 1;
             const int cw = 64 * ch + 2 * lane;  // first of the thread's two channels
             const uint32_t colw = ch * kHalf + ((lane & 3) << 2), slot = lane >> 2;
@@ -524,74 +526,75 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 mbar_arrive(profinal);
             }
         } else {
-        const int d = tid - 128;  // key channel
-        const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
-        // log decay of key channel d over the previous chunk and over the segment so far
-        float b_last = 0.f, b_total = 0.f;
-        for (int n = 0; n < N; ++n) {
-            const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
-            const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
-            if (named_sync_or<kBarPro, 128>(!ok)) {
-                bad = 1;
-                break;
-            }
-            uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k;
-            if (GATE == 1 && d < 64) {
-                fq[d] = __expf((float)(d + 1) * lg);
-                fk[d] = __expf(-(float)(d + 1) * lg);
-            }
-            if (GATE == 1) named_sync<kBarPro, 128>();
-            if (ELU1 || GATE == 1 || c < kC) {
-                // 16-byte pieces: this thread owns slot pc of rows r * 16 + d / 8
-                // (r = 0..3) in both 8 KiB blocks of the q and of the k tile.
-                const int pc = d & 7;
+            // Thread pd (0..255) owns the 16-byte pieces pd + 256 j (j = 0..3) of
+            // each tile: block j / 2, row pd / 8 + 32 (j % 2), slot pd % 8 (the
+            // eight lanes of a quarter warp share a row: no bank conflicts).
+            // Threads pd < 128 also own key channel pd for the decay factors.
+            const int pd = 32 * pw + lane;
+            const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
+            // log decay of key channel pd over the previous chunk and over the segment so far
+            float b_last = 0.f, b_total = 0.f;
+            for (int n = 0; n < N; ++n) {
+                const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
+                const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
+                if (named_sync_or<kBarPro, 256>(!ok)) {
+                    bad = 1;
+                    break;
+                }
+                uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k;
+                if (GATE == 1 && pd < 64) {
+                    fq[pd] = __expf((float)(pd + 1) * lg);
+                    fk[pd] = __expf(-(float)(pd + 1) * lg);
+                }
+                if (GATE == 1) named_sync<kBarPro, 256>();
+                if (ELU1 || GATE == 1 || c < kC) {
 #pragma unroll
-                for (int isk = SO ? 1 : 0; isk < 2; ++isk) {
-                    uint8_t *tile = isk ? sK : sQ;
-                    const float *fr_arr = isk ? fk : fq;
-                    uint4 w[8];
+                    for (int isk = SO ? 1 : 0; isk < 2; ++isk) {
+                        uint8_t *tile = isk ? sK : sQ;
+                        const float *fr_arr = isk ? fk : fq;
+                        uint4 w[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        w[i] = *reinterpret_cast<const uint4 *>(tile + (i >> 2) * kHalf +
-                                                                ((i & 3) * 16 + (d >> 3)) * 128 + pc * 16);
+                        for (int j = 0; j < 4; ++j)
+                            w[j] = *reinterpret_cast<const uint4 *>(tile + (j >> 1) * kHalf +
+                                                                    ((pd >> 3) + 32 * (j & 1)) * 128 + (pd & 7) * 16);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int row = (i & 3) * 16 + (d >> 3);
-                        uint4 &x = w[i];
-                        if (isk && row >= c) {
-                            x = make_uint4(0u, 0u, 0u, 0u);
-                        } else if (ELU1 || GATE == 1) {
-                            uint32_t u[4] = {x.x, x.y, x.z, x.w};
-                            if (ELU1) {
+                        for (int j = 0; j < 4; ++j) {
+                            const int row = (pd >> 3) + 32 * (j & 1);
+                            uint4 &x = w[j];
+                            if (isk && row >= c) {
+                                x = make_uint4(0u, 0u, 0u, 0u);
+                            } else if (ELU1 || GATE == 1) {
+                                uint32_t u[4] = {x.x, x.y, x.z, x.w};
+                                if (ELU1) {
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) u[e] = phi_elu1_bf16x2(u[e]);
+                                    for (int e = 0; e < 4; ++e) u[e] = phi_elu1_bf16x2(u[e]);
+                                }
+                                if (GATE == 1) {
+                                    const float fr = fr_arr[row];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) u[e] = pack_bf16(bf16lo(u[e]) * fr, bf16hi(u[e]) * fr);
+                                }
+                                x = make_uint4(u[0], u[1], u[2], u[3]);
                             }
-                            if (GATE == 1) {
-                                const float fr = fr_arr[row];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) u[e] = pack_bf16(bf16lo(u[e]) * fr, bf16hi(u[e]) * fr);
-                            }
-                            x = make_uint4(u[0], u[1], u[2], u[3]);
+                            *reinterpret_cast<uint4 *>(tile + (j >> 1) * kHalf + row * 128 + (pd & 7) * 16) = x;
                         }
-                        *reinterpret_cast<uint4 *>(tile + (i >> 2) * kHalf + row * 128 + pc * 16) = x;
                     }
                 }
                 if (GATE == 1) b_last = (float)c * lg;
+                b_total += b_last;
+                if (GATE != 0 && pd < 128) {
+                    fbuf[(n % NF) * 128 + pd] = __expf(b_last);
+                    mbar_arrive(&ffull[n % NF]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&pro[s]);
+                if (GATE == 1) named_sync<kBarPro, 256>();  // fq/fk are rewritten for the next chunk
             }
-            b_total += b_last;
-            if (GATE != 0) {
-                fbuf[(n % NF) * 128 + d] = __expf(b_last);
-                mbar_arrive(&ffull[n % NF]);
+            if (!bad && pd < 128) {
+                ffinal[pd] = GATE == 0 ? 1.f : __expf(b_last);
+                if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + pd] = b_total;
+                mbar_arrive(profinal);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&pro[s]);
-            if (GATE == 1) named_sync<kBarPro, 128>();  // fq/fk are rewritten for the next chunk
-        }
-        if (!bad) {
-            ffinal[d] = GATE == 0 ? 1.f : __expf(b_last);
-            if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + d] = b_total;
-            mbar_arrive(profinal);
-        }
         }
     } else if (warp >= 8 && warp < 12) {
         // ============================================================ state chain
