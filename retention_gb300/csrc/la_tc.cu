@@ -82,39 +82,56 @@ struct TcParams {
 
 constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
 
-// Shared-memory layout. A stage holds q | k | v | (ones) | (g); the ones block
-// is the 64-column swizzle atom that follows v as the third N atom of [V | 1].
-// The state-only pass reads no q and keeps no P, S' or O, so its stages are
-// smaller and its ring deeper (as deep as the budget allows, at most 6). In
-// the full pass the gate tiles g have a ring of their own (GR): the prologue
-// is done with g after its first pass, so g is released early and the next
-// chunk's g is already in place when the prologue turns to it.
+// Shared-memory layout. Tiles are [64 x 128] bf16, kept as two 8 KiB swizzle
+// blocks (columns 0..63 and 64..127) that need not be adjacent.
+//
+// State-only pass (no q, P, S' or O): contiguous stages k | v | (ones) | (g),
+// as many as the budget allows (at most 6).
+//
+// Full pass: stage s holds q, k, v as six blocks whose indices come from a
+// table (one byte per stage in a 32-bit constant). Without the normaliser the
+// stages are contiguous. With it, one constant ones block T serves every
+// stage: [V | 1] reaches its three N atoms at v0, v0 + LBO, v0 + 2 LBO, so
+// stage s puts v1 at T - d and v0 at T - 2d (d = 1, 3, 5), and q, k take the
+// remaining blocks in order. The gate tiles g have a ring of their own (GR):
+// the prologue is done with g after its first pass, so g is released early
+// and the next chunk's g is already in place when the prologue turns to it.
 template <int GATE, bool NORM, bool SO>
 struct Layout {
     static constexpr bool GR = GATE == 2 && !SO;
     // gated without the normaliser: three q|k|v stages and one gate slot fit;
     // with it, two stages and two gate slots
     static constexpr int NG = GR ? (NORM ? 2 : 1) : 0;          // gate ring slots
-    static constexpr uint32_t q = 0;                            // offsets in a stage
-    static constexpr uint32_t k = SO ? 0 : kTile;
-    static constexpr uint32_t v = k + kTile;
-    static constexpr uint32_t ones = v + kTile;
-    static constexpr uint32_t g = ones + (NORM ? kHalf : 0);    // (in the stage unless GR)
-    static constexpr uint32_t stage = g + (GATE == 2 && !GR ? kTile : 0);
+    // state-only stage: k | v | (ones) | (g)
+    static constexpr uint32_t so_stage = 2 * kTile + (NORM ? kHalf : 0) + (GATE == 2 ? kTile : 0);
     // room kept for the float arrays, barriers and alignment slack below
     static constexpr uint32_t kReserve = 8192;
-    static constexpr int NS = !SO ? (NORM ? 2 : 3)
-                                  : ((kSmemBudget - kReserve) / stage < 6 ? (kSmemBudget - kReserve) / stage : 6);
-    static constexpr uint32_t Gring = NS * stage;                          // [NG] g tiles
+    static constexpr int NS = !SO ? ((NORM && GATE != 0) ? 2 : 3)
+                                  : ((kSmemBudget - kReserve) / so_stage < 6 ? (kSmemBudget - kReserve) / so_stage : 6);
+    static constexpr int T = 6 * NS;  // the shared ones block (full pass with the normaliser)
+    static constexpr uint32_t pack(int a, int b, int c) {
+        return (uint32_t)a | ((uint32_t)b << 8) | ((uint32_t)c << 16);
+    }
+    // block table of the full pass: half h of tile tl (0 q, 1 k, 2 v), one byte per stage
+    static constexpr uint32_t table(int tl, int h) {
+        return !NORM    ? pack(2 * tl + h, 6 + 2 * tl + h, 12 + 2 * tl + h)
+               : tl == 2 ? (h ? pack(T - 1, T - 3, T - 5) : pack(T - 2, T - 6, T - 10))
+               : NS == 3 ? (tl == 0 ? (h ? pack(1, 5, 10) : pack(0, 4, 9)) : (h ? pack(3, 7, 14) : pack(2, 6, 11)))
+                         : (tl == 0 ? (h ? pack(1, 5, 0) : pack(0, 4, 0)) : (h ? pack(3, 8, 0) : pack(2, 7, 0)));
+    }
+    static constexpr uint32_t stages = SO ? NS * so_stage : (6 * NS + (NORM ? 1 : 0)) * kHalf;
+    static constexpr uint32_t Gring = stages;                              // [NG] g tiles
     static constexpr uint32_t P = Gring + NG * kTile;                      // bf16 P tile, 8 KiB
     static constexpr uint32_t S = P + (SO ? 0 : 8192);                     // bf16 S_{n-1} (+ z atom), 32 / 48 KiB
     static constexpr uint32_t O = S + (SO ? 0 : (NORM ? 49152 : 32768));   // bf16 O staging, two swizzled halves
-    // floats: fbuf[NF][128] ffinal[128] fq[64] fk[64] (gated: tot[4][128]). fbuf is
-    // a ring of NF = NS + 1 slots: chunk n's decay factor goes to slot n % NF at
-    // the end of its prologue, for the state chain to rescale T_n with.
+    // floats: ffinal[128], then with a gate fbuf[NF][128], with the head gate
+    // fq[64] fk[64], with the channel gate tot[4][128]. fbuf is a ring of
+    // NF = NS + 1 slots: chunk n's decay factor goes to slot n % NF at the end of
+    // its prologue, for the state chain to rescale T_n with.
     static constexpr int NF = NS + 1;
     static constexpr uint32_t F = O + (SO ? 0 : 16384);
-    static constexpr uint32_t Bar = F + (NF * 128 + 128 + 128 + (GATE == 2 ? 512 : 0)) * 4;
+    static constexpr uint32_t nfbuf = GATE != 0 ? NF * 128 : 0, nfq = GATE == 1 ? 128 : 0;
+    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + (GATE == 2 ? 512 : 0)) * 4;
     // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal,
     // drain; gfull, gempty [NG]; ffull [NF]
     static constexpr uint32_t nbar = 3 * NS + 12 + 2 * NG + NF;
@@ -194,10 +211,21 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     const size_t segblk = (size_t)blockIdx.x * blk;
 
     constexpr int NF = LY::NF;
-    float *fbuf = reinterpret_cast<float *>(sm + LY::F);  // [NF][128] chunk n's decay factor e^{b_last(n)}
-    float *ffinal = fbuf + NF * 128;                      // [128] e^{b_last} of the last chunk
-    float *fq = ffinal + 128;                             // [64] retention: gamma^(t+1)
-    float *fk = fq + 64;                                  // [64] retention: gamma^-(t+1)
+    float *ffinal = reinterpret_cast<float *>(sm + LY::F);  // [128] e^{b_last} of the last chunk
+    float *fbuf = ffinal + 128;                             // [NF][128] chunk n's decay factor e^{b_last(n)}
+    float *fq = fbuf + LY::nfbuf;                           // [64] retention: gamma^(t+1)
+    float *fk = fq + 64;                                    // [64] retention: gamma^-(t+1)
+    float *tot = fq + LY::nfq;                              // [4][128] gated: per-quarter log2 decay sums
+    // Shared-memory offset of half h (columns 64h..64h+63) of tile tl of stage
+    // s: tl = 0 q, 1 k, 2 v, 3 g (the g tile of a state-only stage)
+    auto tile_half = [&](int tl, int s, int h) -> uint32_t {
+        if constexpr (SO) {
+            const uint32_t base = s * LY::so_stage + h * kHalf;
+            return tl == 1 ? base : tl == 2 ? base + kTile : base + 2 * kTile + (NORM ? kHalf : 0);
+        } else {
+            return ((LY::table(tl, h) >> (8 * s)) & 255u) * kHalf;
+        }
+    };
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + LY::Bar);
     uint64_t *full = bars, *empty = bars + NS, *pro = bars + 2 * NS;
     uint64_t *ofull = bars + 3 * NS, *oempty = ofull + 2;
@@ -243,12 +271,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         if (GATE == 2) tma_prefetch_desc(&p.tg);
     }
     if (NORM) {
-        // constant blocks: per stage a [64 x 64] atom whose column 0 is 1 (the
-        // ones column of [V | 1]); the z atom of the S' copy starts at zero
-        for (int i = tid; i < NS * 512; i += kThreads) {
+        // constant blocks: the [64 x 64] atom(s) whose column 0 is 1 (the ones
+        // column of [V | 1]: one per state-only stage, one shared by the full
+        // pass's stages); the z atom of the S' copy starts at zero
+        constexpr int nones = SO ? NS : 1;
+        for (int i = tid; i < nones * 512; i += kThreads) {
             const int s = i >> 9, r = (i >> 3) & 63, pc = i & 7;
             const uint32_t one = (((pc ^ r) & 7) == 0) ? 0x3f80u : 0u;  // bf16 1.0 in element 0
-            *reinterpret_cast<uint4 *>(sm + s * LY::stage + LY::ones + r * 128 + pc * 16) = make_uint4(one, 0u, 0u, 0u);
+            const uint32_t base = SO ? s * LY::so_stage + 2 * kTile : LY::T * kHalf;
+            *reinterpret_cast<uint4 *>(sm + base + r * 128 + pc * 16) = make_uint4(one, 0u, 0u, 0u);
         }
         if (!SO)
             for (int i = tid; i < 1024; i += kThreads)
@@ -287,14 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     bad = 1;
                     break;
                 }
-                uint8_t *base = sm + s * LY::stage;
                 mbar_arrive_expect_tx(&full[s], (ntl - (SO ? 1 : 0)) * kTile);
 #pragma unroll 1
                 for (int tl = SO ? 1 : 0; tl < ntl; ++tl) {
                     const CUtensorMap *m = tl == 0 ? &p.tq : tl == 1 ? &p.tk : tl == 2 ? &p.tv : &p.tg;
-                    uint8_t *dst = base + (tl == 0 ? LY::q : tl == 1 ? LY::k : tl == 2 ? LY::v : LY::g);
-                    tma_load_3d(dst, m, &full[s], 0, t0, bh);
-                    tma_load_3d(dst + kHalf, m, &full[s], 64, t0, bh);
+                    tma_load_3d(sm + tile_half(tl, s, 0), m, &full[s], 0, t0, bh);
+                    tma_load_3d(sm + tile_half(tl, s, 1), m, &full[s], 64, t0, bh);
                 }
                 issued = n + 1;
             }
@@ -315,17 +344,25 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             const uint32_t sm0 = smem_u32(sm);
             const uint64_t dS = sdesc_sw128(smem_u32(sS), 16384, 1024);   // S' copy, MN-major
             const uint64_t dP = sdesc_sw128(smem_u32(sP), 16, 1024);      // P, K-major
-            auto dq = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + LY::q, 16, 1024); };
-            auto dkk = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + LY::k, 16, 1024); };
-            auto dkm = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + LY::k, kHalf, 1024); };
-            auto dvm = [&](int n) { return sdesc_sw128(sm0 + (n % NS) * LY::stage + LY::v, kHalf, 1024); };
+            // K-major q and k: one descriptor per 64-column half; MN-major k and
+            // [V | 1]: the halves (and the ones block) are the N atoms, LBO apart
+            auto dkm = [&](int n) {
+                const uint32_t k0 = tile_half(1, n % NS, 0), k1 = tile_half(1, n % NS, 1);
+                return sdesc_sw128(sm0 + k0, k1 - k0, 1024);
+            };
+            auto dvm = [&](int n) {
+                const uint32_t v0 = tile_half(2, n % NS, 0), v1 = tile_half(2, n % NS, 1);
+                return sdesc_sw128(sm0 + v0, v1 - v0, 1024);
+            };
             auto issue_qk = [&](int n) {
-                const uint64_t a = dq(n), bb = dkk(n);
+                const uint64_t a0 = sdesc_sw128(sm0 + tile_half(0, n % NS, 0), 16, 1024);
+                const uint64_t a1 = sdesc_sw128(sm0 + tile_half(0, n % NS, 1), 16, 1024);
+                const uint64_t b0 = sdesc_sw128(sm0 + tile_half(1, n % NS, 0), 16, 1024);
+                const uint64_t b1 = sdesc_sw128(sm0 + tile_half(1, n % NS, 1), 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t off = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
-                    umma_bf16(tmem + LY::colP, a + off, bb + off, id_qk, ks > 0);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16(tmem + LY::colP, (ks < 4 ? a0 : a1) + (ks & 3) * 2, (ks < 4 ? b0 : b1) + (ks & 3) * 2,
+                              id_qk, ks > 0);
                 umma_commit(qk);
             };
             if (SO) {
@@ -353,7 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             for (int n = 0; n < N && !bad && !SO; ++n) {
                 const int s = n % NS, b = n % LY::NOB;
                 const uint32_t dO = tmem + (b ? LY::colO1 : LY::colO0);
-                const uint64_t aq = dq(n), ak = dkm(n), bv = dvm(n);
+                const uint64_t aq0 = sdesc_sw128(sm0 + tile_half(0, s, 0), 16, 1024);
+                const uint64_t aq1 = sdesc_sw128(sm0 + tile_half(0, s, 1), 16, 1024);
+                const uint64_t ak = dkm(n), bv = dvm(n);
                 if ((n > 0 || init) && !mbar_wait(sready, (uint32_t)(n - 1 + (init ? 1 : 0)) & 1u, kWaitNs)) {
                     bad = 1;
                     break;
@@ -373,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        umma_bf16(dO, aq + (((ks >> 2) * kHalf + (ks & 3) * 32) >> 4), dS + ks * 128, id_o, ks > 0);
+                        umma_bf16(dO, (ks < 4 ? aq0 : aq1) + (ks & 3) * 2, dS + ks * 128, id_o, ks > 0);
                 }
                 umma_commit(sfree);
                 // intra: O += P [V | 1]
@@ -426,9 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // decay and writes the state factors.
             const int ch = pw & 1, qr = pw >> 1;
             const int cw = 64 * ch + 2 * lane;  // first of the thread's two channels
-            const uint32_t colw = ch * kHalf + ((lane & 3) << 2), slot = lane >> 2;
+            const uint32_t colw = (lane & 3) << 2, slot = lane >> 2;  // within the block of half ch
             auto offw = [&](int u) { return colw + (16 * qr + u) * 128 + (((slot ^ u) & 7) << 4); };
-            float *tot = fk + 64;  // [4][128] per-quarter log2 decay sums
             // log2 decay of the two channels over the previous chunk and over the
             // segment so far (kept by quarter 3)
             float bl0 = 0.f, bl1 = 0.f, bt0 = 0.f, bt1 = 0.f;
@@ -441,8 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     bad = 1;
                     break;
                 }
-                uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k;
-                const uint8_t *sG = LY::GR ? sm + LY::Gring + (n % NG) * kTile : sm + s * LY::stage + LY::g;
+                // the blocks of this thread's channel half
+                uint8_t *sQ = sm + tile_half(0, s, ch), *sK = sm + tile_half(1, s, ch);
+                const uint8_t *sG = LY::GR ? sm + LY::Gring + (n % NG) * kTile + ch * kHalf : sm + tile_half(3, s, ch);
                 float la0[16], la1[16], s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
@@ -541,7 +580,6 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     bad = 1;
                     break;
                 }
-                uint8_t *sQ = sm + s * LY::stage + LY::q, *sK = sm + s * LY::stage + LY::k;
                 if (GATE == 1 && pd < 64) {
                     fq[pd] = __expf((float)(pd + 1) * lg);
                     fk[pd] = __expf(-(float)(pd + 1) * lg);
@@ -550,12 +588,12 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 if (ELU1 || GATE == 1 || c < kC) {
 #pragma unroll
                     for (int isk = SO ? 1 : 0; isk < 2; ++isk) {
-                        uint8_t *tile = isk ? sK : sQ;
+                        uint8_t *blk0 = sm + tile_half(isk, s, 0), *blk1 = sm + tile_half(isk, s, 1);
                         const float *fr_arr = isk ? fk : fq;
                         uint4 w[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            w[j] = *reinterpret_cast<const uint4 *>(tile + (j >> 1) * kHalf +
+                            w[j] = *reinterpret_cast<const uint4 *>((j >> 1 ? blk1 : blk0) +
                                                                     ((pd >> 3) + 32 * (j & 1)) * 128 + (pd & 7) * 16);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -576,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                                 }
                                 x = make_uint4(u[0], u[1], u[2], u[3]);
                             }
-                            *reinterpret_cast<uint4 *>(tile + (j >> 1) * kHalf + row * 128 + (pd & 7) * 16) = x;
+                            *reinterpret_cast<uint4 *>((j >> 1 ? blk1 : blk0) + row * 128 + (pd & 7) * 16) = x;
                         }
                     }
                 }
@@ -660,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 break;
             }
             tc_fence_after();
-            const float f = fbuf[((n - 1) % NF) * 128 + i];
+            const float f = GATE != 0 ? fbuf[((n - 1) % NF) * 128 + i] : 1.f;
             if (GATE != 0) {
                 // S_{n-1} = diag(f) T_{n-1}, in place (z rides in column 128)
 #pragma unroll 1
