@@ -273,8 +273,11 @@ def bench_chunk(name, steps, warmup, world, pk):
 
 def bench_e2e(cfg, steps, warmup, world):
     """The same call with the inputs in pinned host memory: every step copies
-    q, k, v (and the gate) to the device, runs la_chunk_fwd, and copies the
-    output and final state back, all inside the timed region."""
+    q, k, v to the device, runs la_chunk_fwd, and copies the output and final
+    state back, all inside the timed region. Steps are pipelined the way a
+    serving loop would run them: two device buffer sets and three streams
+    (upload, compute, read-back), so step i+1's upload overlaps step i's
+    compute and read-back."""
     from retention_gb300 import la
     gen = torch.Generator("cpu").manual_seed(1)
     B, H, L, dk, dv = cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"]
@@ -287,24 +290,57 @@ def bench_e2e(cfg, steps, warmup, world):
     ho = torch.empty(B, H, L, dv, dtype=dt).pin_memory()
     blk = la.state_block(dk, dv, cfg["normalize"])
     hs = torch.empty(B, H, blk, dtype=torch.float32).pin_memory()
-    dq, dk_, dv_ = (torch.empty_like(t, device="cuda") for t in (hq, hk, hv))
-    do = torch.empty_like(ho, device="cuda")
-    ds = torch.empty_like(hs, device="cuda")
+    dev = [dict(q=torch.empty_like(hq, device="cuda"), k=torch.empty_like(hk, device="cuda"),
+                v=torch.empty_like(hv, device="cuda"), o=torch.empty_like(ho, device="cuda"),
+                s=torch.empty_like(hs, device="cuda")) for _ in range(2)]
+    s_up, s_run, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    up_done = [torch.cuda.Event() for _ in range(2)]
+    run_done = [torch.cuda.Event() for _ in range(2)]
+    down_done = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk_.copy_(hk, non_blocking=True)
-        dv_.copy_(hv, non_blocking=True)
-        la.chunk_fwd(dq, dk_, dv_, None, phi=cfg["phi"], normalize=cfg["normalize"],
-                     gate_kind=cfg["gate"], chunk=cfg["chunk"], out=do, final_state=ds)
-        ho.copy_(do, non_blocking=True)
-        hs.copy_(ds, non_blocking=True)
+    def run(n):
+        cur = torch.cuda.current_stream()
+        for st in (s_up, s_run, s_down):
+            st.wait_stream(cur)
+        for i in range(n):
+            b, d = i % 2, dev[i % 2]
+            with torch.cuda.stream(s_up):
+                s_up.wait_event(run_done[b])      # step i-2 is done with these inputs
+                d["q"].copy_(hq, non_blocking=True)
+                d["k"].copy_(hk, non_blocking=True)
+                d["v"].copy_(hv, non_blocking=True)
+                up_done[b].record(s_up)
+            with torch.cuda.stream(s_run):
+                s_run.wait_event(up_done[b])
+                s_run.wait_event(down_done[b])    # step i-2's results have left
+                la.chunk_fwd(d["q"], d["k"], d["v"], None, phi=cfg["phi"], normalize=cfg["normalize"],
+                             gate_kind=cfg["gate"], chunk=cfg["chunk"], out=d["o"], final_state=d["s"],
+                             stream=s_run)
+                run_done[b].record(s_run)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(run_done[b])
+                ho.copy_(d["o"], non_blocking=True)
+                hs.copy_(d["s"], non_blocking=True)
+                down_done[b].record(s_down)
+        cur.wait_stream(s_down)
 
-    secs = max_over_ranks(time_calls(step, steps, warmup, world), world)
+    run(warmup)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    secs = max_over_ranks(e0.elapsed_time(e1) / 1000.0, world)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
     return {"value": world * B * L * steps / secs, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": secs / steps * 1e3}
+            "d2h_bytes_per_step": d2h, "ms_per_step": secs / steps * 1e3,
+            "pipelined": "2 buffer sets, upload / compute / read-back streams"}
 
 
 def bench_decode(steps_total, world, pk):
@@ -398,7 +434,7 @@ def main():
         la_res = bench_chunk("la", args.steps, warmup, world, pk)
     clocks = clk.summary()
     cfg = la_res["cfg"]
-    e2e = bench_e2e(cfg, max(3, args.steps // 5), 2, world)
+    e2e = bench_e2e(cfg, max(8, args.steps // 2), 2, world)
     del la_res["inputs"]
     dec = bench_decode(args.decode_steps, world, pk)
     extra = {}
