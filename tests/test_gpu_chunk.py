@@ -96,6 +96,22 @@ def test_bf16_chunk_boundaries(name, L):
     _check(cfg, seed=L)
 
 
+# ------------------------------------------------------------------ bf16, every mode on the tensor cores
+
+@pytest.mark.parametrize("m", FP32_MODES, ids=lambda m: "%s-%s-%s" % (m["phi"], m["normalize"], m["gate"]))
+@pytest.mark.parametrize("B,H,L", [(1, 2, 1000), (2, 40, 200)], ids=["split", "unsplit"])
+def test_bf16_modes_tensor_cores(m, B, H, L):
+    """Every feature-map / normaliser / gate combination through the
+    tensor-core kernel, with few sequences (each cut into segments: state-only
+    pass, scan, full pass) and with one CTA per sequence. The combinations have
+    their own shared-memory layouts (stage count, shared ones block, gate ring)."""
+    from retention_gb300 import la
+    cfg = W.workload("la", B=B, H=H, L=L, **m)
+    mode = la.mode_bits(cfg["phi"], cfg["normalize"], cfg["gate"])
+    assert la.chunk_fwd_path(B, H, L, cfg["dk"], cfg["dv"], mode, cfg["chunk"]) == 1
+    _check(cfg, seed=7)
+
+
 # ------------------------------------------------------------------ full size
 
 @pytest.mark.parametrize("name", ["la", "retention", "gla"])
