@@ -573,6 +573,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
             // log decay of key channel pd over the previous chunk and over the segment so far
             float b_last = 0.f, b_total = 0.f;
+            if (GATE == 1) {
+                // the row factors gamma^(t+1) and gamma^-(t+1) are the same in every chunk
+                if (pd < 64) {
+                    fq[pd] = __expf((float)(pd + 1) * lg);
+                    fk[pd] = __expf(-(float)(pd + 1) * lg);
+                }
+                named_sync<kBarPro, 256>();
+            }
             for (int n = 0; n < N; ++n) {
                 const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
                 const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
@@ -580,11 +588,6 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     bad = 1;
                     break;
                 }
-                if (GATE == 1 && pd < 64) {
-                    fq[pd] = __expf((float)(pd + 1) * lg);
-                    fk[pd] = __expf(-(float)(pd + 1) * lg);
-                }
-                if (GATE == 1) named_sync<kBarPro, 256>();
                 if (ELU1 || GATE == 1 || c < kC) {
 #pragma unroll
                     for (int isk = SO ? 1 : 0; isk < 2; ++isk) {
@@ -626,7 +629,6 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&pro[s]);
-                if (GATE == 1) named_sync<kBarPro, 256>();  // fq/fk are rewritten for the next chunk
             }
             if (!bad && pd < 128) {
                 ffinal[pd] = GATE == 0 ? 1.f : __expf(b_last);
