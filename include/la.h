@@ -68,7 +68,8 @@ typedef enum {
 
 /*
  * la_chunk_fwd -- the chunkwise-parallel forward pass over whole sequences,
- * starting from S_0 = 0 (and z_0 = 0).
+ * starting from S_0 = 0 (and z_0 = 0) (ajkdrag zettel "causal linear
+ * attention as an RNN": the recurrence starts from an empty state).
  *
  * Chunkwise form (learnllm m22 "The Three Faces of Retention";
  * linear_sparse_attention.py linear_attn_chunkwise): the L tokens are cut into
@@ -89,19 +90,40 @@ typedef enum {
  *          returns LA_ERR_UNSUPPORTED when its tiles do not fit on chip.
  *   mode   LA_PHI_* | LA_NORMALIZE | LA_GATE_* | LA_DTYPE_F32 | LA_KERNEL_SIMT
  *
- * Scratch: when the batch has too few (b, h) sequences to fill the GPU, the
- * gated tensor-core path splits each sequence into segments and takes
- * stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`) for the
- * per-segment states; a failed allocation returns LA_ERR_CUDA.
+ * Scratch: when the batch has too few (b, h) sequences to fill the GPU (2 B H
+ * at most the number of SMs), the tensor-core path splits each sequence into
+ * segments and takes stream-ordered scratch (cudaMallocAsync / cudaFreeAsync
+ * on `stream`) for the per-segment states; a failed allocation returns
+ * LA_ERR_CUDA.
  *
  * Range of the tensor-core kernel: it factors the decay inside a chunk as
- * exp(b_t - beta) * exp(beta - b_s) around the chunk's middle, which is exact
+ * exp(b_t) * exp(-b_s), b the log decay from the chunk start, which is exact
  * in real arithmetic and stays in fp32/bf16 range while the log-decay over one
- * chunk, per channel, is above -170 (retention: gamma^chunk > 1e-74).
+ * chunk, per channel, is above about -87 (retention: gamma^chunk > 1.6e-38);
+ * the general kernel (LA_KERNEL_SIMT) has no such limit.
  */
 int la_chunk_fwd(const void *q, const void *k, const void *v, const void *gate,
                  void *out, float *final_state, int B, int H, int L, int dk,
                  int dv, int mode, int chunk, la_stream_t stream);
+
+/*
+ * la_chunk_fwd_from_state -- la_chunk_fwd starting from a given state instead
+ * of zero: the continuation of a sequence whose first part is summarised by
+ * that state (learnllm m22 "Code: The Two Faces": the state is all a sequence
+ * needs to go on; a prefill's final_state continues here, or in
+ * la_decode_step, and this call's final_state continues in either).
+ *
+ *   initial_state  NULL (then exactly la_chunk_fwd), or [B][H][block] fp32,
+ *                  the state S (then z when LA_NORMALIZE) before the first
+ *                  token of each sequence; 16-byte aligned; read only, and it
+ *                  must not overlap final_state or out
+ *   every other argument, the results and the errors as in la_chunk_fwd; with
+ *   L = 0 the final state is a copy of the initial state.
+ */
+int la_chunk_fwd_from_state(const void *q, const void *k, const void *v, const void *gate,
+                            const float *initial_state, void *out, float *final_state, int B,
+                            int H, int L, int dk, int dv, int mode, int chunk,
+                            la_stream_t stream);
 
 /*
  * la_decode_step -- one recurrent step for every (b, h), in place on `state`

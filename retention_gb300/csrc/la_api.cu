@@ -26,13 +26,9 @@ int check_mode(int mode, const void *gate, bool decode) {
     return LA_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int la_chunk_fwd(const void *q, const void *k, const void *v, const void *gate, void *out,
-                 float *final_state, int B, int H, int L, int dk, int dv, int mode, int chunk,
-                 la_stream_t stream) {
+int chunk_fwd(const void *q, const void *k, const void *v, const void *gate, const float *initial_state,
+              void *out, float *final_state, int B, int H, int L, int dk, int dv, int mode, int chunk,
+              la_stream_t stream) {
     if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
     if (chunk < 1 || chunk > 128) return LA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
@@ -43,13 +39,16 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const void *gate, 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool norm = mode & LA_NORMALIZE;
     if (nbh == 0) return LA_OK;
+    if (initial_state && !aligned16(initial_state)) return LA_ERR_MISALIGNED;
     if (L == 0) {
-        // an empty sequence leaves S_0 = 0 (and z_0 = 0)
+        // an empty sequence leaves the starting state: S_0 = 0 (and z_0 = 0) or the given one
         if (final_state) {
             if (!aligned16(final_state)) return LA_ERR_MISALIGNED;
-            const size_t blk = (size_t)dk * dv + (norm ? dk : 0);
-            if (cudaMemsetAsync(final_state, 0, (size_t)nbh * blk * sizeof(float), s) != cudaSuccess)
-                return LA_ERR_CUDA;
+            const size_t bytes = (size_t)nbh * ((size_t)dk * dv + (norm ? dk : 0)) * sizeof(float);
+            const cudaError_t e = initial_state
+                ? cudaMemcpyAsync(final_state, initial_state, bytes, cudaMemcpyDeviceToDevice, s)
+                : cudaMemsetAsync(final_state, 0, bytes, s);
+            if (e != cudaSuccess) return LA_ERR_CUDA;
         }
         return LA_OK;
     }
@@ -59,7 +58,7 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const void *gate, 
     if ((mode & LA_GATE_CHANNEL) && !aligned16(gate)) return LA_ERR_MISALIGNED;
     if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
 
-    la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode, chunk};
+    la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode, chunk, initial_state};
     int launches = 0;
     if (!(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a))
         rc = la::launch_chunk_tc(a, s, &launches);
@@ -67,6 +66,22 @@ int la_chunk_fwd(const void *q, const void *k, const void *v, const void *gate, 
         rc = la::launch_chunk_simt(a, s, &launches);
     g_launches += (unsigned long long)launches;
     return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int la_chunk_fwd(const void *q, const void *k, const void *v, const void *gate, void *out,
+                 float *final_state, int B, int H, int L, int dk, int dv, int mode, int chunk,
+                 la_stream_t stream) {
+    return chunk_fwd(q, k, v, gate, nullptr, out, final_state, B, H, L, dk, dv, mode, chunk, stream);
+}
+
+int la_chunk_fwd_from_state(const void *q, const void *k, const void *v, const void *gate,
+                            const float *initial_state, void *out, float *final_state, int B, int H,
+                            int L, int dk, int dv, int mode, int chunk, la_stream_t stream) {
+    return chunk_fwd(q, k, v, gate, initial_state, out, final_state, B, H, L, dk, dv, mode, chunk, stream);
 }
 
 int la_decode_step(const void *q, const void *k, const void *v, const void *gate, float *state,

@@ -41,6 +41,7 @@ struct ChunkArgs {
     void *out;
     float *final_state;
     int B, H, L, dk, dv, mode, chunk;
+    const float *initial_state;  // [B][H][block] state before the first token, or null (zero)
 };
 
 struct DecodeArgs {

@@ -67,8 +67,10 @@ __global__ void __launch_bounds__(kSimtThreads) chunk_simt_kernel(ChunkArgs a, i
     const float gamma = ghead ? ((const float *)a.gate)[h] : 1.f;
     T *out = (T *)a.out + (size_t)bh * L * dv;
 
-    for (int i = tid; i < dk * dvt; i += nt) Ss[i] = 0.f;
-    for (int i = tid; i < dk; i += nt) zs[i] = 0.f;
+    // the state before the first token: zero, or this CTA's columns of the given one
+    const float *S0 = a.initial_state ? a.initial_state + (size_t)bh * ((size_t)dk * dv + (norm ? dk : 0)) : nullptr;
+    for (int i = tid; i < dk * dvt; i += nt) Ss[i] = S0 ? S0[(size_t)(i / dvt) * dv + col0 + i % dvt] : 0.f;
+    for (int i = tid; i < dk; i += nt) zs[i] = (S0 && norm) ? S0[(size_t)dk * dv + i] : 0.f;
     __syncthreads();
 
     for (int t0 = 0; t0 < L; t0 += C) {

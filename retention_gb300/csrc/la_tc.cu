@@ -78,6 +78,7 @@ struct TcParams {
     float *seg_state;        // [BH][nseg][blk]: segment-local end state (state-only pass)
     float *seg_logdecay;     // [BH][nseg][128]: log decay over each segment (state-only pass)
     int H, L, mode, nseg, seg_chunks;
+    int init0;               // segment 0 starts from state_in too (a given initial state)
 };
 
 constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     const int bh = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg, h = bh % p.H, L = p.L;
     const int c0 = seg * p.seg_chunks;
     const int N = max(0, min(p.seg_chunks, (L + kC - 1) / kC - c0));
-    const bool init = !SO && p.state_in != nullptr && seg > 0;  // start from a carried state
+    const bool init = !SO && p.state_in != nullptr && (seg > 0 || p.init0);  // start from a carried state
     const size_t blk = (size_t)kD * kD + (NORM ? kD : 0);
     const size_t segblk = (size_t)blockIdx.x * blk;
 
@@ -885,11 +886,13 @@ bool make_map(CUtensorMap *m, const void *base, int L, int BH) {
     return r == CUDA_SUCCESS;
 }
 
-// Segment scan: S_in(0) = 0, S_in(p+1) = diag(e^{B_p}) S_in(p) + dS_p, and the
-// state after the last segment is the final state. One thread per state
-// element (z included), a sequential loop over the segments.
+// Segment scan: S_in(0) = S_0 (the initial state, or 0), S_in(p+1) =
+// diag(e^{B_p}) S_in(p) + dS_p, and the state after the last segment is the
+// final state. One thread per state element (z included), a sequential loop
+// over the segments.
 __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restrict__ seg_state,
                                                           const float *__restrict__ seg_logdecay,
+                                                          const float *__restrict__ initial,
                                                           float *__restrict__ state_in, float *final_state,
                                                           int nseg, int blk) {
     const int bh = blockIdx.x;
@@ -897,9 +900,9 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
     if (e >= blk) return;
     const int d = e < kD * kD ? e / kD : e - kD * kD;  // key channel of this element
     const size_t base = (size_t)bh * nseg;
-    float acc = 0.f;
+    float acc = initial ? initial[(size_t)bh * blk + e] : 0.f;
     for (int sgi = 0; sgi < nseg; ++sgi) {
-        if (sgi > 0) state_in[(base + sgi) * blk + e] = acc;
+        if (sgi > 0 || initial) state_in[(base + sgi) * blk + e] = acc;
         acc = __expf(seg_logdecay[(base + sgi) * kD + d]) * acc + seg_state[(base + sgi) * blk + e];
     }
     if (final_state) final_state[(size_t)bh * blk + e] = acc;
@@ -978,7 +981,9 @@ int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches) {
     prm.L = a.L;
     prm.mode = a.mode;
     prm.nseg = tc_segments(BH, nchunks, &prm.seg_chunks);
+    prm.init0 = a.initial_state != nullptr;
     if (prm.nseg == 1) {
+        prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
         const int rc = launch_mode<false>(prm, BH, s, a.mode);
         if (rc == LA_OK) *launches += 1;
         return rc;
@@ -1000,7 +1005,7 @@ int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches) {
     if (rc == LA_OK) {
         *launches += 1;
         la_seg_scan_kernel<<<dim3((unsigned)BH, (unsigned)((blk + 255) / 256)), 256, 0, s>>>(
-            seg_state, seg_logdecay, state_in, a.final_state, prm.nseg, (int)blk);
+            seg_state, seg_logdecay, a.initial_state, state_in, a.final_state, prm.nseg, (int)blk);
         rc = cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
     }
     if (rc == LA_OK) {
@@ -1047,7 +1052,9 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.L = a.L;
     prm.mode = a.mode;
     prm.nseg = tc_segments(BH, nchunks, &prm.seg_chunks);
+    prm.init0 = a.initial_state != nullptr;
     if (prm.nseg == 1) {
+        prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
         const int rc = launch_mode<false>(prm, BH, s, a.mode);
         if (rc == LA_OK) *launches += 1;
         return rc;
@@ -1065,7 +1072,7 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     if (rc != LA_OK) return rc;
     *launches += 1;
     la_seg_scan_kernel<<<dim3((unsigned)BH, (unsigned)((blk + 255) / 256)), 256, 0, s>>>(
-        seg_state, seg_logdecay, state_in, a.final_state, prm.nseg, (int)blk);
+        seg_state, seg_logdecay, a.initial_state, state_in, a.final_state, prm.nseg, (int)blk);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     *launches += 1;
     prm.state_in = state_in;

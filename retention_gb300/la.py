@@ -31,6 +31,7 @@ SIGNATURES = {
     "la_chunk_fwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_decode_step": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
+    "la_chunk_fwd_from_state": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_path": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "la_status_string": ([_I], ctypes.c_char_p),
     "la_kernel_launches": ([], ctypes.c_ulonglong),
@@ -105,8 +106,10 @@ def state_block(dk, dv, normalize):
 
 
 def chunk_fwd(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None, chunk=64,
-              out=None, final_state=None, want_state=True, simt=False, stream=None):
-    """la_chunk_fwd over q, k [B,H,L,dk], v [B,H,L,dv]. Returns (out, final_state)."""
+              out=None, final_state=None, want_state=True, simt=False, stream=None, initial_state=None):
+    """la_chunk_fwd over q, k [B,H,L,dk], v [B,H,L,dv]. Returns (out, final_state).
+    With ``initial_state`` ([B,H,block] fp32) it is la_chunk_fwd_from_state: the
+    sequences continue from that state instead of zero."""
     B, H, L, dk = q.shape
     dv = v.shape[-1]
     if out is None:
@@ -115,11 +118,21 @@ def chunk_fwd(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None
         final_state = torch.empty(B, H, state_block(dk, dv, normalize), dtype=torch.float32,
                                   device=q.device)
     mode = mode_bits(phi, normalize, gate_kind, q.dtype, simt)
-    rc = load().la_chunk_fwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
-                             _dev(out, "out"), _dev(final_state, "final_state"),
-                             B, H, L, dk, dv, mode, chunk, _stream(stream))
-    if rc != LA_OK:
-        raise LAError("la_chunk_fwd", rc)
+    if initial_state is None:
+        rc = load().la_chunk_fwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
+                                 _dev(out, "out"), _dev(final_state, "final_state"),
+                                 B, H, L, dk, dv, mode, chunk, _stream(stream))
+        if rc != LA_OK:
+            raise LAError("la_chunk_fwd", rc)
+    else:
+        if initial_state.dtype != torch.float32:
+            raise ValueError("initial_state must be float32")
+        rc = load().la_chunk_fwd_from_state(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
+                                            _dev(initial_state, "initial_state"), _dev(out, "out"),
+                                            _dev(final_state, "final_state"),
+                                            B, H, L, dk, dv, mode, chunk, _stream(stream))
+        if rc != LA_OK:
+            raise LAError("la_chunk_fwd_from_state", rc)
     return out, final_state
 
 
