@@ -8,6 +8,7 @@ Two parts:
 
 * ``forward`` / ``decode_step``: the definition, the recurrent form in fp64
   (``la_oracle.c``, called through ctypes, OpenMP over (batch, head)).
+* ``delta_forward``: the delta rule (DeltaNet), recurrent, fp64, same file.
 * ``forms``: independent numpy restatements (parallel masked matmul, brute
   force double sum, chunkwise) used to pin the definition, plus a numpy copy
   of the recurrence for tiny cases.
@@ -47,6 +48,9 @@ def _load():
         lib.oracle_decode_step.argtypes = [f32p, f32p, f32p, f32p, f64p, i, i, i, i, i,
                                            f64p, i]
         lib.oracle_decode_step.restype = i
+        lib.oracle_delta_forward.argtypes = [f32p, f32p, f32p, f32p, f64p, i, i, i, i, i,
+                                             f64p, f64p, i]
+        lib.oracle_delta_forward.restype = i
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i
         _lib = lib
@@ -116,3 +120,28 @@ def decode_step(q, k, v, state, gate=None, mode=0, nthreads=0):
     if rc != 0:
         raise ValueError("oracle_decode_step rejected its arguments")
     return out
+
+
+def delta_forward(q, k, v, beta, state_in=None, nthreads=0):
+    """The delta rule, recurrent, fp64: S = S (I - beta k k^T) + beta v k^T per
+    token, out_t = S q_t. q,k: [B,H,L,dk]; v: [B,H,L,dv]; beta: [B,H,L].
+    State blocks are dv x dk (row = value dimension). Returns (out [B,H,L,dv],
+    state [B,H,dv*dk]), both float64."""
+    lib = _load()
+    q, k, v, beta = _f32(q), _f32(k), _f32(v), _f32(beta)
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape[:3] == q.shape[:3] and beta.shape == q.shape[:3]
+    out = np.empty((B, H, L, dv), dtype=np.float64)
+    st = np.empty((B, H, dv * dk), dtype=np.float64)
+    sin = None
+    if state_in is not None:
+        sin = np.ascontiguousarray(np.asarray(state_in, dtype=np.float64)).reshape(B, H, dv * dk)
+    rc = lib.oracle_delta_forward(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float),
+                                  _ptr(v, ctypes.c_float), _ptr(beta, ctypes.c_float),
+                                  _ptr(sin, ctypes.c_double), B, H, L, dk, dv,
+                                  _ptr(out, ctypes.c_double), _ptr(st, ctypes.c_double),
+                                  int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_delta_forward rejected its arguments")
+    return out, st

@@ -159,3 +159,30 @@ def chunkwise(q, k, v, a, C, elu1=False, normalize=False):
             newz = newz + w * kf[s0 + s]
         R, zR = newR, newz
     return out, R, zR
+
+
+def delta_recurrent(K, V, beta, Q=None, use_delta=True, S0=None):
+    """The delta rule as matrix products, one token at a time
+    (linear_sparse_attention.py, "delta_rule_recurrent"): S is d_v x d_k,
+        S <- S (I - beta_t k_t k_t^T)   (skipped when use_delta is False)
+        S <- S + beta_t v_t k_t^T
+    and, with queries, out_t = S q_t after the update. K, Q: [L, dk]; V: [L, dv];
+    beta: [L]. Returns (states [L, dv, dk], out [L, dv] or None)."""
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    beta = np.asarray(beta, dtype=np.float64)
+    L, dk = K.shape
+    dv = V.shape[1]
+    S = np.zeros((dv, dk)) if S0 is None else np.array(S0, dtype=np.float64).reshape(dv, dk)
+    eye = np.eye(dk)
+    states = np.zeros((L, dv, dk))
+    out = None if Q is None else np.zeros((L, dv))
+    for t in range(L):
+        k = K[t]
+        if use_delta:
+            S = S @ (eye - beta[t] * np.outer(k, k))
+        S = S + beta[t] * np.outer(V[t], k)
+        states[t] = S
+        if Q is not None:
+            out[t] = S @ np.asarray(Q[t], dtype=np.float64)
+    return states, out

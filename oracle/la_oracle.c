@@ -177,6 +177,73 @@ int oracle_decode_step(const float *q, const float *k, const float *v,
     return 0;
 }
 
+/*
+ * oracle_delta_forward: the delta rule (DeltaNet), recurrent, fp64
+ * (linear_sparse_attention.py, "delta_rule_recurrent"). The state is d_v x d_k,
+ * the v k^T orientation of that function; per token, in the page's two steps:
+ *     S = S (I - beta_t k_t k_t^T)      erase what S returns for k_t
+ *     S = S + beta_t v_t k_t^T          write v_t in its place
+ *     out_t = S q_t                     read AFTER the update (the reading of
+ *                                       the other forms; the page returns states)
+ * k_t is taken as given (the page assumes unit-norm keys and leaves the
+ * normalisation to the caller).
+ *   q, k: [B,H,L,dk]; v: [B,H,L,dv]; beta: [B,H,L]
+ *   state_in: NULL (start from zero) or [B,H] blocks of dv*dk (row i = value
+ *             dimension i); out: [B,H,L,dv]; state_out: same blocks as state_in
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_delta_forward(const float *q, const float *k, const float *v,
+                         const float *beta, const double *state_in, int B, int H,
+                         int L, int dk, int dv, double *out, double *state_out,
+                         int nthreads)
+{
+    if (B < 0 || H < 0 || L < 0 || dk <= 0 || dv <= 0 || !beta) return -1;
+    const size_t blk = (size_t)dv * dk;
+    const long nbh = (long)B * H;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (long bh = 0; bh < nbh; ++bh) {
+        double *S = state_out + (size_t)bh * blk;
+        if (state_in) memcpy(S, state_in + (size_t)bh * blk, blk * sizeof(double));
+        else memset(S, 0, blk * sizeof(double));
+        double *kt = (double *)malloc(sizeof(double) * ((size_t)dk * 2 + dv));
+        double *qt = kt + dk;
+        double *Sk = qt + dk;
+        for (int t = 0; t < L; ++t) {
+            const size_t tk = ((size_t)bh * L + t) * dk, tv = ((size_t)bh * L + t) * dv;
+            const double b = (double)beta[(size_t)bh * L + t];
+            for (int j = 0; j < dk; ++j) {
+                kt[j] = (double)k[tk + j];
+                qt[j] = (double)q[tk + j];
+            }
+            /* S (I - b k k^T) = S - b (S k) k^T */
+            for (int i = 0; i < dv; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * kt[j];
+                Sk[i] = acc;
+            }
+            for (int i = 0; i < dv; ++i)
+                for (int j = 0; j < dk; ++j) S[(size_t)i * dk + j] -= b * Sk[i] * kt[j];
+            /* + b v k^T */
+            for (int i = 0; i < dv; ++i) {
+                const double vi = (double)v[tv + i];
+                for (int j = 0; j < dk; ++j) S[(size_t)i * dk + j] += b * vi * kt[j];
+            }
+            double *ot = out + tv;
+            for (int i = 0; i < dv; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * qt[j];
+                ot[i] = acc;
+            }
+        }
+        free(kt);
+    }
+    (void)nthreads;
+    return 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP
