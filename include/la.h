@@ -126,6 +126,31 @@ int la_chunk_fwd_from_state(const void *q, const void *k, const void *v, const v
                             la_stream_t stream);
 
 /*
+ * la_delta_fwd -- the delta rule (DeltaNet) over whole sequences, recurrent
+ * form, from S_0 = 0 (linear_sparse_attention.py, "delta_rule_recurrent"):
+ *
+ *   S <- S (I - beta_t k_t k_t^T) + beta_t v_t k_t^T ;  out_t = S q_t
+ *
+ * Each token first erases what S returns for its key, then writes its value
+ * there; the output is read after the update. S is d_v x d_k (the v k^T
+ * orientation of that function). Keys are used as given: the rule expects
+ * unit-norm keys and the caller normalises them (as that page does).
+ *
+ *   q, k   [B][H][L][d_k]     v, out [B][H][L][d_v]   (bf16, or fp32 with LA_DTYPE_F32)
+ *   beta   [B][H][L], the same type; usually in (0, 1]
+ *   final_state  NULL, or [B][H][d_v][d_k] fp32: S after the last token
+ *   mode   0 or LA_DTYPE_F32 (no feature map, normaliser or gate)
+ *   d_k, d_v in {16, 32, 64, 128}; B, H, L >= 0 (L = 0 writes a zero state)
+ *
+ * Every token depends on the previous state, so each sequence is processed
+ * one token after another (6 d_k d_v flops a token, on the CUDA cores in fp32).
+ * Errors as la_chunk_fwd; beta needs only element alignment.
+ */
+int la_delta_fwd(const void *q, const void *k, const void *v, const void *beta,
+                 void *out, float *final_state, int B, int H, int L, int dk,
+                 int dv, int mode, la_stream_t stream);
+
+/*
  * la_decode_step -- one recurrent step for every (b, h), in place on `state`
  * (learnllm m22 "Code: The Two Faces", the LinearAttentionState.step object;
  * insideout lesson 16: S <- S + k v^T, z <- z + k, out = q^T S / (q . z)):

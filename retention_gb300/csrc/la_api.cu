@@ -105,6 +105,33 @@ int la_decode_step(const void *q, const void *k, const void *v, const void *gate
     return rc;
 }
 
+int la_delta_fwd(const void *q, const void *k, const void *v, const void *beta, void *out,
+                 float *final_state, int B, int H, int L, int dk, int dv, int mode, la_stream_t stream) {
+    if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
+    if (mode & ~LA_DTYPE_F32) return LA_ERR_INVALID_ARG;
+    const long nbh = (long)B * H;
+    if (nbh > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
+    if (nbh == 0) return LA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (final_state && !aligned16(final_state)) return LA_ERR_MISALIGNED;
+    if (L == 0) {
+        // no token: the state stays S_0 = 0
+        if (final_state &&
+            cudaMemsetAsync(final_state, 0, (size_t)nbh * dk * dv * sizeof(float), s) != cudaSuccess)
+            return LA_ERR_CUDA;
+        return LA_OK;
+    }
+    if (!q || !k || !v || !beta || !out) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LA_ERR_MISALIGNED;
+    if ((uintptr_t)beta & ((mode & LA_DTYPE_F32) ? 3u : 1u)) return LA_ERR_MISALIGNED;
+    la::DeltaArgs a{q, k, v, beta, out, final_state, B, H, L, dk, dv, mode};
+    int launches = 0;
+    const int rc = la::launch_delta(a, s, &launches);
+    g_launches += (unsigned long long)launches;
+    return rc;
+}
+
 int la_chunk_fwd_path(int B, int H, int L, int dk, int dv, int mode, int chunk) {
     if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
     if (chunk < 1 || chunk > 128) return LA_ERR_INVALID_ARG;

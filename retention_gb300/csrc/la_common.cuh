@@ -51,9 +51,17 @@ struct DecodeArgs {
     int B, H, dk, dv, mode;
 };
 
+struct DeltaArgs {
+    const void *q, *k, *v, *beta;
+    void *out;
+    float *final_state;
+    int B, H, L, dk, dv, mode;
+};
+
 // Each returns LA_OK or an la_status; `launches` counts kernels launched.
 int launch_chunk_simt(const ChunkArgs &a, cudaStream_t s, int *launches);
 int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
+int launch_delta(const DeltaArgs &a, cudaStream_t s, int *launches);
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a);

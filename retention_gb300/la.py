@@ -32,6 +32,7 @@ SIGNATURES = {
     "la_decode_step": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_from_state": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
+    "la_delta_fwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_path": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "la_status_string": ([_I], ctypes.c_char_p),
     "la_kernel_launches": ([], ctypes.c_ulonglong),
@@ -166,6 +167,29 @@ def decode_step(q, k, v, state, gate=None, *, phi="elu1", normalize=False, gate_
     if rc != LA_OK:
         raise LAError("la_decode_step", rc)
     return out
+
+
+def delta_fwd(q, k, v, beta, *, out=None, final_state=None, want_state=True, stream=None):
+    """la_delta_fwd: the delta rule over q, k [B,H,L,dk], v [B,H,L,dv], beta
+    [B,H,L] (keys as given: normalise them first). Returns (out, final_state
+    [B,H,dv*dk] fp32, rows = value dimensions)."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, H, L, dv, dtype=q.dtype, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty(B, H, dv * dk, dtype=torch.float32, device=q.device)
+    if beta.dtype != q.dtype or not beta.is_contiguous():
+        raise ValueError("beta must be contiguous and of q's dtype")
+    mode = LA_DTYPE_F32 if q.dtype == torch.float32 else 0
+    if q.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("q, k, v must be bfloat16 or float32")
+    rc = load().la_delta_fwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(beta, "beta"),
+                             _dev(out, "out"), _dev(final_state, "final_state"),
+                             B, H, L, dk, dv, mode, _stream(stream))
+    if rc != LA_OK:
+        raise LAError("la_delta_fwd", rc)
+    return out, final_state
 
 
 def chunk_fwd_path(B, H, L, dk, dv, mode, chunk):

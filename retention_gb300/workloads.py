@@ -16,6 +16,9 @@ Workloads (shapes, feature map, normaliser, gate, chunk), as named:
                 gamma_h = 1 - 2^(-5 - h/4), C=64
 * ``gla``       B=1 H=8 L=131072 d=128 bf16, elu+1, no normaliser,
                 g = bf16(N(0,1)) [B,H,L,d], C=64
+* ``delta``     B=8 H=16 L=4096 d=128 bf16 for the delta rule: q, k rows
+                of unit length, v N(0,1)/sqrt(128), beta = sigmoid(N(0,1))
+                per token (``delta_inputs``)
 * ``decode``    256 sequences x H=32, d=128; fp32 S ~ N(0, var 0.01),
                 z ~ U(0,1); per step one bf16 token N(0,1)/sqrt(128) per
                 sequence; elu+1, normalised; 1000 steps
@@ -33,6 +36,8 @@ WORKLOADS = {
                       normalize=False, gate="head", chunk=64, scale=1.0 / math.sqrt(128)),
     "gla": dict(B=1, H=8, L=131072, dk=128, dv=128, dtype="bf16", phi="elu1",
                 normalize=False, gate="channel", chunk=64, scale=1.0 / math.sqrt(128)),
+    "delta": dict(B=8, H=16, L=4096, dk=128, dv=128, dtype="bf16", phi="identity",
+                  normalize=False, gate=None, chunk=1, scale=1.0 / math.sqrt(128)),
     "decode": dict(B=256, H=32, dk=128, dv=128, dtype="bf16", phi="elu1",
                    normalize=True, gate=None, steps=1000, scale=1.0 / math.sqrt(128),
                    state_std=0.1),
@@ -114,3 +119,19 @@ def decode_tokens(cfg, step, seed=0, batch=None):
     elif cfg["gate"] == "head":
         out["gate"] = retention_gammas(H, cfg.get("gamma_step", 0.25))
     return out
+
+
+def delta_inputs(cfg, seed=0):
+    """q, k, v and beta for the delta rule, on the CPU: q, k [B,H,L,dk] rows of
+    unit length (the page normalises its keys), v [B,H,L,dv] N(0,1) scaled,
+    beta [B,H,L] = sigmoid(N(0,1)); all in the workload dtype."""
+    B, H, L, dk, dv = cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"]
+    dt = TORCH_DTYPES[cfg["dtype"]]
+    gen = torch.Generator("cpu").manual_seed(seed)
+    q = torch.randn(B, H, L, dk, generator=gen)
+    k = torch.randn(B, H, L, dk, generator=gen)
+    v = torch.randn(B, H, L, dv, generator=gen) * cfg["scale"]
+    beta = torch.sigmoid(torch.randn(B, H, L, generator=gen))
+    q = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+    return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), beta=beta.to(dt))
