@@ -271,6 +271,33 @@ def bench_chunk(name, steps, warmup, world, pk):
     }
 
 
+def bench_delta(steps, warmup, world):
+    """The delta rule (la_delta_fwd) on its workload. Recurrent, so the bound is
+    the FP32 FMA pipe: 6 d_k d_v flops per (token, head) against SMs x 128
+    lanes x 2 flops x the 2070 MHz maximum SM clock."""
+    from retention_gb300 import la
+    cfg = W.workload("delta")
+    B, H, L, dk, dv = cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    q = torch.randn(B, H, L, dk, generator=g, device="cuda")
+    k = torch.randn(B, H, L, dk, generator=g, device="cuda")
+    v = (torch.randn(B, H, L, dv, generator=g, device="cuda") * cfg["scale"]).bfloat16()
+    beta = torch.sigmoid(torch.randn(B, H, L, generator=g, device="cuda")).bfloat16()
+    q = (q / q.norm(dim=-1, keepdim=True)).bfloat16()
+    k = (k / k.norm(dim=-1, keepdim=True)).bfloat16()
+    out = torch.empty_like(v)
+    st = torch.empty(B, H, dv * dk, device="cuda")
+    secs = max_over_ranks(time_calls(lambda: la.delta_fwd(q, k, v, beta, out=out, final_state=st),
+                                     steps, warmup, world), world)
+    t = secs / steps
+    flops = 6.0 * B * H * L * dk * dv
+    peak = torch.cuda.get_device_properties(0).multi_processor_count * 128 * 2 * 2.07e9 / 1e12
+    return {"tokens_per_s": world * B * L / t, "ms_per_step": t * 1e3, "tflops": flops / t / 1e12,
+            "roofline": {"bound": "alu", "peak": peak, "unit": "TFLOP/s", "frac": flops / t / 1e12 / peak,
+                         "peak_source": "SMs x 128 FP32 lanes x 2 x 2070 MHz"},
+            "workload": "delta rule, recurrent: B=8, H=16, L=4096, d=128 bf16, unit q/k, beta=sigmoid(N(0,1))"}
+
+
 def bench_e2e(cfg, steps, warmup, world):
     """The same call with the inputs in pinned host memory: every step copies
     q, k, v to the device, runs la_chunk_fwd, and copies the output and final
@@ -410,7 +437,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=1000)
-    ap.add_argument("--no-extra", action="store_true", help="skip the retention/gated lines")
+    ap.add_argument("--no-extra", action="store_true", help="skip the retention/gated/delta lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
@@ -446,6 +473,8 @@ def main():
                            "gbs": r["gbs"], "roofline_frac": r["roofline_frac"],
                            "launches_per_step": r["launches_per_step"]}
             torch.cuda.empty_cache()
+        extra["delta"] = bench_delta(max(3, args.steps // 4), 2, world)
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
