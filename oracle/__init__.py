@@ -9,6 +9,8 @@ Two parts:
 * ``forward`` / ``decode_step``: the definition, the recurrent form in fp64
   (``la_oracle.c``, called through ctypes, OpenMP over (batch, head)).
 * ``delta_forward``: the delta rule (DeltaNet), recurrent, fp64, same file.
+* ``group_norm_swish``: the RetNet output epilogue (GroupNorm per head, then
+  the swish output gate), fp64, same file.
 * ``forms``: independent numpy restatements (parallel masked matmul, brute
   force double sum, chunkwise) used to pin the definition, plus a numpy copy
   of the recurrence for tiny cases.
@@ -51,6 +53,8 @@ def _load():
         lib.oracle_delta_forward.argtypes = [f32p, f32p, f32p, f32p, f64p, i, i, i, i, i,
                                              f64p, f64p, i]
         lib.oracle_delta_forward.restype = i
+        lib.oracle_group_norm_swish.argtypes = [f64p, f32p, f32p, f32p, ctypes.c_double, i, i, i, i, f64p]
+        lib.oracle_group_norm_swish.restype = i
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i
         _lib = lib
@@ -145,3 +149,24 @@ def delta_forward(q, k, v, beta, state_in=None, nthreads=0):
     if rc != 0:
         raise ValueError("oracle_delta_forward rejected its arguments")
     return out, st
+
+
+def group_norm_swish(x, og, weight=None, bias=None, eps=1e-5):
+    """The RetNet output epilogue in fp64: each (b, h, t) row of x [B,H,L,dv]
+    normalised over its dv values (biased variance, eps inside the root),
+    scaled by weight[h] and shifted by bias[h] ([H,dv] or None), times
+    swish(og). Returns float64 [B,H,L,dv]."""
+    lib = _load()
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    og, weight, bias = _f32(og), _f32(weight), _f32(bias)
+    B, H, L, dv = x.shape
+    assert og.shape == x.shape
+    for a in (weight, bias):
+        assert a is None or a.size == H * dv
+    out = np.empty_like(x)
+    rc = lib.oracle_group_norm_swish(_ptr(x, ctypes.c_double), _ptr(og, ctypes.c_float),
+                                     _ptr(weight, ctypes.c_float), _ptr(bias, ctypes.c_float),
+                                     float(eps), B, H, L, dv, _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle_group_norm_swish rejected its arguments")
+    return out

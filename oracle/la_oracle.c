@@ -244,6 +244,56 @@ int oracle_delta_forward(const float *q, const float *k, const float *v,
     return 0;
 }
 
+/*
+ * oracle_group_norm_swish: the RetNet output epilogue, fp64 (learnllm m22,
+ * "Retention": retention keeps no normaliser; RetNet steadies its output with
+ * a GroupNorm and a swish gate instead). One group per head, so every
+ * (b, h, t) row of dv outputs is normalised on its own:
+ *     mean = sum_i x_i / dv,   var = sum_i (x_i - mean)^2 / dv   (biased)
+ *     y_i  = (x_i - mean) / sqrt(var + eps) * weight[h][i] + bias[h][i]
+ *     out_i = swish(og_i) * y_i,   swish(u) = u sigmoid(u) = u / (1 + e^-u)
+ * og is the output gate (the caller's projection of the layer input); the
+ * output projection that follows is the caller's too.
+ *   x, out: [B,H,L,dv] fp64 (out may be x); og: [B,H,L,dv];
+ *   weight, bias: [H][dv], or NULL for 1 and 0
+ * Returns 0, or -1 on a bad argument.
+ */
+static double or_swish(double u)
+{
+    /* u / (1 + e^-u), written so that neither tail overflows */
+    if (u >= 0.0) return u / (1.0 + exp(-u));
+    const double e = exp(u);
+    return u * e / (1.0 + e);
+}
+
+int oracle_group_norm_swish(const double *x, const float *og, const float *weight,
+                            const float *bias, double eps, int B, int H, int L, int dv,
+                            double *out)
+{
+    if (B < 0 || H < 0 || L < 0 || dv <= 0 || !(eps >= 0.0) || !x || !og || !out) return -1;
+    const long rows = (long)B * H * L;
+    for (long r = 0; r < rows; ++r) {
+        const int h = (int)((r / L) % H);
+        const double *xr = x + (size_t)r * dv;
+        const float *gr = og + (size_t)r * dv;
+        double *orow = out + (size_t)r * dv;
+        double mean = 0.0;
+        for (int i = 0; i < dv; ++i) mean += xr[i];
+        mean /= dv;
+        double var = 0.0;
+        for (int i = 0; i < dv; ++i) var += (xr[i] - mean) * (xr[i] - mean);
+        var /= dv;
+        const double rstd = 1.0 / sqrt(var + eps);
+        for (int i = 0; i < dv; ++i) {
+            double y = (xr[i] - mean) * rstd;
+            if (weight) y *= (double)weight[(size_t)h * dv + i];
+            if (bias) y += (double)bias[(size_t)h * dv + i];
+            orow[i] = or_swish((double)gr[i]) * y;
+        }
+    }
+    return 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP
