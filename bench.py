@@ -54,12 +54,15 @@ def peaks():
 def chunk_work(cfg):
     """Algorithmic bytes and flops of one la_chunk_fwd (per-(token, head)
     flops 2*C*dk + 2*C*dv + 2*dk*dv + 2*dk*dv; bytes: q, k, v (+g) read once,
-    out written once, final state written once)."""
+    out written once, final state written once; with the RetNet epilogue the
+    output gate is read once too)."""
     B, H, L, dk, dv, C = cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"], cfg["chunk"]
     esz = 2 if cfg["dtype"] == "bf16" else 4
     n = B * H * L
     flops = n * (2 * C * dk + 2 * C * dv + 4 * dk * dv)
     inb = n * (2 * dk + dv) * esz + (n * dk * esz if cfg["gate"] == "channel" else 0)
+    if "gn_eps" in cfg:
+        inb += n * dv * esz
     outb = n * dv * esz
     stb = B * H * (dk * dv + (dk if cfg["normalize"] else 0)) * 4
     return inb + outb + stb, flops
@@ -248,9 +251,21 @@ def bench_chunk(name, steps, warmup, world, pk):
     st = torch.empty(B, H, la.state_block(dk, dv, cfg["normalize"]), dtype=torch.float32,
                      device="cuda")
 
-    def step():
-        la.chunk_fwd(q, k, v, gate, phi=cfg["phi"], normalize=cfg["normalize"],
-                     gate_kind=cfg["gate"], chunk=cfg["chunk"], out=out, final_state=st)
+    if "gn_eps" in cfg:
+        # RetNet: the output epilogue swish(og) * GroupNorm_h(o) in the same call
+        g = torch.Generator(device="cuda").manual_seed(1)
+        og = torch.randn(B, H, L, dv, generator=g, device="cuda").to(q.dtype)
+        gw = 1.0 + 0.1 * torch.randn(H, dv, generator=g, device="cuda")
+        gb = 0.1 * torch.randn(H, dv, generator=g, device="cuda")
+
+        def step():
+            la.chunk_fwd_gn_swish(q, k, v, og, gate, gn_weight=gw, gn_bias=gb, gn_eps=cfg["gn_eps"],
+                                  phi=cfg["phi"], normalize=cfg["normalize"], gate_kind=cfg["gate"],
+                                  chunk=cfg["chunk"], out=out, final_state=st)
+    else:
+        def step():
+            la.chunk_fwd(q, k, v, gate, phi=cfg["phi"], normalize=cfg["normalize"],
+                         gate_kind=cfg["gate"], chunk=cfg["chunk"], out=out, final_state=st)
 
     n0 = la.kernel_launches()
     step()
@@ -437,7 +452,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=1000)
-    ap.add_argument("--no-extra", action="store_true", help="skip the retention/gated/delta lines")
+    ap.add_argument("--no-extra", action="store_true", help="skip the retention/retnet/gated/delta lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
@@ -466,7 +481,7 @@ def main():
     dec = bench_decode(args.decode_steps, world, pk)
     extra = {}
     if not args.no_extra:
-        for name in ("retention", "gla"):
+        for name in ("retention", "retnet", "gla"):
             r = bench_chunk(name, max(5, args.steps // 2), warmup, world, pk)
             del r["inputs"]
             extra[name] = {"tokens_per_s": r["tokens_per_s"], "ms_per_step": r["ms_per_step"],

@@ -151,6 +151,48 @@ int la_delta_fwd(const void *q, const void *k, const void *v, const void *beta,
                  int dv, int mode, la_stream_t stream);
 
 /*
+ * la_group_norm_swish -- the RetNet output epilogue (learnllm m22,
+ * "Retention": retention has no normaliser; RetNet steadies its output with a
+ * GroupNorm and a swish gate instead). One group per head: each (b, h, t) row
+ * of d_v values is normalised on its own,
+ *
+ *   y   = (x - mean) / sqrt(var + eps) * weight[h] + bias[h]   (var biased, over the d_v values)
+ *   out = swish(ogate) * y,   swish(u) = u sigmoid(u)
+ *
+ * ogate is the output gate, the caller's projection of the layer input (X W_G
+ * in RetNet); the output projection after it is the caller's too.
+ *
+ *   x, ogate, out  [B][H][L][d_v] (bf16, or fp32 with LA_DTYPE_F32); out may
+ *                  be x (in place), otherwise no overlap
+ *   weight, bias   NULL (1 and 0) or fp32 [H][d_v], 16-byte aligned
+ *   eps            >= 0 and finite (LA_ERR_INVALID_ARG otherwise)
+ *   mode           0 or LA_DTYPE_F32
+ * Decode outputs ([B][H][d_v]) are the case L = 1. Errors as la_chunk_fwd.
+ */
+int la_group_norm_swish(const void *x, const void *ogate, const float *gn_weight,
+                        const float *gn_bias, float gn_eps, void *out, int B, int H,
+                        int L, int dv, int mode, la_stream_t stream);
+
+/*
+ * la_chunk_fwd_gn_swish -- la_chunk_fwd_from_state followed by the RetNet
+ * output epilogue of la_group_norm_swish on its output: out is
+ * swish(ogate) * GroupNorm_h(o), o the attention output (after the division by
+ * the normaliser when LA_NORMALIZE is set). The epilogue is a second kernel on
+ * the same stream, in place on out.
+ *
+ *   ogate          [B][H][L][d_v], the type of q; required
+ *   gn_weight, gn_bias, gn_eps   as la_group_norm_swish
+ *   every other argument, the results and the errors as la_chunk_fwd_from_state
+ *   (initial_state may be NULL); the final state is that of the attention,
+ *   untouched by the epilogue.
+ */
+int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const void *gate,
+                          const float *initial_state, const void *ogate,
+                          const float *gn_weight, const float *gn_bias, float gn_eps,
+                          void *out, float *final_state, int B, int H, int L, int dk,
+                          int dv, int mode, int chunk, la_stream_t stream);
+
+/*
  * la_decode_step -- one recurrent step for every (b, h), in place on `state`
  * (learnllm m22 "Code: The Two Faces", the LinearAttentionState.step object;
  * insideout lesson 16: S <- S + k v^T, z <- z + k, out = q^T S / (q . z)):

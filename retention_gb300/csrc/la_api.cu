@@ -2,6 +2,7 @@
 // status strings. Every check runs before any launch; nothing is allocated
 // here.
 #include <atomic>
+#include <cmath>
 #include <mutex>
 #include <stdint.h>
 
@@ -26,9 +27,23 @@ int check_mode(int mode, const void *gate, bool decode) {
     return LA_OK;
 }
 
+// The output epilogue's own arguments (ogate null: no epilogue).
+struct Epilogue {
+    const void *ogate;
+    const float *weight, *bias;
+    float eps;
+};
+
+int check_epilogue(const Epilogue &ep) {
+    if (!(ep.eps >= 0.f) || std::isinf(ep.eps)) return LA_ERR_INVALID_ARG;
+    if (!aligned16(ep.ogate)) return LA_ERR_MISALIGNED;
+    if ((ep.weight && !aligned16(ep.weight)) || (ep.bias && !aligned16(ep.bias))) return LA_ERR_MISALIGNED;
+    return LA_OK;
+}
+
 int chunk_fwd(const void *q, const void *k, const void *v, const void *gate, const float *initial_state,
               void *out, float *final_state, int B, int H, int L, int dk, int dv, int mode, int chunk,
-              la_stream_t stream) {
+              la_stream_t stream, const Epilogue &ep = Epilogue{nullptr, nullptr, nullptr, 0.f}) {
     if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
     if (chunk < 1 || chunk > 128) return LA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
@@ -57,6 +72,7 @@ int chunk_fwd(const void *q, const void *k, const void *v, const void *gate, con
     if (final_state && !aligned16(final_state)) return LA_ERR_MISALIGNED;
     if ((mode & LA_GATE_CHANNEL) && !aligned16(gate)) return LA_ERR_MISALIGNED;
     if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
+    if (ep.ogate && (rc = check_epilogue(ep)) != LA_OK) return rc;
 
     la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode, chunk, initial_state};
     int launches = 0;
@@ -64,6 +80,11 @@ int chunk_fwd(const void *q, const void *k, const void *v, const void *gate, con
         rc = la::launch_chunk_tc(a, s, &launches);
     else
         rc = la::launch_chunk_simt(a, s, &launches);
+    if (rc == LA_OK && ep.ogate) {
+        // the output epilogue: a streaming pass of its own, in place on out
+        la::GnArgs g{out, ep.ogate, ep.weight, ep.bias, ep.eps, out, B, H, L, dv, mode & LA_DTYPE_F32};
+        rc = la::launch_gn_swish(g, s, &launches);
+    }
     g_launches += (unsigned long long)launches;
     return rc;
 }
@@ -82,6 +103,32 @@ int la_chunk_fwd_from_state(const void *q, const void *k, const void *v, const v
                             const float *initial_state, void *out, float *final_state, int B, int H,
                             int L, int dk, int dv, int mode, int chunk, la_stream_t stream) {
     return chunk_fwd(q, k, v, gate, initial_state, out, final_state, B, H, L, dk, dv, mode, chunk, stream);
+}
+
+int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const void *gate,
+                          const float *initial_state, const void *ogate, const float *gn_weight,
+                          const float *gn_bias, float gn_eps, void *out, float *final_state, int B, int H,
+                          int L, int dk, int dv, int mode, int chunk, la_stream_t stream) {
+    if (ogate == nullptr && L > 0 && (long)B * H > 0) return LA_ERR_INVALID_ARG;
+    return chunk_fwd(q, k, v, gate, initial_state, out, final_state, B, H, L, dk, dv, mode, chunk, stream,
+                     Epilogue{ogate, gn_weight, gn_bias, gn_eps});
+}
+
+int la_group_norm_swish(const void *x, const void *ogate, const float *gn_weight, const float *gn_bias,
+                        float gn_eps, void *out, int B, int H, int L, int dv, int mode, la_stream_t stream) {
+    if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(dv)) return LA_ERR_UNSUPPORTED;
+    if (mode & ~LA_DTYPE_F32) return LA_ERR_INVALID_ARG;
+    if ((long)B * H * L == 0) return LA_OK;
+    if (!x || !ogate || !out) return LA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out)) return LA_ERR_MISALIGNED;
+    int rc = check_epilogue(Epilogue{ogate, gn_weight, gn_bias, gn_eps});
+    if (rc != LA_OK) return rc;
+    la::GnArgs g{x, ogate, gn_weight, gn_bias, gn_eps, out, B, H, L, dv, mode};
+    int launches = 0;
+    rc = la::launch_gn_swish(g, reinterpret_cast<cudaStream_t>(stream), &launches);
+    g_launches += (unsigned long long)launches;
+    return rc;
 }
 
 int la_decode_step(const void *q, const void *k, const void *v, const void *gate, float *state,

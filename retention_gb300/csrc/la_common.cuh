@@ -44,6 +44,14 @@ struct ChunkArgs {
     const float *initial_state;  // [B][H][block] state before the first token, or null (zero)
 };
 
+struct GnArgs {
+    const void *x, *ogate;       // [B][H][L][dv]
+    const float *weight, *bias;  // [H][dv] or null
+    float eps;
+    void *out;                   // may be x
+    int B, H, L, dv, mode;
+};
+
 struct DecodeArgs {
     const void *q, *k, *v, *gate;
     float *state;
@@ -62,6 +70,7 @@ struct DeltaArgs {
 int launch_chunk_simt(const ChunkArgs &a, cudaStream_t s, int *launches);
 int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
 int launch_delta(const DeltaArgs &a, cudaStream_t s, int *launches);
+int launch_gn_swish(const GnArgs &a, cudaStream_t s, int *launches);
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a);

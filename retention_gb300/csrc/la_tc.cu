@@ -965,61 +965,6 @@ int tc_segments(int BH, int nchunks, int *seg_chunks) {
     return (nchunks + cs - 1) / cs;
 }
 
-int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches) {
-    if (!get_encode()) return LA_ERR_CUDA;
-    const int BH = a.B * a.H;
-    const int nchunks = (a.L + kC - 1) / kC;
-    TcParams prm;
-    memset(&prm, 0, sizeof(prm));
-    if (!make_map(&prm.tq, a.q, a.L, BH) || !make_map(&prm.tk, a.k, a.L, BH) ||
-        !make_map(&prm.tv, a.v, a.L, BH) || !make_map(&prm.to, a.out, a.L, BH))
-        return LA_ERR_CUDA;
-    if ((a.mode & LA_GATE_CHANNEL) && !make_map(&prm.tg, a.gate, a.L, BH)) return LA_ERR_CUDA;
-    prm.gamma = (a.mode & LA_GATE_HEAD) ? static_cast<const float *>(a.gate) : nullptr;
-    prm.final_state = a.final_state;
-    prm.H = a.H;
-    prm.L = a.L;
-    prm.mode = a.mode;
-    prm.nseg = tc_segments(BH, nchunks, &prm.seg_chunks);
-    prm.init0 = a.initial_state != nullptr;
-    if (prm.nseg == 1) {
-        prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
-        const int rc = launch_mode<false>(prm, BH, s, a.mode);
-        if (rc == LA_OK) *launches += 1;
-        return rc;
-    }
-    // split sequences: state-only pass, segment scan, full pass from the
-    // carried states; scratch is stream-ordered
-    const size_t blk = (size_t)kD * kD + ((a.mode & LA_NORMALIZE) ? kD : 0);
-    const size_t nsb = (size_t)BH * prm.nseg;
-    const size_t bytes = (2 * nsb * blk + nsb * kD) * sizeof(float);
-    void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
-    float *seg_state = static_cast<float *>(scratch);
-    float *state_in = seg_state + nsb * blk;
-    float *seg_logdecay = state_in + nsb * blk;
-    prm.seg_state = seg_state;
-    prm.seg_logdecay = seg_logdecay;
-    prm.final_state = nullptr;
-    int rc = launch_mode<true>(prm, (int)nsb, s, a.mode);
-    if (rc == LA_OK) {
-        *launches += 1;
-        la_seg_scan_kernel<<<dim3((unsigned)BH, (unsigned)((blk + 255) / 256)), 256, 0, s>>>(
-            seg_state, seg_logdecay, a.initial_state, state_in, a.final_state, prm.nseg, (int)blk);
-        rc = cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
-    }
-    if (rc == LA_OK) {
-        *launches += 1;
-        prm.state_in = state_in;
-        prm.seg_state = nullptr;
-        prm.seg_logdecay = nullptr;
-        rc = launch_mode<false>(prm, (int)nsb, s, a.mode);
-        if (rc == LA_OK) *launches += 1;
-    }
-    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
-    return rc;
-}
-
 // Scratch bytes the tensor-core path needs for these arguments (0 when the
 // sequences are not split).
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a) {
@@ -1033,8 +978,9 @@ size_t chunk_tc_scratch_bytes(const ChunkArgs &a) {
 }
 
 // The tensor-core path with caller-provided scratch (at least
-// chunk_tc_scratch_bytes(a) bytes, 256-byte aligned): the same three
-// launches as launch_chunk_tc, with no allocation and no free.
+// chunk_tc_scratch_bytes(a) bytes, 256-byte aligned). A sequence that is not
+// split is one launch; split sequences take three: the state-only pass, the
+// segment scan and the full pass from the carried states.
 int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch,
                          size_t scratch_bytes) {
     if (!get_encode()) return LA_ERR_CUDA;
@@ -1080,6 +1026,18 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.seg_logdecay = nullptr;
     rc = launch_mode<false>(prm, (int)nsb, s, a.mode);
     if (rc == LA_OK) *launches += 1;
+    return rc;
+}
+
+// The tensor-core path with its scratch (if any) allocated and freed in
+// stream order around the launches.
+int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches) {
+    const size_t bytes = chunk_tc_scratch_bytes(a);
+    if (bytes == 0) return launch_chunk_tc_into(a, s, launches, nullptr, 0);
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    int rc = launch_chunk_tc_into(a, s, launches, scratch, bytes);
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
     return rc;
 }
 

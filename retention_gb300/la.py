@@ -33,6 +33,9 @@ SIGNATURES = {
     "la_chunk_fwd_noalloc": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_from_state": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_delta_fwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP], _I),
+    "la_group_norm_swish": ([_VP, _VP, _VP, _VP, ctypes.c_float, _VP, _I, _I, _I, _I, _I, _VP], _I),
+    "la_chunk_fwd_gn_swish": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP, _VP,
+                               _I, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_path": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "la_status_string": ([_I], ctypes.c_char_p),
     "la_kernel_launches": ([], ctypes.c_ulonglong),
@@ -135,6 +138,65 @@ def chunk_fwd(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None
         if rc != LA_OK:
             raise LAError("la_chunk_fwd_from_state", rc)
     return out, final_state
+
+
+def _gn_params(weight, bias, H, dv):
+    for name, t in (("gn_weight", weight), ("gn_bias", bias)):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != H * dv):
+            raise ValueError("%s must be float32 with H*dv elements" % name)
+    return _dev(weight, "gn_weight"), _dev(bias, "gn_bias")
+
+
+def chunk_fwd_gn_swish(q, k, v, ogate, gate=None, *, gn_weight=None, gn_bias=None, gn_eps=1e-5,
+                       phi="elu1", normalize=False, gate_kind=None, chunk=64, out=None, final_state=None,
+                       want_state=True, simt=False, stream=None, initial_state=None):
+    """la_chunk_fwd_gn_swish: chunk_fwd whose output goes through the RetNet
+    epilogue swish(ogate) * GroupNorm_h(o) (ogate [B,H,L,dv], q's dtype;
+    gn_weight, gn_bias [H,dv] fp32 or None). Returns (out, final_state)."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty(B, H, L, dv, dtype=q.dtype, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty(B, H, state_block(dk, dv, normalize), dtype=torch.float32,
+                                  device=q.device)
+    if ogate.dtype != q.dtype or ogate.shape != out.shape:
+        raise ValueError("ogate must have out's shape and q's dtype")
+    if initial_state is not None and initial_state.dtype != torch.float32:
+        raise ValueError("initial_state must be float32")
+    w, b = _gn_params(gn_weight, gn_bias, H, dv)
+    mode = mode_bits(phi, normalize, gate_kind, q.dtype, simt)
+    rc = load().la_chunk_fwd_gn_swish(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
+                                      _dev(initial_state, "initial_state"), _dev(ogate, "ogate"), w, b,
+                                      float(gn_eps), _dev(out, "out"), _dev(final_state, "final_state"),
+                                      B, H, L, dk, dv, mode, chunk, _stream(stream))
+    if rc != LA_OK:
+        raise LAError("la_chunk_fwd_gn_swish", rc)
+    return out, final_state
+
+
+def group_norm_swish(x, ogate, *, gn_weight=None, gn_bias=None, gn_eps=1e-5, out=None, stream=None):
+    """la_group_norm_swish over x [B,H,L,dv] (or [B,H,dv], a decode output):
+    swish(ogate) * GroupNorm_h(x). ``out`` may be ``x``."""
+    shape = x.shape
+    if x.dim() == 3:
+        B, H, dv = shape
+        L = 1
+    else:
+        B, H, L, dv = shape
+    if out is None:
+        out = torch.empty_like(x)
+    if ogate.dtype != x.dtype or ogate.shape != shape or out.shape != shape or out.dtype != x.dtype:
+        raise ValueError("x, ogate and out must share shape and dtype")
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("x must be bfloat16 or float32")
+    w, b = _gn_params(gn_weight, gn_bias, H, dv)
+    mode = LA_DTYPE_F32 if x.dtype == torch.float32 else 0
+    rc = load().la_group_norm_swish(_dev(x, "x"), _dev(ogate, "ogate"), w, b, float(gn_eps), _dev(out, "out"),
+                                    B, H, L, dv, mode, _stream(stream))
+    if rc != LA_OK:
+        raise LAError("la_group_norm_swish", rc)
+    return out
 
 
 def chunk_fwd_noalloc(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None, chunk=64,

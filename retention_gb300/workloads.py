@@ -19,6 +19,10 @@ Workloads (shapes, feature map, normaliser, gate, chunk), as named:
 * ``delta``     B=8 H=16 L=4096 d=128 bf16 for the delta rule: q, k rows
                 of unit length, v N(0,1)/sqrt(128), beta = sigmoid(N(0,1))
                 per token (``delta_inputs``)
+* ``retnet``    the ``retention`` workload followed by the RetNet output
+                epilogue: output gate og = bf16(N(0,1)) [B,H,L,d], GroupNorm
+                weight N(1, 0.1^2) and bias N(0, 0.1^2) fp32 [H,d], eps 1e-5
+                (``epilogue_inputs``)
 * ``decode``    256 sequences x H=32, d=128; fp32 S ~ N(0, var 0.01),
                 z ~ U(0,1); per step one bf16 token N(0,1)/sqrt(128) per
                 sequence; elu+1, normalised; 1000 steps
@@ -36,6 +40,8 @@ WORKLOADS = {
                       normalize=False, gate="head", chunk=64, scale=1.0 / math.sqrt(128)),
     "gla": dict(B=1, H=8, L=131072, dk=128, dv=128, dtype="bf16", phi="elu1",
                 normalize=False, gate="channel", chunk=64, scale=1.0 / math.sqrt(128)),
+    "retnet": dict(B=8, H=16, L=4096, dk=128, dv=128, dtype="bf16", phi="identity",
+                   normalize=False, gate="head", chunk=64, scale=1.0 / math.sqrt(128), gn_eps=1e-5),
     "delta": dict(B=8, H=16, L=4096, dk=128, dv=128, dtype="bf16", phi="identity",
                   normalize=False, gate=None, chunk=1, scale=1.0 / math.sqrt(128)),
     "decode": dict(B=256, H=32, dk=128, dv=128, dtype="bf16", phi="elu1",
@@ -135,3 +141,16 @@ def delta_inputs(cfg, seed=0):
     q = q / q.norm(dim=-1, keepdim=True).clamp_min(1e-12)
     k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
     return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), beta=beta.to(dt))
+
+
+def epilogue_inputs(cfg, seed=0):
+    """The RetNet output epilogue's inputs, on the CPU, from a generator of
+    their own (seed offset by 7919 from the chunk inputs' seed): the output
+    gate og [B,H,L,dv] = N(0,1) in the workload dtype, then the GroupNorm
+    weight [H,dv] ~ N(1, 0.1^2) and bias [H,dv] ~ N(0, 0.1^2), float32."""
+    B, H, L, dv = cfg["B"], cfg["H"], cfg["L"], cfg["dv"]
+    gen = torch.Generator("cpu").manual_seed(seed + 7919)
+    og = torch.randn(B, H, L, dv, generator=gen).to(TORCH_DTYPES[cfg["dtype"]])
+    weight = 1.0 + 0.1 * torch.randn(H, dv, generator=gen)
+    bias = 0.1 * torch.randn(H, dv, generator=gen)
+    return dict(og=og, weight=weight, bias=bias)
