@@ -9,6 +9,9 @@ Two parts:
 * ``forward`` / ``decode_step``: the definition, the recurrent form in fp64
   (``la_oracle.c``, called through ctypes, OpenMP over (batch, head)).
 * ``delta_forward``: the delta rule (DeltaNet), recurrent, fp64, same file.
+* ``backward``: gradients of ``forward`` (from a zero state) with respect to
+  q, k, v and the per-channel gate, by the chain rule on the recurrence,
+  fp64, same file.
 * ``group_norm_swish``: the RetNet output epilogue (GroupNorm per head, then
   the swish output gate), fp64, same file.
 * ``forms``: independent numpy restatements (parallel masked matmul, brute
@@ -55,6 +58,9 @@ def _load():
         lib.oracle_delta_forward.restype = i
         lib.oracle_group_norm_swish.argtypes = [f64p, f32p, f32p, f32p, ctypes.c_double, i, i, i, i, f64p]
         lib.oracle_group_norm_swish.restype = i
+        lib.oracle_backward.argtypes = [f32p, f32p, f32p, f32p, f32p, i, i, i, i, i, i,
+                                        f64p, f64p, f64p, f64p, i]
+        lib.oracle_backward.restype = i
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i
         _lib = lib
@@ -170,3 +176,24 @@ def group_norm_swish(x, og, weight=None, bias=None, eps=1e-5):
     if rc != 0:
         raise ValueError("oracle_group_norm_swish rejected its arguments")
     return out
+
+
+def backward(q, k, v, dout, gate=None, mode=0, nthreads=0):
+    """Gradients of ``forward`` (from S_0 = 0) given dout [B,H,L,dv]: returns
+    (dq, dk [B,H,L,dk], dv [B,H,L,dv], dg [B,H,L,dk] or None), float64."""
+    lib = _load()
+    q, k, v, gate, dout = _f32(q), _f32(k), _f32(v), _f32(gate), _f32(dout)
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == q.shape and v.shape[:3] == q.shape[:3] and dout.shape == v.shape
+    dq = np.empty((B, H, L, dk), dtype=np.float64)
+    dkk = np.empty_like(dq)
+    dvv = np.empty((B, H, L, dv), dtype=np.float64)
+    dg = np.empty_like(dq) if mode & GATE_CHANNEL else None
+    rc = lib.oracle_backward(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float), _ptr(v, ctypes.c_float),
+                             _ptr(gate, ctypes.c_float), _ptr(dout, ctypes.c_float), B, H, L, dk, dv, mode,
+                             _ptr(dq, ctypes.c_double), _ptr(dkk, ctypes.c_double), _ptr(dvv, ctypes.c_double),
+                             _ptr(dg, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_backward rejected its arguments")
+    return dq, dkk, dvv, dg

@@ -294,6 +294,146 @@ int oracle_group_norm_swish(const double *x, const float *og, const float *weigh
     return 0;
 }
 
+/*
+ * oracle_backward: gradients of the forward pass (from S_0 = 0) with respect to
+ * q, k, v and the per-channel gate g, given the gradient dout of its output.
+ * The pages give no gradient; this is the chain rule applied to the recurrence
+ * above, in fp64, one (b, h) at a time:
+ *
+ *   forward sweep   S_t, z_t as in or_sequence; num_t = qf^T S_t, den_t = qf.z_t
+ *                   w_t = dout_t (unnormalised), or, with the normaliser,
+ *                   w_t = dout_t / den_t and e_t = -(dout_t . out_t) / den_t
+ *                   (out = num / den: d num = dout / den, d den = -dout.out/den)
+ *                   dQ_t = S_t w_t + z_t e_t              (gradient of qf_t)
+ *   reverse sweep   dS_t = diag(a_{t+1}) dS_{t+1} + qf_t w_t^T   (a_L taken as 0)
+ *                   dz_t = a_{t+1} * dz_{t+1} + qf_t e_t
+ *                   dK_t = dS_t v_t + dz_t                (gradient of kf_t)
+ *                   dv_t = dS_t^T kf_t
+ *   feature map     dq = dQ * phi'(q), dk = dK * phi'(k); elu+1: phi'(x) = 1
+ *                   for x > 0, e^x otherwise
+ *   channel gate    with B_t = sum_{r<=t} log a_r, every term of the output
+ *                   carries e^{B_t - B_s} (query t, key s), so
+ *                   dl/dB_t = qf_t * dQ_t - kf_t * dK_t, and log a_r enters
+ *                   every B_t with t >= r: dl/dlog a_r = sum_{t>=r} dl/dB_t.
+ *                   log a = logsigmoid(g) / 16 gives
+ *                   dg_r = (dl/dlog a_r) * sigmoid(-g_r) / 16.
+ *
+ *   q, k, g, dq, dk, dg: [B,H,L,dk]; v, dout, dv: [B,H,L,dv]; gate as in
+ *   oracle_forward; dg may be NULL (and is not written without the channel
+ *   gate). Outputs are doubles. Returns 0, or -1 on a bad argument.
+ */
+int oracle_backward(const float *q, const float *k, const float *v,
+                    const float *gate, const float *dout, int B, int H, int L,
+                    int dk, int dv, int mode, double *dq, double *dkk,
+                    double *dvv, double *dg, int nthreads)
+{
+    if (B < 0 || H < 0 || L < 0 || dk <= 0 || dv <= 0) return -1;
+    if ((mode & (OR_GATE_HEAD | OR_GATE_CHANNEL)) && !gate) return -1;
+    const int elu1 = (mode & OR_PHI_ELU1) != 0;
+    const int norm = (mode & OR_NORMALIZE) != 0;
+    const long nbh = (long)B * H;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (long bh = 0; bh < nbh; ++bh) {
+        const size_t ok = (size_t)bh * L * dk, ov = (size_t)bh * L * dv;
+        const float *qb = q + ok, *kb = k + ok, *vb = v + ov, *db = dout + ov;
+        const float *gb = (mode & OR_GATE_CHANNEL) ? gate + ok : NULL;
+        const double gamma = (mode & OR_GATE_HEAD) ? (double)gate[bh % H] : 1.0;
+        /* per token: qf, kf, a (dk each), w (dv), e (1); the states */
+        double *qf = (double *)malloc(sizeof(double) * ((size_t)L * (3 * (size_t)dk + dv + 1) +
+                                                        2 * ((size_t)dk * dv + dk)));
+        double *kf = qf + (size_t)L * dk, *a = kf + (size_t)L * dk, *w = a + (size_t)L * dk;
+        double *e = w + (size_t)L * dv, *S = e + L, *z = S + (size_t)dk * dv;
+        double *dS = z + dk, *dz = dS + (size_t)dk * dv;
+        double *dQ = dq + ok, *dK = dkk + ok, *dV = dvv + ov;
+        for (int t = 0; t < L; ++t)
+            for (int i = 0; i < dk; ++i) {
+                const size_t x = (size_t)t * dk + i;
+                qf[x] = or_phi((double)qb[x], elu1);
+                kf[x] = or_phi((double)kb[x], elu1);
+                a[x] = gb ? exp(or_log_sigmoid((double)gb[x]) / 16.0) : gamma;
+            }
+        /* forward sweep */
+        memset(S, 0, sizeof(double) * ((size_t)dk * dv + dk));
+        for (int t = 0; t < L; ++t) {
+            const double *qt = qf + (size_t)t * dk, *kt = kf + (size_t)t * dk, *at = a + (size_t)t * dk;
+            for (int i = 0; i < dk; ++i) {
+                for (int j = 0; j < dv; ++j)
+                    S[(size_t)i * dv + j] = at[i] * S[(size_t)i * dv + j] + kt[i] * (double)vb[(size_t)t * dv + j];
+                z[i] = at[i] * z[i] + kt[i];
+            }
+            double *wt = w + (size_t)t * dv;
+            const float *dt = db + (size_t)t * dv;
+            if (norm) {
+                double den = 0.0, dot = 0.0;
+                for (int i = 0; i < dk; ++i) den += qt[i] * z[i];
+                for (int j = 0; j < dv; ++j) {
+                    double num = 0.0;
+                    for (int i = 0; i < dk; ++i) num += qt[i] * S[(size_t)i * dv + j];
+                    dot += (double)dt[j] * (num / den);
+                    wt[j] = (double)dt[j] / den;
+                }
+                e[t] = -dot / den;
+            } else {
+                for (int j = 0; j < dv; ++j) wt[j] = (double)dt[j];
+                e[t] = 0.0;
+            }
+            for (int i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dv; ++j) acc += S[(size_t)i * dv + j] * wt[j];
+                dQ[(size_t)t * dk + i] = acc + z[i] * e[t];
+            }
+        }
+        /* reverse sweep */
+        memset(dS, 0, sizeof(double) * ((size_t)dk * dv + dk));
+        for (int t = L - 1; t >= 0; --t) {
+            const double *qt = qf + (size_t)t * dk, *kt = kf + (size_t)t * dk;
+            const double *an = t + 1 < L ? a + (size_t)(t + 1) * dk : NULL;
+            const double *wt = w + (size_t)t * dv;
+            for (int i = 0; i < dk; ++i) {
+                const double ai = an ? an[i] : 0.0;
+                for (int j = 0; j < dv; ++j)
+                    dS[(size_t)i * dv + j] = ai * dS[(size_t)i * dv + j] + qt[i] * wt[j];
+                dz[i] = ai * dz[i] + qt[i] * e[t];
+            }
+            for (int i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < dv; ++j) acc += dS[(size_t)i * dv + j] * (double)vb[(size_t)t * dv + j];
+                dK[(size_t)t * dk + i] = acc + (norm ? dz[i] : 0.0);
+            }
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i) acc += dS[(size_t)i * dv + j] * kt[i];
+                dV[(size_t)t * dv + j] = acc;
+            }
+        }
+        /* channel gate: reverse running sum of qf dQ - kf dK */
+        if (gb && dg) {
+            for (int i = 0; i < dk; ++i) {
+                double c = 0.0;
+                for (int t = L - 1; t >= 0; --t) {
+                    const size_t x = (size_t)t * dk + i;
+                    c += qf[x] * dQ[x] - kf[x] * dK[x];
+                    const double gx = (double)gb[x];
+                    /* sigmoid(-g), split so that neither branch overflows */
+                    const double sm = gx >= 0.0 ? exp(-gx) / (1.0 + exp(-gx)) : 1.0 / (1.0 + exp(gx));
+                    dg[ok + x] = c * sm / 16.0;
+                }
+            }
+        }
+        /* through the feature map */
+        for (size_t x = 0; x < (size_t)L * dk; ++x) {
+            if (elu1 && (double)qb[x] <= 0.0) dQ[x] *= exp((double)qb[x]);
+            if (elu1 && (double)kb[x] <= 0.0) dK[x] *= exp((double)kb[x]);
+        }
+        free(qf);
+    }
+    (void)nthreads;
+    return 0;
+}
+
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP
