@@ -193,6 +193,38 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
                           int dv, int mode, int chunk, la_stream_t stream);
 
 /*
+ * la_chunk_bwd -- the backward pass of la_chunk_fwd (from S_0 = 0): given the
+ * gradient dout of the output, the gradients of q, k, v and of the per-channel
+ * gate g. The pages give no gradient (learnllm m22 "The Three Faces of
+ * Retention" motivates the chunkwise form for training); this is the chain
+ * rule on the recurrence:
+ *
+ *   forward sweep   dQ_t = S_t w_t + z_t e_t
+ *   reverse sweep   dS_t = diag(A_{t+1}) dS_{t+1} + phi(q_t) w_t^T  (dz_t with e_t)
+ *                   dK_t = dS_t v_t + dz_t,   dv_t = dS_t^T phi(k_t)
+ *   dq = dQ * phi'(q),  dk = dK * phi'(k)
+ *   dg_r = sigmoid(-g_r) / 16 * sum_{t >= r} (phi(q_t) dQ_t - phi(k_t) dK_t)
+ *
+ * with w_t = dout_t, e_t = 0 without the normaliser, and w_t = dout_t / den_t,
+ * e_t = -(dout_t . out_t) / den_t with it (formed inside from S_t w_t, so the
+ * forward's output is not needed).
+ *
+ *   q, k, v, gate, B, H, L, dk, dv, mode   as given to la_chunk_fwd (the chunk
+ *          size does not enter the gradient; LA_KERNEL_SIMT is ignored)
+ *   dout   [B][H][L][d_v]; dq, dk [B][H][L][d_k] and dv [B][H][L][d_v] are
+ *          written, in the type of q
+ *   dgate  with LA_GATE_CHANNEL: NULL (not computed) or [B][H][L][d_k] in the
+ *          type of q; ignored otherwise (no gradient is formed for gamma)
+ * No gradient flows into a final state or out of an initial one. Scratch: two
+ * fp32 [B][H][L][d_k] arrays (and two [B][H][L] ones with LA_NORMALIZE), taken
+ * stream-ordered with cudaMallocAsync on `stream` (LA_ERR_CUDA if that fails).
+ * Errors as la_chunk_fwd; no output may overlap an input.
+ */
+int la_chunk_bwd(const void *q, const void *k, const void *v, const void *gate,
+                 const void *dout, void *dq, void *dk, void *dv, void *dgate, int B,
+                 int H, int L, int dk_, int dv_, int mode, la_stream_t stream);
+
+/*
  * la_decode_step -- one recurrent step for every (b, h), in place on `state`
  * (learnllm m22 "Code: The Two Faces", the LinearAttentionState.step object;
  * insideout lesson 16: S <- S + k v^T, z <- z + k, out = q^T S / (q . z)):

@@ -131,6 +131,30 @@ int la_group_norm_swish(const void *x, const void *ogate, const float *gn_weight
     return rc;
 }
 
+int la_chunk_bwd(const void *q, const void *k, const void *v, const void *gate, const void *dout, void *dq,
+                 void *dk_, void *dv_, void *dgate, int B, int H, int L, int dk, int dv, int mode,
+                 la_stream_t stream) {
+    if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
+    int rc = check_mode(mode, gate, false);
+    if (rc != LA_OK) return rc;
+    const long nbh = (long)B * H;
+    if (nbh > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
+    if (nbh == 0 || L == 0) return LA_OK;
+    if (!q || !k || !v || !dout || !dq || !dk_ || !dv_) return LA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, dout, dq, dk_, dv_};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr)) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_CHANNEL) && (!aligned16(gate) || (dgate && !aligned16(dgate)))) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
+    la::BwdArgs a{q, k, v, gate, dout, dq, dk_, dv_,
+                  (mode & LA_GATE_CHANNEL) ? dgate : nullptr, B, H, L, dk, dv, mode & ~LA_KERNEL_SIMT};
+    int launches = 0;
+    rc = la::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream), &launches);
+    g_launches += (unsigned long long)launches;
+    return rc;
+}
+
 int la_decode_step(const void *q, const void *k, const void *v, const void *gate, float *state,
                    void *out, int B, int H, int dk, int dv, int mode, la_stream_t stream) {
     if (B < 0 || H < 0) return LA_ERR_INVALID_ARG;

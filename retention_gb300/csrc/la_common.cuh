@@ -52,6 +52,12 @@ struct GnArgs {
     int B, H, L, dv, mode;
 };
 
+struct BwdArgs {
+    const void *q, *k, *v, *gate, *dout;
+    void *grad_q, *grad_k, *grad_v, *grad_g;    // grad_g: [B][H][L][dk] with the channel gate, or null
+    int B, H, L, dk, dv, mode;
+};
+
 struct DecodeArgs {
     const void *q, *k, *v, *gate;
     float *state;
@@ -71,6 +77,8 @@ int launch_chunk_simt(const ChunkArgs &a, cudaStream_t s, int *launches);
 int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
 int launch_delta(const DeltaArgs &a, cudaStream_t s, int *launches);
 int launch_gn_swish(const GnArgs &a, cudaStream_t s, int *launches);
+int launch_bwd(const BwdArgs &a, cudaStream_t s, int *launches);
+size_t bwd_scratch_bytes(const BwdArgs &a);
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a);

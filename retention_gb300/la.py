@@ -36,6 +36,7 @@ SIGNATURES = {
     "la_group_norm_swish": ([_VP, _VP, _VP, _VP, ctypes.c_float, _VP, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_gn_swish": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP, _VP,
                                _I, _I, _I, _I, _I, _I, _I, _VP], _I),
+    "la_chunk_bwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP], _I),
     "la_chunk_fwd_path": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "la_status_string": ([_I], ctypes.c_char_p),
     "la_kernel_launches": ([], ctypes.c_ulonglong),
@@ -197,6 +198,27 @@ def group_norm_swish(x, ogate, *, gn_weight=None, gn_bias=None, gn_eps=1e-5, out
     if rc != LA_OK:
         raise LAError("la_group_norm_swish", rc)
     return out
+
+
+def chunk_bwd(q, k, v, dout, gate=None, *, phi="elu1", normalize=False, gate_kind=None,
+              dq=None, dk=None, dv=None, dgate=None, want_dgate=True, stream=None):
+    """la_chunk_bwd: gradients of chunk_fwd (from a zero state) given dout.
+    Returns (dq, dk, dv, dgate); dgate is None unless gate_kind == "channel"."""
+    B, H, L, d_k = q.shape
+    d_v = v.shape[-1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if gate_kind == "channel" and want_dgate and dgate is None:
+        dgate = torch.empty_like(q)
+    if gate_kind != "channel":
+        dgate = None
+    mode = mode_bits(phi, normalize, gate_kind, q.dtype)
+    rc = load().la_chunk_bwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"), _dev(dout, "dout"), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"),
+                             _dev(dgate, "dgate"), B, H, L, d_k, d_v, mode, _stream(stream))
+    if rc != LA_OK:
+        raise LAError("la_chunk_bwd", rc)
+    return dq, dk, dv, dgate
 
 
 def chunk_fwd_noalloc(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None, chunk=64,

@@ -154,3 +154,12 @@ def epilogue_inputs(cfg, seed=0):
     weight = 1.0 + 0.1 * torch.randn(H, dv, generator=gen)
     bias = 0.1 * torch.randn(H, dv, generator=gen)
     return dict(og=og, weight=weight, bias=bias)
+
+
+def bwd_inputs(cfg, seed=0):
+    """The output gradient for a backward workload, on the CPU, from a
+    generator of its own (seed offset by 104729): dout [B,H,L,dv] = N(0,1) in
+    the workload dtype."""
+    B, H, L, dv = cfg["B"], cfg["H"], cfg["L"], cfg["dv"]
+    gen = torch.Generator("cpu").manual_seed(seed + 104729)
+    return torch.randn(B, H, L, dv, generator=gen).to(TORCH_DTYPES[cfg["dtype"]])
