@@ -210,14 +210,22 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
  * forward's output is not needed).
  *
  *   q, k, v, gate, B, H, L, dk, dv, mode   as given to la_chunk_fwd (the chunk
- *          size does not enter the gradient; LA_KERNEL_SIMT is ignored)
+ *          size does not enter the gradient)
+ *
+ * Two routes: bf16 with d_k = d_v = 128, no normaliser and no per-channel gate
+ * (retention, RetNet) runs on the tensor-core forward kernel, since each
+ * gradient is then a causal linear-attention forward with its roles permuted,
+ * two of them in reversed token order; every other case (and LA_KERNEL_SIMT)
+ * runs three sweeps over the sequence on the CUDA cores.
  *   dout   [B][H][L][d_v]; dq, dk [B][H][L][d_k] and dv [B][H][L][d_v] are
  *          written, in the type of q
  *   dgate  with LA_GATE_CHANNEL: NULL (not computed) or [B][H][L][d_k] in the
  *          type of q; ignored otherwise (no gradient is formed for gamma)
- * No gradient flows into a final state or out of an initial one. Scratch: two
- * fp32 [B][H][L][d_k] arrays (and two [B][H][L] ones with LA_NORMALIZE), taken
- * stream-ordered with cudaMallocAsync on `stream` (LA_ERR_CUDA if that fails).
+ * No gradient flows into a final state or out of an initial one. Scratch,
+ * taken stream-ordered with cudaMallocAsync on `stream` (LA_ERR_CUDA if that
+ * fails): six (eight with LA_PHI_ELU1) bf16 [B][H][L][128] arrays on the
+ * tensor-core route; one fp32 [B][H][L][d_k] array (two, plus three [B][H][L],
+ * with LA_NORMALIZE) on the other.
  * Errors as la_chunk_fwd; no output may overlap an input.
  */
 int la_chunk_bwd(const void *q, const void *k, const void *v, const void *gate,

@@ -150,7 +150,9 @@ int la_chunk_bwd(const void *q, const void *k, const void *v, const void *gate, 
     la::BwdArgs a{q, k, v, gate, dout, dq, dk_, dv_,
                   (mode & LA_GATE_CHANNEL) ? dgate : nullptr, B, H, L, dk, dv, mode & ~LA_KERNEL_SIMT};
     int launches = 0;
-    rc = la::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream), &launches);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    rc = (!(mode & LA_KERNEL_SIMT) && la::bwd_tc_supports(a)) ? la::launch_bwd_tc(a, s, &launches)
+                                                               : la::launch_bwd(a, s, &launches);
     g_launches += (unsigned long long)launches;
     return rc;
 }

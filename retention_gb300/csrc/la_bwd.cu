@@ -4,13 +4,13 @@
 // The pages motivate the chunkwise form "for training" (learnllm m22, "The
 // Three Faces of Retention") but give no gradient; this is the chain rule on
 // the recurrence S_t = diag(a_t) S_{t-1} + K_t v_t^T, out_t = S_t^T Q_t
-// (Q = phi(q), K = phi(k); with the normaliser, out = num / den and the
-// value is widened by a column of ones whose state is z):
+// (Q = phi(q), K = phi(k); with the normaliser, out = num / den and the value
+// is widened by a column of ones whose state is z):
 //
-//   w_t  = dout_t                      e_t = 0                      (no normaliser)
+//   w_t  = dout_t                      e_t = 0                    (no normaliser)
 //   w_t  = dout_t / den_t              e_t = -(dout_t . out_t) / den_t
-//                                          = -(Q_t . S_t w_t) / den_t
-//   dQ_t = S_t w_t + z_t e_t                                    forward sweep
+//                                          = -(Q_t . S_t dout_t) / den_t^2
+//   dQ_t = S_t w_t + z_t e_t                                   forward sweep
 //   dS_t = diag(a_{t+1}) dS_{t+1} + Q_t w_t^T,  dz_t likewise with e_t   reverse
 //   dK_t = dS_t v_t + dz_t,   dv_t = dS_t^T K_t
 //   dq = dQ * phi'(q),  dk = dK * phi'(k)
@@ -18,224 +18,319 @@
 //
 // (the last line: every term of the output carries e^{B_t - B_s} with
 // B_t = sum_{r<=t} log a_r, so dl/dB_t = Q_t dQ_t - K_t dK_t, and log a_r
-// enters every B_t with t >= r).
+// enters every B_t with t >= r). e_t is formed from S_t dout_t, the dQ
+// sweep's own product, not from the forward's stored output, whose rounding
+// the difference S_t w_t + z_t e_t would magnify.
 //
-// e_t is formed from S_t w_t (the dQ sweep's own product) rather than from the
-// forward's stored output, whose rounding the difference S_t w_t + z_t e_t
-// would magnify.
+// Three sweeps, each carrying one matrix in registers through the sequence
+// with one rank-1 update and one matrix-vector product per token, laid out so
+// that every reduction stays inside a thread's row group:
+//   dQ sweep  rows = key channels (16 per CTA), columns = value channels,
+//             forward; with the normaliser it also carries z and adds each
+//             CTA's share of den_t atomically
+//   (normaliser only: e_t, 1/den_t and the finished dQ_t, one warp per token)
+//   dK sweep  rows = key channels, columns = value channels, reverse; it
+//             finishes dq, dk (phi') and the gate gradient (the running sum
+//             runs backwards with it)
+//   dV sweep  rows = value channels, columns = key channels (dS transposed),
+//             reverse
+// Each sweep stages blocks of kTB tokens in shared memory; the next block's
+// 16-byte loads are in flight in registers while a block is processed.
 //
-// Kernels, in stream order: the normaliser's den_t (only with it); three
-// sweeps that each carry one matrix in registers through the sequence, one
-// rank-1 update and one matrix-vector product per token, so that every
-// reduction stays inside a thread's row group:
-//   dQ sweep  rows = key channels (16 per CTA), columns = value channels, forward
-//   (e_t, one warp per token, with the normaliser)
-//   dK sweep  rows = key channels, columns = value channels, reverse
-//   dV sweep  rows = value channels, columns = key channels (dS transposed), reverse
-// and a last pass that adds z_t e_t, applies phi' and forms the gate gradient.
+// With a scalar gate and no normaliser (retention, RetNet) in bf16 at head
+// dim 128, the gradients go through the tensor-core forward kernel instead
+// (launch_bwd_tc below).
 #include "la_common.cuh"
 
 namespace la {
 namespace {
 
-constexpr int kTB = 16;        // tokens per staged block
-constexpr int kRows = 16;      // matrix rows per CTA
-constexpr int kFinThreads = 128;
+constexpr int kTB = 16;    // tokens per staged block
+constexpr int kRows = 16;  // matrix rows per CTA
 
 struct BwdParams {
     const void *q, *k, *v, *gate, *dout;
     void *grad_q, *grad_k, *grad_v, *grad_g;
-    float *gq, *gk;            // [BH][L][dk] fp32: gradients with respect to Q = phi(q), K = phi(k)
-    float *den_inv, *ecol;     // [BH][L]: 1 / den_t and e_t (normaliser only)
+    float *gq;                     // [BH][L][dk]: dQ (pre phi'); S_t dout_t before the normaliser's finish
+    float *zb;                     // [BH][L][dk]: z_t (normaliser)
+    float *den, *dinv, *ecol;      // [BH][L] (normaliser)
     int B, H, L, dk, dv, mode;
 };
 
 __device__ __forceinline__ float dphi(float x, bool elu1) { return (elu1 && x <= 0.f) ? __expf(x) : 1.f; }
+__device__ __forceinline__ float chan_gate(float g) { return __expf(channel_log_decay(g)); }
 
-// gate value of key channel d at token t of sequence bh (1 without a gate)
-template <typename T>
-__device__ __forceinline__ float gate_value(const BwdParams &p, int bh, int t, int d) {
-    if (p.mode & LA_GATE_CHANNEL)
-        return __expf(channel_log_decay(to_f32(static_cast<const T *>(p.gate)[((size_t)bh * p.L + t) * p.dk + d])));
-    if (p.mode & LA_GATE_HEAD) return static_cast<const float *>(p.gate)[bh % p.H];
-    return 1.f;
-}
-
-// ---------------------------------------------------------------- normaliser
-// den_t = Q_t . z_t with z_t = a_t * z_{t-1} + K_t. One CTA per sequence, one
-// thread per key channel; tokens in blocks of kTB, the per-channel products
-// reduced per token through shared memory.
-template <typename T>
-__global__ void __launch_bounds__(128) bwd_den_kernel(BwdParams p) {
-    __shared__ float prod[kTB][129];
-    const int bh = blockIdx.x, i = threadIdx.x, dk = p.dk, L = p.L;
-    const bool elu1 = p.mode & LA_PHI_ELU1;
-    const T *q = static_cast<const T *>(p.q) + (size_t)bh * L * dk;
-    const T *k = static_cast<const T *>(p.k) + (size_t)bh * L * dk;
-    float z = 0.f;
-    for (int t0 = 0; t0 < L; t0 += kTB) {
-        const int nt = min(kTB, L - t0);
-        if (i < dk)
-            for (int tt = 0; tt < nt; ++tt) {
-                const int t = t0 + tt;
-                z = gate_value<T>(p, bh, t, i) * z + phi(to_f32(k[(size_t)t * dk + i]), elu1);
-                prod[tt][i] = phi(to_f32(q[(size_t)t * dk + i]), elu1) * z;
+// A staged stream: per token, NE consecutive elements of a [BH][L][ld] array
+// starting at column col0, from token t + off, moved as 16-byte chunks; the
+// threads of the CTA take chunks tid, tid + NT, ...
+template <typename E, int NE, int NT>
+struct Stream {
+    static constexpr int EPC = 16 / (int)sizeof(E);
+    static constexpr int CPT = NE / EPC;            // chunks per token
+    static constexpr int N = kTB * CPT;             // chunks per block
+    static constexpr int R = (N + NT - 1) / NT;     // chunks per thread
+    uint4 r[R];
+    __device__ __forceinline__ void fetch(const E *base, int ld, int col0, int t0, int off, int L, int tid) {
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int ci = tid + i * NT;
+            r[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (ci < N) {
+                const int t = t0 + ci / CPT + off;
+                if (t < L) r[i] = __ldcs(reinterpret_cast<const uint4 *>(base + (size_t)t * ld + col0) + ci % CPT);
             }
-        __syncthreads();
-        // warp w reduces tokens w, w + 4, ...
-        const int warp = i >> 5, lane = i & 31;
-        for (int tt = warp; tt < nt; tt += 4) {
-            float den = 0.f;
-            for (int c = lane; c < dk; c += 32) den += prod[tt][c];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-            if (lane == 0) p.den_inv[(size_t)bh * L + t0 + tt] = 1.f / den;
         }
-        __syncthreads();
     }
-}
-
-// e_t = -(Q_t . gq_t) / den_t, gq_t = S_t w_t from the dQ sweep: one warp per
-// token.
-template <typename T>
-__global__ void __launch_bounds__(256) bwd_ecol_kernel(BwdParams p) {
-    const long w = ((long)blockIdx.x * 256 + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31, dk = p.dk;
-    if (w >= (long)p.B * p.H * p.L) return;
-    const bool elu1 = p.mode & LA_PHI_ELU1;
-    const T *q = static_cast<const T *>(p.q) + (size_t)w * dk;
-    const float *gq = p.gq + (size_t)w * dk;
-    float s = 0.f;
-    for (int c = lane; c < dk; c += 32) s += phi(to_f32(q[c]), elu1) * gq[c];
+    // element e of token tt goes to dst[tt * ldd + pos(e)], as f(value, in range)
+    template <typename Pos, typename F>
+    __device__ __forceinline__ void stash(float *dst, int ldd, Pos pos, F f, int t0, int off, int L, int tid) const {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) p.ecol[w] = -s * p.den_inv[w];
-}
+        for (int i = 0; i < R; ++i) {
+            const int ci = tid + i * NT;
+            if (ci < N) {
+                const int tt = ci / CPT, e0 = (ci % CPT) * EPC;
+                const bool in = t0 + tt + off < L;
+                const E *el = reinterpret_cast<const E *>(&r[i]);
+#pragma unroll
+                for (int x = 0; x < EPC; ++x) dst[tt * ldd + pos(e0 + x)] = f(to_f32(el[x]), in);
+            }
+        }
+    }
+};
 
-// ---------------------------------------------------------------- sweeps
-enum { kSweepDQ = 0, kSweepDK = 1, kSweepDV = 2 };
-
-// C columns per row (dv for the dQ and dK sweeps, dk for the dV sweep). A
-// compute thread holds rows 2 rg, 2 rg + 1 of the CTA's 16 and columns
-// 16 cg .. 16 cg + 15; the C / 16 threads of a row group are consecutive lanes.
-template <int SW, int C>
+template <int C>
 struct SweepCfg {
-    static constexpr int NCG = C / 16;
-    static constexpr int NTC = (kRows / 2) * NCG;
+    static constexpr int NCG = C / 16;              // column groups (lanes of a row group)
+    static constexpr int NRG = kRows / 2;           // row groups (two rows each)
+    static constexpr int NTC = NRG * NCG;           // compute threads
     static constexpr int NT = NTC < 64 ? 64 : NTC;
-    static constexpr int SEG = 20;                 // padded 16-column segment
-    static constexpr int ROWP = NCG * SEG;
+    static constexpr int ROWP = NCG * 20;           // padded row: 16-column segments of 20
     static constexpr unsigned MASK = NTC >= 32 ? 0xffffffffu : ((1u << NTC) - 1u);
 };
 
-template <int SW, int C, typename T>
-__global__ void __launch_bounds__(SweepCfg<SW, C>::NT) bwd_sweep_kernel(BwdParams p) {
-    using G = SweepCfg<SW, C>;
-    constexpr bool REV = SW != kSweepDQ;
-    __shared__ float xs[kTB][kRows];        // row-side factor of the rank-1 update
-    __shared__ float dr[kTB][kRows];        // per-row decay (dQ, dK sweeps)
-    __shared__ __align__(16) float ys[kTB][G::ROWP];   // column-side factor
-    __shared__ __align__(16) float us[kTB][G::ROWP];   // contracted vector
-    __shared__ __align__(16) float dc[kTB][SW == kSweepDV ? G::ROWP : 4];  // per-column decay (dV sweep)
-    __shared__ float es[kTB];
-    __shared__ float os[kTB][kRows];
+// positions in a staged row: padded 16-column segments, or plain
+struct ColPos {
+    __device__ __forceinline__ int operator()(int c) const { return (c >> 4) * 20 + (c & 15); }
+};
+struct RowPos {
+    __device__ __forceinline__ int operator()(int r) const { return r; }
+};
+struct Raw {
+    __device__ __forceinline__ float operator()(float x, bool) const { return x; }
+};
+struct Phi {
+    bool elu1;
+    __device__ __forceinline__ float operator()(float x, bool) const { return phi(x, elu1); }
+};
+struct Gate {  // a = exp(logsigmoid(g) / 16); 1 beyond the sequence
+    __device__ __forceinline__ float operator()(float x, bool in) const { return in ? chan_gate(x) : 1.f; }
+};
+
+// the 16 columns of column group cg of a padded staged row
+__device__ __forceinline__ void load16(const float *row, int cg, float (&x)[16]) {
+    const float *p = row + cg * 20;
+#pragma unroll
+    for (int j = 0; j < 16; j += 4) {
+        const float4 v4 = *reinterpret_cast<const float4 *>(p + j);
+        x[j] = v4.x, x[j + 1] = v4.y, x[j + 2] = v4.z, x[j + 3] = v4.w;
+    }
+}
+
+// ---------------------------------------------------------------- dQ sweep
+template <int C, typename T>
+__global__ void __launch_bounds__(SweepCfg<C>::NT) bwd_dq_kernel(BwdParams p) {
+    using G = SweepCfg<C>;
+    constexpr int NT = G::NT;
+    __shared__ float xk[kTB][kRows], xq[kTB][kRows], ar[kTB][kRows], os[kTB][kRows], oz[kTB][kRows];
+    __shared__ float pden[kTB][G::NRG];
+    __shared__ __align__(16) float ys[kTB][G::ROWP], us[kTB][G::ROWP];
     const int tid = threadIdx.x, rg = tid / G::NCG, cg = tid % G::NCG;
-    const bool compute = tid < G::NTC;
-    const int bh = blockIdx.x, row0 = blockIdx.y * kRows;
-    const int L = p.L, dk = p.dk, dv = p.dv;
-    const bool elu1 = p.mode & LA_PHI_ELU1, norm = p.mode & LA_NORMALIZE;
-    const bool gchan = p.mode & LA_GATE_CHANNEL, ghead = p.mode & LA_GATE_HEAD;
-    const float gamma = ghead ? static_cast<const float *>(p.gate)[bh % p.H] : 1.f;
-    const T *q = static_cast<const T *>(p.q) + (size_t)bh * L * dk;
-    const T *k = static_cast<const T *>(p.k) + (size_t)bh * L * dk;
-    const T *v = static_cast<const T *>(p.v) + (size_t)bh * L * dv;
-    const T *d = static_cast<const T *>(p.dout) + (size_t)bh * L * dv;
-    const float *dinv = norm ? p.den_inv + (size_t)bh * L : nullptr;
-    const float *ec = norm ? p.ecol + (size_t)bh * L : nullptr;
-    auto colp = [](int c) { return (c >> 4) * G::SEG + (c & 15); };
+    const int bh = blockIdx.x, row0 = blockIdx.y * kRows, L = p.L, dk = p.dk, dv = p.dv;
+    const bool elu1 = p.mode & LA_PHI_ELU1, norm = p.mode & LA_NORMALIZE, gchan = p.mode & LA_GATE_CHANNEL;
+    const float gamma = (p.mode & LA_GATE_HEAD) ? static_cast<const float *>(p.gate)[bh % p.H] : 1.f;
+    const T *k = static_cast<const T *>(p.k) + (size_t)bh * L * dk, *q = static_cast<const T *>(p.q) + (size_t)bh * L * dk;
+    const T *g = gchan ? static_cast<const T *>(p.gate) + (size_t)bh * L * dk : nullptr;
+    const T *v = static_cast<const T *>(p.v) + (size_t)bh * L * dv, *d = static_cast<const T *>(p.dout) + (size_t)bh * L * dv;
+    Stream<T, kRows, NT> sk, sq, sg;
+    Stream<T, C, NT> sv, sd;
+    auto fetch = [&](int t0) {
+        sk.fetch(k, dk, row0, t0, 0, L, tid);
+        if (norm) sq.fetch(q, dk, row0, t0, 0, L, tid);
+        if (gchan) sg.fetch(g, dk, row0, t0, 0, L, tid);
+        sv.fetch(v, dv, 0, t0, 0, L, tid);
+        sd.fetch(d, dv, 0, t0, 0, L, tid);
+    };
 
     float M[2][16], zr[2] = {0.f, 0.f};
 #pragma unroll
     for (int r = 0; r < 2; ++r)
 #pragma unroll
         for (int j = 0; j < 16; ++j) M[r][j] = 0.f;
-
-    const int nblk = (L + kTB - 1) / kTB;
-    for (int bi = 0; bi < nblk; ++bi) {
-        const int blk = REV ? nblk - 1 - bi : bi, t0 = blk * kTB, nt = min(kTB, L - t0);
-        __syncthreads();  // the previous block's shared rows are consumed
-        // stage the block: decays of token t (dQ sweep) or t + 1 (reverse sweeps)
-        for (int x = tid; x < nt * kRows; x += G::NT) {
-            const int tt = x / kRows, r = x % kRows, t = t0 + tt, row = row0 + r;
-            float xv;
-            if (SW == kSweepDQ) xv = phi(to_f32(k[(size_t)t * dk + row]), elu1);
-            else if (SW == kSweepDK) xv = phi(to_f32(q[(size_t)t * dk + row]), elu1);
-            else xv = to_f32(d[(size_t)t * dv + row]) * (norm ? dinv[t] : 1.f);
-            xs[tt][r] = xv;
-            if (SW != kSweepDV && gchan) {
-                const int tg = SW == kSweepDQ ? t : t + 1;
-                dr[tt][r] = tg < L ? gate_value<T>(p, bh, tg, row) : 1.f;
-            }
-        }
-        for (int x = tid; x < nt * C; x += G::NT) {
-            const int tt = x / C, c = x % C, t = t0 + tt;
-            float yv, uv;
-            if (SW == kSweepDQ) {
-                yv = to_f32(v[(size_t)t * dv + c]);
-                uv = to_f32(d[(size_t)t * dv + c]) * (norm ? dinv[t] : 1.f);
-            } else if (SW == kSweepDK) {
-                yv = to_f32(d[(size_t)t * dv + c]) * (norm ? dinv[t] : 1.f);
-                uv = to_f32(v[(size_t)t * dv + c]);
-            } else {
-                yv = phi(to_f32(q[(size_t)t * dk + c]), elu1);
-                uv = phi(to_f32(k[(size_t)t * dk + c]), elu1);
-                if (gchan) dc[tt][colp(c)] = t + 1 < L ? gate_value<T>(p, bh, t + 1, c) : 1.f;
-            }
-            ys[tt][colp(c)] = yv;
-            us[tt][colp(c)] = uv;
-        }
-        if (norm && SW == kSweepDK)
-            for (int x = tid; x < nt; x += G::NT) es[x] = ec[t0 + x];
+    fetch(0);
+    for (int t0 = 0; t0 < L; t0 += kTB) {
+        const int nt = min(kTB, L - t0);
+        sk.stash(&xk[0][0], kRows, RowPos(), Phi{elu1}, t0, 0, L, tid);
+        if (norm) sq.stash(&xq[0][0], kRows, RowPos(), Phi{elu1}, t0, 0, L, tid);
+        if (gchan) sg.stash(&ar[0][0], kRows, RowPos(), Gate(), t0, 0, L, tid);
+        sv.stash(&ys[0][0], G::ROWP, ColPos(), Raw(), t0, 0, L, tid);
+        sd.stash(&us[0][0], G::ROWP, ColPos(), Raw(), t0, 0, L, tid);
         __syncthreads();
-        if (compute) {
-            for (int s = 0; s < nt; ++s) {
-                const int tt = REV ? nt - 1 - s : s;
-                float yy[16], uu[16], dd[16];
-                const float *yp = &ys[tt][cg * G::SEG], *up = &us[tt][cg * G::SEG];
-#pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    const float4 y4 = *reinterpret_cast<const float4 *>(yp + j);
-                    const float4 u4 = *reinterpret_cast<const float4 *>(up + j);
-                    yy[j] = y4.x, yy[j + 1] = y4.y, yy[j + 2] = y4.z, yy[j + 3] = y4.w;
-                    uu[j] = u4.x, uu[j + 1] = u4.y, uu[j + 2] = u4.z, uu[j + 3] = u4.w;
-                }
-                // decay of this step: per row (dQ, dK sweeps) or per column (dV sweep)
-                float drow[2] = {gamma, gamma};
-                if (SW != kSweepDV) {
-                    if (gchan) drow[0] = dr[tt][2 * rg], drow[1] = dr[tt][2 * rg + 1];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) dd[j] = gamma;
-                    if (gchan) {
-                        const float *dp = &dc[tt][cg * G::SEG];
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 d4 = *reinterpret_cast<const float4 *>(dp + j);
-                            dd[j] = d4.x, dd[j + 1] = d4.y, dd[j + 2] = d4.z, dd[j + 3] = d4.w;
-                        }
-                    }
-                }
+        if (t0 + kTB < L) fetch(t0 + kTB);  // in flight while this block runs
+        if (tid < G::NTC) {
+            for (int tt = 0; tt < nt; ++tt) {
+                float yy[16], uu[16];
+                load16(ys[tt], cg, yy);
+                load16(us[tt], cg, uu);
+                float a[2] = {gamma, gamma};
+                if (gchan) a[0] = ar[tt][2 * rg], a[1] = ar[tt][2 * rg + 1];
                 float acc[2];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float xr = xs[tt][2 * rg + r];
+                    const float xr = xk[tt][2 * rg + r];
                     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                     for (int j = 0; j < 16; j += 2) {
-                        const float d0 = SW == kSweepDV ? dd[j] : drow[r];
-                        const float d1 = SW == kSweepDV ? dd[j + 1] : drow[r];
-                        M[r][j] = fmaf(xr, yy[j], d0 * M[r][j]);
-                        M[r][j + 1] = fmaf(xr, yy[j + 1], d1 * M[r][j + 1]);
+                        M[r][j] = fmaf(xr, yy[j], a[r] * M[r][j]);
+                        M[r][j + 1] = fmaf(xr, yy[j + 1], a[r] * M[r][j + 1]);
+                        a0 = fmaf(M[r][j], uu[j], a0);
+                        a1 = fmaf(M[r][j + 1], uu[j + 1], a1);
+                    }
+                    acc[r] = a0 + a1;
+                }
+#pragma unroll
+                for (int off = 1; off < G::NCG; off <<= 1)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) acc[r] += __shfl_xor_sync(G::MASK, acc[r], off);
+                if (cg == 0) {
+                    float pd = 0.f;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        os[tt][2 * rg + r] = acc[r];
+                        if (norm) {
+                            zr[r] = fmaf(a[r], zr[r], xk[tt][2 * rg + r]);
+                            oz[tt][2 * rg + r] = zr[r];
+                            pd = fmaf(xq[tt][2 * rg + r], zr[r], pd);
+                        }
+                    }
+                    if (norm) pden[tt][rg] = pd;
+                }
+            }
+        }
+        __syncthreads();
+        for (int x = tid; x < nt * kRows; x += NT) {
+            const int tt = x / kRows, r = x % kRows;
+            const size_t o = ((size_t)bh * L + t0 + tt) * dk + row0 + r;
+            p.gq[o] = os[tt][r];
+            if (norm) p.zb[o] = oz[tt][r];
+        }
+        if (norm)
+            for (int tt = tid; tt < nt; tt += NT) {
+                float s = 0.f;
+#pragma unroll
+                for (int x = 0; x < G::NRG; ++x) s += pden[tt][x];
+                atomicAdd(p.den + (size_t)bh * L + t0 + tt, s);
+            }
+        __syncthreads();  // the staged rows are free for the next block
+    }
+}
+
+// ---------------------------------------------------------------- normaliser
+// Per token (one warp): den_t complete, e_t = -(Q_t . S_t dout_t) / den_t^2,
+// dQ_t = S_t dout_t / den_t + z_t e_t.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_norm_kernel(BwdParams p) {
+    const long w = ((long)blockIdx.x * 256 + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31, dk = p.dk;
+    if (w >= (long)p.B * p.H * p.L) return;
+    const bool elu1 = p.mode & LA_PHI_ELU1;
+    const T *q = static_cast<const T *>(p.q) + (size_t)w * dk;
+    float *gq = p.gq + (size_t)w * dk;
+    const float *z = p.zb + (size_t)w * dk;
+    float s = 0.f;
+    for (int c = lane; c < dk; c += 32) s += phi(to_f32(q[c]), elu1) * gq[c];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    const float di = 1.f / p.den[w], e = -s * di * di;
+    for (int c = lane; c < dk; c += 32) gq[c] = fmaf(gq[c], di, z[c] * e);
+    if (lane == 0) {
+        p.dinv[w] = di;
+        p.ecol[w] = e;
+    }
+}
+
+// ---------------------------------------------------------------- dK sweep
+template <int C, typename T>
+__global__ void __launch_bounds__(SweepCfg<C>::NT) bwd_dk_kernel(BwdParams p) {
+    using G = SweepCfg<C>;
+    constexpr int NT = G::NT;
+    __shared__ float xq[kTB][kRows], xk[kTB][kRows], xg[kTB][kRows], an[kTB][kRows], gr[kTB][kRows];
+    __shared__ float odq[kTB][kRows], odk[kTB][kRows], odg[kTB][kRows];
+    __shared__ float dis[kTB], es[kTB];
+    __shared__ __align__(16) float ys[kTB][G::ROWP], us[kTB][G::ROWP];
+    const int tid = threadIdx.x, rg = tid / G::NCG, cg = tid % G::NCG;
+    const int bh = blockIdx.x, row0 = blockIdx.y * kRows, L = p.L, dk = p.dk, dv = p.dv;
+    const bool elu1 = p.mode & LA_PHI_ELU1, norm = p.mode & LA_NORMALIZE, gchan = p.mode & LA_GATE_CHANNEL;
+    const bool want_dg = gchan && p.grad_g != nullptr;
+    const float gamma = (p.mode & LA_GATE_HEAD) ? static_cast<const float *>(p.gate)[bh % p.H] : 1.f;
+    const T *q = static_cast<const T *>(p.q) + (size_t)bh * L * dk, *k = static_cast<const T *>(p.k) + (size_t)bh * L * dk;
+    const T *g = gchan ? static_cast<const T *>(p.gate) + (size_t)bh * L * dk : nullptr;
+    const T *v = static_cast<const T *>(p.v) + (size_t)bh * L * dv, *d = static_cast<const T *>(p.dout) + (size_t)bh * L * dv;
+    const float *gqb = p.gq + (size_t)bh * L * dk;
+    Stream<T, kRows, NT> sq, sk, sgn, sgc;
+    Stream<float, kRows, NT> sdq;
+    Stream<T, C, NT> sd, sv;
+    float pdi = 1.f, pe = 0.f;
+    auto fetch = [&](int t0) {
+        sq.fetch(q, dk, row0, t0, 0, L, tid);
+        sk.fetch(k, dk, row0, t0, 0, L, tid);
+        sdq.fetch(gqb, dk, row0, t0, 0, L, tid);
+        if (gchan) sgn.fetch(g, dk, row0, t0, 1, L, tid);
+        if (want_dg) sgc.fetch(g, dk, row0, t0, 0, L, tid);
+        sd.fetch(d, dv, 0, t0, 0, L, tid);
+        sv.fetch(v, dv, 0, t0, 0, L, tid);
+        if (norm && tid < kTB && t0 + tid < L) {
+            pdi = p.dinv[(size_t)bh * L + t0 + tid];
+            pe = p.ecol[(size_t)bh * L + t0 + tid];
+        }
+    };
+
+    float M[2][16], dz[2] = {0.f, 0.f}, cs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) M[r][j] = 0.f;
+    const int nblk = (L + kTB - 1) / kTB;
+    fetch((nblk - 1) * kTB);
+    for (int bi = nblk - 1; bi >= 0; --bi) {
+        const int t0 = bi * kTB, nt = min(kTB, L - t0);
+        sq.stash(&xq[0][0], kRows, RowPos(), Raw(), t0, 0, L, tid);
+        sk.stash(&xk[0][0], kRows, RowPos(), Raw(), t0, 0, L, tid);
+        sdq.stash(&xg[0][0], kRows, RowPos(), Raw(), t0, 0, L, tid);
+        if (gchan) sgn.stash(&an[0][0], kRows, RowPos(), Gate(), t0, 1, L, tid);
+        if (want_dg) sgc.stash(&gr[0][0], kRows, RowPos(), Raw(), t0, 0, L, tid);
+        sd.stash(&ys[0][0], G::ROWP, ColPos(), Raw(), t0, 0, L, tid);
+        sv.stash(&us[0][0], G::ROWP, ColPos(), Raw(), t0, 0, L, tid);
+        if (tid < kTB) dis[tid] = pdi, es[tid] = pe;
+        __syncthreads();
+        if (bi > 0) fetch(t0 - kTB);  // in flight while this block runs
+        if (tid < G::NTC) {
+            for (int tt = nt - 1; tt >= 0; --tt) {
+                float yy[16], uu[16];
+                load16(ys[tt], cg, yy);
+                load16(us[tt], cg, uu);
+                float a[2] = {gamma, gamma};
+                if (gchan) a[0] = an[tt][2 * rg], a[1] = an[tt][2 * rg + 1];
+                const float di = norm ? dis[tt] : 1.f;
+                float Qf[2], acc[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    Qf[r] = phi(xq[tt][2 * rg + r], elu1);
+                    const float xr = Qf[r] * di;  // Q_t w_t^T with w_t = dout_t / den_t
+                    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        M[r][j] = fmaf(xr, yy[j], a[r] * M[r][j]);
+                        M[r][j + 1] = fmaf(xr, yy[j + 1], a[r] * M[r][j + 1]);
                         a0 = fmaf(M[r][j], uu[j], a0);
                         a1 = fmaf(M[r][j + 1], uu[j + 1], a1);
                     }
@@ -248,137 +343,295 @@ __global__ void __launch_bounds__(SweepCfg<SW, C>::NT) bwd_sweep_kernel(BwdParam
                 if (cg == 0) {
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        float o = acc[r];
-                        if (norm && SW == kSweepDK) {
-                            // dz_t = a_{t+1} dz_{t+1} + Q_t e_t; dK_t += dz_t
-                            zr[r] = fmaf(drow[r], zr[r], xs[tt][2 * rg + r] * es[tt]);
-                            o += zr[r];
+                        const int rr = 2 * rg + r;
+                        float dK = acc[r];
+                        if (norm) {
+                            dz[r] = fmaf(a[r], dz[r], Qf[r] * es[tt]);
+                            dK += dz[r];
                         }
-                        os[tt][2 * rg + r] = o;
+                        const float kx = xk[tt][rr], qx = xq[tt][rr], dQ = xg[tt][rr];
+                        odk[tt][rr] = dK * dphi(kx, elu1);
+                        odq[tt][rr] = dQ * dphi(qx, elu1);
+                        if (want_dg) {
+                            cs[r] += Qf[r] * dQ - phi(kx, elu1) * dK;
+                            // times sigmoid(-g) / 16, with e^g capped so that it stays finite
+                            odg[tt][rr] = cs[r] * 0.0625f / (1.f + __expf(fminf(gr[tt][rr], 80.f)));
+                        }
                     }
                 }
             }
         }
         __syncthreads();
-        // the block's outputs, one row of 16 values per token
-        for (int x = tid; x < nt * kRows; x += G::NT) {
-            const int tt = x / kRows, r = x % kRows, t = t0 + tt;
-            if (SW == kSweepDQ) p.gq[((size_t)bh * L + t) * dk + row0 + r] = os[tt][r];
-            else if (SW == kSweepDK) p.gk[((size_t)bh * L + t) * dk + row0 + r] = os[tt][r];
-            else static_cast<T *>(p.grad_v)[((size_t)bh * L + t) * dv + row0 + r] = from_f32<T>(os[tt][r]);
+        T *dq = static_cast<T *>(p.grad_q), *dkk = static_cast<T *>(p.grad_k), *dg = static_cast<T *>(p.grad_g);
+        for (int x = tid; x < nt * kRows; x += NT) {
+            const int tt = x / kRows, r = x % kRows;
+            const size_t o = ((size_t)bh * L + t0 + tt) * dk + row0 + r;
+            dq[o] = from_f32<T>(odq[tt][r]);
+            dkk[o] = from_f32<T>(odk[tt][r]);
+            if (want_dg) dg[o] = from_f32<T>(odg[tt][r]);
         }
+        __syncthreads();  // the staged rows are free for the next block
     }
 }
 
-// ---------------------------------------------------------------- finish
-// dQ = gq + z e (normaliser), dq = dQ phi'(q), dk = dK phi'(k), and with the
-// per-channel gate the running sum for dg. Without either, an elementwise
-// pass; otherwise one thread per (sequence, key channel) walks the tokens:
-// forwards for z (normaliser), backwards for the running sum (channel gate).
-template <typename T>
-__global__ void __launch_bounds__(kFinThreads) bwd_finish_kernel(BwdParams p) {
-    const int dk = p.dk, L = p.L;
+// ---------------------------------------------------------------- dV sweep
+template <int C, typename T>
+__global__ void __launch_bounds__(SweepCfg<C>::NT) bwd_dv_kernel(BwdParams p) {
+    using G = SweepCfg<C>;
+    constexpr int NT = G::NT;
+    __shared__ float xd[kTB][kRows], os[kTB][kRows], dis[kTB];
+    __shared__ __align__(16) float ys[kTB][G::ROWP], us[kTB][G::ROWP], dc[kTB][G::ROWP];
+    const int tid = threadIdx.x, rg = tid / G::NCG, cg = tid % G::NCG;
+    const int bh = blockIdx.x, row0 = blockIdx.y * kRows, L = p.L, dk = p.dk, dv = p.dv;
     const bool elu1 = p.mode & LA_PHI_ELU1, norm = p.mode & LA_NORMALIZE, gchan = p.mode & LA_GATE_CHANNEL;
-    const T *q = static_cast<const T *>(p.q), *k = static_cast<const T *>(p.k);
-    T *dq = static_cast<T *>(p.grad_q), *dkk = static_cast<T *>(p.grad_k);
-    if (!norm && !gchan) {
-        const size_t n = (size_t)p.B * p.H * L * dk;
-        for (size_t x = (size_t)blockIdx.x * kFinThreads + threadIdx.x; x < n; x += (size_t)gridDim.x * kFinThreads) {
-            dq[x] = from_f32<T>(p.gq[x] * dphi(to_f32(q[x]), elu1));
-            dkk[x] = from_f32<T>(p.gk[x] * dphi(to_f32(k[x]), elu1));
-        }
-        return;
-    }
-    const long lane = (long)blockIdx.x * kFinThreads + threadIdx.x;
-    if (lane >= (long)p.B * p.H * dk) return;
-    const int bh = (int)(lane / dk), i = (int)(lane % dk);
-    const size_t base = (size_t)bh * L * dk + i;
-    if (norm) {
-        float z = 0.f;
-#pragma unroll 4
-        for (int t = 0; t < L; ++t) {
-            const size_t x = base + (size_t)t * dk;
-            z = gate_value<T>(p, bh, t, i) * z + phi(to_f32(k[x]), elu1);
-            const float gq = fmaf(z, p.ecol[(size_t)bh * L + t], p.gq[x]);
-            if (gchan) {
-                p.gq[x] = gq;  // the running sum below reads the completed dQ
-            } else {
-                dq[x] = from_f32<T>(gq * dphi(to_f32(q[x]), elu1));
-                dkk[x] = from_f32<T>(p.gk[x] * dphi(to_f32(k[x]), elu1));
+    const float gamma = (p.mode & LA_GATE_HEAD) ? static_cast<const float *>(p.gate)[bh % p.H] : 1.f;
+    const T *q = static_cast<const T *>(p.q) + (size_t)bh * L * dk, *k = static_cast<const T *>(p.k) + (size_t)bh * L * dk;
+    const T *g = gchan ? static_cast<const T *>(p.gate) + (size_t)bh * L * dk : nullptr;
+    const T *d = static_cast<const T *>(p.dout) + (size_t)bh * L * dv;
+    Stream<T, kRows, NT> sd;
+    Stream<T, C, NT> sq, sk, sg;
+    float pdi = 1.f;
+    auto fetch = [&](int t0) {
+        sd.fetch(d, dv, row0, t0, 0, L, tid);
+        sq.fetch(q, dk, 0, t0, 0, L, tid);
+        sk.fetch(k, dk, 0, t0, 0, L, tid);
+        if (gchan) sg.fetch(g, dk, 0, t0, 1, L, tid);
+        if (norm && tid < kTB && t0 + tid < L) pdi = p.dinv[(size_t)bh * L + t0 + tid];
+    };
+
+    float M[2][16];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) M[r][j] = 0.f;
+    const int nblk = (L + kTB - 1) / kTB;
+    fetch((nblk - 1) * kTB);
+    for (int bi = nblk - 1; bi >= 0; --bi) {
+        const int t0 = bi * kTB, nt = min(kTB, L - t0);
+        sd.stash(&xd[0][0], kRows, RowPos(), Raw(), t0, 0, L, tid);
+        sq.stash(&ys[0][0], G::ROWP, ColPos(), Phi{elu1}, t0, 0, L, tid);
+        sk.stash(&us[0][0], G::ROWP, ColPos(), Phi{elu1}, t0, 0, L, tid);
+        if (gchan) sg.stash(&dc[0][0], G::ROWP, ColPos(), Gate(), t0, 1, L, tid);
+        if (tid < kTB) dis[tid] = pdi;
+        __syncthreads();
+        if (bi > 0) fetch(t0 - kTB);
+        if (tid < G::NTC) {
+            for (int tt = nt - 1; tt >= 0; --tt) {
+                float yy[16], uu[16], aa[16];
+                load16(ys[tt], cg, yy);
+                load16(us[tt], cg, uu);
+                if (gchan) {
+                    load16(dc[tt], cg, aa);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) aa[j] = gamma;
+                }
+                const float di = norm ? dis[tt] : 1.f;
+                float acc[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float xr = xd[tt][2 * rg + r] * di;
+                    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        M[r][j] = fmaf(xr, yy[j], aa[j] * M[r][j]);
+                        M[r][j + 1] = fmaf(xr, yy[j + 1], aa[j + 1] * M[r][j + 1]);
+                        a0 = fmaf(M[r][j], uu[j], a0);
+                        a1 = fmaf(M[r][j + 1], uu[j + 1], a1);
+                    }
+                    acc[r] = a0 + a1;
+                }
+#pragma unroll
+                for (int off = 1; off < G::NCG; off <<= 1)
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) acc[r] += __shfl_xor_sync(G::MASK, acc[r], off);
+                if (cg == 0) os[tt][2 * rg] = acc[0], os[tt][2 * rg + 1] = acc[1];
             }
         }
-        if (!gchan) return;
-    }
-    const T *g = static_cast<const T *>(p.gate);
-    T *dg = static_cast<T *>(p.grad_g);
-    float c = 0.f;
-#pragma unroll 4
-    for (int t = L - 1; t >= 0; --t) {
-        const size_t x = base + (size_t)t * dk;
-        const float qx = to_f32(q[x]), kx = to_f32(k[x]), gq = p.gq[x], gk = p.gk[x];
-        dq[x] = from_f32<T>(gq * dphi(qx, elu1));
-        dkk[x] = from_f32<T>(gk * dphi(kx, elu1));
-        c += phi(qx, elu1) * gq - phi(kx, elu1) * gk;
-        if (dg) {
-            const float gx = to_f32(g[x]);
-            const float sm = 1.f / (1.f + __expf(fminf(gx, 80.f)));  // sigmoid(-g)
-            dg[x] = from_f32<T>(c * sm * 0.0625f);
+        __syncthreads();
+        T *dvo = static_cast<T *>(p.grad_v);
+        for (int x = tid; x < nt * kRows; x += NT) {
+            const int tt = x / kRows, r = x % kRows;
+            dvo[((size_t)bh * L + t0 + tt) * dv + row0 + r] = from_f32<T>(os[tt][r]);
         }
+        __syncthreads();  // the staged rows are free for the next block
     }
 }
 
-template <int SW, typename T>
-cudaError_t launch_sweep(const BwdParams &p, cudaStream_t s) {
-    const int cols = SW == kSweepDV ? p.dk : p.dv, rows = SW == kSweepDV ? p.dv : p.dk;
-    const dim3 grid((unsigned)(p.B * p.H), (unsigned)(rows / kRows));
-#define LA_BWD_SWEEP(CC) \
-    if (cols == CC) { bwd_sweep_kernel<SW, CC, T><<<grid, SweepCfg<SW, CC>::NT, 0, s>>>(p); return cudaGetLastError(); }
-    LA_BWD_SWEEP(16)
-    LA_BWD_SWEEP(32)
-    LA_BWD_SWEEP(64)
-    LA_BWD_SWEEP(128)
-#undef LA_BWD_SWEEP
-    return cudaErrorInvalidValue;
-}
+#define LA_BWD_DISPATCH(NAME)                                                                   \
+    template <typename T>                                                                       \
+    cudaError_t launch_##NAME(const BwdParams &p, int cols, int rows, cudaStream_t s) {         \
+        const dim3 grid((unsigned)(p.B * p.H), (unsigned)(rows / kRows));                       \
+        switch (cols) {                                                                         \
+            case 16: bwd_##NAME##_kernel<16, T><<<grid, SweepCfg<16>::NT, 0, s>>>(p); break;    \
+            case 32: bwd_##NAME##_kernel<32, T><<<grid, SweepCfg<32>::NT, 0, s>>>(p); break;    \
+            case 64: bwd_##NAME##_kernel<64, T><<<grid, SweepCfg<64>::NT, 0, s>>>(p); break;    \
+            case 128: bwd_##NAME##_kernel<128, T><<<grid, SweepCfg<128>::NT, 0, s>>>(p); break; \
+            default: return cudaErrorInvalidValue;                                              \
+        }                                                                                       \
+        return cudaGetLastError();                                                              \
+    }
+LA_BWD_DISPATCH(dq)
+LA_BWD_DISPATCH(dk)
+LA_BWD_DISPATCH(dv)
+#undef LA_BWD_DISPATCH
 
 template <typename T>
 cudaError_t launch_all(const BwdParams &p, cudaStream_t s, int *launches) {
     cudaError_t e = cudaSuccess;
-    if (p.mode & LA_NORMALIZE) {
-        bwd_den_kernel<T><<<(unsigned)(p.B * p.H), 128, 0, s>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        ++*launches;
-    }
-    if ((e = launch_sweep<kSweepDQ, T>(p, s)) != cudaSuccess) return e;
+    const bool norm = p.mode & LA_NORMALIZE;
+    if (norm && (e = cudaMemsetAsync(p.den, 0, sizeof(float) * (size_t)p.B * p.H * p.L, s)) != cudaSuccess) return e;
+    if ((e = launch_dq<T>(p, p.dv, p.dk, s)) != cudaSuccess) return e;
     ++*launches;
-    if (p.mode & LA_NORMALIZE) {
+    if (norm) {
         const long warps = (long)p.B * p.H * p.L;
-        bwd_ecol_kernel<T><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(p);
+        bwd_norm_kernel<T><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         ++*launches;
     }
-    if ((e = launch_sweep<kSweepDK, T>(p, s)) != cudaSuccess) return e;
+    if ((e = launch_dk<T>(p, p.dv, p.dk, s)) != cudaSuccess) return e;
     ++*launches;
-    if ((e = launch_sweep<kSweepDV, T>(p, s)) != cudaSuccess) return e;
-    ++*launches;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const bool per_channel = p.mode & (LA_GATE_CHANNEL | LA_NORMALIZE);
-    const long n = per_channel ? (long)p.B * p.H * p.dk : (long)p.B * p.H * p.L * p.dk;
-    long blocks = (n + kFinThreads - 1) / kFinThreads;
-    if (!per_channel && blocks > (long)sms * 16) blocks = (long)sms * 16;
-    bwd_finish_kernel<T><<<(unsigned)blocks, kFinThreads, 0, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dv<T>(p, p.dk, p.dv, s)) != cudaSuccess) return e;
     ++*launches;
     return cudaSuccess;
 }
 
+// ---------------------------------------------------------------- tensor-core route
+// With a scalar gate (A_t = gamma_h or 1) and no normaliser, each gradient is
+// itself a causal linear-attention forward with its roles permuted (all with
+// the identity feature map, the decay gamma^(t-s) symmetric in the roles):
+//   dQ_t = sum_{s<=t} gamma^{t-s} (dout_t . v_s) K_s      = fwd(dout, v, K)
+//   dK_s = sum_{t>=s} gamma^{t-s} (v_s . dout_t) Q_t      = rev fwd(rev v, rev dout, rev Q)
+//   dv_s = sum_{t>=s} gamma^{t-s} (K_s . Q_t) dout_t      = rev fwd(rev K, rev Q, rev dout)
+// (rev reverses the token order; t >= s becomes t' <= s'). They run on the
+// tensor-core forward kernel; a prep pass writes the reversed (and phi-applied)
+// operands, a last pass un-reverses dK, dv and applies phi'.
+constexpr int kEw = 256;  // threads of the elementwise passes
+constexpr int kD = 128;   // the tensor-core kernel's head dim
+
+__device__ __forceinline__ uint4 phi8(uint4 x, bool elu1) {
+    if (!elu1) return x;
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = phi(__uint_as_float(w[i] << 16), true), hi = phi(__uint_as_float(w[i] & 0xffff0000u), true);
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// reversed copies of v, dout, phi(q), phi(k), and phi(k) in order (elu1 only).
+// One uint4 (8 bf16) per step; rows of 128 stay contiguous.
+__global__ void __launch_bounds__(kEw) bwd_prep_kernel(const uint4 *q, const uint4 *k, const uint4 *v, const uint4 *d,
+                                                       uint4 *rv, uint4 *rd, uint4 *rq, uint4 *rk, uint4 *kf,
+                                                       long rows, int L, bool elu1) {
+    constexpr int CPR = kD / 8;  // chunks per row
+    const long n = rows * CPR;
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long row = x / CPR;
+        const int c = (int)(x % CPR), t = (int)(row % L);
+        const long rr = (row - t + (L - 1 - t)) * CPR + c;  // same sequence, token L-1-t
+        const uint4 kk = phi8(__ldcs(k + x), elu1);
+        rv[rr] = __ldcs(v + x);
+        rd[rr] = __ldcs(d + x);
+        rq[rr] = phi8(__ldcs(q + x), elu1);
+        rk[rr] = kk;
+        if (kf) kf[x] = kk;
+    }
+}
+
+// dq = dQ phi'(q) (in place when dq holds dQ), dk = rev(rdK) phi'(k), dv = rev(rdv)
+__global__ void __launch_bounds__(kEw) bwd_post_kernel(const uint4 *q, const uint4 *k, const uint4 *dQ, const uint4 *rdk,
+                                                       const uint4 *rdv, uint4 *dq, uint4 *dk, uint4 *dv, long rows,
+                                                       int L, bool elu1) {
+    constexpr int CPR = kD / 8;
+    const long n = rows * CPR;
+    auto scale = [](uint4 g, uint4 x) {  // g * phi'(x), elu1: 1 for x > 0, e^x otherwise
+        uint32_t gw[4] = {g.x, g.y, g.z, g.w}, xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xffff0000u);
+            const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xffff0000u);
+            __nv_bfloat162 h = __floats2bfloat162_rn(x0 > 0.f ? g0 : g0 * __expf(x0), x1 > 0.f ? g1 : g1 * __expf(x1));
+            gw[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(gw[0], gw[1], gw[2], gw[3]);
+    };
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long row = x / CPR;
+        const int c = (int)(x % CPR), t = (int)(row % L);
+        const long rr = (row - t + (L - 1 - t)) * CPR + c;
+        const uint4 gk = __ldcs(rdk + rr), gv = __ldcs(rdv + rr);
+        if (elu1) {
+            dq[x] = scale(__ldcs(dQ + x), __ldg(q + x));
+            dk[x] = scale(gk, __ldg(k + x));
+        } else {
+            dk[x] = gk;
+        }
+        dv[x] = gv;
+    }
+}
+
+int ew_blocks(long n) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 132;
+    const long need = (n + kEw - 1) / kEw, cap = (long)sms * 8;
+    return (int)(need < cap ? need : cap);
+}
+
 }  // namespace
+
+bool bwd_tc_supports(const BwdArgs &a) {
+    if (a.mode & (LA_DTYPE_F32 | LA_NORMALIZE | LA_GATE_CHANNEL)) return false;
+    if (a.dk != kD || a.dv != kD || a.L < 1) return false;
+    ChunkArgs c{a.q, a.k, a.v, a.gate, nullptr, nullptr, a.B, a.H, a.L, kD, kD, a.mode & LA_GATE_HEAD, 64, nullptr};
+    return chunk_tc_supports(c);
+}
+
+int launch_bwd_tc(const BwdArgs &a, cudaStream_t s, int *launches) {
+    const long rows = (long)a.B * a.H * a.L;
+    const size_t arr = (size_t)rows * kD * sizeof(__nv_bfloat16);
+    const bool elu1 = a.mode & LA_PHI_ELU1;
+    // rv, rd, rq, rk, rdk, rdv; with elu1 also K = phi(k) and dQ
+    const int narr = elu1 ? 8 : 6;
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, narr * arr, s) != cudaSuccess) return LA_ERR_CUDA;
+    char *b = static_cast<char *>(scratch);
+    uint4 *rv = reinterpret_cast<uint4 *>(b), *rd = reinterpret_cast<uint4 *>(b + arr);
+    uint4 *rq = reinterpret_cast<uint4 *>(b + 2 * arr), *rk = reinterpret_cast<uint4 *>(b + 3 * arr);
+    uint4 *rdk = reinterpret_cast<uint4 *>(b + 4 * arr), *rdv = reinterpret_cast<uint4 *>(b + 5 * arr);
+    uint4 *kf = elu1 ? reinterpret_cast<uint4 *>(b + 6 * arr) : nullptr;
+    uint4 *dQ = elu1 ? reinterpret_cast<uint4 *>(b + 7 * arr) : static_cast<uint4 *>(a.grad_q);
+    const int mode = a.mode & LA_GATE_HEAD;  // identity feature map, bf16, no normaliser
+    const int nb = ew_blocks(rows * (kD / 8));
+    int rc = LA_OK;
+    bwd_prep_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
+                                       static_cast<const uint4 *>(a.v), static_cast<const uint4 *>(a.dout), rv, rd, rq,
+                                       rk, kf, rows, a.L, elu1);
+    if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
+    else ++*launches;
+    const ChunkArgs calls[3] = {
+        {a.dout, a.v, elu1 ? kf : a.k, a.gate, dQ, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
+        {rv, rd, rq, a.gate, rdk, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
+        {rk, rq, rd, a.gate, rdv, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
+    };
+    for (int i = 0; i < 3 && rc == LA_OK; ++i) rc = launch_chunk_tc(calls[i], s, launches);
+    if (rc == LA_OK) {
+        bwd_post_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), dQ, rdk,
+                                           rdv, static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k),
+                                           static_cast<uint4 *>(a.grad_v), rows, a.L, elu1);
+        if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
+        else ++*launches;
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
+    return rc;
+}
 
 size_t bwd_scratch_bytes(const BwdArgs &a) {
     const size_t n = (size_t)a.B * a.H * a.L;
-    return (2 * n * a.dk + ((a.mode & LA_NORMALIZE) ? 2 * n : 0)) * sizeof(float);
+    return (n * a.dk + ((a.mode & LA_NORMALIZE) ? n * a.dk + 3 * n : 0)) * sizeof(float);
 }
 
 int launch_bwd(const BwdArgs &a, cudaStream_t s, int *launches) {
@@ -386,12 +639,14 @@ int launch_bwd(const BwdArgs &a, cudaStream_t s, int *launches) {
     void *scratch = nullptr;
     if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
     const size_t n = (size_t)a.B * a.H * a.L;
+    float *f = static_cast<float *>(scratch);
     BwdParams p{a.q, a.k, a.v, a.gate, a.dout, a.grad_q, a.grad_k, a.grad_v, a.grad_g,
-                static_cast<float *>(scratch), static_cast<float *>(scratch) + n * a.dk, nullptr, nullptr,
-                a.B, a.H, a.L, a.dk, a.dv, a.mode};
+                f, nullptr, nullptr, nullptr, nullptr, a.B, a.H, a.L, a.dk, a.dv, a.mode};
     if (a.mode & LA_NORMALIZE) {
-        p.den_inv = p.gk + n * a.dk;
-        p.ecol = p.den_inv + n;
+        p.zb = f + n * a.dk;
+        p.den = p.zb + n * a.dk;
+        p.dinv = p.den + n;
+        p.ecol = p.dinv + n;
     }
     const cudaError_t e = (a.mode & LA_DTYPE_F32) ? launch_all<float>(p, s, launches)
                                                   : launch_all<__nv_bfloat16>(p, s, launches);

@@ -78,6 +78,8 @@ int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
 int launch_delta(const DeltaArgs &a, cudaStream_t s, int *launches);
 int launch_gn_swish(const GnArgs &a, cudaStream_t s, int *launches);
 int launch_bwd(const BwdArgs &a, cudaStream_t s, int *launches);
+bool bwd_tc_supports(const BwdArgs &a);
+int launch_bwd_tc(const BwdArgs &a, cudaStream_t s, int *launches);
 size_t bwd_scratch_bytes(const BwdArgs &a);
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);

@@ -201,9 +201,10 @@ def group_norm_swish(x, ogate, *, gn_weight=None, gn_bias=None, gn_eps=1e-5, out
 
 
 def chunk_bwd(q, k, v, dout, gate=None, *, phi="elu1", normalize=False, gate_kind=None,
-              dq=None, dk=None, dv=None, dgate=None, want_dgate=True, stream=None):
+              dq=None, dk=None, dv=None, dgate=None, want_dgate=True, simt=False, stream=None):
     """la_chunk_bwd: gradients of chunk_fwd (from a zero state) given dout.
-    Returns (dq, dk, dv, dgate); dgate is None unless gate_kind == "channel"."""
+    Returns (dq, dk, dv, dgate); dgate is None unless gate_kind == "channel".
+    ``simt`` forces the CUDA-core sweeps."""
     B, H, L, d_k = q.shape
     d_v = v.shape[-1]
     dq = torch.empty_like(q) if dq is None else dq
@@ -213,7 +214,7 @@ def chunk_bwd(q, k, v, dout, gate=None, *, phi="elu1", normalize=False, gate_kin
         dgate = torch.empty_like(q)
     if gate_kind != "channel":
         dgate = None
-    mode = mode_bits(phi, normalize, gate_kind, q.dtype)
+    mode = mode_bits(phi, normalize, gate_kind, q.dtype, simt)
     rc = load().la_chunk_bwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"), _dev(dout, "dout"), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"),
                              _dev(dgate, "dgate"), B, H, L, d_k, d_v, mode, _stream(stream))
     if rc != LA_OK:

@@ -29,7 +29,7 @@ def _host(t):
     return None if t is None else t.float().numpy()
 
 
-def _check(cfg, seed=0, heads=None, tol=None):
+def _check(cfg, seed=0, heads=None, tol=None, simt=False):
     """GPU gradients against the oracle's; ``heads`` limits the oracle to the
     first few heads of every batch row (the GPU computes all of them)."""
     from retention_gb300 import la
@@ -42,7 +42,7 @@ def _check(cfg, seed=0, heads=None, tol=None):
     dg = nan(x["q"]) if cfg["gate"] == "channel" else None
     n0 = la.kernel_launches()
     la.chunk_bwd(x["q"], x["k"], x["v"], d, x["gate"], phi=cfg["phi"], normalize=cfg["normalize"],
-                 gate_kind=cfg["gate"], dq=dq, dk=dk, dv=dv, dgate=dg)
+                 gate_kind=cfg["gate"], dq=dq, dk=dk, dv=dv, dgate=dg, simt=simt)
     torch.cuda.synchronize()
     launches = la.kernel_launches() - n0
     hs = slice(None) if heads is None else slice(0, heads)
@@ -83,9 +83,23 @@ def test_fp32_head_dims(dk, dv):
 
 
 @pytest.mark.parametrize("m", MODES, ids=MID)
-def test_bf16_modes(m):
+@pytest.mark.parametrize("simt", [False, True], ids=["default", "simt"])
+def test_bf16_modes(m, simt):
+    """Every mode; without the normaliser and the per-channel gate the default
+    route is the tensor-core one (prep, three forwards, post)."""
+    from retention_gb300 import la
     cfg = W.workload("la", B=2, H=3, L=333, **m)
-    _check(cfg, seed=3)
+    launches = _check(cfg, seed=3, simt=simt)
+    tc = not simt and not m["normalize"] and m["gate"] != "channel"
+    # prep + three forwards (three launches each when the short batch is split) + post
+    assert (launches in (5, 11)) if tc else launches == (4 if m["normalize"] else 3), launches
+
+
+@pytest.mark.parametrize("m", [MODES[1], MODES[3]], ids=MID)
+@pytest.mark.parametrize("B,H,L", [(1, 2, 1000), (2, 40, 200), (1, 1, 1), (1, 3, 65)])
+def test_bf16_tensor_core_route_shapes(m, B, H, L):
+    """Split and unsplit sequences, one token, a ragged chunk."""
+    _check(W.workload("la", B=B, H=H, L=L, **m), seed=B + H + L)
 
 
 def test_bf16_gated_long_sequence():
@@ -97,8 +111,10 @@ def test_bf16_gated_long_sequence():
 def test_full_size_sampled_heads(name):
     """The full workload shapes on the GPU, the oracle on two heads of every
     batch row."""
-    launches = _check(W.workload(name), seed=0, heads=2)
-    assert launches >= 4
+    cfg = W.workload(name)
+    launches = _check(cfg, seed=0, heads=2)
+    # retention: prep, three tensor-core forwards, post; la: dQ, normaliser, dK, dV sweeps
+    assert launches == (4 if cfg["normalize"] else 5)
 
 
 def test_without_the_gate_gradient():
