@@ -313,6 +313,42 @@ def bench_delta(steps, warmup, world):
             "workload": "delta rule, recurrent: B=8, H=16, L=4096, d=128 bf16, unit q/k, beta=sigmoid(N(0,1))"}
 
 
+def bench_bwd(name, steps, warmup, world, pk):
+    """la_chunk_bwd on a workload's shapes (dout ~ N(0,1)). Roofline: the
+    gradients' HBM floor, reading q, k, v, dout (and g) and writing dq, dk, dv
+    (and dg) once each, against the flops of a chunkwise backward (twice the
+    forward's dense products)."""
+    from retention_gb300 import la
+    cfg = W.workload(name)
+    q, k, v, gate = device_inputs(cfg)
+    g = torch.Generator(device="cuda").manual_seed(2)
+    d = torch.randn(v.shape, generator=g, device="cuda").to(v.dtype)
+    B, H, L, dk, dv = cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"]
+    dq, dkk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg = torch.empty_like(q) if cfg["gate"] == "channel" else None
+
+    def step():
+        la.chunk_bwd(q, k, v, d, gate, phi=cfg["phi"], normalize=cfg["normalize"], gate_kind=cfg["gate"],
+                     dq=dq, dk=dkk, dv=dvv, dgate=dg)
+
+    n0 = la.kernel_launches()
+    step()
+    torch.cuda.synchronize()
+    per_step = la.kernel_launches() - n0
+    secs = max_over_ranks(time_calls(step, steps, warmup, world), world)
+    t = secs / steps
+    n = B * H * L
+    esz = 2 if cfg["dtype"] == "bf16" else 4
+    gated = cfg["gate"] == "channel"
+    bytes_ = n * (4 * dk + 3 * dv + (2 * dk if gated else 0)) * esz  # read q, k, v, dout (g); write dq, dk, dv (dg)
+    flops = 2 * n * (2 * cfg["chunk"] * dk + 2 * cfg["chunk"] * dv + 4 * dk * dv)
+    t_roof = max(bytes_ / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+    route = "tensor-core forwards" if la.mode_bits(cfg["phi"], cfg["normalize"], cfg["gate"]) & (
+        la.LA_NORMALIZE | la.LA_GATE_CHANNEL) == 0 else "CUDA-core sweeps"
+    return {"tokens_per_s": world * B * L / t, "ms_per_step": t * 1e3, "launches_per_step": per_step,
+            "roofline_frac": t_roof / t, "route": route, "algorithmic_bytes": bytes_}
+
+
 def bench_e2e(cfg, steps, warmup, world):
     """The same call with the inputs in pinned host memory: every step copies
     q, k, v to the device, runs la_chunk_fwd, and copies the output and final
@@ -452,8 +488,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--decode-steps", type=int, default=1000)
-    ap.add_argument("--no-extra", action="store_true", help="skip the retention/retnet/gated/delta lines")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the retention/retnet/gated/delta/backward lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--only", default=None,
+                    choices=["la", "retention", "retnet", "gla", "delta", "retention_bwd", "la_bwd", "gla_bwd"],
+                    help="time one workload alone and print its line (for profiling)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -471,6 +511,18 @@ def main():
     pk = peaks()
     from retention_gb300 import la
     la.load()
+    if args.only:
+        name = args.only
+        if name == "delta":
+            r = bench_delta(args.steps, warmup, world)
+        elif name.endswith("_bwd"):
+            r = bench_bwd(name[:-4], args.steps, warmup, world, pk)
+        else:
+            r = bench_chunk(name, args.steps, warmup, world, pk)
+            r = {key: r[key] for key in ("tokens_per_s", "ms_per_step", "gbs", "roofline_frac", "launches_per_step")}
+        if rank == 0:
+            print(json.dumps({"only": name, **r}), flush=True)
+        return
 
     with Clocks(local) as clk:
         la_res = bench_chunk("la", args.steps, warmup, world, pk)
@@ -490,6 +542,9 @@ def main():
             torch.cuda.empty_cache()
         extra["delta"] = bench_delta(max(3, args.steps // 4), 2, world)
         torch.cuda.empty_cache()
+        for name, st in (("retention", max(5, args.steps // 4)), ("la", 3), ("gla", 2)):
+            extra[name + "_bwd"] = bench_bwd(name, st, 1 if name == "gla" else 3, world, pk)
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
