@@ -186,3 +186,37 @@ def delta_recurrent(K, V, beta, Q=None, use_delta=True, S0=None):
         if Q is not None:
             out[t] = S @ np.asarray(Q[t], dtype=np.float64)
     return states, out
+
+
+def delta_chunkwise(K, V, beta, Q, C, S0=None):
+    """The delta rule over chunks of C tokens (the last one ragged), the form a
+    chunked kernel computes. No page gives it; it follows from the recurrence.
+    Write each step as S_t = S_{t-1} + u_t k_t^T with the pseudo-value
+    u_t = beta_t (v_t - S_{t-1} k_t). Inside a chunk starting from S0,
+    S_{t-1} = S0 + sum_{s<t} u_s k_s^T, so
+        u_t + beta_t sum_{s<t} (k_t . k_s) u_s = beta_t (v_t - S0 k_t),
+    a unit lower-triangular system: (I + A) Ut = diag(beta) (V - K S0^T) with
+    A[t, s] = beta_t k_t . k_s for s < t. With T = (I + A)^-1 diag(beta),
+    W = T K and U = T V (both free of the state):
+        Ut  = U - W S0^T
+        out = Q S0^T + tril(Q K^T) Ut        (diagonal included: read after the update)
+        S   = S0 + Ut^T K
+    K, Q: [L, dk]; V: [L, dv]; beta: [L]. Returns (out [L, dv], S [dv, dk])."""
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    Q = np.asarray(Q, dtype=np.float64)
+    beta = np.asarray(beta, dtype=np.float64)
+    L, dk = K.shape
+    dv = V.shape[1]
+    S = np.zeros((dv, dk)) if S0 is None else np.array(S0, dtype=np.float64).reshape(dv, dk)
+    out = np.zeros((L, dv))
+    for c0 in range(0, L, C):
+        k, v, q, b = K[c0:c0 + C], V[c0:c0 + C], Q[c0:c0 + C], beta[c0:c0 + C]
+        n = k.shape[0]
+        A = np.tril(b[:, None] * (k @ k.T), -1)
+        T = np.linalg.solve(np.eye(n) + A, np.diag(b))
+        W, U = T @ k, T @ v
+        Ut = U - W @ S.T
+        out[c0:c0 + n] = q @ S.T + np.tril(q @ k.T) @ Ut
+        S = S + Ut.T @ k
+    return out, S

@@ -119,6 +119,19 @@ def test_continuing_from_a_state_equals_one_run():
     np.testing.assert_allclose(st2, st, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("C", [1, 4, 7, 16, 64])
+def test_chunkwise_form_equals_the_recurrence(C):
+    """The chunked (triangular-solve) form restated in numpy against the page's
+    recurrence, on a ragged length, from a state."""
+    q, k, v, beta = _rand(1, 2, 37, 8, 6, seed=11)
+    S0 = np.random.default_rng(12).standard_normal((6, 8))
+    for h in range(2):
+        states, o = forms.delta_recurrent(k[0, h], v[0, h], beta[0, h], Q=q[0, h], S0=S0)
+        out, S = forms.delta_chunkwise(k[0, h], v[0, h], beta[0, h], q[0, h], C, S0=S0)
+        np.testing.assert_allclose(out, o, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(S, states[-1], rtol=0, atol=1e-11)
+
+
 PINS = [test_matches_the_matrix_form, test_single_token, test_orthonormal_keys_with_unit_beta_are_additive,
         test_overlapping_keys_are_not_additive, test_same_key_twice_overwrites,
         test_reading_with_the_key_returns_the_value_just_written, test_zero_beta_keeps_the_state,
