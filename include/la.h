@@ -139,11 +139,17 @@ int la_chunk_fwd_from_state(const void *q, const void *k, const void *v, const v
  *   q, k   [B][H][L][d_k]     v, out [B][H][L][d_v]   (bf16, or fp32 with LA_DTYPE_F32)
  *   beta   [B][H][L], the same type; usually in (0, 1]
  *   final_state  NULL, or [B][H][d_v][d_k] fp32: S after the last token
- *   mode   0 or LA_DTYPE_F32 (no feature map, normaliser or gate)
+ *   mode   0 or LA_DTYPE_F32 (no feature map, normaliser or gate), optionally
+ *          | LA_KERNEL_SIMT to force the recurrent kernel
  *   d_k, d_v in {16, 32, 64, 128}; B, H, L >= 0 (L = 0 writes a zero state)
  *
- * Every token depends on the previous state, so each sequence is processed
- * one token after another (6 d_k d_v flops a token, on the CUDA cores in fp32).
+ * bf16 with d_k = d_v = 128 runs in chunks of 64 tokens on the tensor cores:
+ * each step is S_t = S_{t-1} + u_t k_t^T with u_t = beta_t (v_t - S_{t-1} k_t),
+ * and inside a chunk the u_t solve a unit lower-triangular system (I + A) U =
+ * diag(beta) (V - K S0^T), A[t][s] = beta_t k_t . k_s for s < t, so a chunk
+ * is a triangular inverse and a few matrix products (the recurrence
+ * rearranged; no page gives this form). Every other case runs the recurrence
+ * token by token on the CUDA cores in fp32 (6 d_k d_v flops a token).
  * Errors as la_chunk_fwd; beta needs only element alignment.
  */
 int la_delta_fwd(const void *q, const void *k, const void *v, const void *beta,

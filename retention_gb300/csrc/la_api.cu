@@ -182,7 +182,7 @@ int la_delta_fwd(const void *q, const void *k, const void *v, const void *beta, 
                  float *final_state, int B, int H, int L, int dk, int dv, int mode, la_stream_t stream) {
     if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
-    if (mode & ~LA_DTYPE_F32) return LA_ERR_INVALID_ARG;
+    if (mode & ~(LA_DTYPE_F32 | LA_KERNEL_SIMT)) return LA_ERR_INVALID_ARG;
     const long nbh = (long)B * H;
     if (nbh > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
     if (nbh == 0) return LA_OK;
@@ -198,9 +198,10 @@ int la_delta_fwd(const void *q, const void *k, const void *v, const void *beta, 
     if (!q || !k || !v || !beta || !out) return LA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LA_ERR_MISALIGNED;
     if ((uintptr_t)beta & ((mode & LA_DTYPE_F32) ? 3u : 1u)) return LA_ERR_MISALIGNED;
-    la::DeltaArgs a{q, k, v, beta, out, final_state, B, H, L, dk, dv, mode};
+    la::DeltaArgs a{q, k, v, beta, out, final_state, B, H, L, dk, dv, mode & LA_DTYPE_F32};
     int launches = 0;
-    const int rc = la::launch_delta(a, s, &launches);
+    const int rc = (!(mode & LA_KERNEL_SIMT) && la::delta_tc_supports(a)) ? la::launch_delta_tc(a, s, &launches)
+                                                                          : la::launch_delta(a, s, &launches);
     g_launches += (unsigned long long)launches;
     return rc;
 }

@@ -76,6 +76,9 @@ struct DeltaArgs {
 int launch_chunk_simt(const ChunkArgs &a, cudaStream_t s, int *launches);
 int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
 int launch_delta(const DeltaArgs &a, cudaStream_t s, int *launches);
+// the delta rule in chunks on the tensor cores (bf16, d_k = d_v = 128)
+bool delta_tc_supports(const DeltaArgs &a);
+int launch_delta_tc(const DeltaArgs &a, cudaStream_t s, int *launches);
 int launch_gn_swish(const GnArgs &a, cudaStream_t s, int *launches);
 int launch_bwd(const BwdArgs &a, cudaStream_t s, int *launches);
 bool bwd_tc_supports(const BwdArgs &a);

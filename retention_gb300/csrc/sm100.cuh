@@ -66,7 +66,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 // Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
 // of wall time. Returns false on time-out (the caller records it and leaves).
 // The loop lives out of line so that each wait site costs a few instructions.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;

@@ -254,7 +254,7 @@ def decode_step(q, k, v, state, gate=None, *, phi="elu1", normalize=False, gate_
     return out
 
 
-def delta_fwd(q, k, v, beta, *, out=None, final_state=None, want_state=True, stream=None):
+def delta_fwd(q, k, v, beta, *, out=None, final_state=None, want_state=True, simt=False, stream=None):
     """la_delta_fwd: the delta rule over q, k [B,H,L,dk], v [B,H,L,dv], beta
     [B,H,L] (keys as given: normalise them first). Returns (out, final_state
     [B,H,dv*dk] fp32, rows = value dimensions)."""
@@ -266,7 +266,7 @@ def delta_fwd(q, k, v, beta, *, out=None, final_state=None, want_state=True, str
         final_state = torch.empty(B, H, dv * dk, dtype=torch.float32, device=q.device)
     if beta.dtype != q.dtype or not beta.is_contiguous():
         raise ValueError("beta must be contiguous and of q's dtype")
-    mode = LA_DTYPE_F32 if q.dtype == torch.float32 else 0
+    mode = (LA_DTYPE_F32 if q.dtype == torch.float32 else 0) | (LA_KERNEL_SIMT if simt else 0)
     if q.dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("q, k, v must be bfloat16 or float32")
     rc = load().la_delta_fwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(beta, "beta"),
