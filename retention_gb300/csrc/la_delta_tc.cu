@@ -42,15 +42,17 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // far beyond any legitimate wait
 
 // shared memory (offsets from a 1024-byte aligned base). A operands of M = 128
 // products read 64 rows past their 64-row tiles; every such tile is followed
-// by at least 8 KiB of other tiles.
-constexpr uint32_t kQ = 0, kK = 16384, kV = 32768;  // [64 x 128] bf16 tiles, two 8 KiB halves
-constexpr uint32_t kW = 49152;                      // W, K-major, two halves
-constexpr uint32_t kT = 65536;                      // T, K-major [64 x 64]
-constexpr uint32_t kP = 73728;                      // P, K-major [64 x 64]
-constexpr uint32_t kU = 81920;                      // Ut, MN-major [64 tokens x 128], two halves
-constexpr uint32_t kS = 98304;                      // S^T copy, MN-major: 128 lines x 128 values, two 16 KiB halves
+// by at least 8 KiB of other tiles. q, k, v come in two sets: chunk n + 1's
+// tiles are copied in (cp.async) while chunk n is processed.
+constexpr uint32_t kSet = 49152;                    // one set: q, k, v
+constexpr uint32_t kQ = 0, kK = 16384, kV = 32768;  // [64 x 128] bf16 tiles in a set, two 8 KiB halves
+constexpr uint32_t kW = 2 * kSet;                   // W, K-major, two halves
+constexpr uint32_t kT = kW + 16384;                 // T, K-major [64 x 64]
+constexpr uint32_t kP = kT + 8192;                  // P, K-major [64 x 64]
+constexpr uint32_t kU = kP + 8192;                  // Ut, MN-major [64 tokens x 128], two halves
+constexpr uint32_t kS = kU + 16384;                 // S^T copy, MN-major: 128 lines x 128 values, two 16 KiB halves
 constexpr int kLd = 65;                             // padded fp32 row
-constexpr uint32_t kL = 131072;                     // L = I + A, fp32 [64][65]
+constexpr uint32_t kL = kS + 32768;                 // L = I + A, fp32 [64][65]
 constexpr uint32_t kLi = kL + 64 * kLd * 4;         // L^-1, fp32 [64][65]
 constexpr uint32_t kY = kLi + 64 * kLd * 4;         // block-row partial products, fp32 [3][16][17]
 constexpr uint32_t kB = kY + 3 * 16 * 17 * 4;       // beta [64]
@@ -60,6 +62,13 @@ constexpr uint32_t kSmem = kBar + 16 + 1024;        // + alignment slack
 constexpr uint32_t cS = 0, cA = 128, cP = 192, cX = 256, cU = 384, kTmemCols = 512;
 
 __device__ unsigned int g_delta_tc_error;
+
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -130,40 +139,49 @@ __global__ void __launch_bounds__(kThreads, 1) delta_tc_kernel(const DeltaArgs a
     };
 
     const int nchunks = (L + kC - 1) / kC;
+    // chunk m's q, k, v into tile set m % 2: 3 x 64 rows x 16 chunks of 16
+    // bytes, 24 per thread; rows past the sequence are zero-filled
+    auto fetch = [&](int m) {
+        const int f0 = m * kC, fn = min(kC, L - f0);
+        const uint32_t set = sm0 + (uint32_t)(m & 1) * kSet;
+#pragma unroll
+        for (int u = 0; u < 24; ++u) {
+            const int x = tid + u * kThreads;
+            const int mm = x / (kC * 16), r = (x / 16) % kC, c8 = x % 16;
+            const bf16 *src = mm == 0 ? q : mm == 1 ? k : v;
+            const bool in = r < fn;
+            cp_async16(set + (mm == 0 ? kQ : mm == 1 ? kK : kV) + chunk_off(r, c8, 8192),
+                       src + (size_t)(f0 + (in ? r : 0)) * kD + c8 * 8, in ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+    fetch(0);
+    float bpre = (tid < kC && tid < L) ? to_f32(beta[tid]) : 0.f;
     for (int n = 0; n < nchunks; ++n) {
         const int t0 = n * kC, nt = min(kC, L - t0);
-        // ---------------------------------------------------------------- load q, k, v, beta
-        // 3 x 64 rows x 16 chunks of 16 bytes, 24 per thread, in batches of 8
-        // whose loads are all in flight before the first store
-#pragma unroll 1
-        for (int b8 = 0; b8 < 3; ++b8) {
-            uint4 val[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int x = tid + (8 * b8 + u) * kThreads;
-                const int m = x / (kC * 16), r = (x / 16) % kC, c8 = x % 16;
-                const bf16 *src = m == 0 ? q : m == 1 ? k : v;
-                val[u] = r < nt ? __ldcs(reinterpret_cast<const uint4 *>(src + (size_t)(t0 + r) * kD) + c8)
-                                : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int x = tid + (8 * b8 + u) * kThreads;
-                const int m = x / (kC * 16), r = (x / 16) % kC, c8 = x % 16;
-                *reinterpret_cast<uint4 *>(sm + (m == 0 ? kQ : m == 1 ? kK : kV) + chunk_off(r, c8, 8192)) = val[u];
-            }
-        }
-        if (tid < kC) bs[tid] = tid < nt ? to_f32(beta[t0 + tid]) : 0.f;
+        const uint32_t set = (uint32_t)(n & 1) * kSet;
+        const uint32_t sQ = set + kQ, sK = set + kK, sV = set + kV;
+        // ---------------------------------------------------------------- this chunk's tiles
+        if (tid < kC) bs[tid] = bpre;
+        cp_async_wait_all();
         fence_proxy_async_smem();
         __syncthreads();
+
         // ---------------------------------------------------------------- round 1: K K^T, Q K^T
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) umma_bf16(tmem + cA, kmaj2(kK, ks), kmaj2(kK, ks), id64, ks > 0);
+            for (int ks = 0; ks < 8; ++ks) umma_bf16(tmem + cA, kmaj2(sK, ks), kmaj2(sK, ks), id64, ks > 0);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) umma_bf16(tmem + cP, kmaj2(kQ, ks), kmaj2(kK, ks), id64, ks > 0);
+            for (int ks = 0; ks < 8; ++ks) umma_bf16(tmem + cP, kmaj2(sQ, ks), kmaj2(sK, ks), id64, ks > 0);
             umma_commit(mb);
+        }
+        if (n + 1 < nchunks) {
+            // the next chunk's tiles and beta, in flight while this chunk runs
+            // (its tile set was last read by chunk n - 1's MMAs, which are done)
+            fetch(n + 1);
+            const int nb = t0 + kC + tid;
+            bpre = (tid < kC && nb < L) ? to_f32(beta[nb]) : 0.f;
         }
         if (__syncthreads_or(!wait_mma())) {
             bad = 1;
@@ -217,20 +235,50 @@ __global__ void __launch_bounds__(kThreads, 1) delta_tc_kernel(const DeltaArgs a
             for (int r = 0; r < 16; ++r) Li[(o + r) * kLd + o + c] = x[r];
         }
         __syncthreads();
+#pragma unroll
         for (int bi = 1; bi < 4; ++bi) {
-            // block row bi: Y_bj = sum_{m=j}^{bi-1} L_bi,m Li_m,j, then Li_bi,j = -Li_bi,bi Y_bj
-            for (int e = tid; e < bi * 256; e += kThreads) {
-                const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                float acc = 0.f;
-                for (int m = 16 * j; m < 16 * bi; ++m) acc = fmaf(Lm[(16 * bi + r) * kLd + m], Li[m * kLd + 16 * j + c], acc);
-                Yb[(j * 16 + r) * 17 + c] = acc;
+            // block row bi: Y_bj = sum_{m=j}^{bi-1} L_bi,m Li_m,j, then Li_bi,j = -Li_bi,bi Y_bj.
+            // Each 16-term product is unrolled (its 32 loads issue together);
+            // the zeros above the diagonal of Li_bi,bi make the second a full
+            // 16-term sum.
+#pragma unroll
+            for (int e0 = 0; e0 < bi * 256; e0 += kThreads) {
+                const int e = e0 + tid, j = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                const float *lrow = Lm + (16 * bi + r) * kLd;
+                float acc0 = 0.f, acc1 = 0.f;
+                for (int kb = j; kb < bi; ++kb) {
+                    float lv[16], iv[16];
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        lv[m] = lrow[16 * kb + m];
+                        iv[m] = Li[(16 * kb + m) * kLd + 16 * j + c];
+                    }
+#pragma unroll
+                    for (int m = 0; m < 16; m += 2) {
+                        acc0 = fmaf(lv[m], iv[m], acc0);
+                        acc1 = fmaf(lv[m + 1], iv[m + 1], acc1);
+                    }
+                }
+                Yb[(j * 16 + r) * 17 + c] = acc0 + acc1;
             }
             __syncthreads();
-            for (int e = tid; e < bi * 256; e += kThreads) {
-                const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                float acc = 0.f;
-                for (int m = 0; m <= r; ++m) acc = fmaf(Li[(16 * bi + r) * kLd + 16 * bi + m], Yb[(j * 16 + m) * 17 + c], acc);
-                Li[(16 * bi + r) * kLd + 16 * j + c] = -acc;
+#pragma unroll
+            for (int e0 = 0; e0 < bi * 256; e0 += kThreads) {
+                const int e = e0 + tid, j = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                const float *irow = Li + (16 * bi + r) * kLd + 16 * bi;
+                float iv[16], yv[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    iv[m] = irow[m];
+                    yv[m] = Yb[(j * 16 + m) * 17 + c];
+                }
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    acc0 = fmaf(iv[m], yv[m], acc0);
+                    acc1 = fmaf(iv[m + 1], yv[m + 1], acc1);
+                }
+                Li[(16 * bi + r) * kLd + 16 * j + c] = -(acc0 + acc1);
             }
             __syncthreads();
         }
@@ -251,9 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1) delta_tc_kernel(const DeltaArgs a
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + cX, kmaj1(kT, ks), mnmaj(kK, 8192, ks), idKM, ks > 0);
+            for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + cX, kmaj1(kT, ks), mnmaj(sK, 8192, ks), idKM, ks > 0);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + cU, kmaj1(kT, ks), mnmaj(kV, 8192, ks), idKM, ks > 0);
+            for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + cU, kmaj1(kT, ks), mnmaj(sV, 8192, ks), idKM, ks > 0);
             umma_commit(mb);
         }
         if (__syncthreads_or(!wait_mma())) {
@@ -323,12 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1) delta_tc_kernel(const DeltaArgs a
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) umma_bf16(tmem + cX, kmaj2(kQ, ks), mnmaj(kS, 16384, ks), idKM, ks > 0);
+            for (int ks = 0; ks < 8; ++ks) umma_bf16(tmem + cX, kmaj2(sQ, ks), mnmaj(kS, 16384, ks), idKM, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + cX, kmaj1(kP, ks), mnmaj(kU, 8192, ks), idKM, 1);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(tmem + cS, mnmaj(kK, 8192, ks), mnmaj(kU, 8192, ks), idMM, (n > 0 || ks > 0));
+                umma_bf16(tmem + cS, mnmaj(sK, 8192, ks), mnmaj(kU, 8192, ks), idMM, (n > 0 || ks > 0));
             umma_commit(mb);
         }
         if (__syncthreads_or(!wait_mma())) {
@@ -392,8 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1) delta_tc_kernel(const DeltaArgs a
             for (int e = 0; e < 32; ++e) fs[(size_t)(32 * j + e) * kD + i] = __uint_as_float(r[e]);
         }
     }
-    // teardown: every MMA issued has completed (the last wait saw it, or on a
-    // time-out a final commit is waited for, bounded)
+    // teardown: no copy may still be landing in shared memory, and every MMA
+    // issued has completed (the last wait saw it, or on a time-out a final
+    // commit is waited for, bounded)
+    cp_async_wait_all();
     if (bad) {
         if (tid == 0) {
             atomicOr(&g_delta_tc_error, 1u);
