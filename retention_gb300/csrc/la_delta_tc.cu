@@ -51,11 +51,12 @@ constexpr uint32_t kT = kW + 16384;                 // T, K-major [64 x 64]
 constexpr uint32_t kP = kT + 8192;                  // P, K-major [64 x 64]
 constexpr uint32_t kU = kP + 8192;                  // Ut, MN-major [64 tokens x 128], two halves
 constexpr uint32_t kS = kU + 16384;                 // S^T copy, MN-major: 128 lines x 128 values, two 16 KiB halves
-constexpr int kLd = 65;                             // padded fp32 row
-constexpr uint32_t kL = kS + 32768;                 // L = I + A, fp32 [64][65]
-constexpr uint32_t kLi = kL + 64 * kLd * 4;         // L^-1, fp32 [64][65]
-constexpr uint32_t kY = kLi + 64 * kLd * 4;         // block-row partial products, fp32 [3][16][17]
-constexpr uint32_t kB = kY + 3 * 16 * 17 * 4;       // beta [64]
+constexpr int kLd = 68;                             // fp32 row: 16-byte aligned, rows 4 banks apart
+constexpr uint32_t kL = kS + 32768;                 // L = I + A, fp32 [64][kLd]
+constexpr uint32_t kLi = kL + 64 * kLd * 4;         // L^-1, fp32 [64][kLd]
+constexpr int kYd = 20;                             // Y row: 16 + 4, 16-byte aligned
+constexpr uint32_t kY = kLi + 64 * kLd * 4;         // block-row partial products, fp32 [3][16][kYd]
+constexpr uint32_t kB = kY + 3 * 16 * kYd * 4;      // beta [64]
 constexpr uint32_t kBar = kB + 64 * 4;              // mbarrier, TMEM address
 constexpr uint32_t kSmem = kBar + 16 + 1024;        // + alignment slack
 // TMEM columns
@@ -197,9 +198,15 @@ __global__ void __launch_bounds__(kThreads, 1) delta_tc_kernel(const DeltaArgs a
             tmem_ld32(tmem + lane_base + cA + 32, r1);
             tmem_ld_wait();
 #pragma unroll
-            for (int s = 0; s < 64; ++s) {
-                const float x = __uint_as_float(s < 32 ? r0[s] : r1[s - 32]);
-                Lm[t * kLd + s] = s < t ? bt * x : (s == t ? 1.f : 0.f);
+            for (int s4 = 0; s4 < 64; s4 += 4) {
+                float l4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = s4 + e;
+                    const float x = __uint_as_float(s < 32 ? r0[s] : r1[s - 32]);
+                    l4[e] = s < t ? bt * x : (s == t ? 1.f : 0.f);
+                }
+                *reinterpret_cast<float4 *>(Lm + t * kLd + s4) = make_float4(l4[0], l4[1], l4[2], l4[3]);
             }
             tmem_ld32(tmem + lane_base + cP, r0);
             tmem_ld32(tmem + lane_base + cP + 32, r1);
@@ -238,58 +245,83 @@ __global__ void __launch_bounds__(kThreads, 1) delta_tc_kernel(const DeltaArgs a
 #pragma unroll
         for (int bi = 1; bi < 4; ++bi) {
             // block row bi: Y_bj = sum_{m=j}^{bi-1} L_bi,m Li_m,j, then Li_bi,j = -Li_bi,bi Y_bj.
-            // Each 16-term product is unrolled (its 32 loads issue together);
-            // the zeros above the diagonal of Li_bi,bi make the second a full
-            // 16-term sum.
+            // A thread takes four adjacent columns of one row (float4 loads of
+            // Li and Y rows, one L value per four products); the zeros above
+            // the diagonal of Li_bi,bi make the second product a full 16 terms.
 #pragma unroll
-            for (int e0 = 0; e0 < bi * 256; e0 += kThreads) {
-                const int e = e0 + tid, j = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                const float *lrow = Lm + (16 * bi + r) * kLd;
-                float acc0 = 0.f, acc1 = 0.f;
-                for (int kb = j; kb < bi; ++kb) {
-                    float lv[16], iv[16];
+            for (int e0 = 0; e0 < bi * 64; e0 += kThreads) {
+                const int e = e0 + tid;
+                if (e < bi * 64) {
+                    const int j = e >> 6, r = (e >> 2) & 15, c0 = 4 * (e & 3);
+                    const float *lrow = Lm + (16 * bi + r) * kLd;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int kb = j; kb < bi; ++kb) {
+                        float lv[16];
+                        float4 iv[16];
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        lv[m] = lrow[16 * kb + m];
-                        iv[m] = Li[(16 * kb + m) * kLd + 16 * j + c];
+                        for (int m = 0; m < 16; m += 4) {
+                            const float4 l4 = *reinterpret_cast<const float4 *>(lrow + 16 * kb + m);
+                            lv[m] = l4.x, lv[m + 1] = l4.y, lv[m + 2] = l4.z, lv[m + 3] = l4.w;
+                        }
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            iv[m] = *reinterpret_cast<const float4 *>(Li + (16 * kb + m) * kLd + 16 * j + c0);
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            acc.x = fmaf(lv[m], iv[m].x, acc.x);
+                            acc.y = fmaf(lv[m], iv[m].y, acc.y);
+                            acc.z = fmaf(lv[m], iv[m].z, acc.z);
+                            acc.w = fmaf(lv[m], iv[m].w, acc.w);
+                        }
                     }
-#pragma unroll
-                    for (int m = 0; m < 16; m += 2) {
-                        acc0 = fmaf(lv[m], iv[m], acc0);
-                        acc1 = fmaf(lv[m + 1], iv[m + 1], acc1);
-                    }
+                    *reinterpret_cast<float4 *>(Yb + (j * 16 + r) * kYd + c0) = acc;
                 }
-                Yb[(j * 16 + r) * 17 + c] = acc0 + acc1;
             }
             __syncthreads();
 #pragma unroll
-            for (int e0 = 0; e0 < bi * 256; e0 += kThreads) {
-                const int e = e0 + tid, j = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                const float *irow = Li + (16 * bi + r) * kLd + 16 * bi;
-                float iv[16], yv[16];
+            for (int e0 = 0; e0 < bi * 64; e0 += kThreads) {
+                const int e = e0 + tid;
+                if (e < bi * 64) {
+                    const int j = e >> 6, r = (e >> 2) & 15, c0 = 4 * (e & 3);
+                    const float *irow = Li + (16 * bi + r) * kLd + 16 * bi;
+                    float lv[16];
+                    float4 yv[16];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    iv[m] = irow[m];
-                    yv[m] = Yb[(j * 16 + m) * 17 + c];
-                }
-                float acc0 = 0.f, acc1 = 0.f;
+                    for (int m = 0; m < 16; m += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(irow + m);
+                        lv[m] = l4.x, lv[m + 1] = l4.y, lv[m + 2] = l4.z, lv[m + 3] = l4.w;
+                    }
 #pragma unroll
-                for (int m = 0; m < 16; m += 2) {
-                    acc0 = fmaf(iv[m], yv[m], acc0);
-                    acc1 = fmaf(iv[m + 1], yv[m + 1], acc1);
+                    for (int m = 0; m < 16; ++m) yv[m] = *reinterpret_cast<const float4 *>(Yb + (j * 16 + m) * kYd + c0);
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        acc.x = fmaf(lv[m], yv[m].x, acc.x);
+                        acc.y = fmaf(lv[m], yv[m].y, acc.y);
+                        acc.z = fmaf(lv[m], yv[m].z, acc.z);
+                        acc.w = fmaf(lv[m], yv[m].w, acc.w);
+                    }
+                    *reinterpret_cast<float4 *>(Li + (16 * bi + r) * kLd + 16 * j + c0) =
+                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
-                Li[(16 * bi + r) * kLd + 16 * j + c] = -(acc0 + acc1);
             }
             __syncthreads();
         }
         // T = L^-1 diag(beta), lower triangular, bf16 K-major
-        for (int x = tid; x < kC * 8; x += kThreads) {
-            const int t = x >> 3, c8 = x & 7;
+#pragma unroll
+        for (int x0 = 0; x0 < kC * 8; x0 += kThreads) {
+            const int x = x0 + tid, t = x >> 3, c8 = x & 7;
+            const float4 l0 = *reinterpret_cast<const float4 *>(Li + t * kLd + 8 * c8);
+            const float4 l1 = *reinterpret_cast<const float4 *>(Li + t * kLd + 8 * c8 + 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(bs + 8 * c8);
+            const float4 b1 = *reinterpret_cast<const float4 *>(bs + 8 * c8 + 4);
+            const float lv[8] = {l0.x * b0.x, l0.y * b0.y, l0.z * b0.z, l0.w * b0.w,
+                                 l1.x * b1.x, l1.y * b1.y, l1.z * b1.z, l1.w * b1.w};
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int s = c8 * 8 + 2 * e;
-                w[e] = pack2(s <= t ? Li[t * kLd + s] * bs[s] : 0.f, s + 1 <= t ? Li[t * kLd + s + 1] * bs[s + 1] : 0.f);
+                w[e] = pack2(s <= t ? lv[2 * e] : 0.f, s + 1 <= t ? lv[2 * e + 1] : 0.f);
             }
             *reinterpret_cast<uint4 *>(sm + kT + chunk_off(t, c8, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
