@@ -286,10 +286,13 @@ def bench_chunk(name, steps, warmup, world, pk):
     }
 
 
-def bench_delta(steps, warmup, world):
-    """The delta rule (la_delta_fwd) on its workload. Recurrent, so the bound is
-    the FP32 FMA pipe: 6 d_k d_v flops per (token, head) against SMs x 128
-    lanes x 2 flops x the 2070 MHz maximum SM clock."""
+def bench_delta(steps, warmup, world, pk):
+    """The delta rule (la_delta_fwd) on its workload. The default kernel works
+    in chunks of 64 on the tensor cores; its roofline is HBM (read q, k, v,
+    beta, write out and the final state once) against the chunked form's
+    products (about 11 MFLOP per 64-token chunk and head). The recurrent kernel
+    (LA_KERNEL_SIMT) is timed beside it against the FP32 FMA pipe: 6 d_k d_v
+    flops per token and head, SMs x 128 lanes x 2 flops x 2070 MHz."""
     from retention_gb300 import la
     cfg = W.workload("delta")
     B, H, L, dk, dv = cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"]
@@ -302,15 +305,26 @@ def bench_delta(steps, warmup, world):
     k = (k / k.norm(dim=-1, keepdim=True)).bfloat16()
     out = torch.empty_like(v)
     st = torch.empty(B, H, dv * dk, device="cuda")
-    secs = max_over_ranks(time_calls(lambda: la.delta_fwd(q, k, v, beta, out=out, final_state=st),
-                                     steps, warmup, world), world)
-    t = secs / steps
-    flops = 6.0 * B * H * L * dk * dv
-    peak = torch.cuda.get_device_properties(0).multi_processor_count * 128 * 2 * 2.07e9 / 1e12
-    return {"tokens_per_s": world * B * L / t, "ms_per_step": t * 1e3, "tflops": flops / t / 1e12,
-            "roofline": {"bound": "alu", "peak": peak, "unit": "TFLOP/s", "frac": flops / t / 1e12 / peak,
-                         "peak_source": "SMs x 128 FP32 lanes x 2 x 2070 MHz"},
-            "workload": "delta rule, recurrent: B=8, H=16, L=4096, d=128 bf16, unit q/k, beta=sigmoid(N(0,1))"}
+    res = {}
+    for simt in (False, True):
+        secs = max_over_ranks(time_calls(lambda: la.delta_fwd(q, k, v, beta, out=out, final_state=st, simt=simt),
+                                         steps, warmup, world), world)
+        res[simt] = secs / steps
+    t, tr = res[False], res[True]
+    n = B * H * L
+    bytes_ = n * (2 * dk + 2 * dv + 1) * 2 + B * H * dk * dv * 4
+    C = 64
+    # per chunk: K K^T, Q K^T; T K, T V; W S0^T, Q S0^T, K^T Ut; P Ut
+    flops = n / C * (2 * 2 * C * C * dk + 2 * C * C * (dk + dv) + 3 * 2 * C * dk * dv + 2 * C * C * dv)
+    t_roof = max(bytes_ / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
+    fma_peak = torch.cuda.get_device_properties(0).multi_processor_count * 128 * 2 * 2.07e9 / 1e12
+    rflops = 6.0 * n * dk * dv
+    return {"tokens_per_s": world * B * L / t, "ms_per_step": t * 1e3,
+            "roofline": {"bound": "hbm", "frac": t_roof / t, "algorithmic_bytes": bytes_,
+                         "tensor_tflops": flops / t / 1e12},
+            "recurrent": {"ms_per_step": tr * 1e3, "tflops": rflops / tr / 1e12,
+                          "frac_of_fp32_fma": rflops / tr / 1e12 / fma_peak},
+            "workload": "delta rule: B=8, H=16, L=4096, d=128 bf16, unit q/k, beta=sigmoid(N(0,1))"}
 
 
 def bench_bwd(name, steps, warmup, world, pk):
@@ -514,7 +528,7 @@ def main():
     if args.only:
         name = args.only
         if name == "delta":
-            r = bench_delta(args.steps, warmup, world)
+            r = bench_delta(args.steps, warmup, world, pk)
         elif name.endswith("_bwd"):
             r = bench_bwd(name[:-4], args.steps, warmup, world, pk)
         else:
@@ -540,7 +554,7 @@ def main():
                            "gbs": r["gbs"], "roofline_frac": r["roofline_frac"],
                            "launches_per_step": r["launches_per_step"]}
             torch.cuda.empty_cache()
-        extra["delta"] = bench_delta(max(3, args.steps // 4), 2, world)
+        extra["delta"] = bench_delta(max(3, args.steps // 4), 3, world, pk)
         torch.cuda.empty_cache()
         for name, st in (("retention", max(5, args.steps // 4)), ("la", 3), ("gla", 2)):
             extra[name + "_bwd"] = bench_bwd(name, st, 1 if name == "gla" else 3, world, pk)
