@@ -573,6 +573,126 @@ __global__ void __launch_bounds__(kEw) bwd_post_kernel(const uint4 *q, const uin
     }
 }
 
+// ---------------------------------------------------------------- tensor-core route, normalised
+// With the normaliser (w_t = dout_t / den_t, e_t = -(Q_t . S_t w_t) / den_t):
+//   den_t = Q_t . z_t                   = fwd(Q, K, 1)            (every column)
+//   U_t   = S_t w_t                     = fwd(w, v, K)
+//   z_t e_t                             = fwd(E, J, K)            E_t = (e_t hi, e_t lo, 0 ..), J_s = (1, 1, 0 ..)
+//   dK_s  = sum_{t>=s} Q_t (v_s . w_t) + sum_{t>=s} Q_t e_t
+//         = rev fwd(rev v, rev w, rev Q) + rev fwd(J, rev E, rev Q)
+//   dv_s  = rev fwd(rev K, rev Q, rev w)
+//   dQ_t  = U_t + z_t e_t
+// dQ and dK are differences of nearly equal terms, so those forwards write
+// fp32 and e_t travels as two bf16 parts (hi + lo).
+constexpr int CPR = kD / 8;  // 16-byte chunks per row
+
+__device__ __forceinline__ long rev_chunk(long x, int L) {
+    const long row = x / CPR;
+    const int c = (int)(x % CPR), t = (int)(row % L);
+    return (row - t + (L - 1 - t)) * CPR + c;
+}
+
+// Q = phi(q), K = phi(k) in order; rev v, rev Q, rev K; the constants 1 and J
+__global__ void __launch_bounds__(kEw) bwdn_prep1_kernel(const uint4 *q, const uint4 *k, const uint4 *v, uint4 *Qf,
+                                                         uint4 *Kf, uint4 *rv, uint4 *rq, uint4 *rk, uint4 *ones,
+                                                         uint4 *J, long rows, int L, bool elu1) {
+    const long n = rows * CPR;
+    const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 twice
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long rr = rev_chunk(x, L);
+        const uint4 qq = phi8(__ldcs(q + x), elu1), kk = phi8(__ldcs(k + x), elu1);
+        Qf[x] = qq;
+        Kf[x] = kk;
+        rq[rr] = qq;
+        rk[rr] = kk;
+        rv[rr] = __ldcs(v + x);
+        ones[x] = make_uint4(one2, one2, one2, one2);
+        J[x] = (x % CPR) == 0 ? make_uint4(one2, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// w = dout / den (den from column 0 of the fp32 forward with unit values), in order and reversed
+__global__ void __launch_bounds__(kEw) bwdn_prep2_kernel(const uint4 *d, const float *den_full, uint4 *w, uint4 *rw,
+                                                         float *den, long rows, int L) {
+    const long n = rows * CPR;
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long row = x / CPR;
+        const float dn = den_full[row * kD];
+        if (x % CPR == 0) den[row] = dn;
+        const float r = 1.f / dn;
+        const uint4 g = __ldcs(d + x);
+        uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(gw[i] << 16) * r, __uint_as_float(gw[i] & 0xffff0000u) * r);
+            gw[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        const uint4 o = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+        w[x] = o;
+        rw[rev_chunk(x, L)] = o;
+    }
+}
+
+// e_t = -(Q_t . U_t) / den_t, one warp per token; E_t = (hi, lo, 0 ..) in order and reversed
+__global__ void __launch_bounds__(kEw) bwdn_prep3_kernel(const uint4 *Qf, const float *U, const float *den, uint4 *E,
+                                                         uint4 *rE, long rows, int L) {
+    const long row = ((long)blockIdx.x * kEw + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    // lane covers columns 4 lane .. 4 lane + 3
+    const uint2 qq = reinterpret_cast<const uint2 *>(Qf + row * CPR)[lane];
+    const float4 uu = reinterpret_cast<const float4 *>(U + row * kD)[lane];
+    float sdot = __uint_as_float(qq.x << 16) * uu.x + __uint_as_float(qq.x & 0xffff0000u) * uu.y +
+                 __uint_as_float(qq.y << 16) * uu.z + __uint_as_float(qq.y & 0xffff0000u) * uu.w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, off);
+    const float e = -sdot / den[row];
+    if (lane < CPR) {
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (lane == 0) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(e);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(e - __bfloat162float(hi));
+            __nv_bfloat162 h2;
+            h2.x = hi;
+            h2.y = lo;
+            o.x = *reinterpret_cast<uint32_t *>(&h2);
+        }
+        const long x = row * CPR + lane;
+        E[x] = o;
+        rE[rev_chunk(x, L)] = o;
+    }
+}
+
+// dq = (U + ZE) phi'(q), dk = rev(rdKm + rdz) phi'(k), dv = rev(rdv)
+__global__ void __launch_bounds__(kEw) bwdn_post_kernel(const uint4 *q, const uint4 *k, const float4 *U,
+                                                        const float4 *ZE, const float4 *rdkm, const float4 *rdz,
+                                                        const uint4 *rdv, uint4 *dq, uint4 *dk, uint4 *dv, long rows,
+                                                        int L, bool elu1) {
+    const long n = rows * CPR;
+    auto combine = [elu1](float4 a0, float4 a1, float4 b0, float4 b1, uint4 x) {
+        const float g[8] = {a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w,
+                            a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w};
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xffff0000u);
+            const float g0 = (elu1 && x0 <= 0.f) ? g[2 * i] * __expf(x0) : g[2 * i];
+            const float g1 = (elu1 && x1 <= 0.f) ? g[2 * i + 1] * __expf(x1) : g[2 * i + 1];
+            __nv_bfloat162 h = __floats2bfloat162_rn(g0, g1);
+            o[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long rr = rev_chunk(x, L);
+        dq[x] = combine(__ldcs(U + 2 * x), __ldcs(U + 2 * x + 1), __ldcs(ZE + 2 * x), __ldcs(ZE + 2 * x + 1), __ldg(q + x));
+        dk[x] = combine(__ldcs(rdkm + 2 * rr), __ldcs(rdkm + 2 * rr + 1), __ldcs(rdz + 2 * rr), __ldcs(rdz + 2 * rr + 1),
+                        __ldg(k + x));
+        dv[x] = __ldcs(rdv + rr);
+    }
+}
+
 int ew_blocks(long n) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -584,13 +704,72 @@ int ew_blocks(long n) {
 }  // namespace
 
 bool bwd_tc_supports(const BwdArgs &a) {
-    if (a.mode & (LA_DTYPE_F32 | LA_NORMALIZE | LA_GATE_CHANNEL)) return false;
+    if (a.mode & (LA_DTYPE_F32 | LA_GATE_CHANNEL)) return false;
     if (a.dk != kD || a.dv != kD || a.L < 1) return false;
     ChunkArgs c{a.q, a.k, a.v, a.gate, nullptr, nullptr, a.B, a.H, a.L, kD, kD, a.mode & LA_GATE_HEAD, 64, nullptr};
     return chunk_tc_supports(c);
 }
 
+int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
+    const long rows = (long)a.B * a.H * a.L;
+    const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16), fb = 2 * hb;
+    // bf16: Q K 1 J w E rv rw rq rk rE rdv; fp32: den_full U ZE rdkm rdz; den [rows]
+    const size_t bytes = 12 * hb + 5 * fb + (size_t)rows * sizeof(float);
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    char *b = static_cast<char *>(scratch);
+    uint4 *h[12];
+    for (int i = 0; i < 12; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
+    uint4 *Qf = h[0], *Kf = h[1], *ones = h[2], *J = h[3], *w = h[4], *E = h[5], *rv = h[6], *rw = h[7], *rq = h[8],
+          *rk = h[9], *rE = h[10], *rdv = h[11];
+    float *f[5];
+    for (int i = 0; i < 5; ++i) f[i] = reinterpret_cast<float *>(b + 12 * hb + i * fb);
+    float *den_full = f[0], *U = f[1], *ZE = f[2], *rdkm = f[3], *rdz = f[4];
+    float *den = reinterpret_cast<float *>(b + 12 * hb + 5 * fb);
+    const bool elu1 = a.mode & LA_PHI_ELU1;
+    const int mode = a.mode & LA_GATE_HEAD;  // identity feature map, bf16, no normaliser
+    const int nb = ew_blocks(rows * CPR);
+    int rc = LA_OK;
+    auto ok = [&]() {
+        if (rc == LA_OK && cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
+        if (rc == LA_OK) ++*launches;
+    };
+    auto fwd = [&](const void *q, const void *k, const void *v, void *out, bool f32) {
+        if (rc != LA_OK) return;
+        ChunkArgs c{q, k, v, a.gate, out, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr, f32 ? 1 : 0};
+        rc = launch_chunk_tc(c, s, launches);
+    };
+    bwdn_prep1_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
+                                         static_cast<const uint4 *>(a.v), Qf, Kf, rv, rq, rk, ones, J, rows, a.L, elu1);
+    ok();
+    fwd(Qf, Kf, ones, den_full, true);  // den_t in every column
+    if (rc == LA_OK) {
+        bwdn_prep2_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.dout), den_full, w, rw, den, rows, a.L);
+        ok();
+    }
+    fwd(w, a.v, Kf, U, true);  // U_t = S_t w_t
+    if (rc == LA_OK) {
+        bwdn_prep3_kernel<<<(unsigned)((rows + kEw / 32 - 1) / (kEw / 32)), kEw, 0, s>>>(Qf, U, den, E, rE, rows, a.L);
+        ok();
+    }
+    fwd(E, J, Kf, ZE, true);    // z_t e_t
+    fwd(rv, rw, rq, rdkm, true);
+    fwd(J, rE, rq, rdz, true);
+    fwd(rk, rq, rw, rdv, false);
+    if (rc == LA_OK) {
+        bwdn_post_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
+                                            reinterpret_cast<const float4 *>(U), reinterpret_cast<const float4 *>(ZE),
+                                            reinterpret_cast<const float4 *>(rdkm), reinterpret_cast<const float4 *>(rdz),
+                                            rdv, static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k),
+                                            static_cast<uint4 *>(a.grad_v), rows, a.L, elu1);
+        ok();
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
+    return rc;
+}
+
 int launch_bwd_tc(const BwdArgs &a, cudaStream_t s, int *launches) {
+    if (a.mode & LA_NORMALIZE) return launch_bwd_tc_norm(a, s, launches);
     const long rows = (long)a.B * a.H * a.L;
     const size_t arr = (size_t)rows * kD * sizeof(__nv_bfloat16);
     const bool elu1 = a.mode & LA_PHI_ELU1;

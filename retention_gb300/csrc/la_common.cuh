@@ -42,6 +42,7 @@ struct ChunkArgs {
     float *final_state;
     int B, H, L, dk, dv, mode, chunk;
     const float *initial_state;  // [B][H][block] state before the first token, or null (zero)
+    int out_f32;                 // tensor-core path only: out is fp32 (identity phi, no normaliser, no channel gate)
 };
 
 struct GnArgs {

@@ -97,7 +97,7 @@ constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
 // remaining blocks in order. The gate tiles g have a ring of their own (GR):
 // the prologue is done with g after its first pass, so g is released early
 // and the next chunk's g is already in place when the prologue turns to it.
-template <int GATE, bool NORM, bool SO>
+template <int GATE, bool NORM, bool SO, bool OF32 = false>
 struct Layout {
     static constexpr bool GR = GATE == 2 && !SO;
     // gated without the normaliser: three q|k|v stages and one gate slot fit;
@@ -124,13 +124,13 @@ struct Layout {
     static constexpr uint32_t Gring = stages;                              // [NG] g tiles
     static constexpr uint32_t P = Gring + NG * kTile;                      // bf16 P tile, 8 KiB
     static constexpr uint32_t S = P + (SO ? 0 : 8192);                     // bf16 S_{n-1} (+ z atom), 32 / 48 KiB
-    static constexpr uint32_t O = S + (SO ? 0 : (NORM ? 49152 : 32768));   // bf16 O staging, two swizzled halves
+    static constexpr uint32_t O = S + (SO ? 0 : (NORM ? 49152 : 32768));   // O staging: bf16 halves or fp32 quarters
     // floats: ffinal[128], then with a gate fbuf[NF][128], with the head gate
     // fq[64] fk[64], with the channel gate tot[4][128]. fbuf is a ring of
     // NF = NS + 1 slots: chunk n's decay factor goes to slot n % NF at the end of
     // its prologue, for the state chain to rescale T_n with.
     static constexpr int NF = NS + 1;
-    static constexpr uint32_t F = O + (SO ? 0 : 16384);
+    static constexpr uint32_t F = O + (SO ? 0 : (OF32 ? 32768 : 16384));
     static constexpr uint32_t nfbuf = GATE != 0 ? NF * 128 : 0, nfq = GATE == 1 ? 128 : 0;
     static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + (GATE == 2 ? 512 : 0)) * 4;
     // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal,
@@ -192,9 +192,9 @@ __device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
 // SO (state only): the first pass over a split sequence. Each CTA runs one
 // segment from a zero state and keeps only the state update (no QK, no
 // outputs): it writes the segment's end state and its total log decay.
-template <int GATE, bool ELU1, bool NORM, bool SO>
+template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
-    using LY = Layout<GATE, NORM, SO>;
+    using LY = Layout<GATE, NORM, SO, OF32>;
     constexpr int NS = LY::NS;
     constexpr int NG = LY::GR ? LY::NG : 1;  // gate ring slots (the ring exists only if GR)
     extern __shared__ uint8_t smem_raw[];
@@ -820,17 +820,27 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 uint32_t r[32];
                 tmem_ld32(tO + 32 * j, r);
                 tmem_ld_wait();
-                // staging: two [64 x 64] halves with the 128-byte swizzle (TMA store box 64 x 64)
-                uint8_t *row = sO + (j >> 1) * 8192 + t * 128;
+                if constexpr (OF32) {
+                    // staging: four [64 x 32] fp32 quarters with the 128-byte swizzle (box 32 x 64)
+                    uint8_t *row = sO + j * 8192 + t * 128;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int lc = 4 * (j & 1) + q4;
-                    uint4 w;
-                    w.x = pack_bf16(__uint_as_float(r[8 * q4 + 0]) * rden, __uint_as_float(r[8 * q4 + 1]) * rden);
-                    w.y = pack_bf16(__uint_as_float(r[8 * q4 + 2]) * rden, __uint_as_float(r[8 * q4 + 3]) * rden);
-                    w.z = pack_bf16(__uint_as_float(r[8 * q4 + 4]) * rden, __uint_as_float(r[8 * q4 + 5]) * rden);
-                    w.w = pack_bf16(__uint_as_float(r[8 * q4 + 6]) * rden, __uint_as_float(r[8 * q4 + 7]) * rden);
-                    *reinterpret_cast<uint4 *>(row + ((lc ^ (t & 7)) << 4)) = w;
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4 *>(row + ((c ^ (t & 7)) << 4)) = make_uint4(
+                            __float_as_uint(__uint_as_float(r[4 * c]) * rden), __float_as_uint(__uint_as_float(r[4 * c + 1]) * rden),
+                            __float_as_uint(__uint_as_float(r[4 * c + 2]) * rden), __float_as_uint(__uint_as_float(r[4 * c + 3]) * rden));
+                } else {
+                    // staging: two [64 x 64] halves with the 128-byte swizzle (TMA store box 64 x 64)
+                    uint8_t *row = sO + (j >> 1) * 8192 + t * 128;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int lc = 4 * (j & 1) + q4;
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(r[8 * q4 + 0]) * rden, __uint_as_float(r[8 * q4 + 1]) * rden);
+                        w.y = pack_bf16(__uint_as_float(r[8 * q4 + 2]) * rden, __uint_as_float(r[8 * q4 + 3]) * rden);
+                        w.z = pack_bf16(__uint_as_float(r[8 * q4 + 4]) * rden, __uint_as_float(r[8 * q4 + 5]) * rden);
+                        w.w = pack_bf16(__uint_as_float(r[8 * q4 + 6]) * rden, __uint_as_float(r[8 * q4 + 7]) * rden);
+                        *reinterpret_cast<uint4 *>(row + ((lc ^ (t & 7)) << 4)) = w;
+                    }
                 }
             }
             tc_fence_before();
@@ -838,8 +848,13 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             fence_proxy_async_smem();
             named_sync<kBarOut, 64>();
             if (t == 0) {
-                tma_store_3d(&p.to, sO, 0, t0, bh);
-                tma_store_3d(&p.to, sO + 8192, 64, t0, bh);
+                if constexpr (OF32) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tma_store_3d(&p.to, sO + j * 8192, 32 * j, t0, bh);
+                } else {
+                    tma_store_3d(&p.to, sO, 0, t0, bh);
+                    tma_store_3d(&p.to, sO + 8192, 64, t0, bh);
+                }
                 bulk_commit();
             }
         }
@@ -886,6 +901,19 @@ bool make_map(CUtensorMap *m, const void *base, int L, int BH) {
     return r == CUDA_SUCCESS;
 }
 
+// fp32 [BH][L][128] as {128, L, BH}; box {32, 64, 1} (128 bytes inner) with
+// the 128-byte swizzle: the output map of the fp32-output instances.
+bool make_map_f32(CUtensorMap *m, const void *base, int L, int BH) {
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)L * kD * 4};
+    cuuint32_t box[3] = {32, (cuuint32_t)kC, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Segment scan: S_in(0) = S_0 (the initial state, or 0), S_in(p+1) =
 // diag(e^{B_p}) S_in(p) + dS_p, and the state after the last segment is the
 // final state. One thread per state element (z included), a sequential loop
@@ -908,12 +936,12 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
     if (final_state) final_state[(size_t)bh * blk + e] = acc;
 }
 
-template <int GATE, bool ELU1, bool NORM, bool SO>
+template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false>
 int launch_t(const TcParams &prm, int grid, cudaStream_t s) {
-    using LY = Layout<GATE, NORM, SO>;
+    using LY = Layout<GATE, NORM, SO, OF32>;
     static_assert(LY::NS >= 2 && LY::bytes <= kSmemBudget, "shared memory budget");
     static_assert(LY::colP + 64 <= kTmemCols && LY::colO1 + LY::NW <= LY::colP, "TMEM budget");
-    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO>;
+    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO, OF32>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes) != cudaSuccess)
         return LA_ERR_CUDA;
     kern<<<grid, kThreads, LY::bytes, s>>>(prm);
@@ -928,8 +956,14 @@ int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm
 }
 
 template <bool SO>
-int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode) {
+int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false) {
     const bool elu1 = mode & LA_PHI_ELU1, norm = mode & LA_NORMALIZE;
+    if (out_f32 && !SO) {
+        // fp32 output: identity feature map, no normaliser, no gate or the head gate
+        if (elu1 || norm || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
+        return (mode & LA_GATE_HEAD) ? launch_t<1, false, false, false, true>(prm, grid, s)
+                                     : launch_t<0, false, false, false, true>(prm, grid, s);
+    }
     if (mode & LA_GATE_CHANNEL) return launch_g<2, SO>(prm, grid, s, elu1, norm);
     if (mode & LA_GATE_HEAD) return launch_g<1, SO>(prm, grid, s, elu1, norm);
     return launch_g<0, SO>(prm, grid, s, elu1, norm);
@@ -988,8 +1022,8 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     const int nchunks = (a.L + kC - 1) / kC;
     TcParams prm;
     memset(&prm, 0, sizeof(prm));
-    if (!make_map(&prm.tq, a.q, a.L, BH) || !make_map(&prm.tk, a.k, a.L, BH) ||
-        !make_map(&prm.tv, a.v, a.L, BH) || !make_map(&prm.to, a.out, a.L, BH))
+    if (!make_map(&prm.tq, a.q, a.L, BH) || !make_map(&prm.tk, a.k, a.L, BH) || !make_map(&prm.tv, a.v, a.L, BH) ||
+        !(a.out_f32 ? make_map_f32(&prm.to, a.out, a.L, BH) : make_map(&prm.to, a.out, a.L, BH)))
         return LA_ERR_CUDA;
     if ((a.mode & LA_GATE_CHANNEL) && !make_map(&prm.tg, a.gate, a.L, BH)) return LA_ERR_CUDA;
     prm.gamma = (a.mode & LA_GATE_HEAD) ? static_cast<const float *>(a.gate) : nullptr;
@@ -1001,7 +1035,7 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.init0 = a.initial_state != nullptr;
     if (prm.nseg == 1) {
         prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
-        const int rc = launch_mode<false>(prm, BH, s, a.mode);
+        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32);
         if (rc == LA_OK) *launches += 1;
         return rc;
     }
@@ -1024,7 +1058,7 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.state_in = state_in;
     prm.seg_state = nullptr;
     prm.seg_logdecay = nullptr;
-    rc = launch_mode<false>(prm, (int)nsb, s, a.mode);
+    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32);
     if (rc == LA_OK) *launches += 1;
     return rc;
 }
