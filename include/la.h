@@ -232,7 +232,7 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
  * No gradient flows into a final state or out of an initial one. Scratch,
  * taken stream-ordered with cudaMallocAsync on `stream` (LA_ERR_CUDA if that
  * fails): on the tensor-core route six (eight with LA_PHI_ELU1) bf16
- * [B][H][L][128] arrays, or with LA_NORMALIZE twelve bf16 and five fp32 ones;
+ * [B][H][L][128] arrays, or with LA_NORMALIZE eleven bf16 and five fp32 ones;
  * on the other one fp32 [B][H][L][d_k] array (two, plus three [B][H][L], with
  * LA_NORMALIZE).
  * Errors as la_chunk_fwd; no output may overlap an input.

@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kEw) bwd_post_kernel(const uint4 *q, const uin
 
 // ---------------------------------------------------------------- tensor-core route, normalised
 // With the normaliser (w_t = dout_t / den_t, e_t = -(Q_t . S_t w_t) / den_t):
-//   den_t = Q_t . z_t                   = fwd(Q, K, 1)            (every column)
+//   den_t = Q_t . z_t                   = fwd(Q, K, J)            (columns 0 and 1)
 //   U_t   = S_t w_t                     = fwd(w, v, K)
 //   z_t e_t                             = fwd(E, J, K)            E_t = (e_t hi, e_t lo, 0 ..), J_s = (1, 1, 0 ..)
 //   dK_s  = sum_{t>=s} Q_t (v_s . w_t) + sum_{t>=s} Q_t e_t
@@ -592,10 +592,10 @@ __device__ __forceinline__ long rev_chunk(long x, int L) {
     return (row - t + (L - 1 - t)) * CPR + c;
 }
 
-// Q = phi(q), K = phi(k) in order; rev v, rev Q, rev K; the constants 1 and J
+// Q = phi(q), K = phi(k) in order; rev v, rev Q, rev K; the constant J
 __global__ void __launch_bounds__(kEw) bwdn_prep1_kernel(const uint4 *q, const uint4 *k, const uint4 *v, uint4 *Qf,
-                                                         uint4 *Kf, uint4 *rv, uint4 *rq, uint4 *rk, uint4 *ones,
-                                                         uint4 *J, long rows, int L, bool elu1) {
+                                                         uint4 *Kf, uint4 *rv, uint4 *rq, uint4 *rk, uint4 *J,
+                                                         long rows, int L, bool elu1) {
     const long n = rows * CPR;
     const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 twice
     for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
@@ -606,12 +606,11 @@ __global__ void __launch_bounds__(kEw) bwdn_prep1_kernel(const uint4 *q, const u
         rq[rr] = qq;
         rk[rr] = kk;
         rv[rr] = __ldcs(v + x);
-        ones[x] = make_uint4(one2, one2, one2, one2);
         J[x] = (x % CPR) == 0 ? make_uint4(one2, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-// w = dout / den (den from column 0 of the fp32 forward with unit values), in order and reversed
+// w = dout / den (den from column 0 of the fp32 forward with values J), in order and reversed
 __global__ void __launch_bounds__(kEw) bwdn_prep2_kernel(const uint4 *d, const float *den_full, uint4 *w, uint4 *rw,
                                                          float *den, long rows, int L) {
     const long n = rows * CPR;
@@ -713,19 +712,19 @@ bool bwd_tc_supports(const BwdArgs &a) {
 int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
     const long rows = (long)a.B * a.H * a.L;
     const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16), fb = 2 * hb;
-    // bf16: Q K 1 J w E rv rw rq rk rE rdv; fp32: den_full U ZE rdkm rdz; den [rows]
-    const size_t bytes = 12 * hb + 5 * fb + (size_t)rows * sizeof(float);
+    // bf16: Q K J w E rv rw rq rk rE rdv; fp32: den_full U ZE rdkm rdz; den [rows]
+    const size_t bytes = 11 * hb + 5 * fb + (size_t)rows * sizeof(float);
     void *scratch = nullptr;
     if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
     char *b = static_cast<char *>(scratch);
-    uint4 *h[12];
-    for (int i = 0; i < 12; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
-    uint4 *Qf = h[0], *Kf = h[1], *ones = h[2], *J = h[3], *w = h[4], *E = h[5], *rv = h[6], *rw = h[7], *rq = h[8],
-          *rk = h[9], *rE = h[10], *rdv = h[11];
+    uint4 *h[11];
+    for (int i = 0; i < 11; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
+    uint4 *Qf = h[0], *Kf = h[1], *J = h[2], *w = h[3], *E = h[4], *rv = h[5], *rw = h[6], *rq = h[7], *rk = h[8],
+          *rE = h[9], *rdv = h[10];
     float *f[5];
-    for (int i = 0; i < 5; ++i) f[i] = reinterpret_cast<float *>(b + 12 * hb + i * fb);
+    for (int i = 0; i < 5; ++i) f[i] = reinterpret_cast<float *>(b + 11 * hb + i * fb);
     float *den_full = f[0], *U = f[1], *ZE = f[2], *rdkm = f[3], *rdz = f[4];
-    float *den = reinterpret_cast<float *>(b + 12 * hb + 5 * fb);
+    float *den = reinterpret_cast<float *>(b + 11 * hb + 5 * fb);
     const bool elu1 = a.mode & LA_PHI_ELU1;
     const int mode = a.mode & LA_GATE_HEAD;  // identity feature map, bf16, no normaliser
     const int nb = ew_blocks(rows * CPR);
@@ -740,9 +739,9 @@ int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
         rc = launch_chunk_tc(c, s, launches);
     };
     bwdn_prep1_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
-                                         static_cast<const uint4 *>(a.v), Qf, Kf, rv, rq, rk, ones, J, rows, a.L, elu1);
+                                         static_cast<const uint4 *>(a.v), Qf, Kf, rv, rq, rk, J, rows, a.L, elu1);
     ok();
-    fwd(Qf, Kf, ones, den_full, true);  // den_t in every column
+    fwd(Qf, Kf, J, den_full, true);  // den_t in columns 0 and 1
     if (rc == LA_OK) {
         bwdn_prep2_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.dout), den_full, w, rw, den, rows, a.L);
         ok();
