@@ -692,6 +692,132 @@ __global__ void __launch_bounds__(kEw) bwdn_post_kernel(const uint4 *q, const ui
     }
 }
 
+// ---------------------------------------------------------------- tensor-core route, per-channel gate
+// With the gate diag(alpha_t) on the key channels (B_t = sum_{r<=t} log alpha_r):
+//   dv_s    = sum_{t>=s} (Q_t . K_s e^{B_t - B_s}) dout_t        = rev fwd_key(rev K, rev Q, rev dout; g')
+//   dQ_t[i] = sum_{s<=t} e^{B_t[i] - B_s[i]} K_s[i] (dout_t . v_s)  = fwd_value(dout, v, K; g)
+//   dK_s[i] = sum_{t>=s} e^{B_t[i] - B_s[i]} Q_t[i] (v_s . dout_t)  = rev fwd_value(rev v, rev dout, rev Q; g')
+// fwd_value is the forward with the decay on the value channels (the kernel
+// writes it without the factor e^{b_t}, b the log decay since the chunk start,
+// which the passes after apply). g' is g reversed and shifted by one token
+// (g'_u = g_{L-u}; g'_0 decays nothing), so the reversed forwards take the
+// same gate products. Then dg_r = sigmoid(-g_r) / 16 sum_{t>=r} (Q dQ - K dK)_t
+// by a segmented reverse scan over chunks of 64 tokens.
+constexpr float kNoDecay = 3.0e38f;  // a gate value whose alpha is 1
+
+__device__ __forceinline__ float bf16_at(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
+
+// K = phi(k) in order; rev v, rev dout, rev phi(q), rev phi(k), and g'
+__global__ void __launch_bounds__(kEw) bwdg_prep_kernel(const uint4 *q, const uint4 *k, const uint4 *v, const uint4 *d,
+                                                        const uint4 *g, uint4 *Kf, uint4 *rv, uint4 *rd, uint4 *rq,
+                                                        uint4 *rk, uint4 *rg, long rows, int L, bool elu1) {
+    const long n = rows * CPR;
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long row = x / CPR;
+        const int c = (int)(x % CPR), t = (int)(row % L);
+        const long rr = rev_chunk(x, L);
+        const uint4 kk = phi8(__ldcs(k + x), elu1);
+        Kf[x] = kk;
+        rk[rr] = kk;
+        rq[rr] = phi8(__ldcs(q + x), elu1);
+        rv[rr] = __ldcs(v + x);
+        rd[rr] = __ldcs(d + x);
+        // g at token t goes to reversed token L - t; reversed token 0 decays nothing
+        const long base = (row - t) * CPR;
+        if (t >= 1) rg[base + (long)(L - t) * CPR + c] = __ldcs(g + x);
+        else {
+            __nv_bfloat162 h = __floats2bfloat162_rn(kNoDecay, kNoDecay);
+            const uint32_t w = *reinterpret_cast<uint32_t *>(&h);
+            rg[base + c] = make_uint4(w, w, w, w);
+        }
+    }
+}
+
+// dQ_t = e^{b_t} * bracket_t (chunks of 64 from token 0); dq = dQ phi'(q); dQ kept (fp32) for dg.
+// One thread per (sequence, chunk, channel), walking the chunk's tokens.
+__global__ void __launch_bounds__(kEw) bwdg_postq_kernel(const __nv_bfloat16 *q, const __nv_bfloat16 *g,
+                                                         const __nv_bfloat16 *br, __nv_bfloat16 *dq, float *dQ,
+                                                         long nbh, int L, bool elu1) {
+    const int nch = (L + 63) / 64;
+    const long x = (long)blockIdx.x * kEw + threadIdx.x;
+    if (x >= nbh * nch * kD) return;
+    const int i = (int)(x % kD), c = (int)((x / kD) % nch);
+    const long bh = x / kD / nch;
+    float b = 0.f;
+    for (int t = 64 * c; t < min(L, 64 * c + 64); ++t) {
+        const size_t o = ((size_t)bh * L + t) * kD + i;
+        b += channel_log_decay(bf16_at(g, o));
+        const float v = __expf(b) * bf16_at(br, o);
+        dQ[o] = v;
+        dq[o] = __float2bfloat16_rn(v * dphi(bf16_at(q, o), elu1));
+    }
+}
+
+// dK (reversed chunks of 64 from reversed token 0, gate g'), un-reversed:
+// dk = dK phi'(k); dv un-reversed; r = phi(q) dQ - phi(k) dK in place of dQ.
+__global__ void __launch_bounds__(kEw) bwdg_postk_kernel(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                                                         const __nv_bfloat16 *rg, const __nv_bfloat16 *rbr,
+                                                         const __nv_bfloat16 *rdv, __nv_bfloat16 *dk,
+                                                         __nv_bfloat16 *dv, float *r, long nbh, int L, bool elu1) {
+    const int nch = (L + 63) / 64;
+    const long x = (long)blockIdx.x * kEw + threadIdx.x;
+    if (x >= nbh * nch * kD) return;
+    const int i = (int)(x % kD), c = (int)((x / kD) % nch);
+    const long bh = x / kD / nch;
+    float b = 0.f;
+    for (int u = 64 * c; u < min(L, 64 * c + 64); ++u) {
+        const size_t ou = ((size_t)bh * L + u) * kD + i, ot = ((size_t)bh * L + (L - 1 - u)) * kD + i;
+        b += channel_log_decay(bf16_at(rg, ou));
+        const float dK = __expf(b) * bf16_at(rbr, ou);
+        const float kx = bf16_at(k, ot), qx = bf16_at(q, ot);
+        dk[ot] = __float2bfloat16_rn(dK * dphi(kx, elu1));
+        dv[ot] = rdv[ou];
+        r[ot] = phi(qx, elu1) * r[ot] - phi(kx, elu1) * dK;
+    }
+}
+
+// chunk totals of r, then (one thread per sequence and channel) the sums over
+// all later chunks, then dg = sigmoid(-g) / 16 (later chunks + the chunk's tail)
+__global__ void __launch_bounds__(kEw) bwdg_tot_kernel(const float *r, float *tot, long nbh, int L) {
+    const int nch = (L + 63) / 64;
+    const long x = (long)blockIdx.x * kEw + threadIdx.x;
+    if (x >= nbh * nch * kD) return;
+    const int i = (int)(x % kD), c = (int)((x / kD) % nch);
+    const long bh = x / kD / nch;
+    float s = 0.f;
+    for (int t = 64 * c; t < min(L, 64 * c + 64); ++t) s += r[((size_t)bh * L + t) * kD + i];
+    tot[x] = s;
+}
+__global__ void __launch_bounds__(kEw) bwdg_carry_kernel(float *tot, long nbh, int L) {
+    const int nch = (L + 63) / 64;
+    const long x = (long)blockIdx.x * kEw + threadIdx.x;
+    if (x >= nbh * kD) return;
+    const int i = (int)(x % kD);
+    const long bh = x / kD;
+    float acc = 0.f;
+    for (int c = nch - 1; c >= 0; --c) {
+        float *p = tot + ((size_t)bh * nch + c) * kD + i;
+        const float v = *p;
+        *p = acc;  // the sum over chunks after c
+        acc += v;
+    }
+}
+__global__ void __launch_bounds__(kEw) bwdg_dg_kernel(const float *r, const float *carry, const __nv_bfloat16 *g,
+                                                      __nv_bfloat16 *dg, long nbh, int L) {
+    const int nch = (L + 63) / 64;
+    const long x = (long)blockIdx.x * kEw + threadIdx.x;
+    if (x >= nbh * nch * kD) return;
+    const int i = (int)(x % kD), c = (int)((x / kD) % nch);
+    const long bh = x / kD / nch;
+    float acc = carry[x];
+    for (int t = min(L, 64 * c + 64) - 1; t >= 64 * c; --t) {
+        const size_t o = ((size_t)bh * L + t) * kD + i;
+        acc += r[o];
+        const float gx = bf16_at(g, o);
+        dg[o] = __float2bfloat16_rn(acc * 0.0625f / (1.f + __expf(fminf(gx, 80.f))));
+    }
+}
+
 int ew_blocks(long n) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -703,10 +829,75 @@ int ew_blocks(long n) {
 }  // namespace
 
 bool bwd_tc_supports(const BwdArgs &a) {
-    if (a.mode & (LA_DTYPE_F32 | LA_GATE_CHANNEL)) return false;
+    if (a.mode & LA_DTYPE_F32) return false;
+    if ((a.mode & LA_GATE_CHANNEL) && (a.mode & LA_NORMALIZE)) return false;
     if (a.dk != kD || a.dv != kD || a.L < 1) return false;
     ChunkArgs c{a.q, a.k, a.v, a.gate, nullptr, nullptr, a.B, a.H, a.L, kD, kD, a.mode & LA_GATE_HEAD, 64, nullptr};
     return chunk_tc_supports(c);
+}
+
+int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) {
+    const long nbh = (long)a.B * a.H, rows = nbh * a.L;
+    const int nch = (a.L + 63) / 64;
+    const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16);
+    // bf16: K rv rd rq rk g' bracket_q bracket_k rdv; fp32: dQ / r; chunk totals
+    const size_t bytes = 9 * hb + 2 * hb + (size_t)nbh * nch * kD * sizeof(float);
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    char *b = static_cast<char *>(scratch);
+    uint4 *h[9];
+    for (int i = 0; i < 9; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
+    uint4 *Kf = h[0], *rv = h[1], *rd = h[2], *rq = h[3], *rk = h[4], *rg = h[5], *brq = h[6], *brk = h[7], *rdv = h[8];
+    float *rf = reinterpret_cast<float *>(b + 9 * hb), *tot = reinterpret_cast<float *>(b + 11 * hb);
+    const bool elu1 = a.mode & LA_PHI_ELU1;
+    int rc = LA_OK;
+    auto ok = [&]() {
+        if (rc == LA_OK && cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
+        if (rc == LA_OK) ++*launches;
+    };
+    auto fwd = [&](const void *q, const void *k, const void *v, const void *g, void *out, bool value_side) {
+        if (rc != LA_OK) return;
+        ChunkArgs c{q, k, v, g, out, nullptr, a.B, a.H, a.L, kD, kD, LA_GATE_CHANNEL, 64, nullptr, 0, value_side ? 1 : 0};
+        rc = launch_chunk_tc(c, s, launches);
+    };
+    using bf = __nv_bfloat16;
+    bwdg_prep_kernel<<<ew_blocks(rows * CPR), kEw, 0, s>>>(
+        static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), static_cast<const uint4 *>(a.v),
+        static_cast<const uint4 *>(a.dout), static_cast<const uint4 *>(a.gate), Kf, rv, rd, rq, rk, rg, rows, a.L, elu1);
+    ok();
+    fwd(a.dout, a.v, Kf, a.gate, brq, true);  // dQ without e^{b_t}
+    fwd(rv, rd, rq, rg, brk, true);           // reversed dK without e^{b'_u}
+    fwd(rk, rq, rd, rg, rdv, false);          // reversed dv
+    const long nt = nbh * nch * kD;
+    const unsigned nbk = (unsigned)((nt + kEw - 1) / kEw);
+    if (rc == LA_OK) {
+        bwdg_postq_kernel<<<nbk, kEw, 0, s>>>(static_cast<const bf *>(a.q), static_cast<const bf *>(a.gate),
+                                              reinterpret_cast<const bf *>(brq), static_cast<bf *>(a.grad_q), rf, nbh,
+                                              a.L, elu1);
+        ok();
+    }
+    if (rc == LA_OK) {
+        bwdg_postk_kernel<<<nbk, kEw, 0, s>>>(static_cast<const bf *>(a.q), static_cast<const bf *>(a.k),
+                                              reinterpret_cast<const bf *>(rg), reinterpret_cast<const bf *>(brk),
+                                              reinterpret_cast<const bf *>(rdv), static_cast<bf *>(a.grad_k),
+                                              static_cast<bf *>(a.grad_v), rf, nbh, a.L, elu1);
+        ok();
+    }
+    if (rc == LA_OK && a.grad_g) {
+        bwdg_tot_kernel<<<nbk, kEw, 0, s>>>(rf, tot, nbh, a.L);
+        ok();
+        if (rc == LA_OK) {
+            bwdg_carry_kernel<<<(unsigned)((nbh * kD + kEw - 1) / kEw), kEw, 0, s>>>(tot, nbh, a.L);
+            ok();
+        }
+        if (rc == LA_OK) {
+            bwdg_dg_kernel<<<nbk, kEw, 0, s>>>(rf, tot, static_cast<const bf *>(a.gate), static_cast<bf *>(a.grad_g),
+                                               nbh, a.L);
+            ok();
+        }
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
+    return rc;
 }
 
 int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
@@ -768,6 +959,7 @@ int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
 }
 
 int launch_bwd_tc(const BwdArgs &a, cudaStream_t s, int *launches) {
+    if (a.mode & LA_GATE_CHANNEL) return launch_bwd_tc_gated(a, s, launches);
     if (a.mode & LA_NORMALIZE) return launch_bwd_tc_norm(a, s, launches);
     const long rows = (long)a.B * a.H * a.L;
     const size_t arr = (size_t)rows * kD * sizeof(__nv_bfloat16);

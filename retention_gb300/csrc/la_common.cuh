@@ -42,7 +42,11 @@ struct ChunkArgs {
     float *final_state;
     int B, H, L, dk, dv, mode, chunk;
     const float *initial_state;  // [B][H][block] state before the first token, or null (zero)
-    int out_f32;                 // tensor-core path only: out is fp32 (identity phi, no normaliser, no channel gate)
+    int out_f32;                 // tensor-core path only: out is fp32 (identity phi, no normaliser)
+    // tensor-core path only, with LA_GATE_CHANNEL: the gate g [B][H][L][dv] decays
+    // the value channels (out_t[j] = sum_s (q_t . k_s) v_s[j] prod alpha[j]);
+    // the kernel writes out_t / e^{b_t}, b_t the log decay since the chunk start
+    int value_gate;
 };
 
 struct GnArgs {

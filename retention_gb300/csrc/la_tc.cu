@@ -99,12 +99,12 @@ constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
 // and the next chunk's g is already in place when the prologue turns to it.
 template <int GATE, bool NORM, bool SO, bool OF32 = false>
 struct Layout {
-    static constexpr bool GR = GATE == 2 && !SO;
+    static constexpr bool GR = GATE >= 2 && !SO;
     // gated without the normaliser: three q|k|v stages and one gate slot fit;
     // with it, two stages and two gate slots
     static constexpr int NG = GR ? (NORM ? 2 : 1) : 0;          // gate ring slots
     // state-only stage: k | v | (ones) | (g)
-    static constexpr uint32_t so_stage = 2 * kTile + (NORM ? kHalf : 0) + (GATE == 2 ? kTile : 0);
+    static constexpr uint32_t so_stage = 2 * kTile + (NORM ? kHalf : 0) + (GATE >= 2 ? kTile : 0);
     // room kept for the float arrays, barriers and alignment slack below
     static constexpr uint32_t kReserve = 8192;
     static constexpr int NS = !SO ? ((NORM && GATE != 0) ? 2 : 3)
@@ -132,7 +132,7 @@ struct Layout {
     static constexpr int NF = NS + 1;
     static constexpr uint32_t F = O + (SO ? 0 : (OF32 ? 32768 : 16384));
     static constexpr uint32_t nfbuf = GATE != 0 ? NF * 128 : 0, nfq = GATE == 1 ? 128 : 0;
-    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + (GATE == 2 ? 512 : 0)) * 4;
+    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + (GATE >= 2 ? 512 : 0)) * 4;
     // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal,
     // drain; gfull, gempty [NG]; ffull [NF]
     static constexpr uint32_t nbar = 3 * NS + 12 + 2 * NG + NF;
@@ -195,6 +195,7 @@ __device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
 template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     using LY = Layout<GATE, NORM, SO, OF32>;
+    static_assert(GATE != 3 || (!ELU1 && !NORM), "the value-side gate takes features as given, no normaliser");
     constexpr int NS = LY::NS;
     constexpr int NG = LY::GR ? LY::NG : 1;  // gate ring slots (the ring exists only if GR)
     extern __shared__ uint8_t smem_raw[];
@@ -261,15 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         mbar_init(sdone, 1);
         mbar_init(sfree, 1);
         mbar_init(sready, 128);
-        mbar_init(profinal, GATE == 2 ? 64 : 128);
-        for (int j = 0; j < NF; ++j) mbar_init(&ffull[j], GATE == 2 ? 64 : 128);
+        mbar_init(profinal, GATE >= 2 ? 64 : 128);
+        for (int j = 0; j < NF; ++j) mbar_init(&ffull[j], GATE >= 2 ? 64 : 128);
         mbar_init(drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
         tma_prefetch_desc(&p.tk);
         tma_prefetch_desc(&p.tv);
         tma_prefetch_desc(&p.to);
-        if (GATE == 2) tma_prefetch_desc(&p.tg);
+        if (GATE >= 2) tma_prefetch_desc(&p.tg);
     }
     if (NORM) {
         // constant blocks: the [64 x 64] atom(s) whose column 0 is 1 (the ones
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         // ============================================================ TMA producer
         if (lane == 0) {
             int issued = 0, gissued = 0;
-            constexpr int ntl = (GATE == 2 && !LY::GR) ? 4 : 3;  // q, k, v (, g) tiles of a stage
+            constexpr int ntl = (GATE >= 2 && !LY::GR) ? 4 : 3;  // q, k, v (, g) tiles of a stage
             for (int n = 0; n < N; ++n) {
                 const int s = n % NS;
                 const int t0 = (c0 + n) * kC;
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         // 256 threads in eight warps, two on each SM sub-partition: prologue warp
         // pw = warps 4..7 -> 0..3, warps 0, 1 -> 4, 5, warps 14, 15 -> 6, 7
         const int pw = (warp >= 4 && warp < 8) ? warp - 4 : warp < 2 ? warp + 4 : warp - 8;
-        if constexpr (GATE == 2) {
+        if constexpr (GATE >= 2) {
             // Prologue warp pw takes the channel half ch = pw % 2 and the row
             // quarter qr = pw / 2;
             // lane l owns key channels 64 ch + 2l and 64 ch + 2l + 1 (one bf16x2
@@ -508,12 +509,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     b1 += tt.y;
                 }
                 // pass 2 in two groups of eight rows; the second group's words are
-                // loaded before the first group's results are stored
+                // loaded before the first group's results are stored. With the
+                // gate on the value side (GATE 3) the tile scaled by 2^-b is v's,
+                // and q stays as it is.
+                if constexpr (GATE == 3) sK = sm + tile_half(2, s, ch);
                 uint32_t kw[8], qw[8], kn[8], qn[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     kw[u] = *reinterpret_cast<const uint32_t *>(sK + offw(u));
-                    if (!SO) qw[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(u));
+                    if (!SO && GATE == 2) qw[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(u));
                 }
 #pragma unroll
                 for (int g8 = 0; g8 < 2; ++g8) {
@@ -521,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
                             kn[u] = *reinterpret_cast<const uint32_t *>(sK + offw(8 + u));
-                            if (!SO) qn[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(8 + u));
+                            if (!SO && GATE == 2) qn[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(8 + u));
                         }
                     }
                     uint32_t ko[8], qo[8];
@@ -533,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         uint32_t kx = kw[u];
                         if (ELU1) kx = phi_elu1_bf16x2(kx);
                         ko[u] = 16 * qr + uu < c ? pack_bf16(bf16lo(kx) * ex2f(-b0), bf16hi(kx) * ex2f(-b1)) : 0u;
-                        if (!SO) {
+                        if (!SO && GATE == 2) {
                             uint32_t qx = qw[u];
                             if (ELU1) qx = phi_elu1_bf16x2(qx);
                             qo[u] = pack_bf16(bf16lo(qx) * ex2f(b0), bf16hi(qx) * ex2f(b1));
@@ -542,9 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         *reinterpret_cast<uint32_t *>(sK + offw(8 * g8 + u)) = ko[u];
-                        if (!SO) *reinterpret_cast<uint32_t *>(sQ + offw(8 * g8 + u)) = qo[u];
+                        if (!SO && GATE == 2) *reinterpret_cast<uint32_t *>(sQ + offw(8 * g8 + u)) = qo[u];
                         kw[u] = kn[u];
-                        if (!SO) qw[u] = qn[u];
+                        if (!SO && GATE == 2) qw[u] = qn[u];
                     }
                 }
                 if (qr == 3) {
@@ -701,16 +705,19 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 break;
             }
             tc_fence_after();
-            const float f = GATE != 0 ? fbuf[((n - 1) % NF) * 128 + i] : 1.f;
+            const float *fcol = fbuf + ((n - 1) % NF) * 128;
+            const float f = GATE != 0 ? fcol[i] : 1.f;
             if (GATE != 0) {
-                // S_{n-1} = diag(f) T_{n-1}, in place (z rides in column 128)
+                // S_{n-1} = diag(f) T_{n-1} (key-side gate) or T_{n-1} diag(f)
+                // (value-side gate), in place (z rides in column 128)
 #pragma unroll 1
                 for (int j = 0; j < 4; ++j) {
                     uint32_t r[32];
                     tmem_ld32(tS + 32 * j, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                    for (int e = 0; e < 32; ++e)
+                        r[e] = __float_as_uint(__uint_as_float(r[e]) * (GATE == 3 ? fcol[32 * j + e] : f));
                     tmem_st32(tS + 32 * j, r);
                 }
                 if (NORM) {
@@ -741,7 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             if (named_sync_or<kBarState, 128>(!ok)) {
                 bad = 1;
             } else if (dst != nullptr) {
-                // end state S = diag(e^{b_last}) T (with z in column 128)
+                // end state S = diag(e^{b_last}) T (with z in column 128), or
+                // T diag(e^{b_last}) with the gate on the value side
                 tc_fence_after();
                 const float ff = ffinal[i];
                 float *row = dst + (size_t)i * kD;
@@ -751,10 +759,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     tmem_ld32(tS + 32 * j, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        float f4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) f4[e] = GATE == 3 ? ffinal[32 * j + 4 * q4 + e] : ff;
                         reinterpret_cast<float4 *>(row + 32 * j)[q4] = make_float4(
-                            __uint_as_float(r[4 * q4]) * ff, __uint_as_float(r[4 * q4 + 1]) * ff,
-                            __uint_as_float(r[4 * q4 + 2]) * ff, __uint_as_float(r[4 * q4 + 3]) * ff);
+                            __uint_as_float(r[4 * q4]) * f4[0], __uint_as_float(r[4 * q4 + 1]) * f4[1],
+                            __uint_as_float(r[4 * q4 + 2]) * f4[2], __uint_as_float(r[4 * q4 + 3]) * f4[3]);
+                    }
                 }
                 if (NORM) {
                     uint32_t z;
@@ -922,11 +934,13 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
                                                           const float *__restrict__ seg_logdecay,
                                                           const float *__restrict__ initial,
                                                           float *__restrict__ state_in, float *final_state,
-                                                          int nseg, int blk) {
+                                                          int nseg, int blk, int value_side) {
     const int bh = blockIdx.x;
     const int e = blockIdx.y * blockDim.x + threadIdx.x;
     if (e >= blk) return;
-    const int d = e < kD * kD ? e / kD : e - kD * kD;  // key channel of this element
+    // the gated channel of this element: its key channel (row), or its value
+    // channel (column) with the gate on the value side
+    const int d = e < kD * kD ? (value_side ? e % kD : e / kD) : e - kD * kD;
     const size_t base = (size_t)bh * nseg;
     float acc = initial ? initial[(size_t)bh * blk + e] : 0.f;
     for (int sgi = 0; sgi < nseg; ++sgi) {
@@ -956,8 +970,14 @@ int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm
 }
 
 template <bool SO>
-int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false) {
+int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false, bool value_gate = false) {
     const bool elu1 = mode & LA_PHI_ELU1, norm = mode & LA_NORMALIZE;
+    if (value_gate) {
+        // the per-channel gate on the value side: identity feature map, no
+        // normaliser, bf16 output
+        if (elu1 || norm || !(mode & LA_GATE_CHANNEL) || out_f32) return LA_ERR_INTERNAL;
+        return SO ? launch_t<3, false, false, true>(prm, grid, s) : launch_t<3, false, false, false>(prm, grid, s);
+    }
     if (out_f32 && !SO) {
         // fp32 output: identity feature map, no normaliser, no gate or the head gate
         if (elu1 || norm || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
@@ -1035,7 +1055,7 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.init0 = a.initial_state != nullptr;
     if (prm.nseg == 1) {
         prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
-        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32);
+        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32, a.value_gate);
         if (rc == LA_OK) *launches += 1;
         return rc;
     }
@@ -1048,17 +1068,17 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.seg_state = seg_state;
     prm.seg_logdecay = seg_logdecay;
     prm.final_state = nullptr;
-    int rc = launch_mode<true>(prm, (int)nsb, s, a.mode);
+    int rc = launch_mode<true>(prm, (int)nsb, s, a.mode, false, a.value_gate);
     if (rc != LA_OK) return rc;
     *launches += 1;
     la_seg_scan_kernel<<<dim3((unsigned)BH, (unsigned)((blk + 255) / 256)), 256, 0, s>>>(
-        seg_state, seg_logdecay, a.initial_state, state_in, a.final_state, prm.nseg, (int)blk);
+        seg_state, seg_logdecay, a.initial_state, state_in, a.final_state, prm.nseg, (int)blk, a.value_gate);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     *launches += 1;
     prm.state_in = state_in;
     prm.seg_state = nullptr;
     prm.seg_logdecay = nullptr;
-    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32);
+    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate);
     if (rc == LA_OK) *launches += 1;
     return rc;
 }

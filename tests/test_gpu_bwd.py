@@ -85,20 +85,24 @@ def test_fp32_head_dims(dk, dv):
 @pytest.mark.parametrize("m", MODES, ids=MID)
 @pytest.mark.parametrize("simt", [False, True], ids=["default", "simt"])
 def test_bf16_modes(m, simt):
-    """Every mode; without the per-channel gate the default route is the
-    tensor-core one: prep, three forwards, post (unnormalised); three preps,
-    six forwards (four of them writing fp32), post (normalised)."""
+    """Every mode; except the per-channel gate with the normaliser the default
+    route is the tensor-core one: prep, three forwards, post (scalar gate);
+    three preps, six forwards (five writing fp32), post (normalised); prep,
+    three forwards (two with the gate on the value side), two posts and the
+    gate gradient's scan (per-channel gate)."""
     cfg = W.workload("la", B=2, H=3, L=333, **m)
     launches = _check(cfg, seed=3, simt=simt)
-    tc = not simt and m["gate"] != "channel"
+    tc = not simt and not (m["normalize"] and m["gate"] == "channel")
     # a forward is three launches when the short batch is split into segments
-    if tc:
+    if tc and m["gate"] == "channel":
+        assert launches in (9, 15), launches  # prep, three forwards, two posts, the dg scan
+    elif tc:
         assert launches in ((10, 22) if m["normalize"] else (5, 11)), launches
     else:
         assert launches == (4 if m["normalize"] else 3), launches
 
 
-@pytest.mark.parametrize("m", [MODES[0], MODES[1], MODES[3], MODES[4]], ids=MID)
+@pytest.mark.parametrize("m", [MODES[0], MODES[1], MODES[3], MODES[4], MODES[5], MODES[7]], ids=MID)
 @pytest.mark.parametrize("B,H,L", [(1, 2, 1000), (2, 40, 200), (1, 1, 1), (1, 3, 65)])
 def test_bf16_tensor_core_route_shapes(m, B, H, L):
     """Split and unsplit sequences, one token, a ragged chunk."""
