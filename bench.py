@@ -357,7 +357,7 @@ def bench_bwd(name, steps, warmup, world, pk):
     bytes_ = n * (4 * dk + 3 * dv + (2 * dk if gated else 0)) * esz  # read q, k, v, dout (g); write dq, dk, dv (dg)
     flops = 2 * n * (2 * cfg["chunk"] * dk + 2 * cfg["chunk"] * dv + 4 * dk * dv)
     t_roof = max(bytes_ / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
-    route = "CUDA-core sweeps" if cfg["gate"] == "channel" else "tensor-core forwards"
+    route = "CUDA-core sweeps" if (cfg["gate"] == "channel" and cfg["normalize"]) else "tensor-core forwards"
     return {"tokens_per_s": world * B * L / t, "ms_per_step": t * 1e3, "launches_per_step": per_step,
             "roofline_frac": t_roof / t, "route": route, "algorithmic_bytes": bytes_}
 

@@ -218,13 +218,14 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
  *   q, k, v, gate, B, H, L, dk, dv, mode   as given to la_chunk_fwd (the chunk
  *          size does not enter the gradient)
  *
- * Two routes: bf16 with d_k = d_v = 128 and no per-channel gate (linear
- * attention, retention, RetNet) runs on the tensor-core forward kernel, since
- * with a decay that does not depend on the channel each gradient term is a
- * causal linear-attention forward with its roles permuted (some in reversed
- * token order; with the normaliser also den_t, z_t e_t and sum Q_t e_t, the
- * cancelling terms in fp32); every other case (and LA_KERNEL_SIMT) runs three
- * sweeps over the sequence on the CUDA cores.
+ * Two routes. bf16 with d_k = d_v = 128 runs on the tensor-core forward kernel
+ * (except the per-channel gate together with the normaliser): each gradient
+ * term is a causal linear-attention forward with its roles permuted, some in
+ * reversed token order; with the normaliser also den_t, z_t e_t and
+ * sum Q_t e_t (the cancelling terms in fp32); with the per-channel gate dv is a
+ * reversed gated forward and dQ, dK are forwards whose decay falls on the value
+ * channel, and dg comes from a segmented reverse scan. Every other case (and
+ * LA_KERNEL_SIMT) runs three sweeps over the sequence on the CUDA cores.
  *   dout   [B][H][L][d_v]; dq, dk [B][H][L][d_k] and dv [B][H][L][d_v] are
  *          written, in the type of q
  *   dgate  with LA_GATE_CHANNEL: NULL (not computed) or [B][H][L][d_k] in the
@@ -232,9 +233,9 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
  * No gradient flows into a final state or out of an initial one. Scratch,
  * taken stream-ordered with cudaMallocAsync on `stream` (LA_ERR_CUDA if that
  * fails): on the tensor-core route six (eight with LA_PHI_ELU1) bf16
- * [B][H][L][128] arrays, or with LA_NORMALIZE eleven bf16 and five fp32 ones;
- * on the other one fp32 [B][H][L][d_k] array (two, plus three [B][H][L], with
- * LA_NORMALIZE).
+ * [B][H][L][128] arrays, with LA_NORMALIZE eleven bf16 and five fp32 ones, with
+ * LA_GATE_CHANNEL nine bf16 and one fp32 one plus per-chunk sums; on the other
+ * one fp32 [B][H][L][d_k] array (two, plus three [B][H][L], with LA_NORMALIZE).
  * Errors as la_chunk_fwd; no output may overlap an input.
  */
 int la_chunk_bwd(const void *q, const void *k, const void *v, const void *gate,

@@ -705,8 +705,6 @@ __global__ void __launch_bounds__(kEw) bwdn_post_kernel(const uint4 *q, const ui
 // by a segmented reverse scan over chunks of 64 tokens.
 constexpr float kNoDecay = 3.0e38f;  // a gate value whose alpha is 1
 
-__device__ __forceinline__ float bf16_at(const __nv_bfloat16 *p, size_t i) { return __bfloat162float(p[i]); }
-
 // K = phi(k) in order; rev v, rev dout, rev phi(q), rev phi(k), and g'
 __global__ void __launch_bounds__(kEw) bwdg_prep_kernel(const uint4 *q, const uint4 *k, const uint4 *v, const uint4 *d,
                                                         const uint4 *g, uint4 *Kf, uint4 *rv, uint4 *rd, uint4 *rq,
@@ -733,88 +731,158 @@ __global__ void __launch_bounds__(kEw) bwdg_prep_kernel(const uint4 *q, const ui
     }
 }
 
-// dQ_t = e^{b_t} * bracket_t (chunks of 64 from token 0); dq = dQ phi'(q); dQ kept (fp32) for dg.
-// One thread per (sequence, chunk, channel), walking the chunk's tokens.
-__global__ void __launch_bounds__(kEw) bwdg_postq_kernel(const __nv_bfloat16 *q, const __nv_bfloat16 *g,
-                                                         const __nv_bfloat16 *br, __nv_bfloat16 *dq, float *dQ,
-                                                         long nbh, int L, bool elu1) {
+// The passes below take one thread per (sequence, chunk of 64 tokens, group
+// of 8 channels) and walk the chunk's tokens: 16-byte loads of bf16 rows
+// (two of fp32), consecutive threads on consecutive channel groups.
+struct Grp {
+    long bh;
+    int c, i0;  // chunk, first channel
+};
+__device__ __forceinline__ bool grp_of(long x, long nbh, int L, Grp &g) {
     const int nch = (L + 63) / 64;
-    const long x = (long)blockIdx.x * kEw + threadIdx.x;
-    if (x >= nbh * nch * kD) return;
-    const int i = (int)(x % kD), c = (int)((x / kD) % nch);
-    const long bh = x / kD / nch;
-    float b = 0.f;
-    for (int t = 64 * c; t < min(L, 64 * c + 64); ++t) {
-        const size_t o = ((size_t)bh * L + t) * kD + i;
-        b += channel_log_decay(bf16_at(g, o));
-        const float v = __expf(b) * bf16_at(br, o);
-        dQ[o] = v;
-        dq[o] = __float2bfloat16_rn(v * dphi(bf16_at(q, o), elu1));
+    if (x >= nbh * nch * CPR) return false;
+    g.i0 = 8 * (int)(x % CPR);
+    g.c = (int)((x / CPR) % nch);
+    g.bh = x / CPR / nch;
+    return true;
+}
+__device__ __forceinline__ void unpack8(uint4 w, float (&f)[8]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[2 * i] = __uint_as_float(u[i] << 16), f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        u[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+}
+__device__ __forceinline__ void ld8f(const float *p, float (&f)[8]) {
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p)), b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
+__device__ __forceinline__ void st8f(float *p, const float (&f)[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+// dQ_t = e^{b_t} * bracket_t (chunks of 64 from token 0); dq = dQ phi'(q); dQ kept (fp32) for dg
+__global__ void __launch_bounds__(kEw) bwdg_postq_kernel(const uint4 *q, const uint4 *g, const uint4 *br, uint4 *dq,
+                                                         float *dQ, long nbh, int L, bool elu1) {
+    Grp G;
+    if (!grp_of((long)blockIdx.x * kEw + threadIdx.x, nbh, L, G)) return;
+    float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int t = 64 * G.c; t < min(L, 64 * G.c + 64); ++t) {
+        const size_t o = ((size_t)G.bh * L + t) * kD + G.i0;
+        float gv[8], bv[8], qv[8], out[8], d[8];
+        unpack8(__ldcs(g + o / 8), gv);
+        unpack8(__ldcs(br + o / 8), bv);
+        unpack8(__ldg(q + o / 8), qv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            b[e] += channel_log_decay(gv[e]);
+            d[e] = __expf(b[e]) * bv[e];
+            out[e] = d[e] * dphi(qv[e], elu1);
+        }
+        st8f(dQ + o, d);
+        dq[o / 8] = pack8(out);
     }
 }
 
 // dK (reversed chunks of 64 from reversed token 0, gate g'), un-reversed:
-// dk = dK phi'(k); dv un-reversed; r = phi(q) dQ - phi(k) dK in place of dQ.
-__global__ void __launch_bounds__(kEw) bwdg_postk_kernel(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
-                                                         const __nv_bfloat16 *rg, const __nv_bfloat16 *rbr,
-                                                         const __nv_bfloat16 *rdv, __nv_bfloat16 *dk,
-                                                         __nv_bfloat16 *dv, float *r, long nbh, int L, bool elu1) {
-    const int nch = (L + 63) / 64;
-    const long x = (long)blockIdx.x * kEw + threadIdx.x;
-    if (x >= nbh * nch * kD) return;
-    const int i = (int)(x % kD), c = (int)((x / kD) % nch);
-    const long bh = x / kD / nch;
-    float b = 0.f;
-    for (int u = 64 * c; u < min(L, 64 * c + 64); ++u) {
-        const size_t ou = ((size_t)bh * L + u) * kD + i, ot = ((size_t)bh * L + (L - 1 - u)) * kD + i;
-        b += channel_log_decay(bf16_at(rg, ou));
-        const float dK = __expf(b) * bf16_at(rbr, ou);
-        const float kx = bf16_at(k, ot), qx = bf16_at(q, ot);
-        dk[ot] = __float2bfloat16_rn(dK * dphi(kx, elu1));
-        dv[ot] = rdv[ou];
-        r[ot] = phi(qx, elu1) * r[ot] - phi(kx, elu1) * dK;
+// dk = dK phi'(k); dv un-reversed; r = phi(q) dQ - phi(k) dK in place of dQ
+__global__ void __launch_bounds__(kEw) bwdg_postk_kernel(const uint4 *q, const uint4 *k, const uint4 *rg,
+                                                         const uint4 *rbr, const uint4 *rdv, uint4 *dk, uint4 *dv,
+                                                         float *r, long nbh, int L, bool elu1) {
+    Grp G;
+    if (!grp_of((long)blockIdx.x * kEw + threadIdx.x, nbh, L, G)) return;
+    float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int u = 64 * G.c; u < min(L, 64 * G.c + 64); ++u) {
+        const size_t ou = ((size_t)G.bh * L + u) * kD + G.i0, ot = ((size_t)G.bh * L + (L - 1 - u)) * kD + G.i0;
+        float gv[8], bv[8], kv[8], qv[8], rv[8], outk[8];
+        unpack8(__ldcs(rg + ou / 8), gv);
+        unpack8(__ldcs(rbr + ou / 8), bv);
+        unpack8(__ldg(k + ot / 8), kv);
+        unpack8(__ldg(q + ot / 8), qv);
+        ld8f(r + ot, rv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            b[e] += channel_log_decay(gv[e]);
+            const float dK = __expf(b[e]) * bv[e];
+            outk[e] = dK * dphi(kv[e], elu1);
+            rv[e] = phi(qv[e], elu1) * rv[e] - phi(kv[e], elu1) * dK;
+        }
+        dk[ot / 8] = pack8(outk);
+        dv[ot / 8] = __ldcs(rdv + ou / 8);
+        st8f(r + ot, rv);
     }
 }
 
-// chunk totals of r, then (one thread per sequence and channel) the sums over
-// all later chunks, then dg = sigmoid(-g) / 16 (later chunks + the chunk's tail)
+// chunk totals of r, then (one thread per sequence and channel group) the
+// sums over all later chunks, then dg = sigmoid(-g) / 16 (later chunks + the
+// chunk's tail)
 __global__ void __launch_bounds__(kEw) bwdg_tot_kernel(const float *r, float *tot, long nbh, int L) {
-    const int nch = (L + 63) / 64;
+    Grp G;
     const long x = (long)blockIdx.x * kEw + threadIdx.x;
-    if (x >= nbh * nch * kD) return;
-    const int i = (int)(x % kD), c = (int)((x / kD) % nch);
-    const long bh = x / kD / nch;
-    float s = 0.f;
-    for (int t = 64 * c; t < min(L, 64 * c + 64); ++t) s += r[((size_t)bh * L + t) * kD + i];
-    tot[x] = s;
+    if (!grp_of(x, nbh, L, G)) return;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int t = 64 * G.c; t < min(L, 64 * G.c + 64); ++t) {
+        float v[8];
+        ld8f(r + ((size_t)G.bh * L + t) * kD + G.i0, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s[e] += v[e];
+    }
+    st8f(tot + (size_t)x * 8, s);
 }
 __global__ void __launch_bounds__(kEw) bwdg_carry_kernel(float *tot, long nbh, int L) {
     const int nch = (L + 63) / 64;
     const long x = (long)blockIdx.x * kEw + threadIdx.x;
-    if (x >= nbh * kD) return;
-    const int i = (int)(x % kD);
-    const long bh = x / kD;
-    float acc = 0.f;
-    for (int c = nch - 1; c >= 0; --c) {
-        float *p = tot + ((size_t)bh * nch + c) * kD + i;
-        const float v = *p;
-        *p = acc;  // the sum over chunks after c
-        acc += v;
+    if (x >= nbh * CPR) return;
+    const long bh = x / CPR;
+    const int i0 = 8 * (int)(x % CPR);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // chunks from the last, four at a time: their loads go out together
+    for (int c1 = nch; c1 > 0; c1 -= 4) {
+        const int n4 = min(4, c1);
+        float v[4][8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (j < n4) ld8f(tot + ((size_t)bh * nch + c1 - 1 - j) * kD + i0, v[j]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < n4) {
+                st8f(tot + ((size_t)bh * nch + c1 - 1 - j) * kD + i0, acc);  // the sum over later chunks
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] += v[j][e];
+            }
+        }
     }
 }
-__global__ void __launch_bounds__(kEw) bwdg_dg_kernel(const float *r, const float *carry, const __nv_bfloat16 *g,
-                                                      __nv_bfloat16 *dg, long nbh, int L) {
-    const int nch = (L + 63) / 64;
+__global__ void __launch_bounds__(kEw) bwdg_dg_kernel(const float *r, const float *carry, const uint4 *g, uint4 *dg,
+                                                      long nbh, int L) {
+    Grp G;
     const long x = (long)blockIdx.x * kEw + threadIdx.x;
-    if (x >= nbh * nch * kD) return;
-    const int i = (int)(x % kD), c = (int)((x / kD) % nch);
-    const long bh = x / kD / nch;
-    float acc = carry[x];
-    for (int t = min(L, 64 * c + 64) - 1; t >= 64 * c; --t) {
-        const size_t o = ((size_t)bh * L + t) * kD + i;
-        acc += r[o];
-        const float gx = bf16_at(g, o);
-        dg[o] = __float2bfloat16_rn(acc * 0.0625f / (1.f + __expf(fminf(gx, 80.f))));
+    if (!grp_of(x, nbh, L, G)) return;
+    float acc[8];
+    ld8f(carry + (size_t)x * 8, acc);
+#pragma unroll 2
+    for (int t = min(L, 64 * G.c + 64) - 1; t >= 64 * G.c; --t) {
+        const size_t o = ((size_t)G.bh * L + t) * kD + G.i0;
+        float v[8], gv[8], out[8];
+        ld8f(r + o, v);
+        unpack8(__ldcs(g + o / 8), gv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            acc[e] += v[e];
+            out[e] = acc[e] * 0.0625f / (1.f + __expf(fminf(gv[e], 80.f)));
+        }
+        dg[o / 8] = pack8(out);
     }
 }
 
@@ -860,7 +928,6 @@ int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) {
         ChunkArgs c{q, k, v, g, out, nullptr, a.B, a.H, a.L, kD, kD, LA_GATE_CHANNEL, 64, nullptr, 0, value_side ? 1 : 0};
         rc = launch_chunk_tc(c, s, launches);
     };
-    using bf = __nv_bfloat16;
     bwdg_prep_kernel<<<ew_blocks(rows * CPR), kEw, 0, s>>>(
         static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), static_cast<const uint4 *>(a.v),
         static_cast<const uint4 *>(a.dout), static_cast<const uint4 *>(a.gate), Kf, rv, rd, rq, rk, rg, rows, a.L, elu1);
@@ -868,31 +935,29 @@ int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) {
     fwd(a.dout, a.v, Kf, a.gate, brq, true);  // dQ without e^{b_t}
     fwd(rv, rd, rq, rg, brk, true);           // reversed dK without e^{b'_u}
     fwd(rk, rq, rd, rg, rdv, false);          // reversed dv
-    const long nt = nbh * nch * kD;
+    const long nt = nbh * nch * CPR;  // (sequence, chunk, channel group) threads
     const unsigned nbk = (unsigned)((nt + kEw - 1) / kEw);
     if (rc == LA_OK) {
-        bwdg_postq_kernel<<<nbk, kEw, 0, s>>>(static_cast<const bf *>(a.q), static_cast<const bf *>(a.gate),
-                                              reinterpret_cast<const bf *>(brq), static_cast<bf *>(a.grad_q), rf, nbh,
-                                              a.L, elu1);
+        bwdg_postq_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.gate), brq,
+                                              static_cast<uint4 *>(a.grad_q), rf, nbh, a.L, elu1);
         ok();
     }
     if (rc == LA_OK) {
-        bwdg_postk_kernel<<<nbk, kEw, 0, s>>>(static_cast<const bf *>(a.q), static_cast<const bf *>(a.k),
-                                              reinterpret_cast<const bf *>(rg), reinterpret_cast<const bf *>(brk),
-                                              reinterpret_cast<const bf *>(rdv), static_cast<bf *>(a.grad_k),
-                                              static_cast<bf *>(a.grad_v), rf, nbh, a.L, elu1);
+        bwdg_postk_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), rg, brk,
+                                              rdv, static_cast<uint4 *>(a.grad_k), static_cast<uint4 *>(a.grad_v), rf,
+                                              nbh, a.L, elu1);
         ok();
     }
     if (rc == LA_OK && a.grad_g) {
         bwdg_tot_kernel<<<nbk, kEw, 0, s>>>(rf, tot, nbh, a.L);
         ok();
         if (rc == LA_OK) {
-            bwdg_carry_kernel<<<(unsigned)((nbh * kD + kEw - 1) / kEw), kEw, 0, s>>>(tot, nbh, a.L);
+            bwdg_carry_kernel<<<(unsigned)((nbh * CPR + kEw - 1) / kEw), kEw, 0, s>>>(tot, nbh, a.L);
             ok();
         }
         if (rc == LA_OK) {
-            bwdg_dg_kernel<<<nbk, kEw, 0, s>>>(rf, tot, static_cast<const bf *>(a.gate), static_cast<bf *>(a.grad_g),
-                                               nbh, a.L);
+            bwdg_dg_kernel<<<nbk, kEw, 0, s>>>(rf, tot, static_cast<const uint4 *>(a.gate),
+                                               static_cast<uint4 *>(a.grad_g), nbh, a.L);
             ok();
         }
     }
