@@ -1,0 +1,583 @@
+// la_bwd_tc.cu -- the backward pass on the tensor cores: each gradient term as
+// a causal linear-attention forward with its roles permuted, run on the
+// tensor-core forward kernel (bf16, d_k = d_v = 128).
+//
+// The gradients themselves are those of la_bwd.cu (the chain rule on the
+// recurrence; the pages give no gradient). With a decay that does not depend on
+// the channel (A_t = 1 or gamma_h), (Q_t . K_s) gamma^{t-s} is symmetric in the
+// roles, so
+//   dQ_t = sum_{s<=t} gamma^{t-s} (dout_t . v_s) K_s        = fwd(dout, v, K)
+//   dK_s = sum_{t>=s} gamma^{t-s} (v_s . dout_t) Q_t        = rev fwd(rev v, rev dout, rev Q)
+//   dv_s = sum_{t>=s} gamma^{t-s} (K_s . Q_t) dout_t        = rev fwd(rev K, rev Q, rev dout)
+// (rev reverses the token order: t >= s becomes t' <= s'). The normaliser and
+// the per-channel gate add the terms described above their routes below.
+#include "la_common.cuh"
+
+namespace la {
+namespace {
+
+__device__ __forceinline__ float dphi(float x, bool elu1) { return (elu1 && x <= 0.f) ? __expf(x) : 1.f; }
+
+// ---------------------------------------------------------------- scalar gate, no normaliser
+// A prep pass writes the reversed (and phi-applied) operands, three forwards,
+// a last pass un-reverses dK, dv and applies phi'.
+constexpr int kEw = 256;  // threads of the elementwise passes
+constexpr int kD = 128;   // the tensor-core kernel's head dim
+
+__device__ __forceinline__ uint4 phi8(uint4 x, bool elu1) {
+    if (!elu1) return x;
+    uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = phi(__uint_as_float(w[i] << 16), true), hi = phi(__uint_as_float(w[i] & 0xffff0000u), true);
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// reversed copies of v, dout, phi(q), phi(k), and phi(k) in order (elu1 only).
+// One uint4 (8 bf16) per step; rows of 128 stay contiguous.
+__global__ void __launch_bounds__(kEw) bwd_prep_kernel(const uint4 *q, const uint4 *k, const uint4 *v, const uint4 *d,
+                                                       uint4 *rv, uint4 *rd, uint4 *rq, uint4 *rk, uint4 *kf,
+                                                       long rows, int L, bool elu1) {
+    constexpr int CPR = kD / 8;  // chunks per row
+    const long n = rows * CPR;
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long row = x / CPR;
+        const int c = (int)(x % CPR), t = (int)(row % L);
+        const long rr = (row - t + (L - 1 - t)) * CPR + c;  // same sequence, token L-1-t
+        const uint4 kk = phi8(__ldcs(k + x), elu1);
+        rv[rr] = __ldcs(v + x);
+        rd[rr] = __ldcs(d + x);
+        rq[rr] = phi8(__ldcs(q + x), elu1);
+        rk[rr] = kk;
+        if (kf) kf[x] = kk;
+    }
+}
+
+// dq = dQ phi'(q) (in place when dq holds dQ), dk = rev(rdK) phi'(k), dv = rev(rdv)
+__global__ void __launch_bounds__(kEw) bwd_post_kernel(const uint4 *q, const uint4 *k, const uint4 *dQ, const uint4 *rdk,
+                                                       const uint4 *rdv, uint4 *dq, uint4 *dk, uint4 *dv, long rows,
+                                                       int L, bool elu1) {
+    constexpr int CPR = kD / 8;
+    const long n = rows * CPR;
+    auto scale = [](uint4 g, uint4 x) {  // g * phi'(x), elu1: 1 for x > 0, e^x otherwise
+        uint32_t gw[4] = {g.x, g.y, g.z, g.w}, xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xffff0000u);
+            const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xffff0000u);
+            __nv_bfloat162 h = __floats2bfloat162_rn(x0 > 0.f ? g0 : g0 * __expf(x0), x1 > 0.f ? g1 : g1 * __expf(x1));
+            gw[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(gw[0], gw[1], gw[2], gw[3]);
+    };
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long row = x / CPR;
+        const int c = (int)(x % CPR), t = (int)(row % L);
+        const long rr = (row - t + (L - 1 - t)) * CPR + c;
+        const uint4 gk = __ldcs(rdk + rr), gv = __ldcs(rdv + rr);
+        if (elu1) {
+            dq[x] = scale(__ldcs(dQ + x), __ldg(q + x));
+            dk[x] = scale(gk, __ldg(k + x));
+        } else {
+            dk[x] = gk;
+        }
+        dv[x] = gv;
+    }
+}
+
+// ---------------------------------------------------------------- tensor-core route, normalised
+// With the normaliser (w_t = dout_t / den_t, e_t = -(Q_t . S_t w_t) / den_t):
+//   den_t = Q_t . z_t                   = fwd(Q, K, J)            (columns 0 and 1)
+//   U_t   = S_t w_t                     = fwd(w, v, K)
+//   z_t e_t                             = fwd(E, J, K)            E_t = (e_t hi, e_t lo, 0 ..), J_s = (1, 1, 0 ..)
+//   dK_s  = sum_{t>=s} Q_t (v_s . w_t) + sum_{t>=s} Q_t e_t
+//         = rev fwd(rev v, rev w, rev Q) + rev fwd(J, rev E, rev Q)
+//   dv_s  = rev fwd(rev K, rev Q, rev w)
+//   dQ_t  = U_t + z_t e_t
+// dQ and dK are differences of nearly equal terms, so those forwards write
+// fp32 and e_t travels as two bf16 parts (hi + lo).
+constexpr int CPR = kD / 8;  // 16-byte chunks per row
+
+__device__ __forceinline__ long rev_chunk(long x, int L) {
+    const long row = x / CPR;
+    const int c = (int)(x % CPR), t = (int)(row % L);
+    return (row - t + (L - 1 - t)) * CPR + c;
+}
+
+// Q = phi(q), K = phi(k) in order; rev v, rev Q, rev K; the constant J
+__global__ void __launch_bounds__(kEw) bwdn_prep1_kernel(const uint4 *q, const uint4 *k, const uint4 *v, uint4 *Qf,
+                                                         uint4 *Kf, uint4 *rv, uint4 *rq, uint4 *rk, uint4 *J,
+                                                         long rows, int L, bool elu1) {
+    const long n = rows * CPR;
+    const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 twice
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long rr = rev_chunk(x, L);
+        const uint4 qq = phi8(__ldcs(q + x), elu1), kk = phi8(__ldcs(k + x), elu1);
+        Qf[x] = qq;
+        Kf[x] = kk;
+        rq[rr] = qq;
+        rk[rr] = kk;
+        rv[rr] = __ldcs(v + x);
+        J[x] = (x % CPR) == 0 ? make_uint4(one2, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// w = dout / den (den from column 0 of the fp32 forward with values J), in order and reversed
+__global__ void __launch_bounds__(kEw) bwdn_prep2_kernel(const uint4 *d, const float *den_full, uint4 *w, uint4 *rw,
+                                                         float *den, long rows, int L) {
+    const long n = rows * CPR;
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long row = x / CPR;
+        const float dn = den_full[row * kD];
+        if (x % CPR == 0) den[row] = dn;
+        const float r = 1.f / dn;
+        const uint4 g = __ldcs(d + x);
+        uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(gw[i] << 16) * r, __uint_as_float(gw[i] & 0xffff0000u) * r);
+            gw[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        const uint4 o = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+        w[x] = o;
+        rw[rev_chunk(x, L)] = o;
+    }
+}
+
+// e_t = -(Q_t . U_t) / den_t, one warp per token; E_t = (hi, lo, 0 ..) in order and reversed
+__global__ void __launch_bounds__(kEw) bwdn_prep3_kernel(const uint4 *Qf, const float *U, const float *den, uint4 *E,
+                                                         uint4 *rE, long rows, int L) {
+    const long row = ((long)blockIdx.x * kEw + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    // lane covers columns 4 lane .. 4 lane + 3
+    const uint2 qq = reinterpret_cast<const uint2 *>(Qf + row * CPR)[lane];
+    const float4 uu = reinterpret_cast<const float4 *>(U + row * kD)[lane];
+    float sdot = __uint_as_float(qq.x << 16) * uu.x + __uint_as_float(qq.x & 0xffff0000u) * uu.y +
+                 __uint_as_float(qq.y << 16) * uu.z + __uint_as_float(qq.y & 0xffff0000u) * uu.w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, off);
+    const float e = -sdot / den[row];
+    if (lane < CPR) {
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (lane == 0) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(e);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(e - __bfloat162float(hi));
+            __nv_bfloat162 h2;
+            h2.x = hi;
+            h2.y = lo;
+            o.x = *reinterpret_cast<uint32_t *>(&h2);
+        }
+        const long x = row * CPR + lane;
+        E[x] = o;
+        rE[rev_chunk(x, L)] = o;
+    }
+}
+
+// dq = (U + ZE) phi'(q), dk = rev(rdKm + rdz) phi'(k), dv = rev(rdv)
+__global__ void __launch_bounds__(kEw) bwdn_post_kernel(const uint4 *q, const uint4 *k, const float4 *U,
+                                                        const float4 *ZE, const float4 *rdkm, const float4 *rdz,
+                                                        const uint4 *rdv, uint4 *dq, uint4 *dk, uint4 *dv, long rows,
+                                                        int L, bool elu1) {
+    const long n = rows * CPR;
+    auto combine = [elu1](float4 a0, float4 a1, float4 b0, float4 b1, uint4 x) {
+        const float g[8] = {a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w,
+                            a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w};
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xffff0000u);
+            const float g0 = (elu1 && x0 <= 0.f) ? g[2 * i] * __expf(x0) : g[2 * i];
+            const float g1 = (elu1 && x1 <= 0.f) ? g[2 * i + 1] * __expf(x1) : g[2 * i + 1];
+            __nv_bfloat162 h = __floats2bfloat162_rn(g0, g1);
+            o[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long rr = rev_chunk(x, L);
+        dq[x] = combine(__ldcs(U + 2 * x), __ldcs(U + 2 * x + 1), __ldcs(ZE + 2 * x), __ldcs(ZE + 2 * x + 1), __ldg(q + x));
+        dk[x] = combine(__ldcs(rdkm + 2 * rr), __ldcs(rdkm + 2 * rr + 1), __ldcs(rdz + 2 * rr), __ldcs(rdz + 2 * rr + 1),
+                        __ldg(k + x));
+        dv[x] = __ldcs(rdv + rr);
+    }
+}
+
+// ---------------------------------------------------------------- tensor-core route, per-channel gate
+// With the gate diag(alpha_t) on the key channels (B_t = sum_{r<=t} log alpha_r):
+//   dv_s    = sum_{t>=s} (Q_t . K_s e^{B_t - B_s}) dout_t        = rev fwd_key(rev K, rev Q, rev dout; g')
+//   dQ_t[i] = sum_{s<=t} e^{B_t[i] - B_s[i]} K_s[i] (dout_t . v_s)  = fwd_value(dout, v, K; g)
+//   dK_s[i] = sum_{t>=s} e^{B_t[i] - B_s[i]} Q_t[i] (v_s . dout_t)  = rev fwd_value(rev v, rev dout, rev Q; g')
+// fwd_value is the forward with the decay on the value channels (the kernel
+// writes it without the factor e^{b_t}, b the log decay since the chunk start,
+// which the passes after apply). g' is g reversed and shifted by one token
+// (g'_u = g_{L-u}; g'_0 decays nothing), so the reversed forwards take the
+// same gate products. Then dg_r = sigmoid(-g_r) / 16 sum_{t>=r} (Q dQ - K dK)_t
+// by a segmented reverse scan over chunks of 64 tokens.
+constexpr float kNoDecay = 3.0e38f;  // a gate value whose alpha is 1
+
+// K = phi(k) in order; rev v, rev dout, rev phi(q), rev phi(k), and g'
+__global__ void __launch_bounds__(kEw) bwdg_prep_kernel(const uint4 *q, const uint4 *k, const uint4 *v, const uint4 *d,
+                                                        const uint4 *g, uint4 *Kf, uint4 *rv, uint4 *rd, uint4 *rq,
+                                                        uint4 *rk, uint4 *rg, long rows, int L, bool elu1) {
+    const long n = rows * CPR;
+    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
+        const long row = x / CPR;
+        const int c = (int)(x % CPR), t = (int)(row % L);
+        const long rr = rev_chunk(x, L);
+        const uint4 kk = phi8(__ldcs(k + x), elu1);
+        Kf[x] = kk;
+        rk[rr] = kk;
+        rq[rr] = phi8(__ldcs(q + x), elu1);
+        rv[rr] = __ldcs(v + x);
+        rd[rr] = __ldcs(d + x);
+        // g at token t goes to reversed token L - t; reversed token 0 decays nothing
+        const long base = (row - t) * CPR;
+        if (t >= 1) rg[base + (long)(L - t) * CPR + c] = __ldcs(g + x);
+        else {
+            __nv_bfloat162 h = __floats2bfloat162_rn(kNoDecay, kNoDecay);
+            const uint32_t w = *reinterpret_cast<uint32_t *>(&h);
+            rg[base + c] = make_uint4(w, w, w, w);
+        }
+    }
+}
+
+// The passes below take one thread per (sequence, chunk of 64 tokens, group
+// of 8 channels) and walk the chunk's tokens: 16-byte loads of bf16 rows
+// (two of fp32), consecutive threads on consecutive channel groups.
+struct Grp {
+    long bh;
+    int c, i0;  // chunk, first channel
+};
+__device__ __forceinline__ bool grp_of(long x, long nbh, int L, Grp &g) {
+    const int nch = (L + 63) / 64;
+    if (x >= nbh * nch * CPR) return false;
+    g.i0 = 8 * (int)(x % CPR);
+    g.c = (int)((x / CPR) % nch);
+    g.bh = x / CPR / nch;
+    return true;
+}
+__device__ __forceinline__ void unpack8(uint4 w, float (&f)[8]) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[2 * i] = __uint_as_float(u[i] << 16), f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        u[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+}
+__device__ __forceinline__ void ld8f(const float *p, float (&f)[8]) {
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(p)), b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
+__device__ __forceinline__ void st8f(float *p, const float (&f)[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+// dQ_t = e^{b_t} * bracket_t (chunks of 64 from token 0); dq = dQ phi'(q); dQ kept (fp32) for dg
+__global__ void __launch_bounds__(kEw) bwdg_postq_kernel(const uint4 *q, const uint4 *g, const uint4 *br, uint4 *dq,
+                                                         float *dQ, long nbh, int L, bool elu1) {
+    Grp G;
+    if (!grp_of((long)blockIdx.x * kEw + threadIdx.x, nbh, L, G)) return;
+    float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int t = 64 * G.c; t < min(L, 64 * G.c + 64); ++t) {
+        const size_t o = ((size_t)G.bh * L + t) * kD + G.i0;
+        float gv[8], bv[8], qv[8], out[8], d[8];
+        unpack8(__ldcs(g + o / 8), gv);
+        unpack8(__ldcs(br + o / 8), bv);
+        unpack8(__ldg(q + o / 8), qv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            b[e] += channel_log_decay(gv[e]);
+            d[e] = __expf(b[e]) * bv[e];
+            out[e] = d[e] * dphi(qv[e], elu1);
+        }
+        st8f(dQ + o, d);
+        dq[o / 8] = pack8(out);
+    }
+}
+
+// dK (reversed chunks of 64 from reversed token 0, gate g'), un-reversed:
+// dk = dK phi'(k); dv un-reversed; r = phi(q) dQ - phi(k) dK in place of dQ
+__global__ void __launch_bounds__(kEw) bwdg_postk_kernel(const uint4 *q, const uint4 *k, const uint4 *rg,
+                                                         const uint4 *rbr, const uint4 *rdv, uint4 *dk, uint4 *dv,
+                                                         float *r, long nbh, int L, bool elu1) {
+    Grp G;
+    if (!grp_of((long)blockIdx.x * kEw + threadIdx.x, nbh, L, G)) return;
+    float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int u = 64 * G.c; u < min(L, 64 * G.c + 64); ++u) {
+        const size_t ou = ((size_t)G.bh * L + u) * kD + G.i0, ot = ((size_t)G.bh * L + (L - 1 - u)) * kD + G.i0;
+        float gv[8], bv[8], kv[8], qv[8], rv[8], outk[8];
+        unpack8(__ldcs(rg + ou / 8), gv);
+        unpack8(__ldcs(rbr + ou / 8), bv);
+        unpack8(__ldg(k + ot / 8), kv);
+        unpack8(__ldg(q + ot / 8), qv);
+        ld8f(r + ot, rv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            b[e] += channel_log_decay(gv[e]);
+            const float dK = __expf(b[e]) * bv[e];
+            outk[e] = dK * dphi(kv[e], elu1);
+            rv[e] = phi(qv[e], elu1) * rv[e] - phi(kv[e], elu1) * dK;
+        }
+        dk[ot / 8] = pack8(outk);
+        dv[ot / 8] = __ldcs(rdv + ou / 8);
+        st8f(r + ot, rv);
+    }
+}
+
+// chunk totals of r, then (one thread per sequence and channel group) the
+// sums over all later chunks, then dg = sigmoid(-g) / 16 (later chunks + the
+// chunk's tail)
+__global__ void __launch_bounds__(kEw) bwdg_tot_kernel(const float *r, float *tot, long nbh, int L) {
+    Grp G;
+    const long x = (long)blockIdx.x * kEw + threadIdx.x;
+    if (!grp_of(x, nbh, L, G)) return;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int t = 64 * G.c; t < min(L, 64 * G.c + 64); ++t) {
+        float v[8];
+        ld8f(r + ((size_t)G.bh * L + t) * kD + G.i0, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s[e] += v[e];
+    }
+    st8f(tot + (size_t)x * 8, s);
+}
+__global__ void __launch_bounds__(kEw) bwdg_carry_kernel(float *tot, long nbh, int L) {
+    const int nch = (L + 63) / 64;
+    const long x = (long)blockIdx.x * kEw + threadIdx.x;
+    if (x >= nbh * CPR) return;
+    const long bh = x / CPR;
+    const int i0 = 8 * (int)(x % CPR);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // chunks from the last, four at a time: their loads go out together
+    for (int c1 = nch; c1 > 0; c1 -= 4) {
+        const int n4 = min(4, c1);
+        float v[4][8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (j < n4) ld8f(tot + ((size_t)bh * nch + c1 - 1 - j) * kD + i0, v[j]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < n4) {
+                st8f(tot + ((size_t)bh * nch + c1 - 1 - j) * kD + i0, acc);  // the sum over later chunks
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] += v[j][e];
+            }
+        }
+    }
+}
+__global__ void __launch_bounds__(kEw) bwdg_dg_kernel(const float *r, const float *carry, const uint4 *g, uint4 *dg,
+                                                      long nbh, int L) {
+    Grp G;
+    const long x = (long)blockIdx.x * kEw + threadIdx.x;
+    if (!grp_of(x, nbh, L, G)) return;
+    float acc[8];
+    ld8f(carry + (size_t)x * 8, acc);
+#pragma unroll 2
+    for (int t = min(L, 64 * G.c + 64) - 1; t >= 64 * G.c; --t) {
+        const size_t o = ((size_t)G.bh * L + t) * kD + G.i0;
+        float v[8], gv[8], out[8];
+        ld8f(r + o, v);
+        unpack8(__ldcs(g + o / 8), gv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            acc[e] += v[e];
+            out[e] = acc[e] * 0.0625f / (1.f + __expf(fminf(gv[e], 80.f)));
+        }
+        dg[o / 8] = pack8(out);
+    }
+}
+
+int ew_blocks(long n) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 132;
+    const long need = (n + kEw - 1) / kEw, cap = (long)sms * 8;
+    return (int)(need < cap ? need : cap);
+}
+
+}  // namespace
+
+bool bwd_tc_supports(const BwdArgs &a) {
+    if (a.mode & LA_DTYPE_F32) return false;
+    if ((a.mode & LA_GATE_CHANNEL) && (a.mode & LA_NORMALIZE)) return false;
+    if (a.dk != kD || a.dv != kD || a.L < 1) return false;
+    ChunkArgs c{a.q, a.k, a.v, a.gate, nullptr, nullptr, a.B, a.H, a.L, kD, kD, a.mode & LA_GATE_HEAD, 64, nullptr};
+    return chunk_tc_supports(c);
+}
+
+static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) {
+    const long nbh = (long)a.B * a.H, rows = nbh * a.L;
+    const int nch = (a.L + 63) / 64;
+    const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16);
+    // bf16: K rv rd rq rk g' bracket_q bracket_k rdv; fp32: dQ / r; chunk totals
+    const size_t bytes = 9 * hb + 2 * hb + (size_t)nbh * nch * kD * sizeof(float);
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    char *b = static_cast<char *>(scratch);
+    uint4 *h[9];
+    for (int i = 0; i < 9; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
+    uint4 *Kf = h[0], *rv = h[1], *rd = h[2], *rq = h[3], *rk = h[4], *rg = h[5], *brq = h[6], *brk = h[7], *rdv = h[8];
+    float *rf = reinterpret_cast<float *>(b + 9 * hb), *tot = reinterpret_cast<float *>(b + 11 * hb);
+    const bool elu1 = a.mode & LA_PHI_ELU1;
+    int rc = LA_OK;
+    auto ok = [&]() {
+        if (rc == LA_OK && cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
+        if (rc == LA_OK) ++*launches;
+    };
+    auto fwd = [&](const void *q, const void *k, const void *v, const void *g, void *out, bool value_side) {
+        if (rc != LA_OK) return;
+        ChunkArgs c{q, k, v, g, out, nullptr, a.B, a.H, a.L, kD, kD, LA_GATE_CHANNEL, 64, nullptr, 0, value_side ? 1 : 0};
+        rc = launch_chunk_tc(c, s, launches);
+    };
+    bwdg_prep_kernel<<<ew_blocks(rows * CPR), kEw, 0, s>>>(
+        static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), static_cast<const uint4 *>(a.v),
+        static_cast<const uint4 *>(a.dout), static_cast<const uint4 *>(a.gate), Kf, rv, rd, rq, rk, rg, rows, a.L, elu1);
+    ok();
+    fwd(a.dout, a.v, Kf, a.gate, brq, true);  // dQ without e^{b_t}
+    fwd(rv, rd, rq, rg, brk, true);           // reversed dK without e^{b'_u}
+    fwd(rk, rq, rd, rg, rdv, false);          // reversed dv
+    const long nt = nbh * nch * CPR;  // (sequence, chunk, channel group) threads
+    const unsigned nbk = (unsigned)((nt + kEw - 1) / kEw);
+    if (rc == LA_OK) {
+        bwdg_postq_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.gate), brq,
+                                              static_cast<uint4 *>(a.grad_q), rf, nbh, a.L, elu1);
+        ok();
+    }
+    if (rc == LA_OK) {
+        bwdg_postk_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), rg, brk,
+                                              rdv, static_cast<uint4 *>(a.grad_k), static_cast<uint4 *>(a.grad_v), rf,
+                                              nbh, a.L, elu1);
+        ok();
+    }
+    if (rc == LA_OK && a.grad_g) {
+        bwdg_tot_kernel<<<nbk, kEw, 0, s>>>(rf, tot, nbh, a.L);
+        ok();
+        if (rc == LA_OK) {
+            bwdg_carry_kernel<<<(unsigned)((nbh * CPR + kEw - 1) / kEw), kEw, 0, s>>>(tot, nbh, a.L);
+            ok();
+        }
+        if (rc == LA_OK) {
+            bwdg_dg_kernel<<<nbk, kEw, 0, s>>>(rf, tot, static_cast<const uint4 *>(a.gate),
+                                               static_cast<uint4 *>(a.grad_g), nbh, a.L);
+            ok();
+        }
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
+    return rc;
+}
+
+static int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
+    const long rows = (long)a.B * a.H * a.L;
+    const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16), fb = 2 * hb;
+    // bf16: Q K J w E rv rw rq rk rE rdv; fp32: den_full U ZE rdkm rdz; den [rows]
+    const size_t bytes = 11 * hb + 5 * fb + (size_t)rows * sizeof(float);
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    char *b = static_cast<char *>(scratch);
+    uint4 *h[11];
+    for (int i = 0; i < 11; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
+    uint4 *Qf = h[0], *Kf = h[1], *J = h[2], *w = h[3], *E = h[4], *rv = h[5], *rw = h[6], *rq = h[7], *rk = h[8],
+          *rE = h[9], *rdv = h[10];
+    float *f[5];
+    for (int i = 0; i < 5; ++i) f[i] = reinterpret_cast<float *>(b + 11 * hb + i * fb);
+    float *den_full = f[0], *U = f[1], *ZE = f[2], *rdkm = f[3], *rdz = f[4];
+    float *den = reinterpret_cast<float *>(b + 11 * hb + 5 * fb);
+    const bool elu1 = a.mode & LA_PHI_ELU1;
+    const int mode = a.mode & LA_GATE_HEAD;  // identity feature map, bf16, no normaliser
+    const int nb = ew_blocks(rows * CPR);
+    int rc = LA_OK;
+    auto ok = [&]() {
+        if (rc == LA_OK && cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
+        if (rc == LA_OK) ++*launches;
+    };
+    auto fwd = [&](const void *q, const void *k, const void *v, void *out, bool f32) {
+        if (rc != LA_OK) return;
+        ChunkArgs c{q, k, v, a.gate, out, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr, f32 ? 1 : 0};
+        rc = launch_chunk_tc(c, s, launches);
+    };
+    bwdn_prep1_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
+                                         static_cast<const uint4 *>(a.v), Qf, Kf, rv, rq, rk, J, rows, a.L, elu1);
+    ok();
+    fwd(Qf, Kf, J, den_full, true);  // den_t in columns 0 and 1
+    if (rc == LA_OK) {
+        bwdn_prep2_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.dout), den_full, w, rw, den, rows, a.L);
+        ok();
+    }
+    fwd(w, a.v, Kf, U, true);  // U_t = S_t w_t
+    if (rc == LA_OK) {
+        bwdn_prep3_kernel<<<(unsigned)((rows + kEw / 32 - 1) / (kEw / 32)), kEw, 0, s>>>(Qf, U, den, E, rE, rows, a.L);
+        ok();
+    }
+    fwd(E, J, Kf, ZE, true);    // z_t e_t
+    fwd(rv, rw, rq, rdkm, true);
+    fwd(J, rE, rq, rdz, true);
+    fwd(rk, rq, rw, rdv, false);
+    if (rc == LA_OK) {
+        bwdn_post_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
+                                            reinterpret_cast<const float4 *>(U), reinterpret_cast<const float4 *>(ZE),
+                                            reinterpret_cast<const float4 *>(rdkm), reinterpret_cast<const float4 *>(rdz),
+                                            rdv, static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k),
+                                            static_cast<uint4 *>(a.grad_v), rows, a.L, elu1);
+        ok();
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
+    return rc;
+}
+
+int launch_bwd_tc(const BwdArgs &a, cudaStream_t s, int *launches) {
+    if (a.mode & LA_GATE_CHANNEL) return launch_bwd_tc_gated(a, s, launches);
+    if (a.mode & LA_NORMALIZE) return launch_bwd_tc_norm(a, s, launches);
+    const long rows = (long)a.B * a.H * a.L;
+    const size_t arr = (size_t)rows * kD * sizeof(__nv_bfloat16);
+    const bool elu1 = a.mode & LA_PHI_ELU1;
+    // rv, rd, rq, rk, rdk, rdv; with elu1 also K = phi(k) and dQ
+    const int narr = elu1 ? 8 : 6;
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, narr * arr, s) != cudaSuccess) return LA_ERR_CUDA;
+    char *b = static_cast<char *>(scratch);
+    uint4 *rv = reinterpret_cast<uint4 *>(b), *rd = reinterpret_cast<uint4 *>(b + arr);
+    uint4 *rq = reinterpret_cast<uint4 *>(b + 2 * arr), *rk = reinterpret_cast<uint4 *>(b + 3 * arr);
+    uint4 *rdk = reinterpret_cast<uint4 *>(b + 4 * arr), *rdv = reinterpret_cast<uint4 *>(b + 5 * arr);
+    uint4 *kf = elu1 ? reinterpret_cast<uint4 *>(b + 6 * arr) : nullptr;
+    uint4 *dQ = elu1 ? reinterpret_cast<uint4 *>(b + 7 * arr) : static_cast<uint4 *>(a.grad_q);
+    const int mode = a.mode & LA_GATE_HEAD;  // identity feature map, bf16, no normaliser
+    const int nb = ew_blocks(rows * (kD / 8));
+    int rc = LA_OK;
+    bwd_prep_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
+                                       static_cast<const uint4 *>(a.v), static_cast<const uint4 *>(a.dout), rv, rd, rq,
+                                       rk, kf, rows, a.L, elu1);
+    if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
+    else ++*launches;
+    const ChunkArgs calls[3] = {
+        {a.dout, a.v, elu1 ? kf : a.k, a.gate, dQ, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
+        {rv, rd, rq, a.gate, rdk, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
+        {rk, rq, rd, a.gate, rdv, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
+    };
+    for (int i = 0; i < 3 && rc == LA_OK; ++i) rc = launch_chunk_tc(calls[i], s, launches);
+    if (rc == LA_OK) {
+        bwd_post_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), dQ, rdk,
+                                           rdv, static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k),
+                                           static_cast<uint4 *>(a.grad_v), rows, a.L, elu1);
+        if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
+        else ++*launches;
+    }
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
+    return rc;
+}
+
+
+}  // namespace la
