@@ -17,11 +17,12 @@
 //
 // Two kernels. W and U do not depend on the state, so they are made for every
 // chunk at once, and only the state recurrence runs chunk after chunk:
-//   delta_prep_kernel   one CTA of 128 threads per (b, h, chunk), two CTAs per SM.
-//       round 1  K K^T -> L = I + A (fp32, shared); L^-1 by blocks of 16
-//                (diagonal blocks by substitution, then block rows) -> T (bf16)
-//       round 2  W = T K, U = T V -> bf16, written to a scratch array as the
-//                shared-memory images the second kernel's operands need
+//   delta_prep_kernel   one CTA of 128 threads per (b, h, chunk), four CTAs per SM.
+//       round 1  K K^T -> L = I + A (fp32, shared); L^-1 in place by blocks of
+//                16 (diagonal blocks by substitution, then block rows) -> T (bf16)
+//       round 2  W = T K, then U = T V (one 128-column accumulator) -> bf16,
+//                written to a scratch array as the shared-memory images the
+//                second kernel's operands need
 //   delta_state_kernel  one CTA of 256 threads per (b, h), chunks in order; the
 //       state kept transposed in TMEM (S^T: lane = key channel i, column =
 //       value channel j, fp32) with a bf16 copy in shared memory. Per chunk:
@@ -51,17 +52,17 @@ constexpr uint32_t kImg = 32768;             // scratch per chunk: W image | U i
 // every such tile is followed by at least 8 KiB of other data.
 constexpr int kPrepThreads = 128;
 constexpr uint32_t pK = 0, pV = 16384;   // [64 x 128] bf16 tiles, two 8 KiB halves
-constexpr uint32_t pT = 32768;           // T, K-major [64 x 64]
 constexpr int kLd = 68;                  // fp32 row: 16-byte aligned, rows 4 banks apart
-constexpr uint32_t kL = pT + 8192;       // L = I + A, fp32 [64][kLd]
-constexpr uint32_t kLi = kL + 64 * kLd * 4;     // L^-1, fp32 [64][kLd]
+constexpr uint32_t kM = 32768;           // L = I + A, then L^-1 in place, fp32 [64][kLd];
+constexpr uint32_t pT = kM;              // then T over it, K-major bf16 [64 x 64]
 constexpr int kYd = 20;                         // Y row: 16 + 4, 16-byte aligned
-constexpr uint32_t kY = kLi + 64 * kLd * 4;     // block-row partial products, fp32 [3][16][kYd]
+constexpr uint32_t kY = kM + 64 * kLd * 4;      // block-row partial products, fp32 [3][16][kYd]
 constexpr uint32_t kB = kY + 3 * 16 * kYd * 4;  // beta [64]
 constexpr uint32_t pBar = kB + 64 * 4;          // mbarriers (MMA, drain), TMEM address
 constexpr uint32_t kPrepSmem = pBar + 24 + 1024;
-// TMEM: A (64 columns) is read out before W and U are made over it
-constexpr uint32_t pcA = 0, pcW = 0, pcU = 128, kPrepCols = 256;
+// TMEM: A (64 columns), then W, then U, each read out before the next product
+constexpr uint32_t pcA = 0, pcW = 0, pcU = 0, kPrepCols = 128;
+constexpr int kPrepPerSm = 4;
 
 // ---- delta_state_kernel shared memory
 constexpr int kStateThreads = 256;
@@ -73,7 +74,8 @@ constexpr uint32_t kS = kU + 16384;        // S^T copy, MN-major: 128 lines x 12
 constexpr uint32_t kBar = kS + 32768;      // mbarriers P, X, S, O, drain; TMEM address
 constexpr uint32_t kStateSmem = kBar + 48 + 1024;
 constexpr uint32_t cS = 0, cX = 128, cO = 256, cP = 384, kStateCols = 512;
-static_assert(kPrepSmem * 2 + 2048 <= 232448, "two prep CTAs per SM");
+static_assert((kPrepSmem + 1024) * kPrepPerSm <= 233472 && kPrepCols * kPrepPerSm <= 512, "four prep CTAs per SM");
+static_assert(64 * kLd * 4 >= 16384, "T's M = 128 operand reads 8 KiB past T inside the fp32 block");
 static_assert(kStateSmem <= 232448, "state kernel shared memory");
 
 __device__ unsigned int g_delta_tc_error;
@@ -118,14 +120,16 @@ constexpr uint32_t idKM = idesc_bf16(128, 128, false, true);   // K-major A, MN-
 constexpr uint32_t idMM = idesc_bf16(128, 128, true, true);    // MN-major A and B
 
 // ============================================================================ W, U
-__global__ void __launch_bounds__(kPrepThreads, 2) delta_prep_kernel(const DeltaArgs a, uint8_t *img, int nch) {
+__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(const DeltaArgs a, uint8_t *img, int nch) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int bh = blockIdx.x / nch, n = blockIdx.x % nch, L = a.L;
     const int t0 = n * kC, nt = min(kC, L - t0);
     constexpr int kThreads = kPrepThreads;
-    float *Lm = reinterpret_cast<float *>(sm + kL), *Li = reinterpret_cast<float *>(sm + kLi);
+    // L and L^-1 share one array: each block of L^-1 is written over the block of
+    // L that no later step reads
+    float *Lm = reinterpret_cast<float *>(sm + kM), *Li = Lm;
     float *Yb = reinterpret_cast<float *>(sm + kY), *bs = reinterpret_cast<float *>(sm + kB);
     uint64_t *mb = reinterpret_cast<uint64_t *>(sm + pBar), *drain = mb + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + pBar + 16);
@@ -204,138 +208,157 @@ __global__ void __launch_bounds__(kPrepThreads, 2) delta_prep_kernel(const Delta
         }
         tc_fence_before();
         __syncthreads();
-    // ---------------------------------------------------------------- L^-1 by 16 x 16 blocks
-    if (tid < kC) {
-        // diagonal block b, column c: forward substitution of a unit lower-triangular system
-        const int b = tid >> 4, c = tid & 15, o = 16 * b;
-        float x[16];
+        // ---------------------------------------------------------------- L^-1 by 16 x 16 blocks
+        {
+            // diagonal block b, column c: forward substitution of a unit
+            // lower-triangular system; written over L's block once all are solved
+            const int b = (tid >> 4) & 3, c = tid & 15, o = 16 * b;
+            float x[16];
+            if (tid < kC) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = r == c ? 1.f : 0.f;
+                for (int r = 0; r < 16; ++r) {
+                    float acc = r == c ? 1.f : 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc = fmaf(-Lm[(o + r) * kLd + o + s], x[s], acc);
-            x[r] = r < c ? 0.f : acc;
+                    for (int s = 0; s < r; ++s) acc = fmaf(-Lm[(o + r) * kLd + o + s], x[s], acc);
+                    x[r] = r < c ? 0.f : acc;
+                }
+            }
+            __syncthreads();
+            if (tid < kC) {
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Li[(o + r) * kLd + o + c] = x[r];
+            }
         }
+        __syncthreads();
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Li[(o + r) * kLd + o + c] = x[r];
-    }
-    __syncthreads();
+        for (int bi = 1; bi < 4; ++bi) {
+            // block row bi: Y_bj = sum_{m=j}^{bi-1} L_bi,m Li_m,j, then Li_bi,j = -Li_bi,bi Y_bj.
+            // A thread takes four adjacent columns of one row (float4 loads of
+            // Li and Y rows, one L value per four products); the zeros above
+            // the diagonal of Li_bi,bi make the second product a full 16 terms.
 #pragma unroll
-    for (int bi = 1; bi < 4; ++bi) {
-        // block row bi: Y_bj = sum_{m=j}^{bi-1} L_bi,m Li_m,j, then Li_bi,j = -Li_bi,bi Y_bj.
-        // A thread takes four adjacent columns of one row (float4 loads of
-        // Li and Y rows, one L value per four products); the zeros above
-        // the diagonal of Li_bi,bi make the second product a full 16 terms.
+            for (int e0 = 0; e0 < bi * 64; e0 += kThreads) {
+                const int e = e0 + tid;
+                if (e < bi * 64) {
+                    const int j = e >> 6, r = (e >> 2) & 15, c0 = 4 * (e & 3);
+                    const float *lrow = Lm + (16 * bi + r) * kLd;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int kb = j; kb < bi; ++kb) {
+                        float lv[16];
+                        float4 iv[16];
 #pragma unroll
-        for (int e0 = 0; e0 < bi * 64; e0 += kThreads) {
-            const int e = e0 + tid;
-            if (e < bi * 64) {
-                const int j = e >> 6, r = (e >> 2) & 15, c0 = 4 * (e & 3);
-                const float *lrow = Lm + (16 * bi + r) * kLd;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int kb = j; kb < bi; ++kb) {
+                        for (int m = 0; m < 16; m += 4) {
+                            const float4 l4 = *reinterpret_cast<const float4 *>(lrow + 16 * kb + m);
+                            lv[m] = l4.x, lv[m + 1] = l4.y, lv[m + 2] = l4.z, lv[m + 3] = l4.w;
+                        }
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            iv[m] = *reinterpret_cast<const float4 *>(Li + (16 * kb + m) * kLd + 16 * j + c0);
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            acc.x = fmaf(lv[m], iv[m].x, acc.x);
+                            acc.y = fmaf(lv[m], iv[m].y, acc.y);
+                            acc.z = fmaf(lv[m], iv[m].z, acc.z);
+                            acc.w = fmaf(lv[m], iv[m].w, acc.w);
+                        }
+                    }
+                    *reinterpret_cast<float4 *>(Yb + (j * 16 + r) * kYd + c0) = acc;
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int e0 = 0; e0 < bi * 64; e0 += kThreads) {
+                const int e = e0 + tid;
+                if (e < bi * 64) {
+                    const int j = e >> 6, r = (e >> 2) & 15, c0 = 4 * (e & 3);
+                    const float *irow = Li + (16 * bi + r) * kLd + 16 * bi;
                     float lv[16];
-                    float4 iv[16];
+                    float4 yv[16];
 #pragma unroll
                     for (int m = 0; m < 16; m += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4 *>(lrow + 16 * kb + m);
+                        const float4 l4 = *reinterpret_cast<const float4 *>(irow + m);
                         lv[m] = l4.x, lv[m + 1] = l4.y, lv[m + 2] = l4.z, lv[m + 3] = l4.w;
                     }
 #pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        iv[m] = *reinterpret_cast<const float4 *>(Li + (16 * kb + m) * kLd + 16 * j + c0);
+                    for (int m = 0; m < 16; ++m) yv[m] = *reinterpret_cast<const float4 *>(Yb + (j * 16 + m) * kYd + c0);
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int m = 0; m < 16; ++m) {
-                        acc.x = fmaf(lv[m], iv[m].x, acc.x);
-                        acc.y = fmaf(lv[m], iv[m].y, acc.y);
-                        acc.z = fmaf(lv[m], iv[m].z, acc.z);
-                        acc.w = fmaf(lv[m], iv[m].w, acc.w);
+                        acc.x = fmaf(lv[m], yv[m].x, acc.x);
+                        acc.y = fmaf(lv[m], yv[m].y, acc.y);
+                        acc.z = fmaf(lv[m], yv[m].z, acc.z);
+                        acc.w = fmaf(lv[m], yv[m].w, acc.w);
                     }
+                    *reinterpret_cast<float4 *>(Li + (16 * bi + r) * kLd + 16 * j + c0) =
+                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
-                *reinterpret_cast<float4 *>(Yb + (j * 16 + r) * kYd + c0) = acc;
+            }
+            __syncthreads();
+        }
+        // T = L^-1 diag(beta), lower triangular, bf16 K-major, written over the
+        // fp32 block once every thread has read its share
+        {
+            uint4 tw[kC * 8 / kThreads];
+#pragma unroll
+            for (int u = 0; u < kC * 8 / kThreads; ++u) {
+                const int x = u * kThreads + tid, t = x >> 3, c8 = x & 7;
+                const float4 l0 = *reinterpret_cast<const float4 *>(Li + t * kLd + 8 * c8);
+                const float4 l1 = *reinterpret_cast<const float4 *>(Li + t * kLd + 8 * c8 + 4);
+                const float4 b0 = *reinterpret_cast<const float4 *>(bs + 8 * c8);
+                const float4 b1 = *reinterpret_cast<const float4 *>(bs + 8 * c8 + 4);
+                const float lv[8] = {l0.x * b0.x, l0.y * b0.y, l0.z * b0.z, l0.w * b0.w,
+                                     l1.x * b1.x, l1.y * b1.y, l1.z * b1.z, l1.w * b1.w};
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = c8 * 8 + 2 * e;
+                    w[e] = pack2(s <= t ? lv[2 * e] : 0.f, s + 1 <= t ? lv[2 * e + 1] : 0.f);
+                }
+                tw[u] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < kC * 8 / kThreads; ++u) {
+                const int x = u * kThreads + tid, t = x >> 3, c8 = x & 7;
+                *reinterpret_cast<uint4 *>(sm + pT + chunk_off(t, c8, 0)) = tw[u];
             }
         }
-        __syncthreads();
-#pragma unroll
-        for (int e0 = 0; e0 < bi * 64; e0 += kThreads) {
-            const int e = e0 + tid;
-            if (e < bi * 64) {
-                const int j = e >> 6, r = (e >> 2) & 15, c0 = 4 * (e & 3);
-                const float *irow = Li + (16 * bi + r) * kLd + 16 * bi;
-                float lv[16];
-                float4 yv[16];
-#pragma unroll
-                for (int m = 0; m < 16; m += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(irow + m);
-                    lv[m] = l4.x, lv[m + 1] = l4.y, lv[m + 2] = l4.z, lv[m + 3] = l4.w;
-                }
-#pragma unroll
-                for (int m = 0; m < 16; ++m) yv[m] = *reinterpret_cast<const float4 *>(Yb + (j * 16 + m) * kYd + c0);
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    acc.x = fmaf(lv[m], yv[m].x, acc.x);
-                    acc.y = fmaf(lv[m], yv[m].y, acc.y);
-                    acc.z = fmaf(lv[m], yv[m].z, acc.z);
-                    acc.w = fmaf(lv[m], yv[m].w, acc.w);
-                }
-                *reinterpret_cast<float4 *>(Li + (16 * bi + r) * kLd + 16 * j + c0) =
-                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-            }
-        }
-        __syncthreads();
-    }
-    // T = L^-1 diag(beta), lower triangular, bf16 K-major
-#pragma unroll
-    for (int x0 = 0; x0 < kC * 8; x0 += kThreads) {
-        const int x = x0 + tid, t = x >> 3, c8 = x & 7;
-        const float4 l0 = *reinterpret_cast<const float4 *>(Li + t * kLd + 8 * c8);
-        const float4 l1 = *reinterpret_cast<const float4 *>(Li + t * kLd + 8 * c8 + 4);
-        const float4 b0 = *reinterpret_cast<const float4 *>(bs + 8 * c8);
-        const float4 b1 = *reinterpret_cast<const float4 *>(bs + 8 * c8 + 4);
-        const float lv[8] = {l0.x * b0.x, l0.y * b0.y, l0.z * b0.z, l0.w * b0.w,
-                             l1.x * b1.x, l1.y * b1.y, l1.z * b1.z, l1.w * b1.w};
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int s = c8 * 8 + 2 * e;
-            w[e] = pack2(s <= t ? lv[2 * e] : 0.f, s + 1 <= t ? lv[2 * e + 1] : 0.f);
-        }
-        *reinterpret_cast<uint4 *>(sm + pT + chunk_off(t, c8, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
         fence_proxy_async_smem();
         __syncthreads();
-        // ---------------------------------------------------------------- round 2: W = T K, U = T V
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(tmem + pcW, kmaj1(sm0 + pT, ks), mnmaj(sm0 + pK, 8192, ks), idKM, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(tmem + pcU, kmaj1(sm0 + pT, ks), mnmaj(sm0 + pV, 8192, ks), idKM, ks > 0);
-            umma_commit(mb);
-        }
-        if (__syncthreads_or(!wait_mma())) {
-            bad = 1;
-            break;
-        }
-        if (tid < kC) {
-            // rows of W and U -> bf16 images over the k and v tiles (their MMAs are done)
-            const int t = tid;
+        // ---------------------------------------------------------------- round 2: W = T K, then U = T V
+        // into the same accumulator; each becomes a bf16 image over the tile it
+        // was made from (k after W's product, v after U's)
 #pragma unroll 1
-            for (int j = 0; j < 8; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + (j < 4 ? pcW : pcU) + 32 * (j & 3), r);
-                tmem_ld_wait();
+        for (int wu = 0; wu < 2 && !bad; ++wu) {
+            if (tid == 0) {
+                tc_fence_after();
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    *reinterpret_cast<uint4 *>(sm + (j < 4 ? pK : pV) + chunk_off(t, 4 * (j & 3) + c4, 8192)) =
-                        pack8(r + 8 * c4);
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16(tmem + (wu ? pcU : pcW), kmaj1(sm0 + pT, ks), mnmaj(sm0 + (wu ? pV : pK), 8192, ks),
+                              idKM, ks > 0);
+                umma_commit(mb);
             }
+            if (__syncthreads_or(!wait_mma())) {
+                bad = 1;
+                break;
+            }
+            if (tid < kC) {
+                const int t = tid;
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + (wu ? pcU : pcW) + 32 * j, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        *reinterpret_cast<uint4 *>(sm + (wu ? pV : pK) + chunk_off(t, 4 * j + c4, 8192)) =
+                            pack8(r + 8 * c4);
+                }
+            }
+            tc_fence_before();
+            __syncthreads();
         }
-        tc_fence_before();
-        __syncthreads();
+        if (bad) break;
         // both images, 32 KiB, to the chunk's scratch slot
         uint4 *dst = reinterpret_cast<uint4 *>(img + ((size_t)bh * nch + n) * kImg);
         const uint4 *src = reinterpret_cast<const uint4 *>(sm + pK);
