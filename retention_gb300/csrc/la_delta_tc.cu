@@ -26,15 +26,21 @@
 //   delta_state_kernel  one CTA of 256 threads per (b, h), chunks in order; the
 //       state kept transposed in TMEM (S^T: lane = key channel i, column =
 //       value channel j, fp32) with a bf16 copy in shared memory. Per chunk:
-//       round 3  P = Q K^T, X = W S0^T, O = Q S0^T
-//                -> masked P (bf16), Ut = U - X (bf16)
-//       round 4  S^T += K^T Ut, O += P Ut -> the new bf16 copy of S^T, out (bf16)
-//       q, k and the chunk's W and U images come in two sets: chunk n + 1's are
-//       copied in (cp.async) while chunk n is processed.
+//       round 3  X = W S0^T, P = Q K^T, then O = Q S0^T
+//                -> Ut = U - X (bf16), masked P (bf16)
+//       round 4  S^T += K^T Ut, O += P Ut -> the new bf16 copy of S^T
+//       The tensor pipe runs products in issue order, so the state chain
+//       (X, Ut, S^T, the bf16 copy) leads each round; a chunk's out rows are
+//       read out of O while the next chunk's X and P run, before its O starts.
+//       q, k (TMA tiles) and the chunk's W and U images (one bulk copy) come
+//       in two sets; a set is refilled with chunk n + 2 as soon as chunk n's
+//       state product has read it.
 // Accumulators with 64 valid rows are M = 128 products whose rows 64..127 are
 // not read; warps 0, 1, 4 and 5 (TMEM lanes 0..63) own those rows, the two
 // warps of a lane quarter splitting the columns.
+#include <cudaTypedefs.h>
 #include <cstring>
+#include <mutex>
 
 #include "la_common.cuh"
 #include "sm100.cuh"
@@ -71,14 +77,22 @@ constexpr uint32_t sQo = 0, sKo = 16384, sWo = 32768, sUo = 49152;  // two 8 KiB
 constexpr uint32_t kP = 2 * kSet;          // P, K-major [64 x 64]
 constexpr uint32_t kU = kP + 8192;         // Ut, MN-major [64 tokens x 128], two halves
 constexpr uint32_t kS = kU + 16384;        // S^T copy, MN-major: 128 lines x 128 values, two 16 KiB halves
-constexpr uint32_t kBar = kS + 32768;      // mbarriers P, X, S, O, drain; TMEM address
-constexpr uint32_t kStateSmem = kBar + 48 + 1024;
+constexpr uint32_t kBar = kS + 32768;      // mbarriers P, X, S, O, drain, full[2]; TMEM address
+constexpr uint32_t kStateSmem = kBar + 64 + 1024;
 constexpr uint32_t cS = 0, cX = 128, cO = 256, cP = 384, kStateCols = 512;
 static_assert((kPrepSmem + 1024) * kPrepPerSm <= 233472 && kPrepCols * kPrepPerSm <= 512, "four prep CTAs per SM");
 static_assert(64 * kLd * 4 >= 16384, "T's M = 128 operand reads 8 KiB past T inside the fp32 block");
 static_assert(kStateSmem <= 232448, "state kernel shared memory");
 
 __device__ unsigned int g_delta_tc_error;
+
+// bulk global -> shared copy of `bytes` (a multiple of 16, both ends 16-byte
+// aligned) that completes a transaction count on `bar`
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 
 // 16-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -384,18 +398,25 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
 }
 
 // ============================================================================ state recurrence
-__global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const DeltaArgs a, const uint8_t *img,
-                                                                       int nch) {
+struct StateParams {
+    CUtensorMap tq, tk;  // [BH][L][128] bf16 as {128, L, BH}, box {64, 64, 1}, 128-byte swizzle
+    DeltaArgs a;
+    const uint8_t *img;
+    int nch;
+};
+
+__global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __grid_constant__ StateParams p) {
+    const DeltaArgs &a = p.a;
+    const uint8_t *img = p.img;
+    const int nch = p.nch;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, L = a.L;
     constexpr int kThreads = kStateThreads;
     uint64_t *mbP = reinterpret_cast<uint64_t *>(sm + kBar), *mbX = mbP + 1, *mbS = mbP + 2, *mbO = mbP + 3;
-    uint64_t *drain = mbP + 4;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kBar + 40);
-    const bf16 *q = static_cast<const bf16 *>(a.q) + (size_t)bh * L * kD;
-    const bf16 *k = static_cast<const bf16 *>(a.k) + (size_t)bh * L * kD;
+    uint64_t *drain = mbP + 4, *full = mbP + 5;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kBar + 56);
     const uint8_t *wu = img + (size_t)bh * nch * kImg;
     bf16 *out = static_cast<bf16 *>(a.out) + (size_t)bh * L * kD;
     const uint32_t sm0 = smem_u32(sm);
@@ -403,40 +424,36 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const Del
     const int qw = warp & 3, hf = warp >> 2;
     const bool low = qw < 2;  // TMEM lanes 0..63: the 64 token rows
     const int t = 32 * qw + lane;  // token row (low warps) or key channel (all warps)
+    // one thread of a high warp issues the MMAs, one of another the loads
+    constexpr int kIssuer = 96, kProducer = 64;  // warp 3 lane 0, warp 2 lane 0
+    const bool issuer = tid == kIssuer, producer = tid == kProducer;
 
-    // chunk m's q, k (swizzled tiles, zero rows past the sequence) and its W, U
-    // images (copied as they are) into set m % 2: 4096 chunks of 16 bytes
-    auto fetch = [&](int m) {
-        const int f0 = m * kC, fn = min(kC, L - f0);
-        const uint32_t set = sm0 + (uint32_t)(m & 1) * kSet;
-        const uint8_t *im = wu + (size_t)m * kImg;
+    // chunk m's q and k tiles (TMA: rows past the sequence read as zeros) and
+    // its W | U images (one bulk copy) into set m % 2, counted on full[m % 2]
+    auto load = [&](int m) {
+        const uint32_t so = (uint32_t)(m & 1) * kSet;
+        uint64_t *bar = full + (m & 1);
+        mbar_arrive_expect_tx(bar, kSet);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int x = tid + u * kThreads;  // q, k
-            const int mm = x >> 10, r = (x >> 4) & 63, c8 = x & 15;
-            const bool in = r < fn;
-            cp_async16(set + (mm ? sKo : sQo) + chunk_off(r, c8, 8192),
-                       (mm ? k : q) + (size_t)(f0 + (in ? r : 0)) * kD + c8 * 8, in ? 16u : 0u);
+        for (int h = 0; h < 2; ++h) {
+            tma_load_3d(sm + so + sQo + h * 8192, &p.tq, bar, 64 * h, m * kC, bh);
+            tma_load_3d(sm + so + sKo + h * 8192, &p.tk, bar, 64 * h, m * kC, bh);
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int x = tid + u * kThreads;  // W | U, contiguous
-            cp_async16(set + sWo + 16u * x, im + 16u * x, 16u);
-        }
-        cp_async_commit();
+        bulk_load(sm0 + so + sWo, wu + (size_t)m * kImg, kImg, bar);
     };
+    int issued = 0;  // loads issued (producer)
 
-    fetch(0);
     if (warp == 0) {
         tmem_alloc(tmem_slot, kStateCols);
         tmem_relinquish();
     }
-    if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(mbP + b, 1);
+    if (issuer) {
+        for (int b = 0; b < 7; ++b) mbar_init(mbP + b, 1);
         fence_mbar_init();
     }
     // S0 = 0: the bf16 copy starts at zero
     for (int i = tid; i < 32768 / 16; i += kThreads) reinterpret_cast<uint4 *>(sm + kS)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // the tensor core reads the copy
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -444,58 +461,72 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const Del
     const uint32_t lane_base = (uint32_t)(qw * 32) << 16;
     int bad = 0;
     const int nchunks = nch;
+    // out rows of chunk m (low warps, value channels 64 hf .. 64 hf + 63), once
+    // mbO has seen its last product; the warp loads together (tcgen05.ld is
+    // collective) and drops rows past a ragged chunk
+    auto read_out = [&](int m) -> bool {
+        const bool ok = mbar_wait(mbO, (uint32_t)m & 1u, kWaitNs);
+        tc_fence_after();
+        const int nt = min(kC, L - m * kC);
+        uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)(m * kC + t) * kD + 64 * hf);
+        uint32_t r[2][32];
+        tmem_ld32(tmem + lane_base + cO + 64 * hf, r[0]);
+        tmem_ld32(tmem + lane_base + cO + 64 * hf + 32, r[1]);
+        tmem_ld_wait();
+        if (t < nt) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) __stcs(dst + 4 * j + c4, pack8(r[j] + 8 * c4));
+        }
+        return ok;
+    };
+    if (producer) {
+        tma_prefetch_desc(&p.tq);
+        tma_prefetch_desc(&p.tk);
+        for (; issued < min(2, nchunks); ++issued) load(issued);
+    }
     for (int n = 0; n < nchunks; ++n) {
-        const int t0 = n * kC, nt = min(kC, L - t0);
         const uint32_t ph = (uint32_t)n & 1u;
         const uint32_t set = sm0 + (uint32_t)(n & 1) * kSet;
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        __syncthreads();
+        // this chunk's tiles (the previous chunk's closing barrier already
+        // ordered its bf16 state copy before this round)
+        int fail = !mbar_wait(full + (n & 1), (uint32_t)(n >> 1) & 1u, kWaitNs);
         // ---------------------------------------------------------------- round 3
-        if (tid == 0) {
+        // X first (the state chain waits on it), then P; O = Q S0^T follows once
+        // the previous chunk's out rows are read out of its accumulator
+        if (issuer) {
             tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                umma_bf16(tmem + cP, kmaj2(set + sQo, ks), kmaj2(set + sKo, ks), id64, ks > 0);
-            umma_commit(mbP);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 umma_bf16(tmem + cX, kmaj2(set + sWo, ks), mnmaj(sm0 + kS, 16384, ks), idKM, ks > 0);
             umma_commit(mbX);
-            // O = Q S0^T runs while the threads form P and Ut
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                umma_bf16(tmem + cO, kmaj2(set + sQo, ks), mnmaj(sm0 + kS, 16384, ks), idKM, ks > 0);
+                umma_bf16(tmem + cP, kmaj2(set + sQo, ks), kmaj2(set + sKo, ks), id64, ks > 0);
+            umma_commit(mbP);
         }
-        // the next chunk's tiles, in flight while this chunk runs (their set
-        // was last read by chunk n - 1's MMAs, which are done)
-        if (n + 1 < nchunks) fetch(n + 1);
-        int fail = 0;
-        if (low) {
-            // P row t, columns 32 hf .. 32 hf + 31: q_t . k_s (s <= t), bf16 K-major
-            if (!mbar_wait(mbP, ph, kWaitNs)) fail = 1;
-            tc_fence_after();
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + cP + 32 * hf, r);
-            tmem_ld_wait();
+        if (low && n > 0 && !read_out(n - 1)) fail = 1;
+        if (low || warp == kIssuer / 32) {
+            tc_fence_before();
+            named_sync<1, 160>();  // the low warps have read chunk n - 1's out rows
+            if (issuer) {
+                tc_fence_after();
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int s = 32 * hf + 8 * c4 + 2 * e;
-                    w[e] = pack2(s <= t ? __uint_as_float(r[8 * c4 + 2 * e]) : 0.f,
-                                 s + 1 <= t ? __uint_as_float(r[8 * c4 + 2 * e + 1]) : 0.f);
-                }
-                *reinterpret_cast<uint4 *>(sm + kP + chunk_off(t, 4 * hf + c4, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16(tmem + cO, kmaj2(set + sQo, ks), mnmaj(sm0 + kS, 16384, ks), idKM, ks > 0);
             }
+        }
+        if (low) {
             // Ut row t, value channels 64 hf .. 64 hf + 63: U - X, bf16 MN-major
             if (!mbar_wait(mbX, ph, kWaitNs)) fail = 1;
             tc_fence_after();
-#pragma unroll 1
+            uint32_t r[2][32];
+            tmem_ld32(tmem + lane_base + cX + 64 * hf, r[0]);
+            tmem_ld32(tmem + lane_base + cX + 64 * hf + 32, r[1]);
+            tmem_ld_wait();
+#pragma unroll
             for (int j = 0; j < 2; ++j) {
-                tmem_ld32(tmem + lane_base + cX + 64 * hf + 32 * j, r);
-                tmem_ld_wait();
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
                     const int c8 = 8 * hf + 4 * j + c4;
@@ -504,10 +535,26 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const Del
                     uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        w[e] = pack2(__uint_as_float(uw[e] << 16) - __uint_as_float(r[8 * c4 + 2 * e]),
-                                     __uint_as_float(uw[e] & 0xffff0000u) - __uint_as_float(r[8 * c4 + 2 * e + 1]));
+                        w[e] = pack2(__uint_as_float(uw[e] << 16) - __uint_as_float(r[j][8 * c4 + 2 * e]),
+                                     __uint_as_float(uw[e] & 0xffff0000u) - __uint_as_float(r[j][8 * c4 + 2 * e + 1]));
                     *reinterpret_cast<uint4 *>(sm + kU + chunk_off(t, c8, 8192)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
+            }
+            // P row t, columns 32 hf .. 32 hf + 31: q_t . k_s (s <= t), bf16 K-major
+            if (!mbar_wait(mbP, ph, kWaitNs)) fail = 1;
+            tc_fence_after();
+            tmem_ld32(tmem + lane_base + cP + 32 * hf, r[0]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int s = 32 * hf + 8 * c4 + 2 * e;
+                    w[e] = pack2(s <= t ? __uint_as_float(r[0][8 * c4 + 2 * e]) : 0.f,
+                                 s + 1 <= t ? __uint_as_float(r[0][8 * c4 + 2 * e + 1]) : 0.f);
+                }
+                *reinterpret_cast<uint4 *>(sm + kP + chunk_off(t, 4 * hf + c4, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
         }
         fence_proxy_async_smem();
@@ -517,7 +564,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const Del
             break;
         }
         // ---------------------------------------------------------------- round 4
-        if (tid == 0) {
+        if (issuer) {
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -529,35 +576,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const Del
             umma_commit(mbO);
         }
         {
-            // S^T line i = t (TMEM lane), value channels 64 hf .. 64 hf + 63 -> bf16 copy
+            // S^T line i = t (TMEM lane), value channels 64 hf .. 64 hf + 63 ->
+            // bf16 copy (every product that read the old copy came before mbS)
             if (!mbar_wait(mbS, ph, kWaitNs)) fail = 1;
             tc_fence_after();
-#pragma unroll 1
-            for (int j = 0; j < 2; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + cS + 64 * hf + 32 * j, r);
-                tmem_ld_wait();
+            // every reader of this chunk's set is done (its products came before
+            // mbS, the U rows were read before round 4): refill it with chunk n + 2
+            if (producer && !fail && issued < nchunks) load(issued++);
+            uint32_t r[2][32];
+            tmem_ld32(tmem + lane_base + cS + 64 * hf, r[0]);
+            tmem_ld32(tmem + lane_base + cS + 64 * hf + 32, r[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
-                    *reinterpret_cast<uint4 *>(sm + kS + chunk_off(t, 8 * hf + 4 * j + c4, 16384)) = pack8(r + 8 * c4);
-            }
-        }
-        if (low) {
-            // out row t, value channels 64 hf .. 64 hf + 63 (the warp loads
-            // together: tcgen05.ld is collective; rows past a ragged chunk are dropped)
-            if (!mbar_wait(mbO, ph, kWaitNs)) fail = 1;
-            tc_fence_after();
-            uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)(t0 + t) * kD + 64 * hf);
-#pragma unroll 1
-            for (int j = 0; j < 2; ++j) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + cO + 64 * hf + 32 * j, r);
-                tmem_ld_wait();
-                if (t < nt) {
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) __stcs(dst + 4 * j + c4, pack8(r + 8 * c4));
-                }
-            }
+                    *reinterpret_cast<uint4 *>(sm + kS + chunk_off(t, 8 * hf + 4 * j + c4, 16384)) = pack8(r[j] + 8 * c4);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -566,6 +600,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const Del
             break;
         }
     }
+    // the last chunk's out rows
+    if (!bad && low && nchunks > 0) {
+        if (!read_out(nchunks - 1)) bad = 1;
+    }
+    bad = __syncthreads_or(bad);
     if (!bad && a.final_state) {
         // S = (S^T)^T: state block [d_v][d_k]; thread (i = t, half hf) writes
         // column i over value rows 64 hf .. 64 hf + 63
@@ -583,11 +622,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const Del
     // teardown: no copy may still be landing in shared memory, and every MMA
     // issued has completed (the waits saw it, or on a time-out a final commit
     // is waited for, bounded)
-    cp_async_wait_all();
     if (bad) {
-        if (tid == 0) {
+        if (issuer) {
             atomicOr(&g_delta_tc_error, 2u);
             umma_commit(drain);
+        }
+        if (producer) {
+            // the last load of each set (every earlier one was waited for)
+            for (int m = max(0, issued - 2); m < issued; ++m) mbar_wait(full + (m & 1), (uint32_t)(m >> 1) & 1u, kWaitNs);
         }
         __syncthreads();
         mbar_wait(drain, 0u, kWaitNs);
@@ -602,12 +644,40 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const Del
 
 }  // namespace
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult qr;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// [BH][L][128] bf16 as {128, L, BH}; box {64 columns, 64 rows, 1}, 128-byte swizzle
+bool make_tile_map(CUtensorMap *m, const void *base, int L, int BH) {
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)L, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)L * kD * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kC, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 bool delta_tc_supports(const DeltaArgs &a) {
     if ((a.mode & LA_DTYPE_F32) || a.dk != kD || a.dv != kD || a.L < 1) return false;
     int dev = 0, major = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
-    return major == 10;
+    return major == 10 && get_encode();
 }
 
 int launch_delta_tc(const DeltaArgs &a, cudaStream_t s, int *launches) {
@@ -619,14 +689,20 @@ int launch_delta_tc(const DeltaArgs &a, cudaStream_t s, int *launches) {
         cudaFuncSetAttribute(delta_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem) !=
             cudaSuccess)
         return LA_ERR_CUDA;
+    StateParams sp;
+    if (!get_encode() || !make_tile_map(&sp.tq, a.q, a.L, (int)nbh) || !make_tile_map(&sp.tk, a.k, a.L, (int)nbh))
+        return LA_ERR_CUDA;
     void *img = nullptr;
     if (cudaMallocAsync(&img, (size_t)nbh * nch * kImg, s) != cudaSuccess) return LA_ERR_CUDA;
+    sp.a = a;
+    sp.img = static_cast<const uint8_t *>(img);
+    sp.nch = nch;
     int rc = LA_OK;
     delta_prep_kernel<<<(unsigned)(nbh * nch), kPrepThreads, kPrepSmem, s>>>(a, static_cast<uint8_t *>(img), nch);
     if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
     if (rc == LA_OK) {
         ++*launches;
-        delta_state_kernel<<<(unsigned)nbh, kStateThreads, kStateSmem, s>>>(a, static_cast<const uint8_t *>(img), nch);
+        delta_state_kernel<<<(unsigned)nbh, kStateThreads, kStateSmem, s>>>(sp);
         if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
         else ++*launches;
     }
