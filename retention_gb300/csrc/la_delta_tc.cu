@@ -77,7 +77,8 @@ constexpr uint32_t sQo = 0, sKo = 16384, sWo = 32768, sUo = 49152;  // two 8 KiB
 constexpr uint32_t kP = 2 * kSet;          // P, K-major [64 x 64]
 constexpr uint32_t kU = kP + 8192;         // Ut, MN-major [64 tokens x 128], two halves
 constexpr uint32_t kS = kU + 16384;        // S^T copy, MN-major: 128 lines x 128 values, two 16 KiB halves
-constexpr uint32_t kBar = kS + 32768;      // mbarriers P, X, S, O, drain, full[2]; TMEM address
+constexpr uint32_t kOs = kS + 32768;       // out rows of a chunk, bf16 [64 x 128] as two swizzled halves (TMA store)
+constexpr uint32_t kBar = kOs + 16384;     // mbarriers P, X, S, O, drain, full[2]; TMEM address
 constexpr uint32_t kStateSmem = kBar + 64 + 1024;
 constexpr uint32_t cS = 0, cX = 128, cO = 256, cP = 384, kStateCols = 512;
 static_assert((kPrepSmem + 1024) * kPrepPerSm <= 233472 && kPrepCols * kPrepPerSm <= 512, "four prep CTAs per SM");
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
 
 // ============================================================================ state recurrence
 struct StateParams {
-    CUtensorMap tq, tk;  // [BH][L][128] bf16 as {128, L, BH}, box {64, 64, 1}, 128-byte swizzle
+    CUtensorMap tq, tk, to;  // [BH][L][128] bf16 as {128, L, BH}, box {64, 64, 1}, 128-byte swizzle
     DeltaArgs a;
     const uint8_t *img;
     int nch;
@@ -412,13 +413,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x, L = a.L;
+    const int bh = blockIdx.x;
     constexpr int kThreads = kStateThreads;
     uint64_t *mbP = reinterpret_cast<uint64_t *>(sm + kBar), *mbX = mbP + 1, *mbS = mbP + 2, *mbO = mbP + 3;
     uint64_t *drain = mbP + 4, *full = mbP + 5;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kBar + 56);
     const uint8_t *wu = img + (size_t)bh * nch * kImg;
-    bf16 *out = static_cast<bf16 *>(a.out) + (size_t)bh * L * kD;
     const uint32_t sm0 = smem_u32(sm);
     // lane quarter of the warp (TMEM lanes 32 qw .. 32 qw + 31) and its column half
     const int qw = warp & 3, hf = warp >> 2;
@@ -462,28 +462,32 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
     int bad = 0;
     const int nchunks = nch;
     // out rows of chunk m (low warps, value channels 64 hf .. 64 hf + 63), once
-    // mbO has seen its last product; the warp loads together (tcgen05.ld is
-    // collective) and drops rows past a ragged chunk
+    // mbO has seen its last product, into the staging tile; store_out(m) then
+    // writes the tile with two TMA stores (rows past the sequence are clipped)
     auto read_out = [&](int m) -> bool {
         const bool ok = mbar_wait(mbO, (uint32_t)m & 1u, kWaitNs);
         tc_fence_after();
-        const int nt = min(kC, L - m * kC);
-        uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t)(m * kC + t) * kD + 64 * hf);
         uint32_t r[2][32];
         tmem_ld32(tmem + lane_base + cO + 64 * hf, r[0]);
         tmem_ld32(tmem + lane_base + cO + 64 * hf + 32, r[1]);
         tmem_ld_wait();
-        if (t < nt) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) __stcs(dst + 4 * j + c4, pack8(r[j] + 8 * c4));
-        }
+            for (int c4 = 0; c4 < 4; ++c4)
+                *reinterpret_cast<uint4 *>(sm + kOs + chunk_off(t, 8 * hf + 4 * j + c4, 8192)) = pack8(r[j] + 8 * c4);
+        fence_proxy_async_smem();
         return ok;
+    };
+    auto store_out = [&](int m) {  // one thread, after the low warps' barrier
+        tma_store_3d(&p.to, sm + kOs, 0, m * kC, bh);
+        tma_store_3d(&p.to, sm + kOs + 8192, 64, m * kC, bh);
+        bulk_commit();
     };
     if (producer) {
         tma_prefetch_desc(&p.tq);
         tma_prefetch_desc(&p.tk);
+        tma_prefetch_desc(&p.to);
         for (; issued < min(2, nchunks); ++issued) load(issued);
     }
     for (int n = 0; n < nchunks; ++n) {
@@ -510,6 +514,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
         if (low || warp == kIssuer / 32) {
             tc_fence_before();
             named_sync<1, 160>();  // the low warps have read chunk n - 1's out rows
+            if (tid == 0 && n > 0) store_out(n - 1);
             if (issuer) {
                 tc_fence_after();
 #pragma unroll
@@ -525,12 +530,18 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
             tmem_ld32(tmem + lane_base + cX + 64 * hf, r[0]);
             tmem_ld32(tmem + lane_base + cX + 64 * hf + 32, r[1]);
             tmem_ld_wait();
+            // the eight U chunks first: the stores below could alias them as far
+            // as the compiler knows
+            uint4 uu[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                uu[c] = *reinterpret_cast<const uint4 *>(sm + (set - sm0) + sUo + chunk_off(t, 8 * hf + c, 8192));
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
                     const int c8 = 8 * hf + 4 * j + c4;
-                    const uint4 u4 = *reinterpret_cast<const uint4 *>(sm + (set - sm0) + sUo + chunk_off(t, c8, 8192));
+                    const uint4 u4 = uu[4 * j + c4];
                     const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
                     uint32_t w[4];
 #pragma unroll
@@ -556,6 +567,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
                 }
                 *reinterpret_cast<uint4 *>(sm + kP + chunk_off(t, 4 * hf + c4, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
+            // the staging tile is free again once the store has read it
+            if (tid == 0) bulk_wait_read<0>();
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -603,6 +616,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
     // the last chunk's out rows
     if (!bad && low && nchunks > 0) {
         if (!read_out(nchunks - 1)) bad = 1;
+        named_sync<2, 128>();
+        if (tid == 0) store_out(nchunks - 1);
     }
     bad = __syncthreads_or(bad);
     if (!bad && a.final_state) {
@@ -622,6 +637,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
     // teardown: no copy may still be landing in shared memory, and every MMA
     // issued has completed (the waits saw it, or on a time-out a final commit
     // is waited for, bounded)
+    if (tid == 0) bulk_wait<0>();  // the out stores are complete
     if (bad) {
         if (issuer) {
             atomicOr(&g_delta_tc_error, 2u);
@@ -690,7 +706,8 @@ int launch_delta_tc(const DeltaArgs &a, cudaStream_t s, int *launches) {
             cudaSuccess)
         return LA_ERR_CUDA;
     StateParams sp;
-    if (!get_encode() || !make_tile_map(&sp.tq, a.q, a.L, (int)nbh) || !make_tile_map(&sp.tk, a.k, a.L, (int)nbh))
+    if (!get_encode() || !make_tile_map(&sp.tq, a.q, a.L, (int)nbh) || !make_tile_map(&sp.tk, a.k, a.L, (int)nbh) ||
+        !make_tile_map(&sp.to, a.out, a.L, (int)nbh))
         return LA_ERR_CUDA;
     void *img = nullptr;
     if (cudaMallocAsync(&img, (size_t)nbh * nch * kImg, s) != cudaSuccess) return LA_ERR_CUDA;
