@@ -18,8 +18,9 @@
 // Two kernels. W and U do not depend on the state, so they are made for every
 // chunk at once, and only the state recurrence runs chunk after chunk:
 //   delta_prep_kernel   one CTA of 128 threads per (b, h, chunk), four CTAs per SM.
-//       round 1  K K^T -> L = I + A (fp32, shared); L^-1 in place by blocks of
-//                16 (diagonal blocks by substitution, then block rows) -> T (bf16)
+//       round 1  K K^T -> L = I + A (fp32, shared); L^-1 in place: the four
+//                16 x 16 diagonal blocks by substitution, then two merges of
+//                lower-triangular block pairs (16 -> 32 -> 64) -> T (bf16)
 //       round 2  W = T K, then U = T V (one 128-column accumulator) -> bf16,
 //                written to a scratch array as the shared-memory images the
 //                second kernel's operands need
@@ -61,9 +62,9 @@ constexpr uint32_t pK = 0, pV = 16384;   // [64 x 128] bf16 tiles, two 8 KiB hal
 constexpr int kLd = 68;                  // fp32 row: 16-byte aligned, rows 4 banks apart
 constexpr uint32_t kM = 32768;           // L = I + A, then L^-1 in place, fp32 [64][kLd];
 constexpr uint32_t pT = kM;              // then T over it, K-major bf16 [64 x 64]
-constexpr int kYd = 20;                         // Y row: 16 + 4, 16-byte aligned
-constexpr uint32_t kY = kM + 64 * kLd * 4;      // block-row partial products, fp32 [3][16][kYd]
-constexpr uint32_t kB = kY + 3 * 16 * kYd * 4;  // beta [64]
+constexpr int kZd = 36;                         // Z row: 32 + 4, 16-byte aligned
+constexpr uint32_t kY = kM + 64 * kLd * 4;      // merge products Z, fp32 [32][kZd]
+constexpr uint32_t kB = kY + 32 * kZd * 4;      // beta [64]
 constexpr uint32_t pBar = kB + 64 * 4;          // mbarriers (MMA, drain), TMEM address
 constexpr uint32_t kPrepSmem = pBar + 24 + 1024;
 // TMEM: A (64 columns), then W, then U, each read out before the next product
@@ -134,6 +135,30 @@ constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);   // K-major A and 
 constexpr uint32_t idKM = idesc_bf16(128, 128, false, true);   // K-major A, MN-major B
 constexpr uint32_t idMM = idesc_bf16(128, 128, true, true);    // MN-major A and B
 
+// D = (neg ? -1 : 1) A B for N x N fp32 blocks (row-major, row strides lda,
+// ldb, ldd multiples of 4 floats): output float4 number `item` (row item /
+// (N / 4), columns 4 (item % (N / 4)) .. + 3), one N-term dot product per column
+template <int N>
+__device__ __forceinline__ void blk_mm(float *D, int ldd, const float *A, int lda, const float *B, int ldb, int item,
+                                       bool neg) {
+    const int r = item / (N / 4), c0 = 4 * (item % (N / 4));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int k4 = 0; k4 < N; k4 += 4) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(A + r * lda + k4);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 b = *reinterpret_cast<const float4 *>(B + (k4 + e) * ldb + c0);
+            acc.x = fmaf(av[e], b.x, acc.x);
+            acc.y = fmaf(av[e], b.y, acc.y);
+            acc.z = fmaf(av[e], b.z, acc.z);
+            acc.w = fmaf(av[e], b.w, acc.w);
+        }
+    }
+    *reinterpret_cast<float4 *>(D + r * ldd + c0) = neg ? make_float4(-acc.x, -acc.y, -acc.z, -acc.w) : acc;
+}
+
 // ============================================================================ W, U
 __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(const DeltaArgs a, uint8_t *img, int nch) {
     extern __shared__ uint8_t smem_raw[];
@@ -145,13 +170,14 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
     // L and L^-1 share one array: each block of L^-1 is written over the block of
     // L that no later step reads
     float *Lm = reinterpret_cast<float *>(sm + kM), *Li = Lm;
-    float *Yb = reinterpret_cast<float *>(sm + kY), *bs = reinterpret_cast<float *>(sm + kB);
+    float *Z = reinterpret_cast<float *>(sm + kY), *bs = reinterpret_cast<float *>(sm + kB);
     uint64_t *mb = reinterpret_cast<uint64_t *>(sm + pBar), *drain = mb + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + pBar + 16);
     const bf16 *k = static_cast<const bf16 *>(a.k) + ((size_t)bh * L + t0) * kD;
     const bf16 *v = static_cast<const bf16 *>(a.v) + ((size_t)bh * L + t0) * kD;
     const bf16 *beta = static_cast<const bf16 *>(a.beta) + (size_t)bh * L + t0;
     const uint32_t sm0 = smem_u32(sm);
+    const float bpre = tid < nt ? to_f32(beta[tid]) : 0.f;  // in flight with the tiles
 
     // this chunk's k and v: 2 x 64 rows x 16 chunks of 16 bytes, 16 per
     // thread; rows past the sequence are zero-filled
@@ -173,7 +199,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
         mbar_init(drain, 1);
         fence_mbar_init();
     }
-    if (tid < kC) bs[tid] = tid < nt ? to_f32(beta[tid]) : 0.f;
+    if (tid < kC) bs[tid] = bpre;
     cp_async_wait_all();
     fence_proxy_async_smem();
     tc_fence_before();
@@ -245,71 +271,26 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int bi = 1; bi < 4; ++bi) {
-            // block row bi: Y_bj = sum_{m=j}^{bi-1} L_bi,m Li_m,j, then Li_bi,j = -Li_bi,bi Y_bj.
-            // A thread takes four adjacent columns of one row (float4 loads of
-            // Li and Y rows, one L value per four products); the zeros above
-            // the diagonal of Li_bi,bi make the second product a full 16 terms.
-#pragma unroll
-            for (int e0 = 0; e0 < bi * 64; e0 += kThreads) {
-                const int e = e0 + tid;
-                if (e < bi * 64) {
-                    const int j = e >> 6, r = (e >> 2) & 15, c0 = 4 * (e & 3);
-                    const float *lrow = Lm + (16 * bi + r) * kLd;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int kb = j; kb < bi; ++kb) {
-                        float lv[16];
-                        float4 iv[16];
-#pragma unroll
-                        for (int m = 0; m < 16; m += 4) {
-                            const float4 l4 = *reinterpret_cast<const float4 *>(lrow + 16 * kb + m);
-                            lv[m] = l4.x, lv[m + 1] = l4.y, lv[m + 2] = l4.z, lv[m + 3] = l4.w;
-                        }
-#pragma unroll
-                        for (int m = 0; m < 16; ++m)
-                            iv[m] = *reinterpret_cast<const float4 *>(Li + (16 * kb + m) * kLd + 16 * j + c0);
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) {
-                            acc.x = fmaf(lv[m], iv[m].x, acc.x);
-                            acc.y = fmaf(lv[m], iv[m].y, acc.y);
-                            acc.z = fmaf(lv[m], iv[m].z, acc.z);
-                            acc.w = fmaf(lv[m], iv[m].w, acc.w);
-                        }
-                    }
-                    *reinterpret_cast<float4 *>(Yb + (j * 16 + r) * kYd + c0) = acc;
-                }
-            }
+        // Merges: for a unit lower-triangular [[P, 0], [R, Q]] with P^-1, Q^-1
+        // known, the inverse's lower-left block is -Q^-1 (R P^-1). First the
+        // pairs of 16 x 16 diagonal blocks (0, 1) and (2, 3), then the two
+        // 32 x 32 halves; each product is written over blocks no later step reads.
+        {
+            const int pr = tid >> 6, it = tid & 63, o = 32 * pr;  // pair 0: rows/cols 0..31, pair 1: 32..63
+            blk_mm<16>(Z + pr * 16 * kZd, kZd, Lm + (o + 16) * kLd + o, kLd, Li + o * kLd + o, kLd, it, false);
             __syncthreads();
-#pragma unroll
-            for (int e0 = 0; e0 < bi * 64; e0 += kThreads) {
-                const int e = e0 + tid;
-                if (e < bi * 64) {
-                    const int j = e >> 6, r = (e >> 2) & 15, c0 = 4 * (e & 3);
-                    const float *irow = Li + (16 * bi + r) * kLd + 16 * bi;
-                    float lv[16];
-                    float4 yv[16];
-#pragma unroll
-                    for (int m = 0; m < 16; m += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4 *>(irow + m);
-                        lv[m] = l4.x, lv[m + 1] = l4.y, lv[m + 2] = l4.z, lv[m + 3] = l4.w;
-                    }
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) yv[m] = *reinterpret_cast<const float4 *>(Yb + (j * 16 + m) * kYd + c0);
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        acc.x = fmaf(lv[m], yv[m].x, acc.x);
-                        acc.y = fmaf(lv[m], yv[m].y, acc.y);
-                        acc.z = fmaf(lv[m], yv[m].z, acc.z);
-                        acc.w = fmaf(lv[m], yv[m].w, acc.w);
-                    }
-                    *reinterpret_cast<float4 *>(Li + (16 * bi + r) * kLd + 16 * j + c0) =
-                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-                }
-            }
+            blk_mm<16>(Li + (o + 16) * kLd + o, kLd, Li + (o + 16) * kLd + o + 16, kLd, Z + pr * 16 * kZd, kZd, it,
+                       true);
             __syncthreads();
         }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            blk_mm<32>(Z, kZd, Lm + 32 * kLd, kLd, Li, kLd, tid + 128 * h, false);
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            blk_mm<32>(Li + 32 * kLd, kLd, Li + 32 * kLd + 32, kLd, Z, kZd, tid + 128 * h, true);
+        __syncthreads();
         // T = L^-1 diag(beta), lower triangular, bf16 K-major, written over the
         // fp32 block once every thread has read its share
         {
@@ -370,15 +351,21 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
                             pack8(r + 8 * c4);
                 }
             }
+            fence_proxy_async_smem();  // the images leave by a bulk copy
             tc_fence_before();
             __syncthreads();
         }
         if (bad) break;
-        // both images, 32 KiB, to the chunk's scratch slot
-        uint4 *dst = reinterpret_cast<uint4 *>(img + ((size_t)bh * nch + n) * kImg);
-        const uint4 *src = reinterpret_cast<const uint4 *>(sm + pK);
-#pragma unroll
-        for (int u = 0; u < (int)(kImg / 16) / kThreads; ++u) dst[tid + u * kThreads] = src[tid + u * kThreads];
+        // both images, 32 KiB, to the chunk's scratch slot: one bulk copy,
+        // complete before the CTA's shared memory goes
+        if (tid == 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             img + ((size_t)bh * nch + n) * kImg),
+                         "r"(sm0 + pK), "r"(kImg)
+                         : "memory");
+            bulk_commit();
+            bulk_wait<0>();
+        }
     } while (0);
     if (bad) {
         // every MMA issued has completed before the TMEM goes: a barrier of its
