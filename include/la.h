@@ -301,6 +301,18 @@ const char *la_status_string(int status);
 /* Number of kernels this library has launched in this process (diagnostics). */
 unsigned long long la_kernel_launches(void);
 
+/*
+ * la_device_status -- waits for the work queued on `stream`, then reports
+ * whether any kernel of this library on the current device gave up a bounded
+ * wait since the last call: LA_ERR_TIMEOUT if one did (its outputs are not
+ * valid; the CUDA context stays usable), LA_OK if none did, LA_ERR_CUDA if the
+ * synchronisation or the read failed. Reading clears the flags. The kernels
+ * with such waits are the tensor-core chunk forward (which the tensor-core
+ * backward also runs) and the chunked delta rule; every wait gives up after
+ * 2 s of wall time, far beyond any legitimate one.
+ */
+int la_device_status(la_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -231,6 +231,16 @@ const char *la_status_string(int status) {
 
 unsigned long long la_kernel_launches(void) { return g_launches.load(); }
 
+int la_device_status(la_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
+    unsigned int tc = 0, delta = 0;
+    int rc = la::tc_error_take(&tc);
+    const int rc2 = la::delta_tc_error_take(&delta);
+    if (rc == LA_OK) rc = rc2;
+    if (rc != LA_OK) return rc;
+    return (tc | delta) ? LA_ERR_TIMEOUT : LA_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

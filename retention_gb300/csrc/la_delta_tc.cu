@@ -675,6 +675,16 @@ bool make_tile_map(CUtensorMap *m, const void *base, int L, int BH) {
 }
 }  // namespace
 
+// The error word of the two delta kernels (set when a bounded wait ran out),
+// read and cleared; the caller has synchronised the work that could set it.
+int delta_tc_error_take(unsigned int *value) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(value, g_delta_tc_error, sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_delta_tc_error, &zero, sizeof(unsigned int)) != cudaSuccess)
+        return LA_ERR_CUDA;
+    return LA_OK;
+}
+
 bool delta_tc_supports(const DeltaArgs &a) {
     if ((a.mode & LA_DTYPE_F32) || a.dk != kD || a.dv != kD || a.L < 1) return false;
     int dev = 0, major = 0;

@@ -998,6 +998,16 @@ int sm_count() {
 
 }  // namespace
 
+// The error word of the tensor-core forward (set when a bounded wait ran out),
+// read and cleared; the caller has synchronised the work that could set it.
+int tc_error_take(unsigned int *value) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(value, g_tc_error, sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(unsigned int)) != cudaSuccess)
+        return LA_ERR_CUDA;
+    return LA_OK;
+}
+
 bool chunk_tc_supports(const ChunkArgs &a) {
     if ((a.mode & LA_DTYPE_F32) || a.dk != kD || a.dv != kD || a.chunk != kC || a.L < 1) return false;
     int dev = 0, major = 0;

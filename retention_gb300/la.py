@@ -40,6 +40,7 @@ SIGNATURES = {
     "la_chunk_fwd_path": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "la_status_string": ([_I], ctypes.c_char_p),
     "la_kernel_launches": ([], ctypes.c_ulonglong),
+    "la_device_status": ([_VP], _I),
 }
 
 _lib = None
@@ -284,3 +285,10 @@ def chunk_fwd_path(B, H, L, dk, dv, mode, chunk):
 
 def kernel_launches():
     return int(load().la_kernel_launches())
+
+
+def device_status(stream=None):
+    """Wait for `stream` (default: torch's current stream) and return the
+    la_status of the library's bounded device-side waits since the last call:
+    0, or -5 (LA_ERR_TIMEOUT) if a kernel gave one up. Clears the flags."""
+    return int(load().la_device_status(_stream(stream)))

@@ -163,3 +163,20 @@ def test_bf16_workloads_take_the_tensor_core_kernel(name):
     assert la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], 128, 128, mode, 64) == 1
     assert la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], 128, 128, mode | la.LA_KERNEL_SIMT, 64) == 0
     assert la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], 128, 128, mode, 32) == 0
+
+
+def test_device_status_is_clean_after_the_bounded_wait_kernels():
+    """la_device_status: none of the kernels with bounded waits (the
+    tensor-core forward, the chunked delta rule) gave one up on ordinary
+    inputs, and a second read finds the flags still clear."""
+    from retention_gb300 import la
+    assert la.device_status() == 0  # no earlier call in this process gave a wait up
+    cfg = W.workload("la", B=1, H=2, L=300)
+    x = {n: t.cuda() for n, t in W.chunk_inputs(cfg, 1).items() if t is not None}
+    la.chunk_fwd(x["q"], x["k"], x["v"], phi="elu1", normalize=True, chunk=64)
+    dcfg = W.workload("delta", B=1, H=2, L=300)
+    d = {n: t.cuda() for n, t in W.delta_inputs(dcfg, 1).items()}
+    la.delta_fwd(d["q"], d["k"], d["v"], d["beta"])
+    assert la.device_status() == 0
+    assert la.device_status() == 0
+    assert la.load().la_status_string(-5).decode().startswith("LA_ERR_TIMEOUT")
