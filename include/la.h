@@ -94,7 +94,10 @@ typedef enum {
  * at most the number of SMs), the tensor-core path splits each sequence into
  * segments and takes stream-ordered scratch (cudaMallocAsync / cudaFreeAsync
  * on `stream`) for the per-segment states; a failed allocation returns
- * LA_ERR_CUDA.
+ * LA_ERR_CUDA. All stream-ordered scratch of this library comes from the
+ * device's default memory pool, whose release threshold the library raises
+ * the first time it allocates on a device: freed scratch stays mapped in the
+ * pool for the next call instead of being unmapped at every synchronisation.
  *
  * Range of the tensor-core kernel: it factors the decay inside a chunk as
  * exp(b_t) * exp(-b_s), b the log decay from the chunk start, which is exact
@@ -148,8 +151,12 @@ int la_chunk_fwd_from_state(const void *q, const void *k, const void *v, const v
  * and inside a chunk the u_t solve a unit lower-triangular system (I + A) U =
  * diag(beta) (V - K S0^T), A[t][s] = beta_t k_t . k_s for s < t, so a chunk
  * is a triangular inverse and a few matrix products (the recurrence
- * rearranged; no page gives this form). Every other case runs the recurrence
- * token by token on the CUDA cores in fp32 (6 d_k d_v flops a token).
+ * rearranged; no page gives this form). W = T K and U = T V (T = (I + A)^-1
+ * diag(beta)) do not depend on the state, so a first kernel makes them for
+ * every chunk at once into stream-ordered scratch (32 KiB per chunk of 64
+ * tokens and head; LA_ERR_CUDA if the allocation fails) and a second runs the
+ * state through the chunks. Every other case runs the recurrence token by
+ * token on the CUDA cores in fp32 (6 d_k d_v flops a token).
  * Errors as la_chunk_fwd; beta needs only element alignment.
  */
 int la_delta_fwd(const void *q, const void *k, const void *v, const void *beta,

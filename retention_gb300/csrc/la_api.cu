@@ -244,6 +244,37 @@ int la_device_status(la_stream_t stream) {
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// Scratch of the multi-kernel paths: stream-ordered allocations from the
+// device's default memory pool. The pool's release threshold is raised once
+// per device, so that memory freed at the end of one call stays mapped for the
+// next instead of being returned at the next synchronisation and mapped
+// again (which costs a large fraction of a call's time at these sizes). The
+// pool then keeps up to the largest scratch any call used.
+namespace la {
+namespace {
+std::mutex g_pool_mu;
+unsigned long long g_pool_done = 0;  // bit d: device d's pool threshold raised
+}  // namespace
+
+int scratch_alloc(void **p, size_t bytes, cudaStream_t s) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+    if (dev >= 0 && dev < 64) {
+        std::lock_guard<std::mutex> lock(g_pool_mu);
+        if (!(g_pool_done & (1ull << dev))) {
+            cudaMemPool_t pool;
+            uint64_t keep = UINT64_MAX;
+            if (cudaDeviceGetDefaultMemPool(&pool, dev) != cudaSuccess ||
+                cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
+                return LA_ERR_CUDA;
+            g_pool_done |= 1ull << dev;
+        }
+    }
+    return cudaMallocAsync(p, bytes, s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+}  // namespace la
+
+// ---------------------------------------------------------------------------
 // la_chunk_fwd_noalloc: la_chunk_fwd for callers that must not allocate device
 // memory. When a short batch makes the tensor-core path split sequences into
 // segments, its scratch comes from this fixed device array instead of

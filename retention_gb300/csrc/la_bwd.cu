@@ -505,7 +505,7 @@ size_t bwd_scratch_bytes(const BwdArgs &a) {
 int launch_bwd(const BwdArgs &a, cudaStream_t s, int *launches) {
     const size_t bytes = bwd_scratch_bytes(a);
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (scratch_alloc(&scratch, bytes, s) != LA_OK) return LA_ERR_CUDA;
     const size_t n = (size_t)a.B * a.H * a.L;
     float *f = static_cast<float *>(scratch);
     BwdParams p{a.q, a.k, a.v, a.gate, a.dout, a.grad_q, a.grad_k, a.grad_v, a.grad_g,

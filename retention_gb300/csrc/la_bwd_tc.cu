@@ -426,7 +426,7 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
     // bf16: K rv rd rq rk g' bracket_q bracket_k rdv; fp32: dQ / r; chunk totals
     const size_t bytes = 9 * hb + 2 * hb + (size_t)nbh * nch * kD * sizeof(float);
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (scratch_alloc(&scratch, bytes, s) != LA_OK) return LA_ERR_CUDA;
     char *b = static_cast<char *>(scratch);
     uint4 *h[9];
     for (int i = 0; i < 9; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
@@ -486,7 +486,7 @@ static int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
     // bf16: Q K J w E rv rw rq rk rE rdv; fp32: den_full U ZE rdkm rdz; den [rows]
     const size_t bytes = 11 * hb + 5 * fb + (size_t)rows * sizeof(float);
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (scratch_alloc(&scratch, bytes, s) != LA_OK) return LA_ERR_CUDA;
     char *b = static_cast<char *>(scratch);
     uint4 *h[11];
     for (int i = 0; i < 11; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
@@ -547,7 +547,7 @@ int launch_bwd_tc(const BwdArgs &a, cudaStream_t s, int *launches) {
     // rv, rd, rq, rk, rdk, rdv; with elu1 also K = phi(k) and dQ
     const int narr = elu1 ? 8 : 6;
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, narr * arr, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (scratch_alloc(&scratch, narr * arr, s) != LA_OK) return LA_ERR_CUDA;
     char *b = static_cast<char *>(scratch);
     uint4 *rv = reinterpret_cast<uint4 *>(b), *rd = reinterpret_cast<uint4 *>(b + arr);
     uint4 *rq = reinterpret_cast<uint4 *>(b + 2 * arr), *rk = reinterpret_cast<uint4 *>(b + 3 * arr);

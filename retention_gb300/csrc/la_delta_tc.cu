@@ -707,7 +707,7 @@ int launch_delta_tc(const DeltaArgs &a, cudaStream_t s, int *launches) {
         !make_tile_map(&sp.to, a.out, a.L, (int)nbh))
         return LA_ERR_CUDA;
     void *img = nullptr;
-    if (cudaMallocAsync(&img, (size_t)nbh * nch * kImg, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (scratch_alloc(&img, (size_t)nbh * nch * kImg, s) != LA_OK) return LA_ERR_CUDA;
     sp.a = a;
     sp.img = static_cast<const uint8_t *>(img);
     sp.nch = nch;

@@ -1099,7 +1099,7 @@ int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches) {
     const size_t bytes = chunk_tc_scratch_bytes(a);
     if (bytes == 0) return launch_chunk_tc_into(a, s, launches, nullptr, 0);
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, bytes, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (scratch_alloc(&scratch, bytes, s) != LA_OK) return LA_ERR_CUDA;
     int rc = launch_chunk_tc_into(a, s, launches, scratch, bytes);
     if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
     return rc;
