@@ -65,8 +65,8 @@ constexpr uint32_t pT = kM;              // then T over it, K-major bf16 [64 x 6
 constexpr int kZd = 36;                         // Z row: 32 + 4, 16-byte aligned
 constexpr uint32_t kY = kM + 64 * kLd * 4;      // merge products Z, fp32 [32][kZd]
 constexpr uint32_t kB = kY + 32 * kZd * 4;      // beta [64]
-constexpr uint32_t pBar = kB + 64 * 4;          // mbarriers (MMA, drain), TMEM address
-constexpr uint32_t kPrepSmem = pBar + 24 + 1024;
+constexpr uint32_t pBar = kB + 64 * 4;          // mbarriers (MMA, drain, tiles), TMEM address
+constexpr uint32_t kPrepSmem = pBar + 32 + 1024;
 // TMEM: A (64 columns), then W, then U, each read out before the next product
 constexpr uint32_t pcA = 0, pcW = 0, pcU = 0, kPrepCols = 128;
 constexpr int kPrepPerSm = 4;
@@ -95,13 +95,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
-
-// 16-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -136,31 +129,51 @@ constexpr uint32_t idKM = idesc_bf16(128, 128, false, true);   // K-major A, MN-
 constexpr uint32_t idMM = idesc_bf16(128, 128, true, true);    // MN-major A and B
 
 // D = (neg ? -1 : 1) A B for N x N fp32 blocks (row-major, row strides lda,
-// ldb, ldd multiples of 4 floats): output float4 number `item` (row item /
-// (N / 4), columns 4 (item % (N / 4)) .. + 3), one N-term dot product per column
+// ldb, ldd multiples of 4 floats), two rows per thread: item (0 .. N^2 / 8 - 1)
+// takes rows r and r + N / 2 (r = item / (N / 4)) and columns 4 (item % (N / 4))
+// .. + 3. The two rows share every load of B: the shared-memory pipe is what
+// bounds this kernel.
 template <int N>
-__device__ __forceinline__ void blk_mm(float *D, int ldd, const float *A, int lda, const float *B, int ldb, int item,
-                                       bool neg) {
+__device__ __forceinline__ void blk_mm2(float *D, int ldd, const float *A, int lda, const float *B, int ldb, int item,
+                                        bool neg) {
     const int r = item / (N / 4), c0 = 4 * (item % (N / 4));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+#pragma unroll 2
     for (int k4 = 0; k4 < N; k4 += 4) {
-        const float4 a4 = *reinterpret_cast<const float4 *>(A + r * lda + k4);
-        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+        const float4 a0 = *reinterpret_cast<const float4 *>(A + r * lda + k4);
+        const float4 a1 = *reinterpret_cast<const float4 *>(A + (r + N / 2) * lda + k4);
+        const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float4 b = *reinterpret_cast<const float4 *>(B + (k4 + e) * ldb + c0);
-            acc.x = fmaf(av[e], b.x, acc.x);
-            acc.y = fmaf(av[e], b.y, acc.y);
-            acc.z = fmaf(av[e], b.z, acc.z);
-            acc.w = fmaf(av[e], b.w, acc.w);
+            acc0.x = fmaf(av0[e], b.x, acc0.x);
+            acc0.y = fmaf(av0[e], b.y, acc0.y);
+            acc0.z = fmaf(av0[e], b.z, acc0.z);
+            acc0.w = fmaf(av0[e], b.w, acc0.w);
+            acc1.x = fmaf(av1[e], b.x, acc1.x);
+            acc1.y = fmaf(av1[e], b.y, acc1.y);
+            acc1.z = fmaf(av1[e], b.z, acc1.z);
+            acc1.w = fmaf(av1[e], b.w, acc1.w);
         }
     }
-    *reinterpret_cast<float4 *>(D + r * ldd + c0) = neg ? make_float4(-acc.x, -acc.y, -acc.z, -acc.w) : acc;
+    const float s = neg ? -1.f : 1.f;
+    *reinterpret_cast<float4 *>(D + r * ldd + c0) = make_float4(s * acc0.x, s * acc0.y, s * acc0.z, s * acc0.w);
+    *reinterpret_cast<float4 *>(D + (r + N / 2) * ldd + c0) =
+        make_float4(s * acc1.x, s * acc1.y, s * acc1.z, s * acc1.w);
 }
 
 // ============================================================================ W, U
-__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(const DeltaArgs a, uint8_t *img, int nch) {
+struct PrepParams {
+    CUtensorMap tk, tv;  // [BH][L][128] bf16 as {128, L, BH}, box {64, 64, 1}, 128-byte swizzle
+    DeltaArgs a;
+    uint8_t *img;
+    int nch;
+};
+
+__global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(const __grid_constant__ PrepParams p) {
+    const DeltaArgs &a = p.a;
+    uint8_t *img = p.img;
+    const int nch = p.nch;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -171,43 +184,36 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
     // L that no later step reads
     float *Lm = reinterpret_cast<float *>(sm + kM), *Li = Lm;
     float *Z = reinterpret_cast<float *>(sm + kY), *bs = reinterpret_cast<float *>(sm + kB);
-    uint64_t *mb = reinterpret_cast<uint64_t *>(sm + pBar), *drain = mb + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + pBar + 16);
-    const bf16 *k = static_cast<const bf16 *>(a.k) + ((size_t)bh * L + t0) * kD;
-    const bf16 *v = static_cast<const bf16 *>(a.v) + ((size_t)bh * L + t0) * kD;
+    uint64_t *mb = reinterpret_cast<uint64_t *>(sm + pBar), *drain = mb + 1, *tiles = mb + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + pBar + 24);
     const bf16 *beta = static_cast<const bf16 *>(a.beta) + (size_t)bh * L + t0;
     const uint32_t sm0 = smem_u32(sm);
     const float bpre = tid < nt ? to_f32(beta[tid]) : 0.f;  // in flight with the tiles
 
-    // this chunk's k and v: 2 x 64 rows x 16 chunks of 16 bytes, 16 per
-    // thread; rows past the sequence are zero-filled
+    // this chunk's k and v tiles by TMA (rows past the sequence read as zeros)
+    if (tid == 0) {
+        mbar_init(mb, 1);
+        mbar_init(drain, 1);
+        mbar_init(tiles, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(tiles, 4 * 8192);
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-        const int x = tid + u * kThreads;
-        const int mm = x >> 10, r = (x >> 4) & 63, c8 = x & 15;
-        const bool in = r < nt;
-        cp_async16(sm0 + (mm ? pV : pK) + chunk_off(r, c8, 8192), (mm ? v : k) + (size_t)(in ? r : 0) * kD + c8 * 8,
-                   in ? 16u : 0u);
+        for (int h = 0; h < 2; ++h) {
+            tma_load_3d(sm + pK + h * 8192, &p.tk, tiles, 64 * h, t0, bh);
+            tma_load_3d(sm + pV + h * 8192, &p.tv, tiles, 64 * h, t0, bh);
+        }
     }
-    cp_async_commit();
     if (warp == 0) {
         tmem_alloc(tmem_slot, kPrepCols);
         tmem_relinquish();
     }
-    if (tid == 0) {
-        mbar_init(mb, 1);
-        mbar_init(drain, 1);
-        fence_mbar_init();
-    }
     if (tid < kC) bs[tid] = bpre;
-    cp_async_wait_all();
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    int bad = 0;
+    int bad = __syncthreads_or(!mbar_wait(tiles, 0u, kWaitNs));
     uint32_t phase = 0;
     auto wait_mma = [&]() -> bool {
         const bool ok = mbar_wait(mb, phase & 1u, kWaitNs);
@@ -216,7 +222,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
         return ok;
     };
 
-    do {
+    while (!bad) {
         // ---------------------------------------------------------------- round 1: K K^T
         if (tid == 0) {
 #pragma unroll
@@ -276,32 +282,32 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
         // pairs of 16 x 16 diagonal blocks (0, 1) and (2, 3), then the two
         // 32 x 32 halves; each product is written over blocks no later step reads.
         {
-            const int pr = tid >> 6, it = tid & 63, o = 32 * pr;  // pair 0: rows/cols 0..31, pair 1: 32..63
-            blk_mm<16>(Z + pr * 16 * kZd, kZd, Lm + (o + 16) * kLd + o, kLd, Li + o * kLd + o, kLd, it, false);
+            // 2 x 32 items: warp 0 takes pair 0 (rows/cols 0..31), warp 1 pair 1 (32..63)
+            const int pr = tid >> 5, it = tid & 31, o = 32 * pr;
+            if (tid < 64)
+                blk_mm2<16>(Z + pr * 16 * kZd, kZd, Lm + (o + 16) * kLd + o, kLd, Li + o * kLd + o, kLd, it, false);
             __syncthreads();
-            blk_mm<16>(Li + (o + 16) * kLd + o, kLd, Li + (o + 16) * kLd + o + 16, kLd, Z + pr * 16 * kZd, kZd, it,
-                       true);
+            if (tid < 64)
+                blk_mm2<16>(Li + (o + 16) * kLd + o, kLd, Li + (o + 16) * kLd + o + 16, kLd, Z + pr * 16 * kZd, kZd,
+                            it, true);
             __syncthreads();
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-            blk_mm<32>(Z, kZd, Lm + 32 * kLd, kLd, Li, kLd, tid + 128 * h, false);
+        blk_mm2<32>(Z, kZd, Lm + 32 * kLd, kLd, Li, kLd, tid, false);
         __syncthreads();
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-            blk_mm<32>(Li + 32 * kLd, kLd, Li + 32 * kLd + 32, kLd, Z, kZd, tid + 128 * h, true);
+        blk_mm2<32>(Li + 32 * kLd, kLd, Li + 32 * kLd + 32, kLd, Z, kZd, tid, true);
         __syncthreads();
         // T = L^-1 diag(beta), lower triangular, bf16 K-major, written over the
         // fp32 block once every thread has read its share
         {
             uint4 tw[kC * 8 / kThreads];
+            // a thread's eight columns are the same in every row it takes
+            const float4 b0 = *reinterpret_cast<const float4 *>(bs + 8 * (tid & 7));
+            const float4 b1 = *reinterpret_cast<const float4 *>(bs + 8 * (tid & 7) + 4);
 #pragma unroll
             for (int u = 0; u < kC * 8 / kThreads; ++u) {
                 const int x = u * kThreads + tid, t = x >> 3, c8 = x & 7;
                 const float4 l0 = *reinterpret_cast<const float4 *>(Li + t * kLd + 8 * c8);
                 const float4 l1 = *reinterpret_cast<const float4 *>(Li + t * kLd + 8 * c8 + 4);
-                const float4 b0 = *reinterpret_cast<const float4 *>(bs + 8 * c8);
-                const float4 b1 = *reinterpret_cast<const float4 *>(bs + 8 * c8 + 4);
                 const float lv[8] = {l0.x * b0.x, l0.y * b0.y, l0.z * b0.z, l0.w * b0.w,
                                      l1.x * b1.x, l1.y * b1.y, l1.z * b1.z, l1.w * b1.w};
                 uint32_t w[4];
@@ -366,16 +372,19 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepPerSm) delta_prep_kernel(co
             bulk_commit();
             bulk_wait<0>();
         }
-    } while (0);
+        break;
+    }
     if (bad) {
         // every MMA issued has completed before the TMEM goes: a barrier of its
-        // own, committed once, so its phase is known whatever timed out (bounded)
+        // own, committed once, so its phase is known whatever timed out; and the
+        // tile loads have landed (both bounded)
         if (tid == 0) {
             atomicOr(&g_delta_tc_error, 1u);
             umma_commit(drain);
         }
         __syncthreads();
         mbar_wait(drain, 0u, kWaitNs);
+        mbar_wait(tiles, 0u, kWaitNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -711,8 +720,17 @@ int launch_delta_tc(const DeltaArgs &a, cudaStream_t s, int *launches) {
     sp.a = a;
     sp.img = static_cast<const uint8_t *>(img);
     sp.nch = nch;
+    PrepParams pp;
+    pp.tk = sp.tk;
+    if (!make_tile_map(&pp.tv, a.v, a.L, (int)nbh)) {
+        cudaFreeAsync(img, s);
+        return LA_ERR_CUDA;
+    }
+    pp.a = a;
+    pp.img = static_cast<uint8_t *>(img);
+    pp.nch = nch;
     int rc = LA_OK;
-    delta_prep_kernel<<<(unsigned)(nbh * nch), kPrepThreads, kPrepSmem, s>>>(a, static_cast<uint8_t *>(img), nch);
+    delta_prep_kernel<<<(unsigned)(nbh * nch), kPrepThreads, kPrepSmem, s>>>(pp);
     if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
     if (rc == LA_OK) {
         ++*launches;
