@@ -79,8 +79,8 @@ constexpr uint32_t kP = 2 * kSet;          // P, K-major [64 x 64]
 constexpr uint32_t kU = kP + 8192;         // Ut, MN-major [64 tokens x 128], two halves
 constexpr uint32_t kS = kU + 16384;        // S^T copy, MN-major: 128 lines x 128 values, two 16 KiB halves
 constexpr uint32_t kOs = kS + 32768;       // out rows of a chunk, bf16 [64 x 128] as two swizzled halves (TMA store)
-constexpr uint32_t kBar = kOs + 16384;     // mbarriers P, X, S, O, drain, full[2]; TMEM address
-constexpr uint32_t kStateSmem = kBar + 64 + 1024;
+constexpr uint32_t kBar = kOs + 16384;     // mbarriers P, X, S, O, drain, full[2], ofree; TMEM address
+constexpr uint32_t kStateSmem = kBar + 80 + 1024;
 constexpr uint32_t cS = 0, cX = 128, cO = 256, cP = 384, kStateCols = 512;
 static_assert((kPrepSmem + 1024) * kPrepPerSm <= 233472 && kPrepCols * kPrepPerSm <= 512, "four prep CTAs per SM");
 static_assert(64 * kLd * 4 >= 16384, "T's M = 128 operand reads 8 KiB past T inside the fp32 block");
@@ -413,7 +413,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
     constexpr int kThreads = kStateThreads;
     uint64_t *mbP = reinterpret_cast<uint64_t *>(sm + kBar), *mbX = mbP + 1, *mbS = mbP + 2, *mbO = mbP + 3;
     uint64_t *drain = mbP + 4, *full = mbP + 5;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kBar + 56);
+    uint64_t *ofree = mbP + 7;  // the low warps have read the previous chunk's out rows (128 arrivals)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kBar + 64);
     const uint8_t *wu = img + (size_t)bh * nch * kImg;
     const uint32_t sm0 = smem_u32(sm);
     // lane quarter of the warp (TMEM lanes 32 qw .. 32 qw + 31) and its column half
@@ -445,6 +446,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
     }
     if (issuer) {
         for (int b = 0; b < 7; ++b) mbar_init(mbP + b, 1);
+        mbar_init(ofree, 128);
         fence_mbar_init();
     }
     // S0 = 0: the bf16 copy starts at zero
@@ -463,6 +465,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
     auto read_out = [&](int m) -> bool {
         const bool ok = mbar_wait(mbO, (uint32_t)m & 1u, kWaitNs);
         tc_fence_after();
+        __syncwarp();  // tcgen05.ld is warp-collective; the waits may leave the lanes apart
         uint32_t r[2][32];
         tmem_ld32(tmem + lane_base + cO + 64 * hf, r[0]);
         tmem_ld32(tmem + lane_base + cO + 64 * hf + 32, r[1]);
@@ -506,22 +509,30 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
                 umma_bf16(tmem + cP, kmaj2(set + sQo, ks), kmaj2(set + sKo, ks), id64, ks > 0);
             umma_commit(mbP);
         }
-        if (low && n > 0 && !read_out(n - 1)) fail = 1;
-        if (low || warp == kIssuer / 32) {
+        // O is free once every low thread has read chunk n - 1's out rows and
+        // staged them (an mbarrier, not a named barrier: the issuer's warp is
+        // diverged while its lane 0 issues)
+        if (low) {
+            if (n > 0 && !read_out(n - 1)) fail = 1;
             tc_fence_before();
-            named_sync<1, 160>();  // the low warps have read chunk n - 1's out rows
-            if (tid == 0 && n > 0) store_out(n - 1);
+            mbar_arrive(ofree);
+        }
+        if (issuer || (tid == 0 && n > 0)) {
+            if (!mbar_wait(ofree, ph, kWaitNs)) fail = 1;
+            tc_fence_after();
             if (issuer) {
-                tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     umma_bf16(tmem + cO, kmaj2(set + sQo, ks), mnmaj(sm0 + kS, 16384, ks), idKM, ks > 0);
+            } else {
+                store_out(n - 1);
             }
         }
         if (low) {
             // Ut row t, value channels 64 hf .. 64 hf + 63: U - X, bf16 MN-major
             if (!mbar_wait(mbX, ph, kWaitNs)) fail = 1;
             tc_fence_after();
+            __syncwarp();
             uint32_t r[2][32];
             tmem_ld32(tmem + lane_base + cX + 64 * hf, r[0]);
             tmem_ld32(tmem + lane_base + cX + 64 * hf + 32, r[1]);
@@ -550,6 +561,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
             // P row t, columns 32 hf .. 32 hf + 31: q_t . k_s (s <= t), bf16 K-major
             if (!mbar_wait(mbP, ph, kWaitNs)) fail = 1;
             tc_fence_after();
+            __syncwarp();
             tmem_ld32(tmem + lane_base + cP + 32 * hf, r[0]);
             tmem_ld_wait();
 #pragma unroll
@@ -568,6 +580,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
         }
         fence_proxy_async_smem();
         tc_fence_before();
+        __syncwarp();
         if (__syncthreads_or(fail)) {
             bad = 1;
             break;
@@ -592,6 +605,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) delta_state_kernel(const __g
             // every reader of this chunk's set is done (its products came before
             // mbS, the U rows were read before round 4): refill it with chunk n + 2
             if (producer && !fail && issued < nchunks) load(issued++);
+            __syncwarp();  // the issuer's and the producer's warps come out of single-lane work
             uint32_t r[2][32];
             tmem_ld32(tmem + lane_base + cS + 64 * hf, r[0]);
             tmem_ld32(tmem + lane_base + cS + 64 * hf + 32, r[1]);
