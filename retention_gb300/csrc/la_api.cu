@@ -282,7 +282,7 @@ int scratch_alloc(void **p, size_t bytes, cudaStream_t s) {
 // stays allocated until the process exits.
 namespace {
 
-__device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;

@@ -174,6 +174,11 @@ constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 __device__ __forceinline__ float log2_alpha(float g) {
     return fmaf(fminf(g, 0.f), kLog2e * 0.0625f, lg2f(1.f + ex2f(fabsf(g) * -kLog2e)) * -0.0625f);
 }
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
 // elu(x) + 1 on two packed bf16 values in bf16 arithmetic:
 // max(x, 0) + 2^(min(x, 0) * log2 e). The exponent argument is rounded to bf16,
 // so for x < 0 the result carries a relative error below 2^-8 |x| on top of the
@@ -509,7 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     b1 += tt.y;
                 }
                 // pass 2 in two groups of eight rows; the second group's words are
-                // loaded before the first group's results are stored. With the
+                // loaded before the first group's results are stored. The group
+                // loop is kept rolled (the prologue's code is the largest of the
+                // roles and instruction fetch stalled it when unrolled), so each
+                // group reads its gate logs from la[0..7] and shifts la[8..15]
+                // down for the next. With the
                 // gate on the value side (GATE 3) the tile scaled by 2^-b is v's,
                 // and q stays as it is.
                 if constexpr (GATE == 3) sK = sm + tile_half(2, s, ch);
@@ -519,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     kw[u] = *reinterpret_cast<const uint32_t *>(sK + offw(u));
                     if (!SO && GATE == 2) qw[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(u));
                 }
-#pragma unroll
+#pragma unroll 1
                 for (int g8 = 0; g8 < 2; ++g8) {
                     if (g8 == 0) {
 #pragma unroll
@@ -532,15 +541,20 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int uu = 8 * g8 + u;
-                        b0 += la0[uu];
-                        b1 += la1[uu];
+                        b0 += la0[u];
+                        b1 += la1[u];
+                        // factors in fp32, rounded to bf16 once and applied
+                        // to both channels in one packed multiply
                         uint32_t kx = kw[u];
                         if (ELU1) kx = phi_elu1_bf16x2(kx);
-                        ko[u] = 16 * qr + uu < c ? pack_bf16(bf16lo(kx) * ex2f(-b0), bf16hi(kx) * ex2f(-b1)) : 0u;
+                        ko[u] = mul_bf16x2(kx, pack_bf16(ex2f(-b0), ex2f(-b1)));
+                        // rows past the end: their v rows are zero, which cancels
+                        // them everywhere but in the ones column of the normaliser
+                        if (NORM && 16 * qr + uu >= c) ko[u] = 0u;
                         if (!SO && GATE == 2) {
                             uint32_t qx = qw[u];
                             if (ELU1) qx = phi_elu1_bf16x2(qx);
-                            qo[u] = pack_bf16(bf16lo(qx) * ex2f(b0), bf16hi(qx) * ex2f(b1));
+                            qo[u] = mul_bf16x2(qx, pack_bf16(ex2f(b0), ex2f(b1)));
                         }
                     }
 #pragma unroll
@@ -549,6 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         if (!SO && GATE == 2) *reinterpret_cast<uint32_t *>(sQ + offw(8 * g8 + u)) = qo[u];
                         kw[u] = kn[u];
                         if (!SO && GATE == 2) qw[u] = qn[u];
+                        la0[u] = la0[u + 8];
+                        la1[u] = la1[u + 8];
                     }
                 }
                 if (qr == 3) {
