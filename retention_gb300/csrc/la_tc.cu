@@ -503,6 +503,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 *reinterpret_cast<float2 *>(tot + qr * 128 + cw) = make_float2(s0, s1);
                 // then the q, k (, v) stage; the barrier also publishes the quarter sums
                 ok = LY::GR ? mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs) : true;
+                if constexpr (GATE == 3) sK = sm + tile_half(2, s, ch);
+                uint32_t kw[8], qw[8], kn[8], qn[8];
+                if (ok) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        kw[u] = *reinterpret_cast<const uint32_t *>(sK + offw(u));
+                        if (!SO && GATE == 2) qw[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(u));
+                    }
+                }
                 if (named_sync_or<kBarPro, 256>(!ok)) {
                     bad = 1;
                     break;
@@ -521,14 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 // down for the next. With the
                 // gate on the value side (GATE 3) the tile scaled by 2^-b is v's,
                 // and q stays as it is.
-                if constexpr (GATE == 3) sK = sm + tile_half(2, s, ch);
-                uint32_t kw[8], qw[8], kn[8], qn[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    kw[u] = *reinterpret_cast<const uint32_t *>(sK + offw(u));
-                    if (!SO && GATE == 2) qw[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(u));
-                }
-#pragma unroll 1
+#pragma unroll(SO ? 2 : 1)
                 for (int g8 = 0; g8 < 2; ++g8) {
                     if (g8 == 0) {
 #pragma unroll
@@ -805,24 +807,46 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             tc_fence_after();
             {
                 // P row t: causal mask (key <= t), bf16, K-major A operand of intra
-                uint32_t r0[32], r1[32];
-                tmem_ld32(tmem + lane_base + LY::colP, r0);
-                tmem_ld32(tmem + lane_base + LY::colP + 32, r1);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(pempty);
                 uint8_t *prow = sP + t * 128;
+                if constexpr (GATE >= 2) {
+                    // the channel-gated kernels carry the largest prologue; here the
+                    // row goes in eight rolled steps of eight columns, which keeps
+                    // this role's code small (instruction fetch stalled them otherwise)
+#pragma unroll 1
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        uint32_t a[8];
+                        tmem_ld8(tmem + lane_base + LY::colP + 8 * q8, a);
+                        tmem_ld_wait();
+                        uint32_t u[4];
 #pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) {
-                    uint32_t u[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int jj = q8 * 8 + 2 * e;
-                        const uint32_t a0 = q8 < 4 ? r0[jj] : r1[jj - 32];
-                        const uint32_t a1 = q8 < 4 ? r0[jj + 1] : r1[jj - 31];
-                        u[e] = pack_bf16(jj <= t ? __uint_as_float(a0) : 0.f, jj + 1 <= t ? __uint_as_float(a1) : 0.f);
+                        for (int e = 0; e < 4; ++e) {
+                            const int jj = q8 * 8 + 2 * e;
+                            u[e] = pack_bf16(jj <= t ? __uint_as_float(a[2 * e]) : 0.f,
+                                             jj + 1 <= t ? __uint_as_float(a[2 * e + 1]) : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
                     }
-                    *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+                    tc_fence_before();
+                    mbar_arrive(pempty);
+                } else {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tmem + lane_base + LY::colP, r0);
+                    tmem_ld32(tmem + lane_base + LY::colP + 32, r1);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(pempty);
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        uint32_t u[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int jj = q8 * 8 + 2 * e;
+                            const uint32_t a0 = q8 < 4 ? r0[jj] : r1[jj - 32];
+                            const uint32_t a1 = q8 < 4 ? r0[jj + 1] : r1[jj - 31];
+                            u[e] = pack_bf16(jj <= t ? __uint_as_float(a0) : 0.f, jj + 1 <= t ? __uint_as_float(a1) : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+                    }
                 }
             }
             fence_proxy_async_smem();
