@@ -692,7 +692,11 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
         };
         if (init) {
-            // the state carried into this segment: into TMEM and its bf16 copy
+            // the state carried into this segment: into TMEM and its bf16 copy.
+            // After a segment scan this launch may have started while the scan
+            // still ran (programmatic dependent launch): wait for it to finish
+            // before reading what it wrote (a no-op for an ordinary launch).
+            griddep_wait();
             const float *src = p.state_in + segblk + (size_t)i * kD;
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
@@ -914,6 +918,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     }
 
     // ============================================================ teardown
+    // a CTA that read no carried state still leaves only after the grid it was
+    // launched behind has finished (a no-op for an ordinary launch)
+    if (tid == 0) griddep_wait();
     const int aborted = __syncthreads_or(bad);
     if (aborted && tid == 0) atomicOr(&g_tc_error, 1u);
     tc_fence_before();
@@ -975,6 +982,10 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
                                                           const float *__restrict__ initial,
                                                           float *__restrict__ state_in, float *final_state,
                                                           int nseg, int blk, int value_side) {
+    // the full pass after this scan may start launching now: its CTAs set up
+    // and begin their first chunks, and wait for this grid before reading the
+    // carried states
+    griddep_launch_dependents();
     const int bh = blockIdx.x;
     const int e = blockIdx.y * blockDim.x + threadIdx.x;
     if (e >= blk) return;
@@ -990,43 +1001,56 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
     if (final_state) final_state[(size_t)bh * blk + e] = acc;
 }
 
+// after_scan: launched behind the segment scan as a programmatic dependent
+// launch, so that its CTAs set up and start on their first chunks while the
+// scan finishes (they wait for it before reading the carried states).
 template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false>
-int launch_t(const TcParams &prm, int grid, cudaStream_t s) {
+int launch_t(const TcParams &prm, int grid, cudaStream_t s, bool after_scan) {
     using LY = Layout<GATE, NORM, SO, OF32>;
     static_assert(LY::NS >= 2 && LY::bytes <= kSmemBudget, "shared memory budget");
     static_assert(LY::colP + 64 <= kTmemCols && LY::colO1 + LY::NW <= LY::colP, "TMEM budget");
     auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO, OF32>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes) != cudaSuccess)
         return LA_ERR_CUDA;
-    kern<<<grid, kThreads, LY::bytes, s>>>(prm);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = LY::bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_scan ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, prm) != cudaSuccess) return LA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
 template <int GATE, bool SO>
-int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm) {
+int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm, bool pdl) {
     if (elu1)
-        return norm ? launch_t<GATE, true, true, SO>(prm, grid, s) : launch_t<GATE, true, false, SO>(prm, grid, s);
-    return norm ? launch_t<GATE, false, true, SO>(prm, grid, s) : launch_t<GATE, false, false, SO>(prm, grid, s);
+        return norm ? launch_t<GATE, true, true, SO>(prm, grid, s, pdl) : launch_t<GATE, true, false, SO>(prm, grid, s, pdl);
+    return norm ? launch_t<GATE, false, true, SO>(prm, grid, s, pdl) : launch_t<GATE, false, false, SO>(prm, grid, s, pdl);
 }
 
 template <bool SO>
-int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false, bool value_gate = false) {
+int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false, bool value_gate = false, bool pdl = false) {
     const bool elu1 = mode & LA_PHI_ELU1, norm = mode & LA_NORMALIZE;
     if (value_gate) {
         // the per-channel gate on the value side: identity feature map, no
         // normaliser, bf16 output
         if (elu1 || norm || !(mode & LA_GATE_CHANNEL) || out_f32) return LA_ERR_INTERNAL;
-        return SO ? launch_t<3, false, false, true>(prm, grid, s) : launch_t<3, false, false, false>(prm, grid, s);
+        return SO ? launch_t<3, false, false, true>(prm, grid, s, pdl) : launch_t<3, false, false, false>(prm, grid, s, pdl);
     }
     if (out_f32 && !SO) {
         // fp32 output: identity feature map, no normaliser, no gate or the head gate
         if (elu1 || norm || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
-        return (mode & LA_GATE_HEAD) ? launch_t<1, false, false, false, true>(prm, grid, s)
-                                     : launch_t<0, false, false, false, true>(prm, grid, s);
+        return (mode & LA_GATE_HEAD) ? launch_t<1, false, false, false, true>(prm, grid, s, pdl)
+                                     : launch_t<0, false, false, false, true>(prm, grid, s, pdl);
     }
-    if (mode & LA_GATE_CHANNEL) return launch_g<2, SO>(prm, grid, s, elu1, norm);
-    if (mode & LA_GATE_HEAD) return launch_g<1, SO>(prm, grid, s, elu1, norm);
-    return launch_g<0, SO>(prm, grid, s, elu1, norm);
+    if (mode & LA_GATE_CHANNEL) return launch_g<2, SO>(prm, grid, s, elu1, norm, pdl);
+    if (mode & LA_GATE_HEAD) return launch_g<1, SO>(prm, grid, s, elu1, norm, pdl);
+    return launch_g<0, SO>(prm, grid, s, elu1, norm, pdl);
 }
 
 int sm_count() {
@@ -1128,7 +1152,7 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.state_in = state_in;
     prm.seg_state = nullptr;
     prm.seg_logdecay = nullptr;
-    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate);
+    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate, true);
     if (rc == LA_OK) *launches += 1;
     return rc;
 }
