@@ -168,11 +168,43 @@ __device__ __forceinline__ float lg2f(float x) {
     return y;
 }
 constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
-// log2 of the channel gate alpha = exp(logsigmoid(g) / 16):
-//   (min(g, 0) log2(e) - log2(1 + 2^(-|g| log2(e)))) / 16
+// two fp32 values in one 64-bit register pair, for the packed fp32x2 arithmetic
+typedef unsigned long long f32x2_t;
+__device__ __forceinline__ f32x2_t f2(float lo, float hi) {
+    f32x2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f32x2_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2_t f2_add(f32x2_t a, f32x2_t b) {
+    f32x2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2_t f2_mul(f32x2_t a, f32x2_t b) {
+    f32x2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2_t f2_fma(f32x2_t a, f32x2_t b, f32x2_t c) {
+    f32x2_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+// log2 of the channel gate alpha = exp(logsigmoid(g) / 16),
+//   (min(g, 0) log2(e) - log2(1 + 2^(-|g| log2(e)))) / 16,
+// for both channels of one packed bf16 word, the fp32 arithmetic around the
+// hardware exponential and logarithm done two channels at a time
 // (g = +huge gives 0: no decay)
-__device__ __forceinline__ float log2_alpha(float g) {
-    return fmaf(fminf(g, 0.f), kLog2e * 0.0625f, lg2f(1.f + ex2f(fabsf(g) * -kLog2e)) * -0.0625f);
+__device__ __forceinline__ f32x2_t log2_alpha2(uint32_t w) {
+    const f32x2_t a = f2(__uint_as_float((w << 16) & 0x7fffffffu), __uint_as_float(w & 0x7fff0000u));  // |g|
+    float t0, t1, u0, u1;
+    f2_split(f2_mul(a, f2(-kLog2e, -kLog2e)), t0, t1);
+    f2_split(f2_add(f2(ex2f(t0), ex2f(t1)), f2(1.f, 1.f)), u0, u1);
+    const f32x2_t m = f2(fminf(__uint_as_float(w << 16), 0.f), fminf(__uint_as_float(w & 0xffff0000u), 0.f));
+    return f2_fma(m, f2(kLog2e * 0.0625f, kLog2e * 0.0625f), f2_mul(f2(lg2f(u0), lg2f(u1)), f2(-0.0625f, -0.0625f)));
 }
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
     uint32_t r;
@@ -489,18 +521,17 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 // the blocks of this thread's channel half
                 uint8_t *sQ = sm + tile_half(0, s, ch), *sK = sm + tile_half(1, s, ch);
                 const uint8_t *sG = LY::GR ? sm + LY::Gring + (n % NG) * kTile + ch * kHalf : sm + tile_half(3, s, ch);
-                float la0[16], la1[16], s0 = 0.f, s1 = 0.f;
+                // gate logs of both channels in packed pairs; rows past the end
+                // read as g = +huge in both halves (no decay)
+                f32x2_t la[16], sq = f2(0.f, 0.f);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(sG + offw(u));
-                    const bool live = 16 * qr + u < c;
-                    la0[u] = log2_alpha(live ? bf16lo(w) : 3.0e38f);
-                    la1[u] = log2_alpha(live ? bf16hi(w) : 3.0e38f);
-                    s0 += la0[u];
-                    s1 += la1[u];
+                    const uint32_t w = 16 * qr + u < c ? *reinterpret_cast<const uint32_t *>(sG + offw(u)) : 0x7F7F7F7Fu;
+                    la[u] = log2_alpha2(w);
+                    sq = f2_add(sq, la[u]);
                 }
                 if (LY::GR) mbar_arrive(&gempty[n % NG]);  // g is in registers now
-                *reinterpret_cast<float2 *>(tot + qr * 128 + cw) = make_float2(s0, s1);
+                *reinterpret_cast<f32x2_t *>(tot + qr * 128 + cw) = sq;
                 // then the q, k (, v) stage; the barrier also publishes the quarter sums
                 ok = LY::GR ? mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs) : true;
                 if constexpr (GATE == 3) sK = sm + tile_half(2, s, ch);
@@ -516,12 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     bad = 1;
                     break;
                 }
-                float b0 = 0.f, b1 = 0.f;
-                for (int r = 0; r < qr; ++r) {
-                    const float2 tt = *reinterpret_cast<const float2 *>(tot + r * 128 + cw);
-                    b0 += tt.x;
-                    b1 += tt.y;
-                }
+                f32x2_t bb = f2(0.f, 0.f);
+                for (int r = 0; r < qr; ++r) bb = f2_add(bb, *reinterpret_cast<const f32x2_t *>(tot + r * 128 + cw));
+                float b0, b1;
                 // pass 2 in two groups of eight rows; the second group's words are
                 // loaded before the first group's results are stored. The group
                 // loop is kept rolled (the prologue's code is the largest of the
@@ -543,8 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const int uu = 8 * g8 + u;
-                        b0 += la0[u];
-                        b1 += la1[u];
+                        bb = f2_add(bb, la[u]);
+                        f2_split(bb, b0, b1);
                         // factors in fp32, rounded to bf16 once and applied
                         // to both channels in one packed multiply
                         uint32_t kx = kw[u];
@@ -565,8 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         if (!SO && GATE == 2) *reinterpret_cast<uint32_t *>(sQ + offw(8 * g8 + u)) = qo[u];
                         kw[u] = kn[u];
                         if (!SO && GATE == 2) qw[u] = qn[u];
-                        la0[u] = la0[u + 8];
-                        la1[u] = la1[u + 8];
+                        la[u] = la[u + 8];
                     }
                 }
                 if (qr == 3) {
