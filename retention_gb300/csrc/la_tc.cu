@@ -126,13 +126,15 @@ struct Layout {
     static constexpr uint32_t S = P + (SO ? 0 : 8192);                     // bf16 S_{n-1} (+ z atom), 32 / 48 KiB
     static constexpr uint32_t O = S + (SO ? 0 : (NORM ? 49152 : 32768));   // O staging: bf16 halves or fp32 quarters
     // floats: ffinal[128], then with a gate fbuf[NF][128], with the head gate
-    // fq[64] fk[64], with the channel gate tot[4][128]. fbuf is a ring of
+    // fq[64] fk[64], with the channel gate tot[4][128] (normalised) or
+    // tot[2][4][128] (two chunks' quarter sums). fbuf is a ring of
     // NF = NS + 1 slots: chunk n's decay factor goes to slot n % NF at the end of
     // its prologue, for the state chain to rescale T_n with.
     static constexpr int NF = NS + 1;
     static constexpr uint32_t F = O + (SO ? 0 : (OF32 ? 32768 : 16384));
     static constexpr uint32_t nfbuf = GATE != 0 ? NF * 128 : 0, nfq = GATE == 1 ? 128 : 0;
-    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + (GATE >= 2 ? 512 : 0)) * 4;
+    static constexpr uint32_t ntot = GATE >= 2 ? (NORM ? 512 : 1024) : 0;  // quarter sums (one or two chunks)
+    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + ntot) * 4;
     // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal,
     // drain; gfull, gempty [NG]; ffull [NF]
     static constexpr uint32_t nbar = 3 * NS + 12 + 2 * NG + NF;
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     float *fbuf = ffinal + 128;                             // [NF][128] chunk n's decay factor e^{b_last(n)}
     float *fq = fbuf + LY::nfbuf;                           // [64] retention: gamma^(t+1)
     float *fk = fq + 64;                                    // [64] retention: gamma^-(t+1)
-    float *tot = fq + LY::nfq;                              // [4][128] gated: per-quarter log2 decay sums
+    float *tot = fq + LY::nfq;                              // [1 or 2][4][128] gated: per-quarter log2 decay sums
     // Shared-memory offset of half h (columns 64h..64h+63) of tile tl of stage
     // s: tl = 0 q, 1 k, 2 v, 3 g (the g tile of a state-only stage)
     auto tile_half = [&](int tl, int s, int h) -> uint32_t {
@@ -495,13 +497,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // conflicts, and the swizzle slot of row 16 qr + u depends on u alone.
             // Per chunk:
             //   pass 1  log2 alpha of the thread's 32 gate values, kept in registers,
-            //           and their sums over the quarter -> tot[qr][channel]
+            //           and their sums over the quarter -> tot[(n % 2)][qr][channel]
             //   barrier; the quarter's starting decay = sum of tot over lower quarters
             //   pass 2  running log2 decay b_t down the quarter; phi(k_t) * 2^-b_t and
             //           phi(q_t) * 2^b_t in place, two channels per packed word.
-            // Rows past the end of the sequence (t >= c) get log2 alpha = 0, k = 0
-            // and keep their (zero-filled) q. Quarter 3 ends at the chunk's total
-            // decay and writes the state factors.
+            // Rows past the end of the sequence (t >= c) get log2 alpha = 0 and keep
+            // their (zero-filled) q; their k is zeroed only with the normaliser
+            // (elsewhere their zero v rows cancel them). Quarter 3 ends at the
+            // chunk's total decay and writes the state factors.
             const int ch = pw & 1, qr = pw >> 1;
             const int cw = 64 * ch + 2 * lane;  // first of the thread's two channels
             const uint32_t colw = (lane & 3) << 2, slot = lane >> 2;  // within the block of half ch
@@ -511,12 +514,19 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             float bl0 = 0.f, bl1 = 0.f, bt0 = 0.f, bt1 = 0.f;
             for (int n = 0; n < N; ++n) {
                 const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
-                // the gate tile first: from its own ring (full pass) or from the stage
+                // the gate tile first: from its own ring (full pass) or from the stage.
+                // Without the normaliser no barrier follows: the quarter sums are
+                // double-buffered, so a warp may start this chunk while others finish
+                // the last one, and a failed wait is made uniform at the barrier after
+                // pass 1 (what pass 1 read then is discarded). The normalised forms
+                // (two stages) measured faster with the barrier kept.
                 bool ok = LY::GR ? mbar_wait(&gfull[n % NG], (uint32_t)(n / NG) & 1u, kWaitNs)
                                  : mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
-                if (named_sync_or<kBarPro, 256>(!ok)) {
-                    bad = 1;
-                    break;
+                if constexpr (NORM) {
+                    if (named_sync_or<kBarPro, 256>(!ok)) {
+                        bad = 1;
+                        break;
+                    }
                 }
                 // the blocks of this thread's channel half
                 uint8_t *sQ = sm + tile_half(0, s, ch), *sK = sm + tile_half(1, s, ch);
@@ -531,9 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     sq = f2_add(sq, la[u]);
                 }
                 if (LY::GR) mbar_arrive(&gempty[n % NG]);  // g is in registers now
-                *reinterpret_cast<f32x2_t *>(tot + qr * 128 + cw) = sq;
+                float *totn = tot + (NORM ? 0 : (n & 1) * 512);
+                *reinterpret_cast<f32x2_t *>(totn + qr * 128 + cw) = sq;
                 // then the q, k (, v) stage; the barrier also publishes the quarter sums
-                ok = LY::GR ? mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs) : true;
+                if (LY::GR && ok) ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
                 if constexpr (GATE == 3) sK = sm + tile_half(2, s, ch);
                 uint32_t kw[8], qw[8], kn[8], qn[8];
                 if (ok) {
@@ -548,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     break;
                 }
                 f32x2_t bb = f2(0.f, 0.f);
-                for (int r = 0; r < qr; ++r) bb = f2_add(bb, *reinterpret_cast<const f32x2_t *>(tot + r * 128 + cw));
+                for (int r = 0; r < qr; ++r) bb = f2_add(bb, *reinterpret_cast<const f32x2_t *>(totn + r * 128 + cw));
                 float b0, b1;
                 // pass 2 in two groups of eight rows; the second group's words are
                 // loaded before the first group's results are stored. The group
