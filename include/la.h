@@ -98,6 +98,11 @@ typedef enum {
  * device's default memory pool, whose release threshold the library raises
  * the first time it allocates on a device: freed scratch stays mapped in the
  * pool for the next call instead of being unmapped at every synchronisation.
+ * A split call issues three kernels on `stream`: the segment end states, a
+ * scan over them, and the full pass. The full pass goes out as a programmatic
+ * dependent launch behind the scan. Its CTAs may start before the scan ends,
+ * but they wait for it before reading what it wrote, and the call's work is
+ * complete, for later work on `stream`, only when all three have finished.
  *
  * Range of the tensor-core kernel: it factors the decay inside a chunk as
  * exp(b_t) * exp(-b_s), b the log decay from the chunk start, which is exact
