@@ -632,8 +632,19 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // Threads pd < 128 also own key channel pd for the decay factors.
             const int pd = 32 * pw + lane;
             const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
+            // Retention applies the state's decay once per window of R chunks instead
+            // of every chunk: m chunks into a window the accumulator holds
+            // S / gamma^(64 m), so q rows take an extra gamma^(64 m) and k rows
+            // gamma^(-64 m), and the state chain rescales only at a window's last
+            // chunk. R keeps those extra factors within e^(+-40).
+            int R = 1;
+            if (GATE == 1) {
+                const float rl = -(float)kC * lg;
+                R = rl > 0.f ? max(1, (int)fminf(40.f / rl, 1048576.f)) : 1048576;
+            }
             // log decay of key channel pd over the previous chunk and over the segment so far
             float b_last = 0.f, b_total = 0.f;
+            int m = 0;  // chunks into the current window
             if (GATE == 1) {
                 // the row factors gamma^(t+1) and gamma^-(t+1) are the same in every chunk
                 if (pd < 64) {
@@ -644,6 +655,12 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             for (int n = 0; n < N; ++n) {
                 const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
+                m = n % R;
+                float gq = 1.f, gk = 1.f;
+                if (GATE == 1 && m > 0) {
+                    gq = __expf((float)(kC * m) * lg);
+                    gk = __expf(-(float)(kC * m) * lg);
+                }
                 const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
                 if (named_sync_or<kBarPro, 256>(!ok)) {
                     bad = 1;
@@ -672,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                                     for (int e = 0; e < 4; ++e) u[e] = phi_elu1_bf16x2(u[e]);
                                 }
                                 if (GATE == 1) {
-                                    const float fr = fr_arr[row];
+                                    const float fr = fr_arr[row] * (isk ? gk : gq);
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) u[e] = pack_bf16(bf16lo(u[e]) * fr, bf16hi(u[e]) * fr);
                                 }
@@ -685,14 +702,18 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 if (GATE == 1) b_last = (float)c * lg;
                 b_total += b_last;
                 if (GATE != 0 && pd < 128) {
-                    fbuf[(n % NF) * 128 + pd] = __expf(b_last);
+                    // retention: 1 inside a window (the state chain leaves the
+                    // accumulator alone), the decay since the window began at its end
+                    float fv = __expf(b_last);
+                    if (GATE == 1) fv = m == R - 1 ? __expf(b_last + (float)(kC * m) * lg) : 1.f;
+                    fbuf[(n % NF) * 128 + pd] = fv;
                     mbar_arrive(&ffull[n % NF]);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&pro[s]);
             }
             if (!bad && pd < 128) {
-                ffinal[pd] = GATE == 0 ? 1.f : __expf(b_last);
+                ffinal[pd] = GATE == 0 ? 1.f : __expf(b_last + (GATE == 1 ? (float)(kC * m) * lg : 0.f));
                 if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + pd] = b_total;
                 mbar_arrive(profinal);
             }
@@ -767,7 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             tc_fence_after();
             const float *fcol = fbuf + ((n - 1) % NF) * 128;
             const float f = GATE != 0 ? fcol[i] : 1.f;
-            if (GATE != 0) {
+            // (retention inside a window: factor 1, the accumulator stays as it is)
+            if (GATE != 0 && !(GATE == 1 && f == 1.f)) {
                 // S_{n-1} = diag(f) T_{n-1} (key-side gate) or T_{n-1} diag(f)
                 // (value-side gate), in place (z rides in column 128)
 #pragma unroll 1
