@@ -13,7 +13,10 @@
 //
 // which is the chunkwise form with the decay from the chunk start to t split
 // into a query factor and a key factor (exact in real arithmetic). For linear
-// attention b = 0 and every factor is 1; for retention b_t = (t+1) ln gamma.
+// attention b = 0 and every factor is 1; for retention b_t = (t+1) ln gamma,
+// and the rescale of the state is deferred to the end of a window of chunks
+// (the accumulator holds S / gamma^(64 m), m chunks into the window, and the q
+// and k rows carry the matching gamma^(+-64 m)).
 //
 // The normaliser z is the state's column for a value that is always 1
 // (z_t = A_t z_{t-1} + phi(k_t)). With LA_NORMALIZE, V is widened by a
@@ -35,8 +38,9 @@
 //   warp 3       MMA issuer (one thread) and TMEM owner
 //   warps 4-7, 0, 1, 14, 15  prologue (256 threads, two warps per SM
 //                sub-partition): phi and decay factors in place on the q and k tiles
-//   warps 8-11   state chain: S_{n-1} = diag(f) T_{n-1} (rescaled in TMEM) and
-//                its bf16 copy for the inter MMA of chunk n; the final state
+//   warps 8-11   state chain: S_{n-1} = diag(f) T_{n-1} (rescaled in TMEM;
+//                retention only at a window's end) and its bf16 copy for the
+//                inter MMA of chunk n; the final state
 //   warps 12-13  outputs: P mask -> bf16; O -> 1/den -> bf16 -> TMA store
 // O lives in two TMEM buffers (one with the normaliser, whose 144-column
 // accumulators leave no room for a second), so chunk n+1's MMAs overlap chunk
