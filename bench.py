@@ -162,7 +162,8 @@ def dist_init():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        # LA_DIST_BACKEND=gloo keeps the ranks on the CPU even where a GPU is visible
+        backend = os.environ.get("LA_DIST_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
         if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend)
@@ -189,20 +190,109 @@ def max_over_ranks(x, world):
 
 # ----------------------------------------------------------------- CPU leg
 
+def _host(t):
+    return None if t is None else t.float().numpy()
+
+
+def _oracle_mode(oracle, cfg):
+    m = oracle.PHI_ELU1 if cfg["phi"] == "elu1" else 0
+    if cfg["normalize"]:
+        m |= oracle.NORMALIZE
+    if cfg["gate"] == "head":
+        m |= oracle.GATE_HEAD
+    elif cfg["gate"] == "channel":
+        m |= oracle.GATE_CHANNEL
+    return m
+
+
+def _cpu_line(value, unit, threads, seqs, desc):
+    """A cpu_baseline object: the oracle's threads work on one (b, h) sequence
+    each, so the cores it used are at most the sample's sequences."""
+    return {"value": value, "unit": unit, "cores": min(threads, seqs), "kind": "oracle", "sample": desc}
+
+
 def oracle_sample(sample_B=2):
-    """The oracle, as it stands, on a bounded sample of the workload:
-    sample_B batch rows x all 16 heads x L = 4096. Returns (tokens/s, threads, desc)."""
-    sys.path.insert(0, ROOT)
+    """The oracle, as it stands, on a bounded sample of the linear-attention
+    workload: sample_B batch rows x all 16 heads x L = 4096. Returns
+    (tokens/s, threads used, description)."""
     import oracle
     cfg = W.workload("la", B=sample_B)
     inp = W.chunk_inputs(cfg, 0)
-    f = lambda t: None if t is None else t.float().numpy()
-    mode = oracle.PHI_ELU1 | oracle.NORMALIZE
     t0 = time.perf_counter()
-    oracle.forward(f(inp["q"]), f(inp["k"]), f(inp["v"]), None, mode)
+    oracle.forward(_host(inp["q"]), _host(inp["k"]), _host(inp["v"]), None, _oracle_mode(oracle, cfg))
     dt = time.perf_counter() - t0
-    desc = "oracle (fp64 recurrent C, OpenMP) on B=%d of 8 batch rows, all 16 heads, L=4096" % sample_B
-    return sample_B * cfg["L"] / dt, oracle.max_threads(), desc
+    desc = "oracle (fp64 recurrent C, OpenMP over sequences) on B=%d of 8 batch rows, all 16 heads, L=4096" % sample_B
+    return sample_B * cfg["L"] / dt, min(oracle.max_threads(), sample_B * cfg["H"]), desc
+
+
+def oracle_baselines():
+    """The oracle, as it stands, timed on a bounded sample of each further
+    workload the benchmark reports, in that line's own unit (tokens/s: B * L
+    tokens per step, all heads; decode: the GPU line's algorithmic bytes per
+    step / time). Samples keep the workload's shapes and cut the batch, or
+    the sequence length of the single long-context batch row."""
+    import oracle
+    thr = oracle.max_threads()
+    res = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    # retention and RetNet (retention + GroupNorm/swish epilogue): B=2 of 8
+    for name in ("retention", "retnet"):
+        cfg = W.workload(name, B=2)
+        inp = W.chunk_inputs(cfg, 0)
+        mode = _oracle_mode(oracle, cfg)
+        args = (_host(inp["q"]), _host(inp["k"]), _host(inp["v"]), _host(inp["gate"]), mode)
+        if name == "retnet":
+            ep = W.epilogue_inputs(cfg, 0)
+
+            def run():
+                o, _ = oracle.forward(*args)
+                oracle.group_norm_swish(o, _host(ep["og"]), _host(ep["weight"]), _host(ep["bias"]), cfg["gn_eps"])
+        else:
+            def run():
+                oracle.forward(*args)
+        dt = timed(run)
+        res[name] = _cpu_line(cfg["B"] * cfg["L"] / dt, UNIT, thr, cfg["B"] * cfg["H"],
+                              "oracle (fp64 recurrent C%s) on B=2 of 8 batch rows, 16 heads, L=4096"
+                              % (" + fp64 GroupNorm/swish" if name == "retnet" else ""))
+    # gated long context: the first 32768 of 131072 tokens, all 8 heads
+    cfg = W.workload("gla", L=32768)
+    inp = W.chunk_inputs(cfg, 0)
+    dt = timed(lambda: oracle.forward(_host(inp["q"]), _host(inp["k"]), _host(inp["v"]), _host(inp["gate"]),
+                                      _oracle_mode(oracle, cfg)))
+    res["gla"] = _cpu_line(cfg["B"] * cfg["L"] / dt, UNIT, thr, cfg["H"],
+                           "oracle (fp64 recurrent C) on the first 32768 of 131072 tokens, 8 heads")
+    # delta rule: B=2 of 8
+    cfg = W.workload("delta", B=2)
+    d = W.delta_inputs(cfg, 0)
+    dt = timed(lambda: oracle.delta_forward(_host(d["q"]), _host(d["k"]), _host(d["v"]), _host(d["beta"])))
+    res["delta"] = _cpu_line(cfg["B"] * cfg["L"] / dt, UNIT, thr, cfg["B"] * cfg["H"],
+                             "oracle delta rule (fp64 recurrent C) on B=2 of 8 batch rows, 16 heads, L=4096")
+    # backward: B=1 of 8 (retention, linear attention); gated: first 8192 tokens
+    for name, over in (("retention", dict(B=1)), ("la", dict(B=1)), ("gla", dict(L=8192))):
+        cfg = W.workload(name, **over)
+        inp = W.chunk_inputs(cfg, 0)
+        dout = W.bwd_inputs(cfg, 0)
+        dt = timed(lambda: oracle.backward(_host(inp["q"]), _host(inp["k"]), _host(inp["v"]), _host(dout),
+                                           _host(inp["gate"]), _oracle_mode(oracle, cfg)))
+        what = "B=1 of 8 batch rows, 16 heads, L=4096" if name != "gla" else "the first 8192 of 131072 tokens, 8 heads"
+        res[name + "_bwd"] = _cpu_line(cfg["B"] * cfg["L"] / dt, UNIT, thr, cfg["B"] * cfg["H"],
+                                       "oracle backward (fp64 chain rule on the recurrence, C) on " + what)
+    # decode: one step of the full batch (256 sequences x 32 heads), fp64 state
+    cfg = W.workload("decode")
+    st = W.decode_state(cfg, 0).double().numpy()
+    tok = W.decode_tokens(cfg, 0, 0)
+    dt = timed(lambda: oracle.decode_step(_host(tok["q"]), _host(tok["k"]), _host(tok["v"]), st, None,
+                                          oracle.PHI_ELU1 | oracle.NORMALIZE))
+    del st
+    res["decode"] = _cpu_line(decode_work(cfg) / dt / 1e9, "GB/s", thr, cfg["B"] * cfg["H"],
+                              "oracle decode step (fp64 C) on the full batch, one step; GB/s of the GPU "
+                              "line's algorithmic bytes (fp32 state read and written, tokens) per step time")
+    return res
 
 
 # ----------------------------------------------------------------- GPU legs
@@ -565,6 +655,12 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu:
         v, cores, desc = oracle_sample(2)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        # the oracle beside every other line too
+        for name, base in oracle_baselines().items():
+            if name == "decode":
+                dec["cpu_baseline"] = base
+            elif name in extra:
+                extra[name]["cpu_baseline"] = base
 
     tc = la.chunk_fwd_path(cfg["B"], cfg["H"], cfg["L"], cfg["dk"], cfg["dv"],
                            la.mode_bits(cfg["phi"], cfg["normalize"], cfg["gate"]), cfg["chunk"]) == 1
@@ -597,7 +693,8 @@ def main():
                        "us_per_step": dec["us_per_step"], "steps": dec["steps"],
                        "frac": dec["frac_of_hbm"], "peak": pk["hbm_gbs"],
                        "bytes_per_step": dec["bytes_per_step"], "launches": dec["launches"],
-                       "workload": "256 seqs x 32 heads, d=128, fp32 state, elu+1, normalised"},
+                       "workload": "256 seqs x 32 heads, d=128, fp32 state, elu+1, normalised",
+                       "cpu_baseline": dec.get("cpu_baseline")},
             "workloads": extra,
         }
         print(json.dumps(line), flush=True)

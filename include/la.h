@@ -94,10 +94,13 @@ typedef enum {
  * at most the number of SMs), the tensor-core path splits each sequence into
  * segments and takes stream-ordered scratch (cudaMallocAsync / cudaFreeAsync
  * on `stream`) for the per-segment states; a failed allocation returns
- * LA_ERR_CUDA. All stream-ordered scratch of this library comes from the
- * device's default memory pool, whose release threshold the library raises
- * the first time it allocates on a device: freed scratch stays mapped in the
- * pool for the next call instead of being unmapped at every synchronisation.
+ * LA_ERR_CUDA. All stream-ordered scratch of this library comes from a memory
+ * pool of its own, created on a device the first time it allocates there
+ * (cudaMemPoolCreate), whose release threshold keeps freed scratch mapped for
+ * the next call instead of unmapping it at every synchronisation: that pool
+ * holds up to the largest scratch any call used until the process exits. The
+ * device's default memory pool is neither used nor changed.
+ * la_chunk_fwd_noalloc is the same call without any allocation.
  * A split call issues three kernels on `stream`: the segment end states, a
  * scan over them, and the full pass. The full pass goes out as a programmatic
  * dependent launch behind the scan. Its CTAs may start before the scan ends,
@@ -286,9 +289,14 @@ int la_decode_step(const void *q, const void *k, const void *v, const void *gate
  * would need more scratch returns LA_ERR_UNSUPPORTED. It never calls cudaMalloc,
  * cudaMallocAsync or cudaFree.
  *
- * - The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before starting
- *   any stream capture.
+ * - Each call that splits looks up the array's device address in the current
+ *   device's context (a lookup, not an allocation). The array lives in the
+ *   library's device code, which the CUDA driver loads lazily by default: the
+ *   first such call in a context is when the driver maps the array's
+ *   LA_NOALLOC_SCRATCH_BYTES on that device. A caller with a fixed memory plan
+ *   should therefore make one call that splits (few sequences, e.g. B = H = 1,
+ *   L = 64 * 152) on each device during set-up, and should make that first
+ *   call before starting any stream capture.
  * - Every call on a device shares the one array and leaves its contents behind.
  *   Nothing in it has to start at zero: each call writes every scratch value
  *   before reading it. Calls whose work overlaps on the GPU (other streams,

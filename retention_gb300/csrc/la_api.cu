@@ -1,6 +1,7 @@
 // la_api.cu -- the C ABI of include/la.h: argument validation, kernel choice,
-// status strings. Every check runs before any launch; nothing is allocated
-// here.
+// status strings, and the scratch memory of the multi-kernel paths (the
+// library's own stream-ordered pool, and the fixed array of
+// la_chunk_fwd_noalloc). Every check runs before any launch.
 #include <atomic>
 #include <cmath>
 #include <mutex>
@@ -244,33 +245,50 @@ int la_device_status(la_stream_t stream) {
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// Scratch of the multi-kernel paths: stream-ordered allocations from the
-// device's default memory pool. The pool's release threshold is raised once
-// per device, so that memory freed at the end of one call stays mapped for the
-// next instead of being returned at the next synchronisation and mapped
-// again (which costs a large fraction of a call's time at these sizes). The
-// pool then keeps up to the largest scratch any call used.
+// Scratch of the multi-kernel paths: stream-ordered allocations from a memory
+// pool of the library's own, one per device, created on first use. Its release
+// threshold is raised so that memory freed at the end of one call stays
+// mapped for the next instead of being returned at the next synchronisation
+// and mapped again (which costs a large fraction of a call's time at these
+// sizes); the pool therefore keeps up to the largest scratch any call used
+// until the process exits. The device's default pool, which belongs to the
+// whole process, is neither used nor changed.
 namespace la {
 namespace {
+constexpr int kMaxPoolDevices = 64;
 std::mutex g_pool_mu;
-unsigned long long g_pool_done = 0;  // bit d: device d's pool threshold raised
+cudaMemPool_t g_pool[kMaxPoolDevices] = {};
+
+int scratch_pool(cudaMemPool_t *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxPoolDevices) return LA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (g_pool[dev] == nullptr) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return LA_ERR_CUDA;
+        uint64_t keep = UINT64_MAX;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return LA_ERR_CUDA;
+        }
+        g_pool[dev] = pool;
+    }
+    *out = g_pool[dev];
+    return LA_OK;
+}
 }  // namespace
 
 int scratch_alloc(void **p, size_t bytes, cudaStream_t s) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
-    if (dev >= 0 && dev < 64) {
-        std::lock_guard<std::mutex> lock(g_pool_mu);
-        if (!(g_pool_done & (1ull << dev))) {
-            cudaMemPool_t pool;
-            uint64_t keep = UINT64_MAX;
-            if (cudaDeviceGetDefaultMemPool(&pool, dev) != cudaSuccess ||
-                cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess)
-                return LA_ERR_CUDA;
-            g_pool_done |= 1ull << dev;
-        }
-    }
-    return cudaMallocAsync(p, bytes, s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    cudaMemPool_t pool = nullptr;
+    const int rc = scratch_pool(&pool);
+    if (rc != LA_OK) return rc == LA_ERR_UNSUPPORTED ? LA_ERR_CUDA : rc;
+    return cudaMallocFromPoolAsync(p, bytes, pool, s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 }  // namespace la
 
@@ -284,25 +302,17 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device. The host-side
-// name of the array is only a stand-in, so the address is looked up once per
-// device (with that device current) and cached; the lookup itself allocates
-// nothing.
+// Device address of the scratch array in the current device's context. The
+// host-side name of the array is only a stand-in, so the address is looked up
+// with the device current. It is looked up on every call rather than cached:
+// a cache keyed by device would keep a dead address after the context is
+// destroyed and created again (cudaDeviceReset), and the lookup allocates
+// nothing. The first lookup in a context loads the module that holds the
+// array, which is when the driver maps it.
 int noalloc_scratch(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return LA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return LA_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return LA_ERR_CUDA;
+    *out = p;
     return LA_OK;
 }
 

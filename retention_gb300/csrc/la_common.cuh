@@ -83,7 +83,7 @@ int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches);
 int launch_delta(const DeltaArgs &a, cudaStream_t s, int *launches);
 // the delta rule in chunks on the tensor cores (bf16, d_k = d_v = 128)
 bool delta_tc_supports(const DeltaArgs &a);
-// stream-ordered scratch from the device's default pool (kept mapped between calls)
+// stream-ordered scratch from the library's own pool on the current device (kept mapped between calls)
 int scratch_alloc(void **p, size_t bytes, cudaStream_t s);
 // read and clear the device error words of the kernels with bounded waits
 int tc_error_take(unsigned int *value);

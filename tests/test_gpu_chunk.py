@@ -180,3 +180,33 @@ def test_device_status_is_clean_after_the_bounded_wait_kernels():
     assert la.device_status() == 0
     assert la.device_status() == 0
     assert la.load().la_status_string(-5).decode().startswith("LA_ERR_TIMEOUT")
+
+
+# ------------------------------------------------------------------ retention windows
+
+# Decays whose rescale windows of the tensor-core kernel (the accumulator holds
+# S / gamma^(64 m) for m chunks, rescaled once per window) close after 1, 2, 5,
+# 12, 20, 41, 62 and 625 chunks, so that short runs cross window ends.
+WINDOW_GAMMAS = [0.5, 0.8, 0.9, 0.95, 0.97, 0.985, 0.99, 0.999]
+
+
+def window_inputs(cfg, seed):
+    inp = W.chunk_inputs(cfg, seed)
+    inp["gate"] = torch.tensor([WINDOW_GAMMAS[h % len(WINDOW_GAMMAS)] for h in range(cfg["H"])],
+                               dtype=torch.float32)
+    return inp
+
+
+@pytest.mark.parametrize("B,H,L", [(1, 8, 6100), (2, 40, 1300)], ids=["split", "unsplit"])
+def test_retention_window_ends(B, H, L):
+    """Retention through the tensor-core kernel with windows that end inside
+    each CTA's run of chunks: split (8 sequences, segments of 6 chunks) and
+    unsplit (80 sequences of 21 chunks), ragged lengths."""
+    from retention_gb300 import la
+    cfg = W.workload("retention", B=B, H=H, L=L)
+    assert la.chunk_fwd_path(B, H, L, 128, 128, la.mode_bits("identity", False, "head"), 64) == 1
+    inp = window_inputs(cfg, seed=21)
+    out_ref, st_ref = run_oracle(inp, cfg)
+    out, st = run_gpu(inp, cfg)
+    e_out, e_st = rel_err(out, out_ref), rel_err(st, st_ref)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)

@@ -110,3 +110,18 @@ def test_misaligned_initial_state_is_rejected():
         la.chunk_fwd(x["q"], x["k"], x["v"], None, phi="elu1", normalize=True,
                      initial_state=s0[1:1 + 2 * (128 * 128 + 128)].view(1, 2, -1))
     assert e.value.status == -3  # LA_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("B,H,L", [(1, 8, 6100), (2, 40, 1300)], ids=["split", "unsplit"])
+def test_retention_window_ends_from_state(B, H, L):
+    """Retention from a given state with decays whose rescale windows close
+    after 1 to 625 chunks (see test_gpu_chunk.WINDOW_GAMMAS), split and
+    unsplit: the carried state enters each window's bookkeeping."""
+    from test_gpu_chunk import window_inputs
+    cfg = W.workload("retention", B=B, H=H, L=L)
+    inp = window_inputs(cfg, seed=22)
+    s0 = _state(cfg, 122)
+    out_ref, st_ref = run_oracle(inp, cfg, state_in=s0.numpy())
+    out, st = run_gpu(inp, cfg, initial_state=s0)
+    e_out, e_st = rel_err(out, out_ref), rel_err(st, st_ref)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)

@@ -21,8 +21,9 @@ def _free_port():
 
 
 def _rank_main(rank, world, port, times, out):
+    # gloo ranks on the CPU, whether or not this machine has GPUs
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), LA_DIST_BACKEND="gloo")
     import sys
     sys.path.insert(0, ROOT)
     import bench
