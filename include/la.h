@@ -65,6 +65,8 @@ typedef enum {
                                 same type as q; A_t = diag(exp(logsigmoid(g_t) / 16)) */
 #define LA_DTYPE_F32 0x10    /* q, k, v, g, out are fp32 instead of bf16 */
 #define LA_KERNEL_SIMT 0x20  /* la_chunk_fwd: force the general CUDA-core kernel */
+#define LA_REVERSE 0x40      /* la_chunk_fwd: the anti-causal form (each token reads itself
+                                and every later token; see la_chunk_fwd) */
 
 /*
  * la_chunk_fwd -- the chunkwise-parallel forward pass over whole sequences,
@@ -88,7 +90,17 @@ typedef enum {
  *   chunk  1..128. The tensor-core kernel (bf16, d_k = d_v = 128, chunk 64)
  *          is chosen automatically; other cases run the general kernel, which
  *          returns LA_ERR_UNSUPPORTED when its tiles do not fit on chip.
- *   mode   LA_PHI_* | LA_NORMALIZE | LA_GATE_* | LA_DTYPE_F32 | LA_KERNEL_SIMT
+ *   mode   LA_PHI_* | LA_NORMALIZE | LA_GATE_* | LA_DTYPE_F32 | LA_KERNEL_SIMT |
+ *          LA_REVERSE
+ *
+ * LA_REVERSE: the anti-causal form, the same sums taken over the token and every
+ * LATER one, out_s = sum_{t >= s} A^{t-s} (q_s . k_t) v_t, with the state carried
+ * from the end of the sequence towards its start (final_state is then the state
+ * before token 0; an initial state of la_chunk_fwd_from_state sits after the
+ * last token). It equals the causal forward of the token-reversed sequence. The
+ * backward pass is built from such sums. Tensor-core kernel only: bf16,
+ * d_k = d_v = 128, chunk 64, identity feature map, no normaliser, no gate or the
+ * head gate; anything else returns LA_ERR_UNSUPPORTED.
  *
  * Scratch: when the batch has too few (b, h) sequences to fill the GPU (2 B H
  * at most the number of SMs), the tensor-core path splits each sequence into
@@ -235,22 +247,25 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
  *
  * Two routes. bf16 with d_k = d_v = 128 runs on the tensor-core forward kernel
  * (except the per-channel gate together with the normaliser): each gradient
- * term is a causal linear-attention forward with its roles permuted, some in
- * reversed token order; with the normaliser also den_t, z_t e_t and
- * sum Q_t e_t (the cancelling terms in fp32); with the per-channel gate dv is a
- * reversed gated forward and dQ, dK are forwards whose decay falls on the value
- * channel, and dg comes from a segmented reverse scan. Every other case (and
- * LA_KERNEL_SIMT) runs three sweeps over the sequence on the CUDA cores.
+ * term is a linear-attention forward with its roles permuted, causal for dQ and
+ * anti-causal (the LA_REVERSE form, over later tokens) for dK and dv; with the
+ * normaliser also den_t, z_t e_t and sum Q_t e_t (the cancelling terms in
+ * fp32); with the per-channel gate dv is a gated forward of token-reversed
+ * copies and dQ, dK are forwards whose decay falls on the value channel, and dg
+ * comes from a segmented reverse scan. Every other case (and LA_KERNEL_SIMT)
+ * runs three sweeps over the sequence on the CUDA cores.
  *   dout   [B][H][L][d_v]; dq, dk [B][H][L][d_k] and dv [B][H][L][d_v] are
  *          written, in the type of q
  *   dgate  with LA_GATE_CHANNEL: NULL (not computed) or [B][H][L][d_k] in the
  *          type of q; ignored otherwise (no gradient is formed for gamma)
  * No gradient flows into a final state or out of an initial one. Scratch,
- * taken stream-ordered with cudaMallocAsync on `stream` (LA_ERR_CUDA if that
- * fails): on the tensor-core route six (eight with LA_PHI_ELU1) bf16
- * [B][H][L][128] arrays, with LA_NORMALIZE eleven bf16 and five fp32 ones, with
- * LA_GATE_CHANNEL nine bf16 and one fp32 one plus per-chunk sums; on the other
- * one fp32 [B][H][L][d_k] array (two, plus three [B][H][L], with LA_NORMALIZE).
+ * taken stream-ordered from the library's pool on `stream` (LA_ERR_CUDA if that
+ * fails): on the tensor-core route none with the identity feature map (beyond
+ * the per-segment states of batches too small to fill the GPU), four bf16
+ * [B][H][L][128] arrays with LA_PHI_ELU1, with LA_NORMALIZE five bf16 and five
+ * fp32 ones, with LA_GATE_CHANNEL nine bf16 and one fp32 one plus per-chunk
+ * sums; on the other one fp32 [B][H][L][d_k] array (two, plus three [B][H][L],
+ * with LA_NORMALIZE).
  * Errors as la_chunk_fwd; no output may overlap an input.
  */
 int la_chunk_bwd(const void *q, const void *k, const void *v, const void *gate,
@@ -332,6 +347,30 @@ unsigned long long la_kernel_launches(void);
  * 2 s of wall time, far beyond any legitimate one.
  */
 int la_device_status(la_stream_t stream);
+
+/*
+ * la_chunk_fwd_stall_test -- diagnostics: makes the bounded waits of the
+ * tensor-core chunk forward run out on purpose, so that a caller (and this
+ * library's tests) can check the time-out path on a GPU without faulting or
+ * hanging it. The forward of la_chunk_fwd (d_k = d_v = 128, chunk 64, bf16,
+ * no final state) is launched once, unsplit, with its TMA producer issuing no
+ * tiles from chunk `stall_chunk` of each sequence on and every wait giving up
+ * after `wait_ns` nanoseconds: the roles left waiting leave their loops, the
+ * kernel drains what it issued, frees its tensor memory, sets the error word
+ * that la_device_status reports as LA_ERR_TIMEOUT, and returns. The CUDA
+ * context stays usable; `out` is not valid afterwards (chunks before
+ * stall_chunk are written). No page of the method has a counterpart.
+ *
+ *   q, k, v, gate, out, B, H, L, mode   as la_chunk_fwd (d_k = d_v = 128)
+ *   stall_chunk   >= 0; at or past the last chunk nothing stalls
+ *   wait_ns       1e5 .. 2e9 (the ordinary calls use 2e9)
+ * Returns LA_ERR_UNSUPPORTED where la_chunk_fwd would not take the
+ * tensor-core kernel or would split the sequences (2 B H at most the number of
+ * SMs); otherwise errors as la_chunk_fwd.
+ */
+int la_chunk_fwd_stall_test(const void *q, const void *k, const void *v, const void *gate,
+                            void *out, int B, int H, int L, int mode, int stall_chunk,
+                            long long wait_ns, la_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -14,14 +14,21 @@ namespace {
 std::atomic<unsigned long long> g_launches{0};
 
 constexpr int kKnownModeBits = LA_PHI_ELU1 | LA_NORMALIZE | LA_GATE_HEAD | LA_GATE_CHANNEL |
-                               LA_DTYPE_F32 | LA_KERNEL_SIMT;
+                               LA_DTYPE_F32 | LA_KERNEL_SIMT | LA_REVERSE;
+// what the anti-causal form does not run with
+constexpr int kNotWithReverse = LA_PHI_ELU1 | LA_NORMALIZE | LA_GATE_CHANNEL | LA_DTYPE_F32 | LA_KERNEL_SIMT;
 
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-int check_mode(int mode, const void *gate, bool decode) {
+// `chunk`: a chunk-forward call (the only kind that takes LA_REVERSE)
+int check_mode(int mode, const void *gate, bool decode, bool chunk = false) {
     if (mode & ~kKnownModeBits) return LA_ERR_INVALID_ARG;
     if (decode && (mode & LA_KERNEL_SIMT)) return LA_ERR_INVALID_ARG;
+    if (mode & LA_REVERSE) {
+        if (!chunk) return LA_ERR_INVALID_ARG;
+        if (mode & kNotWithReverse) return LA_ERR_UNSUPPORTED;
+    }
     const bool gh = mode & LA_GATE_HEAD, gc = mode & LA_GATE_CHANNEL;
     if (gh && gc) return LA_ERR_INVALID_ARG;
     if ((gh || gc) && gate == nullptr) return LA_ERR_INVALID_ARG;
@@ -48,7 +55,7 @@ int chunk_fwd(const void *q, const void *k, const void *v, const void *gate, con
     if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
     if (chunk < 1 || chunk > 128) return LA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
-    int rc = check_mode(mode, gate, false);
+    int rc = check_mode(mode, gate, false, true);
     if (rc != LA_OK) return rc;
     const long nbh = (long)B * H;
     if (nbh > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
@@ -75,10 +82,14 @@ int chunk_fwd(const void *q, const void *k, const void *v, const void *gate, con
     if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
     if (ep.ogate && (rc = check_epilogue(ep)) != LA_OK) return rc;
 
-    la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode, chunk, initial_state};
+    const bool rev = mode & LA_REVERSE;
+    la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode & ~LA_REVERSE, chunk, initial_state,
+                    0, 0, rev ? 1 : 0};
     int launches = 0;
     if (!(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a))
         rc = la::launch_chunk_tc(a, s, &launches);
+    else if (rev)
+        return LA_ERR_UNSUPPORTED;  // the anti-causal form runs on the tensor-core kernel only
     else
         rc = la::launch_chunk_simt(a, s, &launches);
     if (rc == LA_OK && ep.ogate) {
@@ -213,8 +224,11 @@ int la_chunk_fwd_path(int B, int H, int L, int dk, int dv, int mode, int chunk) 
     if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
     if (mode & ~kKnownModeBits) return LA_ERR_INVALID_ARG;
     if ((mode & LA_GATE_HEAD) && (mode & LA_GATE_CHANNEL)) return LA_ERR_INVALID_ARG;
-    la::ChunkArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, L, dk, dv, mode, chunk};
-    return (!(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a)) ? 1 : 0;
+    if ((mode & LA_REVERSE) && (mode & kNotWithReverse)) return LA_ERR_UNSUPPORTED;
+    la::ChunkArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, L, dk, dv, mode & ~LA_REVERSE, chunk};
+    const bool tc = !(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a);
+    if ((mode & LA_REVERSE) && !tc) return LA_ERR_UNSUPPORTED;
+    return tc ? 1 : 0;
 }
 
 const char *la_status_string(int status) {
@@ -231,6 +245,26 @@ const char *la_status_string(int status) {
 }
 
 unsigned long long la_kernel_launches(void) { return g_launches.load(); }
+
+int la_chunk_fwd_stall_test(const void *q, const void *k, const void *v, const void *gate, void *out, int B,
+                            int H, int L, int mode, int stall_chunk, long long wait_ns, la_stream_t stream) {
+    if (B < 1 || H < 1 || L < 1 || stall_chunk < 0) return LA_ERR_INVALID_ARG;
+    if (wait_ns < 100000LL || wait_ns > 2000000000LL) return LA_ERR_INVALID_ARG;
+    int rc = check_mode(mode, gate, false);
+    if (rc != LA_OK) return rc;
+    if ((long)B * H > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !out) return LA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_CHANNEL) && !aligned16(gate)) return LA_ERR_MISALIGNED;
+    if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
+    la::ChunkArgs a{q, k, v, gate, out, nullptr, B, H, L, 128, 128, mode, 64, nullptr};
+    if ((mode & LA_KERNEL_SIMT) || !la::chunk_tc_supports(a)) return LA_ERR_UNSUPPORTED;
+    int launches = 0;
+    rc = la::launch_chunk_tc_stalled(a, reinterpret_cast<cudaStream_t>(stream), &launches, stall_chunk,
+                                     (unsigned long long)wait_ns);
+    g_launches += (unsigned long long)launches;
+    return rc;
+}
 
 int la_device_status(la_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
@@ -324,7 +358,7 @@ extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
     if (B < 0 || H < 0 || L < 0) return LA_ERR_INVALID_ARG;
     if (chunk < 1 || chunk > 128) return LA_ERR_INVALID_ARG;
     if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
-    int rc = check_mode(mode, gate, false);
+    int rc = check_mode(mode, gate, false, true);
     if (rc != LA_OK) return rc;
     const long nbh = (long)B * H;
     if (nbh > 0x7fffffffL) return LA_ERR_UNSUPPORTED;
@@ -345,8 +379,11 @@ extern "C" int la_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
     if ((mode & LA_GATE_CHANNEL) && !aligned16(gate)) return LA_ERR_MISALIGNED;
     if ((mode & LA_GATE_HEAD) && ((uintptr_t)gate & 3u)) return LA_ERR_MISALIGNED;
 
-    la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode, chunk};
+    const bool rev = mode & LA_REVERSE;
+    la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode & ~LA_REVERSE, chunk, nullptr, 0, 0,
+                    rev ? 1 : 0};
     int launches = 0;
+    if (rev && ((mode & LA_KERNEL_SIMT) || !la::chunk_tc_supports(a))) return LA_ERR_UNSUPPORTED;
     if (!(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a)) {
         void *scratch = nullptr;
         if (la::chunk_tc_scratch_bytes(a) > (size_t)LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_UNSUPPORTED;

@@ -7,10 +7,13 @@
 // the channel (A_t = 1 or gamma_h), (Q_t . K_s) gamma^{t-s} is symmetric in the
 // roles, so
 //   dQ_t = sum_{s<=t} gamma^{t-s} (dout_t . v_s) K_s        = fwd(dout, v, K)
-//   dK_s = sum_{t>=s} gamma^{t-s} (v_s . dout_t) Q_t        = rev fwd(rev v, rev dout, rev Q)
-//   dv_s = sum_{t>=s} gamma^{t-s} (K_s . Q_t) dout_t        = rev fwd(rev K, rev Q, rev dout)
-// (rev reverses the token order: t >= s becomes t' <= s'). The normaliser and
-// the per-channel gate add the terms described above their routes below.
+//   dK_s = sum_{t>=s} gamma^{t-s} (v_s . dout_t) Q_t        = afwd(v, dout, Q)
+//   dv_s = sum_{t>=s} gamma^{t-s} (K_s . Q_t) dout_t        = afwd(K, Q, dout)
+// where afwd is the anti-causal instance of the forward kernel (the sum over the
+// token and every later one, chunks taken from the end), run on the arrays in
+// their own order. The normaliser and the per-channel gate add the terms
+// described above their routes below; the per-channel gate still runs its
+// anti-causal sums as causal forwards of token-reversed copies.
 #include "la_common.cuh"
 
 namespace la {
@@ -19,8 +22,9 @@ namespace {
 __device__ __forceinline__ float dphi(float x, bool elu1) { return (elu1 && x <= 0.f) ? __expf(x) : 1.f; }
 
 // ---------------------------------------------------------------- scalar gate, no normaliser
-// A prep pass writes the reversed (and phi-applied) operands, three forwards,
-// a last pass un-reverses dK, dv and applies phi'.
+// With the identity feature map the three forwards read the caller's arrays and
+// write the gradients directly. With phi = elu + 1 a first pass writes phi(q)
+// and phi(k) in order, and a last pass applies phi' to dQ and dK.
 constexpr int kEw = 256;  // threads of the elementwise passes
 constexpr int kD = 128;   // the tensor-core kernel's head dim
 
@@ -36,55 +40,33 @@ __device__ __forceinline__ uint4 phi8(uint4 x, bool elu1) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// reversed copies of v, dout, phi(q), phi(k), and phi(k) in order (elu1 only).
-// One uint4 (8 bf16) per step; rows of 128 stay contiguous.
-__global__ void __launch_bounds__(kEw) bwd_prep_kernel(const uint4 *q, const uint4 *k, const uint4 *v, const uint4 *d,
-                                                       uint4 *rv, uint4 *rd, uint4 *rq, uint4 *rk, uint4 *kf,
-                                                       long rows, int L, bool elu1) {
-    constexpr int CPR = kD / 8;  // chunks per row
-    const long n = rows * CPR;
+// g * phi'(x) on eight bf16 values (elu + 1: 1 for x > 0, e^x otherwise)
+__device__ __forceinline__ uint4 dphi8(uint4 g, uint4 x) {
+    uint32_t gw[4] = {g.x, g.y, g.z, g.w}, xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xffff0000u);
+        const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xffff0000u);
+        __nv_bfloat162 h = __floats2bfloat162_rn(x0 > 0.f ? g0 : g0 * __expf(x0), x1 > 0.f ? g1 : g1 * __expf(x1));
+        gw[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(gw[0], gw[1], gw[2], gw[3]);
+}
+
+// Qf = phi(q), Kf = phi(k), in order; one uint4 (8 bf16) per step
+__global__ void __launch_bounds__(kEw) bwd_phi_kernel(const uint4 *q, const uint4 *k, uint4 *Qf, uint4 *Kf, long n) {
     for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
-        const long row = x / CPR;
-        const int c = (int)(x % CPR), t = (int)(row % L);
-        const long rr = (row - t + (L - 1 - t)) * CPR + c;  // same sequence, token L-1-t
-        const uint4 kk = phi8(__ldcs(k + x), elu1);
-        rv[rr] = __ldcs(v + x);
-        rd[rr] = __ldcs(d + x);
-        rq[rr] = phi8(__ldcs(q + x), elu1);
-        rk[rr] = kk;
-        if (kf) kf[x] = kk;
+        Qf[x] = phi8(__ldcs(q + x), true);
+        Kf[x] = phi8(__ldcs(k + x), true);
     }
 }
 
-// dq = dQ phi'(q) (in place when dq holds dQ), dk = rev(rdK) phi'(k), dv = rev(rdv)
-__global__ void __launch_bounds__(kEw) bwd_post_kernel(const uint4 *q, const uint4 *k, const uint4 *dQ, const uint4 *rdk,
-                                                       const uint4 *rdv, uint4 *dq, uint4 *dk, uint4 *dv, long rows,
-                                                       int L, bool elu1) {
-    constexpr int CPR = kD / 8;
-    const long n = rows * CPR;
-    auto scale = [](uint4 g, uint4 x) {  // g * phi'(x), elu1: 1 for x > 0, e^x otherwise
-        uint32_t gw[4] = {g.x, g.y, g.z, g.w}, xw[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float x0 = __uint_as_float(xw[i] << 16), x1 = __uint_as_float(xw[i] & 0xffff0000u);
-            const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xffff0000u);
-            __nv_bfloat162 h = __floats2bfloat162_rn(x0 > 0.f ? g0 : g0 * __expf(x0), x1 > 0.f ? g1 : g1 * __expf(x1));
-            gw[i] = *reinterpret_cast<uint32_t *>(&h);
-        }
-        return make_uint4(gw[0], gw[1], gw[2], gw[3]);
-    };
+// dq = dQ phi'(q), dk = dK phi'(k), in order
+__global__ void __launch_bounds__(kEw) bwd_dphi_kernel(const uint4 *q, const uint4 *k, const uint4 *dQ, const uint4 *dK,
+                                                       uint4 *dq, uint4 *dk, long n) {
     for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
-        const long row = x / CPR;
-        const int c = (int)(x % CPR), t = (int)(row % L);
-        const long rr = (row - t + (L - 1 - t)) * CPR + c;
-        const uint4 gk = __ldcs(rdk + rr), gv = __ldcs(rdv + rr);
-        if (elu1) {
-            dq[x] = scale(__ldcs(dQ + x), __ldg(q + x));
-            dk[x] = scale(gk, __ldg(k + x));
-        } else {
-            dk[x] = gk;
-        }
-        dv[x] = gv;
+        dq[x] = dphi8(__ldcs(dQ + x), __ldg(q + x));
+        dk[x] = dphi8(__ldcs(dK + x), __ldg(k + x));
     }
 }
 
@@ -94,8 +76,8 @@ __global__ void __launch_bounds__(kEw) bwd_post_kernel(const uint4 *q, const uin
 //   U_t   = S_t w_t                     = fwd(w, v, K)
 //   z_t e_t                             = fwd(E, J, K)            E_t = (e_t hi, e_t lo, 0 ..), J_s = (1, 1, 0 ..)
 //   dK_s  = sum_{t>=s} Q_t (v_s . w_t) + sum_{t>=s} Q_t e_t
-//         = rev fwd(rev v, rev w, rev Q) + rev fwd(J, rev E, rev Q)
-//   dv_s  = rev fwd(rev K, rev Q, rev w)
+//         = afwd(v, w, Q) + afwd(J, E, Q)
+//   dv_s  = afwd(K, Q, w)
 //   dQ_t  = U_t + z_t e_t
 // dQ and dK are differences of nearly equal terms, so those forwards write
 // fp32 and e_t travels as two bf16 parts (hi + lo).
@@ -107,27 +89,21 @@ __device__ __forceinline__ long rev_chunk(long x, int L) {
     return (row - t + (L - 1 - t)) * CPR + c;
 }
 
-// Q = phi(q), K = phi(k) in order; rev v, rev Q, rev K; the constant J
-__global__ void __launch_bounds__(kEw) bwdn_prep1_kernel(const uint4 *q, const uint4 *k, const uint4 *v, uint4 *Qf,
-                                                         uint4 *Kf, uint4 *rv, uint4 *rq, uint4 *rk, uint4 *J,
-                                                         long rows, int L, bool elu1) {
+// Q = phi(q), K = phi(k) in order; the constant J
+__global__ void __launch_bounds__(kEw) bwdn_prep1_kernel(const uint4 *q, const uint4 *k, uint4 *Qf, uint4 *Kf,
+                                                         uint4 *J, long rows, bool elu1) {
     const long n = rows * CPR;
     const uint32_t one2 = 0x3F803F80u;  // bf16 1.0 twice
     for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
-        const long rr = rev_chunk(x, L);
-        const uint4 qq = phi8(__ldcs(q + x), elu1), kk = phi8(__ldcs(k + x), elu1);
-        Qf[x] = qq;
-        Kf[x] = kk;
-        rq[rr] = qq;
-        rk[rr] = kk;
-        rv[rr] = __ldcs(v + x);
+        Qf[x] = phi8(__ldcs(q + x), elu1);
+        Kf[x] = phi8(__ldcs(k + x), elu1);
         J[x] = (x % CPR) == 0 ? make_uint4(one2, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-// w = dout / den (den from column 0 of the fp32 forward with values J), in order and reversed
-__global__ void __launch_bounds__(kEw) bwdn_prep2_kernel(const uint4 *d, const float *den_full, uint4 *w, uint4 *rw,
-                                                         float *den, long rows, int L) {
+// w = dout / den (den from column 0 of the fp32 forward with values J)
+__global__ void __launch_bounds__(kEw) bwdn_prep2_kernel(const uint4 *d, const float *den_full, uint4 *w, float *den,
+                                                         long rows) {
     const long n = rows * CPR;
     for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
         const long row = x / CPR;
@@ -141,15 +117,13 @@ __global__ void __launch_bounds__(kEw) bwdn_prep2_kernel(const uint4 *d, const f
             __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(gw[i] << 16) * r, __uint_as_float(gw[i] & 0xffff0000u) * r);
             gw[i] = *reinterpret_cast<uint32_t *>(&h);
         }
-        const uint4 o = make_uint4(gw[0], gw[1], gw[2], gw[3]);
-        w[x] = o;
-        rw[rev_chunk(x, L)] = o;
+        w[x] = make_uint4(gw[0], gw[1], gw[2], gw[3]);
     }
 }
 
-// e_t = -(Q_t . U_t) / den_t, one warp per token; E_t = (hi, lo, 0 ..) in order and reversed
+// e_t = -(Q_t . U_t) / den_t, one warp per token; E_t = (hi, lo, 0 ..)
 __global__ void __launch_bounds__(kEw) bwdn_prep3_kernel(const uint4 *Qf, const float *U, const float *den, uint4 *E,
-                                                         uint4 *rE, long rows, int L) {
+                                                         long rows) {
     const long row = ((long)blockIdx.x * kEw + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -171,17 +145,14 @@ __global__ void __launch_bounds__(kEw) bwdn_prep3_kernel(const uint4 *Qf, const 
             h2.y = lo;
             o.x = *reinterpret_cast<uint32_t *>(&h2);
         }
-        const long x = row * CPR + lane;
-        E[x] = o;
-        rE[rev_chunk(x, L)] = o;
+        E[row * CPR + lane] = o;
     }
 }
 
-// dq = (U + ZE) phi'(q), dk = rev(rdKm + rdz) phi'(k), dv = rev(rdv)
+// dq = (U + ZE) phi'(q), dk = (dKm + dz) phi'(k), in order
 __global__ void __launch_bounds__(kEw) bwdn_post_kernel(const uint4 *q, const uint4 *k, const float4 *U,
-                                                        const float4 *ZE, const float4 *rdkm, const float4 *rdz,
-                                                        const uint4 *rdv, uint4 *dq, uint4 *dk, uint4 *dv, long rows,
-                                                        int L, bool elu1) {
+                                                        const float4 *ZE, const float4 *dkm, const float4 *dz,
+                                                        uint4 *dq, uint4 *dk, long rows, bool elu1) {
     const long n = rows * CPR;
     auto combine = [elu1](float4 a0, float4 a1, float4 b0, float4 b1, uint4 x) {
         const float g[8] = {a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w,
@@ -199,11 +170,9 @@ __global__ void __launch_bounds__(kEw) bwdn_post_kernel(const uint4 *q, const ui
         return make_uint4(o[0], o[1], o[2], o[3]);
     };
     for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
-        const long rr = rev_chunk(x, L);
         dq[x] = combine(__ldcs(U + 2 * x), __ldcs(U + 2 * x + 1), __ldcs(ZE + 2 * x), __ldcs(ZE + 2 * x + 1), __ldg(q + x));
-        dk[x] = combine(__ldcs(rdkm + 2 * rr), __ldcs(rdkm + 2 * rr + 1), __ldcs(rdz + 2 * rr), __ldcs(rdz + 2 * rr + 1),
+        dk[x] = combine(__ldcs(dkm + 2 * x), __ldcs(dkm + 2 * x + 1), __ldcs(dz + 2 * x), __ldcs(dz + 2 * x + 1),
                         __ldg(k + x));
-        dv[x] = __ldcs(rdv + rr);
     }
 }
 
@@ -483,19 +452,18 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
 static int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
     const long rows = (long)a.B * a.H * a.L;
     const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16), fb = 2 * hb;
-    // bf16: Q K J w E rv rw rq rk rE rdv; fp32: den_full U ZE rdkm rdz; den [rows]
-    const size_t bytes = 11 * hb + 5 * fb + (size_t)rows * sizeof(float);
+    // bf16: Q K J w E; fp32: den_full U ZE dKm dz; den [rows]
+    const size_t bytes = 5 * hb + 5 * fb + (size_t)rows * sizeof(float);
     void *scratch = nullptr;
     if (scratch_alloc(&scratch, bytes, s) != LA_OK) return LA_ERR_CUDA;
     char *b = static_cast<char *>(scratch);
-    uint4 *h[11];
-    for (int i = 0; i < 11; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
-    uint4 *Qf = h[0], *Kf = h[1], *J = h[2], *w = h[3], *E = h[4], *rv = h[5], *rw = h[6], *rq = h[7], *rk = h[8],
-          *rE = h[9], *rdv = h[10];
+    uint4 *h[5];
+    for (int i = 0; i < 5; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
+    uint4 *Qf = h[0], *Kf = h[1], *J = h[2], *w = h[3], *E = h[4];
     float *f[5];
-    for (int i = 0; i < 5; ++i) f[i] = reinterpret_cast<float *>(b + 11 * hb + i * fb);
-    float *den_full = f[0], *U = f[1], *ZE = f[2], *rdkm = f[3], *rdz = f[4];
-    float *den = reinterpret_cast<float *>(b + 11 * hb + 5 * fb);
+    for (int i = 0; i < 5; ++i) f[i] = reinterpret_cast<float *>(b + 5 * hb + i * fb);
+    float *den_full = f[0], *U = f[1], *ZE = f[2], *dkm = f[3], *dz = f[4];
+    float *den = reinterpret_cast<float *>(b + 5 * hb + 5 * fb);
     const bool elu1 = a.mode & LA_PHI_ELU1;
     const int mode = a.mode & LA_GATE_HEAD;  // identity feature map, bf16, no normaliser
     const int nb = ew_blocks(rows * CPR);
@@ -504,34 +472,34 @@ static int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
         if (rc == LA_OK && cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
         if (rc == LA_OK) ++*launches;
     };
-    auto fwd = [&](const void *q, const void *k, const void *v, void *out, bool f32) {
+    auto fwd = [&](const void *q, const void *k, const void *v, void *out, bool f32, bool anti) {
         if (rc != LA_OK) return;
-        ChunkArgs c{q, k, v, a.gate, out, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr, f32 ? 1 : 0};
+        ChunkArgs c{q, k, v, a.gate, out, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr, f32 ? 1 : 0, 0,
+                    anti ? 1 : 0};
         rc = launch_chunk_tc(c, s, launches);
     };
-    bwdn_prep1_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
-                                         static_cast<const uint4 *>(a.v), Qf, Kf, rv, rq, rk, J, rows, a.L, elu1);
+    bwdn_prep1_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), Qf, Kf, J,
+                                         rows, elu1);
     ok();
-    fwd(Qf, Kf, J, den_full, true);  // den_t in columns 0 and 1
+    fwd(Qf, Kf, J, den_full, true, false);  // den_t in columns 0 and 1
     if (rc == LA_OK) {
-        bwdn_prep2_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.dout), den_full, w, rw, den, rows, a.L);
+        bwdn_prep2_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.dout), den_full, w, den, rows);
         ok();
     }
-    fwd(w, a.v, Kf, U, true);  // U_t = S_t w_t
+    fwd(w, a.v, Kf, U, true, false);  // U_t = S_t w_t
     if (rc == LA_OK) {
-        bwdn_prep3_kernel<<<(unsigned)((rows + kEw / 32 - 1) / (kEw / 32)), kEw, 0, s>>>(Qf, U, den, E, rE, rows, a.L);
+        bwdn_prep3_kernel<<<(unsigned)((rows + kEw / 32 - 1) / (kEw / 32)), kEw, 0, s>>>(Qf, U, den, E, rows);
         ok();
     }
-    fwd(E, J, Kf, ZE, true);    // z_t e_t
-    fwd(rv, rw, rq, rdkm, true);
-    fwd(J, rE, rq, rdz, true);
-    fwd(rk, rq, rw, rdv, false);
+    fwd(E, J, Kf, ZE, true, false);   // z_t e_t
+    fwd(a.v, w, Qf, dkm, true, true);  // sum_{t>=s} (v_s . w_t) Q_t
+    fwd(J, E, Qf, dz, true, true);     // sum_{t>=s} e_t Q_t
+    fwd(Kf, Qf, w, a.grad_v, false, true);
     if (rc == LA_OK) {
         bwdn_post_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
                                             reinterpret_cast<const float4 *>(U), reinterpret_cast<const float4 *>(ZE),
-                                            reinterpret_cast<const float4 *>(rdkm), reinterpret_cast<const float4 *>(rdz),
-                                            rdv, static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k),
-                                            static_cast<uint4 *>(a.grad_v), rows, a.L, elu1);
+                                            reinterpret_cast<const float4 *>(dkm), reinterpret_cast<const float4 *>(dz),
+                                            static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k), rows, elu1);
         ok();
     }
     if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
@@ -542,36 +510,39 @@ int launch_bwd_tc(const BwdArgs &a, cudaStream_t s, int *launches) {
     if (a.mode & LA_GATE_CHANNEL) return launch_bwd_tc_gated(a, s, launches);
     if (a.mode & LA_NORMALIZE) return launch_bwd_tc_norm(a, s, launches);
     const long rows = (long)a.B * a.H * a.L;
-    const size_t arr = (size_t)rows * kD * sizeof(__nv_bfloat16);
     const bool elu1 = a.mode & LA_PHI_ELU1;
-    // rv, rd, rq, rk, rdk, rdv; with elu1 also K = phi(k) and dQ
-    const int narr = elu1 ? 8 : 6;
-    void *scratch = nullptr;
-    if (scratch_alloc(&scratch, narr * arr, s) != LA_OK) return LA_ERR_CUDA;
-    char *b = static_cast<char *>(scratch);
-    uint4 *rv = reinterpret_cast<uint4 *>(b), *rd = reinterpret_cast<uint4 *>(b + arr);
-    uint4 *rq = reinterpret_cast<uint4 *>(b + 2 * arr), *rk = reinterpret_cast<uint4 *>(b + 3 * arr);
-    uint4 *rdk = reinterpret_cast<uint4 *>(b + 4 * arr), *rdv = reinterpret_cast<uint4 *>(b + 5 * arr);
-    uint4 *kf = elu1 ? reinterpret_cast<uint4 *>(b + 6 * arr) : nullptr;
-    uint4 *dQ = elu1 ? reinterpret_cast<uint4 *>(b + 7 * arr) : static_cast<uint4 *>(a.grad_q);
     const int mode = a.mode & LA_GATE_HEAD;  // identity feature map, bf16, no normaliser
-    const int nb = ew_blocks(rows * (kD / 8));
     int rc = LA_OK;
-    bwd_prep_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
-                                       static_cast<const uint4 *>(a.v), static_cast<const uint4 *>(a.dout), rv, rd, rq,
-                                       rk, kf, rows, a.L, elu1);
+    auto fwd = [&](const void *q, const void *k, const void *v, void *out, bool anti) {
+        if (rc != LA_OK) return;
+        ChunkArgs c{q, k, v, a.gate, out, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr, 0, 0, anti ? 1 : 0};
+        rc = launch_chunk_tc(c, s, launches);
+    };
+    if (!elu1) {
+        // three forwards on the caller's arrays, straight into the gradients
+        fwd(a.dout, a.v, a.k, a.grad_q, false);
+        fwd(a.v, a.dout, a.q, a.grad_k, true);
+        fwd(a.k, a.q, a.dout, a.grad_v, true);
+        return rc;
+    }
+    // phi(q), phi(k), dQ and dK (before phi') in scratch
+    const size_t arr = (size_t)rows * kD * sizeof(__nv_bfloat16);
+    void *scratch = nullptr;
+    if (scratch_alloc(&scratch, 4 * arr, s) != LA_OK) return LA_ERR_CUDA;
+    char *b = static_cast<char *>(scratch);
+    uint4 *Qf = reinterpret_cast<uint4 *>(b), *Kf = reinterpret_cast<uint4 *>(b + arr);
+    uint4 *dQ = reinterpret_cast<uint4 *>(b + 2 * arr), *dK = reinterpret_cast<uint4 *>(b + 3 * arr);
+    const long n = rows * CPR;
+    const int nb = ew_blocks(n);
+    bwd_phi_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), Qf, Kf, n);
     if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
     else ++*launches;
-    const ChunkArgs calls[3] = {
-        {a.dout, a.v, elu1 ? kf : a.k, a.gate, dQ, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
-        {rv, rd, rq, a.gate, rdk, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
-        {rk, rq, rd, a.gate, rdv, nullptr, a.B, a.H, a.L, kD, kD, mode, 64, nullptr},
-    };
-    for (int i = 0; i < 3 && rc == LA_OK; ++i) rc = launch_chunk_tc(calls[i], s, launches);
+    fwd(a.dout, a.v, Kf, dQ, false);
+    fwd(a.v, a.dout, Qf, dK, true);
+    fwd(Kf, Qf, a.dout, a.grad_v, true);
     if (rc == LA_OK) {
-        bwd_post_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), dQ, rdk,
-                                           rdv, static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k),
-                                           static_cast<uint4 *>(a.grad_v), rows, a.L, elu1);
+        bwd_dphi_kernel<<<nb, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), dQ, dK,
+                                           static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k), n);
         if (cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
         else ++*launches;
     }

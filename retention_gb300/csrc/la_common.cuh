@@ -47,6 +47,10 @@ struct ChunkArgs {
     // the value channels (out_t[j] = sum_s (q_t . k_s) v_s[j] prod alpha[j]);
     // the kernel writes out_t / e^{b_t}, b_t the log decay since the chunk start
     int value_gate;
+    // tensor-core path only, identity phi, no normaliser, no gate or the head gate:
+    // the anti-causal form out_s = sum_{t >= s} gamma^{t-s} (q_s . k_t) v_t, the
+    // chunks taken from the end; final_state is then the state before token 0
+    int reverse;
 };
 
 struct GnArgs {
@@ -98,5 +102,9 @@ int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a);
 int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch, size_t scratch_bytes);
+// diagnostics: the tensor-core forward (unsplit only) with its producer stopping
+// before chunk stall_chunk and every bounded wait limited to wait_ns
+int launch_chunk_tc_stalled(const ChunkArgs &a, cudaStream_t s, int *launches, int stall_chunk,
+                            unsigned long long wait_ns);
 
 }  // namespace la

@@ -66,7 +66,7 @@ constexpr int kThreads = 512;            // 16 warps
 constexpr uint32_t kTile = kC * kD * 2;  // bf16 [64 x 128] tile: 16 KiB = two 8 KiB swizzle blocks
 constexpr uint32_t kHalf = 8192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitNs = 2000000000ull;  // far beyond any legitimate wait
+constexpr uint64_t kWaitNs = 2000000000ull;  // default wait limit: far beyond any legitimate wait
 constexpr int kBarPro = 1, kBarState = 2, kBarOut = 3;  // named barrier ids
 // The producer and the MMA issuer sit on the SM sub-partitions (warp % 4) that
 // host the fewest busy warps, so their short instruction streams issue promptly.
@@ -83,6 +83,8 @@ struct TcParams {
     float *seg_logdecay;     // [BH][nseg][128]: log decay over each segment (state-only pass)
     int H, L, mode, nseg, seg_chunks;
     int init0;               // segment 0 starts from state_in too (a given initial state)
+    uint64_t wait_ns;        // limit of every bounded wait (kWaitNs)
+    int stall_chunk;         // diagnostics: the producer stops before this chunk (-1: never)
 };
 
 constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
@@ -235,10 +237,19 @@ __device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
 // SO (state only): the first pass over a split sequence. Each CTA runs one
 // segment from a zero state and keeps only the state update (no QK, no
 // outputs): it writes the segment's end state and its total log decay.
-template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false>
+//
+// REV (anti-causal): out_s = sum_{t >= s} A(s -> t) (q_s . k_t) v_t, the sum
+// over the token and every later one, with the scalar decay gamma^(t - s).
+// It is the causal form in mirrored coordinates: chunks are taken from the last
+// one (so the ragged chunk comes first), the local index of row r of a chunk of
+// c tokens is c - 1 - r, and the mask keeps key columns at or after the query
+// row. The state carried from chunk to chunk is then the sum over all later
+// tokens, decayed to the start of the chunk after the current one.
+template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     using LY = Layout<GATE, NORM, SO, OF32>;
     static_assert(GATE != 3 || (!ELU1 && !NORM), "the value-side gate takes features as given, no normaliser");
+    static_assert(!REV || (GATE <= 1 && !ELU1 && !NORM), "the anti-causal instance: scalar decay, features as given");
     constexpr int NS = LY::NS;
     constexpr int NG = LY::GR ? LY::NG : 1;  // gate ring slots (the ring exists only if GR)
     extern __shared__ uint8_t smem_raw[];
@@ -247,10 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     // trip would turn them into generic loads and stores)
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint64_t wait_ns = p.wait_ns;  // limit of every bounded wait
     // CTA = (b, h, segment); a segment is seg_chunks consecutive chunks
     const int bh = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg, h = bh % p.H, L = p.L;
     const int c0 = seg * p.seg_chunks;
-    const int N = max(0, min(p.seg_chunks, (L + kC - 1) / kC - c0));
+    const int nch = (L + kC - 1) / kC;
+    const int N = max(0, min(p.seg_chunks, nch - c0));
+    // first token of the n-th chunk this CTA takes (from the end with REV)
+    auto chunk_t0 = [&](int n) { return (REV ? nch - 1 - (c0 + n) : c0 + n) * kC; };
     const bool init = !SO && p.state_in != nullptr && (seg > 0 || p.init0);  // start from a carried state
     const size_t blk = (size_t)kD * kD + (NORM ? kD : 0);
     const size_t segblk = (size_t)blockIdx.x * blk;
@@ -344,12 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             int issued = 0, gissued = 0;
             constexpr int ntl = (GATE >= 2 && !LY::GR) ? 4 : 3;  // q, k, v (, g) tiles of a stage
             for (int n = 0; n < N; ++n) {
+                // diagnostics only: no tiles from chunk stall_chunk on, so that the
+                // other roles' bounded waits run out
+                if (p.stall_chunk >= 0 && n >= p.stall_chunk) break;
                 const int s = n % NS;
-                const int t0 = (c0 + n) * kC;
+                const int t0 = chunk_t0(n);
                 if constexpr (LY::GR) {
                     // g of chunk n goes out before chunk n's stage is waited for
                     const int sg = n % NG;
-                    if (n >= NG && !mbar_wait(&gempty[sg], (uint32_t)(n / NG - 1) & 1u, kWaitNs)) {
+                    if (n >= NG && !mbar_wait(&gempty[sg], (uint32_t)(n / NG - 1) & 1u, wait_ns)) {
                         bad = 1;
                         break;
                     }
@@ -359,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     tma_load_3d(dst + kHalf, &p.tg, &gfull[sg], 64, t0, bh);
                     gissued = n + 1;
                 }
-                if (n >= NS && !mbar_wait(&empty[s], (uint32_t)(n / NS - 1) & 1u, kWaitNs)) {
+                if (n >= NS && !mbar_wait(&empty[s], (uint32_t)(n / NS - 1) & 1u, wait_ns)) {
                     bad = 1;
                     break;
                 }
@@ -374,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             // nothing may still be landing in shared memory when the CTA leaves
             for (int m = issued > NS ? issued - NS : 0; m < issued; ++m)
-                if (!mbar_wait(&full[m % NS], (uint32_t)(m / NS) & 1u, kWaitNs)) bad = 1;
+                if (!mbar_wait(&full[m % NS], (uint32_t)(m / NS) & 1u, wait_ns)) bad = 1;
             for (int m = gissued > NG ? gissued - NG : 0; m < gissued; ++m)
-                if (!mbar_wait(&gfull[m % NG], (uint32_t)(m / NG) & 1u, kWaitNs)) bad = 1;
+                if (!mbar_wait(&gfull[m % NG], (uint32_t)(m / NG) & 1u, wait_ns)) bad = 1;
         }
     } else if (warp == kWarpMma) {
         // ============================================================ MMA issuer
@@ -414,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 // state only: T_n = S_{n-1} + k~^T [V | 1] per chunk
                 for (int n = 0; n < N; ++n) {
                     const int s = n % NS;
-                    if (!mbar_wait(&pro[s], (uint32_t)(n / NS) & 1u, kWaitNs) ||
-                        (n > 0 && !mbar_wait(sready, (uint32_t)(n - 1) & 1u, kWaitNs))) {
+                    if (!mbar_wait(&pro[s], (uint32_t)(n / NS) & 1u, wait_ns) ||
+                        (n > 0 && !mbar_wait(sready, (uint32_t)(n - 1) & 1u, wait_ns))) {
                         bad = 1;
                         break;
                     }
@@ -428,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     umma_commit(&empty[s]);
                 }
             } else if (N > 0) {
-                if (!mbar_wait(&pro[0], 0u, kWaitNs)) bad = 1;
+                if (!mbar_wait(&pro[0], 0u, wait_ns)) bad = 1;
                 tc_fence_after();
                 if (!bad) issue_qk(0);
             }
@@ -438,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 const uint64_t aq0 = sdesc_sw128(sm0 + tile_half(0, s, 0), 16, 1024);
                 const uint64_t aq1 = sdesc_sw128(sm0 + tile_half(0, s, 1), 16, 1024);
                 const uint64_t ak = dkm(n), bv = dvm(n);
-                if ((n > 0 || init) && !mbar_wait(sready, (uint32_t)(n - 1 + (init ? 1 : 0)) & 1u, kWaitNs)) {
+                if ((n > 0 || init) && !mbar_wait(sready, (uint32_t)(n - 1 + (init ? 1 : 0)) & 1u, wait_ns)) {
                     bad = 1;
                     break;
                 }
@@ -450,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 umma_commit(sdone);
                 // inter: O = q~ S_{n-1}
                 if (n > 0 || init) {
-                    if (n >= LY::NOB && !mbar_wait(&oempty[b], (uint32_t)((n - LY::NOB) / LY::NOB) & 1u, kWaitNs)) {
+                    if (n >= LY::NOB && !mbar_wait(&oempty[b], (uint32_t)((n - LY::NOB) / LY::NOB) & 1u, wait_ns)) {
                         bad = 1;
                         break;
                     }
@@ -461,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
                 umma_commit(sfree);
                 // intra: O += P [V | 1]
-                if (!mbar_wait(pfull, (uint32_t)n & 1u, kWaitNs)) {
+                if (!mbar_wait(pfull, (uint32_t)n & 1u, wait_ns)) {
                     bad = 1;
                     break;
                 }
@@ -474,8 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 // QK of the next chunk (P is read out of TMEM by then)
                 if (n + 1 < N) {
                     const int n1 = n + 1;
-                    if (!mbar_wait(&pro[n1 % NS], (uint32_t)(n1 / NS) & 1u, kWaitNs) ||
-                        !mbar_wait(pempty, (uint32_t)n & 1u, kWaitNs)) {
+                    if (!mbar_wait(&pro[n1 % NS], (uint32_t)(n1 / NS) & 1u, wait_ns) ||
+                        !mbar_wait(pempty, (uint32_t)n & 1u, wait_ns)) {
                         bad = 1;
                         break;
                     }
@@ -485,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             // every MMA this thread issued has completed before teardown
             umma_commit(drain);
-            if (!mbar_wait(drain, 0u, kWaitNs)) bad = 1;
+            if (!mbar_wait(drain, 0u, wait_ns)) bad = 1;
         }
     } else if ((warp >= 4 && warp < 8) || warp < 2 || warp >= 14) {
         // ============================================================ prologue
@@ -517,15 +535,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // segment so far (kept by quarter 3)
             float bl0 = 0.f, bl1 = 0.f, bt0 = 0.f, bt1 = 0.f;
             for (int n = 0; n < N; ++n) {
-                const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
+                const int s = n % NS, t0 = chunk_t0(n), c = min(kC, L - t0);
                 // the gate tile first: from its own ring (full pass) or from the stage.
                 // Without the normaliser no barrier follows: the quarter sums are
                 // double-buffered, so a warp may start this chunk while others finish
                 // the last one, and a failed wait is made uniform at the barrier after
                 // pass 1 (what pass 1 read then is discarded). The normalised forms
                 // (two stages) measured faster with the barrier kept.
-                bool ok = LY::GR ? mbar_wait(&gfull[n % NG], (uint32_t)(n / NG) & 1u, kWaitNs)
-                                 : mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
+                bool ok = LY::GR ? mbar_wait(&gfull[n % NG], (uint32_t)(n / NG) & 1u, wait_ns)
+                                 : mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, wait_ns);
                 if constexpr (NORM) {
                     if (named_sync_or<kBarPro, 256>(!ok)) {
                         bad = 1;
@@ -548,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 float *totn = tot + (NORM ? 0 : (n & 1) * 512);
                 *reinterpret_cast<f32x2_t *>(totn + qr * 128 + cw) = sq;
                 // then the q, k (, v) stage; the barrier also publishes the quarter sums
-                if (LY::GR && ok) ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
+                if (LY::GR && ok) ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, wait_ns);
                 if constexpr (GATE == 3) sK = sm + tile_half(2, s, ch);
                 uint32_t kw[8], qw[8], kn[8], qn[8];
                 if (ok) {
@@ -649,6 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // log decay of key channel pd over the previous chunk and over the segment so far
             float b_last = 0.f, b_total = 0.f;
             int m = 0;  // chunks into the current window
+            // REV takes a ragged last chunk first: it closes a window of its own,
+            // so that every window after it holds whole chunks only
+            const int rag0 = (REV && c0 == 0 && (L % kC) != 0) ? 1 : 0;
             if (GATE == 1) {
                 // the row factors gamma^(t+1) and gamma^-(t+1) are the same in every chunk
                 if (pd < 64) {
@@ -658,14 +679,16 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 named_sync<kBarPro, 256>();
             }
             for (int n = 0; n < N; ++n) {
-                const int s = n % NS, t0 = (c0 + n) * kC, c = min(kC, L - t0);
-                m = n % R;
+                const int s = n % NS, t0 = chunk_t0(n), c = min(kC, L - t0);
+                const int nw = n - rag0;  // chunks counted by the windows
+                m = nw < 0 ? 0 : nw % R;
+                const bool wend = nw < 0 || m == R - 1;  // this chunk closes its window
                 float gq = 1.f, gk = 1.f;
                 if (GATE == 1 && m > 0) {
                     gq = __expf((float)(kC * m) * lg);
                     gk = __expf(-(float)(kC * m) * lg);
                 }
-                const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, kWaitNs);
+                const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, wait_ns);
                 if (named_sync_or<kBarPro, 256>(!ok)) {
                     bad = 1;
                     break;
@@ -693,7 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                                     for (int e = 0; e < 4; ++e) u[e] = phi_elu1_bf16x2(u[e]);
                                 }
                                 if (GATE == 1) {
-                                    const float fr = fr_arr[row] * (isk ? gk : gq);
+                                    // (with REV the local index is c - 1 - row; rows past the
+                                    // end hold zeros and take any factor)
+                                    const float fr = fr_arr[REV ? ((c - 1 - row) & (kC - 1)) : row] * (isk ? gk : gq);
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) u[e] = pack_bf16(bf16lo(u[e]) * fr, bf16hi(u[e]) * fr);
                                 }
@@ -709,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     // retention: 1 inside a window (the state chain leaves the
                     // accumulator alone), the decay since the window began at its end
                     float fv = __expf(b_last);
-                    if (GATE == 1) fv = m == R - 1 ? __expf(b_last + (float)(kC * m) * lg) : 1.f;
+                    if (GATE == 1) fv = wend ? __expf(b_last + (float)(kC * m) * lg) : 1.f;
                     fbuf[(n % NF) * 128 + pd] = fv;
                     mbar_arrive(&ffull[n % NF]);
                 }
@@ -783,8 +808,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         }
         for (int n = 1; n < N; ++n) {
             // T_{n-1} is complete, and so is chunk n-1's decay factor
-            bool ok = mbar_wait(sdone, (uint32_t)(n - 1) & 1u, kWaitNs);
-            if (GATE != 0) ok = ok && mbar_wait(&ffull[(n - 1) % NF], (uint32_t)((n - 1) / NF) & 1u, kWaitNs);
+            bool ok = mbar_wait(sdone, (uint32_t)(n - 1) & 1u, wait_ns);
+            if (GATE != 0) ok = ok && mbar_wait(&ffull[(n - 1) % NF], (uint32_t)((n - 1) / NF) & 1u, wait_ns);
             if (named_sync_or<kBarState, 128>(!ok)) {
                 bad = 1;
                 break;
@@ -816,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             if (!SO) {
                 // the inter MMA of chunk n-1 has finished reading the previous copy
-                ok = mbar_wait(sfree, (uint32_t)(n - 1) & 1u, kWaitNs);
+                ok = mbar_wait(sfree, (uint32_t)(n - 1) & 1u, wait_ns);
                 if (named_sync_or<kBarState, 128>(!ok)) {
                     bad = 1;
                     break;
@@ -830,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         float *dst = SO ? p.seg_state + segblk : (p.nseg == 1 ? p.final_state : nullptr);
         if (!SO && dst) dst += (size_t)bh * blk;
         if (!bad && N > 0) {
-            bool ok = mbar_wait(sdone, (uint32_t)(N - 1) & 1u, kWaitNs) && mbar_wait(profinal, 0u, kWaitNs);
+            bool ok = mbar_wait(sdone, (uint32_t)(N - 1) & 1u, wait_ns) && mbar_wait(profinal, 0u, wait_ns);
             if (named_sync_or<kBarState, 128>(!ok)) {
                 bad = 1;
             } else if (dst != nullptr) {
@@ -865,9 +890,11 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     } else if (!SO && (warp == 12 || warp == 13)) {
         // ============================================================ outputs (TMEM lanes 0..63 = rows t)
         const int t = tid - 384;
+        // the mask: key columns at or before the query row (at or after it with REV)
+        auto keep = [&](int j) { return REV ? j >= t : j <= t; };
         for (int n = 0; n < N; ++n) {
-            const int b = n % LY::NOB, t0 = (c0 + n) * kC;
-            bool ok = mbar_wait(qk, (uint32_t)n & 1u, kWaitNs);
+            const int b = n % LY::NOB, t0 = chunk_t0(n);
+            bool ok = mbar_wait(qk, (uint32_t)n & 1u, wait_ns);
             if (named_sync_or<kBarOut, 64>(!ok)) {
                 bad = 1;
                 break;
@@ -911,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                             const int jj = q8 * 8 + 2 * e;
                             const uint32_t a0 = q8 < 4 ? r0[jj] : r1[jj - 32];
                             const uint32_t a1 = q8 < 4 ? r0[jj + 1] : r1[jj - 31];
-                            u[e] = pack_bf16(jj <= t ? __uint_as_float(a0) : 0.f, jj + 1 <= t ? __uint_as_float(a1) : 0.f);
+                            u[e] = pack_bf16(keep(jj) ? __uint_as_float(a0) : 0.f, keep(jj + 1) ? __uint_as_float(a1) : 0.f);
                         }
                         *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
                     }
@@ -920,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             fence_proxy_async_smem();
             mbar_arrive(pfull);
 
-            ok = mbar_wait(&ofull[b], (uint32_t)(n / LY::NOB) & 1u, kWaitNs);
+            ok = mbar_wait(&ofull[b], (uint32_t)(n / LY::NOB) & 1u, wait_ns);
             if (t == 0) bulk_wait_read<0>();  // the previous O tile has left the staging buffer
             if (named_sync_or<kBarOut, 64>(!ok)) {
                 bad = 1;
@@ -1068,12 +1095,12 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
 // after_scan: launched behind the segment scan as a programmatic dependent
 // launch, so that its CTAs set up and start on their first chunks while the
 // scan finishes (they wait for it before reading the carried states).
-template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false>
+template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false>
 int launch_t(const TcParams &prm, int grid, cudaStream_t s, bool after_scan) {
     using LY = Layout<GATE, NORM, SO, OF32>;
     static_assert(LY::NS >= 2 && LY::bytes <= kSmemBudget, "shared memory budget");
     static_assert(LY::colP + 64 <= kTmemCols && LY::colO1 + LY::NW <= LY::colP, "TMEM budget");
-    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO, OF32>;
+    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO, OF32, REV>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes) != cudaSuccess)
         return LA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1098,8 +1125,22 @@ int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm
 }
 
 template <bool SO>
-int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false, bool value_gate = false, bool pdl = false) {
+int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false, bool value_gate = false,
+                bool pdl = false, bool rev = false) {
     const bool elu1 = mode & LA_PHI_ELU1, norm = mode & LA_NORMALIZE;
+    if (rev) {
+        // anti-causal: identity feature map, no normaliser, no gate or the head gate
+        if (elu1 || norm || value_gate || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
+        const bool gh = mode & LA_GATE_HEAD;
+        if (SO)
+            return gh ? launch_t<1, false, false, true, false, true>(prm, grid, s, pdl)
+                      : launch_t<0, false, false, true, false, true>(prm, grid, s, pdl);
+        if (out_f32)
+            return gh ? launch_t<1, false, false, false, true, true>(prm, grid, s, pdl)
+                      : launch_t<0, false, false, false, true, true>(prm, grid, s, pdl);
+        return gh ? launch_t<1, false, false, false, false, true>(prm, grid, s, pdl)
+                  : launch_t<0, false, false, false, false, true>(prm, grid, s, pdl);
+    }
     if (value_gate) {
         // the per-channel gate on the value side: identity feature map, no
         // normaliser, bf16 output
@@ -1173,8 +1214,9 @@ size_t chunk_tc_scratch_bytes(const ChunkArgs &a) {
 // chunk_tc_scratch_bytes(a) bytes, 256-byte aligned). A sequence that is not
 // split is one launch; split sequences take three: the state-only pass, the
 // segment scan and the full pass from the carried states.
-int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch,
-                         size_t scratch_bytes) {
+namespace {
+int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch, size_t scratch_bytes,
+                         uint64_t wait_ns, int stall_chunk) {
     if (!get_encode()) return LA_ERR_CUDA;
     const int BH = a.B * a.H;
     const int nchunks = (a.L + kC - 1) / kC;
@@ -1191,9 +1233,12 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.mode = a.mode;
     prm.nseg = tc_segments(BH, nchunks, &prm.seg_chunks);
     prm.init0 = a.initial_state != nullptr;
+    prm.wait_ns = wait_ns;
+    prm.stall_chunk = stall_chunk;
+    if (stall_chunk >= 0 && prm.nseg != 1) return LA_ERR_UNSUPPORTED;  // the stall runs one launch only
     if (prm.nseg == 1) {
         prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
-        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32, a.value_gate);
+        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32, a.value_gate, false, a.reverse);
         if (rc == LA_OK) *launches += 1;
         return rc;
     }
@@ -1206,7 +1251,7 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.seg_state = seg_state;
     prm.seg_logdecay = seg_logdecay;
     prm.final_state = nullptr;
-    int rc = launch_mode<true>(prm, (int)nsb, s, a.mode, false, a.value_gate);
+    int rc = launch_mode<true>(prm, (int)nsb, s, a.mode, false, a.value_gate, false, a.reverse);
     if (rc != LA_OK) return rc;
     *launches += 1;
     la_seg_scan_kernel<<<dim3((unsigned)BH, (unsigned)((blk + 255) / 256)), 256, 0, s>>>(
@@ -1216,9 +1261,23 @@ int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.state_in = state_in;
     prm.seg_state = nullptr;
     prm.seg_logdecay = nullptr;
-    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate, true);
+    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate, true, a.reverse);
     if (rc == LA_OK) *launches += 1;
     return rc;
+}
+}  // namespace
+
+int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch,
+                         size_t scratch_bytes) {
+    return launch_chunk_tc_impl(a, s, launches, scratch, scratch_bytes, kWaitNs, -1);
+}
+
+// Diagnostics: one unsplit launch whose producer issues no tiles from chunk
+// stall_chunk on and whose bounded waits give up after wait_ns, so that the
+// time-out path (error word, drain, TMEM freed) runs on purpose.
+int launch_chunk_tc_stalled(const ChunkArgs &a, cudaStream_t s, int *launches, int stall_chunk,
+                            unsigned long long wait_ns) {
+    return launch_chunk_tc_impl(a, s, launches, nullptr, 0, wait_ns, stall_chunk);
 }
 
 // The tensor-core path with its scratch (if any) allocated and freed in

@@ -20,6 +20,7 @@ LA_GATE_HEAD = 0x4
 LA_GATE_CHANNEL = 0x8
 LA_DTYPE_F32 = 0x10
 LA_KERNEL_SIMT = 0x20
+LA_REVERSE = 0x40
 
 LA_OK = 0
 STATUS = {0: "LA_OK", -1: "LA_ERR_INVALID_ARG", -2: "LA_ERR_UNSUPPORTED", -3: "LA_ERR_MISALIGNED",
@@ -41,6 +42,7 @@ SIGNATURES = {
     "la_status_string": ([_I], ctypes.c_char_p),
     "la_kernel_launches": ([], ctypes.c_ulonglong),
     "la_device_status": ([_VP], _I),
+    "la_chunk_fwd_stall_test": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, ctypes.c_longlong, _VP], _I),
 }
 
 _lib = None
@@ -72,7 +74,7 @@ def load():
     return _lib
 
 
-def mode_bits(phi="elu1", normalize=False, gate=None, dtype=torch.bfloat16, simt=False):
+def mode_bits(phi="elu1", normalize=False, gate=None, dtype=torch.bfloat16, simt=False, reverse=False):
     m = LA_PHI_ELU1 if phi == "elu1" else LA_PHI_IDENTITY
     if normalize:
         m |= LA_NORMALIZE
@@ -88,6 +90,8 @@ def mode_bits(phi="elu1", normalize=False, gate=None, dtype=torch.bfloat16, simt
         raise ValueError("q, k, v must be bfloat16 or float32")
     if simt:
         m |= LA_KERNEL_SIMT
+    if reverse:
+        m |= LA_REVERSE
     return m
 
 
@@ -112,10 +116,12 @@ def state_block(dk, dv, normalize):
 
 
 def chunk_fwd(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None, chunk=64,
-              out=None, final_state=None, want_state=True, simt=False, stream=None, initial_state=None):
+              out=None, final_state=None, want_state=True, simt=False, stream=None, initial_state=None,
+              reverse=False):
     """la_chunk_fwd over q, k [B,H,L,dk], v [B,H,L,dv]. Returns (out, final_state).
     With ``initial_state`` ([B,H,block] fp32) it is la_chunk_fwd_from_state: the
-    sequences continue from that state instead of zero."""
+    sequences continue from that state instead of zero. ``reverse`` sets
+    LA_REVERSE (the anti-causal form)."""
     B, H, L, dk = q.shape
     dv = v.shape[-1]
     if out is None:
@@ -123,7 +129,7 @@ def chunk_fwd(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None
     if final_state is None and want_state:
         final_state = torch.empty(B, H, state_block(dk, dv, normalize), dtype=torch.float32,
                                   device=q.device)
-    mode = mode_bits(phi, normalize, gate_kind, q.dtype, simt)
+    mode = mode_bits(phi, normalize, gate_kind, q.dtype, simt, reverse)
     if initial_state is None:
         rc = load().la_chunk_fwd(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
                                  _dev(out, "out"), _dev(final_state, "final_state"),
@@ -292,3 +298,21 @@ def device_status(stream=None):
     la_status of the library's bounded device-side waits since the last call:
     0, or -5 (LA_ERR_TIMEOUT) if a kernel gave one up. Clears the flags."""
     return int(load().la_device_status(_stream(stream)))
+
+
+def chunk_fwd_stall_test(q, k, v, gate=None, *, phi="elu1", normalize=False, gate_kind=None, stall_chunk=1,
+                         wait_ns=20_000_000, out=None, stream=None):
+    """la_chunk_fwd_stall_test: the tensor-core forward with its producer
+    stopping before chunk ``stall_chunk`` and every bounded wait limited to
+    ``wait_ns``; afterwards la_device_status reports LA_ERR_TIMEOUT. Returns
+    ``out`` (not valid)."""
+    B, H, L, dk = q.shape
+    if out is None:
+        out = torch.empty(B, H, L, v.shape[-1], dtype=q.dtype, device=q.device)
+    mode = mode_bits(phi, normalize, gate_kind, q.dtype)
+    rc = load().la_chunk_fwd_stall_test(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(gate, "gate"),
+                                        _dev(out, "out"), B, H, L, mode, int(stall_chunk), int(wait_ns),
+                                        _stream(stream))
+    if rc != LA_OK:
+        raise LAError("la_chunk_fwd_stall_test", rc)
+    return out

@@ -36,7 +36,7 @@ def to_dev(inp):
     return {k: (None if v is None else v.to(d)) for k, v in inp.items()}
 
 
-def run_gpu(inp, cfg, chunk=None, simt=False, initial_state=None):
+def run_gpu(inp, cfg, chunk=None, simt=False, initial_state=None, reverse=False):
     """la_chunk_fwd (la_chunk_fwd_from_state with ``initial_state``, a [B,H,block]
     float32 tensor) through the binding; outputs are NaN-poisoned first so that
     an element the kernel never writes fails the comparison."""
@@ -49,7 +49,8 @@ def run_gpu(inp, cfg, chunk=None, simt=False, initial_state=None):
                     dtype=torch.float32, device="cuda")
     la.chunk_fwd(x["q"], x["k"], x["v"], x["gate"], phi=cfg["phi"], normalize=cfg["normalize"],
                  gate_kind=cfg["gate"], chunk=chunk or cfg["chunk"], out=out, final_state=st,
-                 simt=simt, initial_state=None if initial_state is None else initial_state.cuda())
+                 simt=simt, initial_state=None if initial_state is None else initial_state.cuda(),
+                 reverse=reverse)
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), st.cpu().numpy()
 

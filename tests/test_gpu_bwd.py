@@ -86,18 +86,22 @@ def test_fp32_head_dims(dk, dv):
 @pytest.mark.parametrize("simt", [False, True], ids=["default", "simt"])
 def test_bf16_modes(m, simt):
     """Every mode; except the per-channel gate with the normaliser the default
-    route is the tensor-core one: prep, three forwards, post (scalar gate);
-    three preps, six forwards (five writing fp32), post (normalised); prep,
-    three forwards (two with the gate on the value side), two posts and the
-    gate gradient's scan (per-channel gate)."""
+    route is the tensor-core one: three forwards, two of them anti-causal
+    (scalar gate, identity feature map), with phi = elu + 1 a pass before them
+    for phi(q), phi(k) and one after for phi'; three preps, six forwards (five
+    writing fp32, three anti-causal), post (normalised); prep, three forwards
+    (two with the gate on the value side), two posts and the gate gradient's
+    scan (per-channel gate)."""
     cfg = W.workload("la", B=2, H=3, L=333, **m)
     launches = _check(cfg, seed=3, simt=simt)
     tc = not simt and not (m["normalize"] and m["gate"] == "channel")
     # a forward is three launches when the short batch is split into segments
     if tc and m["gate"] == "channel":
         assert launches in (9, 15), launches  # prep, three forwards, two posts, the dg scan
+    elif tc and m["normalize"]:
+        assert launches in (10, 22), launches
     elif tc:
-        assert launches in ((10, 22) if m["normalize"] else (5, 11)), launches
+        assert launches in ((5, 11) if m["phi"] == "elu1" else (3, 9)), launches
     else:
         assert launches == (4 if m["normalize"] else 3), launches
 
@@ -120,8 +124,8 @@ def test_full_size_sampled_heads(name):
     batch row."""
     cfg = W.workload(name)
     launches = _check(cfg, seed=0, heads=2)
-    # retention: prep, three tensor-core forwards, post; la: three preps, six forwards, post
-    assert launches == (10 if cfg["normalize"] else 5)
+    # retention: three tensor-core forwards (two anti-causal); la: three preps, six forwards, post
+    assert launches == (10 if cfg["normalize"] else 3)
 
 
 def test_without_the_gate_gradient():

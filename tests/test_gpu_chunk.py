@@ -210,3 +210,49 @@ def test_retention_window_ends(B, H, L):
     out, st = run_gpu(inp, cfg)
     e_out, e_st = rel_err(out, out_ref), rel_err(st, st_ref)
     assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
+
+
+# ------------------------------------------------------------------ the anti-causal form (LA_REVERSE)
+
+def _flip(inp):
+    return {n: (t.flip(2) if (t is not None and t.dim() == 4) else t) for n, t in inp.items()}
+
+
+def _check_reverse(cfg, inp, initial_state=None):
+    """LA_REVERSE sums over the token and every later one; with a scalar decay
+    that is the causal recurrence of the token-reversed sequence, which the
+    oracle computes (its final state is the state before token 0)."""
+    s0 = None if initial_state is None else initial_state.numpy()
+    out_ref, st_ref = run_oracle(_flip(inp), cfg, state_in=s0)
+    out_ref = out_ref[:, :, ::-1]
+    out, st = run_gpu(inp, cfg, reverse=True, initial_state=initial_state)
+    e_out, e_st = rel_err(out, out_ref), rel_err(st, st_ref)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
+
+
+@pytest.mark.parametrize("gate", [None, "head"])
+@pytest.mark.parametrize("B,H,L", [(1, 4, 1000), (2, 40, 333), (2, 40, 129), (1, 80, 64), (1, 80, 1)],
+                         ids=["split", "unsplit-ragged", "unsplit-129", "one-chunk", "one-token"])
+def test_reverse_matches_the_reversed_causal_oracle(gate, B, H, L):
+    from retention_gb300 import la
+    cfg = W.workload("retention", B=B, H=H, L=L, gate=gate)
+    mode = la.mode_bits("identity", False, gate, reverse=True)
+    assert la.chunk_fwd_path(B, H, L, 128, 128, mode, 64) == 1
+    _check_reverse(cfg, W.chunk_inputs(cfg, seed=L + H))
+
+
+@pytest.mark.parametrize("B,H,L", [(1, 8, 6100), (2, 40, 1300)], ids=["split", "unsplit"])
+def test_reverse_window_ends(B, H, L):
+    """Decays whose rescale windows close after 1 to 625 chunks, on ragged
+    lengths: the reverse form takes the ragged chunk first, and that chunk
+    closes a window of its own."""
+    cfg = W.workload("retention", B=B, H=H, L=L)
+    _check_reverse(cfg, window_inputs(cfg, seed=23))
+
+
+@pytest.mark.parametrize("B,H,L", [(1, 4, 1000), (2, 40, 333)], ids=["split", "unsplit"])
+def test_reverse_from_a_state(B, H, L):
+    """An initial state of the reverse form sits after the last token."""
+    cfg = W.workload("retention", B=B, H=H, L=L)
+    s0 = W.decode_state(dict(cfg, state_std=0.1), 77)
+    _check_reverse(cfg, W.chunk_inputs(cfg, seed=24), initial_state=s0)
