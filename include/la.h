@@ -210,8 +210,14 @@ int la_group_norm_swish(const void *x, const void *ogate, const float *gn_weight
  * la_chunk_fwd_gn_swish -- la_chunk_fwd_from_state followed by the RetNet
  * output epilogue of la_group_norm_swish on its output: out is
  * swish(ogate) * GroupNorm_h(o), o the attention output (after the division by
- * the normaliser when LA_NORMALIZE is set). The epilogue is a second kernel on
- * the same stream, in place on out.
+ * the normaliser when LA_NORMALIZE is set). On the tensor-core kernel without
+ * the normaliser and with no gate or the head gate (RetNet's retention among
+ * them) the epilogue runs in the kernel's store: each token row is normalised
+ * from the fp32 accumulator, and the output gate tile is read by TMA beside it,
+ * so o never goes to memory. Otherwise it is a second kernel on the same
+ * stream, in place on out. The swish in the store is formed in bf16 arithmetic
+ * with the hardware tanh approximation (u sigmoid(u) = h + h tanh(h),
+ * h = u / 2).
  *
  *   ogate          [B][H][L][d_v], the type of q; required
  *   gn_weight, gn_bias, gn_eps   as la_group_norm_swish

@@ -86,13 +86,23 @@ int chunk_fwd(const void *q, const void *k, const void *v, const void *gate, con
     la::ChunkArgs a{q, k, v, gate, out, final_state, B, H, L, dk, dv, mode & ~LA_REVERSE, chunk, initial_state,
                     0, 0, rev ? 1 : 0};
     int launches = 0;
-    if (!(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a))
+    const bool tc = !(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a);
+    // the output epilogue goes into the tensor-core kernel's store where it can
+    bool fused = false;
+    if (ep.ogate && tc && la::chunk_tc_fuses_epilogue(a)) {
+        a.gn_ogate = ep.ogate;
+        a.gn_weight = ep.weight;
+        a.gn_bias = ep.bias;
+        a.gn_eps = ep.eps;
+        fused = true;
+    }
+    if (tc)
         rc = la::launch_chunk_tc(a, s, &launches);
     else if (rev)
         return LA_ERR_UNSUPPORTED;  // the anti-causal form runs on the tensor-core kernel only
     else
         rc = la::launch_chunk_simt(a, s, &launches);
-    if (rc == LA_OK && ep.ogate) {
+    if (rc == LA_OK && ep.ogate && !fused) {
         // the output epilogue: a streaming pass of its own, in place on out
         la::GnArgs g{out, ep.ogate, ep.weight, ep.bias, ep.eps, out, B, H, L, dv, mode & LA_DTYPE_F32};
         rc = la::launch_gn_swish(g, s, &launches);

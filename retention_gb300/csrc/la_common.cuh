@@ -51,6 +51,11 @@ struct ChunkArgs {
     // the anti-causal form out_s = sum_{t >= s} gamma^{t-s} (q_s . k_t) v_t, the
     // chunks taken from the end; final_state is then the state before token 0
     int reverse;
+    // tensor-core path only (chunk_tc_fuses_epilogue): the RetNet output epilogue
+    // applied in the store, out = swish(og) * GroupNorm_h(o); null: none
+    const void *gn_ogate;
+    const float *gn_weight, *gn_bias;
+    float gn_eps;
 };
 
 struct GnArgs {
@@ -100,6 +105,7 @@ int launch_bwd_tc(const BwdArgs &a, cudaStream_t s, int *launches);
 size_t bwd_scratch_bytes(const BwdArgs &a);
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);
+bool chunk_tc_fuses_epilogue(const ChunkArgs &a);
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a);
 int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch, size_t scratch_bytes);
 // diagnostics: the tensor-core forward (unsplit only) with its producer stopping

@@ -67,7 +67,7 @@ constexpr uint32_t kTile = kC * kD * 2;  // bf16 [64 x 128] tile: 16 KiB = two 8
 constexpr uint32_t kHalf = 8192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;  // default wait limit: far beyond any legitimate wait
-constexpr int kBarPro = 1, kBarState = 2, kBarOut = 3;  // named barrier ids
+constexpr int kBarPro = 1, kBarState = 2, kBarOut = 3, kBarP = 4;  // named barrier ids
 // The producer and the MMA issuer sit on the SM sub-partitions (warp % 4) that
 // host the fewest busy warps, so their short instruction streams issue promptly.
 constexpr int kWarpProducer = 2, kWarpMma = 3;
@@ -76,6 +76,9 @@ __device__ unsigned int g_tc_error;
 
 struct TcParams {
     CUtensorMap tq, tk, tv, tg, to;
+    CUtensorMap tog;          // the RetNet output gate og (fused epilogue instances)
+    const float *gn_w, *gn_b; // GroupNorm weight and bias [H][128] or null
+    float gn_eps;
     const float *gamma;
     float *final_state;      // [BH][blk], written by an unsplit full pass
     const float *state_in;   // [BH][nseg][blk]: state at each segment start (full pass)
@@ -103,7 +106,7 @@ constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
 // remaining blocks in order. The gate tiles g have a ring of their own (GR):
 // the prologue is done with g after its first pass, so g is released early
 // and the next chunk's g is already in place when the prologue turns to it.
-template <int GATE, bool NORM, bool SO, bool OF32 = false>
+template <int GATE, bool NORM, bool SO, bool OF32 = false, bool EPI = false>
 struct Layout {
     static constexpr bool GR = GATE >= 2 && !SO;
     // gated without the normaliser: three q|k|v stages and one gate slot fit;
@@ -137,13 +140,17 @@ struct Layout {
     // NF = NS + 1 slots: chunk n's decay factor goes to slot n % NF at the end of
     // its prologue, for the state chain to rescale T_n with.
     static constexpr int NF = NS + 1;
-    static constexpr uint32_t F = O + (SO ? 0 : (OF32 ? 32768 : 16384));
+    // (EPI) a second staging buffer: the og tile of chunk n lands in buffer n % 2
+    // and the chunk's result is written over it there
+    static constexpr uint32_t O2 = O + (SO ? 0 : (OF32 ? 32768 : 16384));
+    static constexpr uint32_t F = O2 + (EPI ? 16384 : 0);
     static constexpr uint32_t nfbuf = GATE != 0 ? NF * 128 : 0, nfq = GATE == 1 ? 128 : 0;
     static constexpr uint32_t ntot = GATE >= 2 ? (NORM ? 512 : 1024) : 0;  // quarter sums (one or two chunks)
-    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + ntot) * 4;
+    static constexpr uint32_t nwb = EPI ? 512 : 0;  // GroupNorm weight, bias [128] each; half-row (m, M2) [2][64][2]
+    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + ntot + nwb) * 4;
     // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal,
-    // drain; gfull, gempty [NG]; ffull [NF]
-    static constexpr uint32_t nbar = 3 * NS + 12 + 2 * NG + NF;
+    // drain; gfull, gempty [NG]; ffull [NF]; (ogfull [2]: the output gate tiles)
+    static constexpr uint32_t nbar = 3 * NS + 12 + 2 * NG + NF + (EPI ? 2 : 0);
     static constexpr uint32_t Misc = Bar + nbar * 8;  // TMEM base address
     static constexpr uint32_t bytes = Misc + 16 + 1024;  // + slack for the 1024-byte alignment
     // TMEM columns (region bases 32-column aligned). With the ones column the
@@ -219,6 +226,23 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
+// swish(u) = u sigmoid(u) = h + h tanh(h), h = u / 2, on two packed bf16
+// values with the hardware tanh approximation (the output is bf16 either way)
+__device__ __forceinline__ uint32_t swish_bf16x2(uint32_t u) {
+    const uint32_t half = 0x3F003F00u;  // bf16 0.5 in both halves
+    uint32_t h, th, r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(h) : "r"(u), "r"(half));
+    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(th) : "r"(h));
+    asm("fma.rn.bf16x2 %0, %1, %2, %1;" : "=r"(r) : "r"(h), "r"(th));
+    return r;
+}
+// two fp32 values rounded to one packed bf16 word (lo in the low half)
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // elu(x) + 1 on two packed bf16 values in bf16 arithmetic:
 // max(x, 0) + 2^(min(x, 0) * log2 e). The exponent argument is rounded to bf16,
 // so for x < 0 the result carries a relative error below 2^-8 |x| on top of the
@@ -245,11 +269,31 @@ __device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
 // c tokens is c - 1 - r, and the mask keeps key columns at or after the query
 // row. The state carried from chunk to chunk is then the sum over all later
 // tokens, decayed to the start of the chunk after the current one.
-template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false>
+//
+// EPI: the RetNet output epilogue in the output role's store (learnllm m22
+// "Retention": a GroupNorm per head and a swish output gate),
+//   out_t = swish(og_t) * ((o_t - mean) / sqrt(var + eps) * weight[h] + bias[h]),
+// mean and the biased variance over the 128 values of row t, from the fp32
+// accumulator. Each output thread owns one token row, so the statistics need
+// no exchange between threads; the og tile comes by TMA into the staging
+// buffer, and each row is overwritten in place by its result.
+template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false, bool EPI = false>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
-    using LY = Layout<GATE, NORM, SO, OF32>;
+    using LY = Layout<GATE, NORM, SO, OF32, EPI>;
     static_assert(GATE != 3 || (!ELU1 && !NORM), "the value-side gate takes features as given, no normaliser");
     static_assert(!REV || (GATE <= 1 && !ELU1 && !NORM), "the anti-causal instance: scalar decay, features as given");
+    static_assert(!EPI || (GATE <= 1 && !NORM && !SO && !OF32 && !REV), "the fused epilogue: bf16 output, no normaliser");
+    // SPLIT (the fused epilogue): P and the outputs are separate roles, so P of
+    // chunk n + 1 is formed while chunk n's outputs are finished. TMEM lanes
+    // 0..63 (the token rows) are reachable from SM sub-partitions 0 and 1 only:
+    // warps 12 and 13 make P, warps 0, 1, 4 and 5 finish the outputs, half a row
+    // each, and the prologue moves to warps 6, 7, 14 and 15 (sub-partitions 2
+    // and 3). Otherwise the prologue runs on warps 4-7, 0, 1, 14, 15 and warps
+    // 12 and 13 make P and the outputs in turn. (The split layout measured
+    // slower without the epilogue: the prologue's work then has the special
+    // function units of two sub-partitions only.)
+    constexpr bool SPLIT = EPI;
+    constexpr int PT = SPLIT ? 128 : 256;  // prologue threads
     constexpr int NS = LY::NS;
     constexpr int NG = LY::GR ? LY::NG : 1;  // gate ring slots (the ring exists only if GR)
     extern __shared__ uint8_t smem_raw[];
@@ -276,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     float *fq = fbuf + LY::nfbuf;                           // [64] retention: gamma^(t+1)
     float *fk = fq + 64;                                    // [64] retention: gamma^-(t+1)
     float *tot = fq + LY::nfq;                              // [1 or 2][4][128] gated: per-quarter log2 decay sums
+    float *gnw = tot + LY::ntot, *gnb = gnw + 128;          // (EPI) GroupNorm weight and bias of head h
     // Shared-memory offset of half h (columns 64h..64h+63) of tile tl of stage
     // s: tl = 0 q, 1 k, 2 v, 3 g (the g tile of a state-only stage)
     auto tile_half = [&](int tl, int s, int h) -> uint32_t {
@@ -293,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     uint64_t *sready = sfree + 1, *profinal = sready + 1, *drain = profinal + 1;
     uint64_t *gfull = drain + 1, *gempty = gfull + LY::NG;  // (empty arrays unless GR)
     uint64_t *ffull = gempty + LY::NG;                      // [NF]: fbuf slot written
+    uint64_t *ogfull = ffull + NF;                          // (EPI) [2]: og tile in staging buffer 0 / 1
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::Misc);
     uint8_t *sP = sm + LY::P, *sS = sm + LY::S, *sO = sm + LY::O;
 
@@ -304,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&pro[s], 256);
+            mbar_init(&pro[s], PT);
         }
         for (int sg = 0; sg < LY::NG; ++sg) {
             mbar_init(&gfull[sg], 1);
@@ -312,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ofull[b], 1);
-            mbar_init(&oempty[b], 64);
+            mbar_init(&oempty[b], SPLIT ? 128 : 64);
         }
         mbar_init(qk, 1);
         mbar_init(pfull, 64);
@@ -322,6 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         mbar_init(sready, 128);
         mbar_init(profinal, GATE >= 2 ? 64 : 128);
         for (int j = 0; j < NF; ++j) mbar_init(&ffull[j], GATE >= 2 ? 64 : 128);
+        if (EPI) {
+            mbar_init(&ogfull[0], 1);
+            mbar_init(&ogfull[1], 1);
+        }
         mbar_init(drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
@@ -329,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         tma_prefetch_desc(&p.tv);
         tma_prefetch_desc(&p.to);
         if (GATE >= 2) tma_prefetch_desc(&p.tg);
+        if (EPI) tma_prefetch_desc(&p.tog);
     }
     if (NORM) {
         // constant blocks: the [64 x 64] atom(s) whose column 0 is 1 (the ones
@@ -505,11 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             umma_commit(drain);
             if (!mbar_wait(drain, 0u, wait_ns)) bad = 1;
         }
-    } else if ((warp >= 4 && warp < 8) || warp < 2 || warp >= 14) {
+    } else if (SPLIT ? (warp == 6 || warp == 7 || warp >= 14) : ((warp >= 4 && warp < 8) || warp < 2 || warp >= 14)) {
         // ============================================================ prologue
         // 256 threads in eight warps, two on each SM sub-partition: prologue warp
         // pw = warps 4..7 -> 0..3, warps 0, 1 -> 4, 5, warps 14, 15 -> 6, 7
-        const int pw = (warp >= 4 && warp < 8) ? warp - 4 : warp < 2 ? warp + 4 : warp - 8;
+        const int pw = SPLIT ? ((warp & 1) | (warp >= 14 ? 2 : 0))
+                           : (warp >= 4 && warp < 8) ? warp - 4 : warp < 2 ? warp + 4 : warp - 8;
         if constexpr (GATE >= 2) {
             // Prologue warp pw takes the channel half ch = pw % 2 and the row
             // quarter qr = pw / 2;
@@ -648,10 +700,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 mbar_arrive(profinal);
             }
         } else {
-            // Thread pd (0..255) owns the 16-byte pieces pd + 256 j (j = 0..3) of
-            // each tile: block j / 2, row pd / 8 + 32 (j % 2), slot pd % 8 (the
-            // eight lanes of a quarter warp share a row: no bank conflicts).
-            // Threads pd < 128 also own key channel pd for the decay factors.
+            // Thread pd (0..PT-1) owns the 16-byte pieces pd + PT j of each tile
+            // (block, row and slot below; the eight lanes of a quarter warp share a
+            // row: no bank conflicts). Threads pd < 128 also own key channel pd for
+            // the decay factors.
             const int pd = 32 * pw + lane;
             const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
             // Retention applies the state's decay once per window of R chunks instead
@@ -676,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     fq[pd] = __expf((float)(pd + 1) * lg);
                     fk[pd] = __expf(-(float)(pd + 1) * lg);
                 }
-                named_sync<kBarPro, 256>();
+                named_sync<kBarPro, PT>();
             }
             for (int n = 0; n < N; ++n) {
                 const int s = n % NS, t0 = chunk_t0(n), c = min(kC, L - t0);
@@ -689,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     gk = __expf(-(float)(kC * m) * lg);
                 }
                 const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, wait_ns);
-                if (named_sync_or<kBarPro, 256>(!ok)) {
+                if (named_sync_or<kBarPro, PT>(!ok)) {
                     bad = 1;
                     break;
                 }
@@ -698,14 +750,16 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     for (int isk = SO ? 1 : 0; isk < 2; ++isk) {
                         uint8_t *blk0 = sm + tile_half(isk, s, 0), *blk1 = sm + tile_half(isk, s, 1);
                         const float *fr_arr = isk ? fk : fq;
-                        uint4 w[4];
+                        // piece x = pd + PT j: block x / 512, row (x / 8) % 64, slot x % 8
+                        constexpr int NJ = 1024 / PT;
+                        uint4 w[NJ];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            w[j] = *reinterpret_cast<const uint4 *>((j >> 1 ? blk1 : blk0) +
-                                                                    ((pd >> 3) + 32 * (j & 1)) * 128 + (pd & 7) * 16);
+                        for (int j = 0; j < NJ; ++j)
+                            w[j] = *reinterpret_cast<const uint4 *>(((pd + PT * j) >> 9 ? blk1 : blk0) +
+                                                                    (((pd + PT * j) >> 3) & 63) * 128 + (pd & 7) * 16);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int row = (pd >> 3) + 32 * (j & 1);
+                        for (int j = 0; j < NJ; ++j) {
+                            const int row = ((pd + PT * j) >> 3) & 63;
                             uint4 &x = w[j];
                             if (isk && row >= c) {
                                 x = make_uint4(0u, 0u, 0u, 0u);
@@ -724,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                                 }
                                 x = make_uint4(u[0], u[1], u[2], u[3]);
                             }
-                            *reinterpret_cast<uint4 *>((j >> 1 ? blk1 : blk0) + row * 128 + (pd & 7) * 16) = x;
+                            *reinterpret_cast<uint4 *>(((pd + PT * j) >> 9 ? blk1 : blk0) + row * 128 + (pd & 7) * 16) = x;
                         }
                     }
                 }
@@ -887,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
             }
         }
-    } else if (!SO && (warp == 12 || warp == 13)) {
+    } else if (!SO && !SPLIT && (warp == 12 || warp == 13)) {
         // ============================================================ outputs (TMEM lanes 0..63 = rows t)
         const int t = tid - 384;
         // the mask: key columns at or before the query row (at or after it with REV)
@@ -1006,6 +1060,162 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
         }
         if (t == 0) bulk_wait<0>();
+    } else if (SPLIT && (warp == 12 || warp == 13)) {
+        // ============================================================ P (split roles)
+        // P row t of every chunk (TMEM lanes 0..63); the outputs are other
+        // warps' work, so P of chunk n + 1 is formed while chunk n is finished
+        const int t = tid - 384;
+        // the mask: key columns at or before the query row (at or after it with REV)
+        auto keep = [&](int j) { return REV ? j >= t : j <= t; };
+        for (int n = 0; n < N; ++n) {
+            // QK of this chunk, and the intra MMA of the last one has read the P tile
+            bool ok = mbar_wait(qk, (uint32_t)n & 1u, wait_ns);
+            if (n > 0) ok = ok && mbar_wait(&ofull[(n - 1) % LY::NOB], (uint32_t)((n - 1) / LY::NOB) & 1u, wait_ns);
+            if (named_sync_or<kBarP, 64>(!ok)) {
+                bad = 1;
+                break;
+            }
+            tc_fence_after();
+            uint8_t *prow = sP + t * 128;
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tmem + lane_base + LY::colP, r0);
+            tmem_ld32(tmem + lane_base + LY::colP + 32, r1);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(pempty);
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) {
+                uint32_t u[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = q8 * 8 + 2 * e;
+                    const uint32_t a0 = q8 < 4 ? r0[jj] : r1[jj - 32];
+                    const uint32_t a1 = q8 < 4 ? r0[jj + 1] : r1[jj - 31];
+                    u[e] = pack_bf16(keep(jj) ? __uint_as_float(a0) : 0.f, keep(jj + 1) ? __uint_as_float(a1) : 0.f);
+                }
+                *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(pfull);
+        }
+    } else if (EPI && (warp == 0 || warp == 1 || warp == 4 || warp == 5)) {
+        // ============================================================ outputs with the RetNet epilogue
+        // TMEM lanes 0..63 = rows t, on SM sub-partitions 0 and 1: warps 0 and 1
+        // finish columns 0..63 of O, warps 4 and 5 columns 64..127. Each thread
+        // reads its half row of O out of TMEM once and keeps it in registers;
+        // the two halves of a row combine their mean and squared deviations
+        // (m, M2) through shared memory: mean = (m0 + m1) / 2,
+        // M2 = M2_0 + M2_1 + (m0 - m1)^2 * 64 * 64 / 128 (the same expressions,
+        // in the same order, in both halves).
+        const int t = (warp & 1) * 32 + lane, oh = warp >= 4 ? 1 : 0;
+        const bool lead = oh == 0 && t == 0;
+        float *part = gnb + kD;  // [2][64] (m, M2) of each half row
+        {
+            const int col = 64 * oh + t;
+            gnw[col] = p.gn_w ? p.gn_w[(size_t)h * kD + col] : 1.f;
+            gnb[col] = p.gn_b ? p.gn_b[(size_t)h * kD + col] : 0.f;
+        }
+        named_sync<kBarOut, 128>();
+        // staging buffer of chunk m, and the request of its og tile
+        auto obuf = [&](int m) { return sm + ((m & 1) ? LY::O2 : LY::O); };
+        auto og_load = [&](int m) {
+            uint8_t *dst = obuf(m);
+            mbar_arrive_expect_tx(&ogfull[m & 1], kTile);
+            tma_load_3d(dst, &p.tog, &ogfull[m & 1], 0, chunk_t0(m), bh);
+            tma_load_3d(dst + kHalf, &p.tog, &ogfull[m & 1], 64, chunk_t0(m), bh);
+        };
+        int ogi = 0;  // (lead) og tiles requested
+        if (lead && N > 0) og_load(ogi++);
+        for (int n = 0; n < N; ++n) {
+            const int b = n % LY::NOB, t0 = chunk_t0(n);
+            bool ok = mbar_wait(&ofull[b], (uint32_t)(n / LY::NOB) & 1u, wait_ns) &&
+                      mbar_wait(&ogfull[n & 1], (uint32_t)(n >> 1) & 1u, wait_ns);
+            if (lead && ok && n + 1 < N) {
+                // the next chunk's og tile into the buffer the store of chunk n - 1
+                // read from
+                if (n > 0) bulk_wait_read<0>();
+                og_load(ogi++);
+            }
+            if (named_sync_or<kBarOut, 128>(!ok)) {
+                bad = 1;
+                break;
+            }
+            tc_fence_after();
+            // this thread's half row of O; the accumulator is free once it is read
+            uint32_t x0[32], x1[32];
+            {
+                const uint32_t tO = tmem + lane_base + (b ? LY::colO1 : LY::colO0) + 64 * oh;
+                tmem_ld32(tO, x0);
+                tmem_ld32(tO + 32, x1);
+                tmem_ld_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(&oempty[b]);
+            // half-row mean and squared deviations
+            f32x2_t acc = f2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                acc = f2_add(acc, f2(__uint_as_float(x0[2 * e]), __uint_as_float(x0[2 * e + 1])));
+                acc = f2_add(acc, f2(__uint_as_float(x1[2 * e]), __uint_as_float(x1[2 * e + 1])));
+            }
+            float a0, a1;
+            f2_split(acc, a0, a1);
+            const float mh = (a0 + a1) * (1.f / 64.f);
+            const f32x2_t nm = f2(-mh, -mh);
+            acc = f2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const f32x2_t d0 = f2_add(f2(__uint_as_float(x0[2 * e]), __uint_as_float(x0[2 * e + 1])), nm);
+                const f32x2_t d1 = f2_add(f2(__uint_as_float(x1[2 * e]), __uint_as_float(x1[2 * e + 1])), nm);
+                acc = f2_fma(d0, d0, acc);
+                acc = f2_fma(d1, d1, acc);
+            }
+            f2_split(acc, a0, a1);
+            const float m2h = a0 + a1;
+            *reinterpret_cast<float2 *>(part + (oh * 64 + t) * 2) = make_float2(mh, m2h);
+            named_sync<kBarOut, 128>();
+            const float2 other = *reinterpret_cast<const float2 *>(part + ((1 - oh) * 64 + t) * 2);
+            const float mean = (mh + other.x) * 0.5f;
+            const float dm = mh - other.x;
+            const float rstd = rsqrtf((m2h + other.y + dm * dm * 32.f) * (1.f / kD) + p.gn_eps);
+            // z = (o - mean) rstd; y = z w + b; out = y swish(og), in place over og
+            const f32x2_t rs = f2(rstd, rstd), mr = f2(-mean * rstd, -mean * rstd);
+            uint8_t *const ob = obuf(n);
+            uint8_t *row = ob + oh * kHalf + t * 128;
+#pragma unroll
+            for (int lc = 0; lc < 8; ++lc) {
+                uint4 *pp = reinterpret_cast<uint4 *>(row + ((lc ^ (t & 7)) << 4));
+                const uint4 og4 = *pp;
+                const uint32_t ogw[4] = {og4.x, og4.y, og4.z, og4.w};
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = 8 * lc + 2 * e, c = 64 * oh + idx;
+                    const uint32_t v0 = idx < 32 ? x0[idx] : x1[idx - 32], v1 = idx < 32 ? x0[idx + 1] : x1[idx - 31];
+                    const f32x2_t z = f2_fma(f2(__uint_as_float(v0), __uint_as_float(v1)), rs, mr);
+                    const f32x2_t y = f2_fma(z, *reinterpret_cast<const f32x2_t *>(gnw + c),
+                                             *reinterpret_cast<const f32x2_t *>(gnb + c));
+                    float y0, y1;
+                    f2_split(y, y0, y1);
+                    w[e] = mul_bf16x2(cvt_bf16x2(y0, y1), swish_bf16x2(ogw[e]));
+                }
+                *pp = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            named_sync<kBarOut, 128>();
+            if (lead) {
+                tma_store_3d(&p.to, ob, 0, t0, bh);
+                tma_store_3d(&p.to, ob + kHalf, 64, t0, bh);
+                bulk_commit();
+            }
+        }
+        if (lead) {
+            bulk_wait<0>();
+            // no og tile may still be landing when the CTA leaves (the last
+            // request on each of the two barriers)
+            for (int m = ogi > 2 ? ogi - 2 : 0; m < ogi; ++m)
+                if (!mbar_wait(&ogfull[m & 1], (uint32_t)(m >> 1) & 1u, wait_ns)) bad = 1;
+        }
     }
 
     // ============================================================ teardown
@@ -1095,12 +1305,12 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
 // after_scan: launched behind the segment scan as a programmatic dependent
 // launch, so that its CTAs set up and start on their first chunks while the
 // scan finishes (they wait for it before reading the carried states).
-template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false>
+template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false, bool EPI = false>
 int launch_t(const TcParams &prm, int grid, cudaStream_t s, bool after_scan) {
-    using LY = Layout<GATE, NORM, SO, OF32>;
+    using LY = Layout<GATE, NORM, SO, OF32, EPI>;
     static_assert(LY::NS >= 2 && LY::bytes <= kSmemBudget, "shared memory budget");
     static_assert(LY::colP + 64 <= kTmemCols && LY::colO1 + LY::NW <= LY::colP, "TMEM budget");
-    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO, OF32, REV>;
+    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO, OF32, REV, EPI>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes) != cudaSuccess)
         return LA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1126,8 +1336,17 @@ int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm
 
 template <bool SO>
 int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false, bool value_gate = false,
-                bool pdl = false, bool rev = false) {
+                bool pdl = false, bool rev = false, bool epi = false) {
     const bool elu1 = mode & LA_PHI_ELU1, norm = mode & LA_NORMALIZE;
+    if (epi && !SO) {
+        // the RetNet epilogue in the store: no normaliser, no gate or the head gate
+        if (norm || out_f32 || value_gate || rev || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
+        if (mode & LA_GATE_HEAD)
+            return elu1 ? launch_t<1, true, false, false, false, false, true>(prm, grid, s, pdl)
+                        : launch_t<1, false, false, false, false, false, true>(prm, grid, s, pdl);
+        return elu1 ? launch_t<0, true, false, false, false, false, true>(prm, grid, s, pdl)
+                    : launch_t<0, false, false, false, false, false, true>(prm, grid, s, pdl);
+    }
     if (rev) {
         // anti-causal: identity feature map, no normaliser, no gate or the head gate
         if (elu1 || norm || value_gate || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
@@ -1175,6 +1394,13 @@ int tc_error_take(unsigned int *value) {
         cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(unsigned int)) != cudaSuccess)
         return LA_ERR_CUDA;
     return LA_OK;
+}
+
+// The RetNet output epilogue runs in the tensor-core kernel's store for bf16
+// output without the normaliser, with no gate or the head gate (causal).
+bool chunk_tc_fuses_epilogue(const ChunkArgs &a) {
+    return !(a.mode & (LA_NORMALIZE | LA_GATE_CHANNEL)) && !a.out_f32 && !a.value_gate && !a.reverse &&
+           chunk_tc_supports(a);
 }
 
 bool chunk_tc_supports(const ChunkArgs &a) {
@@ -1226,6 +1452,13 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
         !(a.out_f32 ? make_map_f32(&prm.to, a.out, a.L, BH) : make_map(&prm.to, a.out, a.L, BH)))
         return LA_ERR_CUDA;
     if ((a.mode & LA_GATE_CHANNEL) && !make_map(&prm.tg, a.gate, a.L, BH)) return LA_ERR_CUDA;
+    const bool epi = a.gn_ogate != nullptr;
+    if (epi) {
+        if (!chunk_tc_fuses_epilogue(a) || !make_map(&prm.tog, a.gn_ogate, a.L, BH)) return LA_ERR_INTERNAL;
+        prm.gn_w = a.gn_weight;
+        prm.gn_b = a.gn_bias;
+        prm.gn_eps = a.gn_eps;
+    }
     prm.gamma = (a.mode & LA_GATE_HEAD) ? static_cast<const float *>(a.gate) : nullptr;
     prm.final_state = a.final_state;
     prm.H = a.H;
@@ -1238,7 +1471,7 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     if (stall_chunk >= 0 && prm.nseg != 1) return LA_ERR_UNSUPPORTED;  // the stall runs one launch only
     if (prm.nseg == 1) {
         prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
-        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32, a.value_gate, false, a.reverse);
+        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32, a.value_gate, false, a.reverse, epi);
         if (rc == LA_OK) *launches += 1;
         return rc;
     }
@@ -1261,7 +1494,7 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.state_in = state_in;
     prm.seg_state = nullptr;
     prm.seg_logdecay = nullptr;
-    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate, true, a.reverse);
+    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate, true, a.reverse, epi);
     if (rc == LA_OK) *launches += 1;
     return rc;
 }
