@@ -347,7 +347,11 @@ unsigned long long la_kernel_launches(void);
  * whether any kernel of this library on the current device gave up a bounded
  * wait since the last call: LA_ERR_TIMEOUT if one did (its outputs are not
  * valid; the CUDA context stays usable), LA_OK if none did, LA_ERR_CUDA if the
- * synchronisation or the read failed. Reading clears the flags. The kernels
+ * synchronisation or the read failed. Reading clears the flags. In a library
+ * built with LA_DEBUG (a test build that checks every shared-memory range, TMA
+ * coordinate, TMEM address and global index of the tensor-core forward and the
+ * decode step before using it, and skips an access that fails) it returns
+ * LA_ERR_INTERNAL when a check failed. The kernels
  * with such waits are the tensor-core chunk forward (which the tensor-core
  * backward also runs) and the chunked delta rule; every wait gives up after
  * 2 s of wall time, far beyond any legitimate one.

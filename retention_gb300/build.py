@@ -2,6 +2,12 @@
 
 One ``-gencode`` (sm_103a), every translation unit compiled in parallel, then
 linked with the static CUDA runtime; no cmake, no torch extension machinery.
+
+``build(debug=True)`` makes the bounds-checking copy
+``retention_gb300/_build_debug/libretention_gb300_debug.so`` (compiled with
+``-DLA_DEBUG``: the kernels check every shared-memory range, TMA coordinate,
+TMEM address and global index before using it and report a failed check
+through ``la_device_status``); the tests load it on demand.
 """
 import concurrent.futures as cf
 import glob
@@ -13,6 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libretention_gb300.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libretention_gb300_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -35,23 +43,27 @@ def _deps():
             glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force=False, verbose=False, extra_flags=()):
-    """Build the library if any source, header or this script is newer."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose=False, extra_flags=(), debug=False):
+    """Build the library (or, with ``debug``, its bounds-checking copy) if any
+    source, header or this script is newer."""
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if debug:
+        extra_flags = tuple(extra_flags) + ("-DLA_DEBUG",)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, "-c", src, "-o", obj] + ARCH + NVCC_FLAGS + list(extra_flags)
         if verbose:
             cmd.append("-Xptxas=-v")
@@ -67,13 +79,13 @@ def build(force=False, verbose=False, extra_flags=()):
             if err:
                 print(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp.%d" % os.getpid()
+    tmp = lib + ".tmp.%d" % os.getpid()
     cmd = [nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -278,11 +278,12 @@ int la_chunk_fwd_stall_test(const void *q, const void *k, const void *v, const v
 
 int la_device_status(la_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
-    unsigned int tc = 0, delta = 0;
-    int rc = la::tc_error_take(&tc);
-    const int rc2 = la::delta_tc_error_take(&delta);
-    if (rc == LA_OK) rc = rc2;
-    if (rc != LA_OK) return rc;
+    unsigned int tc = 0, delta = 0, dbg_tc = 0, dbg_dec = 0;
+    const int rcs[4] = {la::tc_error_take(&tc), la::delta_tc_error_take(&delta), la::tc_debug_take(&dbg_tc),
+                        la::decode_debug_take(&dbg_dec)};
+    for (int rc : rcs)
+        if (rc != LA_OK) return rc;
+    if (dbg_tc | dbg_dec) return LA_ERR_INTERNAL;  // a bounds check of an LA_DEBUG build failed
     return (tc | delta) ? LA_ERR_TIMEOUT : LA_OK;
 }
 

@@ -10,6 +10,24 @@
 
 namespace la {
 
+// ---------------------------------------------------------------- debug build
+// Built with LA_DEBUG (a separate copy of the library, for tests): every
+// shared-memory offset, TMA coordinate, TMEM column and global index the
+// checked kernels compute is compared with its extent before the access. A
+// failed check records its source line in the kernel's debug word (the first
+// one wins) and the access is skipped; nothing traps. la_device_status reports
+// a recorded failure as LA_ERR_INTERNAL. In the ordinary build a check is the
+// constant true and its condition is not evaluated.
+#ifdef LA_DEBUG
+__device__ __forceinline__ bool debug_check(unsigned int *word, bool ok, int line) {
+    if (!ok) atomicCAS(word, 0u, (unsigned int)line);
+    return ok;
+}
+#define LA_CHECK(word, cond) ::la::debug_check(&(word), (cond), __LINE__)
+#else
+#define LA_CHECK(word, cond) true
+#endif
+
 // ---------------------------------------------------------------- elements
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -97,6 +115,9 @@ int scratch_alloc(void **p, size_t bytes, cudaStream_t s);
 // read and clear the device error words of the kernels with bounded waits
 int tc_error_take(unsigned int *value);
 int delta_tc_error_take(unsigned int *value);
+// read and clear the debug words (LA_DEBUG builds: the line of a failed check)
+int tc_debug_take(unsigned int *line);
+int decode_debug_take(unsigned int *line);
 int launch_delta_tc(const DeltaArgs &a, cudaStream_t s, int *launches);
 int launch_gn_swish(const GnArgs &a, cudaStream_t s, int *launches);
 int launch_bwd(const BwdArgs &a, cudaStream_t s, int *launches);

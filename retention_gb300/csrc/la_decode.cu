@@ -27,6 +27,13 @@ constexpr int kDecThreads = 256;
 // reach 97 %.
 constexpr int kDecCtasPerSm = 3;
 
+__device__ unsigned int g_dec_debug;  // LA_DEBUG: source line of the first failed bounds check
+#ifdef LA_DEBUG
+#define DEC_CHECK(cond) LA_CHECK(g_dec_debug, cond)
+#else
+#define DEC_CHECK(cond) true
+#endif
+
 template <int DK, int DV, typename T>
 __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(DecodeArgs a) {
     constexpr int C4 = DV / 4;                  // 16-byte column groups per row
@@ -43,35 +50,38 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(Deco
     const size_t blk = (size_t)DK * DV + (norm ? DK : 0);
     float *S = a.state + (size_t)bh * blk;
     const int c4 = tid % C4, rg = tid / C4;
+    // (LA_DEBUG) this CTA's state block and token rows lie inside the arrays
+    [[maybe_unused]] const size_t nbh = (size_t)a.B * a.H;
+    const bool in = DEC_CHECK((size_t)bh < nbh && h < a.H && c4 * 4 + 3 < DV && rg < RG);
 
     // all state loads first: RPT independent 16-byte loads per thread
     float4 s[RPT];
 #pragma unroll
     for (int r = 0; r < RPT; ++r) {
         const int row = rg + r * RG;
-        if (row < DK) s[r] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)row * DV) + c4);
+        if (row < DK && in) s[r] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)row * DV) + c4);
     }
 
     const T *q = (const T *)a.q + (size_t)bh * DK;
     const T *k = (const T *)a.k + (size_t)bh * DK;
     const T *v = (const T *)a.v + (size_t)bh * DV;
-    const float gamma = ghead ? ((const float *)a.gate)[h] : 1.f;
-    for (int d = tid; d < DK; d += kDecThreads) {
+    const float gamma = ghead && in ? ((const float *)a.gate)[h] : 1.f;
+    for (int d = tid; d < DK && in; d += kDecThreads) {
         qf[d] = phi(to_f32(q[d]), elu1);
         kf[d] = phi(to_f32(k[d]), elu1);
         float aa = gamma;
         if (gchan) aa = expf(channel_log_decay(to_f32(((const T *)a.gate)[(size_t)bh * DK + d])));
         ad[d] = aa;
     }
-    const float v0 = to_f32(v[c4 * 4 + 0]), v1 = to_f32(v[c4 * 4 + 1]);
-    const float v2 = to_f32(v[c4 * 4 + 2]), v3 = to_f32(v[c4 * 4 + 3]);
+    const float v0 = in ? to_f32(v[c4 * 4 + 0]) : 0.f, v1 = in ? to_f32(v[c4 * 4 + 1]) : 0.f;
+    const float v2 = in ? to_f32(v[c4 * 4 + 2]) : 0.f, v3 = in ? to_f32(v[c4 * 4 + 3]) : 0.f;
     __syncthreads();
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < RPT; ++r) {
         const int row = rg + r * RG;
-        if (row < DK) {
+        if (row < DK && in) {
             const float aa = ad[row], kk = kf[row], qq = qf[row];
             float4 x = s[r];
             x.x = aa * x.x + kk * v0;
@@ -87,7 +97,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(Deco
     }
     red[rg][c4] = acc;
 
-    if (norm && tid < 32) {
+    if (norm && tid < 32 && in) {
         float part = 0.f;
         float *z = S + (size_t)DK * DV;
         for (int d = tid; d < DK; d += 32) {
@@ -110,7 +120,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm) decode_kernel(Deco
             sum += comp == 0 ? p.x : comp == 1 ? p.y : comp == 2 ? p.z : p.w;
         }
         if (norm) sum = sum / den_s;
-        ((T *)a.out)[(size_t)bh * DV + tid] = from_f32<T>(sum);
+        if (in) ((T *)a.out)[(size_t)bh * DV + tid] = from_f32<T>(sum);
     }
 }
 
@@ -133,6 +143,16 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t s) {
 }
 
 }  // namespace
+
+// The decode kernel's debug word (LA_DEBUG builds: the source line of the
+// first failed bounds check; always 0 otherwise), read and cleared.
+int decode_debug_take(unsigned int *line) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(line, g_dec_debug, sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_dec_debug, &zero, sizeof(unsigned int)) != cudaSuccess)
+        return LA_ERR_CUDA;
+    return LA_OK;
+}
 
 int launch_decode(const DecodeArgs &a, cudaStream_t s, int *launches) {
     cudaError_t e = (a.mode & LA_DTYPE_F32) ? launch_t<float>(a, s) : launch_t<__nv_bfloat16>(a, s);

@@ -73,6 +73,12 @@ constexpr int kBarPro = 1, kBarState = 2, kBarOut = 3, kBarP = 4;  // named barr
 constexpr int kWarpProducer = 2, kWarpMma = 3;
 
 __device__ unsigned int g_tc_error;
+__device__ unsigned int g_tc_debug;  // LA_DEBUG: source line of the first failed bounds check
+#ifdef LA_DEBUG
+#define TC_CHECK(cond) LA_CHECK(g_tc_debug, cond)
+#else
+#define TC_CHECK(cond) true
+#endif
 
 struct TcParams {
     CUtensorMap tq, tk, tv, tg, to;
@@ -88,6 +94,8 @@ struct TcParams {
     int init0;               // segment 0 starts from state_in too (a given initial state)
     uint64_t wait_ns;        // limit of every bounded wait (kWaitNs)
     int stall_chunk;         // diagnostics: the producer stops before this chunk (-1: never)
+    // extents (floats) of the global arrays, for the bounds checks of LA_DEBUG builds
+    size_t n_final, n_state_in, n_seg_state, n_seg_logdecay;
 };
 
 constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
@@ -342,6 +350,28 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::Misc);
     uint8_t *sP = sm + LY::P, *sS = sm + LY::S, *sO = sm + LY::O;
 
+    // Checked accesses: in an LA_DEBUG build every shared-memory range, TMA
+    // coordinate, TMEM address and global index below is compared with its
+    // extent first, and a failed check skips the access (and records its line);
+    // in the ordinary build each check is the constant true.
+    [[maybe_unused]] const uint32_t sm_lo = smem_u32(sm), sm_hi = smem_u32(smem_raw) + LY::bytes;
+    [[maybe_unused]] const int nbh_grid = (int)gridDim.x / p.nseg;
+    auto sok = [&](const void *ptr, uint32_t n) {
+        return TC_CHECK(smem_u32(ptr) >= sm_lo && smem_u32(ptr) + n <= sm_hi);
+    };
+    auto gok = [&](size_t i, size_t n) { return TC_CHECK(i < n); };
+    // a [64 x 64] bf16 box (or [64 x 32] fp32): inner coordinate on a 16-byte boundary
+    auto tma_in = [&](const void *s_ptr, int x, int y) {
+        return TC_CHECK(smem_u32(s_ptr) >= sm_lo && smem_u32(s_ptr) + kHalf <= sm_hi && x >= 0 && x < kD &&
+                        (x & 7) == 0 && y >= 0 && y < L && bh < nbh_grid);
+    };
+    auto tload = [&](void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+        if (tma_in(dst, x, y)) tma_load_3d(dst, map, bar, x, y, bh);
+    };
+    auto tstore = [&](const CUtensorMap *map, const void *src, int x, int y) {
+        if (tma_in(src, x, y)) tma_store_3d(map, src, x, y, bh);
+    };
+
     if (warp == kWarpMma) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -390,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             const int s = i >> 9, r = (i >> 3) & 63, pc = i & 7;
             const uint32_t one = (((pc ^ r) & 7) == 0) ? 0x3f80u : 0u;  // bf16 1.0 in element 0
             const uint32_t base = SO ? s * LY::so_stage + 2 * kTile : LY::T * kHalf;
-            *reinterpret_cast<uint4 *>(sm + base + r * 128 + pc * 16) = make_uint4(one, 0u, 0u, 0u);
+            uint8_t *pw16 = sm + base + r * 128 + pc * 16;
+            if (sok(pw16, 16)) *reinterpret_cast<uint4 *>(pw16) = make_uint4(one, 0u, 0u, 0u);
         }
         if (!SO)
             for (int i = tid; i < 1024; i += kThreads)
@@ -403,6 +434,37 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int bad = 0;
+    // TMEM: a warp reaches its own lane quarter only, columns inside the allocation
+    auto tok = [&](uint32_t ta, uint32_t ncols) {
+        return TC_CHECK((ta >> 16) == (uint32_t)((warp & 3) * 32) && (ta & 0xFFFFu) >= (tmem & 0xFFFFu) &&
+                        (ta & 0xFFFFu) + ncols <= (tmem & 0xFFFFu) + kTmemCols);
+    };
+    auto tld32 = [&](uint32_t ta, uint32_t(&r)[32]) {
+        if (tok(ta, 32)) tmem_ld32(ta, r);
+    };
+    auto tst32 = [&](uint32_t ta, const uint32_t(&r)[32]) {
+        if (tok(ta, 32)) tmem_st32(ta, r);
+    };
+    auto tld8 = [&](uint32_t ta, uint32_t(&r)[8]) {
+        if (tok(ta, 8)) tmem_ld8(ta, r);
+    };
+    auto tld1 = [&](uint32_t ta, uint32_t &r) {
+        if (tok(ta, 1)) tmem_ld1(ta, r);
+    };
+    auto tst1 = [&](uint32_t ta, uint32_t r) {
+        if (tok(ta, 1)) tmem_st1(ta, r);
+    };
+    // shared-memory words at computed offsets (a skipped load reads zero)
+    auto ld4 = [&](const uint8_t *ptr) { return sok(ptr, 4) ? *reinterpret_cast<const uint32_t *>(ptr) : 0u; };
+    auto st4 = [&](uint8_t *ptr, uint32_t v) {
+        if (sok(ptr, 4)) *reinterpret_cast<uint32_t *>(ptr) = v;
+    };
+    auto ld16 = [&](const uint8_t *ptr) {
+        return sok(ptr, 16) ? *reinterpret_cast<const uint4 *>(ptr) : make_uint4(0u, 0u, 0u, 0u);
+    };
+    auto st16 = [&](uint8_t *ptr, uint4 v) {
+        if (sok(ptr, 16)) *reinterpret_cast<uint4 *>(ptr) = v;
+    };
 
     if (warp == kWarpProducer) {
         // ============================================================ TMA producer
@@ -424,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     }
                     uint8_t *dst = sm + LY::Gring + sg * kTile;
                     mbar_arrive_expect_tx(&gfull[sg], kTile);
-                    tma_load_3d(dst, &p.tg, &gfull[sg], 0, t0, bh);
-                    tma_load_3d(dst + kHalf, &p.tg, &gfull[sg], 64, t0, bh);
+                    tload(dst, &p.tg, &gfull[sg], 0, t0);
+                    tload(dst + kHalf, &p.tg, &gfull[sg], 64, t0);
                     gissued = n + 1;
                 }
                 if (n >= NS && !mbar_wait(&empty[s], (uint32_t)(n / NS - 1) & 1u, wait_ns)) {
@@ -436,8 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll 1
                 for (int tl = SO ? 1 : 0; tl < ntl; ++tl) {
                     const CUtensorMap *m = tl == 0 ? &p.tq : tl == 1 ? &p.tk : tl == 2 ? &p.tv : &p.tg;
-                    tma_load_3d(sm + tile_half(tl, s, 0), m, &full[s], 0, t0, bh);
-                    tma_load_3d(sm + tile_half(tl, s, 1), m, &full[s], 64, t0, bh);
+                    tload(sm + tile_half(tl, s, 0), m, &full[s], 0, t0);
+                    tload(sm + tile_half(tl, s, 1), m, &full[s], 64, t0);
                 }
                 issued = n + 1;
             }
@@ -468,7 +530,13 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 const uint32_t v0 = tile_half(2, n % NS, 0), v1 = tile_half(2, n % NS, 1);
                 return sdesc_sw128(sm0 + v0, v1 - v0, 1024);
             };
+            // operand ranges (LA_DEBUG): an M = 128 A operand reads 16 KiB from its
+            // start, a 64-row operand (or N atom) 8 KiB
+            auto opok = [&](uint32_t off, uint32_t span) { return sok(sm + off, span); };
             auto issue_qk = [&](int n) {
+                if (!(opok(tile_half(0, n % NS, 0), 16384) && opok(tile_half(0, n % NS, 1), 16384) &&
+                      opok(tile_half(1, n % NS, 0), 8192) && opok(tile_half(1, n % NS, 1), 8192)))
+                    return;
                 const uint64_t a0 = sdesc_sw128(sm0 + tile_half(0, n % NS, 0), 16, 1024);
                 const uint64_t a1 = sdesc_sw128(sm0 + tile_half(0, n % NS, 1), 16, 1024);
                 const uint64_t b0 = sdesc_sw128(sm0 + tile_half(1, n % NS, 0), 16, 1024);
@@ -490,9 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     }
                     tc_fence_after();
                     const uint64_t ak = dkm(n), bv = dvm(n);
+                    if (opok(tile_half(1, s, 0), 8192) && opok(tile_half(1, s, 1), 8192) && opok(tile_half(2, s, 0), 8192) &&
+                        opok(tile_half(2, s, 1), 8192)) {
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        umma_bf16(tmem + LY::colS, ak + ks * 128, bv + ks * 128, id_s, (n > 0 || ks > 0));
+                        for (int ks = 0; ks < 4; ++ks)
+                            umma_bf16(tmem + LY::colS, ak + ks * 128, bv + ks * 128, id_s, (n > 0 || ks > 0));
+                    }
                     umma_commit(sdone);
                     umma_commit(&empty[s]);
                 }
@@ -507,6 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 const uint64_t aq0 = sdesc_sw128(sm0 + tile_half(0, s, 0), 16, 1024);
                 const uint64_t aq1 = sdesc_sw128(sm0 + tile_half(0, s, 1), 16, 1024);
                 const uint64_t ak = dkm(n), bv = dvm(n);
+                if (!(opok(tile_half(0, s, 0), 16384) && opok(tile_half(0, s, 1), 16384) && opok(tile_half(1, s, 0), 8192) &&
+                      opok(tile_half(1, s, 1), 8192) && opok(tile_half(2, s, 0), 8192) && opok(tile_half(2, s, 1), 8192) &&
+                      opok(LY::P, 16384) && opok(LY::S, NORM ? 49152 : 32768))) {
+                    bad = 1;
+                    break;
+                }
                 if ((n > 0 || init) && !mbar_wait(sready, (uint32_t)(n - 1 + (init ? 1 : 0)) & 1u, wait_ns)) {
                     bad = 1;
                     break;
@@ -610,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 f32x2_t la[16], sq = f2(0.f, 0.f);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const uint32_t w = 16 * qr + u < c ? *reinterpret_cast<const uint32_t *>(sG + offw(u)) : 0x7F7F7F7Fu;
+                    const uint32_t w = 16 * qr + u < c ? ld4(sG + offw(u)) : 0x7F7F7F7Fu;
                     la[u] = log2_alpha2(w);
                     sq = f2_add(sq, la[u]);
                 }
@@ -624,8 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 if (ok) {
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        kw[u] = *reinterpret_cast<const uint32_t *>(sK + offw(u));
-                        if (!SO && GATE == 2) qw[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(u));
+                        kw[u] = ld4(sK + offw(u));
+                        if (!SO && GATE == 2) qw[u] = ld4(sQ + offw(u));
                     }
                 }
                 if (named_sync_or<kBarPro, 256>(!ok)) {
@@ -648,8 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     if (g8 == 0) {
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
-                            kn[u] = *reinterpret_cast<const uint32_t *>(sK + offw(8 + u));
-                            if (!SO && GATE == 2) qn[u] = *reinterpret_cast<const uint32_t *>(sQ + offw(8 + u));
+                            kn[u] = ld4(sK + offw(8 + u));
+                            if (!SO && GATE == 2) qn[u] = ld4(sQ + offw(8 + u));
                         }
                     }
                     uint32_t ko[8], qo[8];
@@ -674,8 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     }
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        *reinterpret_cast<uint32_t *>(sK + offw(8 * g8 + u)) = ko[u];
-                        if (!SO && GATE == 2) *reinterpret_cast<uint32_t *>(sQ + offw(8 * g8 + u)) = qo[u];
+                        st4(sK + offw(8 * g8 + u), ko[u]);
+                        if (!SO && GATE == 2) st4(sQ + offw(8 * g8 + u), qo[u]);
                         kw[u] = kn[u];
                         if (!SO && GATE == 2) qw[u] = qn[u];
                         la[u] = la[u + 8];
@@ -695,8 +772,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             if (!bad && qr == 3) {
                 *reinterpret_cast<float2 *>(ffinal + cw) = make_float2(ex2f(bl0), ex2f(bl1));
                 if (SO)
-                    *reinterpret_cast<float2 *>(p.seg_logdecay + (size_t)blockIdx.x * kD + cw) =
-                        make_float2(bt0 * kLn2, bt1 * kLn2);
+                    if (gok((size_t)blockIdx.x * kD + cw + 1, p.n_seg_logdecay))
+                        *reinterpret_cast<float2 *>(p.seg_logdecay + (size_t)blockIdx.x * kD + cw) =
+                            make_float2(bt0 * kLn2, bt1 * kLn2);
                 mbar_arrive(profinal);
             }
         } else {
@@ -705,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // row: no bank conflicts). Threads pd < 128 also own key channel pd for
             // the decay factors.
             const int pd = 32 * pw + lane;
-            const float lg = GATE == 1 ? __logf(p.gamma[h]) : 0.f;
+            const float lg = GATE == 1 && gok(h, p.H) ? __logf(p.gamma[h]) : 0.f;
             // Retention applies the state's decay once per window of R chunks instead
             // of every chunk: m chunks into a window the accumulator holds
             // S / gamma^(64 m), so q rows take an extra gamma^(64 m) and k rows
@@ -755,8 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         uint4 w[NJ];
 #pragma unroll
                         for (int j = 0; j < NJ; ++j)
-                            w[j] = *reinterpret_cast<const uint4 *>(((pd + PT * j) >> 9 ? blk1 : blk0) +
-                                                                    (((pd + PT * j) >> 3) & 63) * 128 + (pd & 7) * 16);
+                            w[j] = ld16(((pd + PT * j) >> 9 ? blk1 : blk0) + (((pd + PT * j) >> 3) & 63) * 128 + (pd & 7) * 16);
 #pragma unroll
                         for (int j = 0; j < NJ; ++j) {
                             const int row = ((pd + PT * j) >> 3) & 63;
@@ -778,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                                 }
                                 x = make_uint4(u[0], u[1], u[2], u[3]);
                             }
-                            *reinterpret_cast<uint4 *>(((pd + PT * j) >> 9 ? blk1 : blk0) + row * 128 + (pd & 7) * 16) = x;
+                            st16(((pd + PT * j) >> 9 ? blk1 : blk0) + row * 128 + (pd & 7) * 16, x);
                         }
                     }
                 }
@@ -797,7 +874,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             if (!bad && pd < 128) {
                 ffinal[pd] = GATE == 0 ? 1.f : __expf(b_last + (GATE == 1 ? (float)(kC * m) * lg : 0.f));
-                if (SO) p.seg_logdecay[(size_t)blockIdx.x * kD + pd] = b_total;
+                if (SO && gok((size_t)blockIdx.x * kD + pd, p.n_seg_logdecay))
+                    p.seg_logdecay[(size_t)blockIdx.x * kD + pd] = b_total;
                 mbar_arrive(profinal);
             }
         }
@@ -811,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
                 uint32_t r[32];
-                tmem_ld32(tS + 32 * j, r);
+                tld32(tS + 32 * j, r);
                 tmem_ld_wait();
                 uint8_t *row = sS + (j >> 1) * 16384 + i * 128;
 #pragma unroll
@@ -822,15 +900,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     w.y = pack_bf16(__uint_as_float(r[8 * q4 + 2]), __uint_as_float(r[8 * q4 + 3]));
                     w.z = pack_bf16(__uint_as_float(r[8 * q4 + 4]), __uint_as_float(r[8 * q4 + 5]));
                     w.w = pack_bf16(__uint_as_float(r[8 * q4 + 6]), __uint_as_float(r[8 * q4 + 7]));
-                    *reinterpret_cast<uint4 *>(row + ((lc ^ (i & 7)) << 4)) = w;
+                    st16(row + ((lc ^ (i & 7)) << 4), w);
                 }
             }
             if (NORM) {
                 uint32_t z;
-                tmem_ld1(tS + 128, z);
+                tld1(tS + 128, z);
                 tmem_ld_wait();
-                *reinterpret_cast<uint4 *>(sS + 32768 + i * 128 + ((i & 7) << 4)) =
-                    make_uint4(pack_bf16(__uint_as_float(z), 0.f), 0u, 0u, 0u);
+                st16(sS + 32768 + i * 128 + ((i & 7) << 4), make_uint4(pack_bf16(__uint_as_float(z), 0.f), 0u, 0u, 0u));
             }
         };
         if (init) {
@@ -840,20 +917,22 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // before reading what it wrote (a no-op for an ordinary launch).
             griddep_wait();
             const float *src = p.state_in + segblk + (size_t)i * kD;
+            if (!gok(segblk + (size_t)i * kD + kD - 1, p.n_state_in)) src = nullptr;
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
                 uint32_t r[32];
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
-                    const float4 v4 = reinterpret_cast<const float4 *>(src + 32 * j)[q4];
+                    const float4 v4 = src ? reinterpret_cast<const float4 *>(src + 32 * j)[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
                     r[4 * q4] = __float_as_uint(v4.x);
                     r[4 * q4 + 1] = __float_as_uint(v4.y);
                     r[4 * q4 + 2] = __float_as_uint(v4.z);
                     r[4 * q4 + 3] = __float_as_uint(v4.w);
                 }
-                tmem_st32(tS + 32 * j, r);
+                tst32(tS + 32 * j, r);
             }
-            if (NORM) tmem_st1(tS + 128, __float_as_uint(p.state_in[segblk + (size_t)kD * kD + i]));
+            if (NORM && gok(segblk + (size_t)kD * kD + i, p.n_state_in))
+                tst1(tS + 128, __float_as_uint(p.state_in[segblk + (size_t)kD * kD + i]));
             tmem_st_wait();
             write_copy();
             fence_proxy_async_smem();
@@ -878,18 +957,18 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll 1
                 for (int j = 0; j < 4; ++j) {
                     uint32_t r[32];
-                    tmem_ld32(tS + 32 * j, r);
+                    tld32(tS + 32 * j, r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         r[e] = __float_as_uint(__uint_as_float(r[e]) * (GATE == 3 ? fcol[32 * j + e] : f));
-                    tmem_st32(tS + 32 * j, r);
+                    tst32(tS + 32 * j, r);
                 }
                 if (NORM) {
                     uint32_t z;
-                    tmem_ld1(tS + 128, z);
+                    tld1(tS + 128, z);
                     tmem_ld_wait();
-                    tmem_st1(tS + 128, __float_as_uint(__uint_as_float(z) * f));
+                    tst1(tS + 128, __float_as_uint(__uint_as_float(z) * f));
                 }
                 tmem_st_wait();
             }
@@ -908,6 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         }
         float *dst = SO ? p.seg_state + segblk : (p.nseg == 1 ? p.final_state : nullptr);
         if (!SO && dst) dst += (size_t)bh * blk;
+        if (dst && !gok((SO ? segblk : (size_t)bh * blk) + blk - 1, SO ? p.n_seg_state : p.n_final)) dst = nullptr;
         if (!bad && N > 0) {
             bool ok = mbar_wait(sdone, (uint32_t)(N - 1) & 1u, wait_ns) && mbar_wait(profinal, 0u, wait_ns);
             if (named_sync_or<kBarState, 128>(!ok)) {
@@ -921,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll 1
                 for (int j = 0; j < 4; ++j) {
                     uint32_t r[32];
-                    tmem_ld32(tS + 32 * j, r);
+                    tld32(tS + 32 * j, r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4) {
@@ -935,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
                 if (NORM) {
                     uint32_t z;
-                    tmem_ld1(tS + 128, z);
+                    tld1(tS + 128, z);
                     tmem_ld_wait();
                     dst[(size_t)kD * kD + i] = __uint_as_float(z) * ff;
                 }
@@ -964,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll 1
                     for (int q8 = 0; q8 < 8; ++q8) {
                         uint32_t a[8];
-                        tmem_ld8(tmem + lane_base + LY::colP + 8 * q8, a);
+                        tld8(tmem + lane_base + LY::colP + 8 * q8, a);
                         tmem_ld_wait();
                         uint32_t u[4];
 #pragma unroll
@@ -973,14 +1053,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                             u[e] = pack_bf16(jj <= t ? __uint_as_float(a[2 * e]) : 0.f,
                                              jj + 1 <= t ? __uint_as_float(a[2 * e + 1]) : 0.f);
                         }
-                        *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+                        st16(prow + (((q8 ^ t) & 7) << 4), make_uint4(u[0], u[1], u[2], u[3]));
                     }
                     tc_fence_before();
                     mbar_arrive(pempty);
                 } else {
                     uint32_t r0[32], r1[32];
-                    tmem_ld32(tmem + lane_base + LY::colP, r0);
-                    tmem_ld32(tmem + lane_base + LY::colP + 32, r1);
+                    tld32(tmem + lane_base + LY::colP, r0);
+                    tld32(tmem + lane_base + LY::colP + 32, r1);
                     tmem_ld_wait();
                     tc_fence_before();
                     mbar_arrive(pempty);
@@ -994,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                             const uint32_t a1 = q8 < 4 ? r0[jj + 1] : r1[jj - 31];
                             u[e] = pack_bf16(keep(jj) ? __uint_as_float(a0) : 0.f, keep(jj + 1) ? __uint_as_float(a1) : 0.f);
                         }
-                        *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+                        st16(prow + (((q8 ^ t) & 7) << 4), make_uint4(u[0], u[1], u[2], u[3]));
                     }
                 }
             }
@@ -1012,23 +1092,23 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             float rden = 1.f;
             if (NORM) {
                 uint32_t dd;
-                tmem_ld1(tO + 128, dd);
+                tld1(tO + 128, dd);
                 tmem_ld_wait();
                 rden = 1.f / __uint_as_float(dd);
             }
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
                 uint32_t r[32];
-                tmem_ld32(tO + 32 * j, r);
+                tld32(tO + 32 * j, r);
                 tmem_ld_wait();
                 if constexpr (OF32) {
                     // staging: four [64 x 32] fp32 quarters with the 128-byte swizzle (box 32 x 64)
                     uint8_t *row = sO + j * 8192 + t * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(row + ((c ^ (t & 7)) << 4)) = make_uint4(
+                        st16(row + ((c ^ (t & 7)) << 4), make_uint4(
                             __float_as_uint(__uint_as_float(r[4 * c]) * rden), __float_as_uint(__uint_as_float(r[4 * c + 1]) * rden),
-                            __float_as_uint(__uint_as_float(r[4 * c + 2]) * rden), __float_as_uint(__uint_as_float(r[4 * c + 3]) * rden));
+                            __float_as_uint(__uint_as_float(r[4 * c + 2]) * rden), __float_as_uint(__uint_as_float(r[4 * c + 3]) * rden)));
                 } else {
                     // staging: two [64 x 64] halves with the 128-byte swizzle (TMA store box 64 x 64)
                     uint8_t *row = sO + (j >> 1) * 8192 + t * 128;
@@ -1040,7 +1120,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         w.y = pack_bf16(__uint_as_float(r[8 * q4 + 2]) * rden, __uint_as_float(r[8 * q4 + 3]) * rden);
                         w.z = pack_bf16(__uint_as_float(r[8 * q4 + 4]) * rden, __uint_as_float(r[8 * q4 + 5]) * rden);
                         w.w = pack_bf16(__uint_as_float(r[8 * q4 + 6]) * rden, __uint_as_float(r[8 * q4 + 7]) * rden);
-                        *reinterpret_cast<uint4 *>(row + ((lc ^ (t & 7)) << 4)) = w;
+                        st16(row + ((lc ^ (t & 7)) << 4), w);
                     }
                 }
             }
@@ -1051,10 +1131,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             if (t == 0) {
                 if constexpr (OF32) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) tma_store_3d(&p.to, sO + j * 8192, 32 * j, t0, bh);
+                    for (int j = 0; j < 4; ++j) tstore(&p.to, sO + j * 8192, 32 * j, t0);
                 } else {
-                    tma_store_3d(&p.to, sO, 0, t0, bh);
-                    tma_store_3d(&p.to, sO + 8192, 64, t0, bh);
+                    tstore(&p.to, sO, 0, t0);
+                    tstore(&p.to, sO + 8192, 64, t0);
                 }
                 bulk_commit();
             }
@@ -1078,8 +1158,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             tc_fence_after();
             uint8_t *prow = sP + t * 128;
             uint32_t r0[32], r1[32];
-            tmem_ld32(tmem + lane_base + LY::colP, r0);
-            tmem_ld32(tmem + lane_base + LY::colP + 32, r1);
+            tld32(tmem + lane_base + LY::colP, r0);
+            tld32(tmem + lane_base + LY::colP + 32, r1);
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(pempty);
@@ -1093,7 +1173,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     const uint32_t a1 = q8 < 4 ? r0[jj + 1] : r1[jj - 31];
                     u[e] = pack_bf16(keep(jj) ? __uint_as_float(a0) : 0.f, keep(jj + 1) ? __uint_as_float(a1) : 0.f);
                 }
-                *reinterpret_cast<uint4 *>(prow + (((q8 ^ t) & 7) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+                st16(prow + (((q8 ^ t) & 7) << 4), make_uint4(u[0], u[1], u[2], u[3]));
             }
             fence_proxy_async_smem();
             mbar_arrive(pfull);
@@ -1112,8 +1192,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         float *part = gnb + kD;  // [2][64] (m, M2) of each half row
         {
             const int col = 64 * oh + t;
-            gnw[col] = p.gn_w ? p.gn_w[(size_t)h * kD + col] : 1.f;
-            gnb[col] = p.gn_b ? p.gn_b[(size_t)h * kD + col] : 0.f;
+            const bool hin = gok(h, p.H);
+            gnw[col] = p.gn_w && hin ? p.gn_w[(size_t)h * kD + col] : 1.f;
+            gnb[col] = p.gn_b && hin ? p.gn_b[(size_t)h * kD + col] : 0.f;
         }
         named_sync<kBarOut, 128>();
         // staging buffer of chunk m, and the request of its og tile
@@ -1121,8 +1202,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         auto og_load = [&](int m) {
             uint8_t *dst = obuf(m);
             mbar_arrive_expect_tx(&ogfull[m & 1], kTile);
-            tma_load_3d(dst, &p.tog, &ogfull[m & 1], 0, chunk_t0(m), bh);
-            tma_load_3d(dst + kHalf, &p.tog, &ogfull[m & 1], 64, chunk_t0(m), bh);
+            tload(dst, &p.tog, &ogfull[m & 1], 0, chunk_t0(m));
+            tload(dst + kHalf, &p.tog, &ogfull[m & 1], 64, chunk_t0(m));
         };
         int ogi = 0;  // (lead) og tiles requested
         if (lead && N > 0) og_load(ogi++);
@@ -1145,8 +1226,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             uint32_t x0[32], x1[32];
             {
                 const uint32_t tO = tmem + lane_base + (b ? LY::colO1 : LY::colO0) + 64 * oh;
-                tmem_ld32(tO, x0);
-                tmem_ld32(tO + 32, x1);
+                tld32(tO, x0);
+                tld32(tO + 32, x1);
                 tmem_ld_wait();
             }
             tc_fence_before();
@@ -1184,8 +1265,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             uint8_t *row = ob + oh * kHalf + t * 128;
 #pragma unroll
             for (int lc = 0; lc < 8; ++lc) {
-                uint4 *pp = reinterpret_cast<uint4 *>(row + ((lc ^ (t & 7)) << 4));
-                const uint4 og4 = *pp;
+                uint8_t *pp = row + ((lc ^ (t & 7)) << 4);
+                const uint4 og4 = ld16(pp);
                 const uint32_t ogw[4] = {og4.x, og4.y, og4.z, og4.w};
                 uint32_t w[4];
 #pragma unroll
@@ -1199,13 +1280,13 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     f2_split(y, y0, y1);
                     w[e] = mul_bf16x2(cvt_bf16x2(y0, y1), swish_bf16x2(ogw[e]));
                 }
-                *pp = make_uint4(w[0], w[1], w[2], w[3]);
+                st16(pp, make_uint4(w[0], w[1], w[2], w[3]));
             }
             fence_proxy_async_smem();
             named_sync<kBarOut, 128>();
             if (lead) {
-                tma_store_3d(&p.to, ob, 0, t0, bh);
-                tma_store_3d(&p.to, ob + kHalf, 64, t0, bh);
+                tstore(&p.to, ob, 0, t0);
+                tstore(&p.to, ob + kHalf, 64, t0);
                 bulk_commit();
             }
         }
@@ -1403,6 +1484,16 @@ bool chunk_tc_fuses_epilogue(const ChunkArgs &a) {
            chunk_tc_supports(a);
 }
 
+// The debug word of the tensor-core forward (LA_DEBUG builds: the source line
+// of the first failed bounds check; always 0 otherwise), read and cleared.
+int tc_debug_take(unsigned int *line) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(line, g_tc_debug, sizeof(unsigned int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_tc_debug, &zero, sizeof(unsigned int)) != cudaSuccess)
+        return LA_ERR_CUDA;
+    return LA_OK;
+}
+
 bool chunk_tc_supports(const ChunkArgs &a) {
     if ((a.mode & LA_DTYPE_F32) || a.dk != kD || a.dv != kD || a.chunk != kC || a.L < 1) return false;
     int dev = 0, major = 0;
@@ -1468,6 +1559,9 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.init0 = a.initial_state != nullptr;
     prm.wait_ns = wait_ns;
     prm.stall_chunk = stall_chunk;
+    const size_t blkf = (size_t)kD * kD + ((a.mode & LA_NORMALIZE) ? kD : 0);
+    prm.n_final = a.final_state ? (size_t)BH * blkf : 0;
+    prm.n_state_in = a.initial_state ? (size_t)BH * blkf : 0;  // (split: the carried states, below)
     if (stall_chunk >= 0 && prm.nseg != 1) return LA_ERR_UNSUPPORTED;  // the stall runs one launch only
     if (prm.nseg == 1) {
         prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
@@ -1483,7 +1577,10 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     float *seg_logdecay = state_in + nsb * blk;
     prm.seg_state = seg_state;
     prm.seg_logdecay = seg_logdecay;
+    prm.n_seg_state = nsb * blk;
+    prm.n_seg_logdecay = nsb * kD;
     prm.final_state = nullptr;
+    prm.n_final = 0;
     int rc = launch_mode<true>(prm, (int)nsb, s, a.mode, false, a.value_gate, false, a.reverse);
     if (rc != LA_OK) return rc;
     *launches += 1;
@@ -1492,8 +1589,10 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     *launches += 1;
     prm.state_in = state_in;
+    prm.n_state_in = nsb * blk;
     prm.seg_state = nullptr;
     prm.seg_logdecay = nullptr;
+    prm.n_seg_state = prm.n_seg_logdecay = 0;
     rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate, true, a.reverse, epi);
     if (rc == LA_OK) *launches += 1;
     return rc;

@@ -4,6 +4,7 @@ step of the computation runs in the CUDA library; if the library has not been
 built, or there is no CUDA device, the calls raise instead of computing
 anything another way.
 """
+import contextlib
 import ctypes
 import os
 
@@ -58,20 +59,36 @@ def library_path():
     return _build.LIB
 
 
+def _open(path):
+    if not os.path.exists(path):
+        raise RuntimeError("the CUDA library %s is not built; run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
 def load():
     """Load the built library (building it is ``__graft_entry__.build()``)."""
     global _lib
     if _lib is None:
-        path = _build.LIB
-        if not os.path.exists(path):
-            raise RuntimeError("the CUDA library %s is not built; run __graft_entry__.build()" % path)
-        lib = ctypes.CDLL(path)
-        for name, (args, res) in SIGNATURES.items():
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = res
-        _lib = lib
+        _lib = _open(_build.LIB)
     return _lib
+
+
+@contextlib.contextmanager
+def library(path):
+    """Route every call of this module to the library at ``path`` (e.g. the
+    bounds-checking build ``build.LIB_DEBUG``) inside the ``with`` block."""
+    global _lib
+    saved = load()
+    _lib = _open(path)
+    try:
+        yield _lib
+    finally:
+        _lib = saved
 
 
 def mode_bits(phi="elu1", normalize=False, gate=None, dtype=torch.bfloat16, simt=False, reverse=False):
