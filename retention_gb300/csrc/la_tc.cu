@@ -850,8 +850,18 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                                     // (with REV the local index is c - 1 - row; rows past the
                                     // end hold zeros and take any factor)
                                     const float fr = fr_arr[REV ? ((c - 1 - row) & (kC - 1)) : row] * (isk ? gk : gq);
+                                    if constexpr (OF32) {
+                                        // the fp32-output instances serve differences of nearly
+                                        // equal terms: one rounding of the exact product
 #pragma unroll
-                                    for (int e = 0; e < 4; ++e) u[e] = pack_bf16(bf16lo(u[e]) * fr, bf16hi(u[e]) * fr);
+                                        for (int e = 0; e < 4; ++e) u[e] = pack_bf16(bf16lo(u[e]) * fr, bf16hi(u[e]) * fr);
+                                    } else {
+                                        // the factor rounded to bf16 once, applied to two values
+                                        // by one packed multiply
+                                        const uint32_t fr2 = pack_bf16(fr, fr);
+#pragma unroll
+                                        for (int e = 0; e < 4; ++e) u[e] = mul_bf16x2(u[e], fr2);
+                                    }
                                 }
                                 x = make_uint4(u[0], u[1], u[2], u[3]);
                             }
