@@ -107,11 +107,14 @@ typedef enum {
  * segments and takes stream-ordered scratch (cudaMallocAsync / cudaFreeAsync
  * on `stream`) for the per-segment states; a failed allocation returns
  * LA_ERR_CUDA. All stream-ordered scratch of this library comes from a memory
- * pool of its own, created on a device the first time it allocates there
- * (cudaMemPoolCreate), whose release threshold keeps freed scratch mapped for
- * the next call instead of unmapping it at every synchronisation: that pool
- * holds up to the largest scratch any call used until the process exits. The
- * device's default memory pool is neither used nor changed.
+ * pool of its own, created on a device (in each context, found by its unique
+ * id, so a context made again after cudaDeviceReset gets a new pool) the first
+ * time the library allocates there (cudaMemPoolCreate); its release threshold
+ * keeps freed scratch mapped for the next call instead of unmapping it at every
+ * synchronisation, so the pool holds up to the largest scratch any call used
+ * until its context ends. The device's default memory pool is neither used nor
+ * changed. The first call that takes scratch in a context creates the pool and
+ * should come before any stream capture.
  * la_chunk_fwd_noalloc is the same call without any allocation.
  * A split call issues three kernels on `stream`: the segment end states, a
  * scan over them, and the full pass. The full pass goes out as a programmatic

@@ -3,6 +3,7 @@
 // library's own stream-ordered pool, and the fixed array of
 // la_chunk_fwd_noalloc). Every check runs before any launch.
 #include <atomic>
+#include <cuda.h>
 #include <cmath>
 #include <mutex>
 #include <stdint.h>
@@ -300,31 +301,79 @@ int la_device_status(la_stream_t stream) {
 // whole process, is neither used nor changed.
 namespace la {
 namespace {
-constexpr int kMaxPoolDevices = 64;
+constexpr int kMaxPoolDevices = 64, kPoolSlots = 4;
 std::mutex g_pool_mu;
-cudaMemPool_t g_pool[kMaxPoolDevices] = {};
+// per device, a few (context id, pool) pairs: a pool dies with its context
+// (e.g. at cudaDeviceReset), and a context made again gets a new id, so a dead
+// pool is never used; a caller alternating between contexts on one device
+// keeps one pool in each
+struct PoolSlot {
+    unsigned long long ctx;
+    cudaMemPool_t pool;
+};
+PoolSlot g_pool[kMaxPoolDevices][kPoolSlots] = {};
+unsigned int g_pool_next[kMaxPoolDevices] = {};  // slot to replace when all are taken
+
+typedef CUresult (*PfnCtxGetCurrent)(CUcontext *);
+typedef CUresult (*PfnCtxGetId)(CUcontext, unsigned long long *);
+PfnCtxGetCurrent g_ctx_get_current = nullptr;
+PfnCtxGetId g_ctx_get_id = nullptr;
+std::once_flag g_ctx_once;
+
+// Unique id of the current context (0 when it cannot be had). The driver calls
+// come through the runtime's entry-point query, so nothing links the driver.
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<PfnCtxGetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<PfnCtxGetId>(f);
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&c) != CUDA_SUCCESS || c == nullptr || g_ctx_get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 int scratch_pool(cudaMemPool_t *out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxPoolDevices) return LA_ERR_UNSUPPORTED;
+    const unsigned long long ctx = current_context_id();  // 0: unknown (e.g. no context current yet)
     std::lock_guard<std::mutex> lock(g_pool_mu);
-    if (g_pool[dev] == nullptr) {
-        cudaMemPoolProps props = {};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.handleTypes = cudaMemHandleTypeNone;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        cudaMemPool_t pool = nullptr;
-        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return LA_ERR_CUDA;
-        uint64_t keep = UINT64_MAX;
-        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
-            cudaMemPoolDestroy(pool);
-            return LA_ERR_CUDA;
+    PoolSlot *slots = g_pool[dev];
+    for (int i = 0; i < kPoolSlots; ++i) {
+        // with the context id unknown the first pool made on the device serves
+        if (slots[i].pool != nullptr && (slots[i].ctx == ctx || ctx == 0)) {
+            *out = slots[i].pool;
+            return LA_OK;
         }
-        g_pool[dev] = pool;
     }
-    *out = g_pool[dev];
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return LA_ERR_CUDA;
+    uint64_t keep = UINT64_MAX;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+        cudaMemPoolDestroy(pool);
+        return LA_ERR_CUDA;
+    }
+    // an empty slot, else the oldest (most likely of a context that is gone)
+    int slot = -1;
+    for (int i = 0; i < kPoolSlots && slot < 0; ++i)
+        if (slots[i].pool == nullptr) slot = i;
+    if (slot < 0) slot = (int)(g_pool_next[dev]++ % kPoolSlots);
+    slots[slot] = PoolSlot{ctx, pool};
+    *out = pool;
     return LA_OK;
 }
 }  // namespace

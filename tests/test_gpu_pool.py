@@ -51,3 +51,33 @@ def test_scratch_leaves_the_default_pool_unchanged():
     torch.cuda.synchronize()
     assert la.device_status() == 0
     assert _default_pool_attrs() == before
+
+
+def test_split_forward_replays_from_a_cuda_graph():
+    """The split forward takes its scratch from the library's pool with
+    stream-ordered calls, so after one ordinary call (which creates the pool)
+    it can be captured into a CUDA graph; the replay matches the oracle."""
+    from parity import TOL, rel_err, run_oracle
+    cfg = W.workload("gla", B=1, H=8, L=4096)
+    inp = W.chunk_inputs(cfg, 3)
+    x = {n: t.cuda() for n, t in inp.items() if t is not None}
+    out = torch.empty(1, 8, 4096, 128, dtype=torch.bfloat16, device="cuda")
+    st = torch.empty(1, 8, 128 * 128, device="cuda")
+
+    def call():
+        la.chunk_fwd(x["q"], x["k"], x["v"], x["gate"], phi="elu1", gate_kind="channel", chunk=64, out=out,
+                     final_state=st)
+
+    call()
+    torch.cuda.synchronize()
+    graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=side):
+        call()
+    out.fill_(float("nan"))
+    st.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    ro, rs = run_oracle(inp, cfg)
+    assert rel_err(out.float().cpu().numpy(), ro) <= TOL["bf16"]
+    assert rel_err(st.cpu().numpy(), rs) <= TOL["bf16"]
+    assert la.device_status() == 0
