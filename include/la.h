@@ -99,8 +99,9 @@ typedef enum {
  * before token 0; an initial state of la_chunk_fwd_from_state sits after the
  * last token). It equals the causal forward of the token-reversed sequence. The
  * backward pass is built from such sums. Tensor-core kernel only: bf16,
- * d_k = d_v = 128, chunk 64, identity feature map, no normaliser, no gate or the
- * head gate; anything else returns LA_ERR_UNSUPPORTED.
+ * d_k = d_v = 128, chunk 64, no normaliser, and either no gate (either feature
+ * map) or the head gate (identity feature map); anything else returns
+ * LA_ERR_UNSUPPORTED.
  *
  * Scratch: when the batch has too few (b, h) sequences to fill the GPU (2 B H
  * at most the number of SMs), the tensor-core path splits each sequence into

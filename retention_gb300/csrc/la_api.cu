@@ -16,8 +16,11 @@ std::atomic<unsigned long long> g_launches{0};
 
 constexpr int kKnownModeBits = LA_PHI_ELU1 | LA_NORMALIZE | LA_GATE_HEAD | LA_GATE_CHANNEL |
                                LA_DTYPE_F32 | LA_KERNEL_SIMT | LA_REVERSE;
-// what the anti-causal form does not run with
-constexpr int kNotWithReverse = LA_PHI_ELU1 | LA_NORMALIZE | LA_GATE_CHANNEL | LA_DTYPE_F32 | LA_KERNEL_SIMT;
+// what the anti-causal form does not run with (and elu+1 together with the head gate)
+constexpr int kNotWithReverse = LA_NORMALIZE | LA_GATE_CHANNEL | LA_DTYPE_F32 | LA_KERNEL_SIMT;
+bool reverse_unsupported(int mode) {
+    return (mode & kNotWithReverse) || ((mode & LA_PHI_ELU1) && (mode & LA_GATE_HEAD));
+}
 
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -28,7 +31,7 @@ int check_mode(int mode, const void *gate, bool decode, bool chunk = false) {
     if (decode && (mode & LA_KERNEL_SIMT)) return LA_ERR_INVALID_ARG;
     if (mode & LA_REVERSE) {
         if (!chunk) return LA_ERR_INVALID_ARG;
-        if (mode & kNotWithReverse) return LA_ERR_UNSUPPORTED;
+        if (reverse_unsupported(mode)) return LA_ERR_UNSUPPORTED;
     }
     const bool gh = mode & LA_GATE_HEAD, gc = mode & LA_GATE_CHANNEL;
     if (gh && gc) return LA_ERR_INVALID_ARG;
@@ -235,7 +238,7 @@ int la_chunk_fwd_path(int B, int H, int L, int dk, int dv, int mode, int chunk) 
     if (!dim_ok(dk) || !dim_ok(dv)) return LA_ERR_UNSUPPORTED;
     if (mode & ~kKnownModeBits) return LA_ERR_INVALID_ARG;
     if ((mode & LA_GATE_HEAD) && (mode & LA_GATE_CHANNEL)) return LA_ERR_INVALID_ARG;
-    if ((mode & LA_REVERSE) && (mode & kNotWithReverse)) return LA_ERR_UNSUPPORTED;
+    if ((mode & LA_REVERSE) && reverse_unsupported(mode)) return LA_ERR_UNSUPPORTED;
     la::ChunkArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, L, dk, dv, mode & ~LA_REVERSE, chunk};
     const bool tc = !(mode & LA_KERNEL_SIMT) && la::chunk_tc_supports(a);
     if ((mode & LA_REVERSE) && !tc) return LA_ERR_UNSUPPORTED;

@@ -449,7 +449,59 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
     return rc;
 }
 
+// The normalised form without a gate, one CTA per sequence: four launches. With
+// num_t = Q_t S_t and den_t = Q_t . z_t of the forward, w_t = dout_t / den_t and
+// e_t = -(dout_t . num_t) / den_t^2:
+//   dQ_t = sum_{s<=t} K_s (v_s . w_t + e_t)     causal, e on the query row
+//   dK_s = sum_{t>=s} Q_t (v_s . w_t + e_t)     anti-causal, e on the key column
+//   dv_s = sum_{t>=s} (K_s . Q_t) w_t           anti-causal
+// The forward kernel's backward-prep instance gives w and e in one pass (num_t
+// stays in its fp32 accumulator), and its bias instances add the e terms
+// inside the chunk (on the scores, before the mask) and across chunks (a
+// carried sum of value rows), so the cancelling sums are formed in fp32 and
+// leave as the bf16 gradients. With elu+1 the bias instances also take phi'
+// of q (dQ) or k (dK) in their store, so the gradients leave finished.
+static int launch_bwd_tc_norm_fused(const BwdArgs &a, cudaStream_t s, int *launches) {
+    const long rows = (long)a.B * a.H * a.L;
+    const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16);
+    const bool elu1 = a.mode & LA_PHI_ELU1;
+    // bf16 w; fp32 e [rows]
+    void *scratch = nullptr;
+    if (scratch_alloc(&scratch, hb + (size_t)rows * sizeof(float), s) != LA_OK) return LA_ERR_CUDA;
+    char *b = static_cast<char *>(scratch);
+    uint4 *w = reinterpret_cast<uint4 *>(b);
+    float *e = reinterpret_cast<float *>(b + hb);
+    const int phi = elu1 ? LA_PHI_ELU1 : 0;
+    int rc = LA_OK;
+    // the feature map runs inside each forward: on q and k (the prep, dv) or on
+    // the value tile (the bias instances, which take phi' of x in the store)
+    auto fwd = [&](const void *q, const void *k, const void *v, void *out, bool anti, int bias, const void *x) {
+        if (rc != LA_OK) return;
+        ChunkArgs c{q, k, v, nullptr, out, nullptr, a.B, a.H, a.L, kD, kD, phi, 64, nullptr, 0, 0, anti ? 1 : 0};
+        c.bias = bias;
+        c.bias_e = bias ? e : nullptr;
+        c.bias_x = x;
+        rc = launch_chunk_tc(c, s, launches);
+    };
+    {
+        // w and e from the normalised forward
+        ChunkArgs c{a.q, a.k, a.v, nullptr, w, nullptr, a.B, a.H, a.L, kD, kD, LA_NORMALIZE | phi, 64, nullptr};
+        c.bp_dout = a.dout;
+        c.bp_e = e;
+        rc = launch_chunk_tc(c, s, launches);
+    }
+    fwd(w, a.v, a.k, a.grad_q, false, 1, a.q);  // values phi(k); rows phi'(q)
+    fwd(a.v, w, a.q, a.grad_k, true, 2, a.k);   // values phi(q); rows phi'(k)
+    fwd(a.k, a.q, w, a.grad_v, true, 0, nullptr);  // phi(k) . phi(q)
+    if (cudaFreeAsync(scratch, s) != cudaSuccess && rc == LA_OK) rc = LA_ERR_CUDA;
+    return rc;
+}
+
 static int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
+    {
+        ChunkArgs c{a.q, a.k, a.v, nullptr, nullptr, nullptr, a.B, a.H, a.L, kD, kD, a.mode & LA_NORMALIZE, 64, nullptr};
+        if (!(a.mode & LA_GATE_HEAD) && chunk_tc_unsplit(c)) return launch_bwd_tc_norm_fused(a, s, launches);
+    }
     const long rows = (long)a.B * a.H * a.L;
     const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16), fb = 2 * hb;
     // bf16: Q K J w E; fp32: den_full U ZE dKm dz; den [rows]

@@ -74,6 +74,19 @@ struct ChunkArgs {
     const void *gn_ogate;
     const float *gn_weight, *gn_bias;
     float gn_eps;
+    // tensor-core path only, normalised causal form without a gate: the first step
+    // of the normalised backward in the store. out receives w = dout / den (bf16)
+    // and bp_e e_t = -(dout_t . num_t) / den_t^2 (fp32 [B][H][L]); null: none
+    const void *bp_dout;
+    float *bp_e;
+    // tensor-core path only, no gate or normaliser, unsplit: the score of every
+    // (query, key) pair gets e_t added (1: e of the query token, causal; 2: e of
+    // the key token, with reverse), bias_e [B][H][L] fp32; 0: none. With elu+1
+    // the feature map applies to v alone, and every output row is multiplied by
+    // phi'(x_t) = e^min(x_t, 0) of bias_x ([B][H][L][d] bf16, the map's input)
+    int bias;
+    const float *bias_e;
+    const void *bias_x;
 };
 
 struct GnArgs {
@@ -127,6 +140,7 @@ size_t bwd_scratch_bytes(const BwdArgs &a);
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);
 bool chunk_tc_fuses_epilogue(const ChunkArgs &a);
+bool chunk_tc_unsplit(const ChunkArgs &a);
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a);
 int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch, size_t scratch_bytes);
 // diagnostics: the tensor-core forward (unsplit only) with its producer stopping

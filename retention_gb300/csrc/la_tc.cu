@@ -94,8 +94,10 @@ struct TcParams {
     int init0;               // segment 0 starts from state_in too (a given initial state)
     uint64_t wait_ns;        // limit of every bounded wait (kWaitNs)
     int stall_chunk;         // diagnostics: the producer stops before this chunk (-1: never)
+    float *e_out;             // (backward prep) e_t per token, [BH][L]
+    const float *e_in;        // (bias instances) e_t per token, [BH][L]
     // extents (floats) of the global arrays, for the bounds checks of LA_DEBUG builds
-    size_t n_final, n_state_in, n_seg_state, n_seg_logdecay;
+    size_t n_final, n_state_in, n_seg_state, n_seg_logdecay, n_e;
 };
 
 constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
@@ -114,7 +116,7 @@ constexpr uint32_t kSmemBudget = 232448;  // dynamic shared memory of one CTA
 // remaining blocks in order. The gate tiles g have a ring of their own (GR):
 // the prologue is done with g after its first pass, so g is released early
 // and the next chunk's g is already in place when the prologue turns to it.
-template <int GATE, bool NORM, bool SO, bool OF32 = false, bool EPI = false>
+template <int GATE, bool NORM, bool SO, bool OF32 = false, int EPI = 0, int BIAS = 0>
 struct Layout {
     static constexpr bool GR = GATE >= 2 && !SO;
     // gated without the normaliser: three q|k|v stages and one gate slot fit;
@@ -124,7 +126,7 @@ struct Layout {
     static constexpr uint32_t so_stage = 2 * kTile + (NORM ? kHalf : 0) + (GATE >= 2 ? kTile : 0);
     // room kept for the float arrays, barriers and alignment slack below
     static constexpr uint32_t kReserve = 8192;
-    static constexpr int NS = !SO ? ((NORM && GATE != 0) ? 2 : 3)
+    static constexpr int NS = !SO ? ((NORM && (GATE != 0 || EPI != 0)) ? 2 : 3)
                                   : ((kSmemBudget - kReserve) / so_stage < 6 ? (kSmemBudget - kReserve) / so_stage : 6);
     static constexpr int T = 6 * NS;  // the shared ones block (full pass with the normaliser)
     static constexpr uint32_t pack(int a, int b, int c) {
@@ -148,17 +150,21 @@ struct Layout {
     // NF = NS + 1 slots: chunk n's decay factor goes to slot n % NF at the end of
     // its prologue, for the state chain to rescale T_n with.
     static constexpr int NF = NS + 1;
-    // (EPI) a second staging buffer: the og tile of chunk n lands in buffer n % 2
-    // and the chunk's result is written over it there
+    // (EPI, BIAS) a second staging buffer: chunk n is staged in buffer n % 2,
+    // where its og tile (EPI) or x tile (BIAS with elu+1) lands first and the
+    // chunk's result is written over it
     static constexpr uint32_t O2 = O + (SO ? 0 : (OF32 ? 32768 : 16384));
-    static constexpr uint32_t F = O2 + (EPI ? 16384 : 0);
+    static constexpr uint32_t F = O2 + ((EPI || BIAS) ? 16384 : 0);
     static constexpr uint32_t nfbuf = GATE != 0 ? NF * 128 : 0, nfq = GATE == 1 ? 128 : 0;
     static constexpr uint32_t ntot = GATE >= 2 ? (NORM ? 512 : 1024) : 0;  // quarter sums (one or two chunks)
     static constexpr uint32_t nwb = EPI ? 512 : 0;  // GroupNorm weight, bias [128] each; half-row (m, M2) [2][64][2]
-    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + ntot + nwb) * 4;
+    // (bias instances) per-chunk column sums [NF][128], the carried vector [128],
+    // e of the chunk's tokens for the prologue [64] and for the output role [64]
+    static constexpr uint32_t nbias = BIAS ? (NF * 128 + 128 + 64 + 64) : 0;
+    static constexpr uint32_t Bar = F + (128 + nfbuf + nfq + ntot + nwb + nbias) * 4;
     // full, empty, pro [NS]; ofull, oempty [2]; qk, pfull, pempty, sdone, sfree, sready, profinal,
-    // drain; gfull, gempty [NG]; ffull [NF]; (ogfull [2]: the output gate tiles)
-    static constexpr uint32_t nbar = 3 * NS + 12 + 2 * NG + NF + (EPI ? 2 : 0);
+    // drain; gfull, gempty [NG]; ffull [NF]; (ogfull [2]: the og or x tiles; cfull, cempty [NF])
+    static constexpr uint32_t nbar = 3 * NS + 12 + 2 * NG + NF + ((EPI || BIAS) ? 2 : 0) + (BIAS ? 2 * NF : 0);
     static constexpr uint32_t Misc = Bar + nbar * 8;  // TMEM base address
     static constexpr uint32_t bytes = Misc + 16 + 1024;  // + slack for the 1024-byte alignment
     // TMEM columns (region bases 32-column aligned). With the ones column the
@@ -266,6 +272,17 @@ __device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
     return r;
 }
 
+// phi'(x) = e^min(x, 0) of two bf16 values, in the arithmetic phi_elu1_bf16x2
+// takes for its exponential part
+__device__ __forceinline__ uint32_t dphi_elu1_bf16x2(uint32_t x) {
+    const uint32_t zero = 0u, log2e = 0x3FB93FB9u;
+    uint32_t m, y, e;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(x), "r"(zero));
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(y) : "r"(m), "r"(log2e));
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(y));
+    return e;
+}
+
 // SO (state only): the first pass over a split sequence. Each CTA runs one
 // segment from a zero state and keeps only the state update (no QK, no
 // outputs): it writes the segment's end state and its total log decay.
@@ -278,29 +295,57 @@ __device__ __forceinline__ uint32_t phi_elu1_bf16x2(uint32_t x) {
 // row. The state carried from chunk to chunk is then the sum over all later
 // tokens, decayed to the start of the chunk after the current one.
 //
-// EPI: the RetNet output epilogue in the output role's store (learnllm m22
+// EPI = 1: the RetNet output epilogue in the output role's store (learnllm m22
 // "Retention": a GroupNorm per head and a swish output gate),
 //   out_t = swish(og_t) * ((o_t - mean) / sqrt(var + eps) * weight[h] + bias[h]),
 // mean and the biased variance over the 128 values of row t, from the fp32
 // accumulator. Each output thread owns one token row, so the statistics need
 // no exchange between threads; the og tile comes by TMA into the staging
 // buffer, and each row is overwritten in place by its result.
-template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false, bool EPI = false>
+//
+// EPI = 2: the first step of the normalised backward, in the same store: with
+// num_t (columns 0..127 of O) and den_t (column 128) of the normalised forward
+// and the output gradient g_t (its tile by TMA, like og), each row writes
+//   w_t = g_t / den_t            (bf16, the call's output tensor)
+//   e_t = -(g_t . num_t) / den_t^2   (fp32, one value per token)
+// num_t never leaves the accumulator, so e_t, a difference the later
+// gradients cancel against, is formed from fp32 values.
+//
+// BIAS (the later steps of the normalised backward; identity features, no
+// gate, no normaliser): one more term e_t on every score, carried into the
+// output by a vector of value-row sums,
+//   BIAS = 1 (causal):      out_t = sum_{s<=t} (q_t . k_s + e_t) v_s
+//                                 = [causal form]_t + e_t (sum_{s<=t} v_s)
+//   BIAS = 2 (anti-causal): out_s = sum_{t>=s} (q_s . k_t + e_t) v_t
+//                                 = [anti-causal form]_s + sum_{t>=s} e_t v_t
+// Inside a chunk e rides on P before the mask; the sum over earlier chunks
+// (later ones with REV) is a carried vector added to each output row. The
+// prologue forms each chunk's weighted column sums of the value tile while it
+// holds the stage.
+template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false, int EPI = 0, int BIAS = 0>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
-    using LY = Layout<GATE, NORM, SO, OF32, EPI>;
+    using LY = Layout<GATE, NORM, SO, OF32, EPI, BIAS>;
     static_assert(GATE != 3 || (!ELU1 && !NORM), "the value-side gate takes features as given, no normaliser");
-    static_assert(!REV || (GATE <= 1 && !ELU1 && !NORM), "the anti-causal instance: scalar decay, features as given");
-    static_assert(!EPI || (GATE <= 1 && !NORM && !SO && !OF32 && !REV), "the fused epilogue: bf16 output, no normaliser");
-    // SPLIT (the fused epilogue): P and the outputs are separate roles, so P of
-    // chunk n + 1 is formed while chunk n's outputs are finished. TMEM lanes
-    // 0..63 (the token rows) are reachable from SM sub-partitions 0 and 1 only:
-    // warps 12 and 13 make P, warps 0, 1, 4 and 5 finish the outputs, half a row
-    // each, and the prologue moves to warps 6, 7, 14 and 15 (sub-partitions 2
-    // and 3). Otherwise the prologue runs on warps 4-7, 0, 1, 14, 15 and warps
-    // 12 and 13 make P and the outputs in turn. (The split layout measured
-    // slower without the epilogue: the prologue's work then has the special
-    // function units of two sub-partitions only.)
-    constexpr bool SPLIT = EPI;
+    static_assert(!REV || (GATE <= 1 && !NORM && (!ELU1 || GATE == 0)), "the anti-causal instance: scalar decay");
+    static_assert(EPI != 1 || (GATE <= 1 && !NORM && !SO && !OF32 && !REV), "the fused epilogue: bf16 output, no normaliser");
+    static_assert(EPI != 2 || (GATE == 0 && NORM && !SO && !OF32 && !REV), "the backward prep: the normalised causal form");
+    static_assert(BIAS == 0 || (GATE == 0 && !NORM && !SO && !OF32 && EPI == 0 && REV == (BIAS == 2)),
+                  "the bias instances: no gate or normaliser, bf16 output");
+    // (bias instances with ELU1) the feature map applies to the value tile, the
+    // query and key tiles are taken as given, and each output row is multiplied
+    // by phi'(x_t) = e^min(x_t, 0), x the tile of the map tog (the feature map's
+    // input whose gradient this is), which TMA brings to the staging buffer
+    constexpr bool PHIV = BIAS != 0 && ELU1;
+    // SPLIT (the fused epilogue, the bias instances): P and the outputs are
+    // separate roles, so P of chunk n + 1 is formed while chunk n's outputs are
+    // finished. TMEM lanes 0..63 (the token rows) are reachable from SM
+    // sub-partitions 0 and 1 only: warps 12 and 13 make P, warps 0, 1, 4 and 5
+    // finish the outputs, half a row each, and the prologue moves to warps 6, 7,
+    // 14 and 15 (sub-partitions 2 and 3). Otherwise the prologue runs on warps
+    // 4-7, 0, 1, 14, 15 and warps 12 and 13 make P and the outputs in turn. (The
+    // split layout measured slower for the plain forms: the prologue's work then
+    // has the special function units of two sub-partitions only.)
+    constexpr bool SPLIT = EPI != 0 || BIAS != 0;
     constexpr int PT = SPLIT ? 128 : 256;  // prologue threads
     constexpr int NS = LY::NS;
     constexpr int NG = LY::GR ? LY::NG : 1;  // gate ring slots (the ring exists only if GR)
@@ -329,6 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     float *fk = fq + 64;                                    // [64] retention: gamma^-(t+1)
     float *tot = fq + LY::nfq;                              // [1 or 2][4][128] gated: per-quarter log2 decay sums
     float *gnw = tot + LY::ntot, *gnb = gnw + 128;          // (EPI) GroupNorm weight and bias of head h
+    float *csum = gnw + LY::nwb;                            // (BIAS) [NF][128] weighted column sums of V per chunk
+    float *cvec = csum + (BIAS ? NF * 128 : 0);             // (BIAS) [128] the carried vector
+    float *pebuf = cvec + (BIAS ? 128 : 0);                 // (BIAS) [64] e of the prologue's chunk
+    float *oebuf = pebuf + (BIAS ? 64 : 0);                 // (BIAS) [64] e of the output role's chunk
     // Shared-memory offset of half h (columns 64h..64h+63) of tile tl of stage
     // s: tl = 0 q, 1 k, 2 v, 3 g (the g tile of a state-only stage)
     auto tile_half = [&](int tl, int s, int h) -> uint32_t {
@@ -346,7 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     uint64_t *sready = sfree + 1, *profinal = sready + 1, *drain = profinal + 1;
     uint64_t *gfull = drain + 1, *gempty = gfull + LY::NG;  // (empty arrays unless GR)
     uint64_t *ffull = gempty + LY::NG;                      // [NF]: fbuf slot written
-    uint64_t *ogfull = ffull + NF;                          // (EPI) [2]: og tile in staging buffer 0 / 1
+    uint64_t *ogfull = ffull + NF;                          // (EPI, BIAS) [2]: og / x tile in staging buffer 0 / 1
+    uint64_t *cfull = ogfull + ((EPI || BIAS) ? 2 : 0);     // (BIAS) [NF]: csum slot written
+    uint64_t *cempty = cfull + (BIAS ? NF : 0);             // (BIAS) [NF]: csum slot read
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + LY::Misc);
     uint8_t *sP = sm + LY::P, *sS = sm + LY::S, *sO = sm + LY::O;
 
@@ -398,10 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         mbar_init(sready, 128);
         mbar_init(profinal, GATE >= 2 ? 64 : 128);
         for (int j = 0; j < NF; ++j) mbar_init(&ffull[j], GATE >= 2 ? 64 : 128);
-        if (EPI) {
+        if (EPI || BIAS) {
             mbar_init(&ogfull[0], 1);
             mbar_init(&ogfull[1], 1);
         }
+        if (BIAS)
+            for (int j = 0; j < NF; ++j) {
+                mbar_init(&cfull[j], 16);  // one arrival per 8-column group
+                mbar_init(&cempty[j], 1);
+            }
         mbar_init(drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&p.tq);
@@ -409,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         tma_prefetch_desc(&p.tv);
         tma_prefetch_desc(&p.to);
         if (GATE >= 2) tma_prefetch_desc(&p.tg);
-        if (EPI) tma_prefetch_desc(&p.tog);
+        if (EPI || PHIV) tma_prefetch_desc(&p.tog);
     }
     if (NORM) {
         // constant blocks: the [64 x 64] atom(s) whose column 0 is 1 (the ones
@@ -800,6 +856,13 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // REV takes a ragged last chunk first: it closes a window of its own,
             // so that every window after it holds whole chunks only
             const int rag0 = (REV && c0 == 0 && (L % kC) != 0) ? 1 : 0;
+            // (BIAS 2) e of token pd of a chunk, read a chunk ahead of its use
+            auto e_at = [&](int m) {
+                const int tm = chunk_t0(m) + pd;
+                const size_t ei = (size_t)bh * L + tm;
+                return (tm < L && gok(ei, p.n_e)) ? p.e_in[ei] : 0.f;
+            };
+            float pe_next = (BIAS == 2 && pd < kC && N > 0) ? e_at(0) : 0.f;
             if (GATE == 1) {
                 // the row factors gamma^(t+1) and gamma^-(t+1) are the same in every chunk
                 if (pd < 64) {
@@ -818,15 +881,22 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     gq = __expf((float)(kC * m) * lg);
                     gk = __expf(-(float)(kC * m) * lg);
                 }
-                const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, wait_ns);
+                // (BIAS) the outputs, which may trail the MMAs, have read the column
+                // sums of chunk n - NF out of the slot this chunk's go to
+                const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, wait_ns) &&
+                                (BIAS == 0 || n < NF || mbar_wait(&cempty[n % NF], (uint32_t)(n / NF - 1) & 1u, wait_ns));
                 if (named_sync_or<kBarPro, PT>(!ok)) {
                     bad = 1;
                     break;
                 }
                 if (ELU1 || GATE == 1 || c < kC) {
+                    // the tiles taken: q and k (k only in the state-only pass), or v
+                    // alone with the feature map on the value tile
+                    constexpr int TL0 = PHIV ? 2 : (SO ? 1 : 0), TL1 = PHIV ? 3 : 2;
 #pragma unroll
-                    for (int isk = SO ? 1 : 0; isk < 2; ++isk) {
-                        uint8_t *blk0 = sm + tile_half(isk, s, 0), *blk1 = sm + tile_half(isk, s, 1);
+                    for (int tl = TL0; tl < TL1; ++tl) {
+                        const bool isk = tl != 0;  // rows past the end are zeroed (k, or v)
+                        uint8_t *blk0 = sm + tile_half(tl, s, 0), *blk1 = sm + tile_half(tl, s, 1);
                         const float *fr_arr = isk ? fk : fq;
                         // piece x = pd + PT j: block x / 512, row (x / 8) % 64, slot x % 8
                         constexpr int NJ = 1024 / PT;
@@ -878,6 +948,46 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     if (GATE == 1) fv = wend ? __expf(b_last + (float)(kC * m) * lg) : 1.f;
                     fbuf[(n % NF) * 128 + pd] = fv;
                     mbar_arrive(&ffull[n % NF]);
+                }
+                if constexpr (BIAS != 0) {
+                    // column sums of this chunk's value tile, each row weighted by 1
+                    // (BIAS 1) or by e of its token (BIAS 2): the sixteen 16-byte column
+                    // groups (block bv, slot lc) take TG = PT / 16 threads each, thread
+                    // pd group pd / TG over rows g, g + TG, ... (g = pd % TG); the TG
+                    // threads of a group sit in one warp and reduce by shuffles
+                    if (BIAS == 2 && pd < kC) {
+                        pebuf[pd] = pe_next;
+                        if (n + 1 < N) pe_next = e_at(n + 1);
+                    }
+                    // (the value tile was just rewritten with the feature map by other
+                    // threads' pieces)
+                    if (BIAS == 2 || PHIV) named_sync<kBarPro, PT>();
+                    constexpr int TG = PT / 16;
+                    const int bc = pd / TG, g = pd % TG, bv = bc >> 3, lc = bc & 7;
+                    const uint8_t *vt = sm + tile_half(2, s, bv);
+                    float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int rr = 0; rr < kC / TG; ++rr) {
+                        const int row = g + TG * rr;
+                        const float cw = BIAS == 2 ? pebuf[row] : 1.f;
+                        const uint4 x = ld16(vt + row * 128 + ((lc ^ (row & 7)) << 4));
+                        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            cs[2 * e] = fmaf(cw, bf16lo(xw[e]), cs[2 * e]);
+                            cs[2 * e + 1] = fmaf(cw, bf16hi(xw[e]), cs[2 * e + 1]);
+                        }
+                    }
+#pragma unroll
+                    for (int off = 1; off < TG; off <<= 1)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) cs[e] += __shfl_xor_sync(0xffffffffu, cs[e], off);
+                    if (g == 0) {
+                        float *dst = csum + (n % NF) * 128 + bv * 64 + lc * 8;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) dst[e] = cs[e];
+                        mbar_arrive(&cfull[n % NF]);
+                    }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&pro[s]);
@@ -1157,6 +1267,13 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
         const int t = tid - 384;
         // the mask: key columns at or before the query row (at or after it with REV)
         auto keep = [&](int j) { return REV ? j >= t : j <= t; };
+        // (BIAS) e of token t of a chunk, read a chunk ahead of its use
+        auto e_at = [&](int m) {
+            const int tm = chunk_t0(m) + t;
+            const size_t ei = (size_t)bh * L + tm;
+            return (tm < L && gok(ei, p.n_e)) ? p.e_in[ei] : 0.f;
+        };
+        float e_next = (BIAS != 0 && N > 0) ? e_at(0) : 0.f;
         for (int n = 0; n < N; ++n) {
             // QK of this chunk, and the intra MMA of the last one has read the P tile
             bool ok = mbar_wait(qk, (uint32_t)n & 1u, wait_ns);
@@ -1166,6 +1283,19 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 break;
             }
             tc_fence_after();
+            // (BIAS) e on every score of the row: the query token's (1), or each
+            // key column's (2, shared through oebuf)
+            float e_row = 0.f;
+            if constexpr (BIAS != 0) {
+                const float ev = e_next;
+                if (n + 1 < N) e_next = e_at(n + 1);
+                if (BIAS == 1) {
+                    e_row = ev;
+                } else {
+                    oebuf[t] = ev;
+                    named_sync<kBarP, 64>();
+                }
+            }
             uint8_t *prow = sP + t * 128;
             uint32_t r0[32], r1[32];
             tld32(tmem + lane_base + LY::colP, r0);
@@ -1181,31 +1311,50 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     const int jj = q8 * 8 + 2 * e;
                     const uint32_t a0 = q8 < 4 ? r0[jj] : r1[jj - 32];
                     const uint32_t a1 = q8 < 4 ? r0[jj + 1] : r1[jj - 31];
-                    u[e] = pack_bf16(keep(jj) ? __uint_as_float(a0) : 0.f, keep(jj + 1) ? __uint_as_float(a1) : 0.f);
+                    float p0 = __uint_as_float(a0), p1 = __uint_as_float(a1);
+                    if (BIAS == 1) {
+                        p0 += e_row;
+                        p1 += e_row;
+                    } else if (BIAS == 2) {
+                        p0 += oebuf[jj];
+                        p1 += oebuf[jj + 1];
+                    }
+                    u[e] = pack_bf16(keep(jj) ? p0 : 0.f, keep(jj + 1) ? p1 : 0.f);
                 }
                 st16(prow + (((q8 ^ t) & 7) << 4), make_uint4(u[0], u[1], u[2], u[3]));
             }
             fence_proxy_async_smem();
             mbar_arrive(pfull);
         }
-    } else if (EPI && (warp == 0 || warp == 1 || warp == 4 || warp == 5)) {
-        // ============================================================ outputs with the RetNet epilogue
+    } else if (SPLIT && (warp == 0 || warp == 1 || warp == 4 || warp == 5)) {
+        // ============================================================ outputs (split roles)
         // TMEM lanes 0..63 = rows t, on SM sub-partitions 0 and 1: warps 0 and 1
         // finish columns 0..63 of O, warps 4 and 5 columns 64..127. Each thread
-        // reads its half row of O out of TMEM once and keeps it in registers;
-        // the two halves of a row combine their mean and squared deviations
-        // (m, M2) through shared memory: mean = (m0 + m1) / 2,
+        // reads its half row of O out of TMEM once and keeps it in registers.
+        // With the RetNet epilogue the two halves of a row combine their mean and
+        // squared deviations (m, M2) through shared memory: mean = (m0 + m1) / 2,
         // M2 = M2_0 + M2_1 + (m0 - m1)^2 * 64 * 64 / 128 (the same expressions,
         // in the same order, in both halves).
         const int t = (warp & 1) * 32 + lane, oh = warp >= 4 ? 1 : 0;
         const bool lead = oh == 0 && t == 0;
-        float *part = gnb + kD;  // [2][64] (m, M2) of each half row
-        {
+        // a tile comes by TMA into each chunk's staging buffer first: og, the
+        // output gradient, or (bias instances with elu+1) x
+        constexpr bool TILE_IN = EPI != 0 || PHIV;
+        float *part = gnb + kD;  // [2][64] per half row: (m, M2), or the partial g . num
+        if constexpr (EPI == 1) {
             const int col = 64 * oh + t;
             const bool hin = gok(h, p.H);
             gnw[col] = p.gn_w && hin ? p.gn_w[(size_t)h * kD + col] : 1.f;
             gnb[col] = p.gn_b && hin ? p.gn_b[(size_t)h * kD + col] : 0.f;
         }
+        if (BIAS) cvec[64 * oh + t] = 0.f;  // the carried vector starts at zero
+        // (BIAS 1) e of row t's token, read a chunk ahead of its use
+        auto e_at = [&](int m) {
+            const int tm = chunk_t0(m) + t;
+            const size_t ei = (size_t)bh * L + tm;
+            return (tm < L && gok(ei, p.n_e)) ? p.e_in[ei] : 0.f;
+        };
+        float e_next = (BIAS == 1 && N > 0) ? e_at(0) : 0.f;
         named_sync<kBarOut, 128>();
         // staging buffer of chunk m, and the request of its og tile
         auto obuf = [&](int m) { return sm + ((m & 1) ? LY::O2 : LY::O); };
@@ -1216,32 +1365,105 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             tload(dst + kHalf, &p.tog, &ogfull[m & 1], 64, chunk_t0(m));
         };
         int ogi = 0;  // (lead) og tiles requested
-        if (lead && N > 0) og_load(ogi++);
+        if (TILE_IN && lead && N > 0) og_load(ogi++);
         for (int n = 0; n < N; ++n) {
             const int b = n % LY::NOB, t0 = chunk_t0(n);
             bool ok = mbar_wait(&ofull[b], (uint32_t)(n / LY::NOB) & 1u, wait_ns) &&
-                      mbar_wait(&ogfull[n & 1], (uint32_t)(n >> 1) & 1u, wait_ns);
-            if (lead && ok && n + 1 < N) {
-                // the next chunk's og tile into the buffer the store of chunk n - 1
+                      (!TILE_IN || mbar_wait(&ogfull[n & 1], (uint32_t)(n >> 1) & 1u, wait_ns));
+            if (TILE_IN && lead && ok && n + 1 < N) {
+                // the next chunk's tile into the buffer the store of chunk n - 1
                 // read from
                 if (n > 0) bulk_wait_read<0>();
                 og_load(ogi++);
             }
+            // (no tile in) the store of chunk n - 2 has left this chunk's buffer
+            if (!TILE_IN && lead && n > 1) bulk_wait_read<1>();
             if (named_sync_or<kBarOut, 128>(!ok)) {
                 bad = 1;
                 break;
             }
             tc_fence_after();
             // this thread's half row of O; the accumulator is free once it is read
-            uint32_t x0[32], x1[32];
+            uint32_t x0[32], x1[32], dd = 0;
             {
-                const uint32_t tO = tmem + lane_base + (b ? LY::colO1 : LY::colO0) + 64 * oh;
-                tld32(tO, x0);
-                tld32(tO + 32, x1);
+                const uint32_t tO = tmem + lane_base + (b ? LY::colO1 : LY::colO0);
+                if (EPI == 2) tld1(tO + 128, dd);  // den_t
+                tld32(tO + 64 * oh, x0);
+                tld32(tO + 64 * oh + 32, x1);
                 tmem_ld_wait();
             }
             tc_fence_before();
             mbar_arrive(&oempty[b]);
+            bool okc = true;  // (BIAS) the chunk's column sums arrived
+            if constexpr (EPI == 2) {
+                // w = g / den over this half row, in place over g; the half row's
+                // share of g . num, combined with the other half's through shared memory
+                const float rden = 1.f / __uint_as_float(dd);
+                uint8_t *const ob = obuf(n);
+                uint8_t *row = ob + oh * kHalf + t * 128;
+                f32x2_t acc = f2(0.f, 0.f);
+#pragma unroll
+                for (int lc = 0; lc < 8; ++lc) {
+                    uint8_t *pp = row + ((lc ^ (t & 7)) << 4);
+                    const uint4 g4 = ld16(pp);
+                    const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int idx = 8 * lc + 2 * e;
+                        const uint32_t v0 = idx < 32 ? x0[idx] : x1[idx - 32], v1 = idx < 32 ? x0[idx + 1] : x1[idx - 31];
+                        const float g0 = bf16lo(gw[e]), g1 = bf16hi(gw[e]);
+                        acc = f2_fma(f2(g0, g1), f2(__uint_as_float(v0), __uint_as_float(v1)), acc);
+                        w[e] = cvt_bf16x2(g0 * rden, g1 * rden);
+                    }
+                    st16(pp, make_uint4(w[0], w[1], w[2], w[3]));
+                }
+                float a0, a1;
+                f2_split(acc, a0, a1);
+                const float ph = a0 + a1;
+                *reinterpret_cast<float2 *>(part + (oh * 64 + t) * 2) = make_float2(ph, 0.f);
+                named_sync<kBarOut, 128>();
+                const float other = part[((1 - oh) * 64 + t) * 2];
+                const float e_t = -(oh == 0 ? ph + other : other + ph) * rden * rden;
+                const size_t ei = (size_t)bh * L + t0 + t;
+                if (oh == 0 && t0 + t < L && gok(ei, p.n_e)) p.e_out[ei] = e_t;
+            } else if constexpr (BIAS != 0) {
+                // the carried vector's share, e_t cvec (1) or cvec (2), and (PHIV)
+                // the factor phi'(x) of the x value in the same place; two columns
+                // at a time, in place over x
+                const float e_row = e_next;
+                if (BIAS == 1 && n + 1 < N) e_next = e_at(n + 1);
+                const f32x2_t er = f2(e_row, e_row);
+                uint8_t *const ob = obuf(n);
+                uint8_t *row = ob + oh * kHalf + t * 128;
+#pragma unroll
+                for (int lc = 0; lc < 8; ++lc) {
+                    uint8_t *pp = row + ((lc ^ (t & 7)) << 4);
+                    const uint4 xv = PHIV ? ld16(pp) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int idx = 8 * lc + 2 * e;
+                        const uint32_t v0 = idx < 32 ? x0[idx] : x1[idx - 32], v1 = idx < 32 ? x0[idx + 1] : x1[idx - 31];
+                        const f32x2_t cv = *reinterpret_cast<const f32x2_t *>(cvec + 64 * oh + idx);
+                        f32x2_t y = f2(__uint_as_float(v0), __uint_as_float(v1));
+                        y = BIAS == 1 ? f2_fma(er, cv, y) : f2_add(y, cv);
+                        if (PHIV) {
+                            const uint32_t d = dphi_elu1_bf16x2(xw[e]);
+                            y = f2_mul(y, f2(bf16lo(d), bf16hi(d)));
+                        }
+                        float y0, y1;
+                        f2_split(y, y0, y1);
+                        w[e] = cvt_bf16x2(y0, y1);
+                    }
+                    st16(pp, make_uint4(w[0], w[1], w[2], w[3]));
+                }
+                // every row has used the carried vector: add this chunk's column sums
+                named_sync<kBarOut, 128>();
+                okc = mbar_wait(&cfull[n % NF], (uint32_t)(n / NF) & 1u, wait_ns);
+                if (okc) cvec[64 * oh + t] += csum[(n % NF) * 128 + 64 * oh + t];
+            } else {
             // half-row mean and squared deviations
             f32x2_t acc = f2(0.f, 0.f);
 #pragma unroll
@@ -1292,8 +1514,18 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 }
                 st16(pp, make_uint4(w[0], w[1], w[2], w[3]));
             }
+            }  // (EPI == 1)
+            uint8_t *const ob = obuf(n);
             fence_proxy_async_smem();
-            named_sync<kBarOut, 128>();
+            if constexpr (BIAS != 0) {
+                if (named_sync_or<kBarOut, 128>(!okc)) {
+                    bad = 1;
+                    break;
+                }
+                if (lead) mbar_arrive(&cempty[n % NF]);
+            } else {
+                named_sync<kBarOut, 128>();
+            }
             if (lead) {
                 tstore(&p.to, ob, 0, t0);
                 tstore(&p.to, ob + kHalf, 64, t0);
@@ -1396,12 +1628,12 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
 // after_scan: launched behind the segment scan as a programmatic dependent
 // launch, so that its CTAs set up and start on their first chunks while the
 // scan finishes (they wait for it before reading the carried states).
-template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false, bool EPI = false>
+template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false, int EPI = 0, int BIAS = 0>
 int launch_t(const TcParams &prm, int grid, cudaStream_t s, bool after_scan) {
-    using LY = Layout<GATE, NORM, SO, OF32, EPI>;
+    using LY = Layout<GATE, NORM, SO, OF32, EPI, BIAS>;
     static_assert(LY::NS >= 2 && LY::bytes <= kSmemBudget, "shared memory budget");
     static_assert(LY::colP + 64 <= kTmemCols && LY::colO1 + LY::NW <= LY::colP, "TMEM budget");
-    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO, OF32, REV, EPI>;
+    auto kern = la_chunk_tc_kernel<GATE, ELU1, NORM, SO, OF32, REV, EPI, BIAS>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::bytes) != cudaSuccess)
         return LA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1427,21 +1659,45 @@ int launch_g(const TcParams &prm, int grid, cudaStream_t s, bool elu1, bool norm
 
 template <bool SO>
 int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool out_f32 = false, bool value_gate = false,
-                bool pdl = false, bool rev = false, bool epi = false) {
+                bool pdl = false, bool rev = false, int epi = 0, int bias = 0) {
     const bool elu1 = mode & LA_PHI_ELU1, norm = mode & LA_NORMALIZE;
-    if (epi && !SO) {
+    if (bias != 0) {
+        // the bias instances: no gate or normaliser, bf16 output, unsplit; with
+        // LA_PHI_ELU1 the feature map applies to the value tile
+        if (SO || norm || out_f32 || value_gate || epi || (mode & (LA_GATE_HEAD | LA_GATE_CHANNEL)) ||
+            rev != (bias == 2))
+            return LA_ERR_INTERNAL;
+        if (bias == 1)
+            return elu1 ? launch_t<0, true, false, false, false, false, 0, 1>(prm, grid, s, pdl)
+                        : launch_t<0, false, false, false, false, false, 0, 1>(prm, grid, s, pdl);
+        return elu1 ? launch_t<0, true, false, false, false, true, 0, 2>(prm, grid, s, pdl)
+                    : launch_t<0, false, false, false, false, true, 0, 2>(prm, grid, s, pdl);
+    }
+    if (epi == 2 && !SO) {
+        // the backward prep: the normalised causal form, no gate
+        if (!norm || out_f32 || value_gate || rev || (mode & (LA_GATE_HEAD | LA_GATE_CHANNEL))) return LA_ERR_INTERNAL;
+        return elu1 ? launch_t<0, true, true, false, false, false, 2>(prm, grid, s, pdl)
+                    : launch_t<0, false, true, false, false, false, 2>(prm, grid, s, pdl);
+    }
+    if (epi == 1 && !SO) {
         // the RetNet epilogue in the store: no normaliser, no gate or the head gate
         if (norm || out_f32 || value_gate || rev || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
         if (mode & LA_GATE_HEAD)
-            return elu1 ? launch_t<1, true, false, false, false, false, true>(prm, grid, s, pdl)
-                        : launch_t<1, false, false, false, false, false, true>(prm, grid, s, pdl);
-        return elu1 ? launch_t<0, true, false, false, false, false, true>(prm, grid, s, pdl)
-                    : launch_t<0, false, false, false, false, false, true>(prm, grid, s, pdl);
+            return elu1 ? launch_t<1, true, false, false, false, false, 1>(prm, grid, s, pdl)
+                        : launch_t<1, false, false, false, false, false, 1>(prm, grid, s, pdl);
+        return elu1 ? launch_t<0, true, false, false, false, false, 1>(prm, grid, s, pdl)
+                    : launch_t<0, false, false, false, false, false, 1>(prm, grid, s, pdl);
     }
     if (rev) {
-        // anti-causal: identity feature map, no normaliser, no gate or the head gate
-        if (elu1 || norm || value_gate || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
+        // anti-causal: no normaliser; no gate (with either feature map) or the head
+        // gate (identity feature map)
+        if (norm || value_gate || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
         const bool gh = mode & LA_GATE_HEAD;
+        if (elu1) {
+            if (gh || out_f32) return LA_ERR_INTERNAL;
+            return SO ? launch_t<0, true, false, true, false, true>(prm, grid, s, pdl)
+                      : launch_t<0, true, false, false, false, true>(prm, grid, s, pdl);
+        }
         if (SO)
             return gh ? launch_t<1, false, false, true, false, true>(prm, grid, s, pdl)
                       : launch_t<0, false, false, true, false, true>(prm, grid, s, pdl);
@@ -1525,6 +1781,13 @@ int tc_segments(int BH, int nchunks, int *seg_chunks) {
     return (nchunks + cs - 1) / cs;
 }
 
+// Whether the tensor-core path runs these arguments as one CTA per sequence
+// (no split into segments).
+bool chunk_tc_unsplit(const ChunkArgs &a) {
+    int seg_chunks = 0;
+    return tc_segments(a.B * a.H, (a.L + kC - 1) / kC, &seg_chunks) == 1;
+}
+
 // Scratch bytes the tensor-core path needs for these arguments (0 when the
 // sequences are not split).
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a) {
@@ -1553,12 +1816,27 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
         !(a.out_f32 ? make_map_f32(&prm.to, a.out, a.L, BH) : make_map(&prm.to, a.out, a.L, BH)))
         return LA_ERR_CUDA;
     if ((a.mode & LA_GATE_CHANNEL) && !make_map(&prm.tg, a.gate, a.L, BH)) return LA_ERR_CUDA;
-    const bool epi = a.gn_ogate != nullptr;
-    if (epi) {
+    const int epi = a.gn_ogate != nullptr ? 1 : a.bp_dout != nullptr ? 2 : 0;
+    if (epi == 1) {
         if (!chunk_tc_fuses_epilogue(a) || !make_map(&prm.tog, a.gn_ogate, a.L, BH)) return LA_ERR_INTERNAL;
         prm.gn_w = a.gn_weight;
         prm.gn_b = a.gn_bias;
         prm.gn_eps = a.gn_eps;
+    } else if (epi == 2) {
+        // the backward prep: the output gradient's tile rides where og would
+        if (a.bp_e == nullptr || !make_map(&prm.tog, a.bp_dout, a.L, BH)) return LA_ERR_INTERNAL;
+        prm.e_out = a.bp_e;
+        prm.n_e = (size_t)BH * a.L;
+    }
+    if (a.bias != 0) {
+        // the carried vector runs over whole sequences: one CTA per sequence only
+        if (a.bias_e == nullptr || epi != 0) return LA_ERR_INTERNAL;
+        prm.e_in = a.bias_e;
+        prm.n_e = (size_t)BH * a.L;
+        if (a.mode & LA_PHI_ELU1) {
+            // phi' of the map's input multiplies the store: its tile rides where og would
+            if (a.bias_x == nullptr || !make_map(&prm.tog, a.bias_x, a.L, BH)) return LA_ERR_INTERNAL;
+        }
     }
     prm.gamma = (a.mode & LA_GATE_HEAD) ? static_cast<const float *>(a.gate) : nullptr;
     prm.final_state = a.final_state;
@@ -1573,9 +1851,10 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.n_final = a.final_state ? (size_t)BH * blkf : 0;
     prm.n_state_in = a.initial_state ? (size_t)BH * blkf : 0;  // (split: the carried states, below)
     if (stall_chunk >= 0 && prm.nseg != 1) return LA_ERR_UNSUPPORTED;  // the stall runs one launch only
+    if (a.bias != 0 && prm.nseg != 1) return LA_ERR_UNSUPPORTED;        // (as above)
     if (prm.nseg == 1) {
         prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
-        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32, a.value_gate, false, a.reverse, epi);
+        const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32, a.value_gate, false, a.reverse, epi, a.bias);
         if (rc == LA_OK) *launches += 1;
         return rc;
     }

@@ -230,13 +230,13 @@ def _check_reverse(cfg, inp, initial_state=None):
     assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
 
 
-@pytest.mark.parametrize("gate", [None, "head"])
+@pytest.mark.parametrize("phi,gate", [("identity", None), ("identity", "head"), ("elu1", None)])
 @pytest.mark.parametrize("B,H,L", [(1, 4, 1000), (2, 40, 333), (2, 40, 129), (1, 80, 64), (1, 80, 1)],
                          ids=["split", "unsplit-ragged", "unsplit-129", "one-chunk", "one-token"])
-def test_reverse_matches_the_reversed_causal_oracle(gate, B, H, L):
+def test_reverse_matches_the_reversed_causal_oracle(phi, gate, B, H, L):
     from retention_gb300 import la
-    cfg = W.workload("retention", B=B, H=H, L=L, gate=gate)
-    mode = la.mode_bits("identity", False, gate, reverse=True)
+    cfg = W.workload("retention", B=B, H=H, L=L, gate=gate, phi=phi)
+    mode = la.mode_bits(phi, False, gate, reverse=True)
     assert la.chunk_fwd_path(B, H, L, 128, 128, mode, 64) == 1
     _check_reverse(cfg, W.chunk_inputs(cfg, seed=L + H))
 
