@@ -379,10 +379,10 @@ def bench_chunk(name, steps, warmup, world, pk):
 
 def bench_delta(steps, warmup, world, pk):
     """The delta rule (la_delta_fwd) on its workload. The default path works
-    in chunks of 64 on the tensor cores (two kernels: W and U of every chunk,
-    then the state recurrence); its roofline is HBM (read q, k, v, beta, write
-    out and the final state once) against the chunked form's products (about
-    11 MFLOP per 64-token chunk and head). The recurrent kernel
+    in chunks of 64 on the tensor cores (one kernel: T of the next chunk made
+    beside the state recurrence); its roofline is HBM (read q, k, v, beta,
+    write out and the final state once) against the chunked form's products
+    (about 10.5 MFLOP per 64-token chunk and head). The recurrent kernel
     (LA_KERNEL_SIMT) is timed beside it against the FP32 FMA pipe: 6 d_k d_v
     flops per token and head, SMs x 128 lanes x 2 flops x 2070 MHz."""
     from retention_gb300 import la
@@ -406,12 +406,12 @@ def bench_delta(steps, warmup, world, pk):
     n = B * H * L
     bytes_ = n * (2 * dk + 2 * dv + 1) * 2 + B * H * dk * dv * 4
     C = 64
-    # per chunk: K K^T, Q K^T; T K, T V; W S0^T, Q S0^T, K^T Ut; P Ut
-    flops = n / C * (2 * 2 * C * C * dk + 2 * C * C * (dk + dv) + 3 * 2 * C * dk * dv + 2 * C * C * dv)
+    # per chunk: K K^T, Q K^T; K S0^T, Q S0^T, K^T Ut; T Vt, P Ut
+    flops = n / C * (2 * 2 * C * C * dk + 3 * 2 * C * dk * dv + 2 * 2 * C * C * dv)
     t_roof = max(bytes_ / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
     fma_peak = torch.cuda.get_device_properties(0).multi_processor_count * 128 * 2 * 2.07e9 / 1e12
     rflops = 6.0 * n * dk * dv
-    return {"tokens_per_s": world * B * L / t, "ms_per_step": t * 1e3, "launches_per_step": 2,
+    return {"tokens_per_s": world * B * L / t, "ms_per_step": t * 1e3, "launches_per_step": 1,
             "roofline": {"bound": "hbm", "frac": t_roof / t, "algorithmic_bytes": bytes_,
                          "tensor_tflops": flops / t / 1e12},
             "recurrent": {"ms_per_step": tr * 1e3, "tflops": rflops / tr / 1e12,

@@ -175,12 +175,11 @@ int la_chunk_fwd_from_state(const void *q, const void *k, const void *v, const v
  * and inside a chunk the u_t solve a unit lower-triangular system (I + A) U =
  * diag(beta) (V - K S0^T), A[t][s] = beta_t k_t . k_s for s < t, so a chunk
  * is a triangular inverse and a few matrix products (the recurrence
- * rearranged; no page gives this form). W = T K and U = T V (T = (I + A)^-1
- * diag(beta)) do not depend on the state, so a first kernel makes them for
- * every chunk at once into stream-ordered scratch (32 KiB per chunk of 64
- * tokens and head; LA_ERR_CUDA if the allocation fails) and a second runs the
- * state through the chunks. Every other case runs the recurrence token by
- * token on the CUDA cores in fp32 (6 d_k d_v flops a token).
+ * rearranged; no page gives this form). T = (I + A)^-1 diag(beta) does not
+ * depend on the state, so one kernel (a CTA per sequence) makes T of the next
+ * chunk while the state runs through the current one; it allocates nothing.
+ * Every other case runs the recurrence token by token on the CUDA cores in
+ * fp32 (6 d_k d_v flops a token).
  * Errors as la_chunk_fwd; beta needs only element alignment.
  */
 int la_delta_fwd(const void *q, const void *k, const void *v, const void *beta,

@@ -21,6 +21,7 @@ MODES = [
     dict(phi="elu1", normalize=False, gate="channel"),
     dict(phi="elu1", normalize=True, gate="channel"),
     dict(phi="identity", normalize=False, gate="channel"),
+    dict(phi="identity", normalize=True, gate=None),
 ]
 MID = lambda m: "%s-%s-%s" % (m["phi"], m["normalize"], m["gate"])
 
@@ -34,6 +35,11 @@ def _check(cfg, seed=0, heads=None, tol=None, simt=False):
     first few heads of every batch row (the GPU computes all of them)."""
     from retention_gb300 import la
     inp = W.chunk_inputs(cfg, seed)
+    if cfg["phi"] == "identity" and cfg["normalize"]:
+        # with the identity map the normaliser needs features that are already
+        # positive: den_t = q_t . z_t then stays away from zero (signed inputs
+        # let it cross zero, where the form has no precision left to compare)
+        inp = dict(inp, q=inp["q"].abs(), k=inp["k"].abs())
     dout = W.bwd_inputs(cfg, seed)
     x = to_dev(inp)
     d = dout.cuda()
@@ -106,7 +112,7 @@ def test_bf16_modes(m, simt):
         assert launches == (4 if m["normalize"] else 3), launches
 
 
-@pytest.mark.parametrize("m", [MODES[0], MODES[1], MODES[3], MODES[4], MODES[5], MODES[7]], ids=MID)
+@pytest.mark.parametrize("m", [MODES[0], MODES[1], MODES[3], MODES[4], MODES[5], MODES[7], MODES[8]], ids=MID)
 @pytest.mark.parametrize("B,H,L", [(1, 2, 1000), (2, 40, 200), (1, 1, 1), (1, 3, 65)])
 def test_bf16_tensor_core_route_shapes(m, B, H, L):
     """Split and unsplit sequences, one token, a ragged chunk."""

@@ -63,14 +63,14 @@ def test_full_size_workload(simt):
     _check(W.workload("delta"), seed=0, simt=simt)
 
 
-def test_chunked_kernels_are_the_default_and_two_launches():
-    """W and U for every chunk, then the state recurrence."""
+def test_chunked_kernel_is_the_default_and_one_launch():
+    """T of every chunk and the state recurrence in one kernel."""
     cfg = W.workload("delta", B=2, H=2, L=100)
     d = {n: t.cuda() for n, t in W.delta_inputs(cfg, 0).items()}
     n0 = la.kernel_launches()
     la.delta_fwd(d["q"], d["k"], d["v"], d["beta"])
     torch.cuda.synchronize()
-    assert la.kernel_launches() - n0 == 2
+    assert la.kernel_launches() - n0 == 1
 
 
 @pytest.mark.parametrize("simt", [False, True], ids=["chunked", "recurrent"])

@@ -1,6 +1,6 @@
 """The library's scratch memory leaves the process's default memory pool
-alone: the split chunk forward, the chunked delta rule and the backward take
-their stream-ordered scratch from a pool of the library's own. The default
+alone: the split chunk forward and the backward take their stream-ordered
+scratch from a pool of the library's own (the chunked delta rule takes none). The default
 pool's release threshold and reserved size are read through the CUDA driver
 before and after those calls and must not change."""
 import ctypes
@@ -39,11 +39,11 @@ def test_scratch_leaves_the_default_pool_unchanged():
     mode = la.mode_bits(cfg["phi"], cfg["normalize"], cfg["gate"])
     assert la.chunk_fwd_path(1, 8, 4096, 128, 128, mode, 64) == 1
     la.chunk_fwd(x["q"], x["k"], x["v"], x["gate"], phi="elu1", gate_kind="channel", chunk=64)
-    # chunked delta rule: W | U images in scratch
+    # chunked delta rule: no scratch at all
     dcfg = W.workload("delta", B=1, H=4, L=512)
     d = {n: t.cuda() for n, t in W.delta_inputs(dcfg, 3).items()}
     la.delta_fwd(d["q"], d["k"], d["v"], d["beta"])
-    # backward: reversed copies and partial gradients in scratch
+    # backward of a short batch: the split forwards' segment states in scratch
     rcfg = W.workload("retention", B=1, H=4, L=512)
     r = {n: t.cuda() for n, t in W.chunk_inputs(rcfg, 3).items() if t is not None}
     dout = torch.randn_like(r["v"])
