@@ -403,9 +403,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
             int fail = bad || !mbar_wait(full + (n & 1), (uint32_t)(n >> 1) & 1u, kWaitNs) ||
                        !mbar_wait(kfull + n % 3, (uint32_t)(n / 3) & 1u, kWaitNs);
             // ------------------------------------------------------------ round 3
-            // Y first (the recurrence waits on it), then P; O = Q S0^T follows
-            // once the previous chunk's out rows are read out of its
-            // accumulator, then the next chunk's K K^T
+            // Y first (the recurrence waits on it), then P, then the next
+            // chunk's K K^T (for the solvers) while Vt is formed
+            bool kk_next = false;  // (issuer) K K^T of chunk n + 1 issued
             if (issuer) {
                 tc_fence_after();
 #pragma unroll
@@ -416,30 +416,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 for (int ks = 0; ks < 8; ++ks)
                     umma_bf16(tmem + cP, kmaj2(set + fQo, ks), kmaj2(kt, ks), id64, ks > 0);
                 umma_commit(mbP);
-            }
-            if (low) {
-                if (n > 0 && !read_out(n - 1)) fail = 1;
-                tc_fence_before();
-                mbar_arrive(ofree);
-            }
-            if (issuer || (tid == 0 && n > 0)) {
-                if (!mbar_wait(ofree, ph, kWaitNs)) fail = 1;
-                tc_fence_after();
-                if (issuer) {
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        umma_bf16(tmem + cO, kmaj2(set + fQo, ks), mnmaj(sm0 + fS, 16384, ks), idKM, ks > 0);
-                    // the next chunk's K K^T, once its k tile has landed and the
-                    // solvers have read this chunk's out of cA
-                    if (n + 1 < nchunks) {
-                        if (!mbar_wait(kfull + (n + 1) % 3, (uint32_t)((n + 1) / 3) & 1u, kWaitNs) ||
-                            !mbar_wait(afree, ph, kWaitNs))
-                            fail = 1;
-                        else
-                            issue_kk(n + 1);
-                    }
-                } else {
-                    store_out(n - 1);
+                // if its k tile has landed and the solvers have read this
+                // chunk's out of cA (else after round 4)
+                if (n + 1 < nchunks && mbar_try_wait(kfull + (n + 1) % 3, (uint32_t)((n + 1) / 3) & 1u) &&
+                    mbar_try_wait(afree, ph)) {
+                    issue_kk(n + 1);
+                    kk_next = true;
                 }
             }
             if (low) {
@@ -484,7 +466,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                     }
                     *reinterpret_cast<uint4 *>(sm + fP + chunk_off(t, 4 * hf + c4, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                // the staging tile is free again once the store has read it
+                // the staging tile is free again once the store of chunk n - 2 has read it
                 if (tid == 0) bulk_wait_read<0>();
             }
             fence_proxy_async_smem();
@@ -495,6 +477,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 break;
             }
             // ------------------------------------------------------------ round 3b: Ut = T Vt
+            // then O = Q S0^T once the previous chunk's out rows are read out of
+            // its accumulator (the low warps do that while Ut is made)
             if (issuer) {
                 // (a commit with nothing before it still completes, so the wait
                 // below ends either way; the failure leaves at the next barrier)
@@ -507,6 +491,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                                   mnmaj(set + fVo, 8192, ks), idKM, ks > 0);
                 }
                 umma_commit(mbU);
+            }
+            if (low) {
+                if (n > 0 && !read_out(n - 1)) fail = 1;
+                tc_fence_before();
+                mbar_arrive(ofree);
+            }
+            if (issuer || (tid == 0 && n > 0)) {
+                if (!mbar_wait(ofree, ph, kWaitNs)) fail = 1;
+                tc_fence_after();
+                if (issuer) {
+                    if (!fail) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            umma_bf16(tmem + cO, kmaj2(set + fQo, ks), mnmaj(sm0 + fS, 16384, ks), idKM, ks > 0);
+                    }
+                } else {
+                    store_out(n - 1);
+                }
             }
             if (low) {
                 // Ut row t, value channels 64 hf .. 64 hf + 63, bf16 MN-major
@@ -542,6 +544,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 for (int ks = 0; ks < 4; ++ks)
                     umma_bf16(tmem + cO, kmaj1(sm0 + fP, ks), mnmaj(sm0 + fU, 8192, ks), idKM, 1);
                 umma_commit(mbO);
+                // else the next chunk's K K^T now, behind this round's products
+                if (n + 1 < nchunks && !kk_next) {
+                    if (!mbar_wait(kfull + (n + 1) % 3, (uint32_t)((n + 1) / 3) & 1u, kWaitNs) ||
+                        !mbar_wait(afree, ph, kWaitNs))
+                        fail = 1;
+                    else
+                        issue_kk(n + 1);
+                }
             }
             {
                 // S^T line i = t (TMEM lane), value channels 64 hf .. 64 hf + 63 ->
@@ -575,8 +585,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 break;
             }
         }
-        // the last chunk's out rows
+        // the last chunk's out rows, once the store of the one before has left
+        // the staging tile
         if (!bad && low && nchunks > 0) {
+            if (tid == 0) bulk_wait_read<0>();
+            __syncwarp();
+            named_sync<2, 128>();
             if (!read_out(nchunks - 1)) bad = 1;
             named_sync<2, 128>();
             if (tid == 0) store_out(nchunks - 1);
