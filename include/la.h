@@ -117,8 +117,9 @@ typedef enum {
  * changed. The first call that takes scratch in a context creates the pool and
  * should come before any stream capture.
  * la_chunk_fwd_noalloc is the same call without any allocation.
- * A split call issues three kernels on `stream`: the segment end states, a
- * scan over them, and the full pass. The full pass goes out as a programmatic
+ * A split call issues three kernels on `stream`: the segment end states (of
+ * every segment but each sequence's last), a scan over them, and the full pass
+ * (which writes final_state from its last segments). The full pass goes out as a programmatic
  * dependent launch behind the scan. Its CTAs may start before the scan ends,
  * but they wait for it before reading what it wrote, and the call's work is
  * complete, for later work on `stream`, only when all three have finished.

@@ -86,7 +86,7 @@ struct TcParams {
     const float *gn_w, *gn_b; // GroupNorm weight and bias [H][128] or null
     float gn_eps;
     const float *gamma;
-    float *final_state;      // [BH][blk], written by an unsplit full pass
+    float *final_state;      // [BH][blk], written by the full pass's last segment of each sequence
     const float *state_in;   // [BH][nseg][blk]: state at each segment start (full pass)
     float *seg_state;        // [BH][nseg][blk]: segment-local end state (state-only pass)
     float *seg_logdecay;     // [BH][nseg][128]: log decay over each segment (state-only pass)
@@ -357,7 +357,11 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t wait_ns = p.wait_ns;  // limit of every bounded wait
     // CTA = (b, h, segment); a segment is seg_chunks consecutive chunks
-    const int bh = blockIdx.x / p.nseg, seg = blockIdx.x % p.nseg, h = bh % p.H, L = p.L;
+    // (the state-only pass has no CTA for a sequence's last segment: the full
+    // pass holds that segment's end state, which is the final state)
+    const int gseg = SO ? p.nseg - 1 : p.nseg;  // this grid's segments per sequence
+    const int bh = blockIdx.x / gseg, seg = blockIdx.x % gseg, h = bh % p.H, L = p.L;
+    const int sgi = bh * p.nseg + seg;  // segment index in the scratch arrays
     const int c0 = seg * p.seg_chunks;
     const int nch = (L + kC - 1) / kC;
     const int N = max(0, min(p.seg_chunks, nch - c0));
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     auto chunk_t0 = [&](int n) { return (REV ? nch - 1 - (c0 + n) : c0 + n) * kC; };
     const bool init = !SO && p.state_in != nullptr && (seg > 0 || p.init0);  // start from a carried state
     const size_t blk = (size_t)kD * kD + (NORM ? kD : 0);
-    const size_t segblk = (size_t)blockIdx.x * blk;
+    const size_t segblk = (size_t)sgi * blk;
 
     constexpr int NF = LY::NF;
     float *ffinal = reinterpret_cast<float *>(sm + LY::F);  // [128] e^{b_last} of the last chunk
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     // extent first, and a failed check skips the access (and records its line);
     // in the ordinary build each check is the constant true.
     [[maybe_unused]] const uint32_t sm_lo = smem_u32(sm), sm_hi = smem_u32(smem_raw) + LY::bytes;
-    [[maybe_unused]] const int nbh_grid = (int)gridDim.x / p.nseg;
+    [[maybe_unused]] const int nbh_grid = (int)gridDim.x / gseg;
     auto sok = [&](const void *ptr, uint32_t n) {
         return TC_CHECK(smem_u32(ptr) >= sm_lo && smem_u32(ptr) + n <= sm_hi);
     };
@@ -828,8 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             if (!bad && qr == 3) {
                 *reinterpret_cast<float2 *>(ffinal + cw) = make_float2(ex2f(bl0), ex2f(bl1));
                 if (SO)
-                    if (gok((size_t)blockIdx.x * kD + cw + 1, p.n_seg_logdecay))
-                        *reinterpret_cast<float2 *>(p.seg_logdecay + (size_t)blockIdx.x * kD + cw) =
+                    if (gok((size_t)sgi * kD + cw + 1, p.n_seg_logdecay))
+                        *reinterpret_cast<float2 *>(p.seg_logdecay + (size_t)sgi * kD + cw) =
                             make_float2(bt0 * kLn2, bt1 * kLn2);
                 mbar_arrive(profinal);
             }
@@ -994,8 +998,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             if (!bad && pd < 128) {
                 ffinal[pd] = GATE == 0 ? 1.f : __expf(b_last + (GATE == 1 ? (float)(kC * m) * lg : 0.f));
-                if (SO && gok((size_t)blockIdx.x * kD + pd, p.n_seg_logdecay))
-                    p.seg_logdecay[(size_t)blockIdx.x * kD + pd] = b_total;
+                if (SO && gok((size_t)sgi * kD + pd, p.n_seg_logdecay))
+                    p.seg_logdecay[(size_t)sgi * kD + pd] = b_total;
                 mbar_arrive(profinal);
             }
         }
@@ -1105,7 +1109,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             tc_fence_before();
             mbar_arrive(sready);
         }
-        float *dst = SO ? p.seg_state + segblk : (p.nseg == 1 ? p.final_state : nullptr);
+        float *dst = SO ? p.seg_state + segblk : (seg == p.nseg - 1 ? p.final_state : nullptr);
         if (!SO && dst) dst += (size_t)bh * blk;
         if (dst && !gok((SO ? segblk : (size_t)bh * blk) + blk - 1, SO ? p.n_seg_state : p.n_final)) dst = nullptr;
         if (!bad && N > 0) {
@@ -1598,14 +1602,14 @@ bool make_map_f32(CUtensorMap *m, const void *base, int L, int BH) {
 }
 
 // Segment scan: S_in(0) = S_0 (the initial state, or 0), S_in(p+1) =
-// diag(e^{B_p}) S_in(p) + dS_p, and the state after the last segment is the
-// final state. One thread per state element (z included), a sequential loop
-// over the segments.
+// diag(e^{B_p}) S_in(p) + dS_p for every segment p but the last (the full
+// pass writes the final state). One thread per state element (z included), a
+// sequential loop over the segments.
 __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restrict__ seg_state,
                                                           const float *__restrict__ seg_logdecay,
                                                           const float *__restrict__ initial,
-                                                          float *__restrict__ state_in, float *final_state,
-                                                          int nseg, int blk, int value_side) {
+                                                          float *__restrict__ state_in, int nseg, int blk,
+                                                          int value_side) {
     // the full pass after this scan may start launching now: its CTAs set up
     // and begin their first chunks, and wait for this grid before reading the
     // carried states
@@ -1618,11 +1622,12 @@ __global__ void __launch_bounds__(256) la_seg_scan_kernel(const float *__restric
     const int d = e < kD * kD ? (value_side ? e % kD : e / kD) : e - kD * kD;
     const size_t base = (size_t)bh * nseg;
     float acc = initial ? initial[(size_t)bh * blk + e] : 0.f;
+    // the state carried into each segment; the last one's end state (the final
+    // state) comes from the full pass, so there is none to read for it
     for (int sgi = 0; sgi < nseg; ++sgi) {
         if (sgi > 0 || initial) state_in[(base + sgi) * blk + e] = acc;
-        acc = __expf(seg_logdecay[(base + sgi) * kD + d]) * acc + seg_state[(base + sgi) * blk + e];
+        if (sgi + 1 < nseg) acc = __expf(seg_logdecay[(base + sgi) * kD + d]) * acc + seg_state[(base + sgi) * blk + e];
     }
-    if (final_state) final_state[(size_t)bh * blk + e] = acc;
 }
 
 // after_scan: launched behind the segment scan as a programmatic dependent
@@ -1868,13 +1873,12 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.seg_logdecay = seg_logdecay;
     prm.n_seg_state = nsb * blk;
     prm.n_seg_logdecay = nsb * kD;
-    prm.final_state = nullptr;
-    prm.n_final = 0;
-    int rc = launch_mode<true>(prm, (int)nsb, s, a.mode, false, a.value_gate, false, a.reverse);
+    // the state-only pass: every segment but each sequence's last
+    int rc = launch_mode<true>(prm, BH * (prm.nseg - 1), s, a.mode, false, a.value_gate, false, a.reverse);
     if (rc != LA_OK) return rc;
     *launches += 1;
     la_seg_scan_kernel<<<dim3((unsigned)BH, (unsigned)((blk + 255) / 256)), 256, 0, s>>>(
-        seg_state, seg_logdecay, a.initial_state, state_in, a.final_state, prm.nseg, (int)blk, a.value_gate);
+        seg_state, seg_logdecay, a.initial_state, state_in, prm.nseg, (int)blk, a.value_gate);
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
     *launches += 1;
     prm.state_in = state_in;
