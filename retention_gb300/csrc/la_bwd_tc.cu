@@ -307,8 +307,8 @@ __global__ void __launch_bounds__(kEw) bwdg_postk_kernel(const uint4 *q, const u
     }
 }
 
-// chunk totals of r, then (one thread per sequence and channel group) the
-// sums over all later chunks, then dg = sigmoid(-g) / 16 (later chunks + the
+// chunk totals of r, then (one CTA per sequence and channel group) the sums
+// over all later chunks, then dg = sigmoid(-g) / 16 (later chunks + the
 // chunk's tail)
 __global__ void __launch_bounds__(kEw) bwdg_tot_kernel(const float *r, float *tot, long nbh, int L) {
     Grp G;
@@ -324,28 +324,55 @@ __global__ void __launch_bounds__(kEw) bwdg_tot_kernel(const float *r, float *to
     }
     st8f(tot + (size_t)x * 8, s);
 }
-__global__ void __launch_bounds__(kEw) bwdg_carry_kernel(float *tot, long nbh, int L) {
+// One CTA per (sequence, group of 8 channels): thread j takes a run of
+// consecutive chunks, the runs' totals are summed over the later runs (a suffix
+// scan across the warp by shuffles, then across the warps through shared
+// memory), and each thread walks its run from the last chunk, writing the sum
+// over all later chunks in place of each chunk's total.
+__global__ void __launch_bounds__(kEw) bwdg_carry_kernel(float *tot, int L) {
+    __shared__ float wt[kEw / 32][8];
     const int nch = (L + 63) / 64;
-    const long x = (long)blockIdx.x * kEw + threadIdx.x;
-    if (x >= nbh * CPR) return;
-    const long bh = x / CPR;
-    const int i0 = 8 * (int)(x % CPR);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // chunks from the last, four at a time: their loads go out together
-    for (int c1 = nch; c1 > 0; c1 -= 4) {
-        const int n4 = min(4, c1);
-        float v[4][8];
+    const long bh = blockIdx.x / CPR;
+    const int i0 = 8 * (int)(blockIdx.x % CPR), j = threadIdx.x, lane = j & 31, w = j >> 5;
+    const int per = (nch + kEw - 1) / kEw, c0 = min(nch, j * per), c1 = min(nch, c0 + per);
+    float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c = c0; c < c1; ++c) {
+        float v[8];
+        ld8f(tot + ((size_t)bh * nch + c) * kD + i0, v);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (j < n4) ld8f(tot + ((size_t)bh * nch + c1 - 1 - j) * kD + i0, v[j]);
+        for (int e = 0; e < 8; ++e) run[e] += v[e];
+    }
+    // inclusive suffix sums of the runs within the warp
+    float suf[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (j < n4) {
-                st8f(tot + ((size_t)bh * nch + c1 - 1 - j) * kD + i0, acc);  // the sum over later chunks
+    for (int e = 0; e < 8; ++e) suf[e] = run[e];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] += v[j][e];
-            }
+    for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float o = __shfl_down_sync(0xffffffffu, suf[e], off);
+            if (lane + off < 32) suf[e] += o;
         }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) wt[w][e] = suf[e];
+    }
+    __syncthreads();
+    // the sum over every later run: later lanes of this warp, then later warps
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        acc[e] = suf[e] - run[e];
+        for (int w2 = w + 1; w2 < kEw / 32; ++w2) acc[e] += wt[w2][e];
+    }
+    for (int c = c1 - 1; c >= c0; --c) {
+        float *p = tot + ((size_t)bh * nch + c) * kD + i0;
+        float v[8];
+        ld8f(p, v);
+        st8f(p, acc);  // the sum over later chunks
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += v[e];
     }
 }
 __global__ void __launch_bounds__(kEw) bwdg_dg_kernel(const float *r, const float *carry, const uint4 *g, uint4 *dg,
@@ -436,7 +463,7 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
         bwdg_tot_kernel<<<nbk, kEw, 0, s>>>(rf, tot, nbh, a.L);
         ok();
         if (rc == LA_OK) {
-            bwdg_carry_kernel<<<(unsigned)((nbh * CPR + kEw - 1) / kEw), kEw, 0, s>>>(tot, nbh, a.L);
+            bwdg_carry_kernel<<<(unsigned)(nbh * CPR), kEw, 0, s>>>(tot, a.L);
             ok();
         }
         if (rc == LA_OK) {

@@ -124,6 +124,13 @@ def test_bf16_gated_long_sequence():
     _check(cfg, seed=4)
 
 
+def test_bf16_gated_more_chunks_than_scan_threads():
+    """313 chunks: the gate gradient's carry scan gives each of its 256 threads
+    a run of two chunks (and some none), with a ragged last chunk."""
+    cfg = W.workload("gla", B=1, H=2, L=20000)
+    _check(cfg, seed=6, heads=1)
+
+
 @pytest.mark.parametrize("name", ["retention", "la"])
 def test_full_size_sampled_heads(name):
     """The full workload shapes on the GPU, the oracle on two heads of every
