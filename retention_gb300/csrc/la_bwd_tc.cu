@@ -83,12 +83,6 @@ __global__ void __launch_bounds__(kEw) bwd_dphi_kernel(const uint4 *q, const uin
 // fp32 and e_t travels as two bf16 parts (hi + lo).
 constexpr int CPR = kD / 8;  // 16-byte chunks per row
 
-__device__ __forceinline__ long rev_chunk(long x, int L) {
-    const long row = x / CPR;
-    const int c = (int)(x % CPR), t = (int)(row % L);
-    return (row - t + (L - 1 - t)) * CPR + c;
-}
-
 // Q = phi(q), K = phi(k) in order; the constant J
 __global__ void __launch_bounds__(kEw) bwdn_prep1_kernel(const uint4 *q, const uint4 *k, uint4 *Qf, uint4 *Kf,
                                                          uint4 *J, long rows, bool elu1) {
@@ -178,42 +172,16 @@ __global__ void __launch_bounds__(kEw) bwdn_post_kernel(const uint4 *q, const ui
 
 // ---------------------------------------------------------------- tensor-core route, per-channel gate
 // With the gate diag(alpha_t) on the key channels (B_t = sum_{r<=t} log alpha_r):
-//   dv_s    = sum_{t>=s} (Q_t . K_s e^{B_t - B_s}) dout_t        = rev fwd_key(rev K, rev Q, rev dout; g')
-//   dQ_t[i] = sum_{s<=t} e^{B_t[i] - B_s[i]} K_s[i] (dout_t . v_s)  = fwd_value(dout, v, K; g)
-//   dK_s[i] = sum_{t>=s} e^{B_t[i] - B_s[i]} Q_t[i] (v_s . dout_t)  = rev fwd_value(rev v, rev dout, rev Q; g')
+//   dv_s    = sum_{t>=s} (Q_t . K_s e^{B_t - B_s}) dout_t        = afwd_key(K, Q, dout)
+//   dQ_t[i] = sum_{s<=t} e^{B_t[i] - B_s[i]} K_s[i] (dout_t . v_s)  = fwd_value(dout, v, K)
+//   dK_s[i] = sum_{t>=s} e^{B_t[i] - B_s[i]} Q_t[i] (v_s . dout_t)  = afwd_value(v, dout, Q)
 // fwd_value is the forward with the decay on the value channels (the kernel
 // writes it without the factor e^{b_t}, b the log decay since the chunk start,
-// which the passes after apply). g' is g reversed and shifted by one token
-// (g'_u = g_{L-u}; g'_0 decays nothing), so the reversed forwards take the
-// same gate products. Then dg_r = sigmoid(-g_r) / 16 sum_{t>=r} (Q dQ - K dK)_t
-// by a segmented reverse scan over chunks of 64 tokens.
-constexpr float kNoDecay = 3.0e38f;  // a gate value whose alpha is 1
-
-// K = phi(k) in order; rev v, rev dout, rev phi(q), rev phi(k), and g'
-__global__ void __launch_bounds__(kEw) bwdg_prep_kernel(const uint4 *q, const uint4 *k, const uint4 *v, const uint4 *d,
-                                                        const uint4 *g, uint4 *Kf, uint4 *rv, uint4 *rd, uint4 *rq,
-                                                        uint4 *rk, uint4 *rg, long rows, int L, bool elu1) {
-    const long n = rows * CPR;
-    for (long x = (long)blockIdx.x * kEw + threadIdx.x; x < n; x += (long)gridDim.x * kEw) {
-        const long row = x / CPR;
-        const int c = (int)(x % CPR), t = (int)(row % L);
-        const long rr = rev_chunk(x, L);
-        const uint4 kk = phi8(__ldcs(k + x), elu1);
-        Kf[x] = kk;
-        rk[rr] = kk;
-        rq[rr] = phi8(__ldcs(q + x), elu1);
-        rv[rr] = __ldcs(v + x);
-        rd[rr] = __ldcs(d + x);
-        // g at token t goes to reversed token L - t; reversed token 0 decays nothing
-        const long base = (row - t) * CPR;
-        if (t >= 1) rg[base + (long)(L - t) * CPR + c] = __ldcs(g + x);
-        else {
-            __nv_bfloat162 h = __floats2bfloat162_rn(kNoDecay, kNoDecay);
-            const uint32_t w = *reinterpret_cast<uint32_t *>(&h);
-            rg[base + c] = make_uint4(w, w, w, w);
-        }
-    }
-}
+// which the passes after apply); afwd is the anti-causal instance, whose
+// mirrored sequence decays token t by the gate of token t + 1, so its products
+// are the same gate products. With elu+1 each forward applies the feature map
+// itself (the value-side ones to their value tile). Then dg_r = sigmoid(-g_r) / 16 sum_{t>=r} (Q dQ -
+// K dK)_t by a segmented reverse scan over chunks of 64 tokens.
 
 // The passes below take one thread per (sequence, chunk of 64 tokens, group
 // of 8 channels) and walk the chunk's tokens: 16-byte loads of bf16 rows
@@ -277,33 +245,35 @@ __global__ void __launch_bounds__(kEw) bwdg_postq_kernel(const uint4 *q, const u
     }
 }
 
-// dK (reversed chunks of 64 from reversed token 0, gate g'), un-reversed:
-// dk = dK phi'(k); dv un-reversed; r = phi(q) dQ - phi(k) dK in place of dQ
-__global__ void __launch_bounds__(kEw) bwdg_postk_kernel(const uint4 *q, const uint4 *k, const uint4 *rg,
-                                                         const uint4 *rbr, const uint4 *rdv, uint4 *dk, uint4 *dv,
-                                                         float *r, long nbh, int L, bool elu1) {
+// dK in order from the anti-causal value-side forward: dK_t = e^{b_t} bracket_t,
+// b_t the sum of log alpha(g_{t'+1}) over t' = t .. the last token of t's chunk
+// (the sequence's last token decays nothing), so each thread walks its chunk
+// from the end; dk = dK phi'(k); r = phi(q) dQ - phi(k) dK in place of dQ
+__global__ void __launch_bounds__(kEw) bwdg_postk_kernel(const uint4 *q, const uint4 *k, const uint4 *g,
+                                                         const uint4 *brk, uint4 *dk, float *r, long nbh, int L,
+                                                         bool elu1) {
     Grp G;
     if (!grp_of((long)blockIdx.x * kEw + threadIdx.x, nbh, L, G)) return;
     float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
-    for (int u = 64 * G.c; u < min(L, 64 * G.c + 64); ++u) {
-        const size_t ou = ((size_t)G.bh * L + u) * kD + G.i0, ot = ((size_t)G.bh * L + (L - 1 - u)) * kD + G.i0;
+    for (int t = min(L, 64 * G.c + 64) - 1; t >= 64 * G.c; --t) {
+        const size_t o = ((size_t)G.bh * L + t) * kD + G.i0;
         float gv[8], bv[8], kv[8], qv[8], rv[8], outk[8];
-        unpack8(__ldcs(rg + ou / 8), gv);
-        unpack8(__ldcs(rbr + ou / 8), bv);
-        unpack8(__ldg(k + ot / 8), kv);
-        unpack8(__ldg(q + ot / 8), qv);
-        ld8f(r + ot, rv);
+        const bool decays = t + 1 < L;
+        if (decays) unpack8(__ldcs(g + o / 8 + CPR), gv);  // the next token's gate
+        unpack8(__ldcs(brk + o / 8), bv);
+        unpack8(__ldg(k + o / 8), kv);
+        unpack8(__ldg(q + o / 8), qv);
+        ld8f(r + o, rv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            b[e] += channel_log_decay(gv[e]);
+            if (decays) b[e] += channel_log_decay(gv[e]);
             const float dK = __expf(b[e]) * bv[e];
             outk[e] = dK * dphi(kv[e], elu1);
             rv[e] = phi(qv[e], elu1) * rv[e] - phi(kv[e], elu1) * dK;
         }
-        dk[ot / 8] = pack8(outk);
-        dv[ot / 8] = __ldcs(rdv + ou / 8);
-        st8f(r + ot, rv);
+        dk[o / 8] = pack8(outk);
+        st8f(r + o, rv);
     }
 }
 
@@ -419,33 +389,30 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
     const long nbh = (long)a.B * a.H, rows = nbh * a.L;
     const int nch = (a.L + 63) / 64;
     const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16);
-    // bf16: K rv rd rq rk g' bracket_q bracket_k rdv; fp32: dQ / r; chunk totals
-    const size_t bytes = 9 * hb + 2 * hb + (size_t)nbh * nch * kD * sizeof(float);
+    const bool elu1 = a.mode & LA_PHI_ELU1;
+    // bf16: bracket_q bracket_k; fp32: dQ / r; chunk totals
+    const size_t bytes = 2 * hb + 2 * hb + (size_t)nbh * nch * kD * sizeof(float);
     void *scratch = nullptr;
     if (scratch_alloc(&scratch, bytes, s) != LA_OK) return LA_ERR_CUDA;
     char *b = static_cast<char *>(scratch);
-    uint4 *h[9];
-    for (int i = 0; i < 9; ++i) h[i] = reinterpret_cast<uint4 *>(b + i * hb);
-    uint4 *Kf = h[0], *rv = h[1], *rd = h[2], *rq = h[3], *rk = h[4], *rg = h[5], *brq = h[6], *brk = h[7], *rdv = h[8];
-    float *rf = reinterpret_cast<float *>(b + 9 * hb), *tot = reinterpret_cast<float *>(b + 11 * hb);
-    const bool elu1 = a.mode & LA_PHI_ELU1;
+    uint4 *brq = reinterpret_cast<uint4 *>(b), *brk = reinterpret_cast<uint4 *>(b + hb);
+    float *rf = reinterpret_cast<float *>(b + 2 * hb), *tot = reinterpret_cast<float *>(b + 4 * hb);
     int rc = LA_OK;
     auto ok = [&]() {
         if (rc == LA_OK && cudaGetLastError() != cudaSuccess) rc = LA_ERR_CUDA;
         if (rc == LA_OK) ++*launches;
     };
-    auto fwd = [&](const void *q, const void *k, const void *v, const void *g, void *out, bool value_side) {
+    // the feature map runs inside each forward: on the value tile (value side)
+    // or on q and k
+    auto fwd = [&](const void *q, const void *k, const void *v, void *out, bool value_side, bool anti) {
         if (rc != LA_OK) return;
-        ChunkArgs c{q, k, v, g, out, nullptr, a.B, a.H, a.L, kD, kD, LA_GATE_CHANNEL, 64, nullptr, 0, value_side ? 1 : 0};
+        ChunkArgs c{q, k, v, a.gate, out, nullptr, a.B, a.H, a.L, kD, kD, LA_GATE_CHANNEL | (elu1 ? LA_PHI_ELU1 : 0),
+                    64, nullptr, 0, value_side ? 1 : 0, anti ? 1 : 0};
         rc = launch_chunk_tc(c, s, launches);
     };
-    bwdg_prep_kernel<<<ew_blocks(rows * CPR), kEw, 0, s>>>(
-        static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), static_cast<const uint4 *>(a.v),
-        static_cast<const uint4 *>(a.dout), static_cast<const uint4 *>(a.gate), Kf, rv, rd, rq, rk, rg, rows, a.L, elu1);
-    ok();
-    fwd(a.dout, a.v, Kf, a.gate, brq, true);  // dQ without e^{b_t}
-    fwd(rv, rd, rq, rg, brk, true);           // reversed dK without e^{b'_u}
-    fwd(rk, rq, rd, rg, rdv, false);          // reversed dv
+    fwd(a.dout, a.v, a.k, brq, true, false);  // dQ without e^{b_t}; values phi(k)
+    fwd(a.v, a.dout, a.q, brk, true, true);   // dK without e^{b_t}; values phi(q)
+    fwd(a.k, a.q, a.dout, a.grad_v, false, true);  // dv: phi(k) . phi(q)
     const long nt = nbh * nch * CPR;  // (sequence, chunk, channel group) threads
     const unsigned nbk = (unsigned)((nt + kEw - 1) / kEw);
     if (rc == LA_OK) {
@@ -454,9 +421,9 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
         ok();
     }
     if (rc == LA_OK) {
-        bwdg_postk_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k), rg, brk,
-                                              rdv, static_cast<uint4 *>(a.grad_k), static_cast<uint4 *>(a.grad_v), rf,
-                                              nbh, a.L, elu1);
+        bwdg_postk_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
+                                              static_cast<const uint4 *>(a.gate), brk,
+                                              static_cast<uint4 *>(a.grad_k), rf, nbh, a.L, elu1);
         ok();
     }
     if (rc == LA_OK && a.grad_g) {

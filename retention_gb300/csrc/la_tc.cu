@@ -325,8 +325,11 @@ __device__ __forceinline__ uint32_t dphi_elu1_bf16x2(uint32_t x) {
 template <int GATE, bool ELU1, bool NORM, bool SO, bool OF32 = false, bool REV = false, int EPI = 0, int BIAS = 0>
 __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_constant__ TcParams p) {
     using LY = Layout<GATE, NORM, SO, OF32, EPI, BIAS>;
-    static_assert(GATE != 3 || (!ELU1 && !NORM), "the value-side gate takes features as given, no normaliser");
-    static_assert(!REV || (GATE <= 1 && !NORM && (!ELU1 || GATE == 0)), "the anti-causal instance: scalar decay");
+    // (the value-side gate: with ELU1 the feature map applies to the value tile,
+    // the one its prologue scales, and q and k are taken as given)
+    static_assert(GATE != 3 || !NORM, "the value-side gate: no normaliser");
+    static_assert(!REV || (GATE <= 1 && !NORM && (!ELU1 || GATE == 0)) || (GATE >= 2 && !NORM && !OF32),
+                  "the anti-causal instance: a scalar decay, or the channel gate");
     static_assert(EPI != 1 || (GATE <= 1 && !NORM && !SO && !OF32 && !REV), "the fused epilogue: bf16 output, no normaliser");
     static_assert(EPI != 2 || (GATE == 0 && NORM && !SO && !OF32 && !REV), "the backward prep: the normalised causal form");
     static_assert(BIAS == 0 || (GATE == 0 && !NORM && !SO && !OF32 && EPI == 0 && REV == (BIAS == 2)),
@@ -367,6 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     const int N = max(0, min(p.seg_chunks, nch - c0));
     // first token of the n-th chunk this CTA takes (from the end with REV)
     auto chunk_t0 = [&](int n) { return (REV ? nch - 1 - (c0 + n) : c0 + n) * kC; };
+    // first row of the gate tile of the chunk at t0: with REV and the channel
+    // gate, token t of the mirrored sequence decays by the gate of token t + 1
+    // (a tile wholly past the end is never read: every row of it is masked)
+    auto gy = [&](int t0) { return (REV && GATE >= 2) ? min(t0 + 1, L - 1) : t0; };
     const bool init = !SO && p.state_in != nullptr && (seg > 0 || p.init0);  // start from a carried state
     const size_t blk = (size_t)kD * kD + (NORM ? kD : 0);
     const size_t segblk = (size_t)sgi * blk;
@@ -546,8 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     }
                     uint8_t *dst = sm + LY::Gring + sg * kTile;
                     mbar_arrive_expect_tx(&gfull[sg], kTile);
-                    tload(dst, &p.tg, &gfull[sg], 0, t0);
-                    tload(dst + kHalf, &p.tg, &gfull[sg], 64, t0);
+                    tload(dst, &p.tg, &gfull[sg], 0, gy(t0));
+                    tload(dst + kHalf, &p.tg, &gfull[sg], 64, gy(t0));
                     gissued = n + 1;
                 }
                 if (n >= NS && !mbar_wait(&empty[s], (uint32_t)(n / NS - 1) & 1u, wait_ns)) {
@@ -558,8 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll 1
                 for (int tl = SO ? 1 : 0; tl < ntl; ++tl) {
                     const CUtensorMap *m = tl == 0 ? &p.tq : tl == 1 ? &p.tk : tl == 2 ? &p.tv : &p.tg;
-                    tload(sm + tile_half(tl, s, 0), m, &full[s], 0, t0);
-                    tload(sm + tile_half(tl, s, 1), m, &full[s], 64, t0);
+                    const int y = tl == 3 ? gy(t0) : t0;
+                    tload(sm + tile_half(tl, s, 0), m, &full[s], 0, y);
+                    tload(sm + tile_half(tl, s, 1), m, &full[s], 64, y);
                 }
                 issued = n + 1;
             }
@@ -716,15 +724,27 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             // their (zero-filled) q; their k is zeroed only with the normaliser
             // (elsewhere their zero v rows cancel them). Quarter 3 ends at the
             // chunk's total decay and writes the state factors.
+            // REV (the anti-causal form): the mirrored sequence's cumulative decay
+            // is a suffix sum over the chunk's rows, of the gate of the next token
+            // (the tile starts a row later; the sequence's last token decays
+            // nothing). Step u of a quarter takes row 15 - u, the quarter sums are
+            // taken over the quarters above, and quarter 0 ends at the total.
             const int ch = pw & 1, qr = pw >> 1;
             const int cw = 64 * ch + 2 * lane;  // first of the thread's two channels
             const uint32_t colw = (lane & 3) << 2, slot = lane >> 2;  // within the block of half ch
-            auto offw = [&](int u) { return colw + (16 * qr + u) * 128 + (((slot ^ u) & 7) << 4); };
+            constexpr int kLastQ = REV ? 0 : 3;
+            auto rowu = [&](int u) { return REV ? 15 - u : u; };  // row of step u within the quarter
+            auto offw = [&](int u) {
+                const int r = rowu(u);
+                return colw + (16 * qr + r) * 128 + (((slot ^ r) & 7) << 4);
+            };
             // log2 decay of the two channels over the previous chunk and over the
             // segment so far (kept by quarter 3)
             float bl0 = 0.f, bl1 = 0.f, bt0 = 0.f, bt1 = 0.f;
             for (int n = 0; n < N; ++n) {
                 const int s = n % NS, t0 = chunk_t0(n), c = min(kC, L - t0);
+                // rows whose gate is read (REV: not the sequence's last token)
+                const int cg = (REV && t0 + c >= L) ? c - 1 : c;
                 // the gate tile first: from its own ring (full pass) or from the stage.
                 // Without the normaliser no barrier follows: the quarter sums are
                 // double-buffered, so a warp may start this chunk while others finish
@@ -747,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 f32x2_t la[16], sq = f2(0.f, 0.f);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const uint32_t w = 16 * qr + u < c ? ld4(sG + offw(u)) : 0x7F7F7F7Fu;
+                    const uint32_t w = 16 * qr + rowu(u) < cg ? ld4(sG + offw(u)) : 0x7F7F7F7Fu;
                     la[u] = log2_alpha2(w);
                     sq = f2_add(sq, la[u]);
                 }
@@ -770,7 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                     break;
                 }
                 f32x2_t bb = f2(0.f, 0.f);
-                for (int r = 0; r < qr; ++r) bb = f2_add(bb, *reinterpret_cast<const f32x2_t *>(totn + r * 128 + cw));
+                for (int r = REV ? qr + 1 : 0; r < (REV ? 4 : qr); ++r)
+                    bb = f2_add(bb, *reinterpret_cast<const f32x2_t *>(totn + r * 128 + cw));
                 float b0, b1;
                 // pass 2 in two groups of eight rows; the second group's words are
                 // loaded before the first group's results are stored. The group
@@ -802,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         ko[u] = mul_bf16x2(kx, pack_bf16(ex2f(-b0), ex2f(-b1)));
                         // rows past the end: their v rows are zero, which cancels
                         // them everywhere but in the ones column of the normaliser
-                        if (NORM && 16 * qr + uu >= c) ko[u] = 0u;
+                        if (NORM && 16 * qr + rowu(uu) >= c) ko[u] = 0u;
                         if (!SO && GATE == 2) {
                             uint32_t qx = qw[u];
                             if (ELU1) qx = phi_elu1_bf16x2(qx);
@@ -818,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                         la[u] = la[u + 8];
                     }
                 }
-                if (qr == 3) {
+                if (qr == kLastQ) {
                     bl0 = b0;
                     bl1 = b1;
                     bt0 += b0;
@@ -829,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 fence_proxy_async_smem();
                 mbar_arrive(&pro[s]);
             }
-            if (!bad && qr == 3) {
+            if (!bad && qr == kLastQ) {
                 *reinterpret_cast<float2 *>(ffinal + cw) = make_float2(ex2f(bl0), ex2f(bl1));
                 if (SO)
                     if (gok((size_t)sgi * kD + cw + 1, p.n_seg_logdecay))
@@ -1174,8 +1195,8 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int jj = q8 * 8 + 2 * e;
-                            u[e] = pack_bf16(jj <= t ? __uint_as_float(a[2 * e]) : 0.f,
-                                             jj + 1 <= t ? __uint_as_float(a[2 * e + 1]) : 0.f);
+                            u[e] = pack_bf16(keep(jj) ? __uint_as_float(a[2 * e]) : 0.f,
+                                             keep(jj + 1) ? __uint_as_float(a[2 * e + 1]) : 0.f);
                         }
                         st16(prow + (((q8 ^ t) & 7) << 4), make_uint4(u[0], u[1], u[2], u[3]));
                     }
@@ -1694,9 +1715,26 @@ int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool ou
                     : launch_t<0, false, false, false, false, false, 1>(prm, grid, s, pdl);
     }
     if (rev) {
-        // anti-causal: no normaliser; no gate (with either feature map) or the head
-        // gate (identity feature map)
-        if (norm || value_gate || (mode & LA_GATE_CHANNEL)) return LA_ERR_INTERNAL;
+        // anti-causal: no normaliser; no gate (with either feature map), the head
+        // gate or the channel gate (identity feature map; the channel gate also
+        // on the value side)
+        if (norm) return LA_ERR_INTERNAL;
+        if (mode & LA_GATE_CHANNEL) {
+            if (out_f32) return LA_ERR_INTERNAL;
+            if (value_gate) {
+                if (elu1)
+                    return SO ? launch_t<3, true, false, true, false, true>(prm, grid, s, pdl)
+                              : launch_t<3, true, false, false, false, true>(prm, grid, s, pdl);
+                return SO ? launch_t<3, false, false, true, false, true>(prm, grid, s, pdl)
+                          : launch_t<3, false, false, false, false, true>(prm, grid, s, pdl);
+            }
+            if (elu1)
+                return SO ? launch_t<2, true, false, true, false, true>(prm, grid, s, pdl)
+                          : launch_t<2, true, false, false, false, true>(prm, grid, s, pdl);
+            return SO ? launch_t<2, false, false, true, false, true>(prm, grid, s, pdl)
+                      : launch_t<2, false, false, false, false, true>(prm, grid, s, pdl);
+        }
+        if (value_gate) return LA_ERR_INTERNAL;
         const bool gh = mode & LA_GATE_HEAD;
         if (elu1) {
             if (gh || out_f32) return LA_ERR_INTERNAL;
@@ -1713,9 +1751,11 @@ int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool ou
                   : launch_t<0, false, false, false, false, true>(prm, grid, s, pdl);
     }
     if (value_gate) {
-        // the per-channel gate on the value side: identity feature map, no
-        // normaliser, bf16 output
-        if (elu1 || norm || !(mode & LA_GATE_CHANNEL) || out_f32) return LA_ERR_INTERNAL;
+        // the per-channel gate on the value side: no normaliser, bf16 output; with
+        // elu+1 the feature map applies to the value tile alone
+        if (norm || !(mode & LA_GATE_CHANNEL) || out_f32) return LA_ERR_INTERNAL;
+        if (elu1)
+            return SO ? launch_t<3, true, false, true>(prm, grid, s, pdl) : launch_t<3, true, false, false>(prm, grid, s, pdl);
         return SO ? launch_t<3, false, false, true>(prm, grid, s, pdl) : launch_t<3, false, false, false>(prm, grid, s, pdl);
     }
     if (out_f32 && !SO) {
