@@ -221,79 +221,60 @@ __device__ __forceinline__ void st8f(float *p, const float (&f)[8]) {
     reinterpret_cast<float4 *>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
-// dQ_t = e^{b_t} * bracket_t (chunks of 64 from token 0); dq = dQ phi'(q); dQ kept (fp32) for dg
-__global__ void __launch_bounds__(kEw) bwdg_postq_kernel(const uint4 *q, const uint4 *g, const uint4 *br, uint4 *dq,
-                                                         float *dQ, long nbh, int L, bool elu1) {
-    Grp G;
-    if (!grp_of((long)blockIdx.x * kEw + threadIdx.x, nbh, L, G)) return;
-    float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int t = 64 * G.c; t < min(L, 64 * G.c + 64); ++t) {
-        const size_t o = ((size_t)G.bh * L + t) * kD + G.i0;
-        float gv[8], bv[8], qv[8], out[8], d[8];
-        unpack8(__ldcs(g + o / 8), gv);
-        unpack8(__ldcs(br + o / 8), bv);
-        unpack8(__ldg(q + o / 8), qv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            b[e] += channel_log_decay(gv[e]);
-            d[e] = __expf(b[e]) * bv[e];
-            out[e] = d[e] * dphi(qv[e], elu1);
-        }
-        st8f(dQ + o, d);
-        dq[o / 8] = pack8(out);
-    }
-}
-
-// dK in order from the anti-causal value-side forward: dK_t = e^{b_t} bracket_t,
-// b_t the sum of log alpha(g_{t'+1}) over t' = t .. the last token of t's chunk
-// (the sequence's last token decays nothing), so each thread walks its chunk
-// from the end; dk = dK phi'(k); r = phi(q) dQ - phi(k) dK in place of dQ
-__global__ void __launch_bounds__(kEw) bwdg_postk_kernel(const uint4 *q, const uint4 *k, const uint4 *g,
-                                                         const uint4 *brk, uint4 *dk, float *r, long nbh, int L,
-                                                         bool elu1) {
-    Grp G;
-    if (!grp_of((long)blockIdx.x * kEw + threadIdx.x, nbh, L, G)) return;
-    float b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int t = min(L, 64 * G.c + 64) - 1; t >= 64 * G.c; --t) {
-        const size_t o = ((size_t)G.bh * L + t) * kD + G.i0;
-        float gv[8], bv[8], kv[8], qv[8], rv[8], outk[8];
-        const bool decays = t + 1 < L;
-        if (decays) unpack8(__ldcs(g + o / 8 + CPR), gv);  // the next token's gate
-        unpack8(__ldcs(brk + o / 8), bv);
-        unpack8(__ldg(k + o / 8), kv);
-        unpack8(__ldg(q + o / 8), qv);
-        ld8f(r + o, rv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            if (decays) b[e] += channel_log_decay(gv[e]);
-            const float dK = __expf(b[e]) * bv[e];
-            outk[e] = dK * dphi(kv[e], elu1);
-            rv[e] = phi(qv[e], elu1) * rv[e] - phi(kv[e], elu1) * dK;
-        }
-        dk[o / 8] = pack8(outk);
-        st8f(r + o, rv);
-    }
-}
-
-// chunk totals of r, then (one CTA per sequence and channel group) the sums
-// over all later chunks, then dg = sigmoid(-g) / 16 (later chunks + the
-// chunk's tail)
-__global__ void __launch_bounds__(kEw) bwdg_tot_kernel(const float *r, float *tot, long nbh, int L) {
+// One pass over the two brackets, a thread per (sequence, chunk of 64 tokens,
+// group of 8 channels). With P_t the sum of log alpha(g_t') over t' = chunk
+// start .. t (the causal decay since the chunk start) and A the same sum up to
+// the chunk's last token's successor (the sequence's last token decays
+// nothing), the anti-causal decay to the chunk's end is A - P_t, so:
+//   dQ_t = e^{P_t} bracket_q,t      dK_t = e^{A - P_t} bracket_k,t
+//   dq = dQ phi'(q), dk = dK phi'(k), r_t = phi(q) dQ - phi(k) dK (fp32)
+// and the chunk's total of r (r and the totals only when `r` is given). The
+// first walk sums A over the chunk's gates (the second finds them in L2).
+__global__ void __launch_bounds__(kEw) bwdg_post_kernel(const uint4 *q, const uint4 *k, const uint4 *g,
+                                                        const uint4 *brq, const uint4 *brk, uint4 *dq, uint4 *dk,
+                                                        float *r, float *tot, long nbh, int L, bool elu1) {
     Grp G;
     const long x = (long)blockIdx.x * kEw + threadIdx.x;
     if (!grp_of(x, nbh, L, G)) return;
-    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const int t0 = 64 * G.c, t1 = min(L, t0 + 64), umax = min(t1, L - 1);
+    const size_t base = ((size_t)G.bh * L) * kD + G.i0;
+    float A[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-    for (int t = 64 * G.c; t < min(L, 64 * G.c + 64); ++t) {
-        float v[8];
-        ld8f(r + ((size_t)G.bh * L + t) * kD + G.i0, v);
+    for (int t = t0; t <= umax; ++t) {
+        float gv[8];
+        unpack8(__ldg(g + (base + (size_t)t * kD) / 8), gv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s[e] += v[e];
+        for (int e = 0; e < 8; ++e) A[e] += channel_log_decay(gv[e]);
     }
-    st8f(tot + (size_t)x * 8, s);
+    float P[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int t = t0; t < t1; ++t) {
+        const size_t o = base + (size_t)t * kD;
+        float gv[8], bq[8], bk[8], qv[8], kv[8], rv[8], oq[8], ok[8];
+        unpack8(__ldcs(g + o / 8), gv);
+        unpack8(__ldcs(brq + o / 8), bq);
+        unpack8(__ldcs(brk + o / 8), bk);
+        unpack8(__ldg(q + o / 8), qv);
+        unpack8(__ldg(k + o / 8), kv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            P[e] += channel_log_decay(gv[e]);
+            const float dQ = __expf(P[e]) * bq[e], dK = __expf(A[e] - P[e]) * bk[e];
+            oq[e] = dQ * dphi(qv[e], elu1);
+            ok[e] = dK * dphi(kv[e], elu1);
+            rv[e] = phi(qv[e], elu1) * dQ - phi(kv[e], elu1) * dK;
+            rs[e] += rv[e];
+        }
+        dq[o / 8] = pack8(oq);
+        dk[o / 8] = pack8(ok);
+        if (r) st8f(r + o, rv);
+    }
+    if (tot) st8f(tot + (size_t)x * 8, rs);
 }
+
+// The chunk totals of r (from the pass above), then (one CTA per sequence and
+// channel group) the sums over all later chunks, then dg = sigmoid(-g) / 16
+// (later chunks + the chunk's tail).
 // One CTA per (sequence, group of 8 channels): thread j takes a run of
 // consecutive chunks, the runs' totals are summed over the later runs (a suffix
 // scan across the warp by shuffles, then across the warps through shared
@@ -390,7 +371,7 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
     const int nch = (a.L + 63) / 64;
     const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16);
     const bool elu1 = a.mode & LA_PHI_ELU1;
-    // bf16: bracket_q bracket_k; fp32: dQ / r; chunk totals
+    // bf16: bracket_q bracket_k; fp32: r; chunk totals
     const size_t bytes = 2 * hb + 2 * hb + (size_t)nbh * nch * kD * sizeof(float);
     void *scratch = nullptr;
     if (scratch_alloc(&scratch, bytes, s) != LA_OK) return LA_ERR_CUDA;
@@ -416,23 +397,17 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
     const long nt = nbh * nch * CPR;  // (sequence, chunk, channel group) threads
     const unsigned nbk = (unsigned)((nt + kEw - 1) / kEw);
     if (rc == LA_OK) {
-        bwdg_postq_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.gate), brq,
-                                              static_cast<uint4 *>(a.grad_q), rf, nbh, a.L, elu1);
-        ok();
-    }
-    if (rc == LA_OK) {
-        bwdg_postk_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
-                                              static_cast<const uint4 *>(a.gate), brk,
-                                              static_cast<uint4 *>(a.grad_k), rf, nbh, a.L, elu1);
+        // (r and the chunk totals only when the gate gradient is wanted)
+        const bool want_dg = a.grad_g != nullptr;
+        bwdg_post_kernel<<<nbk, kEw, 0, s>>>(static_cast<const uint4 *>(a.q), static_cast<const uint4 *>(a.k),
+                                             static_cast<const uint4 *>(a.gate), brq, brk,
+                                             static_cast<uint4 *>(a.grad_q), static_cast<uint4 *>(a.grad_k),
+                                             want_dg ? rf : nullptr, want_dg ? tot : nullptr, nbh, a.L, elu1);
         ok();
     }
     if (rc == LA_OK && a.grad_g) {
-        bwdg_tot_kernel<<<nbk, kEw, 0, s>>>(rf, tot, nbh, a.L);
+        bwdg_carry_kernel<<<(unsigned)(nbh * CPR), kEw, 0, s>>>(tot, a.L);
         ok();
-        if (rc == LA_OK) {
-            bwdg_carry_kernel<<<(unsigned)(nbh * CPR), kEw, 0, s>>>(tot, a.L);
-            ok();
-        }
         if (rc == LA_OK) {
             bwdg_dg_kernel<<<nbk, kEw, 0, s>>>(rf, tot, static_cast<const uint4 *>(a.gate),
                                                static_cast<uint4 *>(a.grad_g), nbh, a.L);
