@@ -12,14 +12,30 @@
 // where afwd is the anti-causal instance of the forward kernel (the sum over the
 // token and every later one, chunks taken from the end), run on the arrays in
 // their own order. The normaliser and the per-channel gate add the terms
-// described above their routes below; the per-channel gate still runs its
-// anti-causal sums as causal forwards of token-reversed copies.
+// described above their routes below.
 #include "la_common.cuh"
 
 namespace la {
 namespace {
 
-__device__ __forceinline__ float dphi(float x, bool elu1) { return (elu1 && x <= 0.f) ? __expf(x) : 1.f; }
+// The hardware base-2 exponential and logarithm (denormals flushed), for the
+// gated pass after the forwards, which works in log2 units as the forward
+// kernel's gate arithmetic does.
+__device__ __forceinline__ float hw_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float hw_lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+// log2 alpha = log2(sigmoid(g)) / 16 = (min(g, 0) log2 e - log2(1 + 2^(-|g| log2 e))) / 16
+__device__ __forceinline__ float log2_alpha(float g) {
+    return (fminf(g, 0.f) * kLog2e - hw_lg2(1.f + hw_ex2(-fabsf(g) * kLog2e))) * 0.0625f;
+}
 
 // ---------------------------------------------------------------- scalar gate, no normaliser
 // With the identity feature map the three forwards read the caller's arrays and
@@ -238,13 +254,14 @@ __global__ void __launch_bounds__(kEw) bwdg_post_kernel(const uint4 *q, const ui
     if (!grp_of(x, nbh, L, G)) return;
     const int t0 = 64 * G.c, t1 = min(L, t0 + 64), umax = min(t1, L - 1);
     const size_t base = ((size_t)G.bh * L) * kD + G.i0;
+    // (log2 units throughout)
     float A[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int t = t0; t <= umax; ++t) {
         float gv[8];
         unpack8(__ldg(g + (base + (size_t)t * kD) / 8), gv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) A[e] += channel_log_decay(gv[e]);
+        for (int e = 0; e < 8; ++e) A[e] += log2_alpha(gv[e]);
     }
     float P[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
@@ -258,11 +275,20 @@ __global__ void __launch_bounds__(kEw) bwdg_post_kernel(const uint4 *q, const ui
         unpack8(__ldg(k + o / 8), kv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            P[e] += channel_log_decay(gv[e]);
-            const float dQ = __expf(P[e]) * bq[e], dK = __expf(A[e] - P[e]) * bk[e];
-            oq[e] = dQ * dphi(qv[e], elu1);
-            ok[e] = dK * dphi(kv[e], elu1);
-            rv[e] = phi(qv[e], elu1) * dQ - phi(kv[e], elu1) * dK;
+            P[e] += log2_alpha(gv[e]);
+            const float dQ = hw_ex2(P[e]) * bq[e], dK = hw_ex2(A[e] - P[e]) * bk[e];
+            // phi and phi' from one exponential each: e^min(x, 0)
+            float pq = qv[e], dpq = 1.f, pk = kv[e], dpk = 1.f;
+            if (elu1) {
+                const float eq = hw_ex2(fminf(qv[e], 0.f) * kLog2e), ek = hw_ex2(fminf(kv[e], 0.f) * kLog2e);
+                pq = qv[e] > 0.f ? qv[e] + 1.f : eq;
+                dpq = qv[e] > 0.f ? 1.f : eq;
+                pk = kv[e] > 0.f ? kv[e] + 1.f : ek;
+                dpk = kv[e] > 0.f ? 1.f : ek;
+            }
+            oq[e] = dQ * dpq;
+            ok[e] = dK * dpk;
+            rv[e] = pq * dQ - pk * dK;
             rs[e] += rv[e];
         }
         dq[o / 8] = pack8(oq);
