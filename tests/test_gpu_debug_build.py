@@ -6,8 +6,8 @@ quarter) and global index of the tensor-core forward and the decode step
 against its extent before using it; a failed check skips the access and makes
 la_device_status return LA_ERR_INTERNAL. Here that build runs the forward in
 every mode (split and unsplit, ragged), the anti-causal form, the fused RetNet
-epilogue, the forward from a state and the decode step, each matched against
-the oracle, and no check may fail. It stands in for a memory checker, which is
+epilogue, the forward from a state, the decode step and the backward's
+instances, each matched against the oracle, and no check may fail. It stands in for a memory checker, which is
 not available on these GPUs.
 """
 import pytest
@@ -99,3 +99,15 @@ def test_decode_step(checked, m, dk, dv):
                          gate_kind=m["gate"])
     torch.cuda.synchronize()
     _parity(out.float().cpu().numpy(), state.cpu().numpy(), ref, ref_state)
+
+
+@pytest.mark.parametrize("name,B,H,L", [("la", 2, 40, 333), ("gla", 1, 2, 1000), ("gla", 2, 40, 200),
+                                        ("retention", 1, 4, 1000)],
+                         ids=["normalised-unsplit", "gated-split", "gated-unsplit", "retention-split"])
+def test_backward(checked, name, B, H, L):
+    """The backward's forward instances: the backward-prep and bias instances
+    (normalised), the anti-causal gated and value-side instances (gated), the
+    anti-causal scalar-decay instance (retention)."""
+    from test_gpu_bwd import _check
+    _check(W.workload(name, B=B, H=H, L=L), seed=45)
+    assert la.device_status() == 0  # no bounds check failed
