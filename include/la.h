@@ -98,10 +98,14 @@ typedef enum {
  * from the end of the sequence towards its start (final_state is then the state
  * before token 0; an initial state of la_chunk_fwd_from_state sits after the
  * last token). It equals the causal forward of the token-reversed sequence. The
- * backward pass is built from such sums. Tensor-core kernel only: bf16,
- * d_k = d_v = 128, chunk 64, no normaliser, and either no gate (either feature
- * map) or the head gate (identity feature map); anything else returns
- * LA_ERR_UNSUPPORTED.
+ * backward pass is built from such sums. With LA_GATE_CHANNEL the decay from s
+ * to t is prod_{j=s+1..t} alpha_j, so token s is decayed by the gate of token
+ * s + 1 (the last token by none): out_s = sum_{t >= s} (prod_{j=s+1..t}
+ * diag(alpha_j)) applied to phi(k_t)^T v_t, read by phi(q_s), and the final state
+ * is sum_t (prod_{j=1..t} diag(alpha_j)) phi(k_t)^T v_t. Tensor-core kernel only:
+ * bf16, d_k = d_v = 128, chunk 64, no normaliser, and no gate or the
+ * per-channel gate (either feature map) or the head gate (identity feature
+ * map); anything else returns LA_ERR_UNSUPPORTED.
  *
  * Scratch: when the batch has too few (b, h) sequences to fill the GPU (2 B H
  * at most the number of SMs), the tensor-core path splits each sequence into
@@ -259,11 +263,12 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
  * (except the per-channel gate together with the normaliser): each gradient
  * term is a linear-attention forward with its roles permuted, causal for dQ and
  * anti-causal (the LA_REVERSE form, over later tokens) for dK and dv; with the
- * normaliser also den_t, z_t e_t and sum Q_t e_t (the cancelling terms in
- * fp32); with the per-channel gate dv is a gated forward of token-reversed
- * copies and dQ, dK are forwards whose decay falls on the value channel, and dg
- * comes from a segmented reverse scan. Every other case (and LA_KERNEL_SIMT)
- * runs three sweeps over the sequence on the CUDA cores.
+ * normaliser also w_t = dout_t / den_t and e_t = -(dout_t . num_t) / den_t^2 on
+ * the scores and a carried sum (the cancelling terms in fp32); with the
+ * per-channel gate dv is an anti-causal gated forward and dQ, dK are forwards
+ * whose decay falls on the value channel, and dg comes from a segmented
+ * reverse scan. Every other case (and LA_KERNEL_SIMT) runs three sweeps over
+ * the sequence on the CUDA cores.
  *   dout   [B][H][L][d_v]; dq, dk [B][H][L][d_k] and dv [B][H][L][d_v] are
  *          written, in the type of q
  *   dgate  with LA_GATE_CHANNEL: NULL (not computed) or [B][H][L][d_k] in the
@@ -272,10 +277,11 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
  * taken stream-ordered from the library's pool on `stream` (LA_ERR_CUDA if that
  * fails): on the tensor-core route none with the identity feature map (beyond
  * the per-segment states of batches too small to fill the GPU), four bf16
- * [B][H][L][128] arrays with LA_PHI_ELU1, with LA_NORMALIZE five bf16 and five
- * fp32 ones, with LA_GATE_CHANNEL nine bf16 and one fp32 one plus per-chunk
- * sums; on the other one fp32 [B][H][L][d_k] array (two, plus three [B][H][L],
- * with LA_NORMALIZE).
+ * [B][H][L][128] arrays with LA_PHI_ELU1; with LA_NORMALIZE one bf16 array and
+ * one fp32 [B][H][L] one when each sequence is one CTA and there is no gate,
+ * else five bf16 and five fp32 arrays; with LA_GATE_CHANNEL two bf16 arrays and
+ * one fp32 one plus per-chunk sums; on the other route one fp32 [B][H][L][d_k]
+ * array (two, plus three [B][H][L], with LA_NORMALIZE).
  * Errors as la_chunk_fwd; no output may overlap an input.
  */
 int la_chunk_bwd(const void *q, const void *k, const void *v, const void *gate,

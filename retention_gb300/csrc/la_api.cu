@@ -17,7 +17,7 @@ std::atomic<unsigned long long> g_launches{0};
 constexpr int kKnownModeBits = LA_PHI_ELU1 | LA_NORMALIZE | LA_GATE_HEAD | LA_GATE_CHANNEL |
                                LA_DTYPE_F32 | LA_KERNEL_SIMT | LA_REVERSE;
 // what the anti-causal form does not run with (and elu+1 together with the head gate)
-constexpr int kNotWithReverse = LA_NORMALIZE | LA_GATE_CHANNEL | LA_DTYPE_F32 | LA_KERNEL_SIMT;
+constexpr int kNotWithReverse = LA_NORMALIZE | LA_DTYPE_F32 | LA_KERNEL_SIMT;
 bool reverse_unsupported(int mode) {
     return (mode & kNotWithReverse) || ((mode & LA_PHI_ELU1) && (mode & LA_GATE_HEAD));
 }

@@ -91,15 +91,14 @@ def test_decode_validation(lib, kw, expect):
 
 def test_reverse_bit_is_rejected_where_it_does_not_run(lib):
     """LA_REVERSE (the anti-causal form) runs without the normaliser, with no
-    gate (either feature map) or the head gate (identity feature map); the
-    decode step and the backward do not take it. These return during
-    validation."""
+    gate or the per-channel gate (either feature map) or the head gate
+    (identity feature map); the decode step and the backward do not take it.
+    These return during validation."""
     from retention_gb300 import la
     R = la.LA_REVERSE
     for bad in (la.LA_NORMALIZE, la.LA_DTYPE_F32, la.LA_KERNEL_SIMT):
         assert _fwd(lib, mode=R | bad) == -2
     assert _fwd(lib, gate=A, mode=R | la.LA_PHI_ELU1 | la.LA_GATE_HEAD) == -2
-    assert _fwd(lib, gate=A, mode=R | la.LA_GATE_CHANNEL) == -2
     assert _dec(lib, mode=R) == -1
     assert lib.la_chunk_bwd(A, A, A, None, A, A, A, A, None, 1, 1, 8, 16, 16, R, None) == -1
     assert lib.la_chunk_fwd_path(1, 1, 8, 16, 16, R | la.LA_NORMALIZE, 64) == -2

@@ -218,24 +218,37 @@ def _flip(inp):
     return {n: (t.flip(2) if (t is not None and t.dim() == 4) else t) for n, t in inp.items()}
 
 
+def _reversed_inputs(inp, cfg):
+    """The token-reversed sequence; with the per-channel gate, reversed token u
+    decays by the gate of original token L - u, and reversed token 0 by none
+    (a gate of 30: alpha = sigmoid(30)^(1/16), 1 to within 1e-14)."""
+    flip = _flip(inp)
+    if cfg["gate"] == "channel":
+        g = flip["gate"]
+        flip["gate"] = torch.cat([torch.full_like(g[:, :, :1], 30.0), g[:, :, :-1]], dim=2)
+    return flip
+
+
 def _check_reverse(cfg, inp, initial_state=None):
-    """LA_REVERSE sums over the token and every later one; with a scalar decay
-    that is the causal recurrence of the token-reversed sequence, which the
-    oracle computes (its final state is the state before token 0)."""
+    """LA_REVERSE sums over the token and every later one; that is the causal
+    recurrence of the token-reversed sequence (with the per-channel gate, of
+    the gate shifted by a token), which the oracle computes (its final state is
+    the state before token 0)."""
     s0 = None if initial_state is None else initial_state.numpy()
-    out_ref, st_ref = run_oracle(_flip(inp), cfg, state_in=s0)
+    out_ref, st_ref = run_oracle(_reversed_inputs(inp, cfg), cfg, state_in=s0)
     out_ref = out_ref[:, :, ::-1]
     out, st = run_gpu(inp, cfg, reverse=True, initial_state=initial_state)
     e_out, e_st = rel_err(out, out_ref), rel_err(st, st_ref)
     assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
 
 
-@pytest.mark.parametrize("phi,gate", [("identity", None), ("identity", "head"), ("elu1", None)])
+@pytest.mark.parametrize("phi,gate", [("identity", None), ("identity", "head"), ("elu1", None),
+                                      ("identity", "channel"), ("elu1", "channel")])
 @pytest.mark.parametrize("B,H,L", [(1, 4, 1000), (2, 40, 333), (2, 40, 129), (1, 80, 64), (1, 80, 1)],
                          ids=["split", "unsplit-ragged", "unsplit-129", "one-chunk", "one-token"])
 def test_reverse_matches_the_reversed_causal_oracle(phi, gate, B, H, L):
     from retention_gb300 import la
-    cfg = W.workload("retention", B=B, H=H, L=L, gate=gate, phi=phi)
+    cfg = W.workload("gla" if gate == "channel" else "retention", B=B, H=H, L=L, gate=gate, phi=phi)
     mode = la.mode_bits(phi, False, gate, reverse=True)
     assert la.chunk_fwd_path(B, H, L, 128, 128, mode, 64) == 1
     _check_reverse(cfg, W.chunk_inputs(cfg, seed=L + H))
