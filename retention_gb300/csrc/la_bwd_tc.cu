@@ -19,8 +19,8 @@ namespace la {
 namespace {
 
 // The hardware base-2 exponential and logarithm (denormals flushed), for the
-// gated pass after the forwards, which works in log2 units as the forward
-// kernel's gate arithmetic does.
+// elementwise passes around the forwards (the gated pass works in log2 units,
+// as the forward kernel's gate arithmetic does).
 __device__ __forceinline__ float hw_ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -49,7 +49,8 @@ __device__ __forceinline__ uint4 phi8(uint4 x, bool elu1) {
     uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float lo = phi(__uint_as_float(w[i] << 16), true), hi = phi(__uint_as_float(w[i] & 0xffff0000u), true);
+        const float x0 = __uint_as_float(w[i] << 16), x1 = __uint_as_float(w[i] & 0xffff0000u);
+        const float lo = x0 > 0.f ? x0 + 1.f : hw_ex2(x0 * kLog2e), hi = x1 > 0.f ? x1 + 1.f : hw_ex2(x1 * kLog2e);
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         w[i] = *reinterpret_cast<uint32_t *>(&h);
     }

@@ -121,8 +121,13 @@ static_assert(3 * 16 * kZb * 4 <= 3328, "Z blocks");
 // outputs s + 128 u, u < 2I: block J = u / 2, row r = s / 16 + 8 (u % 2),
 // column s % 16. Everything is unrolled with J known, so the loads of all of a
 // thread's outputs can run ahead of their arithmetic.
+// element (i, j) of T = L^-1 diag(beta) into a K-major bf16 [64 x 64] block
+__device__ __forceinline__ void t_store(uint8_t *tb, int i, int j, float x, const float *beta) {
+    *reinterpret_cast<bf16 *>(tb + chunk_off(i, j >> 3, 0) + (j & 7) * 2) = __float2bfloat16_rn(x * beta[j]);
+}
+
 template <int I, typename Sync>
-__device__ __forceinline__ void inverse_block_row(float *M, float *Zs, int s, Sync sync) {
+__device__ __forceinline__ void inverse_block_row(float *M, float *Zs, int s, Sync sync, uint8_t *tb, const float *beta) {
     const int r0 = s >> 4, col = s & 15;
     float z[2 * I];
 #pragma unroll
@@ -159,7 +164,11 @@ __device__ __forceinline__ void inverse_block_row(float *M, float *Zs, int s, Sy
         z[u] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
     }
 #pragma unroll
-    for (int u = 0; u < 2 * I; ++u) M[(16 * I + r0 + 8 * (u & 1)) * kLd + 16 * (u >> 1) + col] = z[u];
+    for (int u = 0; u < 2 * I; ++u) {
+        const int i = 16 * I + r0 + 8 * (u & 1), j = 16 * (u >> 1) + col;
+        M[i * kLd + j] = z[u];
+        t_store(tb, i, j, z[u], beta);
+    }
     sync();
 }
 
@@ -171,7 +180,8 @@ __device__ __forceinline__ void inverse_block_row(float *M, float *Zs, int s, Sy
 // left as they are, the diagonal blocks' upper halves are zero. `sync` is the
 // solvers' barrier.
 template <typename Sync>
-__device__ __forceinline__ void invert_unit_lower(float *M, float *Zs, int s, Sync sync) {
+__device__ __forceinline__ void invert_unit_lower(float *M, float *Zs, int s, Sync sync, uint8_t *tb,
+                                                  const float *beta) {
     float x[16];
     const int b = (s >> 4) & 3, c = s & 15, o = 16 * b;
     if (s < 64) {
@@ -189,12 +199,15 @@ __device__ __forceinline__ void invert_unit_lower(float *M, float *Zs, int s, Sy
     sync();  // every diagonal block is read before any is overwritten
     if (s < 64) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) M[(o + r) * kLd + o + c] = x[r];
+        for (int r = 0; r < 16; ++r) {
+            M[(o + r) * kLd + o + c] = x[r];
+            t_store(tb, o + r, o + c, x[r], beta);
+        }
     }
     sync();
-    inverse_block_row<1>(M, Zs, s, sync);
-    inverse_block_row<2>(M, Zs, s, sync);
-    inverse_block_row<3>(M, Zs, s, sync);
+    inverse_block_row<1>(M, Zs, s, sync, tb, beta);
+    inverse_block_row<2>(M, Zs, s, sync, tb, beta);
+    inverse_block_row<3>(M, Zs, s, sync, tb, beta);
 }
 
 struct FusedParams {
@@ -260,9 +273,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
         mbar_init(afree, 64);
         fence_mbar_init();
     }
-    // S0 = 0: the bf16 copy starts at zero
+    // S0 = 0: the bf16 copy starts at zero; so do both T buffers (the blocks
+    // above the diagonal are never written)
     for (int i = tid; i < 32768 / 16; i += kFusedThreads) reinterpret_cast<uint4 *>(sm + fS)[i] = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();  // the tensor core reads the copy
+    for (int i = tid; i < 16384 / 16; i += kFusedThreads) reinterpret_cast<uint4 *>(sm + fT)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // the tensor core reads the copy and T
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -329,31 +344,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 bad = 1;
                 break;
             }
-            invert_unit_lower(M, Zs, sx, sync);
-            // T = X diag(beta), lower triangular, K-major bf16, into buffer m % 2:
-            // 16-byte piece q = sx + 128 u holds row q / 8, columns 8 (q % 8) ..
-            uint8_t *tb = sm + fT + (uint32_t)(m & 1) * 8192u;
-            const float *bm = bs + (m & 1) * 64;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int q = sx + 128 * u, i = q >> 3, c8 = q & 7;
-                const float4 x0 = *reinterpret_cast<const float4 *>(M + i * kLd + 8 * c8);
-                const float4 x1 = *reinterpret_cast<const float4 *>(M + i * kLd + 8 * c8 + 4);
-                const float4 b0 = *reinterpret_cast<const float4 *>(bm + 8 * c8);
-                const float4 b1 = *reinterpret_cast<const float4 *>(bm + 8 * c8 + 4);
-                const float xv[8] = {x0.x * b0.x, x0.y * b0.y, x0.z * b0.z, x0.w * b0.w,
-                                     x1.x * b1.x, x1.y * b1.y, x1.z * b1.z, x1.w * b1.w};
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = 8 * c8 + 2 * e;
-                    w[e] = pack2(j <= i ? xv[2 * e] : 0.f, j + 1 <= i ? xv[2 * e + 1] : 0.f);
-                }
-                *reinterpret_cast<uint4 *>(tb + chunk_off(i, c8, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+            // L^-1, and T = L^-1 diag(beta) (bf16, K-major) into buffer m % 2 as its
+            // elements are made; the blocks above the diagonal stay zero from the start
+            invert_unit_lower(M, Zs, sx, sync, sm + fT + (uint32_t)(m & 1) * 8192u, bs + (m & 1) * 64);
             fence_proxy_async_smem();
             mbar_arrive(tready + (m & 1));
-            sync();  // M is read: the next chunk's A may go over it
+            // (the next chunk's A may go over M: its last reads were before the
+            // inverse's final barrier)
         }
     } else if (chain) {
         // ============================================================ the recurrence
