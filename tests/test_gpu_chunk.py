@@ -263,9 +263,12 @@ def test_reverse_window_ends(B, H, L):
     _check_reverse(cfg, window_inputs(cfg, seed=23))
 
 
+@pytest.mark.parametrize("name", ["retention", "gla"])
 @pytest.mark.parametrize("B,H,L", [(1, 4, 1000), (2, 40, 333)], ids=["split", "unsplit"])
-def test_reverse_from_a_state(B, H, L):
-    """An initial state of the reverse form sits after the last token."""
-    cfg = W.workload("retention", B=B, H=H, L=L)
+def test_reverse_from_a_state(name, B, H, L):
+    """An initial state of the reverse form sits after the last token (with the
+    per-channel gate it is decayed by the gates of tokens 1 .. L - 1 and by none
+    for the last token's successor, as the reversed sequence's first token is)."""
+    cfg = W.workload(name, B=B, H=H, L=L)
     s0 = W.decode_state(dict(cfg, state_std=0.1), 77)
     _check_reverse(cfg, W.chunk_inputs(cfg, seed=24), initial_state=s0)
