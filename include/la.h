@@ -278,8 +278,8 @@ int la_chunk_fwd_gn_swish(const void *q, const void *k, const void *v, const voi
  * fails): on the tensor-core route none with the identity feature map (beyond
  * the per-segment states of batches too small to fill the GPU), four bf16
  * [B][H][L][128] arrays with LA_PHI_ELU1; with LA_NORMALIZE one bf16 array and
- * one fp32 [B][H][L] one when each sequence is one CTA and there is no gate,
- * else five bf16 and five fp32 arrays; with LA_GATE_CHANNEL two bf16 arrays and
+ * one fp32 [B][H][L] one without a gate (plus the per-segment states), five
+ * bf16 and five fp32 arrays with the head gate; with LA_GATE_CHANNEL two bf16 arrays and
  * one fp32 one plus per-chunk sums; on the other route one fp32 [B][H][L][d_k]
  * array (two, plus three [B][H][L], with LA_NORMALIZE).
  * Errors as la_chunk_fwd; no output may overlap an input.

@@ -494,10 +494,7 @@ static int launch_bwd_tc_norm_fused(const BwdArgs &a, cudaStream_t s, int *launc
 }
 
 static int launch_bwd_tc_norm(const BwdArgs &a, cudaStream_t s, int *launches) {
-    {
-        ChunkArgs c{a.q, a.k, a.v, nullptr, nullptr, nullptr, a.B, a.H, a.L, kD, kD, a.mode & LA_NORMALIZE, 64, nullptr};
-        if (!(a.mode & LA_GATE_HEAD) && chunk_tc_unsplit(c)) return launch_bwd_tc_norm_fused(a, s, launches);
-    }
+    if (!(a.mode & LA_GATE_HEAD)) return launch_bwd_tc_norm_fused(a, s, launches);
     const long rows = (long)a.B * a.H * a.L;
     const size_t hb = (size_t)rows * kD * sizeof(__nv_bfloat16), fb = 2 * hb;
     // bf16: Q K J w E; fp32: den_full U ZE dKm dz; den [rows]

@@ -79,7 +79,7 @@ struct ChunkArgs {
     // and bp_e e_t = -(dout_t . num_t) / den_t^2 (fp32 [B][H][L]); null: none
     const void *bp_dout;
     float *bp_e;
-    // tensor-core path only, no gate or normaliser, unsplit: the score of every
+    // tensor-core path only, no gate, normaliser, initial or final state: the score of every
     // (query, key) pair gets e_t added (1: e of the query token, causal; 2: e of
     // the key token, with reverse), bias_e [B][H][L] fp32; 0: none. With elu+1
     // the feature map applies to v alone, and every output row is multiplied by
@@ -140,7 +140,6 @@ size_t bwd_scratch_bytes(const BwdArgs &a);
 int launch_chunk_tc(const ChunkArgs &a, cudaStream_t s, int *launches);
 bool chunk_tc_supports(const ChunkArgs &a);
 bool chunk_tc_fuses_epilogue(const ChunkArgs &a);
-bool chunk_tc_unsplit(const ChunkArgs &a);
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a);
 int launch_chunk_tc_into(const ChunkArgs &a, cudaStream_t s, int *launches, void *scratch, size_t scratch_bytes);
 // diagnostics: the tensor-core forward (unsplit only) with its producer stopping

@@ -154,7 +154,7 @@ struct Layout {
     // where its og tile (EPI) or x tile (BIAS with elu+1) lands first and the
     // chunk's result is written over it
     static constexpr uint32_t O2 = O + (SO ? 0 : (OF32 ? 32768 : 16384));
-    static constexpr uint32_t F = O2 + ((EPI || BIAS) ? 16384 : 0);
+    static constexpr uint32_t F = O2 + ((!SO && (EPI || BIAS)) ? 16384 : 0);
     static constexpr uint32_t nfbuf = GATE != 0 ? NF * 128 : 0, nfq = GATE == 1 ? 128 : 0;
     static constexpr uint32_t ntot = GATE >= 2 ? (NORM ? 512 : 1024) : 0;  // quarter sums (one or two chunks)
     static constexpr uint32_t nwb = EPI ? 512 : 0;  // GroupNorm weight, bias [128] each; half-row (m, M2) [2][64][2]
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                   "the anti-causal instance: a scalar decay, or the channel gate");
     static_assert(EPI != 1 || (GATE <= 1 && !NORM && !SO && !OF32 && !REV), "the fused epilogue: bf16 output, no normaliser");
     static_assert(EPI != 2 || (GATE == 0 && NORM && !SO && !OF32 && !REV), "the backward prep: the normalised causal form");
-    static_assert(BIAS == 0 || (GATE == 0 && !NORM && !SO && !OF32 && EPI == 0 && REV == (BIAS == 2)),
+    static_assert(BIAS == 0 || (GATE == 0 && !NORM && !OF32 && EPI == 0 && REV == (BIAS == 2)),
                   "the bias instances: no gate or normaliser, bf16 output");
     // (bias instances with ELU1) the feature map applies to the value tile, the
     // query and key tiles are taken as given, and each output row is multiplied
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     // 4-7, 0, 1, 14, 15 and warps 12 and 13 make P and the outputs in turn. (The
     // split layout measured slower for the plain forms: the prologue's work then
     // has the special function units of two sub-partitions only.)
-    constexpr bool SPLIT = EPI != 0 || BIAS != 0;
+    constexpr bool SPLIT = !SO && (EPI != 0 || BIAS != 0);
     constexpr int PT = SPLIT ? 128 : 256;  // prologue threads
     constexpr int NS = LY::NS;
     constexpr int NG = LY::GR ? LY::NG : 1;  // gate ring slots (the ring exists only if GR)
@@ -375,7 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
     // (a tile wholly past the end is never read: every row of it is masked)
     auto gy = [&](int t0) { return (REV && GATE >= 2) ? min(t0 + 1, L - 1) : t0; };
     const bool init = !SO && p.state_in != nullptr && (seg > 0 || p.init0);  // start from a carried state
-    const size_t blk = (size_t)kD * kD + (NORM ? kD : 0);
+    // state block: S (+ z with the normaliser; + the carried vector of the bias
+    // instances, for the segments of a split sequence)
+    const size_t blk = (size_t)kD * kD + (NORM ? kD : 0) + (BIAS ? kD : 0);
     const size_t segblk = (size_t)sgi * blk;
 
     constexpr int NF = LY::NF;
@@ -877,6 +879,9 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             }
             // log decay of key channel pd over the previous chunk and over the segment so far
             float b_last = 0.f, b_total = 0.f;
+            // (BIAS, state-only pass) the segment's column sums so far, held by the
+            // first thread of each column group
+            float crun[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             int m = 0;  // chunks into the current window
             // REV takes a ragged last chunk first: it closes a window of its own,
             // so that every window after it holds whole chunks only
@@ -909,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 // (BIAS) the outputs, which may trail the MMAs, have read the column
                 // sums of chunk n - NF out of the slot this chunk's go to
                 const bool ok = mbar_wait(&full[s], (uint32_t)(n / NS) & 1u, wait_ns) &&
-                                (BIAS == 0 || n < NF || mbar_wait(&cempty[n % NF], (uint32_t)(n / NF - 1) & 1u, wait_ns));
+                                (BIAS == 0 || SO || n < NF || mbar_wait(&cempty[n % NF], (uint32_t)(n / NF - 1) & 1u, wait_ns));
                 if (named_sync_or<kBarPro, PT>(!ok)) {
                     bad = 1;
                     break;
@@ -1008,10 +1013,15 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
 #pragma unroll
                         for (int e = 0; e < 8; ++e) cs[e] += __shfl_xor_sync(0xffffffffu, cs[e], off);
                     if (g == 0) {
-                        float *dst = csum + (n % NF) * 128 + bv * 64 + lc * 8;
+                        if constexpr (SO) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) dst[e] = cs[e];
-                        mbar_arrive(&cfull[n % NF]);
+                            for (int e = 0; e < 8; ++e) crun[e] += cs[e];
+                        } else {
+                            float *dst = csum + (n % NF) * 128 + bv * 64 + lc * 8;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) dst[e] = cs[e];
+                            mbar_arrive(&cfull[n % NF]);
+                        }
                     }
                 }
                 fence_proxy_async_smem();
@@ -1022,6 +1032,17 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
                 if (SO && gok((size_t)sgi * kD + pd, p.n_seg_logdecay))
                     p.seg_logdecay[(size_t)sgi * kD + pd] = b_total;
                 mbar_arrive(profinal);
+            }
+            if constexpr (SO && BIAS != 0) {
+                // the segment's column sums after its state (no decay: the scan adds
+                // them up over the earlier segments)
+                constexpr int TG = PT / 16;
+                const int bc = pd / TG, bv = bc >> 3, lc = bc & 7;
+                const size_t o = segblk + (size_t)kD * kD + bv * 64 + lc * 8;
+                if (!bad && pd % TG == 0 && gok(o + 7, p.n_seg_state)) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) p.seg_state[o + e] = crun[e];
+                }
             }
         }
     } else if (warp >= 8 && warp < 12) {
@@ -1372,7 +1393,14 @@ __global__ void __launch_bounds__(kThreads, 1) la_chunk_tc_kernel(const __grid_c
             gnw[col] = p.gn_w && hin ? p.gn_w[(size_t)h * kD + col] : 1.f;
             gnb[col] = p.gn_b && hin ? p.gn_b[(size_t)h * kD + col] : 0.f;
         }
-        if (BIAS) cvec[64 * oh + t] = 0.f;  // the carried vector starts at zero
+        if (BIAS) {
+            // the carried vector: zero, or (a later segment) the scan's sum over the
+            // earlier segments, after the carried state in its block (read once the
+            // scan this launch may have started behind has finished)
+            const size_t o = segblk + (size_t)kD * kD + 64 * oh + t;
+            if (init) griddep_wait();
+            cvec[64 * oh + t] = (init && gok(o, p.n_state_in)) ? p.state_in[o] : 0.f;
+        }
         // (BIAS 1) e of row t's token, read a chunk ahead of its use
         auto e_at = [&](int m) {
             const int tm = chunk_t0(m) + t;
@@ -1688,16 +1716,15 @@ int launch_mode(const TcParams &prm, int grid, cudaStream_t s, int mode, bool ou
                 bool pdl = false, bool rev = false, int epi = 0, int bias = 0) {
     const bool elu1 = mode & LA_PHI_ELU1, norm = mode & LA_NORMALIZE;
     if (bias != 0) {
-        // the bias instances: no gate or normaliser, bf16 output, unsplit; with
-        // LA_PHI_ELU1 the feature map applies to the value tile
-        if (SO || norm || out_f32 || value_gate || epi || (mode & (LA_GATE_HEAD | LA_GATE_CHANNEL)) ||
-            rev != (bias == 2))
+        // the bias instances: no gate or normaliser, bf16 output; with LA_PHI_ELU1
+        // the feature map applies to the value tile
+        if (norm || out_f32 || value_gate || epi || (mode & (LA_GATE_HEAD | LA_GATE_CHANNEL)) || rev != (bias == 2))
             return LA_ERR_INTERNAL;
         if (bias == 1)
-            return elu1 ? launch_t<0, true, false, false, false, false, 0, 1>(prm, grid, s, pdl)
-                        : launch_t<0, false, false, false, false, false, 0, 1>(prm, grid, s, pdl);
-        return elu1 ? launch_t<0, true, false, false, false, true, 0, 2>(prm, grid, s, pdl)
-                    : launch_t<0, false, false, false, false, true, 0, 2>(prm, grid, s, pdl);
+            return elu1 ? launch_t<0, true, false, SO, false, false, 0, 1>(prm, grid, s, pdl)
+                        : launch_t<0, false, false, SO, false, false, 0, 1>(prm, grid, s, pdl);
+        return elu1 ? launch_t<0, true, false, SO, false, true, 0, 2>(prm, grid, s, pdl)
+                    : launch_t<0, false, false, SO, false, true, 0, 2>(prm, grid, s, pdl);
     }
     if (epi == 2 && !SO) {
         // the backward prep: the normalised causal form, no gate
@@ -1826,13 +1853,6 @@ int tc_segments(int BH, int nchunks, int *seg_chunks) {
     return (nchunks + cs - 1) / cs;
 }
 
-// Whether the tensor-core path runs these arguments as one CTA per sequence
-// (no split into segments).
-bool chunk_tc_unsplit(const ChunkArgs &a) {
-    int seg_chunks = 0;
-    return tc_segments(a.B * a.H, (a.L + kC - 1) / kC, &seg_chunks) == 1;
-}
-
 // Scratch bytes the tensor-core path needs for these arguments (0 when the
 // sequences are not split).
 size_t chunk_tc_scratch_bytes(const ChunkArgs &a) {
@@ -1840,7 +1860,7 @@ size_t chunk_tc_scratch_bytes(const ChunkArgs &a) {
     int seg_chunks = 0;
     const int nseg = tc_segments(BH, (a.L + kC - 1) / kC, &seg_chunks);
     if (nseg == 1) return 0;
-    const size_t blk = (size_t)kD * kD + ((a.mode & LA_NORMALIZE) ? kD : 0);
+    const size_t blk = (size_t)kD * kD + ((a.mode & LA_NORMALIZE) ? kD : 0) + (a.bias ? kD : 0);
     const size_t nsb = (size_t)BH * nseg;
     return (2 * nsb * blk + nsb * kD) * sizeof(float);
 }
@@ -1874,8 +1894,9 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
         prm.n_e = (size_t)BH * a.L;
     }
     if (a.bias != 0) {
-        // the carried vector runs over whole sequences: one CTA per sequence only
-        if (a.bias_e == nullptr || epi != 0) return LA_ERR_INTERNAL;
+        // the carried vector adds to the state block of a split sequence's
+        // segments (it has no layout in a caller's initial or final state)
+        if (a.bias_e == nullptr || epi != 0 || a.initial_state || a.final_state) return LA_ERR_INTERNAL;
         prm.e_in = a.bias_e;
         prm.n_e = (size_t)BH * a.L;
         if (a.mode & LA_PHI_ELU1) {
@@ -1896,14 +1917,13 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.n_final = a.final_state ? (size_t)BH * blkf : 0;
     prm.n_state_in = a.initial_state ? (size_t)BH * blkf : 0;  // (split: the carried states, below)
     if (stall_chunk >= 0 && prm.nseg != 1) return LA_ERR_UNSUPPORTED;  // the stall runs one launch only
-    if (a.bias != 0 && prm.nseg != 1) return LA_ERR_UNSUPPORTED;        // (as above)
     if (prm.nseg == 1) {
         prm.state_in = a.initial_state;  // [BH][blk]: the segment of CTA bh starts there
         const int rc = launch_mode<false>(prm, BH, s, a.mode, a.out_f32, a.value_gate, false, a.reverse, epi, a.bias);
         if (rc == LA_OK) *launches += 1;
         return rc;
     }
-    const size_t blk = (size_t)kD * kD + ((a.mode & LA_NORMALIZE) ? kD : 0);
+    const size_t blk = (size_t)kD * kD + ((a.mode & LA_NORMALIZE) ? kD : 0) + (a.bias ? kD : 0);
     const size_t nsb = (size_t)BH * prm.nseg;
     if (scratch == nullptr || scratch_bytes < (2 * nsb * blk + nsb * kD) * sizeof(float)) return LA_ERR_INTERNAL;
     float *seg_state = static_cast<float *>(scratch);
@@ -1914,7 +1934,7 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.n_seg_state = nsb * blk;
     prm.n_seg_logdecay = nsb * kD;
     // the state-only pass: every segment but each sequence's last
-    int rc = launch_mode<true>(prm, BH * (prm.nseg - 1), s, a.mode, false, a.value_gate, false, a.reverse);
+    int rc = launch_mode<true>(prm, BH * (prm.nseg - 1), s, a.mode, false, a.value_gate, false, a.reverse, 0, a.bias);
     if (rc != LA_OK) return rc;
     *launches += 1;
     la_seg_scan_kernel<<<dim3((unsigned)BH, (unsigned)((blk + 255) / 256)), 256, 0, s>>>(
@@ -1926,7 +1946,7 @@ int launch_chunk_tc_impl(const ChunkArgs &a, cudaStream_t s, int *launches, void
     prm.seg_state = nullptr;
     prm.seg_logdecay = nullptr;
     prm.n_seg_state = prm.n_seg_logdecay = 0;
-    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate, true, a.reverse, epi);
+    rc = launch_mode<false>(prm, (int)nsb, s, a.mode, a.out_f32, a.value_gate, true, a.reverse, epi, a.bias);
     if (rc == LA_OK) *launches += 1;
     return rc;
 }
