@@ -121,6 +121,15 @@ def test_bf16_tensor_core_route_shapes(m, B, H, L):
     _check(W.workload("la", B=B, H=H, L=L, **m), seed=B + H + L)
 
 
+@pytest.mark.parametrize("m", [MODES[0], MODES[8]], ids=MID)
+def test_bf16_normalised_split_segments_of_several_chunks(m):
+    """The normalised route on a short batch whose segments hold two chunks
+    each (79 chunks over 40 segments): the carried sums of the bias instances
+    run inside a segment and across the segment scan."""
+    launches = _check(W.workload("la", B=1, H=2, L=5000, **m), seed=9)
+    assert launches == 12, launches
+
+
 def test_bf16_gated_long_sequence():
     cfg = W.workload("gla", B=1, H=2, L=4096)
     _check(cfg, seed=4)

@@ -101,9 +101,10 @@ def test_decode_step(checked, m, dk, dv):
     _parity(out.float().cpu().numpy(), state.cpu().numpy(), ref, ref_state)
 
 
-@pytest.mark.parametrize("name,B,H,L", [("la", 2, 40, 333), ("gla", 1, 2, 1000), ("gla", 2, 40, 200),
-                                        ("retention", 1, 4, 1000)],
-                         ids=["normalised-unsplit", "gated-split", "gated-unsplit", "retention-split"])
+@pytest.mark.parametrize("name,B,H,L", [("la", 2, 40, 333), ("la", 1, 2, 5000), ("gla", 1, 2, 1000),
+                                        ("gla", 2, 40, 200), ("retention", 1, 4, 1000)],
+                         ids=["normalised-unsplit", "normalised-split", "gated-split", "gated-unsplit",
+                              "retention-split"])
 def test_backward(checked, name, B, H, L):
     """The backward's forward instances: the backward-prep and bias instances
     (normalised), the anti-causal gated and value-side instances (gated), the
