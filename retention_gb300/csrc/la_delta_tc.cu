@@ -121,13 +121,8 @@ static_assert(3 * 16 * kZb * 4 <= 3328, "Z blocks");
 // outputs s + 128 u, u < 2I: block J = u / 2, row r = s / 16 + 8 (u % 2),
 // column s % 16. Everything is unrolled with J known, so the loads of all of a
 // thread's outputs can run ahead of their arithmetic.
-// element (i, j) of T = L^-1 diag(beta) into a K-major bf16 [64 x 64] block
-__device__ __forceinline__ void t_store(uint8_t *tb, int i, int j, float x, const float *beta) {
-    *reinterpret_cast<bf16 *>(tb + chunk_off(i, j >> 3, 0) + (j & 7) * 2) = __float2bfloat16_rn(x * beta[j]);
-}
-
 template <int I, typename Sync>
-__device__ __forceinline__ void inverse_block_row(float *M, float *Zs, int s, Sync sync, uint8_t *tb, const float *beta) {
+__device__ __forceinline__ void inverse_block_row(float *M, float *Zs, int s, Sync sync) {
     const int r0 = s >> 4, col = s & 15;
     float z[2 * I];
 #pragma unroll
@@ -164,50 +159,62 @@ __device__ __forceinline__ void inverse_block_row(float *M, float *Zs, int s, Sy
         z[u] = -((acc[0] + acc[1]) + (acc[2] + acc[3]));
     }
 #pragma unroll
-    for (int u = 0; u < 2 * I; ++u) {
-        const int i = 16 * I + r0 + 8 * (u & 1), j = 16 * (u >> 1) + col;
-        M[i * kLd + j] = z[u];
-        t_store(tb, i, j, z[u], beta);
-    }
+    for (int u = 0; u < 2 * I; ++u) M[(16 * I + r0 + 8 * (u & 1)) * kLd + 16 * (u >> 1) + col] = z[u];
     sync();
 }
 
 // L^-1 for the unit lower-triangular L = I + A (A strictly lower, fp32 rows
 // kLd floats apart) in place over A, by the 128 threads s of the solver warps,
 // in 16 x 16 blocks: the diagonal blocks X_II by forward substitution (thread
-// s < 64 takes column s % 16 of block s / 16: x_r = [r == c] - sum_{j<r} A x_j),
-// then block rows 1..3 (inverse_block_row). The blocks above the diagonal are
-// left as they are, the diagonal blocks' upper halves are zero. `sync` is the
+// s < 64 takes column s % 16 of block s / 16; once x_r is final its share
+// leaves every later row, so the dependent chain is one step per row), then
+// block rows 1..3 (inverse_block_row). The blocks above the diagonal are left
+// as they are, the diagonal blocks' upper halves are zero. `sync` is the
 // solvers' barrier.
 template <typename Sync>
-__device__ __forceinline__ void invert_unit_lower(float *M, float *Zs, int s, Sync sync, uint8_t *tb,
-                                                  const float *beta) {
+__device__ __forceinline__ void invert_unit_lower(float *M, float *Zs, int s, Sync sync) {
     float x[16];
     const int b = (s >> 4) & 3, c = s & 15, o = 16 * b;
     if (s < 64) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc0 = r == c ? 1.f : 0.f, acc1 = 0.f;
+        for (int r = 0; r < 16; ++r) x[r] = r == c ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < r; ++j) {
-                if (j & 1) acc1 = fmaf(-M[(o + r) * kLd + o + j], x[j], acc1);
-                else acc0 = fmaf(-M[(o + r) * kLd + o + j], x[j], acc0);
-            }
-            x[r] = acc0 + acc1;
+        for (int r = 0; r < 16; ++r) {
+#pragma unroll
+            for (int j = r + 1; j < 16; ++j) x[j] = fmaf(-M[(o + j) * kLd + o + r], x[r], x[j]);
         }
     }
     sync();  // every diagonal block is read before any is overwritten
     if (s < 64) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            M[(o + r) * kLd + o + c] = x[r];
-            t_store(tb, o + r, o + c, x[r], beta);
-        }
+        for (int r = 0; r < 16; ++r) M[(o + r) * kLd + o + c] = x[r];
     }
     sync();
-    inverse_block_row<1>(M, Zs, s, sync, tb, beta);
-    inverse_block_row<2>(M, Zs, s, sync, tb, beta);
-    inverse_block_row<3>(M, Zs, s, sync, tb, beta);
+    inverse_block_row<1>(M, Zs, s, sync);
+    inverse_block_row<2>(M, Zs, s, sync);
+    inverse_block_row<3>(M, Zs, s, sync);
+}
+
+// T = L^-1 diag(beta) into a K-major bf16 [64 x 64] block once L^-1 is complete
+// in M: thread s takes row s / 2 and every other 16-byte group of the row's
+// blocks at or left of the diagonal (those to the right stay zero from the
+// start). One pass of 16-byte stores after the inverse took less time than
+// storing each element as it was made.
+__device__ __forceinline__ void t_store(const float *M, int s, uint8_t *tb, const float *beta) {
+    const int i = s >> 1, lastg = 2 * (i >> 4) + 1;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int c8 = (s & 1) + 2 * u;
+        if (c8 <= lastg) {
+            const float4 m0 = *reinterpret_cast<const float4 *>(M + i * kLd + 8 * c8);
+            const float4 m1 = *reinterpret_cast<const float4 *>(M + i * kLd + 8 * c8 + 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(beta + 8 * c8);
+            const float4 b1 = *reinterpret_cast<const float4 *>(beta + 8 * c8 + 4);
+            *reinterpret_cast<uint4 *>(tb + chunk_off(i, c8, 0)) =
+                make_uint4(pack2(m0.x * b0.x, m0.y * b0.y), pack2(m0.z * b0.z, m0.w * b0.w),
+                           pack2(m1.x * b1.x, m1.y * b1.y), pack2(m1.z * b1.z, m1.w * b1.w));
+        }
+    }
 }
 
 struct FusedParams {
@@ -344,13 +351,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 bad = 1;
                 break;
             }
-            // L^-1, and T = L^-1 diag(beta) (bf16, K-major) into buffer m % 2 as its
-            // elements are made; the blocks above the diagonal stay zero from the start
-            invert_unit_lower(M, Zs, sx, sync, sm + fT + (uint32_t)(m & 1) * 8192u, bs + (m & 1) * 64);
+            // L^-1, then T = L^-1 diag(beta) (bf16, K-major) into buffer m % 2
+            invert_unit_lower(M, Zs, sx, sync);
+            t_store(M, sx, sm + fT + (uint32_t)(m & 1) * 8192u, bs + (m & 1) * 64);
             fence_proxy_async_smem();
             mbar_arrive(tready + (m & 1));
-            // (the next chunk's A may go over M: its last reads were before the
-            // inverse's final barrier)
+            sync();  // every read of M is done before the next chunk's A goes over it
         }
     } else if (chain) {
         // ============================================================ the recurrence
