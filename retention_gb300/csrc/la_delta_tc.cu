@@ -20,23 +20,23 @@
 //   warps 0-7    the recurrence. The state is kept transposed in TMEM (S^T:
 //                lane = key channel i, column = value channel j, fp32) with a
 //                bf16 copy in shared memory. Per chunk:
-//                round 3   Y = K S0^T, P = Q K^T, then O = Q S0^T
+//                phase 1   Y = K S0^T, P = Q K^T, then O = Q S0^T
 //                          -> Vt = V - Y (bf16, over the v tile), masked P
-//                round 3b  Ut = T Vt -> bf16
-//                round 4   S^T += K^T Ut, O += P Ut -> the new bf16 copy of S^T
+//                phase 2   Ut = T Vt -> bf16
+//                phase 3   S^T += K^T Ut, O += P Ut -> the new bf16 copy of S^T
 //                The tensor pipe runs products in issue order, so the state
-//                chain (Y, Vt, Ut, S^T, the bf16 copy) leads each round; a
+//                chain (Y, Vt, Ut, S^T, the bf16 copy) leads each phase; a
 //                chunk's out rows are read out of O while the next chunk's Y
 //                and P run, before its O starts.
 //   warps 8-11   T of the next chunk. The issuer puts its K K^T into TMEM
-//                lanes 64..127 during round 3 (the A operand starts 64 rows
+//                lanes 64..127 during phase 1 (the A operand starts 64 rows
 //                before the k tile); warps 10 and 11 (those lanes) write the
 //                strictly lower part A of L; L^-1 by 16 x 16 blocks in place
 //                over A (the diagonal blocks by forward substitution, a column
 //                per thread, then block rows 1..3 of the lower part,
 //                X_IJ = -X_II sum_{J<=K<I} A_IK X_KJ); T = L^-1 diag(beta), bf16.
 // q and v come in two sets, k through a ring of three a chunk ahead of them, so
-// that the next chunk's K K^T can start while this chunk is in round 3. A set
+// that the next chunk's K K^T can start while this chunk is in phase 1. A set
 // (and a ring slot) is refilled as soon as chunk n's state product has read it.
 // Nothing goes to memory but the out rows and the final state.
 //
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
             uint8_t *const setp = sm + (uint32_t)(n & 1) * kFSet;
             int fail = bad || !mbar_wait(full + (n & 1), (uint32_t)(n >> 1) & 1u, kWaitNs) ||
                        !mbar_wait(kfull + n % 3, (uint32_t)(n / 3) & 1u, kWaitNs);
-            // ------------------------------------------------------------ round 3
+            // ------------------------------------------------------------ phase 1
             // Y first (the recurrence waits on it), then P, then the next
             // chunk's K K^T (for the solvers) while Vt is formed
             bool kk_next = false;  // (issuer) K K^T of chunk n + 1 issued
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                     umma_bf16(tmem + cP, kmaj2(set + fQo, ks), kmaj2(kt, ks), id64, ks > 0);
                 umma_commit(mbP);
                 // if its k tile has landed and the solvers have read this
-                // chunk's out of cA (else after round 4)
+                // chunk's out of cA (else after phase 3)
                 if (n + 1 < nchunks && mbar_try_wait(kfull + (n + 1) % 3, (uint32_t)((n + 1) / 3) & 1u) &&
                     mbar_try_wait(afree, ph)) {
                     issue_kk(n + 1);
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 bad = 1;
                 break;
             }
-            // ------------------------------------------------------------ round 3b: Ut = T Vt
+            // ------------------------------------------------------------ phase 2: Ut = T Vt
             // then O = Q S0^T once the previous chunk's out rows are read out of
             // its accumulator (the low warps do that while Ut is made)
             if (issuer) {
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 bad = 1;
                 break;
             }
-            // ------------------------------------------------------------ round 4
+            // ------------------------------------------------------------ phase 3
             if (issuer) {
                 tc_fence_after();
 #pragma unroll
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 for (int ks = 0; ks < 4; ++ks)
                     umma_bf16(tmem + cO, kmaj1(sm0 + fP, ks), mnmaj(sm0 + fU, 8192, ks), idKM, 1);
                 umma_commit(mbO);
-                // else the next chunk's K K^T now, behind this round's products
+                // else the next chunk's K K^T now, behind this phase's products
                 if (n + 1 < nchunks && !kk_next) {
                     if (!mbar_wait(kfull + (n + 1) % 3, (uint32_t)((n + 1) / 3) & 1u, kWaitNs) ||
                         !mbar_wait(afree, ph, kWaitNs))
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) delta_fused_kernel(const __g
                 tc_fence_after();
                 // every reader of this chunk's set and k slot is done (their
                 // products came before mbS; Vt and the tiles were read before
-                // round 4): refill them with chunk n + 2 and n + 3
+                // phase 3): refill them with chunk n + 2 and n + 3
                 if (producer && !fail) {
                     if (issued < nchunks) load_qv(issued++);
                     if (kissued < nchunks) load_k(kissued++);
