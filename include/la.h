@@ -48,7 +48,7 @@ typedef struct CUstream_st *la_stream_t;
 typedef enum {
     LA_OK = 0,
     LA_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad mode combination */
-    LA_ERR_UNSUPPORTED = -2, /* valid request this build does not run (e.g. d_k = 48) */
+    LA_ERR_UNSUPPORTED = -2, /* valid request the library does not run (e.g. d_k = 48) */
     LA_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned */
     LA_ERR_CUDA = -4,        /* a CUDA call or kernel launch failed */
     LA_ERR_TIMEOUT = -5,     /* a bounded device-side wait ran out */

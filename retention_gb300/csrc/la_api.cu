@@ -249,7 +249,7 @@ const char *la_status_string(int status) {
     switch (status) {
         case LA_OK: return "LA_OK";
         case LA_ERR_INVALID_ARG: return "LA_ERR_INVALID_ARG: invalid argument";
-        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: shape or mode not supported by this build";
+        case LA_ERR_UNSUPPORTED: return "LA_ERR_UNSUPPORTED: shape or mode not supported by the library";
         case LA_ERR_MISALIGNED: return "LA_ERR_MISALIGNED: a pointer is not 16-byte aligned";
         case LA_ERR_CUDA: return "LA_ERR_CUDA: a CUDA call or kernel launch failed";
         case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT: a bounded device-side wait ran out";
