@@ -445,7 +445,8 @@ static int launch_bwd_tc_gated(const BwdArgs &a, cudaStream_t s, int *launches) 
     return rc;
 }
 
-// The normalised form without a gate, one CTA per sequence: four launches. With
+// The normalised form without a gate: four forwards (four launches, or twelve
+// when short batches split each sequence into segments). With
 // num_t = Q_t S_t and den_t = Q_t . z_t of the forward, w_t = dout_t / den_t and
 // e_t = -(dout_t . num_t) / den_t^2:
 //   dQ_t = sum_{s<=t} K_s (v_s . w_t + e_t)     causal, e on the query row
